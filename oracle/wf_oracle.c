@@ -1,0 +1,296 @@
+/*
+ * CPU oracle for the WhiFlash verify-and-route round.  TEST INFRASTRUCTURE:
+ * only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * may call it; the library never does.
+ *
+ * Plain, slow, obviously correct: every result is the textbook definition
+ * written out as loops, in double precision, from the same bf16 / fp32 /
+ * int32 inputs the GPU library receives.  No blocking, fusion or
+ * reordering; OpenMP only distributes independent positions / sequences
+ * across host threads (each sum keeps its natural index order).
+ *
+ * Sources (WhiFlash: Accelerating Speculative Decoding with Token-Level
+ * Cross-Paradigm Routing, arXiv 2606.07710, and the Qwen3-4B-EAGLE3 and
+ * Qwen3-4B-NeuralRouter-df-e3 model cards):
+ *   - greedy verification: the target's next-token choice at a verified
+ *     position is the argmax of its logits (paper Sec. 3.3.1, greedy
+ *     decoding; Sec. 4 "Evaluation");
+ *   - the drafted chain / tree is verified in parallel and decoding resumes
+ *     from the last accepted token (paper Sec. 3.2);
+ *   - acceptance length = tokens accepted per verification round
+ *     (paper Sec. 4 "Metrics");
+ *   - neural router: h -> Linear(d, m) -> GELU -> (dropout) -> Linear(m, 1)
+ *     (paper Sec. 3.3.2 and App. A "Neural Router Architecture"); route to
+ *     the autoregressive drafter iff the prediction exceeds tau (paper
+ *     Sec. 3.3.2 "Hardware-Aware Routing Decision");
+ *   - EAGLE-3 draft head over a fixed 32K draft vocabulary with top-k and a
+ *     draft-to-target id map (EAGLE3 model card, "Model Description",
+ *     "Technical Specifications", "Factors").
+ *
+ * Every function is pinned by tests/test_oracle_pins.py against brute force,
+ * closed forms and hand-built cases; none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact widening of a bfloat16 bit pattern (the high half of an IEEE binary32). */
+static double bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One logit: <h_p, W_v> = sum_k h[p,k] * W[v,k], summed for k = 0..d-1. */
+static double logit(const uint16_t* hrow, const uint16_t* wrow, int64_t d) {
+    double s = 0.0;
+    for (int64_t k = 0; k < d; ++k) s += bf16_value(hrow[k]) * bf16_value(wrow[k]);
+    return s;
+}
+
+/*
+ * Target LM head + greedy choice.  For each position p:
+ *   ids[p]      = the lowest v attaining max_v <h_p, W_v>
+ *   maxlogit[p] = that maximum
+ *   gap[p]      = maximum - (largest logit among the other ids)  (0 on a tie)
+ * maxlogit / gap may be NULL.
+ */
+int oracle_lmhead_argmax(const uint16_t* h, const uint16_t* W, int64_t P, int64_t d, int64_t V,
+                         int32_t* ids, double* maxlogit, double* gap) {
+    if (!h || !W || !ids || P < 0 || d <= 0 || V <= 0) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = 0; p < P; ++p) {
+        double best = -INFINITY, second = -INFINITY;
+        int64_t best_v = -1;
+        for (int64_t v = 0; v < V; ++v) {
+            double L = logit(h + p * d, W + v * d, d);
+            if (L > best) {
+                second = best;
+                best = L;
+                best_v = v;
+            } else if (L > second) {
+                second = L;
+            }
+        }
+        ids[p] = (int32_t)best_v;
+        if (maxlogit) maxlogit[p] = best;
+        if (gap) gap[p] = best - second;
+    }
+    return 0;
+}
+
+/*
+ * DFlash block verification for sequence-packed chains.  Sequence b owns
+ * verified rows pos_off[b] .. pos_off[b+1]-1: row pos_off[b] is the last
+ * committed token, row pos_off[b]+1+j holds draft token j.  The target
+ * choice at row pos_off[b]+j checks draft token j.  Drafts of sequence b are
+ * draft[node_off[b] .. node_off[b+1]-1] (K = node count).
+ *   n_accept[b] = largest n with draft[j] == g[root + j] for all j < n
+ *   last_pos[b] = root + n  (global row of the last accepted token)
+ *   bonus[b]    = g[last_pos[b]]  (the target's own next token, committed too)
+ *   path[b*path_stride + j] = j for j < n, -1 after (may be NULL)
+ */
+int oracle_verify_chain(const int32_t* g, const int32_t* draft, const int32_t* pos_off,
+                        const int32_t* node_off, int B, int32_t* n_accept, int32_t* bonus,
+                        int32_t* last_pos, int32_t* path, int path_stride) {
+    if (!g || !draft || !pos_off || !node_off || B < 0) return 1;
+    for (int b = 0; b < B; ++b) {
+        int root = pos_off[b];
+        int K = node_off[b + 1] - node_off[b];
+        const int32_t* dr = draft + node_off[b];
+        int n = 0;
+        while (n < K && dr[n] == g[root + n]) n++;
+        n_accept[b] = n;
+        last_pos[b] = root + n;
+        bonus[b] = g[root + n];
+        if (path)
+            for (int j = 0; j < path_stride; ++j) path[(int64_t)b * path_stride + j] = j < n ? j : -1;
+    }
+    return 0;
+}
+
+/*
+ * EAGLE-3 tree verification.  Sequence b has nodes node_off[b] ..
+ * node_off[b+1]-1 with sequence-local parent indices (-1 = root, otherwise
+ * parent < node) and draft tokens tok[].  Node i of sequence b is verified
+ * at row pos_off[b]+1+i; the root at row pos_off[b].
+ *   node i is accepted iff its token equals the target choice at its
+ *   parent's row and its parent is accepted (the root always is);
+ *   depth(i) = 1 + depth(parent) with depth(root) = 0;
+ *   the deepest accepted node (lowest index on a tie) ends the accepted path;
+ *   n_accept = its depth (0 when no node is accepted), last_pos = its row
+ *   (the root row when none), bonus = g[last_pos], path = node ids from
+ *   depth 1 down to it, -1 padded (may be NULL).
+ * Returns 2 if a parent index is out of range (that sequence gets -1s).
+ */
+int oracle_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* parent,
+                       const int32_t* node_off, const int32_t* pos_off, int B, int32_t* n_accept,
+                       int32_t* bonus, int32_t* last_pos, int32_t* path, int path_stride) {
+    if (!g || !tok || !parent || !pos_off || !node_off || B < 0) return 1;
+    int rc = 0;
+    for (int b = 0; b < B; ++b) {
+        int root = pos_off[b];
+        int N = node_off[b + 1] - node_off[b];
+        const int32_t* tk = tok + node_off[b];
+        const int32_t* pa = parent + node_off[b];
+        char* acc = (char*)calloc((size_t)N + 1, 1);
+        int* depth = (int*)calloc((size_t)N + 1, sizeof(int));
+        int bad = 0, best = -1, best_depth = 0;
+        for (int i = 0; i < N; ++i) {
+            int p = pa[i];
+            if (p < -1 || p >= i) { bad = 1; break; }
+            int prow = (p < 0) ? root : root + 1 + p;
+            int parent_acc = (p < 0) ? 1 : acc[p];
+            acc[i] = (char)(parent_acc && tk[i] == g[prow]);
+            depth[i] = 1 + ((p < 0) ? 0 : depth[p]);
+            if (acc[i] && depth[i] > best_depth) { best_depth = depth[i]; best = i; }
+        }
+        if (bad) {
+            rc = 2;
+            n_accept[b] = bonus[b] = last_pos[b] = -1;
+            if (path) for (int j = 0; j < path_stride; ++j) path[(int64_t)b * path_stride + j] = -1;
+        } else {
+            n_accept[b] = best_depth;
+            last_pos[b] = best < 0 ? root : root + 1 + best;
+            bonus[b] = g[last_pos[b]];
+            if (path) {
+                for (int j = 0; j < path_stride; ++j) path[(int64_t)b * path_stride + j] = -1;
+                for (int i = best; i >= 0; i = pa[i])
+                    if (depth[i] - 1 < path_stride) path[(int64_t)b * path_stride + depth[i] - 1] = i;
+            }
+        }
+        free(acc);
+        free(depth);
+    }
+    return rc;
+}
+
+/* GELU in its exact form: x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)) (paper App. A). */
+double oracle_gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+/*
+ * Neural router f_theta and the threshold decision.  For each b, with
+ * h = hidden[rows[b]] (bf16):
+ *   z_j      = b1[j] + sum_k W1[j,k] * h[k]          (W1 row-major [m, d])
+ *   delta[b] = b2 + sum_j w2[j] * GELU(z_j)           (dropout is the identity)
+ *   route[b] = 1 (EAGLE-3) if delta[b] > tau else 0 (DFlash)
+ */
+int oracle_router(const uint16_t* hidden, const int32_t* rows, int B, int64_t d, int64_t m,
+                  const float* W1, const float* b1, const float* w2, double b2, double tau,
+                  double* delta, int32_t* route) {
+    if (!hidden || !rows || !W1 || !b1 || !w2 || !delta || !route || B < 0) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const uint16_t* h = hidden + (int64_t)rows[b] * d;
+        double out = b2;
+        for (int64_t j = 0; j < m; ++j) {
+            double z = b1[j];
+            for (int64_t k = 0; k < d; ++k) z += (double)W1[j * d + k] * bf16_value(h[k]);
+            out += (double)w2[j] * oracle_gelu(z);
+        }
+        delta[b] = out;
+        route[b] = out > tau ? 1 : 0;
+    }
+    return 0;
+}
+
+typedef struct { double v; int32_t id; } scored_id;
+
+/* order: higher logit first, lower id first on equal logits */
+static int by_logit_desc(const void* a, const void* b) {
+    const scored_id* x = (const scored_id*)a;
+    const scored_id* y = (const scored_id*)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+/*
+ * EAGLE-3 draft head + top-k + draft-to-target map.  For each b:
+ *   logits over the draft vocabulary L_v = <x_b, Wd_v>, v < Vd;
+ *   sort all Vd (logit desc, id asc); the first k draft ids, their logits,
+ *   and their target ids d2t[id];
+ *   lse[b]     = log sum_v exp(L_v)   (may be NULL)
+ *   min_gap[b] = smallest difference between consecutive sorted logits among
+ *                the first k+1 (may be NULL; used by the input generator).
+ */
+int oracle_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int64_t d,
+                      int64_t Vd, int k, int32_t* draft_ids, int32_t* tids, double* vals, double* lse,
+                      double* min_gap) {
+    if (!x || !Wd || !d2t || B < 0 || k < 1 || k > Vd) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        scored_id* s = (scored_id*)malloc((size_t)Vd * sizeof(scored_id));
+        for (int64_t v = 0; v < Vd; ++v) {
+            s[v].v = logit(x + (int64_t)b * d, Wd + v * d, d);
+            s[v].id = (int32_t)v;
+        }
+        qsort(s, (size_t)Vd, sizeof(scored_id), by_logit_desc);
+        for (int j = 0; j < k; ++j) {
+            if (draft_ids) draft_ids[(int64_t)b * k + j] = s[j].id;
+            if (tids) tids[(int64_t)b * k + j] = d2t[s[j].id];
+            if (vals) vals[(int64_t)b * k + j] = s[j].v;
+        }
+        if (lse) {
+            double mx = s[0].v, acc = 0.0;
+            for (int64_t v = 0; v < Vd; ++v) acc += exp(s[v].v - mx);
+            lse[b] = mx + log(acc);
+        }
+        if (min_gap) {
+            double mg = INFINITY;
+            for (int j = 0; j < k && j + 1 < Vd; ++j)
+                if (s[j].v - s[j + 1].v < mg) mg = s[j].v - s[j + 1].v;
+            min_gap[b] = mg;
+        }
+        free(s);
+    }
+    return 0;
+}
+
+/*
+ * One verify-and-route round (paper Sec. 3.2): target argmax at every
+ * verified row, acceptance per sequence (kind[b] 0 = DFlash chain,
+ * 1 = EAGLE-3 tree; kind NULL = all trees), then the router on the hidden
+ * state of each sequence's last accepted row.
+ */
+int oracle_round(const uint16_t* hidden, const uint16_t* W, int64_t d, int64_t V, const int32_t* pos_off,
+                 const int32_t* node_off, const int32_t* kind, const int32_t* tok, const int32_t* parent,
+                 int B, int64_t m, const float* W1, const float* b1, const float* w2, double b2, double tau,
+                 int32_t* ids, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
+                 int path_stride, double* delta, int32_t* route) {
+    int64_t P = pos_off[B];
+    int rc = oracle_lmhead_argmax(hidden, W, P, d, V, ids, NULL, NULL);
+    if (rc) return rc;
+    for (int b = 0; b < B; ++b) {
+        int32_t* pb = path ? path + (int64_t)b * path_stride : NULL;
+        int one_kind = kind ? kind[b] : 1;
+        /* a single sequence at a time, viewed through its own offsets */
+        int32_t po[2] = {0, pos_off[b + 1] - pos_off[b]};
+        int32_t no[2] = {0, node_off[b + 1] - node_off[b]};
+        int32_t na, bo, lp;
+        if (one_kind == 0)
+            rc = oracle_verify_chain(ids + pos_off[b], tok + node_off[b], po, no, 1, &na, &bo, &lp, pb,
+                                     path_stride);
+        else
+            rc = oracle_verify_tree(ids + pos_off[b], tok + node_off[b], parent + node_off[b], no, po, 1,
+                                    &na, &bo, &lp, pb, path_stride);
+        n_accept[b] = na;
+        bonus[b] = bo;
+        last_pos[b] = lp < 0 ? -1 : lp + pos_off[b];
+        if (rc) return rc;
+    }
+    return oracle_router(hidden, last_pos, B, d, m, W1, b1, w2, b2, tau, delta, route);
+}

@@ -1,0 +1,340 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each check takes an ``oracle.Oracle`` and raises AssertionError on a
+mismatch.  Expected values come from brute force written differently from
+the oracle (walk-to-root for trees, numpy/scipy library routines for dot
+products, sorting, erf and log-sum-exp), closed forms, textbook constants,
+and the hand-worked fixtures under tests/golden/.  tests/test_oracle_mutants.py
+compiles deliberately broken copies of the oracle and asserts that these
+checks catch each one.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+
+import numpy as np
+from scipy.special import erf, logsumexp
+
+from speculative_decoding_verify_lm_gb300.synth import bf16_bits_to_f32, to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rand_bf16(rng, shape, std):
+    return to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+def _f64(bits):
+    return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def read_cases(name):
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for ln in f:
+            ln = ln.strip()
+            if not ln or ln.startswith("#"):
+                continue
+            if ln.startswith("case "):
+                cur = {"name": ln[5:]}
+                cases.append(cur)
+                continue
+            key, _, val = ln.partition(":")
+            val = val.strip()
+            if key == "expect":
+                exp = {}
+                for item in val.split():
+                    k, _, v = item.partition("=")
+                    exp[k] = [int(t) for t in v.split(",") if t] if k == "path" else int(v)
+                cur["expect"] = exp
+            else:
+                cur[key] = [int(t) for t in val.split()]
+    return cases
+
+
+# ---------------------------------------------------------------- LM head argmax
+def check_argmax_bruteforce(o):
+    """ids / max logit / top-2 gap against numpy float64 matmul + a full sort.
+
+    Shapes are pairwise distinct so a transposed operand cannot pass."""
+    rng = np.random.default_rng(1)
+    for P, d, V in [(1, 8, 5), (5, 24, 37), (7, 40, 301), (3, 16, 1)]:
+        h = _rand_bf16(rng, (P, d), 1.0)
+        W = _rand_bf16(rng, (V, d), 0.2)
+        L = _f64(h) @ _f64(W).T
+        ids, mx, gap = o.lmhead_argmax(h, W)
+        for p in range(P):
+            order = sorted(range(V), key=lambda v: (-L[p, v], v))
+            assert ids[p] == order[0], (P, d, V, p)
+            assert abs(mx[p] - L[p, order[0]]) <= 1e-12 * max(1.0, abs(L[p, order[0]]))
+            if V > 1:
+                want = L[p, order[0]] - L[p, order[1]]
+                assert abs(gap[p] - want) <= 1e-12 * max(1.0, abs(L[p]).max()), (gap[p], want)
+            else:
+                assert gap[p] == math.inf
+
+
+def check_argmax_ties(o):
+    """Equal maximal logits: the lowest id wins and the gap is exactly 0."""
+    rng = np.random.default_rng(2)
+    d, V = 16, 12
+    h = to_bf16_bits(np.abs(rng.standard_normal((2, d))).astype(np.float32) + np.float32(0.1))
+    W = _rand_bf16(rng, (V, d), 0.05)
+    W[3] = to_bf16_bits(np.full(d, 4.0, np.float32))     # identical rows, far above the rest
+    W[7] = W[3]
+    ids, mx, gap = o.lmhead_argmax(h, W)
+    L = _f64(h) @ _f64(W).T
+    assert list(ids) == [3, 3] and list(gap) == [0.0, 0.0] and np.allclose(mx, L[:, 3], rtol=1e-12)
+
+
+def check_argmax_closed_form(o):
+    """One-hot weight rows: logit(p, v) = c_v * h[p, v mod d], exact in binary."""
+    d, V, P = 8, 20, 3
+    hv = np.array([[1, -2, 3, 0.5, -1, 2, 0.25, 1.5],
+                   [-1, -1, -1, -1, -1, -1, -1, -4],
+                   [2, 2, 2, 2, 2, 2, 2, 2]], np.float32)
+    c = np.array([(v % 7) - 3 for v in range(V)], np.float32)
+    Wv = np.zeros((V, d), np.float32)
+    for v in range(V):
+        Wv[v, v % d] = c[v]
+    ids, mx, gap = o.lmhead_argmax(to_bf16_bits(hv), to_bf16_bits(Wv))
+    for p in range(P):
+        L = [float(c[v]) * float(hv[p, v % d]) for v in range(V)]
+        best = max(L)
+        first = L.index(best)
+        second = max(L[:first] + L[first + 1:])
+        assert ids[p] == first and mx[p] == best and gap[p] == best - second, (p, ids[p], first)
+
+
+# ---------------------------------------------------------------- verification
+def _pack(seqs):
+    """seqs: list of (g_rows, tok, parent) -> packed arrays + offsets."""
+    pos_off, node_off = [0], [0]
+    for g, tok, _ in seqs:
+        pos_off.append(pos_off[-1] + len(g))
+        node_off.append(node_off[-1] + len(tok))
+    g = np.concatenate([np.asarray(s[0], np.int32) for s in seqs])
+    tok = np.concatenate([np.asarray(s[1], np.int32) for s in seqs]) if node_off[-1] else np.zeros(0, np.int32)
+    par = np.concatenate([np.asarray(s[2], np.int32) for s in seqs]) if node_off[-1] else np.zeros(0, np.int32)
+    return g, tok, par, np.array(pos_off, np.int32), np.array(node_off, np.int32)
+
+
+def check_chain_golden(o):
+    cases = read_cases("chains.txt")
+    seqs = [(c["g"], c["draft"], list(range(-1, len(c["draft"]) - 1))) for c in cases]
+    g, tok, _, pos_off, node_off = _pack(seqs)
+    n, bonus, last, path = o.verify_chain(g, tok, pos_off, node_off, path_stride=16)
+    for b, c in enumerate(cases):
+        e = c["expect"]
+        assert n[b] == e["n"] and bonus[b] == e["bonus"] and last[b] - pos_off[b] == e["last"], c["name"]
+        assert list(path[b][: e["n"]]) == list(range(e["n"])) and all(path[b][e["n"]:] == -1), c["name"]
+
+
+def check_tree_golden(o):
+    cases = read_cases("trees.txt")
+    seqs = [(c["g"], c["tok"], c["parent"]) for c in cases]
+    g, tok, par, pos_off, node_off = _pack(seqs)
+    n, bonus, last, path, rc = o.verify_tree(g, tok, par, node_off, pos_off, path_stride=8)
+    assert rc == 0
+    for b, c in enumerate(cases):
+        e = c["expect"]
+        assert n[b] == e["n"], (c["name"], n[b])
+        assert bonus[b] == e["bonus"] and last[b] - pos_off[b] == e["last"], c["name"]
+        assert [x for x in path[b] if x >= 0] == e["path"], (c["name"], path[b])
+
+
+def _brute_tree(g, tok, parent):
+    """Walk every node up to the root and require every hop to match."""
+    N = len(tok)
+
+    def depth(i):
+        return 0 if i < 0 else 1 + depth(parent[i])
+
+    def row(i):
+        return 0 if i < 0 else i + 1
+
+    acc_nodes = []
+    for i in range(N):
+        ok, j = True, i
+        while j >= 0:
+            if tok[j] != g[row(parent[j])]:
+                ok = False
+                break
+            j = parent[j]
+        if ok:
+            acc_nodes.append(i)
+    if not acc_nodes:
+        return 0, 0, []
+    best = min(acc_nodes, key=lambda i: (-depth(i), i))
+    path, j = [], best
+    while j >= 0:
+        path.append(j)
+        j = parent[j]
+    return depth(best), best + 1, path[::-1]
+
+
+def check_tree_bruteforce(o, max_nodes=6):
+    """Every parent array with parent[i] in [-1, i) up to ``max_nodes`` nodes,
+    tokens and target choices over a 2-letter alphabet."""
+    rng = np.random.default_rng(3)
+    seqs, expect = [], []
+    for N in range(0, max_nodes + 1):
+        for parent in itertools.product(*[range(-1, i) for i in range(N)]):
+            for _ in range(2):
+                tok = rng.integers(0, 2, N).tolist()
+                g = rng.integers(0, 2, N + 1).tolist()
+                seqs.append((g, tok, list(parent)))
+                expect.append(_brute_tree(g, tok, list(parent)))
+    g, tok, par, pos_off, node_off = _pack(seqs)
+    n, bonus, last, path, rc = o.verify_tree(g, tok, par, node_off, pos_off, path_stride=max_nodes)
+    assert rc == 0
+    for b, (en, elast, epath) in enumerate(expect):
+        assert n[b] == en and last[b] - pos_off[b] == elast, (b, seqs[b], n[b], en)
+        assert bonus[b] == seqs[b][0][elast]
+        assert [x for x in path[b] if x >= 0] == epath
+
+
+def check_chain_is_linear_tree(o):
+    rng = np.random.default_rng(4)
+    seqs = []
+    for _ in range(200):
+        K = int(rng.integers(0, 17))
+        g = rng.integers(0, 3, K + 1).tolist()
+        draft = rng.integers(0, 3, K).tolist()
+        seqs.append((g, draft, list(range(-1, K - 1))))
+    g, tok, par, pos_off, node_off = _pack(seqs)
+    c = o.verify_chain(g, tok, pos_off, node_off, path_stride=16)
+    t = o.verify_tree(g, tok, par, node_off, pos_off, path_stride=16)
+    for a, b in zip(c[:4], t[:4]):
+        assert np.array_equal(a, b)
+
+
+def check_tree_bad_parent(o):
+    seqs = [([1, 2, 3], [1, 2], [-1, 1]), ([5, 6], [5], [-1]), ([1, 2], [1], [-2])]
+    g, tok, par, pos_off, node_off = _pack(seqs)
+    n, bonus, last, path, rc = o.verify_tree(g, tok, par, node_off, pos_off, path_stride=2)
+    assert rc == 2
+    assert n[0] == bonus[0] == last[0] == -1 and n[2] == -1
+    assert n[1] == 1 and bonus[1] == 6
+
+
+# ---------------------------------------------------------------- router
+PHI_1 = 0.8413447460685429     # standard normal CDF at 1 (textbook table value)
+PHI_3 = 0.9986501019683699     # ... at 3
+
+
+def check_gelu_values(o):
+    assert o.gelu(0.0) == 0.0
+    assert abs(o.gelu(1.0) - PHI_1) < 1e-15
+    assert abs(o.gelu(-1.0) - (-(1.0 - PHI_1))) < 1e-15
+    assert abs(o.gelu(3.0) - 3.0 * PHI_3) < 1e-14
+    assert o.gelu(10.0) == 10.0
+    assert -1e-20 < o.gelu(-10.0) <= 0.0
+
+
+def _router_numpy(h_bits, W1, b1, w2, b2):
+    z = W1.astype(np.float64) @ _f64(h_bits).T + b1.astype(np.float64)[:, None]
+    a = 0.5 * z * (1.0 + erf(z / np.sqrt(2.0)))
+    return b2 + w2.astype(np.float64) @ a
+
+
+def check_router_closed_forms(o):
+    rng = np.random.default_rng(5)
+    d, m, B = 24, 10, 4
+    h = _rand_bf16(rng, (B, d), 1.0)
+    rows = np.arange(B, dtype=np.int32)
+    b1 = rng.standard_normal(m).astype(np.float32)
+    w2 = rng.standard_normal(m).astype(np.float32)
+    b2 = 0.375
+    # W1 = 0: delta = b2 + sum_j w2_j * GELU(b1_j), independent of h
+    delta, _ = o.router(h, rows, np.zeros((m, d), np.float32), b1, w2, b2, 0.0)
+    want = b2 + sum(float(w2[j]) * 0.5 * float(b1[j]) * (1.0 + math.erf(float(b1[j]) / math.sqrt(2.0)))
+                    for j in range(m))
+    assert np.allclose(delta, want, rtol=0, atol=1e-13)
+    # one unit far on the linear side of GELU: delta = b2 + w2 * (b1 + c * h[k])
+    k, c = 5, 0.75
+    W1 = np.zeros((1, d), np.float32)
+    W1[0, k] = c
+    delta, _ = o.router(h, rows, W1, np.array([20.0], np.float32), np.array([-0.5], np.float32), b2, 0.0)
+    want = b2 - 0.5 * (20.0 + c * _f64(h)[:, k])
+    assert np.allclose(delta, want, rtol=0, atol=1e-12)
+    # random weights against numpy / scipy
+    W1 = (rng.standard_normal((m, d)) * 0.3).astype(np.float32)
+    delta, _ = o.router(h, rows[::-1].copy(), W1, b1, w2, b2, 0.0)
+    want = _router_numpy(h[::-1], W1, b1, w2, b2)
+    assert np.allclose(delta, want, rtol=1e-12, atol=1e-12)
+
+
+def check_route_strict(o):
+    """route = 1 only when the prediction strictly exceeds tau; tau -> -inf / +inf
+    gives all-EAGLE-3 / all-DFlash (the standalone drafters)."""
+    d, m = 8, 3
+    h = np.zeros((2, d), np.uint16)
+    rows = np.array([0, 1], np.int32)
+    W1 = np.zeros((m, d), np.float32)
+    z = np.zeros(m, np.float32)
+    b2 = 1.25
+    _, r = o.router(h, rows, W1, z, z, b2, 1.25)
+    assert list(r) == [0, 0]
+    _, r = o.router(h, rows, W1, z, z, b2, 1.2499999)
+    assert list(r) == [1, 1]
+    rng = np.random.default_rng(6)
+    hh = _rand_bf16(rng, (2, d), 1.0)
+    W1 = rng.standard_normal((m, d)).astype(np.float32)
+    w2 = rng.standard_normal(m).astype(np.float32)
+    assert list(o.router(hh, rows, W1, z, w2, 0.0, -math.inf)[1]) == [1, 1]
+    assert list(o.router(hh, rows, W1, z, w2, 0.0, math.inf)[1]) == [0, 0]
+
+
+def router_param_count(d, m):
+    return d * m + m + m + 1
+
+
+def check_router_param_table():
+    """m = d/8 with both biases reproduces the sizes printed in Table 6."""
+    with open(os.path.join(GOLDEN, "router_param_counts.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    for name, d, printed in rows:
+        n = router_param_count(int(d), int(d) // 8)
+        assert round(n / 1e6, 2) == float(printed), (name, n)
+
+
+# ---------------------------------------------------------------- draft head
+def check_topk_bruteforce(o):
+    rng = np.random.default_rng(7)
+    for B, d, Vd, k in [(1, 16, 40, 10), (3, 24, 100, 5), (2, 8, 10, 10), (2, 32, 257, 1)]:
+        x = _rand_bf16(rng, (B, d), 1.0)
+        Wd = _rand_bf16(rng, (Vd, d), 0.3)
+        d2t = rng.permutation(10 * Vd)[:Vd].astype(np.int32)
+        L = _f64(x) @ _f64(Wd).T
+        dids, tids, vals, lse, mg = o.draft_topk(x, Wd, d2t, k)
+        for b in range(B):
+            order = np.lexsort((np.arange(Vd), -L[b]))
+            assert list(dids[b]) == list(order[:k])
+            assert list(tids[b]) == list(d2t[order[:k]])
+            assert np.allclose(vals[b], L[b, order[:k]], rtol=1e-12, atol=1e-12)
+            assert abs(lse[b] - logsumexp(L[b])) < 1e-10
+            srt = L[b, order]
+            want = min(srt[j] - srt[j + 1] for j in range(min(k, Vd - 1))) if Vd > 1 else math.inf
+            assert abs(mg[b] - want) < 1e-10
+
+
+def check_topk_ties(o):
+    """Equal logits keep the lower draft id first."""
+    rng = np.random.default_rng(8)
+    d, Vd = 8, 12
+    x = _rand_bf16(rng, (1, d), 1.0)
+    Wd = _rand_bf16(rng, (Vd, d), 0.01)
+    Wd[9] = to_bf16_bits(np.sign(bf16_bits_to_f32(x[0]) + 1e-3) * np.float32(2.0))
+    Wd[2] = Wd[9]
+    d2t = np.arange(Vd, dtype=np.int32)
+    dids, _, vals, _, mg = o.draft_topk(x, Wd, d2t, 3)
+    assert list(dids[0][:2]) == [2, 9] and vals[0][0] == vals[0][1] and mg[0] == 0.0
+
+
+ALL_CHECKS = [check_argmax_bruteforce, check_argmax_ties, check_argmax_closed_form, check_chain_golden,
+              check_tree_golden, check_tree_bruteforce, check_chain_is_linear_tree, check_tree_bad_parent,
+              check_gelu_values, check_router_closed_forms, check_route_strict, check_topk_bruteforce,
+              check_topk_ties]

@@ -1,0 +1,64 @@
+"""Plausible mistakes planted in copies of the CPU oracle are caught by the pins.
+
+Each mutant is one textual edit of oracle/wf_oracle.c, compiled to a scratch
+directory on the CPU; the test asserts that at least one of the named pin
+checks fails against it (and, as a control, that all of them pass on the
+unmodified oracle)."""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "wf_oracle.c")
+
+MUTANTS = [
+    ("argmax keeps the last of equal maxima", "if (L > best) {", "if (L >= best) {",
+     [pins.check_argmax_ties]),
+    ("weight row stride dropped (operand misindexed)", "logit(h + p * d, W + v * d, d)", "logit(h + p * d, W + v, d)",
+     [pins.check_argmax_bruteforce]),
+    ("second-best not updated when the best moves", "second = best;\n                best = L;",
+     "best = L;", [pins.check_argmax_bruteforce]),
+    ("tree ignores the parent's acceptance", "int parent_acc = (p < 0) ? 1 : acc[p];", "int parent_acc = 1;",
+     [pins.check_tree_golden, pins.check_tree_bruteforce]),
+    ("tree compares against the node's own row", "int prow = (p < 0) ? root : root + 1 + p;",
+     "int prow = root + 1 + i;", [pins.check_tree_golden, pins.check_tree_bruteforce]),
+    ("tree keeps the highest index on equal depth", "depth[i] > best_depth", "depth[i] >= best_depth",
+     [pins.check_tree_golden, pins.check_tree_bruteforce]),
+    ("chain bonus taken one row early", "bonus[b] = g[root + n];", "bonus[b] = g[root + (n > 0 ? n - 1 : 0)];",
+     [pins.check_chain_golden]),
+    ("chain compares draft j with row j+1", "dr[n] == g[root + n]", "dr[n] == g[root + n + 1]",
+     [pins.check_chain_golden, pins.check_chain_is_linear_tree]),
+    ("router drops the first-layer bias", "double z = b1[j];", "double z = 0.0;",
+     [pins.check_router_closed_forms]),
+    ("router drops the second-layer bias", "double out = b2;", "double out = 0.0;",
+     [pins.check_router_closed_forms, pins.check_route_strict]),
+    ("tanh approximation of GELU", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+     "return 0.5 * x * (1.0 + tanh(0.7978845608028654 * (x + 0.044715 * x * x * x)));",
+     [pins.check_gelu_values]),
+    ("route on >= instead of >", "route[b] = out > tau ? 1 : 0;", "route[b] = out >= tau ? 1 : 0;",
+     [pins.check_route_strict]),
+    ("top-k ties keep the higher id", "return (x->id > y->id) - (x->id < y->id);",
+     "return (x->id < y->id) - (x->id > y->id);", [pins.check_topk_ties]),
+    ("log-sum-exp without the max shift", "lse[b] = mx + log(acc);", "lse[b] = log(acc);",
+     [pins.check_topk_bruteforce]),
+    ("top-k maps through the wrong id", "tids[(int64_t)b * k + j] = d2t[s[j].id];",
+     "tids[(int64_t)b * k + j] = s[j].id;", [pins.check_topk_bruteforce]),
+]
+
+
+@pytest.mark.parametrize("desc,old,new,checks", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, desc, old, new, checks):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not unique: {old!r}"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    mo = oracle.Oracle(oracle.compile_c(str(mpath), str(tmp_path / "libmutant.so")))
+    caught = []
+    for chk in checks:
+        try:
+            chk(mo)
+        except AssertionError:
+            caught.append(chk.__name__)
+    assert caught, f"no pin caught: {desc}"
