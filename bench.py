@@ -1,0 +1,391 @@
+#!/usr/bin/env python3
+"""Benchmark of one WhiFlash verify-and-route round on GB300.
+
+A step is one whole round through the library's C ABI (wf_round): target
+LM-head argmax at every verified row, chain / tree acceptance with the bonus
+token, the neural router on each sequence's last accepted row, and (for the
+EAGLE-3 workloads) the draft head's top-10.  Inputs are the seeded synthetic
+workloads of ``speculative_decoding_verify_lm_gb300.synth`` (default: the
+Qwen3-4B-shaped DFlash chain, batch 1, hidden 2560, vocabulary 151,936).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a deliberately slow baseline, not a GPU program).
+Several GPUs run independent replicas (one process per GPU, weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified positions/s and accepted tokens/s per round; % of HBM/TC roofline"
+UNIT = "verified positions/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index 0-4 (default 1: DFlash chain, batch 1)")
+    ap.add_argument("--router-width", type=int, default=None, help="override m (the paper's m = d/8 = 320)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def allreduce_max(pg, value: float, device) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(pg, value: float, device) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        for ln in out.splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verify_lm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j["hbm_gbs"], j["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def traffic_for(kernel: str, workload: str):
+    """ncu DRAM bytes per launch recorded under profiles/ for this exact source, else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(f"{kernel}@{workload}")
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def cpu_sample(wl, budget_s: float):
+    """Time the oracle round on a bounded sample of the workload; returns (positions/s, sample text, cores)."""
+    import oracle
+    o = oracle.default()
+    B = wl.B
+    # sequences in order until the sample is about budget-sized (one probe round first)
+    seqs, rows = [], 0
+    t_probe = None
+    for b in range(B):
+        seqs.append(b)
+        rows += int(wl.pos_off[b + 1] - wl.pos_off[b])
+        if rows >= 17:
+            break
+    sub = _subset(wl, seqs)
+    t0 = time.perf_counter()
+    o.round_(*sub)
+    t_probe = time.perf_counter() - t0
+    reps = max(1, int(budget_s / max(t_probe, 1e-6)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        o.round_(*sub)
+    dt = time.perf_counter() - t0
+    P_sub = int(sub[2][-1])
+    return P_sub * reps / dt, f"{reps} oracle rounds over {len(seqs)} of {B} sequences ({P_sub} verified rows each)", \
+        o.threads(), dt / reps, P_sub
+
+
+def _subset(wl, seqs):
+    rows = np.concatenate([np.arange(wl.pos_off[b], wl.pos_off[b + 1]) for b in seqs])
+    nodes = np.concatenate([np.arange(wl.node_off[b], wl.node_off[b + 1]) for b in seqs])
+    lens = np.array([wl.pos_off[b + 1] - wl.pos_off[b] for b in seqs])
+    pos_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    node_off = np.concatenate([[0], np.cumsum(lens - 1)]).astype(np.int32)
+    return (wl.hidden[rows], wl.W, pos_off, node_off, wl.kind[seqs], wl.tok[nodes], wl.parent[nodes], wl.W1,
+            wl.b1, wl.w2, wl.b2, wl.tau, wl.max_depth)
+
+
+def run_reference(args, cfg_name, wl):
+    """--impl reference: the CPU oracle, as it stands, on the host cores."""
+    import oracle
+    o = oracle.default()
+    per_step_budget = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    value, sample, cores, t_round, P_sub = cpu_sample(wl, per_step_budget)
+    sub = _subset(wl, list(range(min(wl.B, 1))))
+    for _ in range(args.warmup):
+        o.round_(*sub)
+    t0 = time.perf_counter()
+    acc = 0
+    for _ in range(args.steps):
+        out = o.round_(*sub)
+        acc += int((out["n_accept"] + 1).sum())
+    dt = time.perf_counter() - t0
+    P1 = int(sub[2][-1])
+    val = P1 * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg_name, "rows_per_step": P1},
+            "accepted_tokens_per_s": acc / dt,
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: one oracle round over the first sequence ({P1} verified rows)"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup(args)
+    from speculative_decoding_verify_lm_gb300 import synth
+    cfg = synth.CONFIGS[args.config]
+    cfg_name = cfg.name if args.router_width is None else f"{cfg.name}_m{args.router_width}"
+
+    if args.impl == "reference":
+        if rank == 0:
+            import oracle
+            wl = synth.make_workload(args.config, oracle.argmax_fn, reject=False, m=args.router_width,
+                                     plant_seqs=[0])
+            run_reference(args, cfg_name, wl)
+        return
+
+    import torch
+    from speculative_decoding_verify_lm_gb300 import wf
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wf.lib()
+
+    # ---- workload: weights on the device once; the library's own argmax plants the drafts
+    cache = {}
+
+    def gpu_argmax(W, rows):
+        key = id(W)
+        if key not in cache:
+            cache[key] = torch.from_numpy(W.view(np.int16)).to(device)
+        h = torch.from_numpy(np.ascontiguousarray(rows).view(np.int16)).to(device)
+        ws = wf.Workspace(h.shape[0], device=device)
+        ids = wf.wf_lmhead_argmax(h, cache[key], ws)
+        return ids.cpu().numpy(), None
+
+    wl = synth.make_workload(args.config, gpu_argmax, reject=False, m=args.router_width)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16  # noqa: E731
+                                   else np.ascontiguousarray(a)).to(device)
+    Wdev = cache[id(wl.W)]
+    draft = wl.Wd is not None
+    r = wf.Round(t(wl.hidden), Wdev, t(wl.pos_off), t(wl.node_off), t(wl.tok), t(wl.W1), t(wl.b1), t(wl.w2),
+                 wl.b2, wl.tau, kind=t(wl.kind), parent=t(wl.parent), path_stride=wl.max_depth,
+                 x=t(wl.x) if draft else None, Wd=t(wl.Wd) if draft else None, d2t=t(wl.d2t) if draft else None,
+                 k=wl.topk if draft else 0)
+    P, B, d, V = wl.P, wl.B, cfg.d, cfg.V
+    weight_bytes = V * d * 2 + (wl.Wd.nbytes if draft else 0) + wl.W1.nbytes
+    flush = weight_bytes < 2 * L2_BYTES
+    l2buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if flush else None
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(max(args.warmup, 3)):
+        r()
+    torch.cuda.synchronize(device)
+    code, info = r.ws.device_error()
+    if code:
+        raise RuntimeError(f"device error {code} (info {info}) during warm-up")
+
+    # ---- timed region: K whole rounds, CUDA events on the launching stream
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush:
+            l2buf.zero_()
+        ev[i][0].record(stream)
+        r()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dev_s = sum(step_ms) / 1e3
+    out = {k: (v.cpu().numpy() if v is not None else None) for k, v in r.out.items()}
+    accepted = int((out["n_accept"] + 1).sum())
+    max_s = allreduce_max(pg, dev_s, device)
+    tot_rows = allreduce_sum(pg, P * args.steps, device)
+    tot_acc = allreduce_sum(pg, accepted * args.steps, device)
+    value = tot_rows / max_s
+    launches_per_round = 3 + (2 if draft else 0)
+
+    # ---- the dominant kernel on its own (LM head), CUDA events per launch
+    hbm_peak, tc_peak, peak_src = measured_peaks()
+    ids_buf = torch.empty(P, dtype=torch.int32, device=device)
+    hdev = r.inputs["hidden"]
+    ws1 = wf.Workspace(P, device=device)
+    for _ in range(3):
+        wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush:
+            l2buf.zero_()
+        kev[i][0].record(stream)
+        wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)
+        kev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    k_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    alg_bytes = V * d * 2 + P * d * 2 + P * 4
+    alg_flops = 2.0 * P * V * d
+    hbm_bound = alg_flops / alg_bytes < (tc_peak * 1e12) / (hbm_peak * 1e9)
+    kernel_name = "gemm_select_kernel<1>"
+    if hbm_bound:
+        achieved = alg_bytes / (k_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak}
+    else:
+        achieved = alg_flops / (k_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak}
+    roof.update({"traffic": traffic_for(kernel_name, cfg_name), "kernel": kernel_name,
+                 "algorithmic_per_launch": alg_bytes if hbm_bound else alg_flops, "launch_ms": k_ms,
+                 "peak_source": f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'}, burst)"})
+
+    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    names_in = ["hidden", "tok", "parent", "pos_off", "node_off", "kind"] + (["x"] if draft else [])
+    host_in = {n: torch.from_numpy(np.ascontiguousarray(getattr(wl, n)).view(np.int16)
+                                   if getattr(wl, n).dtype == np.uint16 else np.ascontiguousarray(getattr(wl, n))
+                                   ).pin_memory() for n in names_in}
+    names_out = ["n_accept", "bonus", "last_pos", "delta_al", "route"] + (["tids"] if draft else [])
+    host_out = {n: torch.empty_like(r.out[n], device="cpu").pin_memory() for n in names_out}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    for _ in range(2):
+        for n in names_in:
+            r.inputs[n].copy_(host_in[n], non_blocking=True)
+        r()
+        for n in names_out:
+            host_out[n].copy_(r.out[n], non_blocking=True)
+        torch.cuda.synchronize(device)
+    if pg is not None:
+        pg.barrier()
+    e2e_s = 0.0   # per-step wall clock: copies in, round, results out, synchronise (L2 flush excluded)
+    for i in range(args.steps):
+        if flush:
+            l2buf.zero_()
+        torch.cuda.synchronize(device)
+        t1 = time.perf_counter()
+        for n in names_in:
+            r.inputs[n].copy_(host_in[n], non_blocking=True)
+        r()
+        for n in names_out:
+            host_out[n].copy_(r.out[n], non_blocking=True)
+        torch.cuda.synchronize(device)
+        e2e_s += time.perf_counter() - t1
+    e2e_max = allreduce_max(pg, e2e_s, device)
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, sample, cores, _, _ = cpu_sample(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": sum(step_ms) / len(step_ms), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg_name, "P": P, "B": B, "d": d, "V": V, "router_m": int(wl.W1.shape[0]),
+                   "draft_head": f"{cfg.Vd}x{d} top-{wl.topk}" if draft else None,
+                   "l2": "flushed between steps (working set < 2x L2)" if flush
+                   else f"inputs larger than L2 (weights {weight_bytes / 1e6:.0f} MB streamed per step)",
+                   "parallelism": f"replicas x{world}"},
+        "accepted_tokens_per_s": tot_acc / max_s,
+        "mean_acceptance_length": accepted / B,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": tot_rows / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "gpu_launches": launches_per_round * args.steps,
+        "impl": "ours",
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,256 @@
+/*
+ * wf.h - C ABI of the GB300 (sm_103a) verify-and-route library for WhiFlash
+ * token-level cross-paradigm speculative decoding.
+ *
+ * One speculation round of WhiFlash (WhiFlash paper, arXiv 2606.07710,
+ * Sec. 3.2 "Proposed Architecture"): the target model verifies the drafted
+ * candidates in parallel, decoding resumes from the last accepted token, and
+ * the token-level router picks the drafter for the next round (Sec. 3.3).
+ * This library covers the data-parallel arithmetic of that step once the
+ * target's final hidden states exist:
+ *
+ *   wf_lmhead_argmax  target LM head + greedy choice at every verified row
+ *   wf_verify_chain   DFlash block acceptance (longest matched prefix) + bonus
+ *   wf_verify_tree    EAGLE-3 tree acceptance (deepest matched root path) + bonus
+ *   wf_router_mlp     neural router f_theta and the threshold decision
+ *   wf_draft_topk     EAGLE-3 draft head, top-k, draft-to-target id map
+ *   wf_round          all of the above as one stream-ordered round
+ *
+ * Conventions shared by every call
+ * - Pointers named as device buffers must be device (or managed) memory
+ *   allocated by the caller; the library allocates nothing and keeps no
+ *   per-call state outside the caller's workspace.
+ * - bf16 tensors are passed as raw uint16 bit patterns, row-major, densely
+ *   packed (row stride = number of columns), 16-byte aligned.
+ * - Every call is asynchronous on `stream`: it validates its arguments on the
+ *   host, enqueues kernels and returns.  Host-detectable errors (NULL
+ *   pointers, sizes, alignment, workspace too small) are returned at once and
+ *   nothing is enqueued.
+ * - Data errors that only the device can see (a parent index outside
+ *   [-1, node), a sequence longer than WF_MAX_SEQ_NODES, a draft id with no
+ *   valid target id) set a sticky error word in the workspace and turn the
+ *   affected outputs into -1.  The device never traps; read the word with
+ *   wf_read_device_error.  Every wait inside a kernel is bounded
+ *   (wf_set_wait_timeout_ns); a wait that gives up records WF_ERR_TIMEOUT.
+ * - Workspace: caller-owned device memory of at least wf_workspace_bytes()
+ *   bytes, zeroed once with wf_workspace_init() before first use.  Calls
+ *   leave it zeroed where that matters, so it can be reused without
+ *   re-initialisation.  Calls that share a workspace must not overlap in time
+ *   (use one stream, or one workspace per stream).
+ */
+#ifndef WF_H
+#define WF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define WF_API __attribute__((visibility("default")))
+#else
+#define WF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL = the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* wf_stream_t;
+
+typedef enum wf_status {
+    WF_OK = 0,
+    WF_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size or alignment; nothing enqueued */
+    WF_ERR_WORKSPACE = 2,     /* workspace NULL, misaligned or below wf_workspace_bytes() */
+    WF_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+    WF_ERR_UNSUPPORTED = 4,   /* device is not sm_103 (GB300) or shape outside the kernels' range */
+    WF_ERR_BAD_DATA = 5,      /* device-side: malformed tree / id data (see above) */
+    WF_ERR_TIMEOUT = 6        /* device-side: a bounded wait gave up */
+} wf_status;
+
+/* Longest drafted sequence (nodes, not rows) a single sequence may carry. */
+#define WF_MAX_SEQ_NODES 256
+/* Largest k of wf_draft_topk. */
+#define WF_MAX_TOPK 16
+
+/* Human-readable name of a status code (static storage). */
+WF_API const char* wf_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+WF_API int wf_version(void);
+
+/*
+ * Workspace size (bytes) sufficient for every call below with at most
+ * P verified rows, B sequences, router width m, draft vocabulary Vd and
+ * top-k k (pass 0 for Vd / k when the draft head is not used).
+ */
+WF_API size_t wf_workspace_bytes(int P, int B, int m, int Vd, int k);
+
+/* Zero a workspace (asynchronously on `stream`).  Needed once before first use. */
+WF_API wf_status wf_workspace_init(void* ws, size_t ws_bytes, wf_stream_t stream);
+
+/*
+ * Copy the sticky device error word out of the workspace (synchronises
+ * `stream`).  *code is a wf_status (WF_OK if none), *info a call-specific
+ * detail (the offending sequence index for WF_ERR_BAD_DATA).  clear != 0
+ * resets the word afterwards.
+ */
+WF_API wf_status wf_read_device_error(void* ws, int* code, int* info, int clear, wf_stream_t stream);
+
+/*
+ * Upper bound (ns) on any single wait inside a kernel before it gives up with
+ * WF_ERR_TIMEOUT (process-wide; default 2e9 = 2 s; 0 restores the default).
+ * Applies to launches made after the call.
+ */
+WF_API void wf_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Target LM head fused with the greedy choice (WhiFlash paper Sec. 3.3.1:
+ * under greedy decoding the target's next token at a verified position is
+ * the argmax of its next-token distribution; Sec. 4 "Evaluation": greedy
+ * decoding; vocabulary 151,936 and hidden size 2560 for Qwen3-4B per the
+ * Qwen3-4B-EAGLE3 card, "Technical Specifications").
+ *
+ *   ids[p]      = argmax_v sum_k hidden[p,k] * W[v,k]   (lowest v on a tie)
+ *   maxlogit[p] = that maximum logit (fp32), optional (NULL = not written)
+ *
+ * hidden   device, [P, d] bf16 bits, the target's final hidden states
+ * W        device, [V, d] bf16 bits, LM-head weight (out x in)
+ * P        rows, 1 <= P;  d % 8 == 0, 8 <= d <= 16384;  1 <= V < 2^31
+ * ids      device, [P] int32 out
+ * Logits are accumulated in fp32 on the tensor cores and never stored.
+ */
+WF_API wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
+                           int32_t* ids, float* maxlogit, void* ws, size_t ws_bytes,
+                           wf_stream_t stream);
+
+/*
+ * DFlash block verification (paper Sec. 3.2: the parallel block returns to
+ * the target for parallel verification; App. A: block size 16 for Qwen3).
+ * Sequence b owns verified rows pos_off[b] .. pos_off[b+1]-1; row pos_off[b]
+ * holds the last committed token, row pos_off[b]+1+j draft token j.  Its
+ * drafts are draft[node_off[b] .. node_off[b+1]-1]; node count = rows - 1.
+ *
+ *   n_accept[b] = largest n with draft[j] == g[pos_off[b]+j] for all j < n
+ *   last_pos[b] = pos_off[b] + n_accept[b]   (global row, feeds the router)
+ *   bonus[b]    = g[last_pos[b]]              (the target's own next token)
+ *   path[b*path_stride + j] = j for j < n, -1 otherwise (NULL = not written)
+ * Tokens committed this round (the paper's acceptance length, Sec. 4
+ * "Metrics") = n_accept + 1.
+ *
+ * g, draft, pos_off [B+1], node_off [B+1]: device int32.  Outputs: device int32 [B].
+ */
+WF_API wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t* pos_off,
+                          const int32_t* node_off, int B, int path_stride, int32_t* n_accept,
+                          int32_t* bonus, int32_t* last_pos, int32_t* path, void* ws,
+                          size_t ws_bytes, wf_stream_t stream);
+
+/*
+ * EAGLE-3 tree verification (paper Sec. 3.2: the autoregressive drafter
+ * produces a tree of candidates; App. A / Table 7: depth 8, top-k 10, 60
+ * draft tokens).  Same row / node layout as wf_verify_chain; parent[] holds
+ * sequence-local parent indices, -1 = the root, and parent[i] < i.
+ *
+ *   node i is accepted iff tok[i] == g[row of parent(i)] and parent(i) is
+ *   accepted (the root always is); n_accept = depth of the deepest accepted
+ *   node (lowest index on a tie; 0 if none); last_pos = its row (the root row
+ *   if none); bonus = g[last_pos]; path = its ancestors' node ids from depth 1
+ *   down, -1 padded, truncated at path_stride.
+ * A parent outside [-1, i) or more than WF_MAX_SEQ_NODES nodes sets
+ * WF_ERR_BAD_DATA (info = b) and writes -1 to that sequence's outputs.
+ */
+WF_API wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* parent,
+                         const int32_t* node_off, const int32_t* pos_off, int B, int path_stride,
+                         int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
+                         void* ws, size_t ws_bytes, wf_stream_t stream);
+
+/*
+ * Neural router and hardware-aware routing decision (paper Sec. 3.3.2; App. A
+ * "Neural Router Architecture": h -> Linear(d, m) -> GELU -> dropout ->
+ * Linear(m, 1), m = d/8 in the paper; route to the autoregressive drafter iff
+ * the predicted gain exceeds tau_neural).  Dropout is the identity at
+ * inference; GELU is the exact erf form.
+ *
+ *   z_j         = b1[j] + sum_k W1[j,k] * hidden[rows[b], k]
+ *   delta_al[b] = b2 + sum_j w2[j] * GELU(z_j)
+ *   route[b]    = 1 (EAGLE-3, autoregressive) if delta_al[b] > tau, else 0 (DFlash)
+ *
+ * hidden device [*, d] bf16 bits; rows device [B] int32 (row of each sequence,
+ * e.g. last_pos of a verify call); W1 device [m, d] fp32 row-major; b1, w2
+ * device [m] fp32; b2, tau host scalars.  d % 8 == 0; 1 <= m <= 65536.
+ * Outputs: delta_al device [B] fp32, route device [B] int32 (either may be NULL).
+ * fp32 arithmetic; the sum over j is taken in a fixed order (deterministic).
+ */
+WF_API wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int d, int m,
+                        const float* W1, const float* b1, const float* w2, float b2, float tau,
+                        float* delta_al, int32_t* route, void* ws, size_t ws_bytes,
+                        wf_stream_t stream);
+
+/*
+ * EAGLE-3 draft head with top-k and the draft-to-target id map (Qwen3-4B-EAGLE3
+ * card: fixed 32,000-id draft vocabulary, "top-k 10"; the draft vocabulary
+ * cannot propose target ids outside it).
+ *
+ *   logits L[b,v] = sum_k x[b,k] * Wd[v,k], v < Vd
+ *   for each b the k largest (logit desc, draft id asc):
+ *   draft_ids[b,j] (optional), tids[b,j] = d2t[draft id], vals[b,j] = logit (fp32)
+ *
+ * x device [B, d] bf16 bits (drafter hidden state); Wd device [Vd, d] bf16 bits;
+ * d2t device [Vd] int32 absolute target ids; 1 <= k <= WF_MAX_TOPK, k <= Vd.
+ * A d2t entry < 0 sets WF_ERR_BAD_DATA (info = b) and writes -1 for that id.
+ */
+WF_API wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d,
+                        int Vd, int k, int32_t* draft_ids, int32_t* tids, float* vals, void* ws,
+                        size_t ws_bytes, wf_stream_t stream);
+
+/*
+ * One whole verify-and-route round (paper Sec. 3.2 - 3.3): LM-head argmax at
+ * every verified row -> per-sequence acceptance (chain or tree by kind[b])
+ * -> router on each sequence's last accepted row -> route for the next round;
+ * plus, if Wd != NULL, the draft head's top-k for every sequence.  All stages
+ * are stream-ordered on `stream` with no host synchronisation.
+ */
+typedef struct wf_round_args {
+    /* verified rows */
+    const uint16_t* hidden;    /* [P, d] bf16 bits */
+    const uint16_t* W;         /* [V, d] bf16 bits */
+    int P, d, V;
+    /* sequences */
+    int B;
+    const int32_t* pos_off;    /* [B+1] */
+    const int32_t* node_off;   /* [B+1] */
+    const int32_t* kind;       /* [B] 0 = DFlash chain, 1 = EAGLE-3 tree; NULL = all trees */
+    const int32_t* tok;        /* [N] drafted target ids */
+    const int32_t* parent;     /* [N] tree parents; ignored for chains; NULL only if kind marks all chains */
+    int path_stride;           /* columns of path (0 = path not written) */
+    /* router */
+    int m;
+    const float* W1;           /* [m, d] */
+    const float* b1;           /* [m] */
+    const float* w2;           /* [m] */
+    float b2, tau;
+    /* draft head (optional: Wd == NULL skips it) */
+    const uint16_t* x;         /* [B, d] bf16 bits */
+    const uint16_t* Wd;        /* [Vd, d] bf16 bits */
+    const int32_t* d2t;        /* [Vd] */
+    int Vd, k;
+    /* outputs (device) */
+    int32_t* ids;              /* [P] target argmax at every row */
+    float* maxlogit;           /* [P] or NULL */
+    int32_t* n_accept;         /* [B] */
+    int32_t* bonus;            /* [B] */
+    int32_t* last_pos;         /* [B] */
+    int32_t* path;             /* [B, path_stride] or NULL */
+    float* delta_al;           /* [B] */
+    int32_t* route;            /* [B] */
+    int32_t* draft_ids;        /* [B, k] or NULL */
+    int32_t* tids;             /* [B, k] (needed if Wd != NULL) */
+    float* vals;               /* [B, k] or NULL */
+} wf_round_args;
+
+WF_API wf_status wf_round(const wf_round_args* args, void* ws, size_t ws_bytes, wf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WF_H */

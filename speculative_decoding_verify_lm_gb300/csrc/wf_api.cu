@@ -1,0 +1,200 @@
+// C ABI entry points: host-side validation, workspace layout and the
+// stream-ordered composition of one verify-and-route round.
+#include <atomic>
+
+#include "wf_internal.cuh"
+
+namespace wf {
+
+wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                               float* maxlogit, void* ws, cudaStream_t s);
+wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
+                            int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t cand_off,
+                            cudaStream_t s);
+wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
+                        int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
+                        int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
+                        void* ws, cudaStream_t s);
+wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
+                        const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
+                        void* ws, size_t part_off, cudaStream_t s);
+
+static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+static int g_sms[64];
+static signed char g_dev_ok[64];  // 0 unknown, 1 sm_103, -1 other
+
+int num_sms() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 64) return 148;
+    if (!g_sms[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = n > 0 ? n : 148;
+    }
+    return g_sms[dev];
+}
+
+// The kernels are built for sm_103a only (tcgen05, TMA).
+static wf_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && g_dev_ok[dev]) return g_dev_ok[dev] > 0 ? WF_OK : WF_ERR_UNSUPPORTED;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return WF_ERR_CUDA;
+    const bool ok = major == 10 && minor == 3;
+    if (dev < 64) g_dev_ok[dev] = ok ? 1 : -1;
+    return ok ? WF_OK : WF_ERR_UNSUPPORTED;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static wf_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return WF_ERR_WORKSPACE;
+    return ws_bytes >= need ? WF_OK : WF_ERR_WORKSPACE;
+}
+
+static bool bad_gemm_shape(int rows, int d, int n) {
+    return rows < 1 || n < 1 || d < 8 || d % 8 != 0 || d > 16384;
+}
+
+#define WF_TRY(x)                        \
+    do {                                 \
+        const wf_status _st = (x);       \
+        if (_st != WF_OK) return _st;    \
+    } while (0)
+
+}  // namespace wf
+
+using namespace wf;
+
+extern "C" {
+
+const char* wf_status_string(int status) {
+    switch (status) {
+        case WF_OK: return "WF_OK";
+        case WF_ERR_INVALID_ARG: return "WF_ERR_INVALID_ARG: invalid argument";
+        case WF_ERR_WORKSPACE: return "WF_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case WF_ERR_CUDA: return "WF_ERR_CUDA: CUDA runtime error";
+        case WF_ERR_UNSUPPORTED: return "WF_ERR_UNSUPPORTED: needs an sm_103 (GB300) device";
+        case WF_ERR_BAD_DATA: return "WF_ERR_BAD_DATA: malformed tree, offsets or id map";
+        case WF_ERR_TIMEOUT: return "WF_ERR_TIMEOUT: a bounded device wait gave up";
+        default: return "unknown wf_status";
+    }
+}
+
+int wf_version(void) { return 100; }
+
+size_t wf_workspace_bytes(int P, int B, int m, int Vd, int k) { return layout(P, B, m, Vd, k).total; }
+
+void wf_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
+
+wf_status wf_workspace_init(void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (!ws || ws_bytes < sizeof(Control)) return WF_ERR_WORKSPACE;
+    return cudaMemsetAsync(ws, 0, ws_bytes, stream) == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+wf_status wf_read_device_error(void* ws, int* code, int* info, int clear, wf_stream_t stream) {
+    if (!ws || !code) return WF_ERR_INVALID_ARG;
+    uint32_t h[2] = {0, 0};
+    if (cudaMemcpyAsync(h, ws, sizeof h, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return WF_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return WF_ERR_CUDA;
+    *code = (int)h[0];
+    if (info) *info = (int)h[1];
+    if (clear) {
+        if (cudaMemsetAsync(ws, 0, sizeof h, stream) != cudaSuccess) return WF_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return WF_ERR_CUDA;
+    }
+    return WF_OK;
+}
+
+wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                           float* maxlogit, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (!hidden || !W || !ids || bad_gemm_shape(P, d, V)) return WF_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, 0, 0, 0).total));
+    WF_TRY(check_device());
+    return launch_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, ws, stream);
+}
+
+wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t* pos_off, const int32_t* node_off,
+                          int B, int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos,
+                          int32_t* path, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (B < 0 || path_stride < 0 || (path_stride > 0 && !path)) return WF_ERR_INVALID_ARG;
+    if (!g || !draft || !pos_off || !node_off || !n_accept || !bonus || !last_pos) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
+    WF_TRY(check_device());
+    return launch_verify(g, draft, nullptr, nullptr, 0, pos_off, node_off, B, -1, path ? path_stride : 0,
+                         n_accept, bonus, last_pos, path, ws, stream);
+}
+
+wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* node_off,
+                         const int32_t* pos_off, int B, int path_stride, int32_t* n_accept, int32_t* bonus,
+                         int32_t* last_pos, int32_t* path, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (B < 0 || path_stride < 0 || (path_stride > 0 && !path)) return WF_ERR_INVALID_ARG;
+    if (!g || !tok || !parent || !pos_off || !node_off || !n_accept || !bonus || !last_pos)
+        return WF_ERR_INVALID_ARG;
+    WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
+    WF_TRY(check_device());
+    return launch_verify(g, tok, parent, nullptr, 1, pos_off, node_off, B, -1, path ? path_stride : 0, n_accept,
+                         bonus, last_pos, path, ws, stream);
+}
+
+wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, const float* W1,
+                        const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
+                        void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (B < 0 || d < 8 || d % 8 != 0 || m < 1 || m > ROUTER_MAX_WIDTH) return WF_ERR_INVALID_ARG;
+    if (!hidden || !rows || !W1 || !b1 || !w2 || (!delta_al && !route)) return WF_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(W1)) return WF_ERR_INVALID_ARG;
+    const Layout L = layout(0, B, m, 0, 0);
+    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_device());
+    return launch_router(hidden, rows, B, d, m, -1, W1, b1, w2, b2, tau, delta_al, route, ws, L.part, stream);
+}
+
+wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
+                        int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t ws_bytes,
+                        wf_stream_t stream) {
+    if (!x || !Wd || !d2t || bad_gemm_shape(B, d, Vd)) return WF_ERR_INVALID_ARG;
+    if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals)) return WF_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
+    const Layout L = layout(0, B, 0, Vd, k);
+    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_device());
+    return launch_draft_topk(x, Wd, d2t, B, d, Vd, k, draft_ids, tids, vals, ws, L.cand, stream);
+}
+
+wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (!a) return WF_ERR_INVALID_ARG;
+    if (!a->hidden || !a->W || bad_gemm_shape(a->P, a->d, a->V)) return WF_ERR_INVALID_ARG;
+    if (a->B < 1 || !a->pos_off || !a->node_off || !a->tok) return WF_ERR_INVALID_ARG;
+    if (!a->kind && !a->parent) return WF_ERR_INVALID_ARG;
+    if (a->path_stride < 0 || (a->path_stride > 0 && !a->path)) return WF_ERR_INVALID_ARG;
+    if (a->m < 1 || a->m > ROUTER_MAX_WIDTH || !a->W1 || !a->b1 || !a->w2) return WF_ERR_INVALID_ARG;
+    if (!a->ids || !a->n_accept || !a->bonus || !a->last_pos || !a->delta_al || !a->route) return WF_ERR_INVALID_ARG;
+    if (!aligned16(a->hidden) || !aligned16(a->W) || !aligned16(a->W1)) return WF_ERR_INVALID_ARG;
+    const bool draft = a->Wd != nullptr;
+    if (draft) {
+        if (!a->x || !a->d2t || !a->tids || bad_gemm_shape(a->B, a->d, a->Vd)) return WF_ERR_INVALID_ARG;
+        if (a->k < 1 || a->k > WF_MAX_TOPK || a->k > a->Vd) return WF_ERR_INVALID_ARG;
+        if (!aligned16(a->x) || !aligned16(a->Wd)) return WF_ERR_INVALID_ARG;
+    }
+    const Layout L = layout(a->P, a->B, a->m, draft ? a->Vd : 0, draft ? a->k : 0);
+    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_device());
+    WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+    WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                         a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream));
+    WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
+                         a->delta_al, a->route, ws, L.part, stream));
+    if (draft)
+        WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals, ws,
+                                 L.cand, stream));
+    return WF_OK;
+}
+
+}  // extern "C"

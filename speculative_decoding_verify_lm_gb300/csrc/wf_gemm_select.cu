@@ -1,0 +1,420 @@
+// LM head / draft head as a tcgen05 GEMM with the selection fused into the
+// epilogue: out[r] = argmax_v <act_r, W_v> (target LM head, greedy choice) or
+// the top-k of the same logits (EAGLE-3 draft head).  The logits live only in
+// TMEM; they are never written to memory.
+//
+// Per CTA (one per SM, persistent over tiles of BM activation rows x BN
+// weight rows):
+//   warp 0     TMA producer: stages [BK x BM] activation and [BK x BN] weight
+//              boxes (128-byte swizzle) into a STAGES-deep shared-memory ring
+//   warp 1     allocates TMEM (2 x BN fp32 columns = two accumulators) and one
+//              elected lane issues tcgen05.mma (M=128, N=256, K=16) per stage
+//   warps 2-5  epilogue: tcgen05.ld the finished accumulator (thread = one
+//              activation row, 32 columns per load), keep the running best
+//              (argmax) or a sorted top-k per row, and release the
+//              accumulator so the next tile's MMAs overlap this scan.
+// Argmax rows are combined across CTAs with a 64-bit atomicMax on a packed
+// (order-preserving logit, ~id) key; the last CTA to finish converts the keys
+// to ids and resets them to zero.  Top-k rows write one sorted candidate list
+// per tile; wf_topk_merge combines them.
+//
+// Every wait is bounded: a wait that runs out records WF_ERR_TIMEOUT, raises a
+// CTA-wide abort flag, drains its own in-flight copies / MMAs (again bounded)
+// and the CTA frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include "wf_internal.cuh"
+
+namespace wf {
+
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int GEMM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
+constexpr int GEMM_SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+constexpr int KT_TOPK = WF_MAX_TOPK;
+
+struct GemmParams {
+    int M_rows;        // activation rows (P or B)
+    int N_w;           // weight rows (V or Vd)
+    int num_m, num_n, num_k;
+    int k;             // top-k count (top-k mode)
+    int weight_evict_first;
+    uint64_t* keys;    // argmax: [M_rows] packed keys, zero on entry, zero on exit
+    int32_t* ids;      // argmax: [M_rows] out
+    float* maxlogit;   // argmax: [M_rows] out or null
+    uint64_t* cand;    // top-k: [tiles][BM][k]
+    Control* ctrl;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void gemm_fail(Control* ctrl, volatile int* abort_flag, uint32_t where) {
+    *abort_flag = 1;
+    record_error(ctrl, WF_ERR_TIMEOUT, where);
+}
+
+// Insert (v, id) into a descending list of KT entries (earlier entry wins ties).
+template <int KT>
+__device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], float v, int id) {
+#pragma unroll
+    for (int j = KT - 1; j > 0; --j) {
+        const bool shift = tv[j - 1] < v;
+        const bool land = !shift && tv[j] < v;
+        tv[j] = shift ? tv[j - 1] : (land ? v : tv[j]);
+        ti[j] = shift ? ti[j - 1] : (land ? id : ti[j]);
+    }
+    if (tv[0] < v) {
+        tv[0] = v;
+        ti[0] = id;
+    }
+}
+
+template <int KT>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int T = p.num_m * p.num_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = p.weight_evict_first ? policy_evict_first() : policy_evict_normal();
+            const uint64_t pol_a = policy_evict_last();
+            uint32_t it = 0;  // stages issued so far
+            bool ok = true;
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
+                const int m = t % p.num_m, n = t / p.num_m;
+                for (int kc = 0; kc < p.num_k; ++kc, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, p.timeout_ns, abort_flag)) {
+                        gemm_fail(p.ctrl, abort_flag, 0x100 + s);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                    tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kc * BK, m * BM, pol_a);
+                    tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * BN, pol_w);
+                }
+            }
+            if (!ok || *abort_flag) {
+                // let every copy this thread issued land before the CTA exits
+                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                    mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.timeout_ns, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+            uint32_t it = 0, tile_i = 0;
+            bool ok = true, issued = false;
+            for (int t = blockIdx.x; t < T && ok; t += gridDim.x, ++tile_i) {
+                const uint32_t acc = tile_i & 1;
+                const uint32_t acc_ph = (tile_i >> 1) & 1;
+                if (!mbar_wait(&tempty[acc], acc_ph ^ 1, p.timeout_ns, abort_flag)) {
+                    gemm_fail(p.ctrl, abort_flag, 0x200);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kc = 0; kc < p.num_k; ++kc, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
+                        gemm_fail(p.ctrl, abort_flag, 0x210 + s);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = umma_desc_sw128(smem_u32(sA + s * A_BYTES));
+                    const uint64_t bdesc = umma_desc_sw128(smem_u32(sB + s * B_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per step (encoded >> 4)
+                        umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
+                    umma_commit(&empty[s]);
+                    issued = true;
+                }
+                if (ok) umma_commit(&tfull[acc]);
+            }
+            if (!ok && issued) {
+                umma_commit(drain);  // arrives when every MMA issued above has finished
+                mbar_wait(drain, 0, p.timeout_ns, nullptr);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int rit = q * 32 + lane;
+        uint32_t tile_i = 0;
+        for (int t = blockIdx.x; t < T; t += gridDim.x, ++tile_i) {
+            const int m = t % p.num_m, n = t / p.num_m;
+            const uint32_t acc = tile_i & 1;
+            const uint32_t acc_ph = (tile_i >> 1) & 1;
+            const bool quad_live = m * BM + q * 32 < p.M_rows;
+            const int row = m * BM + rit;
+            if (!mbar_wait(&tfull[acc], acc_ph, p.timeout_ns, abort_flag)) {
+                gemm_fail(p.ctrl, abort_flag, 0x300);
+                break;
+            }
+            tc_fence_after();
+            float tv[KT];
+            int ti[KT];
+#pragma unroll
+            for (int j = 0; j < KT; ++j) {
+                tv[j] = -INFINITY;
+                ti[j] = 0;
+            }
+            if (quad_live) {
+                const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tbase + c0, r);
+                    tmem_ld_wait();
+                    const int col0 = n * BN + c0;
+                    const int lim = p.N_w - col0;  // columns >= lim are past the weight matrix
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float v = __uint_as_float(r[j]);
+                        if (j < lim) {
+                            if constexpr (KT == 1) {
+                                if (v > tv[0]) {
+                                    tv[0] = v;
+                                    ti[0] = col0 + j;
+                                }
+                            } else {
+                                if (v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            if (quad_live && row < p.M_rows) {
+                if constexpr (KT == 1) {
+                    atomicMax(reinterpret_cast<unsigned long long*>(p.keys + row),
+                              (unsigned long long)pack_key(tv[0], (uint32_t)ti[0]));
+                } else {
+                    uint64_t* dst = p.cand + ((size_t)t * BM + rit) * p.k;
+                    for (int j = 0; j < KT; ++j)
+                        if (j < p.k) dst[j] = tv[j] == -INFINITY ? 0ull : pack_key(tv[j], (uint32_t)ti[j]);
+                }
+            }
+        }
+        if (KT == 1 && !*abort_flag) {
+            // last CTA to finish turns the keys into ids and zeroes them again
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (threadIdx.x == 64) {
+                const uint32_t prev = atomicAdd(&p.ctrl->gemm_done, 1u);
+                *last_flag = (prev == gridDim.x - 1);
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (*last_flag) {
+                __threadfence();
+                for (int r = threadIdx.x - 64; r < p.M_rows; r += 128) {
+                    const uint64_t key = __ldcg(reinterpret_cast<const unsigned long long*>(p.keys + r));
+                    p.ids[r] = key ? (int32_t)key_id(key) : -1;
+                    if (p.maxlogit) p.maxlogit[r] = key ? key_val(key) : __int_as_float(0x7fc00000);
+                    p.keys[r] = 0;
+                }
+                if (threadIdx.x == 64) p.ctrl->gemm_done = 0;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// --------------------------------------------------------------------- top-k merge
+// One warp per activation row: every lane keeps the 16 best of its share of
+// the per-tile candidate lists, then k rounds of a warp-wide max pick the
+// winners in order.  Keys are unique per row (each weight row lives in one tile).
+__global__ void __launch_bounds__(128) topk_merge_kernel(const uint64_t* __restrict__ cand, int B, int num_m,
+                                                         int num_n, int k, const int32_t* __restrict__ d2t, int Vd,
+                                                         int32_t* draft_ids, int32_t* tids, float* vals,
+                                                         Control* ctrl) {
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= B) return;
+    const int m = row / BM, rit = row % BM;
+    uint64_t loc[KT_TOPK];
+#pragma unroll
+    for (int j = 0; j < KT_TOPK; ++j) loc[j] = 0;
+    const int total = num_n * k;
+    for (int idx = lane; idx < total; idx += 32) {
+        const int n = idx / k, j = idx - n * k;
+        uint64_t* src = const_cast<uint64_t*>(cand) + (((size_t)n * num_m + m) * BM + rit) * k + j;
+        const uint64_t key = *src;
+        *src = 0;  // leave the workspace zeroed
+        if (key > loc[KT_TOPK - 1]) {
+#pragma unroll
+            for (int s = KT_TOPK - 1; s > 0; --s) {
+                const bool shift = loc[s - 1] < key;
+                const bool land = !shift && loc[s] < key;
+                loc[s] = shift ? loc[s - 1] : (land ? key : loc[s]);
+            }
+            if (loc[0] < key) loc[0] = key;
+        }
+    }
+    for (int j = 0; j < k; ++j) {
+        uint64_t best = loc[0];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
+        }
+        if (loc[0] == best && best != 0) {  // the (unique) owner pops its head
+#pragma unroll
+            for (int s = 0; s < KT_TOPK - 1; ++s) loc[s] = loc[s + 1];
+            loc[KT_TOPK - 1] = 0;
+        }
+        if (lane == 0) {
+            const size_t o = (size_t)row * k + j;
+            int32_t id = -1, tid = -1;
+            float v = __int_as_float(0x7fc00000);
+            if (best != 0) {
+                id = (int32_t)key_id(best);
+                v = key_val(best);
+                tid = (id >= 0 && id < Vd) ? d2t[id] : -1;
+                if (tid < 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)row);
+            }
+            if (draft_ids) draft_ids[o] = id;
+            if (tids) tids[o] = tid;
+            if (vals) vals[o] = v;
+        }
+    }
+}
+
+// --------------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// [rows, cols] bf16 row-major; boxes of 64 columns (128 B, swizzled) x box_rows rows.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms();
+
+template <int KT>
+static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, int k,
+                               uint64_t* keys, int32_t* ids, float* maxlogit, uint64_t* cand, Control* ctrl,
+                               cudaStream_t s) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_select_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) !=
+            cudaSuccess)
+            return WF_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, BM)) return WF_ERR_CUDA;
+    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, BN)) return WF_ERR_CUDA;
+    GemmParams p;
+    p.M_rows = M_rows;
+    p.N_w = N_w;
+    p.num_m = cdiv(M_rows, BM);
+    p.num_n = cdiv(N_w, BN);
+    p.num_k = cdiv(d, BK);
+    p.k = k;
+    p.weight_evict_first = p.num_m == 1;
+    p.keys = keys;
+    p.ids = ids;
+    p.maxlogit = maxlogit;
+    p.cand = cand;
+    p.ctrl = ctrl;
+    p.timeout_ns = wait_timeout_ns();
+    const int tiles = p.num_m * p.num_n;
+    const int grid = tiles < num_sms() ? tiles : num_sms();
+    gemm_select_kernel<KT><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, p);
+    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                               float* maxlogit, void* ws, cudaStream_t s) {
+    Control* ctrl = reinterpret_cast<Control*>(ws);
+    uint64_t* keys = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + sizeof(Control));
+    return launch_select<1>(hidden, P, W, V, d, 1, keys, ids, maxlogit, nullptr, ctrl, s);
+}
+
+wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
+                            int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t cand_off,
+                            cudaStream_t s) {
+    Control* ctrl = reinterpret_cast<Control*>(ws);
+    uint64_t* cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    wf_status st = launch_select<KT_TOPK>(x, B, Wd, Vd, d, k, nullptr, nullptr, nullptr, cand, ctrl, s);
+    if (st != WF_OK) return st;
+    topk_merge_kernel<<<cdiv(B, 4), 128, 0, s>>>(cand, B, cdiv(B, BM), cdiv(Vd, BN), k, d2t, Vd, draft_ids, tids,
+                                                 vals, ctrl);
+    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+}  // namespace wf

@@ -1,0 +1,150 @@
+// Neural router f_theta and the hardware-aware routing decision (WhiFlash
+// paper Sec. 3.3.2 and App. A "Neural Router Architecture"):
+//   delta_al[b] = b2 + sum_j w2[j] * GELU(b1[j] + <W1[j, :], h_b>)
+//   route[b]    = delta_al[b] > tau   (1 = autoregressive EAGLE-3 drafter)
+// with h_b the bf16 hidden row rows[b] widened to fp32, exact-erf GELU, and
+// dropout as the identity.
+//
+// One warp per hidden unit j (8 units per CTA).  The CTA stages up to RB
+// hidden rows in shared memory, each warp streams its W1 row with 16-byte
+// loads and keeps RB dot products; units are folded per CTA into
+// w2[j] * GELU(z_j) partials, and the last CTA to finish sums the partials of
+// every sequence in a fixed order (so the result does not depend on CTA
+// scheduling) and writes delta_al and route.
+#include "wf_internal.cuh"
+
+namespace wf {
+
+constexpr int ROUTER_THREADS = ROUTER_UNITS_PER_CTA * 32;
+constexpr int ROUTER_RB = 8;                       // hidden rows staged per pass
+constexpr int ROUTER_SMEM_MAX = 160 * 1024;
+
+__device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
+__global__ void __launch_bounds__(ROUTER_THREADS)
+    router_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
+                  int P, const float* __restrict__ W1, const float* __restrict__ b1, const float* __restrict__ w2,
+                  float b2, float tau, float* delta_al, int32_t* route, float* part, int rb_max, Control* ctrl) {
+    // part: [B][gridDim.x] partial sums, zero on entry and on exit
+    extern __shared__ uint8_t smem_raw[];
+    uint16_t* sh = reinterpret_cast<uint16_t*>(smem_raw);    // [rb_max][d] bf16
+    __shared__ float red[ROUTER_UNITS_PER_CTA][ROUTER_RB];
+    __shared__ int s_row[ROUTER_RB];
+    __shared__ int s_last;
+
+    const int w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int j = blockIdx.x * ROUTER_UNITS_PER_CTA + w;
+    const int nblk = gridDim.x;
+    const bool unit_live = j < m;
+    const float bias1 = unit_live ? b1[j] : 0.f;
+    const float wout = unit_live ? w2[j] : 0.f;
+    const float4* wrow = reinterpret_cast<const float4*>(W1 + (size_t)(unit_live ? j : 0) * d);
+    const int d4 = d >> 2;
+
+    for (int b0 = 0; b0 < B; b0 += rb_max) {
+        const int nb = min(rb_max, B - b0);
+        __syncthreads();
+        if (threadIdx.x < nb) {
+            int r = rows[b0 + threadIdx.x];
+            if (r < 0 || (P >= 0 && r >= P)) r = -1;
+            s_row[threadIdx.x] = r;
+        }
+        __syncthreads();
+        // stage the rows (16-byte chunks); invalid rows are zero-filled
+        const int chunks = d >> 3;
+        for (int idx = threadIdx.x; idx < nb * chunks; idx += blockDim.x) {
+            const int rb = idx / chunks, c = idx - rb * chunks;
+            const int r = s_row[rb];
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r >= 0) v = reinterpret_cast<const uint4*>(hidden + (size_t)r * d)[c];
+            reinterpret_cast<uint4*>(sh + (size_t)rb * d)[c] = v;
+        }
+        __syncthreads();
+        float acc[ROUTER_RB];
+#pragma unroll
+        for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = 0.f;
+        if (unit_live) {
+            for (int c = lane; c < d4; c += 32) {
+                const float4 wv = __ldg(wrow + c);
+#pragma unroll
+                for (int rb = 0; rb < ROUTER_RB; ++rb) {
+                    if (rb < nb) {
+                        const uint2 hv = reinterpret_cast<const uint2*>(sh + (size_t)rb * d)[c];
+                        acc[rb] = fmaf(wv.x, __uint_as_float(hv.x << 16), acc[rb]);
+                        acc[rb] = fmaf(wv.y, __uint_as_float(hv.x & 0xFFFF0000u), acc[rb]);
+                        acc[rb] = fmaf(wv.z, __uint_as_float(hv.y << 16), acc[rb]);
+                        acc[rb] = fmaf(wv.w, __uint_as_float(hv.y & 0xFFFF0000u), acc[rb]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int rb = 0; rb < ROUTER_RB; ++rb) {
+            float v = acc[rb];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0 && rb < nb) red[w][rb] = unit_live ? wout * gelu_erf(v + bias1) : 0.f;
+        }
+        __syncthreads();
+        if (threadIdx.x < nb) {
+            float s = 0.f;
+#pragma unroll
+            for (int u = 0; u < ROUTER_UNITS_PER_CTA; ++u) s += red[u][threadIdx.x];
+            part[(size_t)(b0 + threadIdx.x) * nblk + blockIdx.x] = s;
+        }
+    }
+
+    // the last CTA to finish reduces the partials in a fixed order
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&ctrl->router_done, 1u) == (unsigned)nblk - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        const int r = rows[b];
+        if (r < 0 || (P >= 0 && r >= P)) {
+            if (delta_al) delta_al[b] = __int_as_float(0x7fc00000);
+            if (route) route[b] = -1;
+            record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+            for (int c = 0; c < nblk; ++c) part[(size_t)b * nblk + c] = 0.f;
+            continue;
+        }
+        float s = b2;
+        float* pb = part + (size_t)b * nblk;
+        for (int c = 0; c < nblk; ++c) {
+            s += __ldcg(pb + c);
+            pb[c] = 0.f;  // leave the workspace zeroed
+        }
+        if (delta_al) delta_al[b] = s;
+        if (route) route[b] = s > tau ? 1 : 0;
+    }
+    if (threadIdx.x == 0) ctrl->router_done = 0;
+}
+
+wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
+                        const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
+                        void* ws, size_t part_off, cudaStream_t s) {
+    if (B == 0) return WF_OK;
+    int rb = (int)((size_t)ROUTER_SMEM_MAX / ((size_t)d * 2));
+    rb = rb < 1 ? 1 : (rb > ROUTER_RB ? ROUTER_RB : rb);
+    const size_t smem = (size_t)rb * d * 2;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX) !=
+            cudaSuccess)
+            return WF_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    Control* ctrl = reinterpret_cast<Control*>(ws);
+    float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
+    router_kernel<<<cdiv(m, ROUTER_UNITS_PER_CTA), ROUTER_THREADS, smem, s>>>(hidden, rows, B, d, m, P, W1, b1, w2,
+                                                                             b2, tau, delta_al, route, part, rb,
+                                                                             ctrl);
+    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+}  // namespace wf

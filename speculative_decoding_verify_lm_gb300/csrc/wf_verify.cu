@@ -1,0 +1,181 @@
+// Greedy acceptance of drafted DFlash chains and EAGLE-3 trees, one warp per
+// sequence (WhiFlash paper Sec. 3.2: the drafted block or tree is verified by
+// the target in parallel and decoding resumes from the last accepted token).
+//
+// Chain: the accepted prefix ends at the first drafted token that differs
+// from the target's choice at the row before it - a warp ballot over 32
+// drafts at a time.
+// Tree: node i is accepted iff its token equals the target's choice at its
+// parent's row and every ancestor is accepted.  The warp computes the match
+// flag of every node in parallel, then pointer-jumps (each round doubles the
+// span of ancestors folded in) to get, per node, the AND over its whole root
+// path and its depth; the deepest accepted node (lowest index on a tie) wins
+// a warp max over packed (depth, ~index) keys.
+#include "wf_internal.cuh"
+
+namespace wf {
+
+constexpr int VERIFY_WARPS = 4;
+constexpr int NODES_PER_LANE = WF_MAX_SEQ_NODES / 32;
+
+__global__ void __launch_bounds__(VERIFY_WARPS * 32)
+    verify_kernel(const int32_t* __restrict__ g, const int32_t* __restrict__ tok, const int32_t* __restrict__ parent,
+                  const int32_t* __restrict__ kind, int default_kind, const int32_t* __restrict__ pos_off,
+                  const int32_t* __restrict__ node_off, int B, int P, int path_stride, int32_t* n_accept,
+                  int32_t* bonus, int32_t* last_pos, int32_t* path, Control* ctrl) {
+    __shared__ int16_t s_par[VERIFY_WARPS][WF_MAX_SEQ_NODES];
+    __shared__ int16_t s_anc[VERIFY_WARPS][WF_MAX_SEQ_NODES];
+    __shared__ int16_t s_dist[VERIFY_WARPS][WF_MAX_SEQ_NODES];
+    __shared__ uint8_t s_ok[VERIFY_WARPS][WF_MAX_SEQ_NODES];
+
+    const int w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * VERIFY_WARPS + w;
+    if (b >= B) return;
+    const unsigned FULL = 0xffffffffu;
+
+    const int r0 = pos_off[b], r1 = pos_off[b + 1];
+    const int n0 = node_off[b], n1 = node_off[b + 1];
+    const int N = n1 - n0;
+    const bool shape_ok = r0 >= 0 && r1 > r0 && (P < 0 || r1 <= P) && n0 >= 0 && N >= 0 &&
+                          N == r1 - r0 - 1 && N <= WF_MAX_SEQ_NODES;
+    auto fail = [&]() {
+        if (lane == 0) {
+            record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+            n_accept[b] = -1;
+            bonus[b] = -1;
+            last_pos[b] = -1;
+        }
+        if (path)
+            for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = -1;
+    };
+    if (!shape_ok) {
+        fail();
+        return;
+    }
+    const int kd = kind ? kind[b] : default_kind;
+    if (kd != 0 && !parent) {
+        fail();
+        return;
+    }
+
+    if (kd == 0) {
+        // ---------------------------------------------------------------- chain
+        int n = N;
+        for (int base = 0; base < N; base += 32) {
+            const int j = base + lane;
+            const bool mism = j < N && tok[n0 + j] != g[r0 + j];
+            const unsigned mask = __ballot_sync(FULL, mism);
+            if (mask) {
+                n = base + __ffs(mask) - 1;
+                break;
+            }
+        }
+        if (lane == 0) {
+            n_accept[b] = n;
+            last_pos[b] = r0 + n;
+            bonus[b] = g[r0 + n];
+        }
+        if (path)
+            for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = j < n ? j : -1;
+        return;
+    }
+
+    // -------------------------------------------------------------------- tree
+    int16_t* par = s_par[w];
+    int16_t* anc = s_anc[w];
+    int16_t* dist = s_dist[w];
+    uint8_t* okf = s_ok[w];
+    bool bad = false;
+    for (int i = lane; i < N; i += 32) {
+        const int pi = parent[n0 + i];
+        const bool pbad = pi < -1 || pi >= i;
+        bad |= pbad;
+        const int prow = pi < 0 ? r0 : r0 + 1 + pi;
+        par[i] = (int16_t)(pbad ? -1 : pi);
+        anc[i] = par[i];
+        dist[i] = 1;
+        okf[i] = (uint8_t)(!pbad && tok[n0 + i] == g[prow]);
+    }
+    if (__any_sync(FULL, bad)) {
+        fail();
+        return;
+    }
+    __syncwarp();
+    // pointer jumping: invariant - okf[i] = AND of the match flags of the dist[i]
+    // nodes from i up to (excluding) anc[i]
+    for (int span = 1; span < N; span <<= 1) {
+        int16_t na[NODES_PER_LANE], nd[NODES_PER_LANE];
+        uint8_t no[NODES_PER_LANE];
+        bool live = false;
+#pragma unroll
+        for (int s = 0; s < NODES_PER_LANE; ++s) {
+            const int i = lane + 32 * s;
+            if (i < N) {
+                const int a = anc[i];
+                if (a >= 0) {
+                    na[s] = anc[a];
+                    nd[s] = (int16_t)(dist[i] + dist[a]);
+                    no[s] = okf[i] & okf[a];
+                    live = true;
+                } else {
+                    na[s] = -1;
+                    nd[s] = dist[i];
+                    no[s] = okf[i];
+                }
+            }
+        }
+        if (!__any_sync(FULL, live)) break;
+        __syncwarp();
+#pragma unroll
+        for (int s = 0; s < NODES_PER_LANE; ++s) {
+            const int i = lane + 32 * s;
+            if (i < N) {
+                anc[i] = na[s];
+                dist[i] = nd[s];
+                okf[i] = no[s];
+            }
+        }
+        __syncwarp();
+    }
+    // deepest accepted node, lowest index on equal depth
+    uint32_t best = 0;
+    for (int i = lane; i < N; i += 32)
+        if (okf[i]) {
+            const uint32_t key = ((uint32_t)dist[i] << 16) | (uint32_t)(0xFFFF - i);
+            best = key > best ? key : best;
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const uint32_t o = __shfl_xor_sync(FULL, best, off);
+        best = o > best ? o : best;
+    }
+    const int n = (int)(best >> 16);
+    const int node = best ? 0xFFFF - (int)(best & 0xFFFF) : -1;
+    const int last = node < 0 ? r0 : r0 + 1 + node;
+    if (path) {
+        for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = -1;
+        __syncwarp();
+        if (lane == 0)
+            for (int i = node, dep = n; i >= 0; i = par[i], --dep)
+                if (dep - 1 < path_stride) path[(size_t)b * path_stride + dep - 1] = i;
+    }
+    if (lane == 0) {
+        n_accept[b] = n;
+        last_pos[b] = last;
+        bonus[b] = g[last];
+    }
+}
+
+wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
+                        int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
+                        int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
+                        void* ws, cudaStream_t s) {
+    if (B == 0) return WF_OK;
+    verify_kernel<<<cdiv(B, VERIFY_WARPS), VERIFY_WARPS * 32, 0, s>>>(
+        g, tok, parent, kind, default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path,
+        reinterpret_cast<Control*>(ws));
+    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+}  // namespace wf

@@ -1,0 +1,295 @@
+"""Python binding of ``libwf.so`` (the C ABI declared in include/wf.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+dtype / device / contiguity, and passes raw device pointers and the current
+(or given) CUDA stream to the library; all arithmetic runs in the library's
+kernels.  The functions carry the C names.  If the shared library is missing
+it is built with nvcc; if that fails, loading raises - there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+WF_MAX_SEQ_NODES = 256
+WF_MAX_TOPK = 16
+STATUS = {0: "WF_OK", 1: "WF_ERR_INVALID_ARG", 2: "WF_ERR_WORKSPACE", 3: "WF_ERR_CUDA", 4: "WF_ERR_UNSUPPORTED",
+          5: "WF_ERR_BAD_DATA", 6: "WF_ERR_TIMEOUT"}
+
+
+class WfError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib().wf_status_string(status).decode()} (status {status})")
+
+
+_c_void_p = ctypes.c_void_p
+_i32 = ctypes.c_int
+_f32 = ctypes.c_float
+_u64 = ctypes.c_uint64
+_sz = ctypes.c_size_t
+
+
+class RoundArgs(ctypes.Structure):
+    """Mirror of ``wf_round_args``."""
+    _fields_ = [
+        ("hidden", _c_void_p), ("W", _c_void_p), ("P", _i32), ("d", _i32), ("V", _i32),
+        ("B", _i32), ("pos_off", _c_void_p), ("node_off", _c_void_p), ("kind", _c_void_p), ("tok", _c_void_p),
+        ("parent", _c_void_p), ("path_stride", _i32),
+        ("m", _i32), ("W1", _c_void_p), ("b1", _c_void_p), ("w2", _c_void_p), ("b2", _f32), ("tau", _f32),
+        ("x", _c_void_p), ("Wd", _c_void_p), ("d2t", _c_void_p), ("Vd", _i32), ("k", _i32),
+        ("ids", _c_void_p), ("maxlogit", _c_void_p), ("n_accept", _c_void_p), ("bonus", _c_void_p),
+        ("last_pos", _c_void_p), ("path", _c_void_p), ("delta_al", _c_void_p), ("route", _c_void_p),
+        ("draft_ids", _c_void_p), ("tids", _c_void_p), ("vals", _c_void_p),
+    ]
+
+
+_SIGS = {
+    "wf_status_string": (ctypes.c_char_p, [_i32]),
+    "wf_version": (_i32, []),
+    "wf_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "wf_workspace_init": (_i32, [_c_void_p, _sz, _c_void_p]),
+    "wf_read_device_error": (_i32, [_c_void_p, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32, _c_void_p]),
+    "wf_set_wait_timeout_ns": (None, [_u64]),
+    "wf_lmhead_argmax": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz,
+                                _c_void_p]),
+    "wf_verify_chain": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p,
+                               _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "wf_verify_tree": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
+                              _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "wf_router_mlp": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _f32, _f32,
+                             _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "wf_draft_topk": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p,
+                             _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "wf_round": (_i32, [ctypes.POINTER(RoundArgs), _c_void_p, _sz, _c_void_p]),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load (building first if missing or stale) the native library."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def exported_symbols() -> list:
+    return list(_SIGS)
+
+
+# ------------------------------------------------------------------ marshalling
+def _check(t: Optional[torch.Tensor], name: str, dtypes, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    return t.data_ptr()
+
+
+_BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
+_I32 = (torch.int32,)
+_F32 = (torch.float32,)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _raise(st: int, where: str):
+    if st != 0:
+        raise WfError(st, where)
+
+
+class Workspace:
+    """Caller-owned device workspace sized by wf_workspace_bytes and zeroed once."""
+
+    def __init__(self, P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0, device=None, stream=None):
+        self.nbytes = int(lib().wf_workspace_bytes(P, B, m, Vd, k))
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        _raise(lib().wf_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream)), "wf_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def device_error(self, clear: bool = True, stream=None):
+        code, info = _i32(0), _i32(0)
+        _raise(lib().wf_read_device_error(self.ptr, ctypes.byref(code), ctypes.byref(info), int(clear),
+                                          _stream(stream)), "wf_read_device_error")
+        return code.value, info.value
+
+
+def wf_workspace_bytes(P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0) -> int:
+    return int(lib().wf_workspace_bytes(P, B, m, Vd, k))
+
+
+def wf_set_wait_timeout_ns(ns: int) -> None:
+    lib().wf_set_wait_timeout_ns(int(ns))
+
+
+def wf_lmhead_argmax(hidden, W, ws: Workspace, ids=None, maxlogit=None, stream=None):
+    P, d = hidden.shape
+    V = W.shape[0]
+    if ids is None:
+        ids = torch.empty(P, dtype=torch.int32, device=hidden.device)
+    st = lib().wf_lmhead_argmax(_check(hidden, "hidden", _BF16), _check(W, "W", _BF16), P, d, V,
+                                _check(ids, "ids", _I32), _check(maxlogit, "maxlogit", _F32, True), ws.ptr, ws.nbytes,
+                                _stream(stream))
+    _raise(st, "wf_lmhead_argmax")
+    return ids
+
+
+def _verify_outputs(B, path_stride, device, n_accept, bonus, last_pos, path):
+    mk = lambda: torch.empty(B, dtype=torch.int32, device=device)  # noqa: E731
+    n_accept = mk() if n_accept is None else n_accept
+    bonus = mk() if bonus is None else bonus
+    last_pos = mk() if last_pos is None else last_pos
+    if path is None and path_stride > 0:
+        path = torch.empty((B, path_stride), dtype=torch.int32, device=device)
+    return n_accept, bonus, last_pos, path
+
+
+def wf_verify_chain(g, draft, pos_off, node_off, ws: Workspace, path_stride: int = 0, n_accept=None, bonus=None,
+                    last_pos=None, path=None, stream=None):
+    B = pos_off.numel() - 1
+    n_accept, bonus, last_pos, path = _verify_outputs(B, path_stride, g.device, n_accept, bonus, last_pos, path)
+    st = lib().wf_verify_chain(_check(g, "g", _I32), _check(draft, "draft", _I32), _check(pos_off, "pos_off", _I32),
+                               _check(node_off, "node_off", _I32), B, path_stride, _check(n_accept, "n_accept", _I32),
+                               _check(bonus, "bonus", _I32), _check(last_pos, "last_pos", _I32),
+                               _check(path, "path", _I32, True), ws.ptr, ws.nbytes, _stream(stream))
+    _raise(st, "wf_verify_chain")
+    return n_accept, bonus, last_pos, path
+
+
+def wf_verify_tree(g, tok, parent, node_off, pos_off, ws: Workspace, path_stride: int = 0, n_accept=None,
+                   bonus=None, last_pos=None, path=None, stream=None):
+    B = pos_off.numel() - 1
+    n_accept, bonus, last_pos, path = _verify_outputs(B, path_stride, g.device, n_accept, bonus, last_pos, path)
+    st = lib().wf_verify_tree(_check(g, "g", _I32), _check(tok, "tok", _I32), _check(parent, "parent", _I32),
+                              _check(node_off, "node_off", _I32), _check(pos_off, "pos_off", _I32), B, path_stride,
+                              _check(n_accept, "n_accept", _I32), _check(bonus, "bonus", _I32),
+                              _check(last_pos, "last_pos", _I32), _check(path, "path", _I32, True), ws.ptr,
+                              ws.nbytes, _stream(stream))
+    _raise(st, "wf_verify_tree")
+    return n_accept, bonus, last_pos, path
+
+
+def wf_router_mlp(hidden, rows, W1, b1, w2, b2: float, tau: float, ws: Workspace, delta_al=None, route=None,
+                  stream=None):
+    B = rows.numel()
+    m, d = W1.shape
+    if delta_al is None:
+        delta_al = torch.empty(B, dtype=torch.float32, device=hidden.device)
+    if route is None:
+        route = torch.empty(B, dtype=torch.int32, device=hidden.device)
+    st = lib().wf_router_mlp(_check(hidden, "hidden", _BF16), _check(rows, "rows", _I32), B, d, m,
+                             _check(W1, "W1", _F32), _check(b1, "b1", _F32), _check(w2, "w2", _F32), float(b2),
+                             float(tau), _check(delta_al, "delta_al", _F32), _check(route, "route", _I32), ws.ptr,
+                             ws.nbytes, _stream(stream))
+    _raise(st, "wf_router_mlp")
+    return delta_al, route
+
+
+def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, vals=None, stream=None):
+    B, d = x.shape
+    Vd = Wd.shape[0]
+    dev = x.device
+    draft_ids = torch.empty((B, k), dtype=torch.int32, device=dev) if draft_ids is None else draft_ids
+    tids = torch.empty((B, k), dtype=torch.int32, device=dev) if tids is None else tids
+    vals = torch.empty((B, k), dtype=torch.float32, device=dev) if vals is None else vals
+    st = lib().wf_draft_topk(_check(x, "x", _BF16), _check(Wd, "Wd", _BF16), _check(d2t, "d2t", _I32), B, d, Vd, k,
+                             _check(draft_ids, "draft_ids", _I32), _check(tids, "tids", _I32),
+                             _check(vals, "vals", _F32), ws.ptr, ws.nbytes, _stream(stream))
+    _raise(st, "wf_draft_topk")
+    return draft_ids, tids, vals
+
+
+class Round:
+    """Inputs and output buffers of wf_round, held as device tensors so the
+    call can be repeated (and captured in a CUDA graph) without re-marshalling."""
+
+    def __init__(self, hidden, W, pos_off, node_off, tok, W1, b1, w2, b2: float, tau: float, kind=None, parent=None,
+                 path_stride: int = 0, x=None, Wd=None, d2t=None, k: int = 0, with_maxlogit: bool = False):
+        dev = hidden.device
+        P, d = hidden.shape
+        B = pos_off.numel() - 1
+        m = W1.shape[0]
+        self.inputs = dict(hidden=hidden, W=W, pos_off=pos_off, node_off=node_off, tok=tok, W1=W1, b1=b1, w2=w2,
+                           kind=kind, parent=parent, x=x, Wd=Wd, d2t=d2t)
+        i32 = lambda *s: torch.empty(*s, dtype=torch.int32, device=dev)  # noqa: E731
+        self.out = dict(ids=i32(P), n_accept=i32(B), bonus=i32(B), last_pos=i32(B),
+                        path=i32((B, path_stride)) if path_stride else None,
+                        delta_al=torch.empty(B, dtype=torch.float32, device=dev), route=i32(B),
+                        maxlogit=torch.empty(P, dtype=torch.float32, device=dev) if with_maxlogit else None,
+                        draft_ids=i32((B, k)) if Wd is not None else None,
+                        tids=i32((B, k)) if Wd is not None else None,
+                        vals=torch.empty((B, k), dtype=torch.float32, device=dev) if Wd is not None else None)
+        a = RoundArgs()
+        a.hidden = _check(hidden, "hidden", _BF16)
+        a.W = _check(W, "W", _BF16)
+        a.P, a.d, a.V = P, d, W.shape[0]
+        a.B = B
+        a.pos_off = _check(pos_off, "pos_off", _I32)
+        a.node_off = _check(node_off, "node_off", _I32)
+        a.kind = _check(kind, "kind", _I32, True)
+        a.tok = _check(tok, "tok", _I32)
+        a.parent = _check(parent, "parent", _I32, True)
+        a.path_stride = path_stride
+        a.m = m
+        a.W1 = _check(W1, "W1", _F32)
+        a.b1 = _check(b1, "b1", _F32)
+        a.w2 = _check(w2, "w2", _F32)
+        a.b2, a.tau = float(b2), float(tau)
+        a.x = _check(x, "x", _BF16, True)
+        a.Wd = _check(Wd, "Wd", _BF16, True)
+        a.d2t = _check(d2t, "d2t", _I32, True)
+        a.Vd = Wd.shape[0] if Wd is not None else 0
+        a.k = k if Wd is not None else 0
+        for name in ("ids", "maxlogit", "n_accept", "bonus", "last_pos", "path", "delta_al", "route", "draft_ids",
+                     "tids", "vals"):
+            t = self.out[name]
+            setattr(a, name, t.data_ptr() if t is not None else None)
+        self.args = a
+        self.ws = Workspace(P, B, m, a.Vd, a.k, device=dev)
+
+    def __call__(self, stream=None):
+        _raise(lib().wf_round(ctypes.byref(self.args), self.ws.ptr, self.ws.nbytes, _stream(stream)), "wf_round")
+        return self.out
+
+
+def wf_round(hidden, W, pos_off, node_off, tok, W1, b1, w2, b2, tau, kind=None, parent=None, path_stride=0, x=None,
+             Wd=None, d2t=None, k=0, stream=None):
+    """One-shot round (allocates outputs and a workspace)."""
+    r = Round(hidden, W, pos_off, node_off, tok, W1, b1, w2, b2, tau, kind=kind, parent=parent,
+              path_stride=path_stride, x=x, Wd=Wd, d2t=d2t, k=k)
+    return r(stream)

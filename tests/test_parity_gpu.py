@@ -1,0 +1,266 @@
+"""GPU library vs CPU oracle, through the C ABI.
+
+Integer results (target argmax ids, acceptance lengths, bonus tokens, last
+rows, accepted paths, routes, draft top-k ids) must match bit-exactly; the
+router output within 1e-3 absolute; logits within the worst-case fp32
+accumulation bound 2*d*u*sum|h*w| (u = 2^-24).  Inputs obey the rejection
+rules (top-2 logit gap, router margin and adjacent draft top-k gaps all
+>= 1e-2), so the fp64 oracle and the fp32 kernels take the same decisions.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import DEV, check_round_properties, dev, host, logit_error_bound, round_on_gpu
+from speculative_decoding_verify_lm_gb300 import synth, wf
+
+pytestmark = pytest.mark.gpu
+
+ORACLE = None
+
+
+def o():
+    global ORACLE
+    if ORACLE is None:
+        ORACLE = oracle.default()
+    return ORACLE
+
+
+def _gapped_hidden(seed, P, d, W, reject=True):
+    h = synth.normal_bf16(seed, 1, P, d, 1.0)
+    if not reject:
+        return h
+    for a in range(1, 64):
+        _, _, gap = o().lmhead_argmax(h, W)
+        bad = np.nonzero(gap < synth.GAP_MIN)[0]
+        if not len(bad):
+            return h
+        for r in bad:
+            h[r] = synth.hidden_row(seed, int(r), a, d)
+    raise RuntimeError("gap rule not met")
+
+
+# ------------------------------------------------------------------ LM head
+@pytest.mark.parametrize("P,d,V", [(1, 64, 300), (17, 256, 8192), (61, 128, 1000), (200, 64, 513), (130, 72, 777),
+                                   (5, 8, 40), (256, 192, 2048), (129, 256, 257)])
+def test_lmhead_argmax(P, d, V):
+    W = synth.normal_bf16(7 + P, 0, V, d, 0.02 if d >= 256 else 0.1)
+    h = _gapped_hidden(11 + V, P, d, W)
+    ids_ref, mx_ref, gap = o().lmhead_argmax(h, W)
+    ws = wf.Workspace(P)
+    ids = torch.empty(P, dtype=torch.int32, device=DEV)
+    mx = torch.empty(P, dtype=torch.float32, device=DEV)
+    for _ in range(2):   # the workspace is reused: the second call must see it clean
+        wf.wf_lmhead_argmax(dev(h), dev(W), ws, ids=ids, maxlogit=mx)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(ids), ids_ref)
+        assert np.all(np.abs(host(mx) - mx_ref) <= logit_error_bound(h, W, ids_ref))
+    assert ws.device_error() == (0, 0)
+    assert not ws.buf.any().item(), "workspace must be left zeroed"
+
+
+def test_lmhead_argmax_ties_lowest_id():
+    d, V, P = 64, 600, 3
+    W = synth.normal_bf16(3, 0, V, d, 0.05)
+    W[[17, 333, 599]] = synth.to_bf16_bits(np.full((3, d), 0.5, np.float32))   # identical, dominant rows
+    h = synth.to_bf16_bits(np.abs(np.random.default_rng(0).standard_normal((P, d))).astype(np.float32))
+    ws = wf.Workspace(P)
+    ids = wf.wf_lmhead_argmax(dev(h), dev(W), ws)
+    assert host(ids).tolist() == [17, 17, 17]
+
+
+# ------------------------------------------------------------------ verify
+def _random_trees(seed, B, max_nodes):
+    rng = np.random.default_rng(seed)
+    pos_off, node_off, par, tok, kinds = [0], [0], [], [], []
+    for b in range(B):
+        N = int(rng.integers(0, max_nodes + 1))
+        kinds.append(int(rng.integers(0, 2)))
+        p = [int(rng.integers(-1, i)) if i else -1 for i in range(N)] if kinds[-1] else list(range(-1, N - 1))
+        par += p
+        tok += rng.integers(0, 3, N).tolist()
+        pos_off.append(pos_off[-1] + N + 1)
+        node_off.append(node_off[-1] + N)
+    P = pos_off[-1]
+    g = rng.integers(0, 3, P).astype(np.int32)
+    return (g, np.array(tok, np.int32), np.array(par, np.int32), np.array(pos_off, np.int32),
+            np.array(node_off, np.int32), np.array(kinds, np.int32))
+
+
+@pytest.mark.parametrize("seed,B,max_nodes", [(1, 1, 60), (2, 37, 8), (3, 300, 70), (4, 5, 256), (5, 64, 0)])
+def test_verify_tree_and_chain(seed, B, max_nodes):
+    g, tok, par, pos_off, node_off, kinds = _random_trees(seed, B, max_nodes)
+    ws = wf.Workspace(int(pos_off[-1]), B)
+    ps = 12
+    n, bo, la, pa = wf.wf_verify_tree(dev(g), dev(tok), dev(par), dev(node_off), dev(pos_off), ws, path_stride=ps)
+    rn, rb, rl, rp, rc = o().verify_tree(g, tok, par, node_off, pos_off, ps)
+    assert rc == 0
+    assert np.array_equal(host(n), rn) and np.array_equal(host(bo), rb) and np.array_equal(host(la), rl)
+    assert np.array_equal(host(pa), rp)
+    # chains on their own (every sequence read as a DFlash block)
+    cn, cb, cl, cp = wf.wf_verify_chain(dev(g), dev(tok), dev(pos_off), dev(node_off), ws, path_stride=ps)
+    rn, rb, rl, rp = o().verify_chain(g, tok, pos_off, node_off, ps)
+    assert np.array_equal(host(cn), rn) and np.array_equal(host(cb), rb) and np.array_equal(host(cl), rl)
+    assert np.array_equal(host(cp), rp)
+    assert ws.device_error() == (0, 0)
+
+
+def test_verify_golden_cases():
+    import pins
+    for fname, tree in (("trees.txt", True), ("chains.txt", False)):
+        cases = pins.read_cases(fname)
+        seqs = [(c["g"], c.get("tok", c.get("draft")), c.get("parent", list(range(-1, len(c.get("draft", [])) - 1))))
+                for c in cases]
+        g, tok, par, pos_off, node_off = pins._pack(seqs)
+        ws = wf.Workspace(len(g), len(cases))
+        if tree:
+            n, bo, la, _ = wf.wf_verify_tree(dev(g), dev(tok), dev(par), dev(node_off), dev(pos_off), ws)
+        else:
+            n, bo, la, _ = wf.wf_verify_chain(dev(g), dev(tok), dev(pos_off), dev(node_off), ws)
+        for b, c in enumerate(cases):
+            e = c["expect"]
+            assert host(n)[b] == e["n"] and host(bo)[b] == e["bonus"], c["name"]
+            assert host(la)[b] - pos_off[b] == e["last"], c["name"]
+
+
+def test_verify_bad_parent_sets_error():
+    g = np.array([1, 2, 3, 5, 6, 1, 2], np.int32)
+    tok = np.array([1, 2, 5, 1], np.int32)
+    par = np.array([-1, 1, -1, 3], np.int32)       # seq 0: parent[1] = 1 (not < 1); seq 1 fine
+    pos_off = np.array([0, 3, 5, 7], np.int32)
+    node_off = np.array([0, 2, 3, 4], np.int32)    # seq 2: node 0 has parent 3 (out of range)
+    par = np.array([-1, 1, -1, 3], np.int32)
+    ws = wf.Workspace(7, 3)
+    n, bo, la, _ = wf.wf_verify_tree(dev(g), dev(tok), dev(par), dev(node_off), dev(pos_off), ws)
+    assert host(n)[0] == -1 and host(n)[2] == -1 and host(n)[1] == 1 and host(bo)[1] == 6
+    code, info = ws.device_error()
+    assert code == 5 and info in (0, 2)
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("B,d,m", [(1, 2560, 1024), (1, 2560, 320), (7, 256, 128), (33, 64, 5), (256, 512, 64)])
+def test_router(B, d, m):
+    rng = np.random.default_rng(B * 7 + m)
+    P = B + 3
+    h = synth.normal_bf16(B + d, 1, P, d, 1.0)
+    rows = rng.permutation(P)[:B].astype(np.int32)
+    W1 = (rng.standard_normal((m, d)) * 0.05).astype(np.float32)
+    b1 = (rng.standard_normal(m) * 0.05).astype(np.float32)
+    w2 = (rng.standard_normal(m) * 0.05).astype(np.float32)
+    b2, tau = 0.1, 0.3
+    ref, rroute = o().router(h, rows, W1, b1, w2, b2, tau)
+    ws = wf.Workspace(P, B, m)
+    for _ in range(2):
+        delta, route = wf.wf_router_mlp(dev(h), dev(rows), dev(W1), dev(b1), dev(w2), b2, tau, ws)
+        torch.cuda.synchronize()
+        assert np.max(np.abs(host(delta) - ref)) <= 1e-3
+        clear = np.abs(ref - tau) >= synth.GAP_MIN
+        assert np.array_equal(host(route)[clear], rroute[clear])
+    assert not ws.buf.any().item()
+
+
+# ------------------------------------------------------------------ draft head
+@pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
+                                      (1, 2560, 32000, 10)])
+def test_draft_topk(B, d, Vd, k):
+    Wd = synth.normal_bf16(Vd + d, 0, Vd, d, 0.02 if d >= 256 else 0.1)
+    d2t = np.random.default_rng(Vd).permutation(151936)[:Vd].astype(np.int32)
+    x = synth.normal_bf16(B + 1, 1, B, d, 1.0)
+    for a in range(1, 64):
+        dids, tids, vals, _, mg = o().draft_topk(x, Wd, d2t, k)
+        bad = np.nonzero(mg < synth.GAP_MIN)[0]
+        if not len(bad):
+            break
+        for r in bad:
+            x[r] = synth.hidden_row(B + 1, int(r), a, d)
+    ws = wf.Workspace(1, B, 1, Vd, k)
+    for _ in range(2):
+        gi, gt, gv = wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), k, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(gi), dids) and np.array_equal(host(gt), tids)
+        bound = np.stack([logit_error_bound(x[b:b + 1].repeat(k, 0), Wd, dids[b]) for b in range(B)])
+        assert np.all(np.abs(host(gv) - vals) <= bound)
+    assert ws.device_error() == (0, 0)
+    assert not ws.buf.any().item()
+
+
+def test_draft_topk_bad_map():
+    Wd = synth.normal_bf16(5, 0, 300, 64, 0.1)
+    x = synth.normal_bf16(6, 1, 2, 64, 1.0)
+    d2t = np.full(300, -1, np.int32)
+    ws = wf.Workspace(1, 2, 1, 300, 4)
+    _, gt, _ = wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), 4, ws)
+    assert (host(gt) == -1).all()
+    assert ws.device_error()[0] == 5
+
+
+# ------------------------------------------------------------------ whole rounds
+def _compare_round(wl, out, seqs=None):
+    ref = o().round_(wl.hidden, wl.W, wl.pos_off, wl.node_off, wl.kind, wl.tok, wl.parent, wl.W1, wl.b1, wl.w2,
+                     wl.b2, wl.tau, out["path"].shape[1]) if seqs is None else None
+    if ref is not None:
+        for key in ("ids", "n_accept", "bonus", "last_pos", "path", "route"):
+            assert np.array_equal(out[key], ref[key]), key
+        assert np.max(np.abs(out["delta_al"] - ref["delta"])) <= 1e-3
+    assert np.array_equal(out["n_accept"][wl.planted], wl.cut[wl.planted])
+
+
+@pytest.mark.parametrize("index", [0, 1, 2])
+def test_round_batch1_configs(index):
+    wl = synth.make_workload(index, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn)
+    r, out = round_on_gpu(wl)
+    assert r.ws.device_error() == (0, 0)
+    _compare_round(wl, out)
+    check_round_properties(wl, out)
+    if wl.Wd is not None:
+        dids, tids, vals, _, _ = o().draft_topk(wl.x, wl.Wd, wl.d2t, wl.topk)
+        assert np.array_equal(out["draft_ids"], dids) and np.array_equal(out["tids"], tids)
+    # a second round on the same workspace gives the same answer
+    out2 = {k: host(v) for k, v in r().items()}
+    for key in ("ids", "n_accept", "bonus", "route"):
+        assert np.array_equal(out2[key], out[key])
+
+
+def _sampled_round(index, plant):
+    wl = synth.make_workload(index, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn, plant_seqs=plant)
+    r, out = round_on_gpu(wl)
+    assert r.ws.device_error() == (0, 0)
+    check_round_properties(wl, out)
+    rows = np.concatenate([np.arange(wl.pos_off[b], wl.pos_off[b + 1]) for b in plant])
+    ids, _, _ = o().lmhead_argmax(wl.hidden[rows], wl.W)
+    assert np.array_equal(out["ids"][rows], ids)
+    assert np.array_equal(out["n_accept"][plant], wl.cut[plant])
+    last = np.array([wl.expected_last_pos(b) for b in plant], np.int32)
+    assert np.array_equal(out["last_pos"][plant], last)
+    delta, route = o().router(wl.hidden, last, wl.W1, wl.b1, wl.w2, wl.b2, wl.tau)
+    assert np.max(np.abs(out["delta_al"][plant] - delta)) <= 1e-3
+    assert np.array_equal(out["route"][plant], route)
+    # router at every sequence's own last row (GPU rows, oracle arithmetic)
+    delta_all, _ = o().router(wl.hidden, out["last_pos"], wl.W1, wl.b1, wl.w2, wl.b2, wl.tau)
+    assert np.max(np.abs(out["delta_al"] - delta_all)) <= 1e-3
+    return wl, out
+
+
+def test_round_mixed_batch32_sampled():
+    wl0 = synth._structure(synth.CONFIGS[3], synth.seed_of(3), 32)[0]
+    chains = [b for b in range(32) if wl0[b] == 0][:2]
+    trees = [b for b in range(32) if wl0[b] == 1][:2]
+    _sampled_round(3, chains + trees)
+
+
+def test_round_batch256_sampled():
+    wl, out = _sampled_round(4, [0, 137, 255])
+    xs = [0, 137, 255]
+    dids, tids, _, _, _ = o().draft_topk(wl.x[xs], wl.Wd, wl.d2t, wl.topk)
+    assert np.array_equal(out["draft_ids"][xs], dids) and np.array_equal(out["tids"][xs], tids)
+
+
+def test_round_edge_shapes():
+    """One-row sequences (no drafts), tiny vocabulary, d = 8, a lone chain."""
+    for kinds, d, V in (([0], 8, 40), ([1, 0, 1], 64, 257), ([0, 0], 16, 1)):
+        wl = synth.small_workload(31 + d, d=d, V=V, kinds=kinds, argmax_fn=oracle.argmax_fn, m=8, K=3,
+                                  n_nodes=4, depth=2, branch=2, router_fn=oracle.router_fn, reject=V > 1)
+        r, out = round_on_gpu(wl)
+        assert r.ws.device_error() == (0, 0)
+        _compare_round(wl, out)
