@@ -105,6 +105,15 @@ WF_API wf_status wf_read_device_error(void* ws, int* code, int* info, int clear,
 WF_API void wf_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * Diagnostic for the failure path: enqueues one kernel whose single wait (an
+ * mbarrier nothing ever arrives on, the same bounded wait the pipelined
+ * kernels use) gives up after timeout_ns (<= 1e10) and records WF_ERR_TIMEOUT
+ * in the workspace error word; the context stays usable.  No passage of the
+ * pages corresponds to it.
+ */
+WF_API wf_status wf_probe_bounded_wait(uint64_t timeout_ns, void* ws, size_t ws_bytes, wf_stream_t stream);
+
+/*
  * Target LM head fused with the greedy choice (WhiFlash paper Sec. 3.3.1:
  * under greedy decoding the target's next token at a verified position is
  * the argmax of its next-token distribution; Sec. 4 "Evaluation": greedy

@@ -19,6 +19,8 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s);
 
+wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s);
+
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
 
@@ -110,6 +112,13 @@ wf_status wf_read_device_error(void* ws, int* code, int* info, int clear, wf_str
         if (cudaStreamSynchronize(stream) != cudaSuccess) return WF_ERR_CUDA;
     }
     return WF_OK;
+}
+
+wf_status wf_probe_bounded_wait(uint64_t timeout_ns, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    if (timeout_ns > 10000000000ull) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
+    WF_TRY(check_device());
+    return launch_wait_probe(timeout_ns, ws, stream);
 }
 
 wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,

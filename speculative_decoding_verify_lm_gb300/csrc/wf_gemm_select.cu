@@ -40,6 +40,8 @@ struct GemmParams {
     int N_w;           // weight rows (V or Vd)
     int num_m, num_n, num_k;
     int k;             // top-k count (top-k mode)
+    int bn;            // weight rows per tile (UMMA N): a multiple of 16, 128..256
+    uint32_t idesc;    // instruction descriptor for M = BM, N = bn
     int weight_evict_first;
     uint64_t* keys;    // argmax: [M_rows] packed keys, zero on entry, zero on exit
     int32_t* ids;      // argmax: [M_rows] out
@@ -133,9 +135,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                    mbar_arrive_expect_tx(&full[s], A_BYTES + p.bn * BK * 2);
                     tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kc * BK, m * BM, pol_a);
-                    tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * BN, pol_w);
+                    tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * p.bn, pol_w);
                 }
             }
             if (!ok || *abort_flag) {
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+            const uint32_t idesc = p.idesc;
             uint32_t it = 0, tile_i = 0;
             bool ok = true, issued = false;
             for (int t = blockIdx.x; t < T && ok; t += gridDim.x, ++tile_i) {
@@ -209,12 +211,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             if (quad_live) {
                 const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = 0; c0 < p.bn; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + c0, r);
                     tmem_ld_wait();
-                    const int col0 = n * BN + c0;
-                    const int lim = p.N_w - col0;  // columns >= lim are past the weight matrix
+                    const int col0 = n * p.bn + c0;
+                    // columns >= lim are past the weight matrix or past this tile
+                    const int lim = min(p.N_w - col0, p.bn - c0);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float v = __uint_as_float(r[j]);
@@ -362,6 +365,25 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 
 int num_sms();
 
+// Weight rows per tile.  Several activation tiles: 256 (largest operand reuse).
+// One activation tile (the weight-streaming case): the multiple of 16 in
+// [BN_MIN, 256] that minimises the busiest CTA's rows, waves x (bn + 16) - the
+// 16 standing for a tile's fixed cost - so the last wave is not left mostly idle.
+static int pick_bn(int num_m, int N_w, int sms) {
+    if (num_m > 1) return BN;
+    int best = BN;
+    long best_cost = -1;
+    for (int bn = BN; bn >= BN_MIN; bn -= 16) {
+        const long waves = cdiv(cdiv(N_w, bn), sms);
+        const long cost = waves * (bn + 16);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 template <int KT>
 static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, int k,
                                uint64_t* keys, int32_t* ids, float* maxlogit, uint64_t* cand, Control* ctrl,
@@ -377,12 +399,16 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     }
     CUtensorMap ta, tb;
     if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, BM)) return WF_ERR_CUDA;
-    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, BN)) return WF_ERR_CUDA;
+    const int num_m = cdiv(M_rows, BM);
+    const int bn = pick_bn(num_m, N_w, num_sms());
+    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)bn)) return WF_ERR_CUDA;
     GemmParams p;
     p.M_rows = M_rows;
     p.N_w = N_w;
-    p.num_m = cdiv(M_rows, BM);
-    p.num_n = cdiv(N_w, BN);
+    p.num_m = num_m;
+    p.num_n = cdiv(N_w, bn);
+    p.bn = bn;
+    p.idesc = umma_idesc_bf16(BM, bn);
     p.num_k = cdiv(d, BK);
     p.k = k;
     p.weight_evict_first = p.num_m == 1;
@@ -412,7 +438,8 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     uint64_t* cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
     wf_status st = launch_select<KT_TOPK>(x, B, Wd, Vd, d, k, nullptr, nullptr, nullptr, cand, ctrl, s);
     if (st != WF_OK) return st;
-    topk_merge_kernel<<<cdiv(B, 4), 128, 0, s>>>(cand, B, cdiv(B, BM), cdiv(Vd, BN), k, d2t, Vd, draft_ids, tids,
+    const int bn = pick_bn(cdiv(B, BM), Vd, num_sms());
+    topk_merge_kernel<<<cdiv(B, 4), 128, 0, s>>>(cand, B, cdiv(B, BM), cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids,
                                                  vals, ctrl);
     return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
 }

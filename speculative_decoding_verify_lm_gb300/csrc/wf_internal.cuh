@@ -33,7 +33,8 @@ struct Layout {
 
 // tiles of the draft-head GEMM (rows x weight rows)
 constexpr int BM = 128;    // activation rows per tile  (UMMA M)
-constexpr int BN = 256;    // weight rows per tile      (UMMA N)
+constexpr int BN = 256;    // weight rows per tile      (UMMA N, largest)
+constexpr int BN_MIN = 128;  // smallest weight-row tile the scheduler picks
 constexpr int BK = 64;     // K elements per pipeline stage (128 bytes of bf16)
 constexpr int ROUTER_UNITS_PER_CTA = 8;
 constexpr int ROUTER_MAX_WIDTH = 65536;
@@ -47,7 +48,7 @@ inline Layout layout(int P, int B, int m, int Vd, int k) {
     off = align_up(off + sizeof(uint64_t) * (size_t)(P > 0 ? P : 0), 256);
     L.cand = off;
     if (Vd > 0 && k > 0) {
-        size_t tiles = (size_t)cdiv(B, BM) * (size_t)cdiv(Vd, BN);
+        size_t tiles = (size_t)cdiv(B, BM) * (size_t)cdiv(Vd, BN_MIN);
         off = align_up(off + tiles * BM * (size_t)k * sizeof(uint64_t), 256);
     }
     L.part = off;

@@ -179,3 +179,24 @@ wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* par
 }
 
 }  // namespace wf
+
+namespace wf {
+
+// Exercises the bounded-wait path every pipelined kernel uses: one thread
+// waits on an mbarrier that nothing arrives on, gives up after timeout_ns and
+// records WF_ERR_TIMEOUT in the workspace's error word.
+__global__ void bounded_wait_probe_kernel(uint64_t timeout_ns, Control* ctrl) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (!mbar_wait(&bar, 0, timeout_ns, nullptr)) record_error(ctrl, WF_ERR_TIMEOUT, 0xFFFFu);
+    }
+}
+
+wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s) {
+    bounded_wait_probe_kernel<<<1, 32, 0, s>>>(timeout_ns, reinterpret_cast<Control*>(ws));
+    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+}  // namespace wf

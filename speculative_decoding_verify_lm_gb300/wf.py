@@ -60,6 +60,7 @@ _SIGS = {
     "wf_workspace_init": (_i32, [_c_void_p, _sz, _c_void_p]),
     "wf_read_device_error": (_i32, [_c_void_p, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32, _c_void_p]),
     "wf_set_wait_timeout_ns": (None, [_u64]),
+    "wf_probe_bounded_wait": (_i32, [_u64, _c_void_p, _sz, _c_void_p]),
     "wf_lmhead_argmax": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz,
                                 _c_void_p]),
     "wf_verify_chain": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p,
@@ -155,6 +156,10 @@ def wf_workspace_bytes(P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0) 
 
 def wf_set_wait_timeout_ns(ns: int) -> None:
     lib().wf_set_wait_timeout_ns(int(ns))
+
+
+def wf_probe_bounded_wait(timeout_ns: int, ws: Workspace, stream=None) -> None:
+    _raise(lib().wf_probe_bounded_wait(int(timeout_ns), ws.ptr, ws.nbytes, _stream(stream)), "wf_probe_bounded_wait")
 
 
 def wf_lmhead_argmax(hidden, W, ws: Workspace, ids=None, maxlogit=None, stream=None):

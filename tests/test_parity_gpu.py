@@ -264,3 +264,16 @@ def test_round_edge_shapes():
         r, out = round_on_gpu(wl)
         assert r.ws.device_error() == (0, 0)
         _compare_round(wl, out)
+
+
+# ------------------------------------------------------------------ failure path
+def test_bounded_wait_gives_up_and_context_survives():
+    ws = wf.Workspace(8)
+    wf.wf_probe_bounded_wait(20_000_000, ws)          # 20 ms on a barrier nothing arrives on
+    assert ws.device_error(clear=True) == (6, 0xFFFF)
+    # the context is still usable: a normal call afterwards succeeds
+    W = synth.normal_bf16(1, 0, 300, 64, 0.1)
+    h = _gapped_hidden(2, 4, 64, W)
+    ids = wf.wf_lmhead_argmax(dev(h), dev(W), ws)
+    assert np.array_equal(host(ids), o().lmhead_argmax(h, W)[0])
+    assert ws.device_error() == (0, 0)
