@@ -86,7 +86,7 @@ class ClockSampler:
          "clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index):
         self.proc = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
@@ -274,7 +274,11 @@ def main():
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize(device)
-    sampler = ClockSampler(local)
+    try:   # the physical GPU behind this rank's device (CUDA_VISIBLE_DEVICES may renumber)
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         if flush:

@@ -393,9 +393,10 @@ def small_workload(seed: int, d: int, V: int, kinds: list, argmax_fn: ArgmaxFn,
     """A free-shaped workload for parity sweeps (same distributions as the configs).
 
     kinds: per sequence 0 (chain of K) or 1 (tree of n_nodes, depth ``depth``)."""
+    # weights ~N(0, 1/d): logits of unit scale at any d, as at d = 2560 with std 0.02
     cfg = Config(f"custom_{seed}", d=d, V=V, B=len(kinds), kind="mixed", m=m, cut="uniform16",
                  draft_head=Vd > 0, K=K, n_nodes=n_nodes, depth=depth, branch=branch, Vd=max(Vd, 1),
-                 topk=topk)
+                 topk=topk, w_std=float(d) ** -0.5)
     rng = _rng(seed, _T_STRUCT)
     parents, paths, cuts = [], [], []
     for k in kinds:
@@ -425,7 +426,7 @@ def small_workload(seed: int, d: int, V: int, kinds: list, argmax_fn: ArgmaxFn,
     attempts = {}
     todo = np.arange(P)
     g = np.full(P, -1, np.int64)
-    for _ in range(64):
+    for _ in range(256):
         ids, gap = argmax_fn(W, hidden[todo])
         g[todo] = ids
         if not reject or gap is None:
@@ -453,7 +454,7 @@ def small_workload(seed: int, d: int, V: int, kinds: list, argmax_fn: ArgmaxFn,
                   tau=cfg.tau, cut=np.array(cuts, np.int32), planted=np.ones(B, bool),
                   max_depth=max(K if 0 in kinds else 0, depth if 1 in kinds else 0), path_nodes=paths)
     if reject and router_fn is not None:
-        for _ in range(64):
+        for _ in range(256):
             rows = np.array([wl.expected_last_pos(b) for b in range(B)], np.int64)
             delta = np.asarray(router_fn(W1, b1, w2, b2, hidden[rows]))
             bad = [b for b in range(B) if abs(float(delta[b]) - wl.tau) < GAP_MIN]
@@ -472,7 +473,7 @@ def small_workload(seed: int, d: int, V: int, kinds: list, argmax_fn: ArgmaxFn,
         if reject and topk_gap_fn is not None:
             xa = {}
             todo = np.arange(B)
-            for _ in range(64):
+            for _ in range(256):
                 gaps = np.asarray(topk_gap_fn(wl.Wd, wl.topk, wl.x[todo]))
                 bad = todo[gaps < GAP_MIN]
                 if not len(bad):

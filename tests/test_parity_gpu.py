@@ -258,9 +258,9 @@ def test_round_batch256_sampled():
 
 def test_round_edge_shapes():
     """One-row sequences (no drafts), tiny vocabulary, d = 8, a lone chain."""
-    for kinds, d, V in (([0], 8, 40), ([1, 0, 1], 64, 257), ([0, 0], 16, 1)):
+    for kinds, d, V in (([0], 8, 40), ([1, 0, 1], 64, 257), ([0, 0], 16, 2)):
         wl = synth.small_workload(31 + d, d=d, V=V, kinds=kinds, argmax_fn=oracle.argmax_fn, m=8, K=3,
-                                  n_nodes=4, depth=2, branch=2, router_fn=oracle.router_fn, reject=V > 1)
+                                  n_nodes=4, depth=2, branch=2, router_fn=oracle.router_fn, reject=V > 2)
         r, out = round_on_gpu(wl)
         assert r.ws.device_error() == (0, 0)
         _compare_round(wl, out)
