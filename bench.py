@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--router-width", type=int, default=None, help="override m (the paper's m = d/8 = 320)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct wf_round calls instead of a CUDA graph")
     return ap.parse_args()
 
 
@@ -269,6 +270,19 @@ def main():
     code, info = r.ws.device_error()
     if code:
         raise RuntimeError(f"device error {code} (info {info}) during warm-up")
+    # the round's launches captured once in a CUDA graph and replayed per step
+    step = r
+    if not args.no_graph:
+        ref_ids = r.out["ids"].clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            r()
+        step = g.replay
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize(device)
+        if not torch.equal(ref_ids, r.out["ids"]):
+            raise RuntimeError("graph replay disagrees with a direct wf_round call")
 
     # ---- timed region: K whole rounds, CUDA events on the launching stream
     if pg is not None:
@@ -284,7 +298,7 @@ def main():
         if flush:
             l2buf.zero_()
         ev[i][0].record(stream)
-        r()
+        step()
         ev[i][1].record(stream)
     torch.cuda.synchronize(device)
     if pg is not None:
@@ -378,7 +392,8 @@ def main():
                    "draft_head": f"{cfg.Vd}x{d} top-{wl.topk}" if draft else None,
                    "l2": "flushed between steps (working set < 2x L2)" if flush
                    else f"inputs larger than L2 (weights {weight_bytes / 1e6:.0f} MB streamed per step)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": "direct wf_round calls" if args.no_graph else "wf_round captured in a CUDA graph"},
         "accepted_tokens_per_s": tot_acc / max_s,
         "mean_acceptance_length": accepted / B,
         "roofline": roof,

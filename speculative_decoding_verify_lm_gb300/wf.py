@@ -110,7 +110,18 @@ def _check(t: Optional[torch.Tensor], name: str, dtypes, optional=False):
         raise ValueError(f"{name} must be contiguous")
     if t.dtype not in dtypes:
         raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if t.numel() == 0:   # an empty array still needs a valid (never read) device address
+        return _placeholder(t.device)
     return t.data_ptr()
+
+
+_placeholders = {}
+
+
+def _placeholder(device) -> int:
+    if device not in _placeholders:
+        _placeholders[device] = torch.zeros(16, dtype=torch.int32, device=device)
+    return _placeholders[device].data_ptr()
 
 
 _BF16 = (torch.bfloat16, torch.int16, torch.uint16) if hasattr(torch, "uint16") else (torch.bfloat16, torch.int16)
