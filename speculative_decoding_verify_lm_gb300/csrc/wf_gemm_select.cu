@@ -43,6 +43,7 @@ struct GemmParams {
     int bn;            // weight rows per tile (UMMA N): a multiple of 16, 128..256
     uint32_t idesc;    // instruction descriptor for M = BM, N = bn
     int weight_evict_first;
+    int a_bytes;       // bytes one activation box delivers (box rows x 128 B)
     uint64_t* keys;    // argmax: [M_rows] packed keys, zero on entry, zero on exit
     int32_t* ids;      // argmax: [M_rows] out
     float* maxlogit;   // argmax: [M_rows] out or null
@@ -117,6 +118,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above overlaps the previous kernel on the stream; inputs and
+    // the workspace are touched only after it has finished.  The next kernel
+    // may be scheduled right away (it waits for this one the same way).
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -135,7 +141,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], A_BYTES + p.bn * BK * 2);
+                    mbar_arrive_expect_tx(&full[s], p.a_bytes + p.bn * BK * 2);
                     tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kc * BK, m * BM, pol_a);
                     tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * p.bn, pol_w);
                 }
@@ -283,6 +289,8 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const uint64_t* __restr
                                                          int num_n, int k, const int32_t* __restrict__ d2t, int Vd,
                                                          int32_t* draft_ids, int32_t* tids, float* vals,
                                                          Control* ctrl) {
+    pdl_trigger();
+    pdl_wait();
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= B) return;
@@ -398,8 +406,13 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
         attr_set[dev] = true;
     }
     CUtensorMap ta, tb;
-    if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, BM)) return WF_ERR_CUDA;
     const int num_m = cdiv(M_rows, BM);
+    // With a single activation tile the box covers only the rows that exist
+    // (rounded up to a whole 8-row swizzle atom): no zero rows cross the
+    // crossbar.  The UMMA still reads all BM rows of the stage; rows past the
+    // box hold stale data and produce accumulator rows the epilogue never keeps.
+    const int a_rows = num_m == 1 ? (M_rows + 7) / 8 * 8 : BM;
+    if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, (uint32_t)a_rows)) return WF_ERR_CUDA;
     const int bn = pick_bn(num_m, N_w, num_sms());
     if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)bn)) return WF_ERR_CUDA;
     GemmParams p;
@@ -412,6 +425,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.num_k = cdiv(d, BK);
     p.k = k;
     p.weight_evict_first = p.num_m == 1;
+    p.a_bytes = a_rows * BK * 2;
     p.keys = keys;
     p.ids = ids;
     p.maxlogit = maxlogit;
@@ -420,8 +434,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.timeout_ns = wait_timeout_ns();
     const int tiles = p.num_m * p.num_n;
     const int grid = tiles < num_sms() ? tiles : num_sms();
-    gemm_select_kernel<KT><<<grid, GEMM_THREADS, GEMM_SMEM, s>>>(ta, tb, p);
-    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+    return launch(gemm_select_kernel<KT>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, p);
 }
 
 wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
@@ -439,9 +452,8 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     wf_status st = launch_select<KT_TOPK>(x, B, Wd, Vd, d, k, nullptr, nullptr, nullptr, cand, ctrl, s);
     if (st != WF_OK) return st;
     const int bn = pick_bn(cdiv(B, BM), Vd, num_sms());
-    topk_merge_kernel<<<cdiv(B, 4), 128, 0, s>>>(cand, B, cdiv(B, BM), cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids,
-                                                 vals, ctrl);
-    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+    return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, (const uint64_t*)cand, B, cdiv(B, BM),
+                  cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids, vals, ctrl);
 }
 
 }  // namespace wf

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "wf.h"
 
 namespace wf {
@@ -59,6 +61,31 @@ inline Layout layout(int P, int B, int m, int Vd, int k) {
 
 // process-wide bound on device waits (ns)
 uint64_t wait_timeout_ns();
+
+// ----------------------------------------------------------------- launches
+// Every kernel is launched with programmatic stream serialization: it may be
+// scheduled while its predecessor on the stream is still running, and waits
+// (pdl_wait) for the predecessor's memory before it reads any input.  It lets
+// its own dependent start early with pdl_trigger.  Without the attribute both
+// instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline wf_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
 
 // ----------------------------------------------------------------- device helpers
 __device__ __forceinline__ void record_error(Control* c, uint32_t code, uint32_t info) {

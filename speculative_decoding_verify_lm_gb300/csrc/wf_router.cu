@@ -5,21 +5,32 @@
 // with h_b the bf16 hidden row rows[b] widened to fp32, exact-erf GELU, and
 // dropout as the identity.
 //
-// One warp per hidden unit j (8 units per CTA).  The CTA stages up to RB
-// hidden rows in shared memory, each warp streams its W1 row with 16-byte
-// loads and keeps RB dot products; units are folded per CTA into
-// w2[j] * GELU(z_j) partials, and the last CTA to finish sums the partials of
-// every sequence in a fixed order (so the result does not depend on CTA
-// scheduling) and writes delta_al and route.
+// One warp per hidden unit j (8 units per CTA).  W1 does not depend on the
+// kernels before this one in a round, so each warp loads its W1 row into
+// registers (d <= 2560) before waiting on its predecessor: in a round the
+// router's weights stream while the LM head is still running, and only the
+// hidden rows are read after the wait.  The CTA stages up to RB hidden rows
+// in shared memory and keeps RB dot products per warp; units are folded per
+// CTA into w2[j] * GELU(z_j) partials, and the last CTA to finish sums the
+// partials of every sequence in a fixed order (the result does not depend on
+// CTA scheduling) and writes delta_al and route.
 #include "wf_internal.cuh"
 
 namespace wf {
 
 constexpr int ROUTER_THREADS = ROUTER_UNITS_PER_CTA * 32;
-constexpr int ROUTER_RB = 8;                       // hidden rows staged per pass
+constexpr int ROUTER_RB = 8;        // hidden rows staged per pass
+constexpr int ROUTER_WREG = 20;     // float4 of a W1 row held per lane: d <= 32 * 4 * 20 = 2560
 constexpr int ROUTER_SMEM_MAX = 160 * 1024;
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+
+__device__ __forceinline__ float dot4(const float4 w, const uint2 h, float acc) {
+    acc = fmaf(w.x, __uint_as_float(h.x << 16), acc);
+    acc = fmaf(w.y, __uint_as_float(h.x & 0xFFFF0000u), acc);
+    acc = fmaf(w.z, __uint_as_float(h.y << 16), acc);
+    return fmaf(w.w, __uint_as_float(h.y & 0xFFFF0000u), acc);
+}
 
 __global__ void __launch_bounds__(ROUTER_THREADS)
     router_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
@@ -27,7 +38,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
                   float b2, float tau, float* delta_al, int32_t* route, float* part, int rb_max, Control* ctrl) {
     // part: [B][gridDim.x] partial sums, zero on entry and on exit
     extern __shared__ uint8_t smem_raw[];
-    uint16_t* sh = reinterpret_cast<uint16_t*>(smem_raw);    // [rb_max][d] bf16
+    uint16_t* sh = reinterpret_cast<uint16_t*>(smem_raw);  // [rb_max][d] bf16
     __shared__ float red[ROUTER_UNITS_PER_CTA][ROUTER_RB];
     __shared__ int s_row[ROUTER_RB];
     __shared__ int s_last;
@@ -37,10 +48,22 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     const int j = blockIdx.x * ROUTER_UNITS_PER_CTA + w;
     const int nblk = gridDim.x;
     const bool unit_live = j < m;
-    const float bias1 = unit_live ? b1[j] : 0.f;
-    const float wout = unit_live ? w2[j] : 0.f;
     const float4* wrow = reinterpret_cast<const float4*>(W1 + (size_t)(unit_live ? j : 0) * d);
     const int d4 = d >> 2;
+    const bool in_regs = d4 <= 32 * ROUTER_WREG;
+
+    // ---- independent of the predecessor: weights
+    float4 wv[ROUTER_WREG];
+#pragma unroll
+    for (int u = 0; u < ROUTER_WREG; ++u) {
+        const int c = lane + 32 * u;
+        wv[u] = (in_regs && unit_live && c < d4) ? __ldg(wrow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float bias1 = unit_live ? b1[j] : 0.f;
+    const float wout = unit_live ? w2[j] : 0.f;
+
+    pdl_trigger();
+    pdl_wait();   // rows[] and the hidden states come from the kernels before this one
 
     for (int b0 = 0; b0 < B; b0 += rb_max) {
         const int nb = min(rb_max, B - b0);
@@ -65,16 +88,33 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
 #pragma unroll
         for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = 0.f;
         if (unit_live) {
-            for (int c = lane; c < d4; c += 32) {
-                const float4 wv = __ldg(wrow + c);
+            if (in_regs) {
 #pragma unroll
-                for (int rb = 0; rb < ROUTER_RB; ++rb) {
-                    if (rb < nb) {
-                        const uint2 hv = reinterpret_cast<const uint2*>(sh + (size_t)rb * d)[c];
-                        acc[rb] = fmaf(wv.x, __uint_as_float(hv.x << 16), acc[rb]);
-                        acc[rb] = fmaf(wv.y, __uint_as_float(hv.x & 0xFFFF0000u), acc[rb]);
-                        acc[rb] = fmaf(wv.z, __uint_as_float(hv.y << 16), acc[rb]);
-                        acc[rb] = fmaf(wv.w, __uint_as_float(hv.y & 0xFFFF0000u), acc[rb]);
+                for (int u = 0; u < ROUTER_WREG; ++u) {
+                    const int c = lane + 32 * u;
+                    if (c < d4) {
+#pragma unroll
+                        for (int rb = 0; rb < ROUTER_RB; ++rb)
+                            if (rb < nb)
+                                acc[rb] = dot4(wv[u], reinterpret_cast<const uint2*>(sh + (size_t)rb * d)[c], acc[rb]);
+                    }
+                }
+            } else {
+                for (int c0 = lane; c0 < d4; c0 += 32 * 4) {
+                    float4 wl[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        wl[u] = c0 + 32 * u < d4 ? __ldg(wrow + c0 + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = c0 + 32 * u;
+                        if (c < d4) {
+#pragma unroll
+                            for (int rb = 0; rb < ROUTER_RB; ++rb)
+                                if (rb < nb)
+                                    acc[rb] = dot4(wl[u], reinterpret_cast<const uint2*>(sh + (size_t)rb * d)[c],
+                                                   acc[rb]);
+                        }
                     }
                 }
             }
@@ -104,15 +144,15 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     __threadfence();
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
         const int r = rows[b];
+        float* pb = part + (size_t)b * nblk;
         if (r < 0 || (P >= 0 && r >= P)) {
             if (delta_al) delta_al[b] = __int_as_float(0x7fc00000);
             if (route) route[b] = -1;
             record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
-            for (int c = 0; c < nblk; ++c) part[(size_t)b * nblk + c] = 0.f;
+            for (int c = 0; c < nblk; ++c) pb[c] = 0.f;
             continue;
         }
         float s = b2;
-        float* pb = part + (size_t)b * nblk;
         for (int c = 0; c < nblk; ++c) {
             s += __ldcg(pb + c);
             pb[c] = 0.f;  // leave the workspace zeroed
@@ -127,8 +167,11 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s) {
     if (B == 0) return WF_OK;
+    // rows staged per pass: no more than the batch (a small footprint lets the
+    // CTAs sit next to the LM-head CTAs while they wait), at most what fits
     int rb = (int)((size_t)ROUTER_SMEM_MAX / ((size_t)d * 2));
     rb = rb < 1 ? 1 : (rb > ROUTER_RB ? ROUTER_RB : rb);
+    rb = rb > B ? B : rb;
     const size_t smem = (size_t)rb * d * 2;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -141,10 +184,8 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
     }
     Control* ctrl = reinterpret_cast<Control*>(ws);
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
-    router_kernel<<<cdiv(m, ROUTER_UNITS_PER_CTA), ROUTER_THREADS, smem, s>>>(hidden, rows, B, d, m, P, W1, b1, w2,
-                                                                             b2, tau, delta_al, route, part, rb,
-                                                                             ctrl);
-    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+    return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA)), dim3(ROUTER_THREADS), smem, s, hidden, rows, B,
+                  d, m, P, W1, b1, w2, b2, tau, delta_al, route, part, rb, ctrl);
 }
 
 }  // namespace wf

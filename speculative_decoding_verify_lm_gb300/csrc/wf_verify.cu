@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     __shared__ int16_t s_dist[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ uint8_t s_ok[VERIFY_WARPS][WF_MAX_SEQ_NODES];
 
+    pdl_trigger();
+    pdl_wait();
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * VERIFY_WARPS + w;
@@ -172,10 +174,9 @@ wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* par
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
                         void* ws, cudaStream_t s) {
     if (B == 0) return WF_OK;
-    verify_kernel<<<cdiv(B, VERIFY_WARPS), VERIFY_WARPS * 32, 0, s>>>(
-        g, tok, parent, kind, default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path,
-        reinterpret_cast<Control*>(ws));
-    return cudaGetLastError() == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+    return launch(verify_kernel, dim3(cdiv(B, VERIFY_WARPS)), dim3(VERIFY_WARPS * 32), 0, s, g, tok, parent, kind,
+                  default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path,
+                  reinterpret_cast<Control*>(ws));
 }
 
 }  // namespace wf
