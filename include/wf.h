@@ -134,6 +134,27 @@ WF_API wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int
                            wf_stream_t stream);
 
 /*
+ * wf_lmhead_argmax without a workspace: same inputs, outputs and result as
+ * wf_lmhead_argmax, but the scratch lives in a fixed array inside the
+ * library, for callers that cannot allocate device memory (a plug-in that a
+ * host engine calls with only its input and output buffers, or a decode loop
+ * that may not call cudaMalloc because it synchronises the device).  The
+ * pages have no counterpart to this entry point; it exists for those callers.
+ *
+ * Limits: P <= WF_NOALLOC_MAX_ROWS (else WF_ERR_INVALID_ARG, nothing
+ * enqueued).  Every loaded GPU holds the array (about 128 KB) until the
+ * process exits.  All calls on a device share it: calls that overlap on the
+ * GPU race, so serialise them (one stream).  The first call on a device looks
+ * up the array's address and should come before any stream capture.  It
+ * allocates nothing; each call clears the part of the array it uses.
+ * Device-side timeouts of this variant are not reported (its error word is
+ * cleared by the next call).
+ */
+#define WF_NOALLOC_MAX_ROWS 16384
+WF_API wf_status wf_lmhead_argmax_noalloc(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
+                                          int32_t* ids, float* maxlogit, wf_stream_t stream);
+
+/*
  * DFlash block verification (paper Sec. 3.2: the parallel block returns to
  * the target for parallel verification; App. A: block size 16 for Qwen3).
  * Sequence b owns verified rows pos_off[b] .. pos_off[b+1]-1; row pos_off[b]

@@ -20,6 +20,8 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
                         void* ws, size_t part_off, cudaStream_t s);
 
 wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s);
+wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                                float* maxlogit, cudaStream_t s);
 
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -128,6 +130,14 @@ wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int
     WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, 0, 0, 0).total));
     WF_TRY(check_device());
     return launch_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, ws, stream);
+}
+
+wf_status wf_lmhead_argmax_noalloc(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                                   float* maxlogit, wf_stream_t stream) {
+    if (!hidden || !W || !ids || bad_gemm_shape(P, d, V) || P > WF_NOALLOC_MAX_ROWS) return WF_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_device());
+    return noalloc_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, stream);
 }
 
 wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t* pos_off, const int32_t* node_off,

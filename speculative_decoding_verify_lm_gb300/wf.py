@@ -63,6 +63,7 @@ _SIGS = {
     "wf_probe_bounded_wait": (_i32, [_u64, _c_void_p, _sz, _c_void_p]),
     "wf_lmhead_argmax": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz,
                                 _c_void_p]),
+    "wf_lmhead_argmax_noalloc": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p]),
     "wf_verify_chain": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p,
                                _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "wf_verify_tree": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
@@ -182,6 +183,21 @@ def wf_lmhead_argmax(hidden, W, ws: Workspace, ids=None, maxlogit=None, stream=N
                                 _check(ids, "ids", _I32), _check(maxlogit, "maxlogit", _F32, True), ws.ptr, ws.nbytes,
                                 _stream(stream))
     _raise(st, "wf_lmhead_argmax")
+    return ids
+
+
+def wf_lmhead_argmax_noalloc(hidden, W, ids=None, maxlogit=None, stream=None):
+    """The LM-head argmax without a workspace (scratch in a fixed array inside the
+    library), for callers that cannot allocate device memory.  Calls on one device
+    share that array: do not let them overlap on the GPU."""
+    P, d = hidden.shape
+    V = W.shape[0]
+    if ids is None:
+        ids = torch.empty(P, dtype=torch.int32, device=hidden.device)
+    st = lib().wf_lmhead_argmax_noalloc(_check(hidden, "hidden", _BF16), _check(W, "W", _BF16), P, d, V,
+                                        _check(ids, "ids", _I32), _check(maxlogit, "maxlogit", _F32, True),
+                                        _stream(stream))
+    _raise(st, "wf_lmhead_argmax_noalloc")
     return ids
 
 
