@@ -118,10 +118,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_sha() -> str:
+KERNEL_SOURCES = {"gemm_select_kernel<1>": ("wf_gemm_select.cu", "wf_internal.cuh")}
+
+
+def source_sha(kernel: str) -> str:
+    """Hash of the source files a kernel is built from (its ncu counters go stale when they change)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verify_lm_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -144,7 +148,7 @@ def traffic_for(kernel: str, workload: str):
     with open(p) as f:
         j = json.load(f)
     e = j.get(f"{kernel}@{workload}")
-    if not e or e.get("source_sha") != source_sha():
+    if not e or e.get("source_sha") != source_sha(kernel):
         return None
     return e.get("bytes_per_launch")
 
