@@ -349,37 +349,33 @@ def main():
                  "algorithmic_per_launch": alg_bytes if hbm_bound else alg_flops, "launch_ms": k_ms,
                  "peak_source": f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'}, burst)"})
 
-    # ---- end to end through the public API: pinned host inputs in, results out, every step
-    names_in = ["hidden", "tok", "parent", "pos_off", "node_off", "kind"] + (["x"] if draft else [])
-    host_in = {n: torch.from_numpy(np.ascontiguousarray(getattr(wl, n)).view(np.int16)
-                                   if getattr(wl, n).dtype == np.uint16 else np.ascontiguousarray(getattr(wl, n))
-                                   ).pin_memory() for n in names_in}
-    names_out = ["n_accept", "bonus", "last_pos", "delta_al", "route"] + (["tids"] if draft else [])
-    host_out = {n: torch.empty_like(r.out[n], device="cpu").pin_memory() for n in names_out}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    # ---- end to end through the public API: every step copies the round's inputs
+    # (hidden states, drafts, trees, offsets, drafter states) from one pinned host
+    # buffer, runs wf_round and reads every output back into one pinned buffer
+    host_in = r.pinned_inputs()
+    host_out = r.pinned_outputs()
+    h2d, d2h = host_in.numel(), host_out.numel()
     for _ in range(2):
-        for n in names_in:
-            r.inputs[n].copy_(host_in[n], non_blocking=True)
+        r.upload(host_in)
         r()
-        for n in names_out:
-            host_out[n].copy_(r.out[n], non_blocking=True)
+        r.download(host_out)
         torch.cuda.synchronize(device)
     if pg is not None:
         pg.barrier()
-    e2e_s = 0.0   # per-step wall clock: copies in, round, results out, synchronise (L2 flush excluded)
+    e2e_s = 0.0   # per-step wall clock: copy in, round, copy out, synchronise (L2 flush excluded)
     for i in range(args.steps):
         if flush:
             l2buf.zero_()
         torch.cuda.synchronize(device)
         t1 = time.perf_counter()
-        for n in names_in:
-            r.inputs[n].copy_(host_in[n], non_blocking=True)
+        r.upload(host_in)
         r()
-        for n in names_out:
-            host_out[n].copy_(r.out[n], non_blocking=True)
+        r.download(host_out)
         torch.cuda.synchronize(device)
         e2e_s += time.perf_counter() - t1
+    got = r.host_views(host_out)
+    if not np.array_equal(got["n_accept"].numpy(), r.out["n_accept"].cpu().numpy()):
+        raise RuntimeError("end-to-end outputs disagree with the device outputs")
     e2e_max = allreduce_max(pg, e2e_s, device)
 
     if rank != 0:

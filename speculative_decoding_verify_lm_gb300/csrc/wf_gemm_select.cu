@@ -119,10 +119,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // the prologue above overlaps the previous kernel on the stream; inputs and
-    // the workspace are touched only after it has finished.  The next kernel
-    // may be scheduled right away (it waits for this one the same way).
-    pdl_trigger();
+    // the workspace are touched only after it has finished.  Then the next
+    // kernel may be scheduled (everything before this one is complete by now).
     pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const uint64_t* __restr
                                                          int num_n, int k, const int32_t* __restrict__ d2t, int Vd,
                                                          int32_t* draft_ids, int32_t* tids, float* vals,
                                                          Control* ctrl) {
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= B) return;

@@ -64,10 +64,13 @@ uint64_t wait_timeout_ns();
 
 // ----------------------------------------------------------------- launches
 // Every kernel is launched with programmatic stream serialization: it may be
-// scheduled while its predecessor on the stream is still running, and waits
-// (pdl_wait) for the predecessor's memory before it reads any input.  It lets
-// its own dependent start early with pdl_trigger.  Without the attribute both
-// instructions are no-ops.
+// scheduled while its predecessor on the stream is still running.  Each
+// kernel first waits for its predecessor (pdl_wait), then lets its own
+// dependent be scheduled (pdl_trigger).  So when a kernel starts, everything
+// before its predecessor has completed, and before its own wait it may read
+// any input that its predecessor does not write (weights, draft tokens,
+// offsets) - that prefetch overlaps the predecessor.  Without the launch
+// attribute both instructions are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

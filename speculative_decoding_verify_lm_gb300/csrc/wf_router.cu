@@ -5,11 +5,11 @@
 // with h_b the bf16 hidden row rows[b] widened to fp32, exact-erf GELU, and
 // dropout as the identity.
 //
-// One warp per hidden unit j (8 units per CTA).  W1 does not depend on the
-// kernels before this one in a round, so each warp loads its W1 row into
-// registers (d <= 2560) before waiting on its predecessor: in a round the
-// router's weights stream while the LM head is still running, and only the
-// hidden rows are read after the wait.  The CTA stages up to RB hidden rows
+// One warp per hidden unit j (8 units per CTA).  W1 is not written by the
+// kernel before this one in a round (the acceptance step), so each warp loads
+// its W1 row into registers (d <= 2560) before waiting on that kernel: the
+// weight stream overlaps it, and only the rows to route and the hidden states
+// are read after the wait.  The CTA stages up to RB hidden rows
 // in shared memory and keeps RB dot products per warp; units are folded per
 // CTA into w2[j] * GELU(z_j) partials, and the last CTA to finish sums the
 // partials of every sequence in a fixed order (the result does not depend on
@@ -62,8 +62,8 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     const float bias1 = unit_live ? b1[j] : 0.f;
     const float wout = unit_live ? w2[j] : 0.f;
 
+    pdl_wait();   // rows[] (a verify call's last_pos) comes from the kernel before this one
     pdl_trigger();
-    pdl_wait();   // rows[] and the hidden states come from the kernels before this one
 
     for (int b0 = 0; b0 < B; b0 += rb_max) {
         const int nb = min(rb_max, B - b0);
@@ -142,23 +142,27 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        const int r = rows[b];
+    // one warp per sequence: lane l sums partials l, l+32, ... (independent
+    // loads), then a fixed xor tree - the same order on every run
+    for (int b = w; b < B; b += ROUTER_UNITS_PER_CTA) {
         float* pb = part + (size_t)b * nblk;
-        if (r < 0 || (P >= 0 && r >= P)) {
-            if (delta_al) delta_al[b] = __int_as_float(0x7fc00000);
-            if (route) route[b] = -1;
-            record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
-            for (int c = 0; c < nblk; ++c) pb[c] = 0.f;
-            continue;
+        float s = 0.f;
+        for (int c = lane; c < nblk; c += 32) s += __ldcg(pb + c);
+        for (int c = lane; c < nblk; c += 32) pb[c] = 0.f;  // leave the workspace zeroed
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) {
+            const int r = rows[b];
+            if (r < 0 || (P >= 0 && r >= P)) {
+                if (delta_al) delta_al[b] = __int_as_float(0x7fc00000);
+                if (route) route[b] = -1;
+                record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+            } else {
+                s += b2;
+                if (delta_al) delta_al[b] = s;
+                if (route) route[b] = s > tau ? 1 : 0;
+            }
         }
-        float s = b2;
-        for (int c = 0; c < nblk; ++c) {
-            s += __ldcg(pb + c);
-            pb[c] = 0.f;  // leave the workspace zeroed
-        }
-        if (delta_al) delta_al[b] = s;
-        if (route) route[b] = s > tau ? 1 : 0;
     }
     if (threadIdx.x == 0) ctrl->router_done = 0;
 }

@@ -27,20 +27,39 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     __shared__ int16_t s_anc[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_dist[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ uint8_t s_ok[VERIFY_WARPS][WF_MAX_SEQ_NODES];
+    __shared__ int32_t s_g[VERIFY_WARPS][WF_MAX_SEQ_NODES + 1];
 
-    pdl_trigger();
-    pdl_wait();
+    const unsigned FULL = 0xffffffffu;
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * VERIFY_WARPS + w;
-    if (b >= B) return;
-    const unsigned FULL = 0xffffffffu;
+    const bool live = b < B;
 
-    const int r0 = pos_off[b], r1 = pos_off[b + 1];
-    const int n0 = node_off[b], n1 = node_off[b + 1];
-    const int N = n1 - n0;
-    const bool shape_ok = r0 >= 0 && r1 > r0 && (P < 0 || r1 <= P) && n0 >= 0 && N >= 0 &&
-                          N == r1 - r0 - 1 && N <= WF_MAX_SEQ_NODES;
+    // ---- inputs the predecessor (the LM head, in a round) does not write:
+    // read while it is still running
+    int r0 = 0, N = 0, kd = default_kind;
+    bool shape_ok = false;
+    int tk[NODES_PER_LANE], pa[NODES_PER_LANE];
+    if (live) {
+        r0 = pos_off[b];
+        const int r1 = pos_off[b + 1];
+        const int n0 = node_off[b];
+        N = node_off[b + 1] - n0;
+        shape_ok = r0 >= 0 && r1 > r0 && (P < 0 || r1 <= P) && n0 >= 0 && N >= 0 && N == r1 - r0 - 1 &&
+                   N <= WF_MAX_SEQ_NODES;
+        kd = kind ? kind[b] : default_kind;
+#pragma unroll
+        for (int s = 0; s < NODES_PER_LANE; ++s) {
+            const int i = lane + 32 * s;
+            const bool in = shape_ok && i < N;
+            tk[s] = in ? tok[n0 + i] : 0;
+            pa[s] = (in && kd != 0 && parent) ? parent[n0 + i] : -1;
+        }
+    }
+    pdl_wait();   // the target choices g come from the kernel before this one
+    pdl_trigger();
+    if (!live) return;
+
     auto fail = [&]() {
         if (lane == 0) {
             record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
@@ -51,23 +70,23 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
         if (path)
             for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = -1;
     };
-    if (!shape_ok) {
+    if (!shape_ok || (kd != 0 && !parent)) {
         fail();
         return;
     }
-    const int kd = kind ? kind[b] : default_kind;
-    if (kd != 0 && !parent) {
-        fail();
-        return;
-    }
+    int32_t* gs = s_g[w];   // target choice at each of this sequence's rows
+    for (int r = lane; r <= N; r += 32) gs[r] = g[r0 + r];
+    __syncwarp();
 
     if (kd == 0) {
         // ---------------------------------------------------------------- chain
         int n = N;
-        for (int base = 0; base < N; base += 32) {
+#pragma unroll
+        for (int s = 0; s < NODES_PER_LANE; ++s) {
+            const int base = 32 * s;
+            if (base >= N) break;
             const int j = base + lane;
-            const bool mism = j < N && tok[n0 + j] != g[r0 + j];
-            const unsigned mask = __ballot_sync(FULL, mism);
+            const unsigned mask = __ballot_sync(FULL, j < N && tk[s] != gs[j]);
             if (mask) {
                 n = base + __ffs(mask) - 1;
                 break;
@@ -76,7 +95,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
         if (lane == 0) {
             n_accept[b] = n;
             last_pos[b] = r0 + n;
-            bonus[b] = g[r0 + n];
+            bonus[b] = gs[n];
         }
         if (path)
             for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = j < n ? j : -1;
@@ -89,15 +108,18 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     int16_t* dist = s_dist[w];
     uint8_t* okf = s_ok[w];
     bool bad = false;
-    for (int i = lane; i < N; i += 32) {
-        const int pi = parent[n0 + i];
-        const bool pbad = pi < -1 || pi >= i;
-        bad |= pbad;
-        const int prow = pi < 0 ? r0 : r0 + 1 + pi;
-        par[i] = (int16_t)(pbad ? -1 : pi);
-        anc[i] = par[i];
-        dist[i] = 1;
-        okf[i] = (uint8_t)(!pbad && tok[n0 + i] == g[prow]);
+#pragma unroll
+    for (int s = 0; s < NODES_PER_LANE; ++s) {
+        const int i = lane + 32 * s;
+        if (i < N) {
+            const int pi = pa[s];
+            const bool pbad = pi < -1 || pi >= i;
+            bad |= pbad;
+            par[i] = (int16_t)(pbad ? -1 : pi);
+            anc[i] = par[i];
+            dist[i] = 1;
+            okf[i] = (uint8_t)(!pbad && tk[s] == gs[pi < 0 ? 0 : 1 + pi]);
+        }
     }
     if (__any_sync(FULL, bad)) {
         fail();
@@ -109,7 +131,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     for (int span = 1; span < N; span <<= 1) {
         int16_t na[NODES_PER_LANE], nd[NODES_PER_LANE];
         uint8_t no[NODES_PER_LANE];
-        bool live = false;
+        bool more = false;
 #pragma unroll
         for (int s = 0; s < NODES_PER_LANE; ++s) {
             const int i = lane + 32 * s;
@@ -119,7 +141,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
                     na[s] = anc[a];
                     nd[s] = (int16_t)(dist[i] + dist[a]);
                     no[s] = okf[i] & okf[a];
-                    live = true;
+                    more = true;
                 } else {
                     na[s] = -1;
                     nd[s] = dist[i];
@@ -127,7 +149,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
                 }
             }
         }
-        if (!__any_sync(FULL, live)) break;
+        if (!__any_sync(FULL, more)) break;
         __syncwarp();
 #pragma unroll
         for (int s = 0; s < NODES_PER_LANE; ++s) {
@@ -154,7 +176,6 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     }
     const int n = (int)(best >> 16);
     const int node = best ? 0xFFFF - (int)(best & 0xFFFF) : -1;
-    const int last = node < 0 ? r0 : r0 + 1 + node;
     if (path) {
         for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = -1;
         __syncwarp();
@@ -164,8 +185,8 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     }
     if (lane == 0) {
         n_accept[b] = n;
-        last_pos[b] = last;
-        bonus[b] = g[last];
+        last_pos[b] = r0 + 1 + node;   // the root row when node = -1
+        bonus[b] = gs[1 + node];
     }
 }
 

@@ -266,9 +266,36 @@ def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, 
     return draft_ids, tids, vals
 
 
+def _packed(spec, device):
+    """One uint8 device buffer holding every (name, dtype, shape) of ``spec`` at
+    256-byte aligned offsets; returns (buffer, {name: typed view})."""
+    offs, total = {}, 0
+    for name, dt, shape in spec:
+        n = 1
+        for s in shape:
+            n *= s
+        offs[name] = total
+        total += (n * torch.empty((), dtype=dt).element_size() + 255) // 256 * 256
+    buf = torch.zeros(max(total, 256), dtype=torch.uint8, device=device)
+    views = {}
+    for name, dt, shape in spec:
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        views[name] = buf[offs[name]:offs[name] + nbytes].view(dt).view(*shape)
+    return buf, views
+
+
 class Round:
     """Inputs and output buffers of wf_round, held as device tensors so the
-    call can be repeated (and captured in a CUDA graph) without re-marshalling."""
+    call can be repeated (and captured in a CUDA graph) without re-marshalling.
+
+    The per-round inputs (hidden states, drafted tokens, tree parents, offsets,
+    kinds, drafter hidden states) live in one packed device buffer and all
+    outputs in another, so a host program moves a round in and out with one
+    copy each (pinned_inputs / upload, pinned_outputs / download).  Weights
+    (W, W1, b1, w2, Wd, d2t) stay where the caller keeps them."""
 
     def __init__(self, hidden, W, pos_off, node_off, tok, W1, b1, w2, b2: float, tau: float, kind=None, parent=None,
                  path_stride: int = 0, x=None, Wd=None, d2t=None, k: int = 0, with_maxlogit: bool = False):
@@ -276,16 +303,38 @@ class Round:
         P, d = hidden.shape
         B = pos_off.numel() - 1
         m = W1.shape[0]
-        self.inputs = dict(hidden=hidden, W=W, pos_off=pos_off, node_off=node_off, tok=tok, W1=W1, b1=b1, w2=w2,
-                           kind=kind, parent=parent, x=x, Wd=Wd, d2t=d2t)
-        i32 = lambda *s: torch.empty(*s, dtype=torch.int32, device=dev)  # noqa: E731
-        self.out = dict(ids=i32(P), n_accept=i32(B), bonus=i32(B), last_pos=i32(B),
-                        path=i32((B, path_stride)) if path_stride else None,
-                        delta_al=torch.empty(B, dtype=torch.float32, device=dev), route=i32(B),
-                        maxlogit=torch.empty(P, dtype=torch.float32, device=dev) if with_maxlogit else None,
-                        draft_ids=i32((B, k)) if Wd is not None else None,
-                        tids=i32((B, k)) if Wd is not None else None,
-                        vals=torch.empty((B, k), dtype=torch.float32, device=dev) if Wd is not None else None)
+        N = tok.numel()
+        draft = Wd is not None
+        in_spec = [("hidden", hidden.dtype, (P, d)), ("tok", torch.int32, (N,)), ("pos_off", torch.int32, (B + 1,)),
+                   ("node_off", torch.int32, (B + 1,))]
+        if kind is not None:
+            in_spec.append(("kind", torch.int32, (B,)))
+        if parent is not None:
+            in_spec.append(("parent", torch.int32, (N,)))
+        if draft:
+            in_spec.append(("x", x.dtype, (B, d)))
+        self.in_buf, views = _packed(in_spec, dev)
+        for name, src in (("hidden", hidden), ("tok", tok), ("pos_off", pos_off), ("node_off", node_off),
+                          ("kind", kind), ("parent", parent), ("x", x)):
+            if name in views:
+                views[name].copy_(src.reshape(views[name].shape))
+        self.inputs = dict(W=W, W1=W1, b1=b1, w2=w2, Wd=Wd, d2t=d2t, kind=None, parent=None, x=None)
+        self.inputs.update(views)
+        hidden, tok, pos_off, node_off = views["hidden"], views["tok"], views["pos_off"], views["node_off"]
+        kind, parent, x = views.get("kind"), views.get("parent"), views.get("x")
+        out_spec = [("ids", torch.int32, (P,)), ("n_accept", torch.int32, (B,)), ("bonus", torch.int32, (B,)),
+                    ("last_pos", torch.int32, (B,)), ("delta_al", torch.float32, (B,)), ("route", torch.int32, (B,))]
+        if path_stride:
+            out_spec.append(("path", torch.int32, (B, path_stride)))
+        if with_maxlogit:
+            out_spec.append(("maxlogit", torch.float32, (P,)))
+        if draft:
+            out_spec += [("draft_ids", torch.int32, (B, k)), ("tids", torch.int32, (B, k)),
+                         ("vals", torch.float32, (B, k))]
+        self.out_buf, outs = _packed(out_spec, dev)
+        self.out = {name: outs.get(name) for name in ("ids", "n_accept", "bonus", "last_pos", "path", "delta_al",
+                                                      "route", "maxlogit", "draft_ids", "tids", "vals")}
+        self._in_spec, self._out_spec = in_spec, out_spec
         a = RoundArgs()
         a.hidden = _check(hidden, "hidden", _BF16)
         a.W = _check(W, "W", _BF16)
@@ -317,6 +366,47 @@ class Round:
     def __call__(self, stream=None):
         _raise(lib().wf_round(ctypes.byref(self.args), self.ws.ptr, self.ws.nbytes, _stream(stream)), "wf_round")
         return self.out
+
+    # ---- host staging: one pinned buffer in, one out
+    def pinned_inputs(self):
+        """A pinned host copy of the packed inputs (same layout as the device buffer)."""
+        return self.in_buf.cpu().pin_memory()
+
+    def pinned_outputs(self):
+        return torch.empty(self.out_buf.numel(), dtype=torch.uint8).pin_memory()
+
+    def upload(self, host_inputs, stream=None):
+        with torch.cuda.stream(stream) if stream is not None else _nullctx():
+            self.in_buf.copy_(host_inputs, non_blocking=True)
+
+    def download(self, host_outputs, stream=None):
+        with torch.cuda.stream(stream) if stream is not None else _nullctx():
+            host_outputs.copy_(self.out_buf, non_blocking=True)
+
+    def host_views(self, host_outputs):
+        """Typed views of the outputs inside a downloaded pinned buffer."""
+        _, views = _packed_views(host_outputs, self._out_spec)
+        return views
+
+
+class _nullctx:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *a):
+        return False
+
+
+def _packed_views(buf, spec):
+    off, views = 0, {}
+    for name, dt, shape in spec:
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        views[name] = buf[off:off + nbytes].view(dt).view(*shape)
+        off += (nbytes + 255) // 256 * 256
+    return buf, views
 
 
 def wf_round(hidden, W, pos_off, node_off, tok, W1, b1, w2, b2, tau, kind=None, parent=None, path_stride=0, x=None,
