@@ -1,6 +1,7 @@
 // C ABI entry points: host-side validation, workspace layout and the
 // stream-ordered composition of one verify-and-route round.
 #include <atomic>
+#include <mutex>
 
 #include "wf_internal.cuh"
 
@@ -14,7 +15,7 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
-                        void* ws, cudaStream_t s);
+                        void* ws, cudaStream_t s, RoutePick pick);
 wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s);
@@ -22,6 +23,30 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
 wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s);
 wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, cudaStream_t s);
+
+// A helper stream per device (created on first use, kept for the process)
+// with the two events that fork work onto it and join it back.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    std::mutex mu;
+};
+
+static SideStream* side_stream() {
+    static SideStream g_side[64];
+    static std::mutex g_mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    SideStream& ss = g_side[dev];
+    if (!ss.s) {
+        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    return &ss;
+}
 
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -148,7 +173,7 @@ wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t*
     WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
     WF_TRY(check_device());
     return launch_verify(g, draft, nullptr, nullptr, 0, pos_off, node_off, B, -1, path ? path_stride : 0,
-                         n_accept, bonus, last_pos, path, ws, stream);
+                         n_accept, bonus, last_pos, path, ws, stream, RoutePick{});
 }
 
 wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* node_off,
@@ -160,7 +185,7 @@ wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* pa
     WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
     WF_TRY(check_device());
     return launch_verify(g, tok, parent, nullptr, 1, pos_off, node_off, B, -1, path ? path_stride : 0, n_accept,
-                         bonus, last_pos, path, ws, stream);
+                         bonus, last_pos, path, ws, stream, RoutePick{});
 }
 
 wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, const float* W1,
@@ -205,11 +230,34 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
     const Layout L = layout(a->P, a->B, a->m, draft ? a->Vd : 0, draft ? a->k : 0);
     WF_TRY(check_ws(ws, ws_bytes, L.total));
     WF_TRY(check_device());
-    WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
-    WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
-                         a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream));
-    WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
-                         a->delta_al, a->route, ws, L.part, stream));
+    if (a->P <= ROUTE_ALL_ROWS_MAX) {
+        // Few rows: the router runs on every verified row on a helper stream
+        // while the LM head streams its weights; acceptance then picks the
+        // output of the row it accepted.
+        SideStream* ss = side_stream();
+        if (!ss) return WF_ERR_CUDA;
+        float* dall = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.dall);
+        {
+            std::lock_guard<std::mutex> lock(ss->mu);
+            if (cudaEventRecord(ss->fork, stream) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+                return WF_ERR_CUDA;
+            WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
+                                 nullptr, ws, L.part, ss->s));
+            if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return WF_ERR_CUDA;
+            WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+            if (cudaStreamWaitEvent(stream, ss->join, 0) != cudaSuccess) return WF_ERR_CUDA;
+        }
+        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
+                             RoutePick{dall, a->tau, a->delta_al, a->route}));
+    } else {
+        WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
+                             RoutePick{}));
+        WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
+                             a->delta_al, a->route, ws, L.part, stream));
+    }
     if (draft)
         WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals, ws,
                                  L.cand, stream));

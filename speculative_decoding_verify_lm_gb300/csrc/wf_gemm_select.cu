@@ -73,7 +73,13 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], floa
     }
 }
 
-template <int KT>
+// CL = 1: each CTA loads its own activation and weight boxes.
+// CL = 2: CTAs run in clusters of two on tile pairs (m, n) and (m + 1, n) that
+// share the weight tile: each CTA loads half of it and multicasts that half to
+// both, so every weight byte crosses the L2 -> SM crossbar once per pair.  A
+// stage is then written by both producers, so each CTA's "empty" barrier
+// counts the MMA completions of both CTAs.
+template <int KT, int CL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmParams p) {
@@ -92,12 +98,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int T = p.num_m * p.num_n;
+    // tile pairs (CL = 2) or tiles (CL = 1): u -> (activation tile m, weight tile n)
+    const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
+    const int slot = blockIdx.x / CL, nslots = gridDim.x / CL;
+    const int num_mp = (p.num_m + CL - 1) / CL;
+    const int U = num_mp * p.num_n;
+    constexpr uint16_t kPair = 0x3;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CL);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -116,6 +127,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CL == 2) cluster_sync();   // the peer's barriers exist before anything is multicast to them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // the prologue above overlaps the previous kernel on the stream; inputs and
@@ -129,10 +141,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_w = p.weight_evict_first ? policy_evict_first() : policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
+            const int half = p.bn / CL;                // weight rows this CTA fetches per stage
             uint32_t it = 0;  // stages issued so far
             bool ok = true;
-            for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-                const int m = t % p.num_m, n = t / p.num_m;
+            for (int u = slot; u < U && ok; u += nslots) {
+                const int m = (u % num_mp) * CL + rank, n = u / num_mp;
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -143,7 +156,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                     mbar_arrive_expect_tx(&full[s], p.a_bytes + p.bn * BK * 2);
                     tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kc * BK, m * BM, pol_a);
-                    tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * p.bn, pol_w);
+                    if constexpr (CL == 2)
+                        tma_load_2d_multicast(sB + s * B_BYTES + rank * half * BK * 2, &tmB, &full[s], kc * BK,
+                                              n * p.bn + rank * half, kPair, pol_w);
+                    else
+                        tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * p.bn, pol_w);
                 }
             }
             if (!ok || *abort_flag) {
@@ -158,7 +175,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t idesc = p.idesc;
             uint32_t it = 0, tile_i = 0;
             bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < T && ok; t += gridDim.x, ++tile_i) {
+            for (int u = slot; u < U && ok; u += nslots, ++tile_i) {
                 const uint32_t acc = tile_i & 1;
                 const uint32_t acc_ph = (tile_i >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], acc_ph ^ 1, p.timeout_ns, abort_flag)) {
@@ -182,13 +199,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per step (encoded >> 4)
                         umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
-                    umma_commit(&empty[s]);
+                    if constexpr (CL == 2)
+                        umma_commit_multicast(&empty[s], kPair);   // both CTAs wrote this stage
+                    else
+                        umma_commit(&empty[s]);
                     issued = true;
                 }
                 if (ok) umma_commit(&tfull[acc]);
             }
-            if (!ok && issued) {
-                umma_commit(drain);  // arrives when every MMA issued above has finished
+            if (issued && (!ok || CL == 2)) {
+                // every MMA issued above (and its arrivals, possibly on the peer) has completed
+                umma_commit(drain);
                 mbar_wait(drain, 0, p.timeout_ns, nullptr);
             }
         }
@@ -197,8 +218,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int rit = q * 32 + lane;
         uint32_t tile_i = 0;
-        for (int t = blockIdx.x; t < T; t += gridDim.x, ++tile_i) {
-            const int m = t % p.num_m, n = t / p.num_m;
+        for (int u = slot; u < U; u += nslots, ++tile_i) {
+            const int m = (u % num_mp) * CL + rank, n = u / num_mp;
             const uint32_t acc = tile_i & 1;
             const uint32_t acc_ph = (tile_i >> 1) & 1;
             const bool quad_live = m * BM + q * 32 < p.M_rows;
@@ -247,7 +268,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     atomicMax(reinterpret_cast<unsigned long long*>(p.keys + row),
                               (unsigned long long)pack_key(tv[0], (uint32_t)ti[0]));
                 } else {
-                    uint64_t* dst = p.cand + ((size_t)t * BM + rit) * p.k;
+                    const size_t t = (size_t)n * p.num_m + m;   // the candidate list of tile (m, n)
+                    uint64_t* dst = p.cand + (t * BM + rit) * p.k;
                     for (int j = 0; j < KT; ++j)
                         if (j < p.k) dst[j] = tv[j] == -INFINITY ? 0ull : pack_key(tv[j], (uint32_t)ti[j]);
                 }
@@ -277,6 +299,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (CL == 2) cluster_sync();   // the peer may still arrive on, or copy into, this CTA
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -392,6 +415,31 @@ static int pick_bn(int num_m, int N_w, int sms) {
     return best;
 }
 
+// Clusters of two that can be resident at once (queried once per device).
+template <int KT>
+static int pair_slots(int dev) {
+    static int cached[64];
+    if (dev < 64 && cached[dev]) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 64);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = GEMM_SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, 2>, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = num_sms() / 2;
+    }
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
 template <int KT>
 static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, int k,
                                uint64_t* keys, int32_t* ids, float* maxlogit, uint64_t* cand, Control* ctrl,
@@ -400,13 +448,17 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_select_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_select_kernel<KT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
     }
     CUtensorMap ta, tb;
     const int num_m = cdiv(M_rows, BM);
+    // several activation tiles: pairs of CTAs share each weight tile (multicast)
+    const int CL = num_m > 1 ? 2 : 1;
     // With a single activation tile the box covers only the rows that exist
     // (rounded up to a whole 8-row swizzle atom): no zero rows cross the
     // crossbar.  The UMMA still reads all BM rows of the stage; rows past the
@@ -414,7 +466,8 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     const int a_rows = num_m == 1 ? (M_rows + 7) / 8 * 8 : BM;
     if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, (uint32_t)a_rows)) return WF_ERR_CUDA;
     const int bn = pick_bn(num_m, N_w, num_sms());
-    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)bn)) return WF_ERR_CUDA;
+    // each CTA of a pair fetches half of the weight tile
+    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn / CL))) return WF_ERR_CUDA;
     GemmParams p;
     p.M_rows = M_rows;
     p.N_w = N_w;
@@ -432,9 +485,15 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.cand = cand;
     p.ctrl = ctrl;
     p.timeout_ns = wait_timeout_ns();
-    const int tiles = p.num_m * p.num_n;
-    const int grid = tiles < num_sms() ? tiles : num_sms();
-    return launch(gemm_select_kernel<KT>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, p);
+    if (CL == 1) {
+        const int tiles = p.num_m * p.num_n;
+        const int grid = tiles < num_sms() ? tiles : num_sms();
+        return launch(gemm_select_kernel<KT, 1>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, p);
+    }
+    const int pairs = cdiv(num_m, 2) * p.num_n;
+    const int slots = pair_slots<KT>(dev);
+    const int grid = 2 * (pairs < slots ? pairs : slots);
+    return launch_cluster(gemm_select_kernel<KT, 2>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta, tb, p);
 }
 
 wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,

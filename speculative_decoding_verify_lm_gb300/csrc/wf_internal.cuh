@@ -30,7 +30,28 @@ static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t keys, cand, part, total;
+    size_t keys, cand, part, dall, total;
+};
+
+// A round with at most this many verified rows runs the router on every row,
+// on a second stream while the LM head streams its weights; the acceptance
+// step then just picks the row it accepted.  Larger rounds route only the
+// last accepted row of each sequence, after the acceptance step.
+constexpr int ROUTE_ALL_ROWS_MAX = 128;
+
+// Optional tail of the acceptance step: copy the router output of the
+// accepted row (computed for every row beforehand) and take the decision.
+struct RoutePick {
+    const float* delta_all;   // [P] router output per verified row, or null (no pick)
+    float tau;
+    float* delta_al;          // [B]
+    int32_t* route;           // [B]
+    __device__ __forceinline__ void write(int b, int row) const {
+        if (!delta_all) return;
+        const float v = row >= 0 ? delta_all[row] : __int_as_float(0x7fc00000);
+        delta_al[b] = v;
+        route[b] = row >= 0 ? (v > tau ? 1 : 0) : -1;
+    }
 };
 
 // tiles of the draft-head GEMM (rows x weight rows)
@@ -54,7 +75,10 @@ inline Layout layout(int P, int B, int m, int Vd, int k) {
         off = align_up(off + tiles * BM * (size_t)k * sizeof(uint64_t), 256);
     }
     L.part = off;
-    off = align_up(off + sizeof(float) * (size_t)(B > 0 ? B : 0) * (size_t)cdiv(m > 0 ? m : 1, ROUTER_UNITS_PER_CTA), 256);
+    const int routed = (P > 0 && P <= ROUTE_ALL_ROWS_MAX && P > B) ? P : (B > 0 ? B : 0);
+    off = align_up(off + sizeof(float) * (size_t)routed * (size_t)cdiv(m > 0 ? m : 1, ROUTER_UNITS_PER_CTA), 256);
+    L.dall = off;
+    if (P > 0 && P <= ROUTE_ALL_ROWS_MAX) off = align_up(off + sizeof(float) * (size_t)P, 256);
     L.total = off;
     return L;
 }
@@ -75,19 +99,29 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
-inline wf_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                        Args&&... args) {
+inline wf_status launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                unsigned cluster, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? WF_OK : WF_ERR_CUDA;
+}
+
+template <typename... KArgs, typename... Args>
+inline wf_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        Args&&... args) {
+    return launch_cluster(kernel, grid, block, smem, s, 1u, std::forward<Args>(args)...);
 }
 
 // ----------------------------------------------------------------- device helpers
@@ -171,6 +205,24 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// Same, delivered to the same shared-memory offset (and mbarrier) of every
+// CTA of the cluster named in cta_mask.
+__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                                      int y, uint16_t cta_mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -218,6 +270,14 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+// Same, arriving on the mbarrier at this offset in every CTA of cta_mask.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // 32 lanes x 32 columns of 32-bit words from TMEM: thread t gets its lane's 32 columns.

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
         const int nb = min(rb_max, B - b0);
         __syncthreads();
         if (threadIdx.x < nb) {
-            int r = rows[b0 + threadIdx.x];
+            int r = rows ? rows[b0 + threadIdx.x] : b0 + threadIdx.x;   // no rows: route every row
             if (r < 0 || (P >= 0 && r >= P)) r = -1;
             s_row[threadIdx.x] = r;
         }
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
         if (lane == 0) {
-            const int r = rows[b];
+            const int r = rows ? rows[b] : b;
             if (r < 0 || (P >= 0 && r >= P)) {
                 if (delta_al) delta_al[b] = __int_as_float(0x7fc00000);
                 if (route) route[b] = -1;

@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     verify_kernel(const int32_t* __restrict__ g, const int32_t* __restrict__ tok, const int32_t* __restrict__ parent,
                   const int32_t* __restrict__ kind, int default_kind, const int32_t* __restrict__ pos_off,
                   const int32_t* __restrict__ node_off, int B, int P, int path_stride, int32_t* n_accept,
-                  int32_t* bonus, int32_t* last_pos, int32_t* path, Control* ctrl) {
+                  int32_t* bonus, int32_t* last_pos, int32_t* path, RoutePick pick, Control* ctrl) {
     __shared__ int16_t s_par[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_anc[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_dist[VERIFY_WARPS][WF_MAX_SEQ_NODES];
@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
             n_accept[b] = -1;
             bonus[b] = -1;
             last_pos[b] = -1;
+            pick.write(b, -1);
         }
         if (path)
             for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = -1;
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
             n_accept[b] = n;
             last_pos[b] = r0 + n;
             bonus[b] = gs[n];
+            pick.write(b, r0 + n);
         }
         if (path)
             for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = j < n ? j : -1;
@@ -187,16 +189,17 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
         n_accept[b] = n;
         last_pos[b] = r0 + 1 + node;   // the root row when node = -1
         bonus[b] = gs[1 + node];
+        pick.write(b, r0 + 1 + node);
     }
 }
 
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
-                        void* ws, cudaStream_t s) {
+                        void* ws, cudaStream_t s, RoutePick pick) {
     if (B == 0) return WF_OK;
     return launch(verify_kernel, dim3(cdiv(B, VERIFY_WARPS)), dim3(VERIFY_WARPS * 32), 0, s, g, tok, parent, kind,
-                  default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path,
+                  default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path, pick,
                   reinterpret_cast<Control*>(ws));
 }
 
