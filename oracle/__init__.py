@@ -119,6 +119,21 @@ class Oracle:
         assert rc == 0, rc
         return delta, route
 
+    def entropy(self, hidden, rows, W, tau: float = 0.0):
+        """Entropy of softmax(<h, W_v>) at each row -> (H f64 [B], route int32 [B])."""
+        hidden = np.ascontiguousarray(hidden, np.uint16)
+        rows = np.ascontiguousarray(rows, np.int32)
+        W = np.ascontiguousarray(W, np.uint16)
+        B = len(rows)
+        d = hidden.shape[1]
+        V = W.shape[0]
+        H = np.empty(B, np.float64)
+        route = np.empty(B, np.int32)
+        rc = self.lib.oracle_entropy(_p(hidden), _p(rows), ctypes.c_int(B), _p(W), ctypes.c_int64(d),
+                                     ctypes.c_int64(V), ctypes.c_double(tau), _p(H), _p(route))
+        assert rc == 0, rc
+        return H, route
+
     def draft_topk(self, x, Wd, d2t, k: int):
         """-> (draft_ids [B,k], target_ids [B,k], logits f64 [B,k], lse f64 [B], min_gap f64 [B])."""
         x = np.ascontiguousarray(x, np.uint16)
@@ -200,6 +215,10 @@ def router(*a, **k):
 
 def draft_topk(*a, **k):
     return default().draft_topk(*a, **k)
+
+
+def entropy(*a, **k):
+    return default().entropy(*a, **k)
 
 
 def round_(*a, **k):

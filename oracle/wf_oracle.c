@@ -178,6 +178,40 @@ int oracle_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* pare
     return rc;
 }
 
+/*
+ * Runtime-informed router, WhiFlash-Entropy (paper Sec. 3.3.1): the entropy of
+ * the target's next-token distribution p = softmax(logits) at row rows[b],
+ *   H[b] = - sum_v p_v log p_v   (natural log),
+ * and route[b] = 1 (autoregressive drafter) if H[b] > tau, else 0.
+ * The softmax is written with the usual max shift (it does not change p):
+ * p_v = exp(L_v - M) / sum_u exp(L_u - M), M = max_v L_v.
+ */
+int oracle_entropy(const uint16_t* hidden, const int32_t* rows, int B, const uint16_t* W, int64_t d, int64_t V,
+                   double tau, double* H, int32_t* route) {
+    if (!hidden || !rows || !W || !H || B < 0 || d <= 0 || V <= 0) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const uint16_t* h = hidden + (int64_t)rows[b] * d;
+        double* L = (double*)malloc((size_t)V * sizeof(double));
+        double M = -INFINITY;
+        for (int64_t v = 0; v < V; ++v) {
+            L[v] = logit(h, W + v * d, d);
+            if (L[v] > M) M = L[v];
+        }
+        double S = 0.0;
+        for (int64_t v = 0; v < V; ++v) S += exp(L[v] - M);
+        double ent = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+            const double p = exp(L[v] - M) / S;
+            if (p > 0.0) ent -= p * log(p);
+        }
+        H[b] = ent;
+        if (route) route[b] = ent > tau ? 1 : 0;
+        free(L);
+    }
+    return 0;
+}
+
 /* GELU in its exact form: x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)) (paper App. A). */
 double oracle_gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
 

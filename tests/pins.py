@@ -334,7 +334,55 @@ def check_topk_ties(o):
     assert list(dids[0][:2]) == [2, 9] and vals[0][0] == vals[0][1] and mg[0] == 0.0
 
 
+# ---------------------------------------------------------------- entropy router
+def check_entropy(o):
+    """H = -sum p log p of softmax(<h, W_v>): closed forms and scipy."""
+    from scipy.stats import entropy as sp_entropy
+    from scipy.special import softmax
+    rng = np.random.default_rng(9)
+    d, V = 16, 50
+    h = _rand_bf16(rng, (3, d), 1.0)
+    rows = np.array([0, 1, 2], np.int32)
+    # all logits equal: the uniform distribution, H = log V exactly (up to rounding)
+    H, _ = o.entropy(h, rows, np.zeros((V, d), np.uint16))
+    assert np.allclose(H, math.log(V), rtol=0, atol=1e-12)
+    # two identical rows far above the rest: H -> log 2
+    hp = to_bf16_bits(np.abs(rng.standard_normal((2, d))).astype(np.float32) + np.float32(0.5))
+    W = _rand_bf16(rng, (V, d), 0.01)
+    W[4] = to_bf16_bits(np.full(d, 8.0, np.float32))
+    W[30] = W[4]
+    H, _ = o.entropy(hp, np.array([0, 1], np.int32), W)
+    assert np.allclose(H, math.log(2.0), atol=1e-9)
+    # random weights against scipy
+    W = _rand_bf16(rng, (V, d), 0.5)
+    L = _f64(h) @ _f64(W).T
+    H, _ = o.entropy(h, rows[::-1].copy(), W)
+    want = [sp_entropy(softmax(L[r])) for r in rows[::-1]]
+    assert np.allclose(H, want, rtol=1e-12, atol=1e-12)
+    # softmax is shift invariant: adding 800 to every logit (exp(800) overflows
+    # a double) must leave H unchanged
+    hs, Ws = h.copy(), W.copy()
+    hs[:, -1] = to_bf16_bits(np.array([1.0], np.float32))[0]
+    Ws[:, -1] = to_bf16_bits(np.array([800.0], np.float32))[0]
+    Ls = _f64(hs) @ _f64(Ws).T
+    assert Ls.min() > 700
+    H, _ = o.entropy(hs, rows, Ws)
+    assert np.all(np.isfinite(H))
+    assert np.allclose(H, [sp_entropy(softmax(Ls[r] - 800.0)) for r in rows], rtol=1e-9, atol=1e-9)
+
+
+def check_entropy_route_strict(o):
+    d, V = 8, 16
+    h = np.zeros((1, d), np.uint16)
+    W = np.zeros((V, d), np.uint16)
+    logV = math.log(V)
+    _, r = o.entropy(h, np.array([0], np.int32), W, tau=logV)
+    assert list(r) == [0]
+    _, r = o.entropy(h, np.array([0], np.int32), W, tau=logV - 1e-6)
+    assert list(r) == [1]
+
+
 ALL_CHECKS = [check_argmax_bruteforce, check_argmax_ties, check_argmax_closed_form, check_chain_golden,
               check_tree_golden, check_tree_bruteforce, check_chain_is_linear_tree, check_tree_bad_parent,
               check_gelu_values, check_router_closed_forms, check_route_strict, check_topk_bruteforce,
-              check_topk_ties]
+              check_topk_ties, check_entropy, check_entropy_route_strict]

@@ -43,6 +43,12 @@ MUTANTS = [
      "return (x->id < y->id) - (x->id > y->id);", [pins.check_topk_ties]),
     ("log-sum-exp without the max shift", "lse[b] = mx + log(acc);", "lse[b] = log(acc);",
      [pins.check_topk_bruteforce]),
+    ("entropy without the max shift", "for (int64_t v = 0; v < V; ++v) S += exp(L[v] - M);",
+     "M = 0.0;\n        for (int64_t v = 0; v < V; ++v) S += exp(L[v] - M);", [pins.check_entropy]),
+    ("entropy in bits", "if (p > 0.0) ent -= p * log(p);", "if (p > 0.0) ent -= p * log2(p);",
+     [pins.check_entropy]),
+    ("entropy route on >=", "route[b] = ent > tau ? 1 : 0;", "route[b] = ent >= tau ? 1 : 0;",
+     [pins.check_entropy_route_strict]),
     ("top-k maps through the wrong id", "tids[(int64_t)b * k + j] = d2t[s[j].id];",
      "tids[(int64_t)b * k + j] = s[j].id;", [pins.check_topk_bruteforce]),
 ]
