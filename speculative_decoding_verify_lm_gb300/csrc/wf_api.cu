@@ -40,7 +40,10 @@ static SideStream* side_stream() {
     std::lock_guard<std::mutex> lock(g_mu);
     SideStream& ss = g_side[dev];
     if (!ss.s) {
-        if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        // lowest priority: the LM head, on the caller's stream, is scheduled first
+        int lo = 0, hi = 0;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) lo = 0;
+        if (cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, lo) != cudaSuccess) return nullptr;
         if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
@@ -241,10 +244,10 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
             std::lock_guard<std::mutex> lock(ss->mu);
             if (cudaEventRecord(ss->fork, stream) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
                 return WF_ERR_CUDA;
+            WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
             WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
                                  nullptr, ws, L.part, ss->s));
             if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return WF_ERR_CUDA;
-            WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
             if (cudaStreamWaitEvent(stream, ss->join, 0) != cudaSuccess) return WF_ERR_CUDA;
         }
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,

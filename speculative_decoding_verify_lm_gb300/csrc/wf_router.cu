@@ -22,6 +22,7 @@ constexpr int ROUTER_THREADS = ROUTER_UNITS_PER_CTA * 32;
 constexpr int ROUTER_RB = 8;        // hidden rows staged per pass
 constexpr int ROUTER_WREG = 20;     // float4 of a W1 row held per lane: d <= 32 * 4 * 20 = 2560
 constexpr int ROUTER_SMEM_MAX = 160 * 1024;
+constexpr int ROUTER_SMEM_RESIDENT = 16 * 1024;
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
@@ -171,9 +172,10 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s) {
     if (B == 0) return WF_OK;
-    // rows staged per pass: no more than the batch (a small footprint lets the
-    // CTAs sit next to the LM-head CTAs while they wait), at most what fits
-    int rb = (int)((size_t)ROUTER_SMEM_MAX / ((size_t)d * 2));
+    // rows staged per pass: no more than the batch, in at most 16 KB, so that
+    // the CTAs fit next to the LM-head CTAs (198 KB of shared memory each) when
+    // both run at once
+    int rb = (int)((size_t)ROUTER_SMEM_RESIDENT / ((size_t)d * 2));
     rb = rb < 1 ? 1 : (rb > ROUTER_RB ? ROUTER_RB : rb);
     rb = rb > B ? B : rb;
     const size_t smem = (size_t)rb * d * 2;
