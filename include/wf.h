@@ -81,10 +81,11 @@ WF_API int wf_version(void);
 
 /*
  * Workspace size (bytes) sufficient for every call below with at most
- * P verified rows, B sequences, router width m, draft vocabulary Vd and
- * top-k k (pass 0 for Vd / k when the draft head is not used).
+ * P verified rows, B sequences, hidden size d, router width m, draft
+ * vocabulary Vd and top-k k (pass 0 for Vd / k when the draft head is not
+ * used).
  */
-WF_API size_t wf_workspace_bytes(int P, int B, int m, int Vd, int k);
+WF_API size_t wf_workspace_bytes(int P, int B, int d, int m, int Vd, int k);
 
 /* Zero a workspace (asynchronously on `stream`).  Needed once before first use. */
 WF_API wf_status wf_workspace_init(void* ws, size_t ws_bytes, wf_stream_t stream);
@@ -153,6 +154,23 @@ WF_API wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int
 #define WF_NOALLOC_MAX_ROWS 16384
 WF_API wf_status wf_lmhead_argmax_noalloc(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
                                           int32_t* ids, float* maxlogit, wf_stream_t stream);
+
+/*
+ * Runtime-informed router, WhiFlash-Entropy (paper Sec. 3.3.1): at each
+ * selected row the entropy of the target's next-token distribution,
+ *   H[b]     = - sum_v p_v log p_v,  p = softmax(<hidden[row_b], W_v>) (natural log)
+ *   route[b] = 1 (autoregressive drafter) if H[b] > tau, else 0 (diffusion drafter)
+ * computed in the same weight sweep as an LM-head argmax (the logits stay in
+ * TMEM), with fp32 online softmax statistics.
+ *
+ * hidden device [P, d] bf16 bits; rows device [B] int32 rows of hidden, or
+ * NULL for rows 0 .. B-1 (then B <= P); 1 <= B <= 256; W as for
+ * wf_lmhead_argmax.  H device [B] fp32; route device [B] int32 or NULL.  A
+ * row outside [0, P) sets WF_ERR_BAD_DATA and writes NaN / -1 for it.
+ */
+WF_API wf_status wf_lmhead_entropy(const uint16_t* hidden, int P, int d, const int32_t* rows, int B,
+                                   const uint16_t* W, int V, float tau, float* H, int32_t* route, void* ws,
+                                   size_t ws_bytes, wf_stream_t stream);
 
 /*
  * DFlash block verification (paper Sec. 3.2: the parallel block returns to
@@ -276,7 +294,16 @@ typedef struct wf_round_args {
     int32_t* draft_ids;        /* [B, k] or NULL */
     int32_t* tids;             /* [B, k] (needed if Wd != NULL) */
     float* vals;               /* [B, k] or NULL */
+    /* routing policy: WF_ROUTER_NEURAL (the MLP above) or WF_ROUTER_ENTROPY
+     * (WhiFlash-Entropy: route = H > tau on the target's next-token
+     * distribution at the last accepted row; delta_al then receives H and
+     * W1 / b1 / w2 / m are not read).  The entropy policy needs P <= 128 or
+     * B <= 256. */
+    int router_kind;
 } wf_round_args;
+
+#define WF_ROUTER_NEURAL 0
+#define WF_ROUTER_ENTROPY 1
 
 WF_API wf_status wf_round(const wf_round_args* args, void* ws, size_t ws_bytes, wf_stream_t stream);
 

@@ -21,35 +21,13 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
                         void* ws, size_t part_off, cudaStream_t s);
 
 wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s);
+wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                                float* maxlogit, float* H, int32_t* route, float tau, const int32_t* src_rows,
+                                int src_P, void* ws, size_t ent_off, cudaStream_t s);
+wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t* rows, int B, uint16_t* out,
+                             void* ws, cudaStream_t s);
 wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, cudaStream_t s);
-
-// A helper stream per device (created on first use, kept for the process)
-// with the two events that fork work onto it and join it back.
-struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-    std::mutex mu;
-};
-
-static SideStream* side_stream() {
-    static SideStream g_side[64];
-    static std::mutex g_mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(g_mu);
-    SideStream& ss = g_side[dev];
-    if (!ss.s) {
-        // lowest priority: the LM head, on the caller's stream, is scheduled first
-        int lo = 0, hi = 0;
-        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) lo = 0;
-        if (cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, lo) != cudaSuccess) return nullptr;
-        if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
-            return nullptr;
-    }
-    return &ss;
-}
 
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -121,7 +99,7 @@ const char* wf_status_string(int status) {
 
 int wf_version(void) { return 100; }
 
-size_t wf_workspace_bytes(int P, int B, int m, int Vd, int k) { return layout(P, B, m, Vd, k).total; }
+size_t wf_workspace_bytes(int P, int B, int d, int m, int Vd, int k) { return layout(P, B, d, m, Vd, k).total; }
 
 void wf_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
 
@@ -155,7 +133,7 @@ wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int
                            float* maxlogit, void* ws, size_t ws_bytes, wf_stream_t stream) {
     if (!hidden || !W || !ids || bad_gemm_shape(P, d, V)) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
-    WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, 0, 0, 0).total));
+    WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, d, 0, 0, 0).total));
     WF_TRY(check_device());
     return launch_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, ws, stream);
 }
@@ -166,6 +144,24 @@ wf_status wf_lmhead_argmax_noalloc(const uint16_t* hidden, const uint16_t* W, in
     if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
     WF_TRY(check_device());
     return noalloc_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, stream);
+}
+
+wf_status wf_lmhead_entropy(const uint16_t* hidden, int P, int d, const int32_t* rows, int B, const uint16_t* W,
+                            int V, float tau, float* H, int32_t* route, void* ws, size_t ws_bytes,
+                            wf_stream_t stream) {
+    if (!hidden || !W || !H || bad_gemm_shape(P, d, V) || B < 1 || B > ENT_MAX_ROWS) return WF_ERR_INVALID_ARG;
+    if (!rows && B > P) return WF_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
+    const Layout L = layout(0, B, d, 0, 0, 0);
+    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_device());
+    const uint16_t* act = hidden;
+    if (rows) {
+        uint16_t* gath = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.gath);
+        WF_TRY(launch_gather_rows(hidden, P, d, rows, B, gath, ws, stream));
+        act = gath;
+    }
+    return launch_lmhead_entropy(act, W, B, d, V, nullptr, nullptr, H, route, tau, rows, P, ws, L.ent, stream);
 }
 
 wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t* pos_off, const int32_t* node_off,
@@ -197,7 +193,7 @@ wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int 
     if (B < 0 || d < 8 || d % 8 != 0 || m < 1 || m > ROUTER_MAX_WIDTH) return WF_ERR_INVALID_ARG;
     if (!hidden || !rows || !W1 || !b1 || !w2 || (!delta_al && !route)) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W1)) return WF_ERR_INVALID_ARG;
-    const Layout L = layout(0, B, m, 0, 0);
+    const Layout L = layout(0, B, d, m, 0, 0);
     WF_TRY(check_ws(ws, ws_bytes, L.total));
     WF_TRY(check_device());
     return launch_router(hidden, rows, B, d, m, -1, W1, b1, w2, b2, tau, delta_al, route, ws, L.part, stream);
@@ -209,7 +205,7 @@ wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2
     if (!x || !Wd || !d2t || bad_gemm_shape(B, d, Vd)) return WF_ERR_INVALID_ARG;
     if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals)) return WF_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
-    const Layout L = layout(0, B, 0, Vd, k);
+    const Layout L = layout(0, B, d, 0, Vd, k);
     WF_TRY(check_ws(ws, ws_bytes, L.total));
     WF_TRY(check_device());
     return launch_draft_topk(x, Wd, d2t, B, d, Vd, k, draft_ids, tids, vals, ws, L.cand, stream);
@@ -221,35 +217,48 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
     if (a->B < 1 || !a->pos_off || !a->node_off || !a->tok) return WF_ERR_INVALID_ARG;
     if (!a->kind && !a->parent) return WF_ERR_INVALID_ARG;
     if (a->path_stride < 0 || (a->path_stride > 0 && !a->path)) return WF_ERR_INVALID_ARG;
-    if (a->m < 1 || a->m > ROUTER_MAX_WIDTH || !a->W1 || !a->b1 || !a->w2) return WF_ERR_INVALID_ARG;
+    const bool entropy = a->router_kind == WF_ROUTER_ENTROPY;
+    if (a->router_kind != WF_ROUTER_NEURAL && !entropy) return WF_ERR_INVALID_ARG;
+    if (!entropy && (a->m < 1 || a->m > ROUTER_MAX_WIDTH || !a->W1 || !a->b1 || !a->w2)) return WF_ERR_INVALID_ARG;
+    if (entropy && a->P > ROUTE_ALL_ROWS_MAX && a->B > ENT_MAX_ROWS) return WF_ERR_UNSUPPORTED;
     if (!a->ids || !a->n_accept || !a->bonus || !a->last_pos || !a->delta_al || !a->route) return WF_ERR_INVALID_ARG;
-    if (!aligned16(a->hidden) || !aligned16(a->W) || !aligned16(a->W1)) return WF_ERR_INVALID_ARG;
+    if (!aligned16(a->hidden) || !aligned16(a->W) || (!entropy && !aligned16(a->W1))) return WF_ERR_INVALID_ARG;
     const bool draft = a->Wd != nullptr;
     if (draft) {
         if (!a->x || !a->d2t || !a->tids || bad_gemm_shape(a->B, a->d, a->Vd)) return WF_ERR_INVALID_ARG;
         if (a->k < 1 || a->k > WF_MAX_TOPK || a->k > a->Vd) return WF_ERR_INVALID_ARG;
         if (!aligned16(a->x) || !aligned16(a->Wd)) return WF_ERR_INVALID_ARG;
     }
-    const Layout L = layout(a->P, a->B, a->m, draft ? a->Vd : 0, draft ? a->k : 0);
+    const Layout L = layout(a->P, a->B, a->d, entropy ? 1 : a->m, draft ? a->Vd : 0, draft ? a->k : 0);
     WF_TRY(check_ws(ws, ws_bytes, L.total));
     WF_TRY(check_device());
-    if (a->P <= ROUTE_ALL_ROWS_MAX) {
-        // Few rows: the router runs on every verified row on a helper stream
-        // while the LM head streams its weights; acceptance then picks the
-        // output of the row it accepted.
-        SideStream* ss = side_stream();
-        if (!ss) return WF_ERR_CUDA;
-        float* dall = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.dall);
-        {
-            std::lock_guard<std::mutex> lock(ss->mu);
-            if (cudaEventRecord(ss->fork, stream) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
-                return WF_ERR_CUDA;
-            WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
-            WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
-                                 nullptr, ws, L.part, ss->s));
-            if (cudaEventRecord(ss->join, ss->s) != cudaSuccess) return WF_ERR_CUDA;
-            if (cudaStreamWaitEvent(stream, ss->join, 0) != cudaSuccess) return WF_ERR_CUDA;
-        }
+    float* dall = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.dall);
+    if (entropy && a->P <= ROUTE_ALL_ROWS_MAX) {
+        // WhiFlash-Entropy, few rows: the LM-head sweep also yields the entropy
+        // of every row; acceptance picks the accepted row's
+        WF_TRY(launch_lmhead_entropy(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, dall, nullptr, a->tau,
+                                     nullptr, 0, ws, L.ent, stream));
+        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
+                             RoutePick{dall, a->tau, a->delta_al, a->route}));
+    } else if (entropy) {
+        // many rows: a second sweep over the weights for the B accepted rows only
+        WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
+                             RoutePick{}));
+        uint16_t* gath = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.gath);
+        WF_TRY(launch_gather_rows(a->hidden, a->P, a->d, a->last_pos, a->B, gath, ws, stream));
+        WF_TRY(launch_lmhead_entropy(gath, a->W, a->B, a->d, a->V, nullptr, nullptr, a->delta_al, a->route, a->tau,
+                                     a->last_pos, a->P, ws, L.ent, stream));
+    } else if (a->P <= ROUTE_ALL_ROWS_MAX) {
+        // Few rows: the router runs on every verified row beside the LM head
+        // (it needs only the hidden states and its weights, and waits for the
+        // LM head just before it exits); acceptance then picks the output of
+        // the row it accepted.
+        WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
+                             nullptr, ws, L.part, stream));
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
                              RoutePick{dall, a->tau, a->delta_al, a->route}));

@@ -48,6 +48,12 @@ struct GemmParams {
     int32_t* ids;      // argmax: [M_rows] out
     float* maxlogit;   // argmax: [M_rows] out or null
     uint64_t* cand;    // top-k: [tiles][BM][k]
+    float4* ent;       // entropy: [CTA slot][M_rows] running (max, sum e^z, sum z e^z), z = logit - max
+    float* H;          // entropy: [M_rows] out
+    int32_t* route;    // entropy: [M_rows] out (H > tau) or null
+    float tau;
+    const int32_t* src_rows;   // entropy over gathered rows: the source row of each, or null
+    int src_P;
     Control* ctrl;
     uint64_t timeout_ns;
 };
@@ -55,6 +61,22 @@ struct GemmParams {
 __device__ __forceinline__ void gemm_fail(Control* ctrl, volatile int* abort_flag, uint32_t where) {
     *abort_flag = 1;
     record_error(ctrl, WF_ERR_TIMEOUT, where);
+}
+
+// Merge two partial softmax states (M, S = sum e^(L-M), T = sum (L-M) e^(L-M)).
+__device__ __forceinline__ void ent_merge(float& M, float& S, float& T, float m2, float s2, float t2) {
+    if (!(s2 > 0.f)) return;
+    if (!(S > 0.f)) {
+        M = m2;
+        S = s2;
+        T = t2;
+        return;
+    }
+    const float mx = fmaxf(M, m2);
+    const float a1 = __expf(M - mx), a2 = __expf(m2 - mx);
+    T = (T + (M - mx) * S) * a1 + (t2 + (m2 - mx) * s2) * a2;
+    S = S * a1 + s2 * a2;
+    M = mx;
 }
 
 // Insert (v, id) into a descending list of KT entries (earlier entry wins ties).
@@ -79,7 +101,11 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], floa
 // both, so every weight byte crosses the L2 -> SM crossbar once per pair.  A
 // stage is then written by both producers, so each CTA's "empty" barrier
 // counts the MMA completions of both CTAs.
-template <int KT, int CL>
+// ENT (with KT = 1): also accumulate, per row, the softmax statistics of the
+// logits so that the entropy of the next-token distribution comes out of the
+// same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
+// activation tiles).
+template <int KT, int CL, bool ENT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmParams p) {
@@ -217,6 +243,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int rit = q * 32 + lane;
+        float em = -INFINITY, es = 0.f, et = 0.f;   // ENT: this row's running softmax statistics
         uint32_t tile_i = 0;
         for (int u = slot; u < U; u += nslots, ++tile_i) {
             const int m = (u % num_mp) * CL + rank, n = u / num_mp;
@@ -259,6 +286,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                             }
                         }
                     }
+                    if constexpr (ENT) {
+                        float cmax = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < lim) cmax = fmaxf(cmax, __uint_as_float(r[j]));
+                        if (cmax > em) {   // new running maximum: rescale what was summed so far
+                            if (es > 0.f) {
+                                const float sc = __expf(em - cmax);
+                                et = (et + (em - cmax) * es) * sc;
+                                es *= sc;
+                            }
+                            em = cmax;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < lim) {
+                                const float z = __uint_as_float(r[j]) - em;
+                                const float e = __expf(z);
+                                es += e;
+                                et = fmaf(z, e, et);
+                            }
+                    }
                 }
             }
             tc_fence_before();
@@ -275,6 +324,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
         }
+        if constexpr (ENT) {
+            // this CTA's rows are fixed (rank's activation tile); publish their statistics
+            const int row = rank * BM + rit;
+            if (row < p.M_rows) p.ent[(size_t)slot * p.M_rows + row] = make_float4(em, es, et, 0.f);
+        }
         if (KT == 1 && !*abort_flag) {
             // last CTA to finish turns the keys into ids and zeroes them again
             __threadfence();
@@ -288,9 +342,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 __threadfence();
                 for (int r = threadIdx.x - 64; r < p.M_rows; r += 128) {
                     const uint64_t key = __ldcg(reinterpret_cast<const unsigned long long*>(p.keys + r));
-                    p.ids[r] = key ? (int32_t)key_id(key) : -1;
+                    if (p.ids) p.ids[r] = key ? (int32_t)key_id(key) : -1;
                     if (p.maxlogit) p.maxlogit[r] = key ? key_val(key) : __int_as_float(0x7fc00000);
                     p.keys[r] = 0;
+                }
+                if constexpr (ENT) {
+                    // entropy per row: merge the slots' statistics (one warp per row,
+                    // fixed order), H = log S - T / S
+                    const int wid = (threadIdx.x - 64) >> 5;
+                    for (int r = wid; r < p.M_rows; r += 4) {
+                        float M = -INFINITY, S = 0.f, T = 0.f;
+                        for (int sl = lane; sl < nslots; sl += 32) {
+                            float4* src = p.ent + (size_t)sl * p.M_rows + r;
+                            const float4 st = __ldcg(src);
+                            *src = make_float4(0.f, 0.f, 0.f, 0.f);   // leave the workspace zeroed
+                            ent_merge(M, S, T, st.x, st.y, st.z);
+                        }
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) {
+                            const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+                            const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
+                            const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
+                            ent_merge(M, S, T, m2, s2, t2);
+                        }
+                        if (lane == 0) {
+                            // gathered rows: a source row outside [0, src_P) has no entropy
+                            const bool bad = p.src_rows && (p.src_rows[r] < 0 || p.src_rows[r] >= p.src_P);
+                            const float h = bad ? __int_as_float(0x7fc00000) : logf(S) - T / S;
+                            p.H[r] = h;
+                            if (p.route) p.route[r] = bad ? -1 : (h > p.tau ? 1 : 0);
+                        }
+                    }
                 }
                 if (threadIdx.x == 64) p.ctrl->gemm_done = 0;
             }
@@ -416,7 +498,8 @@ static int pick_bn(int num_m, int N_w, int sms) {
 }
 
 // Clusters of two that can be resident at once (queried once per device).
-template <int KT>
+// Clusters of two that can be resident at once (queried once per device).
+template <int KT, bool ENT>
 static int pair_slots(int dev) {
     static int cached[64];
     if (dev < 64 && cached[dev]) return cached[dev];
@@ -432,7 +515,7 @@ static int pair_slots(int dev) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, 2>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, 2, ENT>, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = num_sms() / 2;
     }
@@ -440,23 +523,23 @@ static int pair_slots(int dev) {
     return n;
 }
 
-template <int KT>
-static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, int k,
-                               uint64_t* keys, int32_t* ids, float* maxlogit, uint64_t* cand, Control* ctrl,
+template <int KT, bool ENT>
+static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, GemmParams p,
                                cudaStream_t s) {
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1, ENT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(gemm_select_kernel<KT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(gemm_select_kernel<KT, 2, ENT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
     }
     CUtensorMap ta, tb;
     const int num_m = cdiv(M_rows, BM);
+    if (ENT && num_m > 2) return WF_ERR_UNSUPPORTED;
     // several activation tiles: pairs of CTAs share each weight tile (multicast)
     const int CL = num_m > 1 ? 2 : 1;
     // With a single activation tile the box covers only the rows that exist
@@ -468,7 +551,6 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     const int bn = pick_bn(num_m, N_w, num_sms());
     // each CTA of a pair fetches half of the weight tile
     if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn / CL))) return WF_ERR_CUDA;
-    GemmParams p;
     p.M_rows = M_rows;
     p.N_w = N_w;
     p.num_m = num_m;
@@ -476,43 +558,67 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.bn = bn;
     p.idesc = umma_idesc_bf16(BM, bn);
     p.num_k = cdiv(d, BK);
-    p.k = k;
     p.weight_evict_first = p.num_m == 1;
     p.a_bytes = a_rows * BK * 2;
-    p.keys = keys;
-    p.ids = ids;
-    p.maxlogit = maxlogit;
-    p.cand = cand;
-    p.ctrl = ctrl;
     p.timeout_ns = wait_timeout_ns();
     if (CL == 1) {
         const int tiles = p.num_m * p.num_n;
-        const int grid = tiles < num_sms() ? tiles : num_sms();
-        return launch(gemm_select_kernel<KT, 1>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, p);
+        int grid = tiles < num_sms() ? tiles : num_sms();
+        if (ENT && grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
+        return launch(gemm_select_kernel<KT, 1, ENT>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, p);
     }
     const int pairs = cdiv(num_m, 2) * p.num_n;
-    const int slots = pair_slots<KT>(dev);
+    int slots = pair_slots<KT, ENT>(dev);
+    if (ENT && slots > ENT_MAX_SLOTS) slots = ENT_MAX_SLOTS;
     const int grid = 2 * (pairs < slots ? pairs : slots);
-    return launch_cluster(gemm_select_kernel<KT, 2>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta, tb, p);
+    return launch_cluster(gemm_select_kernel<KT, 2, ENT>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta, tb,
+                          p);
+}
+
+static GemmParams params_for(void* ws) {
+    GemmParams p = {};
+    p.ctrl = reinterpret_cast<Control*>(ws);
+    p.keys = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + sizeof(Control));
+    return p;
 }
 
 wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                float* maxlogit, void* ws, cudaStream_t s) {
-    Control* ctrl = reinterpret_cast<Control*>(ws);
-    uint64_t* keys = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + sizeof(Control));
-    return launch_select<1>(hidden, P, W, V, d, 1, keys, ids, maxlogit, nullptr, ctrl, s);
+    GemmParams p = params_for(ws);
+    p.k = 1;
+    p.ids = ids;
+    p.maxlogit = maxlogit;
+    return launch_select<1, false>(hidden, P, W, V, d, p, s);
+}
+
+// The same sweep plus the entropy of softmax(logits) per row (rows <= 2 tiles).
+wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                                float* maxlogit, float* H, int32_t* route, float tau, const int32_t* src_rows,
+                                int src_P, void* ws, size_t ent_off, cudaStream_t s) {
+    GemmParams p = params_for(ws);
+    p.k = 1;
+    p.ids = ids;
+    p.maxlogit = maxlogit;
+    p.ent = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(ws) + ent_off);
+    p.H = H;
+    p.route = route;
+    p.tau = tau;
+    p.src_rows = src_rows;
+    p.src_P = src_P;
+    return launch_select<1, true>(hidden, P, W, V, d, p, s);
 }
 
 wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
                             int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t cand_off,
                             cudaStream_t s) {
-    Control* ctrl = reinterpret_cast<Control*>(ws);
-    uint64_t* cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
-    wf_status st = launch_select<KT_TOPK>(x, B, Wd, Vd, d, k, nullptr, nullptr, nullptr, cand, ctrl, s);
+    GemmParams p = params_for(ws);
+    p.k = k;
+    p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s);
     if (st != WF_OK) return st;
     const int bn = pick_bn(cdiv(B, BM), Vd, num_sms());
-    return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, (const uint64_t*)cand, B, cdiv(B, BM),
-                  cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids, vals, ctrl);
+    return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, (const uint64_t*)p.cand, B, cdiv(B, BM),
+                  cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids, vals, p.ctrl);
 }
 
 }  // namespace wf

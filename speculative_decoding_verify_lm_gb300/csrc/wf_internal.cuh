@@ -30,13 +30,18 @@ static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t keys, cand, part, dall, total;
+    size_t keys, cand, part, dall, ent, gath, total;
 };
 
+// Entropy statistics are kept per CTA slot; the LM-head grid never exceeds this.
+constexpr int ENT_MAX_SLOTS = 160;
+// Rows of one entropy sweep (at most two activation tiles).
+constexpr int ENT_MAX_ROWS = 256;
+
 // A round with at most this many verified rows runs the router on every row,
-// on a second stream while the LM head streams its weights; the acceptance
-// step then just picks the row it accepted.  Larger rounds route only the
-// last accepted row of each sequence, after the acceptance step.
+// beside the LM head while it streams its weights; the acceptance step then
+// just picks the row it accepted.  Larger rounds route only the last accepted
+// row of each sequence, after the acceptance step.
 constexpr int ROUTE_ALL_ROWS_MAX = 128;
 
 // Optional tail of the acceptance step: copy the router output of the
@@ -64,21 +69,32 @@ constexpr int ROUTER_MAX_WIDTH = 65536;
 
 inline int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
 
-inline Layout layout(int P, int B, int m, int Vd, int k) {
+// Workspace regions for a call with at most P verified rows, B sequences,
+// hidden size d, router width m, draft vocabulary Vd and top-k k.
+inline Layout layout(int P, int B, int d, int m, int Vd, int k) {
+    P = P > 0 ? P : 0;
+    B = B > 0 ? B : 0;
+    const int ent_rows = B <= ENT_MAX_ROWS ? B : 0;          // rows of a gathered entropy sweep
+    const int small_P = P <= ROUTE_ALL_ROWS_MAX ? P : 0;     // rows routed all at once
     Layout L;
     size_t off = sizeof(Control);
     L.keys = off;
-    off = align_up(off + sizeof(uint64_t) * (size_t)(P > 0 ? P : 0), 256);
+    off = align_up(off + sizeof(uint64_t) * (size_t)(P > ent_rows ? P : ent_rows), 256);
     L.cand = off;
     if (Vd > 0 && k > 0) {
         size_t tiles = (size_t)cdiv(B, BM) * (size_t)cdiv(Vd, BN_MIN);
         off = align_up(off + tiles * BM * (size_t)k * sizeof(uint64_t), 256);
     }
     L.part = off;
-    const int routed = (P > 0 && P <= ROUTE_ALL_ROWS_MAX && P > B) ? P : (B > 0 ? B : 0);
+    const int routed = small_P > B ? small_P : B;
     off = align_up(off + sizeof(float) * (size_t)routed * (size_t)cdiv(m > 0 ? m : 1, ROUTER_UNITS_PER_CTA), 256);
     L.dall = off;
-    if (P > 0 && P <= ROUTE_ALL_ROWS_MAX) off = align_up(off + sizeof(float) * (size_t)P, 256);
+    off = align_up(off + sizeof(float) * (size_t)(small_P > ent_rows ? small_P : ent_rows), 256);
+    L.ent = off;
+    const int er = small_P > ent_rows ? small_P : ent_rows;
+    off = align_up(off + sizeof(float4) * (size_t)ENT_MAX_SLOTS * (size_t)er, 256);
+    L.gath = off;
+    off = align_up(off + 2 * (size_t)ent_rows * (size_t)(d > 0 ? d : 0), 256);
     L.total = off;
     return L;
 }
@@ -88,12 +104,14 @@ uint64_t wait_timeout_ns();
 
 // ----------------------------------------------------------------- launches
 // Every kernel is launched with programmatic stream serialization: it may be
-// scheduled while its predecessor on the stream is still running.  Each
-// kernel first waits for its predecessor (pdl_wait), then lets its own
-// dependent be scheduled (pdl_trigger).  So when a kernel starts, everything
-// before its predecessor has completed, and before its own wait it may read
-// any input that its predecessor does not write (weights, draft tokens,
-// offsets) - that prefetch overlaps the predecessor.  Without the launch
+// scheduled while its predecessor on the stream is still running.  A kernel
+// normally first waits for its predecessor (pdl_wait), then lets its own
+// dependent be scheduled (pdl_trigger); before its wait it reads only inputs
+// that no kernel of the round writes (weights, draft tokens, offsets), so that
+// prefetch overlaps the predecessor.  The one exception, the router over all
+// rows of a small round, needs nothing from its predecessor (the LM head): it
+// triggers at once, computes beside it, and waits for it just before exiting -
+// so its own completion still implies the LM head's.  Without the launch
 // attribute both instructions are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -170,12 +188,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  "r"(bytes)
                  : "memory");
 }
+// The waiting thread is suspended in hardware until the phase completes or
+// about 20 us pass, so waiting warps do not take issue slots from the other
+// warps (or other kernels' CTAs) on the SM.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
         : "memory");
     return ok != 0;
 }

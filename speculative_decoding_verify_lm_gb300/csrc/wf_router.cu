@@ -63,7 +63,12 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     const float bias1 = unit_live ? b1[j] : 0.f;
     const float wout = unit_live ? w2[j] : 0.f;
 
-    pdl_wait();   // rows[] (a verify call's last_pos) comes from the kernel before this one
+    // rows[] (a verify call's last_pos) comes from the kernel before this one.
+    // Routing every row (rows == null) needs nothing from it: the kernel then
+    // runs beside it and waits for it only before exiting, so that the kernel
+    // after this one may rely on both.
+    const bool beside = rows == nullptr;
+    if (!beside) pdl_wait();
     pdl_trigger();
 
     for (int b0 = 0; b0 < B; b0 += rb_max) {
@@ -141,7 +146,10 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     __syncthreads();
     if (threadIdx.x == 0) s_last = atomicAdd(&ctrl->router_done, 1u) == (unsigned)nblk - 1;
     __syncthreads();
-    if (!s_last) return;
+    if (!s_last) {
+        if (beside) pdl_wait();
+        return;
+    }
     __threadfence();
     // one warp per sequence: lane l sums partials l, l+32, ... (independent
     // loads), then a fixed xor tree - the same order on every run
@@ -166,6 +174,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
         }
     }
     if (threadIdx.x == 0) ctrl->router_done = 0;
+    if (beside) pdl_wait();
 }
 
 wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
@@ -192,6 +201,33 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
     return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA)), dim3(ROUTER_THREADS), smem, s, hidden, rows, B,
                   d, m, P, W1, b1, w2, b2, tau, delta_al, route, part, rb, ctrl);
+}
+
+}  // namespace wf
+
+namespace wf {
+
+// Copy hidden[rows[b]] to out[b] (16-byte chunks) for an entropy sweep over
+// selected rows; a row outside [0, P) is zero-filled and flagged.
+__global__ void __launch_bounds__(128)
+    gather_rows_kernel(const uint16_t* __restrict__ hidden, int P, int d, const int32_t* __restrict__ rows,
+                       uint16_t* __restrict__ out, Control* ctrl) {
+    pdl_wait();   // rows may be the previous kernel's last_pos
+    pdl_trigger();
+    const int b = blockIdx.x;
+    const int r = rows[b];
+    const bool bad = r < 0 || r >= P;
+    if (bad && threadIdx.x == 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+    const int chunks = d >> 3;
+    const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)(bad ? 0 : r) * d);
+    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)b * d);
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = bad ? make_uint4(0, 0, 0, 0) : src[c];
+}
+
+wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t* rows, int B, uint16_t* out,
+                             void* ws, cudaStream_t s) {
+    return launch(gather_rows_kernel, dim3(B), dim3(128), 0, s, hidden, P, d, rows, out,
+                  reinterpret_cast<Control*>(ws));
 }
 
 }  // namespace wf

@@ -49,14 +49,20 @@ class RoundArgs(ctypes.Structure):
         ("x", _c_void_p), ("Wd", _c_void_p), ("d2t", _c_void_p), ("Vd", _i32), ("k", _i32),
         ("ids", _c_void_p), ("maxlogit", _c_void_p), ("n_accept", _c_void_p), ("bonus", _c_void_p),
         ("last_pos", _c_void_p), ("path", _c_void_p), ("delta_al", _c_void_p), ("route", _c_void_p),
-        ("draft_ids", _c_void_p), ("tids", _c_void_p), ("vals", _c_void_p),
+        ("draft_ids", _c_void_p), ("tids", _c_void_p), ("vals", _c_void_p), ("router_kind", _i32),
     ]
+
+
+WF_ROUTER_NEURAL = 0
+WF_ROUTER_ENTROPY = 1
 
 
 _SIGS = {
     "wf_status_string": (ctypes.c_char_p, [_i32]),
     "wf_version": (_i32, []),
-    "wf_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "wf_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "wf_lmhead_entropy": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _i32, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
+                                 _c_void_p, _sz, _c_void_p]),
     "wf_workspace_init": (_i32, [_c_void_p, _sz, _c_void_p]),
     "wf_read_device_error": (_i32, [_c_void_p, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32, _c_void_p]),
     "wf_set_wait_timeout_ns": (None, [_u64]),
@@ -146,8 +152,9 @@ def _raise(st: int, where: str):
 class Workspace:
     """Caller-owned device workspace sized by wf_workspace_bytes and zeroed once."""
 
-    def __init__(self, P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0, device=None, stream=None):
-        self.nbytes = int(lib().wf_workspace_bytes(P, B, m, Vd, k))
+    def __init__(self, P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0, device=None, stream=None,
+                 d: int = 0):
+        self.nbytes = int(lib().wf_workspace_bytes(P, B, d, m, Vd, k))
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
         _raise(lib().wf_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream)), "wf_workspace_init")
 
@@ -162,8 +169,23 @@ class Workspace:
         return code.value, info.value
 
 
-def wf_workspace_bytes(P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0) -> int:
-    return int(lib().wf_workspace_bytes(P, B, m, Vd, k))
+def wf_workspace_bytes(P: int, B: int = 1, m: int = 1, Vd: int = 0, k: int = 0, d: int = 0) -> int:
+    return int(lib().wf_workspace_bytes(P, B, d, m, Vd, k))
+
+
+def wf_lmhead_entropy(hidden, W, tau: float, ws: Workspace, rows=None, B=None, H=None, route=None, stream=None):
+    """Entropy of the target's next-token distribution at the given rows (all rows if None) and the
+    WhiFlash-Entropy route (H > tau)."""
+    P, d = hidden.shape
+    V = W.shape[0]
+    B = (rows.numel() if rows is not None else P) if B is None else B
+    H = torch.empty(B, dtype=torch.float32, device=hidden.device) if H is None else H
+    route = torch.empty(B, dtype=torch.int32, device=hidden.device) if route is None else route
+    st = lib().wf_lmhead_entropy(_check(hidden, "hidden", _BF16), P, d, _check(rows, "rows", _I32, True), B,
+                                 _check(W, "W", _BF16), V, float(tau), _check(H, "H", _F32),
+                                 _check(route, "route", _I32, True), ws.ptr, ws.nbytes, _stream(stream))
+    _raise(st, "wf_lmhead_entropy")
+    return H, route
 
 
 def wf_set_wait_timeout_ns(ns: int) -> None:
@@ -298,7 +320,8 @@ class Round:
     (W, W1, b1, w2, Wd, d2t) stay where the caller keeps them."""
 
     def __init__(self, hidden, W, pos_off, node_off, tok, W1, b1, w2, b2: float, tau: float, kind=None, parent=None,
-                 path_stride: int = 0, x=None, Wd=None, d2t=None, k: int = 0, with_maxlogit: bool = False):
+                 path_stride: int = 0, x=None, Wd=None, d2t=None, k: int = 0, with_maxlogit: bool = False,
+                 router_kind: int = WF_ROUTER_NEURAL):
         dev = hidden.device
         P, d = hidden.shape
         B = pos_off.numel() - 1
@@ -356,12 +379,13 @@ class Round:
         a.d2t = _check(d2t, "d2t", _I32, True)
         a.Vd = Wd.shape[0] if Wd is not None else 0
         a.k = k if Wd is not None else 0
+        a.router_kind = int(router_kind)
         for name in ("ids", "maxlogit", "n_accept", "bonus", "last_pos", "path", "delta_al", "route", "draft_ids",
                      "tids", "vals"):
             t = self.out[name]
             setattr(a, name, t.data_ptr() if t is not None else None)
         self.args = a
-        self.ws = Workspace(P, B, m, a.Vd, a.k, device=dev)
+        self.ws = Workspace(P, B, m, a.Vd, a.k, device=dev, d=d)
 
     def __call__(self, stream=None):
         _raise(lib().wf_round(ctypes.byref(self.args), self.ws.ptr, self.ws.nbytes, _stream(stream)), "wf_round")

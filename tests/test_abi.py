@@ -41,8 +41,8 @@ def test_status_strings_and_sizes():
     assert L.wf_version() >= 100
     for s in range(7):
         assert L.wf_status_string(s).decode().startswith(wf.STATUS[s])
-    small = L.wf_workspace_bytes(17, 1, 1024, 0, 0)
-    big = L.wf_workspace_bytes(15616, 256, 1024, 32000, 10)
+    small = L.wf_workspace_bytes(17, 1, 2560, 1024, 0, 0)
+    big = L.wf_workspace_bytes(15616, 256, 2560, 1024, 32000, 10)
     assert 0 < small < big and big % 256 == 0
     # keys for every row + draft candidates + router partials
     assert big >= 256 + 8 * 15616 + 125 * 2 * 128 * 10 * 8 + 4 * 256 * 128

@@ -269,6 +269,62 @@ def test_round_edge_shapes():
         _compare_round(wl, out)
 
 
+# ------------------------------------------------------------------ entropy router
+@pytest.mark.parametrize("P,d,V,rows", [(17, 256, 8192, None), (5, 64, 300, None), (61, 128, 5000, [60, 0, 7]),
+                                        (300, 64, 1000, list(range(299, 43, -1))), (40, 2560, 151936, [3, 39])])
+def test_entropy(P, d, V, rows):
+    W = synth.normal_bf16(V + d, 0, V, d, d ** -0.5 * 2.0)
+    h = synth.normal_bf16(P + d, 1, P, d, 1.0)
+    r = np.arange(P, dtype=np.int32) if rows is None else np.array(rows, np.int32)
+    H_ref, _ = o().entropy(h, r, W)
+    tau = float(np.median(H_ref)) + 0.0037
+    ws = wf.Workspace(P, len(r), d=d)
+    for _ in range(2):
+        H, route = wf.wf_lmhead_entropy(dev(h), dev(W), tau, ws, rows=None if rows is None else dev(r))
+        torch.cuda.synchronize()
+        assert np.max(np.abs(host(H) - H_ref)) <= 1e-3
+        clear = np.abs(H_ref - tau) >= synth.GAP_MIN
+        assert np.array_equal(host(route)[clear], (H_ref > tau).astype(np.int32)[clear])
+    assert ws.device_error() == (0, 0)
+    if rows is None:   # gathered rows stay in their staging area; everything else is left zeroed
+        assert not ws.buf.any().item()
+
+
+def test_entropy_bad_row():
+    W = synth.normal_bf16(3, 0, 500, 64, 0.2)
+    h = synth.normal_bf16(4, 1, 10, 64, 1.0)
+    ws = wf.Workspace(10, 3, d=64)
+    H, route = wf.wf_lmhead_entropy(dev(h), dev(W), 1.0, ws, rows=dev(np.array([2, 10, -1], np.int32)))
+    assert np.isnan(host(H)[1:]).all() and list(host(route)[1:]) == [-1, -1] and not np.isnan(host(H)[0])
+    assert ws.device_error()[0] == 5
+
+
+@pytest.mark.parametrize("kinds", [[0, 1], [1, 1, 1, 0]])
+def test_round_entropy_router(kinds):
+    """WhiFlash-Entropy routing inside a round: fused into the LM-head sweep for
+    <= 128 rows, a second sweep over the accepted rows otherwise."""
+    wl = synth.small_workload(77 + len(kinds), d=128, V=3000, kinds=kinds, argmax_fn=oracle.argmax_fn, m=8,
+                              n_nodes=60, depth=8, branch=10)
+    rr = wl.pos_off[1:]
+    ref = o().round_(wl.hidden, wl.W, wl.pos_off, wl.node_off, wl.kind, wl.tok, wl.parent, wl.W1, wl.b1, wl.w2,
+                     wl.b2, wl.tau, wl.max_depth)
+    H_ref, _ = o().entropy(wl.hidden, ref["last_pos"], wl.W)
+    tau = float(np.median(H_ref)) + 0.0041
+    r = wf.Round(dev(wl.hidden), dev(wl.W), dev(wl.pos_off), dev(wl.node_off), dev(wl.tok), dev(wl.W1),
+                 dev(wl.b1), dev(wl.w2), wl.b2, tau, kind=dev(wl.kind), parent=dev(wl.parent),
+                 path_stride=wl.max_depth, router_kind=wf.WF_ROUTER_ENTROPY)
+    assert (wl.P <= 128) == (len(kinds) == 2) and rr[-1] == wl.P
+    for _ in range(2):
+        out = {k: host(v) for k, v in r().items()}
+        torch.cuda.synchronize()
+        for key in ("ids", "n_accept", "bonus", "last_pos", "path"):
+            assert np.array_equal(out[key], ref[key]), key
+        assert np.max(np.abs(out["delta_al"] - H_ref)) <= 1e-3
+        clear = np.abs(H_ref - tau) >= synth.GAP_MIN
+        assert np.array_equal(out["route"][clear], (H_ref > tau).astype(np.int32)[clear])
+    assert r.ws.device_error() == (0, 0)
+
+
 # ------------------------------------------------------------------ failure path
 def test_bounded_wait_gives_up_and_context_survives():
     ws = wf.Workspace(8)
