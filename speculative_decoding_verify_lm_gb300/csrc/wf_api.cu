@@ -133,7 +133,7 @@ wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int
                            float* maxlogit, void* ws, size_t ws_bytes, wf_stream_t stream) {
     if (!hidden || !W || !ids || bad_gemm_shape(P, d, V)) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
-    WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, d, 0, 0, 0).total));
+    WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, d, 0, 0, 0).cand));   // control block and keys
     WF_TRY(check_device());
     return launch_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, ws, stream);
 }
@@ -153,7 +153,7 @@ wf_status wf_lmhead_entropy(const uint16_t* hidden, int P, int d, const int32_t*
     if (!rows && B > P) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
     const Layout L = layout(0, B, d, 0, 0, 0);
-    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_ws(ws, ws_bytes, rows ? L.total : L.gath));   // the gather area only when rows are given
     WF_TRY(check_device());
     const uint16_t* act = hidden;
     if (rows) {
@@ -194,7 +194,7 @@ wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int 
     if (!hidden || !rows || !W1 || !b1 || !w2 || (!delta_al && !route)) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W1)) return WF_ERR_INVALID_ARG;
     const Layout L = layout(0, B, d, m, 0, 0);
-    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_ws(ws, ws_bytes, L.dall));   // up to the end of the router partials
     WF_TRY(check_device());
     return launch_router(hidden, rows, B, d, m, -1, W1, b1, w2, b2, tau, delta_al, route, ws, L.part, stream);
 }
@@ -206,7 +206,7 @@ wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2
     if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals)) return WF_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
     const Layout L = layout(0, B, d, 0, Vd, k);
-    WF_TRY(check_ws(ws, ws_bytes, L.total));
+    WF_TRY(check_ws(ws, ws_bytes, L.part));   // up to the end of the top-k candidates
     WF_TRY(check_device());
     return launch_draft_topk(x, Wd, d2t, B, d, Vd, k, draft_ids, tids, vals, ws, L.cand, stream);
 }
