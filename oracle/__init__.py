@@ -119,6 +119,32 @@ class Oracle:
         assert rc == 0, rc
         return delta, route
 
+    def build_tree(self, tid, lp, N):
+        """tid int32 [B, D, k, k], lp f32 [B, D, k, k] -> (parent, token, score f32, depth) each [B, N], rc."""
+        tid = np.ascontiguousarray(tid, np.int32)
+        lp = np.ascontiguousarray(lp, np.float32)
+        B, D, k, _ = tid.shape
+        parent = np.empty((B, N), np.int32)
+        token = np.empty((B, N), np.int32)
+        score = np.empty((B, N), np.float32)
+        depth = np.empty((B, N), np.int32)
+        rc = self.lib.oracle_build_tree(_p(tid), _p(lp), ctypes.c_int(B), ctypes.c_int(D), ctypes.c_int(k),
+                                        ctypes.c_int(N), _p(parent), _p(token), _p(score), _p(depth))
+        return parent, token, score, depth, rc
+
+    def accepted_rows(self, n_accept, path, pos_off):
+        """-> (acc_rows int32 [B, path_stride + 1], acc_off int32 [B + 1])."""
+        n_accept = np.ascontiguousarray(n_accept, np.int32)
+        path = np.ascontiguousarray(path, np.int32)
+        pos_off = np.ascontiguousarray(pos_off, np.int32)
+        B, ps = path.shape
+        acc_rows = np.empty((B, ps + 1), np.int32)
+        acc_off = np.empty(B + 1, np.int32)
+        rc = self.lib.oracle_accepted_rows(_p(n_accept), _p(path), ctypes.c_int(ps), _p(pos_off), ctypes.c_int(B),
+                                           _p(acc_rows), _p(acc_off))
+        assert rc == 0, rc
+        return acc_rows, acc_off
+
     def entropy(self, hidden, rows, W, tau: float = 0.0):
         """Entropy of softmax(<h, W_v>) at each row -> (H f64 [B], route int32 [B])."""
         hidden = np.ascontiguousarray(hidden, np.uint16)

@@ -212,6 +212,126 @@ int oracle_entropy(const uint16_t* hidden, const int32_t* rows, int B, const uin
     return 0;
 }
 
+/*
+ * Rows kept after verification (paper Sec. 3.2: decoding continues from the
+ * last accepted token, so the target states of the committed positions are
+ * kept and every other drafted row is dropped).  For sequence b with
+ * n = n_accept[b] accepted drafts along path[b*path_stride ..]:
+ *   acc_rows[b*(path_stride+1) + 0]     = pos_off[b]                (the root row)
+ *   acc_rows[b*(path_stride+1) + j]     = pos_off[b] + 1 + path[j-1], j = 1..n
+ *   acc_rows[b*(path_stride+1) + j]     = -1                        for j > n
+ *   acc_off[0] = 0, acc_off[b+1] = acc_off[b] + n + 1   (packed order of the kept rows)
+ */
+int oracle_accepted_rows(const int32_t* n_accept, const int32_t* path, int path_stride, const int32_t* pos_off,
+                         int B, int32_t* acc_rows, int32_t* acc_off) {
+    if (!n_accept || !pos_off || !acc_rows || !acc_off || B < 0 || path_stride < 0) return 1;
+    acc_off[0] = 0;
+    for (int b = 0; b < B; ++b) {
+        const int n = n_accept[b];
+        int32_t* out = acc_rows + (int64_t)b * (path_stride + 1);
+        for (int j = 0; j <= path_stride; ++j) out[j] = -1;
+        out[0] = pos_off[b];
+        for (int j = 1; j <= n && j <= path_stride; ++j) out[j] = pos_off[b] + 1 + path[(int64_t)b * path_stride + j - 1];
+        acc_off[b + 1] = acc_off[b] + n + 1;
+    }
+    return 0;
+}
+
+/*
+ * EAGLE-3 draft-tree construction (the context-aware dynamic tree; paper
+ * App. A / Table 7: depth 8, top-k 10, 60 draft tokens; EAGLE3 card
+ * "Factors").  Step t = 0 .. D-1 expands the frontier: frontier slot j (only
+ * slot 0, the root, at t = 0) proposes k children with target ids
+ * tid[t][j][c] and draft log-probabilities lp[t][j][c] (<= 0).  A child's
+ * score is its parent's score (0 for the root) plus its lp.  The k best
+ * children of step t (score desc, creation order asc) are the frontier of
+ * step t+1, slot 0 first.  Every child of every step joins the pool; the N
+ * best of the pool (same order) form the tree, listed depth by depth and,
+ * within a depth, in that order; parent[] indexes that list (-1 = root).
+ * Scores are summed in fp32 (the precision the kernel decides in), in this
+ * order, so both sides rank the same numbers.
+ * Creation order: step 0 child c -> c; step t >= 1 -> k + (t-1)k^2 + j*k + c.
+ * Returns 2 (and writes -1s) for a sequence with an lp > 0 or not finite.
+ */
+typedef struct { float s; int32_t idx; } ranked;
+
+static int by_score_then_index(const void* a, const void* b) {
+    const ranked* x = (const ranked*)a;
+    const ranked* y = (const ranked*)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->idx > y->idx) - (x->idx < y->idx);
+}
+
+int oracle_build_tree(const int32_t* tid, const float* lp, int B, int D, int k, int N, int32_t* parent,
+                      int32_t* token, float* score, int32_t* depth) {
+    if (!tid || !lp || !parent || !token || B < 0 || D < 1 || k < 1 || N < 1) return 1;
+    const int pool_n = k + (D - 1) * k * k;
+    if (N > pool_n) return 1;
+    int rc = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t* T = tid + (int64_t)b * D * k * k;
+        const float* L = lp + (int64_t)b * D * k * k;
+        float* ps = (float*)malloc(sizeof(float) * pool_n);       /* pool: score */
+        int32_t* pp = (int32_t*)malloc(sizeof(int32_t) * pool_n); /* parent pool index, -1 root */
+        int32_t* pt = (int32_t*)malloc(sizeof(int32_t) * pool_n); /* token */
+        int32_t* pd = (int32_t*)malloc(sizeof(int32_t) * pool_n); /* depth */
+        ranked* r = (ranked*)malloc(sizeof(ranked) * pool_n);
+        int32_t frontier[64];
+        int bad = 0, made = 0;
+        for (int t = 0; t < D && !bad; ++t) {
+            const int slots = t == 0 ? 1 : k;
+            const int first = made;
+            for (int j = 0; j < slots; ++j)
+                for (int c = 0; c < k; ++c) {
+                    const float l = L[((int64_t)t * k + j) * k + c];
+                    if (!(l <= 0.0f)) bad = 1;
+                    const int par = t == 0 ? -1 : frontier[j];
+                    ps[made] = (par < 0 ? 0.0f : ps[par]) + l;
+                    pp[made] = par;
+                    pt[made] = T[((int64_t)t * k + j) * k + c];
+                    pd[made] = t + 1;
+                    made++;
+                }
+            /* next frontier: the k best children of this step */
+            const int n_step = made - first;
+            for (int i = 0; i < n_step; ++i) { r[i].s = ps[first + i]; r[i].idx = first + i; }
+            qsort(r, (size_t)n_step, sizeof(ranked), by_score_then_index);
+            for (int j = 0; j < k; ++j) frontier[j] = r[j].idx;
+        }
+        int32_t* P_ = parent + (int64_t)b * N;
+        int32_t* T_ = token + (int64_t)b * N;
+        if (bad) {
+            rc = 2;
+            for (int i = 0; i < N; ++i) {
+                P_[i] = T_[i] = -1;
+                if (score) score[(int64_t)b * N + i] = 0.0f;
+                if (depth) depth[(int64_t)b * N + i] = -1;
+            }
+        } else {
+            for (int i = 0; i < pool_n; ++i) { r[i].s = ps[i]; r[i].idx = i; }
+            qsort(r, (size_t)pool_n, sizeof(ranked), by_score_then_index);
+            /* the N best, listed depth by depth (stable within a depth) */
+            int32_t* new_of = (int32_t*)malloc(sizeof(int32_t) * pool_n);
+            for (int i = 0; i < pool_n; ++i) new_of[i] = -1;
+            int out = 0;
+            for (int dd = 1; dd <= D; ++dd)
+                for (int i = 0; i < N; ++i)
+                    if (pd[r[i].idx] == dd) new_of[r[i].idx] = out++;
+            for (int i = 0; i < N; ++i) {
+                const int q = r[i].idx, o = new_of[q];
+                P_[o] = pp[q] < 0 ? -1 : new_of[pp[q]];
+                T_[o] = pt[q];
+                if (score) score[(int64_t)b * N + o] = ps[q];
+                if (depth) depth[(int64_t)b * N + o] = pd[q];
+            }
+            free(new_of);
+        }
+        free(ps); free(pp); free(pt); free(pd); free(r);
+    }
+    return rc;
+}
+
 /* GELU in its exact form: x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt 2)) (paper App. A). */
 double oracle_gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
 

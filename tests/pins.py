@@ -50,7 +50,7 @@ def read_cases(name):
                     exp[k] = [int(t) for t in v.split(",") if t] if k == "path" else int(v)
                 cur["expect"] = exp
             else:
-                cur[key] = [int(t) for t in val.split()]
+                cur[key] = [int(t) if t.lstrip("-").isdigit() else float(t) for t in val.split()]
     return cases
 
 
@@ -382,7 +382,84 @@ def check_entropy_route_strict(o):
     assert list(r) == [1]
 
 
+# ---------------------------------------------------------------- kept rows
+def check_accepted_rows(o):
+    """Hand-worked: the golden trees' accepted paths map to their rows, in order,
+    root first; offsets count n_accept + 1 per sequence."""
+    cases = read_cases("trees.txt")
+    seqs = [(c["g"], c["tok"], c["parent"]) for c in cases]
+    g, tok, par, pos_off, node_off = _pack(seqs)
+    n, _, last, path, _ = o.verify_tree(g, tok, par, node_off, pos_off, path_stride=4)
+    acc_rows, acc_off = o.accepted_rows(n, path, pos_off)
+    for b, c in enumerate(cases):
+        e = c["expect"]
+        want = [int(pos_off[b])] + [int(pos_off[b]) + 1 + x for x in e["path"]]
+        got = [int(x) for x in acc_rows[b] if x >= 0]
+        assert got == want, (c["name"], got, want)
+        assert acc_rows[b][-1 if len(want) <= 4 else 0] == (-1 if len(want) <= 4 else want[0])
+        assert acc_off[b + 1] - acc_off[b] == e["n"] + 1
+        assert got[-1] == last[b]        # the last kept row is the last accepted row
+    assert acc_off[0] == 0
+
+
+# ---------------------------------------------------------------- draft-tree construction
+def _tree_by_beam(tid, lp, N):
+    """The same construction written as an explicit beam search over Python
+    lists (scores in numpy float32, added in the same order)."""
+    D, k = tid.shape[0], tid.shape[1]
+    pool = []                                   # (score, creation index, parent, token, depth)
+    frontier = [None]                           # the root
+    for t in range(D):
+        created = []
+        for j, par in enumerate(frontier if t else [None]):
+            for c in range(k):
+                base = np.float32(0.0) if par is None else pool[par][0]
+                created.append((np.float32(base + np.float32(lp[t, j, c])), len(pool) + len(created), par,
+                                int(tid[t, j, c]), t + 1))
+        pool += created
+        frontier = [e[1] for e in sorted(created, key=lambda e: (-float(e[0]), e[1]))[:k]]
+    best = sorted(pool, key=lambda e: (-float(e[0]), e[1]))[:N]
+    order = sorted(best, key=lambda e: e[4])    # stable: keeps score order within a depth
+    new_of = {e[1]: i for i, e in enumerate(order)}
+    return ([-1 if e[2] is None else new_of[e[2]] for e in order], [e[3] for e in order],
+            [float(e[0]) for e in order], [e[4] for e in order])
+
+
+def check_build_tree(o):
+    c = read_cases("tree_build.txt")[0]
+    D, k, N = c["D"][0], c["k"][0], c["N"][0]
+    tid = np.array(c["tid"], np.int32).reshape(1, D, k, k)
+    lp = np.array(c["lp"], np.float32).reshape(1, D, k, k)
+    parent, token, score, depth, rc = o.build_tree(tid, lp, N)
+    assert rc == 0
+    assert list(parent[0]) == c["expect_parent"] and list(token[0]) == c["expect_token"]
+    assert list(depth[0]) == c["expect_depth"]
+    rng = np.random.default_rng(10)
+    for D, k, N in [(8, 10, 60), (3, 4, 20), (5, 2, 9), (1, 6, 6)]:
+        B = 3
+        tid = rng.integers(0, 1000, (B, D, k, k)).astype(np.int32)
+        lp = np.log(rng.dirichlet(np.ones(k) * 0.7, (B, D, k))).astype(np.float32)
+        parent, token, score, depth, rc = o.build_tree(tid, lp, N)
+        assert rc == 0
+        for b in range(B):
+            wp, wt, ws, wd = _tree_by_beam(tid[b], lp[b], N)
+            assert list(parent[b]) == wp and list(token[b]) == wt and list(depth[b]) == wd
+            assert np.array_equal(score[b], np.array(ws, np.float32))
+            assert all(parent[b][i] < i for i in range(N))          # listed depth by depth
+    # equal scores everywhere: the earlier-created node wins every tie
+    tid = np.arange(3 * 2 * 2, dtype=np.int32).reshape(1, 3, 2, 2)
+    lp = np.full((1, 3, 2, 2), -0.5, np.float32)
+    parent, token, _, depth, rc = o.build_tree(tid, lp, 5)
+    wp, wt, _, wd = _tree_by_beam(tid[0], lp[0], 5)
+    assert rc == 0 and list(parent[0]) == wp and list(token[0]) == wt and list(depth[0]) == wd
+    assert list(token[0]) == [0, 1, 4, 5, 6]
+    bad = np.zeros((1, 2, 2, 2), np.float32)
+    bad[0, 1, 0, 1] = 0.5                                           # a log-probability above 0
+    assert o.build_tree(np.zeros((1, 2, 2, 2), np.int32), bad, 3)[4] == 2
+
+
 ALL_CHECKS = [check_argmax_bruteforce, check_argmax_ties, check_argmax_closed_form, check_chain_golden,
               check_tree_golden, check_tree_bruteforce, check_chain_is_linear_tree, check_tree_bad_parent,
               check_gelu_values, check_router_closed_forms, check_route_strict, check_topk_bruteforce,
-              check_topk_ties, check_entropy, check_entropy_route_strict]
+              check_topk_ties, check_entropy, check_entropy_route_strict, check_accepted_rows,
+              check_build_tree]

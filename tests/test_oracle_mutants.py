@@ -49,6 +49,16 @@ MUTANTS = [
      [pins.check_entropy]),
     ("entropy route on >=", "route[b] = ent > tau ? 1 : 0;", "route[b] = ent >= tau ? 1 : 0;",
      [pins.check_entropy_route_strict]),
+    ("kept rows use the node index as the row", "out[j] = pos_off[b] + 1 + path[(int64_t)b * path_stride + j - 1];",
+     "out[j] = pos_off[b] + path[(int64_t)b * path_stride + j - 1];", [pins.check_accepted_rows]),
+    ("kept-row offsets forget the root", "acc_off[b + 1] = acc_off[b] + n + 1;", "acc_off[b + 1] = acc_off[b] + n;",
+     [pins.check_accepted_rows]),
+    ("tree frontier ranked by log-probability alone", "ps[made] = (par < 0 ? 0.0f : ps[par]) + l;",
+     "ps[made] = l;", [pins.check_build_tree]),
+    ("tree listed in score order, not depth by depth", "if (pd[r[i].idx] == dd) new_of[r[i].idx] = out++;",
+     "if (dd == 1) new_of[r[i].idx] = out++;", [pins.check_build_tree]),
+    ("tree ties keep the later node", "return (x->idx > y->idx) - (x->idx < y->idx);\n}\n\nint oracle_build_tree",
+     "return (x->idx < y->idx) - (x->idx > y->idx);\n}\n\nint oracle_build_tree", [pins.check_build_tree]),
     ("top-k maps through the wrong id", "tids[(int64_t)b * k + j] = d2t[s[j].id];",
      "tids[(int64_t)b * k + j] = s[j].id;", [pins.check_topk_bruteforce]),
 ]

@@ -325,6 +325,22 @@ def test_round_entropy_router(kinds):
     assert r.ws.device_error() == (0, 0)
 
 
+# ------------------------------------------------------------------ kept rows
+@pytest.mark.parametrize("seed,B,max_nodes", [(11, 3, 60), (12, 1500, 12), (13, 7, 0)])
+def test_accepted_rows(seed, B, max_nodes):
+    g, tok, par, pos_off, node_off, kinds = _random_trees(seed, B, max_nodes)
+    ps = max(max_nodes, 1)
+    n, _, _, path, _ = o().verify_tree(g, tok, par, node_off, pos_off, ps)
+    acc_rows, acc_off = o().accepted_rows(n, path, pos_off)
+    d = 64
+    h = synth.normal_bf16(seed, 1, int(pos_off[-1]), d, 1.0)
+    gr, go, gh = wf.wf_accepted_rows(dev(n), dev(path), dev(pos_off), hidden=dev(h))
+    torch.cuda.synchronize()
+    assert np.array_equal(host(gr), acc_rows) and np.array_equal(host(go), acc_off)
+    kept = np.concatenate([acc_rows[b][:n[b] + 1] for b in range(B)])
+    assert np.array_equal(host(gh).view(np.uint16), h[kept])
+
+
 # ------------------------------------------------------------------ failure path
 def test_bounded_wait_gives_up_and_context_survives():
     ws = wf.Workspace(8)
