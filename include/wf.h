@@ -213,6 +213,47 @@ WF_API wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int3
                          void* ws, size_t ws_bytes, wf_stream_t stream);
 
 /*
+ * Rows kept after a round (paper Sec. 3.2: decoding continues from the last
+ * accepted token, so the committed positions - the root and the accepted
+ * path - keep their target states and every other drafted row is dropped):
+ *   acc_rows[b*(path_stride+1) + 0] = pos_off[b]                      (root)
+ *   acc_rows[b*(path_stride+1) + j] = pos_off[b] + 1 + path[b*path_stride + j-1], j = 1..n_accept[b]
+ *   acc_rows[...]                   = -1 after that
+ *   acc_off[0] = 0, acc_off[b+1] = acc_off[b] + n_accept[b] + 1      (packed order)
+ * and, if hidden_out != NULL, hidden_out[acc_off[b] + j] = hidden[acc_rows[b][j]]
+ * (the hidden states the next drafting step conditions on, packed).
+ * n_accept, path as returned by wf_verify_* / wf_round with the same
+ * path_stride (n_accept[b] <= path_stride); pos_off [B+1]; all device int32.
+ * acc_rows [B, path_stride+1], acc_off [B+1] device int32 out; hidden [*, d],
+ * hidden_out [sum(n_accept+1), d] device bf16 bits (both NULL to skip).
+ */
+WF_API wf_status wf_accepted_rows(const int32_t* n_accept, const int32_t* path, int path_stride,
+                                  const int32_t* pos_off, int B, int32_t* acc_rows, int32_t* acc_off,
+                                  const uint16_t* hidden, int d, uint16_t* hidden_out, wf_stream_t stream);
+
+/*
+ * EAGLE-3 draft-tree construction (the context-aware dynamic tree the
+ * autoregressive drafter proposes; paper App. A / Table 7: depth 8, top-k 10,
+ * 60 draft tokens).  Step s = 0 .. D-1 expands the frontier: frontier slot j
+ * (only slot 0, the root, at s = 0) proposes k children, target ids
+ * tid[b][s][j][c] and draft log-probabilities lp[b][s][j][c] <= 0 (e.g. the
+ * top-k of wf_draft_topk, shifted by its log-sum-exp).  A child's score is
+ * its parent's (0 at the root) plus its lp, summed in fp32.  The k best
+ * children of a step (score desc, creation order asc) form the next
+ * frontier, best first; the N best of all children created form the tree,
+ * listed depth by depth (rank order within a depth), so parent[i] < i.
+ *
+ * tid device [B, D, k, k] int32, lp device [B, D, k, k] fp32 (entries of
+ * unused slots at s = 0 are ignored); 1 <= k <= 16, 1 <= D <= 16,
+ * 1 <= N <= k + (D-1) k^2.  Out (device, [B, N]): parent int32 (-1 = root),
+ * token int32, score fp32 and depth int32 (score / depth may be NULL).  An lp
+ * above 0 or not finite sets WF_ERR_BAD_DATA and writes -1 for that sequence.
+ */
+WF_API wf_status wf_build_tree(const int32_t* tid, const float* lp, int B, int D, int k, int N, int32_t* parent,
+                               int32_t* token, float* score, int32_t* depth, void* ws, size_t ws_bytes,
+                               wf_stream_t stream);
+
+/*
  * Neural router and hardware-aware routing decision (paper Sec. 3.3.2; App. A
  * "Neural Router Architecture": h -> Linear(d, m) -> GELU -> dropout ->
  * Linear(m, 1), m = d/8 in the paper; route to the autoregressive drafter iff

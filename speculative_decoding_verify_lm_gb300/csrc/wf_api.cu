@@ -24,6 +24,11 @@ wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s);
 wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, float* H, int32_t* route, float tau, const int32_t* src_rows,
                                 int src_P, void* ws, size_t ent_off, cudaStream_t s);
+wf_status launch_build_tree(const int32_t* tid, const float* lp, int B, int D, int k, int N, int32_t* parent,
+                            int32_t* token, float* score, int32_t* depth, void* ws, cudaStream_t s);
+wf_status launch_accepted_rows(const int32_t* n_accept, const int32_t* path, int path_stride, const int32_t* pos_off,
+                               int B, int32_t* acc_rows, int32_t* acc_off, const uint16_t* hidden, int d,
+                               uint16_t* hidden_out, cudaStream_t s);
 wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t* rows, int B, uint16_t* out,
                              void* ws, cudaStream_t s);
 wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
@@ -162,6 +167,28 @@ wf_status wf_lmhead_entropy(const uint16_t* hidden, int P, int d, const int32_t*
         act = gath;
     }
     return launch_lmhead_entropy(act, W, B, d, V, nullptr, nullptr, H, route, tau, rows, P, ws, L.ent, stream);
+}
+
+wf_status wf_build_tree(const int32_t* tid, const float* lp, int B, int D, int k, int N, int32_t* parent,
+                        int32_t* token, float* score, int32_t* depth, void* ws, size_t ws_bytes,
+                        wf_stream_t stream) {
+    if (!tid || !lp || !parent || !token || B < 0 || k < 1 || k > 16 || D < 1 || D > 16) return WF_ERR_INVALID_ARG;
+    if (N < 1 || N > k + (D - 1) * k * k) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
+    WF_TRY(check_device());
+    return launch_build_tree(tid, lp, B, D, k, N, parent, token, score, depth, ws, stream);
+}
+
+wf_status wf_accepted_rows(const int32_t* n_accept, const int32_t* path, int path_stride, const int32_t* pos_off,
+                           int B, int32_t* acc_rows, int32_t* acc_off, const uint16_t* hidden, int d,
+                           uint16_t* hidden_out, wf_stream_t stream) {
+    if (B < 0 || path_stride < 0 || !n_accept || !pos_off || !acc_rows || !acc_off) return WF_ERR_INVALID_ARG;
+    if (path_stride > 0 && !path) return WF_ERR_INVALID_ARG;
+    if ((hidden == nullptr) != (hidden_out == nullptr)) return WF_ERR_INVALID_ARG;
+    if (hidden && (d < 8 || d % 8 != 0 || !aligned16(hidden) || !aligned16(hidden_out))) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_device());
+    return launch_accepted_rows(n_accept, path, path_stride, pos_off, B, acc_rows, acc_off, hidden, d, hidden_out,
+                                stream);
 }
 
 wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t* pos_off, const int32_t* node_off,

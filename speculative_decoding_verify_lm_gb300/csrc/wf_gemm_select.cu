@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tmem_ld_32x32b_x32(tbase + c0, r);
                     tmem_ld_wait();
                     const int col0 = n * p.bn + c0;
-                    // columns >= lim are past the weight matrix or past this tile
-                    const int lim = min(p.N_w - col0, p.bn - c0);
+                    // columns >= lim are past the weight matrix or past this tile; rows
+                    // past the activations (stale shared-memory rows) take no part
+                    const int lim = row < p.M_rows ? min(p.N_w - col0, p.bn - c0) : 0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float v = __uint_as_float(r[j]);
@@ -404,19 +405,33 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const uint64_t* __restr
 #pragma unroll
     for (int j = 0; j < KT_TOPK; ++j) loc[j] = 0;
     const int total = num_n * k;
-    for (int idx = lane; idx < total; idx += 32) {
-        const int n = idx / k, j = idx - n * k;
-        uint64_t* src = const_cast<uint64_t*>(cand) + (((size_t)n * num_m + m) * BM + rit) * k + j;
-        const uint64_t key = *src;
-        *src = 0;  // leave the workspace zeroed
-        if (key > loc[KT_TOPK - 1]) {
+    constexpr int BATCH = 8;   // candidates in flight per lane
+    for (int base = 0; base < total; base += 32 * BATCH) {
+        uint64_t kb[BATCH];
+        uint64_t* src[BATCH];
 #pragma unroll
-            for (int s = KT_TOPK - 1; s > 0; --s) {
-                const bool shift = loc[s - 1] < key;
-                const bool land = !shift && loc[s] < key;
-                loc[s] = shift ? loc[s - 1] : (land ? key : loc[s]);
+        for (int u = 0; u < BATCH; ++u) {
+            const int idx = base + u * 32 + lane;
+            const int n = idx / k, j = idx - n * k;
+            src[u] = idx < total ? const_cast<uint64_t*>(cand) + (((size_t)n * num_m + m) * BM + rit) * k + j
+                                 : nullptr;
+            kb[u] = src[u] ? *src[u] : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u)
+            if (src[u]) *src[u] = 0;  // leave the workspace zeroed
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const uint64_t key = kb[u];
+            if (key > loc[KT_TOPK - 1]) {
+#pragma unroll
+                for (int s = KT_TOPK - 1; s > 0; --s) {
+                    const bool shift = loc[s - 1] < key;
+                    const bool land = !shift && loc[s] < key;
+                    loc[s] = shift ? loc[s - 1] : (land ? key : loc[s]);
+                }
+                if (loc[0] < key) loc[0] = key;
             }
-            if (loc[0] < key) loc[0] = key;
         }
     }
     for (int j = 0; j < k; ++j) {

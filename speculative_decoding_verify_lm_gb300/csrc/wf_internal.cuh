@@ -27,7 +27,7 @@ struct Control {
 };
 static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 
-constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
     size_t keys, cand, part, dall, ent, gath, total;

@@ -9,8 +9,8 @@
 // kernel before this one in a round (the acceptance step), so each warp loads
 // its W1 row into registers (d <= 2560) before waiting on that kernel: the
 // weight stream overlaps it, and only the rows to route and the hidden states
-// are read after the wait.  The CTA stages up to RB hidden rows
-// in shared memory and keeps RB dot products per warp; units are folded per
+// are read after the wait.  Each pass takes RB hidden rows (read through L1,
+// shared by the CTA's warps) and keeps RB dot products per warp; units are folded per
 // CTA into w2[j] * GELU(z_j) partials, and the last CTA to finish sums the
 // partials of every sequence in a fixed order (the result does not depend on
 // CTA scheduling) and writes delta_al and route.
@@ -21,8 +21,6 @@ namespace wf {
 constexpr int ROUTER_THREADS = ROUTER_UNITS_PER_CTA * 32;
 constexpr int ROUTER_RB = 8;        // hidden rows staged per pass
 constexpr int ROUTER_WREG = 20;     // float4 of a W1 row held per lane: d <= 32 * 4 * 20 = 2560
-constexpr int ROUTER_SMEM_MAX = 160 * 1024;
-constexpr int ROUTER_SMEM_RESIDENT = 16 * 1024;
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
@@ -36,12 +34,9 @@ __device__ __forceinline__ float dot4(const float4 w, const uint2 h, float acc) 
 __global__ void __launch_bounds__(ROUTER_THREADS)
     router_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
                   int P, const float* __restrict__ W1, const float* __restrict__ b1, const float* __restrict__ w2,
-                  float b2, float tau, float* delta_al, int32_t* route, float* part, int rb_max, Control* ctrl) {
+                  float b2, float tau, float* delta_al, int32_t* route, float* part, Control* ctrl) {
     // part: [B][gridDim.x] partial sums, zero on entry and on exit
-    extern __shared__ uint8_t smem_raw[];
-    uint16_t* sh = reinterpret_cast<uint16_t*>(smem_raw);  // [rb_max][d] bf16
     __shared__ float red[ROUTER_UNITS_PER_CTA][ROUTER_RB];
-    __shared__ int s_row[ROUTER_RB];
     __shared__ int s_last;
 
     const int w = threadIdx.x >> 5;
@@ -71,25 +66,22 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     if (!beside) pdl_wait();
     pdl_trigger();
 
-    for (int b0 = 0; b0 < B; b0 += rb_max) {
-        const int nb = min(rb_max, B - b0);
-        __syncthreads();
-        if (threadIdx.x < nb) {
-            int r = rows ? rows[b0 + threadIdx.x] : b0 + threadIdx.x;   // no rows: route every row
-            if (r < 0 || (P >= 0 && r >= P)) r = -1;
-            s_row[threadIdx.x] = r;
+    // RB rows per pass; every warp reads the same hidden rows, straight from
+    // L2 through L1 (no staging), so the CTA needs no dynamic shared memory
+    for (int b0 = 0; b0 < B; b0 += ROUTER_RB) {
+        const int nb = min(ROUTER_RB, B - b0);
+        const uint2* hrow[ROUTER_RB];
+        bool hv[ROUTER_RB];
+#pragma unroll
+        for (int rb = 0; rb < ROUTER_RB; ++rb) {
+            int r = -1;
+            if (rb < nb) {
+                r = rows ? rows[b0 + rb] : b0 + rb;   // no rows: route every row
+                if (r < 0 || (P >= 0 && r >= P)) r = -1;
+            }
+            hv[rb] = r >= 0;
+            hrow[rb] = reinterpret_cast<const uint2*>(hidden + (size_t)(r >= 0 ? r : 0) * d);
         }
-        __syncthreads();
-        // stage the rows (16-byte chunks); invalid rows are zero-filled
-        const int chunks = d >> 3;
-        for (int idx = threadIdx.x; idx < nb * chunks; idx += blockDim.x) {
-            const int rb = idx / chunks, c = idx - rb * chunks;
-            const int r = s_row[rb];
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r >= 0) v = reinterpret_cast<const uint4*>(hidden + (size_t)r * d)[c];
-            reinterpret_cast<uint4*>(sh + (size_t)rb * d)[c] = v;
-        }
-        __syncthreads();
         float acc[ROUTER_RB];
 #pragma unroll
         for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = 0.f;
@@ -101,8 +93,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
                     if (c < d4) {
 #pragma unroll
                         for (int rb = 0; rb < ROUTER_RB; ++rb)
-                            if (rb < nb)
-                                acc[rb] = dot4(wv[u], reinterpret_cast<const uint2*>(sh + (size_t)rb * d)[c], acc[rb]);
+                            if (hv[rb]) acc[rb] = dot4(wv[u], __ldg(hrow[rb] + c), acc[rb]);
                     }
                 }
             } else {
@@ -117,14 +108,13 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
                         if (c < d4) {
 #pragma unroll
                             for (int rb = 0; rb < ROUTER_RB; ++rb)
-                                if (rb < nb)
-                                    acc[rb] = dot4(wl[u], reinterpret_cast<const uint2*>(sh + (size_t)rb * d)[c],
-                                                   acc[rb]);
+                                if (hv[rb]) acc[rb] = dot4(wl[u], __ldg(hrow[rb] + c), acc[rb]);
                         }
                     }
                 }
             }
         }
+        __syncthreads();   // the previous pass has read red[]
 #pragma unroll
         for (int rb = 0; rb < ROUTER_RB; ++rb) {
             float v = acc[rb];
@@ -181,26 +171,10 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s) {
     if (B == 0) return WF_OK;
-    // rows staged per pass: no more than the batch, in at most 16 KB, so that
-    // the CTAs fit next to the LM-head CTAs (198 KB of shared memory each) when
-    // both run at once
-    int rb = (int)((size_t)ROUTER_SMEM_RESIDENT / ((size_t)d * 2));
-    rb = rb < 1 ? 1 : (rb > ROUTER_RB ? ROUTER_RB : rb);
-    rb = rb > B ? B : rb;
-    const size_t smem = (size_t)rb * d * 2;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ROUTER_SMEM_MAX) !=
-            cudaSuccess)
-            return WF_ERR_CUDA;
-        attr_set[dev] = true;
-    }
     Control* ctrl = reinterpret_cast<Control*>(ws);
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
-    return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA)), dim3(ROUTER_THREADS), smem, s, hidden, rows, B,
-                  d, m, P, W1, b1, w2, b2, tau, delta_al, route, part, rb, ctrl);
+    return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA)), dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d,
+                  m, P, W1, b1, w2, b2, tau, delta_al, route, part, ctrl);
 }
 
 }  // namespace wf

@@ -225,3 +225,89 @@ wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s) {
 }
 
 }  // namespace wf
+
+namespace wf {
+
+// Rows kept after a round (the committed positions: the root row and the rows
+// of the accepted path) and their packed offsets, one CTA: a block-wide
+// exclusive scan of n_accept + 1 over the sequences, 1024 at a time.
+__global__ void __launch_bounds__(1024)
+    accepted_rows_kernel(const int32_t* __restrict__ n_accept, const int32_t* __restrict__ path, int path_stride,
+                         const int32_t* __restrict__ pos_off, int B, int32_t* acc_rows, int32_t* acc_off) {
+    __shared__ int32_t warp_sum[32];
+    __shared__ int32_t carry;
+    pdl_wait();   // n_accept / path come from the acceptance step
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        acc_off[0] = 0;
+    }
+    __syncthreads();
+    for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+        const int b = b0 + threadIdx.x;
+        int cnt = 0;
+        if (b < B) {
+            const int n = n_accept[b];
+            cnt = n + 1;
+            int32_t* out = acc_rows + (size_t)b * (path_stride + 1);
+            out[0] = pos_off[b];
+            for (int j = 1; j <= path_stride; ++j)
+                out[j] = j <= n ? pos_off[b] + 1 + path[(size_t)b * path_stride + j - 1] : -1;
+        }
+        // inclusive scan of cnt across the block
+        int v = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += o;
+        }
+        if (lane == 31) warp_sum[w] = v;
+        __syncthreads();
+        if (w == 0) {
+            int s = lane < (int)(blockDim.x >> 5) ? warp_sum[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, s, off);
+                if (lane >= off) s += o;
+            }
+            warp_sum[lane] = s;
+        }
+        __syncthreads();
+        const int incl = v + (w > 0 ? warp_sum[w - 1] : 0) + carry;
+        if (b < B) acc_off[b + 1] = incl;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = incl;
+        __syncthreads();
+    }
+}
+
+// hidden_out[acc_off[b] + j] = hidden[acc_rows[b][j]] for the kept rows of sequence b.
+__global__ void __launch_bounds__(128)
+    gather_kept_kernel(const uint16_t* __restrict__ hidden, int d, const int32_t* __restrict__ acc_rows,
+                       const int32_t* __restrict__ acc_off, int path_stride, uint16_t* __restrict__ hidden_out) {
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x;
+    const int first = acc_off[b], cnt = acc_off[b + 1] - first;
+    const int chunks = d >> 3;
+    for (int j = 0; j < cnt && j <= path_stride; ++j) {
+        const int r = acc_rows[(size_t)b * (path_stride + 1) + j];
+        const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)r * d);
+        uint4* dst = reinterpret_cast<uint4*>(hidden_out + (size_t)(first + j) * d);
+        for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = src[c];
+    }
+}
+
+wf_status launch_accepted_rows(const int32_t* n_accept, const int32_t* path, int path_stride, const int32_t* pos_off,
+                               int B, int32_t* acc_rows, int32_t* acc_off, const uint16_t* hidden, int d,
+                               uint16_t* hidden_out, cudaStream_t s) {
+    if (B == 0) return WF_OK;
+    wf_status st = launch(accepted_rows_kernel, dim3(1), dim3(1024), 0, s, n_accept, path, path_stride, pos_off, B,
+                          acc_rows, acc_off);
+    if (st != WF_OK || !hidden_out) return st;
+    return launch(gather_kept_kernel, dim3(B), dim3(128), 0, s, hidden, d, (const int32_t*)acc_rows,
+                  (const int32_t*)acc_off, path_stride, hidden_out);
+}
+
+}  // namespace wf

@@ -70,6 +70,10 @@ _SIGS = {
     "wf_lmhead_argmax": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz,
                                 _c_void_p]),
     "wf_lmhead_argmax_noalloc": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p]),
+    "wf_build_tree": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                             _c_void_p, _sz, _c_void_p]),
+    "wf_accepted_rows": (_i32, [_c_void_p, _c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _i32,
+                                _c_void_p, _c_void_p]),
     "wf_verify_chain": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p,
                                _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "wf_verify_tree": (_i32, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p,
@@ -221,6 +225,41 @@ def wf_lmhead_argmax_noalloc(hidden, W, ids=None, maxlogit=None, stream=None):
                                         _stream(stream))
     _raise(st, "wf_lmhead_argmax_noalloc")
     return ids
+
+
+def wf_build_tree(tid, lp, N: int, ws: Workspace, stream=None):
+    """EAGLE-3 draft tree from per-step, per-slot top-k children -> (parent, token, score, depth) [B, N]."""
+    B, D, k, _ = tid.shape
+    dev = tid.device
+    parent = torch.empty((B, N), dtype=torch.int32, device=dev)
+    token = torch.empty((B, N), dtype=torch.int32, device=dev)
+    score = torch.empty((B, N), dtype=torch.float32, device=dev)
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    st = lib().wf_build_tree(_check(tid, "tid", _I32), _check(lp, "lp", _F32), B, D, k, N, parent.data_ptr(),
+                             token.data_ptr(), score.data_ptr(), depth.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
+    _raise(st, "wf_build_tree")
+    return parent, token, score, depth
+
+
+def wf_accepted_rows(n_accept, path, pos_off, hidden=None, stream=None):
+    """Kept rows of each sequence (root + accepted path), their packed offsets and,
+    if ``hidden`` is given, the packed hidden states of those rows."""
+    B, ps = path.shape
+    dev = n_accept.device
+    acc_rows = torch.empty((B, ps + 1), dtype=torch.int32, device=dev)
+    acc_off = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    out = None
+    d = 0
+    if hidden is not None:
+        d = hidden.shape[1]
+        total = int(n_accept.clamp(min=-1).add(1).sum().item())   # host read of the packed size
+        out = torch.empty((max(total, 1), d), dtype=hidden.dtype, device=dev)
+    st = lib().wf_accepted_rows(_check(n_accept, "n_accept", _I32), _check(path, "path", _I32), ps,
+                                _check(pos_off, "pos_off", _I32), B, _check(acc_rows, "acc_rows", _I32),
+                                _check(acc_off, "acc_off", _I32), _check(hidden, "hidden", _BF16, True), d,
+                                _check(out, "hidden_out", _BF16, True), _stream(stream))
+    _raise(st, "wf_accepted_rows")
+    return acc_rows, acc_off, out
 
 
 def _verify_outputs(B, path_stride, device, n_accept, bonus, last_pos, path):

@@ -341,6 +341,33 @@ def test_accepted_rows(seed, B, max_nodes):
     assert np.array_equal(host(gh).view(np.uint16), h[kept])
 
 
+# ------------------------------------------------------------------ draft-tree construction
+@pytest.mark.parametrize("B,D,k,N", [(1, 8, 10, 60), (64, 8, 10, 60), (5, 3, 4, 20), (3, 16, 16, 200), (2, 1, 6, 6)])
+def test_build_tree(B, D, k, N):
+    rng = np.random.default_rng(B * 100 + D)
+    tid = rng.integers(0, 151936, (B, D, k, k)).astype(np.int32)
+    lp = np.log(rng.dirichlet(np.ones(k) * 0.7, (B, D, k))).astype(np.float32)
+    lp[lp < -60] = -60.0
+    ref = o().build_tree(tid, lp, N)
+    assert ref[4] == 0
+    ws = wf.Workspace(1)
+    got = wf.wf_build_tree(dev(tid), dev(lp), N, ws)
+    torch.cuda.synchronize()
+    for a, e in zip(got, ref[:4]):
+        assert np.array_equal(host(a), e)
+    assert ws.device_error() == (0, 0)
+
+
+def test_build_tree_bad_logprob():
+    tid = np.zeros((2, 2, 2, 2), np.int32)
+    lp = np.full((2, 2, 2, 2), -0.5, np.float32)
+    lp[1, 1, 1, 0] = 0.25
+    ws = wf.Workspace(1)
+    parent, token, _, _ = wf.wf_build_tree(dev(tid), dev(lp), 3, ws)
+    assert (host(parent)[1] == -1).all() and (host(token)[1] == -1).all() and host(parent)[0][0] == -1
+    assert ws.device_error()[0] == 5
+
+
 # ------------------------------------------------------------------ failure path
 def test_bounded_wait_gives_up_and_context_survives():
     ws = wf.Workspace(8)
