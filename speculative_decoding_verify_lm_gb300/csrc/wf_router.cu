@@ -19,7 +19,8 @@
 namespace wf {
 
 constexpr int ROUTER_THREADS = ROUTER_UNITS_PER_CTA * 32;
-constexpr int ROUTER_RB = 8;        // hidden rows staged per pass
+constexpr int ROUTER_RB = 8;        // hidden rows per pass
+constexpr int ROUTER_ROWS_PER_CTA = 32;   // rows one CTA routes (more rows: more CTAs along y)
 constexpr int ROUTER_WREG = 20;     // float4 of a W1 row held per lane: d <= 32 * 4 * 20 = 2560
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
@@ -68,8 +69,11 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
 
     // RB rows per pass; every warp reads the same hidden rows, straight from
     // L2 through L1 (no staging), so the CTA needs no dynamic shared memory
-    for (int b0 = 0; b0 < B; b0 += ROUTER_RB) {
-        const int nb = min(ROUTER_RB, B - b0);
+    // this CTA's rows: blockIdx.y picks a chunk of ROUTER_ROWS_PER_CTA
+    const int y0 = blockIdx.y * ROUTER_ROWS_PER_CTA;
+    const int y1 = min(B, y0 + ROUTER_ROWS_PER_CTA);
+    for (int b0 = y0; b0 < y1; b0 += ROUTER_RB) {
+        const int nb = min(ROUTER_RB, y1 - b0);
         const uint2* hrow[ROUTER_RB];
         bool hv[ROUTER_RB];
 #pragma unroll
@@ -87,14 +91,22 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
         for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = 0.f;
         if (unit_live) {
             if (in_regs) {
+                // loads of four column groups x RB rows are issued together before
+                // their FMAs, so a lane keeps 32 loads in flight
 #pragma unroll
-                for (int u = 0; u < ROUTER_WREG; ++u) {
-                    const int c = lane + 32 * u;
-                    if (c < d4) {
+                for (int u0 = 0; u0 < ROUTER_WREG; u0 += 4) {
+                    uint2 hx[4][ROUTER_RB];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = lane + 32 * (u0 + u);
 #pragma unroll
                         for (int rb = 0; rb < ROUTER_RB; ++rb)
-                            if (hv[rb]) acc[rb] = dot4(wv[u], __ldg(hrow[rb] + c), acc[rb]);
+                            hx[u][rb] = (hv[rb] && c < d4) ? __ldg(hrow[rb] + c) : make_uint2(0u, 0u);
                     }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+#pragma unroll
+                        for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = dot4(wv[u0 + u], hx[u][rb], acc[rb]);
                 }
             } else {
                 for (int c0 = lane; c0 < d4; c0 += 32 * 4) {
@@ -134,7 +146,7 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
     // the last CTA to finish reduces the partials in a fixed order
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(&ctrl->router_done, 1u) == (unsigned)nblk - 1;
+    if (threadIdx.x == 0) s_last = atomicAdd(&ctrl->router_done, 1u) == (unsigned)(nblk * gridDim.y) - 1;
     __syncthreads();
     if (!s_last) {
         if (beside) pdl_wait();
@@ -173,8 +185,9 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
     if (B == 0) return WF_OK;
     Control* ctrl = reinterpret_cast<Control*>(ws);
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
-    return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA)), dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d,
-                  m, P, W1, b1, w2, b2, tau, delta_al, route, part, ctrl);
+    return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA), cdiv(B, ROUTER_ROWS_PER_CTA)),
+                  dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d, m, P, W1, b1, w2, b2, tau, delta_al, route, part,
+                  ctrl);
 }
 
 }  // namespace wf

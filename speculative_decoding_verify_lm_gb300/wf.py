@@ -446,6 +446,21 @@ class Round:
         with torch.cuda.stream(stream) if stream is not None else _nullctx():
             host_outputs.copy_(self.out_buf, non_blocking=True)
 
+    def capture_host_step(self, host_inputs, host_outputs):
+        """Capture one host-to-host step - copy the packed inputs in from pinned
+        memory, run the round, copy every output back - as a CUDA graph;
+        ``replay_host_step()`` then runs it with one launch.  Call once the round
+        has run eagerly at least once (its kernels are configured on first use)."""
+        self._host_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self._host_graph):
+            self.in_buf.copy_(host_inputs, non_blocking=True)
+            self()
+            host_outputs.copy_(self.out_buf, non_blocking=True)
+        return self._host_graph
+
+    def replay_host_step(self):
+        self._host_graph.replay()
+
     def host_views(self, host_outputs):
         """Typed views of the outputs inside a downloaded pinned buffer."""
         _, views = _packed_views(host_outputs, self._out_spec)
