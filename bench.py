@@ -118,7 +118,8 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"gemm_select_kernel<1>": ("wf_gemm_select.cu", "wf_internal.cuh")}
+KERNEL_SOURCES = {"gemm_select_kernel<1>": ("wf_gemm_select.cu", "wf_internal.cuh"),
+                  "gemm_select_kernel<1,1,0,1>": ("wf_gemm_select.cu", "wf_internal.cuh")}
 
 
 def source_sha(kernel: str) -> str:
@@ -316,28 +317,48 @@ def main():
     tot_rows = allreduce_sum(pg, P * args.steps, device)
     tot_acc = allreduce_sum(pg, accepted * args.steps, device)
     value = tot_rows / max_s
-    launches_per_round = 3 + (2 if draft else 0)
+    # the round's composition (wf_round): with at most 128 verified rows the
+    # router runs beside the LM head and the draft head shares its sweep
+    shared = draft and P <= 128 and B <= 128
+    # (shared: both heads, router, acceptance, top-k merge)
+    launches_per_round = 4 if shared else 3 + (2 if draft else 0)
 
-    # ---- the dominant kernel on its own (LM head), CUDA events per launch
+    # ---- the dominant kernel on its own, CUDA events per launch: the shared
+    # sweep of both heads (timed with its top-k merge) or the LM head alone
     hbm_peak, tc_peak, peak_src = measured_peaks()
     ids_buf = torch.empty(P, dtype=torch.int32, device=device)
     hdev = r.inputs["hidden"]
-    ws1 = wf.Workspace(P, device=device)
+    if shared:
+        k = wl.topk
+        ws1 = wf.Workspace(P, B, 1, wl.Wd.shape[0], k, device=device, d=d)
+        xdev, Wddev, d2tdev = r.inputs["x"], r.inputs["Wd"], r.inputs["d2t"]
+        dbufs = dict(draft_ids=torch.empty((B, k), dtype=torch.int32, device=device),
+                     tids=torch.empty((B, k), dtype=torch.int32, device=device),
+                     vals=torch.empty((B, k), dtype=torch.float32, device=device))
+        kernel_call = lambda: wf.wf_lmhead_draft_topk(hdev, Wdev, xdev, Wddev, d2tdev, k, ws1,  # noqa: E731
+                                                      ids=ids_buf, **dbufs)
+        Vd = wl.Wd.shape[0]
+        alg_bytes = (V + Vd) * d * 2 + (P + B) * d * 2 + Vd * 4 + P * 4 + B * k * 12
+        alg_flops = 2.0 * d * (P * V + B * Vd)
+        kernel_name = "gemm_select_kernel<1,1,0,1>"
+    else:
+        ws1 = wf.Workspace(P, device=device)
+        kernel_call = lambda: wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)  # noqa: E731
+        alg_bytes = V * d * 2 + P * d * 2 + P * 4
+        alg_flops = 2.0 * P * V * d
+        kernel_name = "gemm_select_kernel<1>"
     for _ in range(3):
-        wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)
+        kernel_call()
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         if flush:
             l2buf.zero_()
         kev[i][0].record(stream)
-        wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)
+        kernel_call()
         kev[i][1].record(stream)
     torch.cuda.synchronize(device)
     k_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
-    alg_bytes = V * d * 2 + P * d * 2 + P * 4
-    alg_flops = 2.0 * P * V * d
     hbm_bound = alg_flops / alg_bytes < (tc_peak * 1e12) / (hbm_peak * 1e9)
-    kernel_name = "gemm_select_kernel<1>"
     if hbm_bound:
         achieved = alg_bytes / (k_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak}

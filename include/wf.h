@@ -14,6 +14,7 @@
  *   wf_verify_tree    EAGLE-3 tree acceptance (deepest matched root path) + bonus
  *   wf_router_mlp     neural router f_theta and the threshold decision
  *   wf_draft_topk     EAGLE-3 draft head, top-k, draft-to-target id map
+ *   wf_lmhead_draft_topk  the target and draft heads in one weight sweep
  *   wf_round          all of the above as one stream-ordered round
  *
  * Conventions shared by every call
@@ -293,11 +294,35 @@ WF_API wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int3
                         size_t ws_bytes, wf_stream_t stream);
 
 /*
+ * Both heads of a round in one weight sweep: the results of wf_lmhead_argmax
+ * over the P rows of hidden and of wf_draft_topk over the B rows of x,
+ * bit for bit, from one persistent launch that streams W and then Wd through
+ * the same pipeline (plus a small merge of the draft candidates).  The pages
+ * describe the two heads as separate steps (target verification, WhiFlash
+ * paper Sec. 3.2; EAGLE-3 drafting, Qwen3-4B-EAGLE3 card); reading both
+ * matrices in one pass is this library's scheduling, so that the smaller
+ * draft matrix streams at full bandwidth instead of as a second sweep that
+ * fills the GPU poorly.  No passage corresponds to the fused call itself.
+ *
+ * Arguments as in wf_lmhead_argmax (hidden, W, P, d, V, ids, maxlogit) and
+ * wf_draft_topk (x, Wd, d2t, B, Vd, k, draft_ids, tids, vals), one shared d.
+ * P <= 128 and B <= 128 (one activation tile each), else WF_ERR_UNSUPPORTED:
+ * call the two entry points.  Workspace: wf_workspace_bytes(P, B, d, 0, Vd, k).
+ */
+WF_API wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
+                               int32_t* ids, float* maxlogit, const uint16_t* x, const uint16_t* Wd,
+                               const int32_t* d2t, int B, int Vd, int k, int32_t* draft_ids,
+                               int32_t* tids, float* vals, void* ws, size_t ws_bytes,
+                               wf_stream_t stream);
+
+/*
  * One whole verify-and-route round (paper Sec. 3.2 - 3.3): LM-head argmax at
  * every verified row -> per-sequence acceptance (chain or tree by kind[b])
  * -> router on each sequence's last accepted row -> route for the next round;
  * plus, if Wd != NULL, the draft head's top-k for every sequence.  All stages
- * are stream-ordered on `stream` with no host synchronisation.
+ * are stream-ordered on `stream` with no host synchronisation.  With at most
+ * 128 verified rows the draft head shares the LM head's weight sweep (as in
+ * wf_lmhead_draft_topk).
  */
 typedef struct wf_round_args {
     /* verified rows */

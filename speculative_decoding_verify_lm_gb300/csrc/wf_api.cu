@@ -31,6 +31,11 @@ wf_status launch_accepted_rows(const int32_t* n_accept, const int32_t* path, int
                                uint16_t* hidden_out, cudaStream_t s);
 wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t* rows, int B, uint16_t* out,
                              void* ws, cudaStream_t s);
+wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                              float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
+                              size_t cand_off, int* bn_out, cudaStream_t s);
+wf_status launch_topk_merge(int B, int Vd, int bn, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+                            float* vals, void* ws, size_t cand_off, cudaStream_t s);
 wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, cudaStream_t s);
 
@@ -238,6 +243,23 @@ wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2
     return launch_draft_topk(x, Wd, d2t, B, d, Vd, k, draft_ids, tids, vals, ws, L.cand, stream);
 }
 
+wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B,
+                               int Vd, int k, int32_t* draft_ids, int32_t* tids, float* vals, void* ws,
+                               size_t ws_bytes, wf_stream_t stream) {
+    if (!hidden || !W || !ids || bad_gemm_shape(P, d, V)) return WF_ERR_INVALID_ARG;
+    if (!x || !Wd || !d2t || bad_gemm_shape(B, d, Vd)) return WF_ERR_INVALID_ARG;
+    if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals)) return WF_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || !aligned16(W) || !aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
+    if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
+    const Layout L = layout(P, B, d, 0, Vd, k);
+    WF_TRY(check_ws(ws, ws_bytes, L.part));   // control block, keys and top-k candidates
+    WF_TRY(check_device());
+    int bn = 0;
+    WF_TRY(launch_lmhead_draft(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, L.cand, &bn, stream));
+    return launch_topk_merge(B, Vd, bn, k, d2t, draft_ids, tids, vals, ws, L.cand, stream);
+}
+
 wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {
     if (!a) return WF_ERR_INVALID_ARG;
     if (!a->hidden || !a->W || bad_gemm_shape(a->P, a->d, a->V)) return WF_ERR_INVALID_ARG;
@@ -278,6 +300,20 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         WF_TRY(launch_gather_rows(a->hidden, a->P, a->d, a->last_pos, a->B, gath, ws, stream));
         WF_TRY(launch_lmhead_entropy(gath, a->W, a->B, a->d, a->V, nullptr, nullptr, a->delta_al, a->route, a->tau,
                                      a->last_pos, a->P, ws, L.ent, stream));
+    } else if (draft && a->P <= BM && a->B <= BM) {
+        // One activation tile each: the LM head and the draft head share one
+        // sweep (W, then Wd); the router runs on every row beside it, the
+        // acceptance step picks the accepted row's output, and the draft
+        // candidates are merged last.
+        int bn = 0;
+        WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B, a->Vd,
+                                   a->k, ws, L.cand, &bn, stream));
+        WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
+                             nullptr, ws, L.part, stream));
+        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
+                             RoutePick{dall, a->tau, a->delta_al, a->route}));
+        return launch_topk_merge(a->B, a->Vd, bn, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws, L.cand, stream);
     } else if (a->P <= ROUTE_ALL_ROWS_MAX) {
         // Few rows: the router runs on every verified row beside the LM head
         // (it needs only the hidden states and its weights, and waits for the

@@ -17,6 +17,10 @@
 // (order-preserving logit, ~id) key; the last CTA to finish converts the keys
 // to ids and resets them to zero.  Top-k rows write one sorted candidate list
 // per tile; wf_topk_merge combines them.
+// DUAL: one launch sweeps two problems with one activation tile each - the
+// target LM head (argmax) and then the EAGLE-3 draft head (top-k) - through
+// the same pipeline, so the smaller draft matrix streams at full bandwidth
+// behind the larger one instead of as a second, under-filled sweep.
 //
 // Every wait is bounded: a wait that runs out records WF_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, drains its own in-flight copies / MMAs (again bounded)
@@ -54,6 +58,9 @@ struct GemmParams {
     float tau;
     const int32_t* src_rows;   // entropy over gathered rows: the source row of each, or null
     int src_P;
+    // DUAL: the second problem (top-k, one activation tile) whose num_n2 tiles
+    // follow the first problem's; its candidate lists go to cand
+    int M_rows2, N_w2, num_n2, a_bytes2;
     Control* ctrl;
     uint64_t timeout_ns;
 };
@@ -95,6 +102,97 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], floa
     }
 }
 
+// One finished accumulator as epilogue thread rit sees it (activation row
+// m * BM + rit of a problem with M_rows rows and N_w weight rows): wait for
+// it, keep the row's best (KT = 1) or top KT over the tile's columns and, with
+// ENT, fold the columns into the row's softmax statistics; hand the
+// accumulator back to the MMA warp, then publish the row's result (a packed
+// key for argmax, the tile's sorted candidate list for top-k).
+template <int KT, bool ENT>
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfull, uint64_t* tempty,
+                                              volatile int* abort_flag, uint32_t tmem_base, uint32_t tile_i, int q,
+                                              int rit, int M_rows, int N_w, int m, int n, int cand_num_m, float& em,
+                                              float& es, float& et) {
+    const uint32_t acc = tile_i & 1;
+    const uint32_t acc_ph = (tile_i >> 1) & 1;
+    const bool quad_live = m * BM + q * 32 < M_rows;
+    const int row = m * BM + rit;
+    if (!mbar_wait(&tfull[acc], acc_ph, p.timeout_ns, abort_flag)) {
+        gemm_fail(p.ctrl, abort_flag, 0x300);
+        return false;
+    }
+    tc_fence_after();
+    float tv[KT];
+    int ti[KT];
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+        tv[j] = -INFINITY;
+        ti[j] = 0;
+    }
+    if (quad_live) {
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+        for (int c0 = 0; c0 < p.bn; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c0, r);
+            tmem_ld_wait();
+            const int col0 = n * p.bn + c0;
+            // columns >= lim are past the weight matrix or past this tile; rows
+            // past the activations (stale shared-memory rows) take no part
+            const int lim = row < M_rows ? min(N_w - col0, p.bn - c0) : 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float v = __uint_as_float(r[j]);
+                if (j < lim) {
+                    if constexpr (KT == 1) {
+                        if (v > tv[0]) {
+                            tv[0] = v;
+                            ti[0] = col0 + j;
+                        }
+                    } else {
+                        if (v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
+                    }
+                }
+            }
+            if constexpr (ENT) {
+                float cmax = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < lim) cmax = fmaxf(cmax, __uint_as_float(r[j]));
+                if (cmax > em) {   // new running maximum: rescale what was summed so far
+                    if (es > 0.f) {
+                        const float sc = __expf(em - cmax);
+                        et = (et + (em - cmax) * es) * sc;
+                        es *= sc;
+                    }
+                    em = cmax;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < lim) {
+                        const float z = __uint_as_float(r[j]) - em;
+                        const float e = __expf(z);
+                        es += e;
+                        et = fmaf(z, e, et);
+                    }
+            }
+        }
+    }
+    tc_fence_before();
+    mbar_arrive(&tempty[acc]);
+    if (quad_live && row < M_rows) {
+        if constexpr (KT == 1) {
+            atomicMax(reinterpret_cast<unsigned long long*>(p.keys + row),
+                      (unsigned long long)pack_key(tv[0], (uint32_t)ti[0]));
+        } else {
+            const size_t t = (size_t)n * cand_num_m + m;   // the candidate list of tile (m, n)
+            uint64_t* dst = p.cand + (t * BM + rit) * p.k;
+            for (int j = 0; j < KT; ++j)
+                if (j < p.k) dst[j] = tv[j] == -INFINITY ? 0ull : pack_key(tv[j], (uint32_t)ti[j]);
+        }
+    }
+    return true;
+}
+
 // CL = 1: each CTA loads its own activation and weight boxes.
 // CL = 2: CTAs run in clusters of two on tile pairs (m, n) and (m + 1, n) that
 // share the weight tile: each CTA loads half of it and multicasts that half to
@@ -105,10 +203,14 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], floa
 // logits so that the entropy of the next-token distribution comes out of the
 // same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
 // activation tiles).
-template <int KT, int CL, bool ENT>
+// DUAL (with KT = 1, CL = 1, no ENT): tiles U0.. are the second problem's
+// (activation map tmA2, weight map tmB2, top-k into p.cand).
+template <int KT, int CL, bool ENT, bool DUAL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                        const GemmParams p) {
+    static_assert(!DUAL || (KT == 1 && CL == 1 && !ENT), "the dual sweep pairs an argmax head with a top-k head");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -128,7 +230,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
     const int slot = blockIdx.x / CL, nslots = gridDim.x / CL;
     const int num_mp = (p.num_m + CL - 1) / CL;
-    const int U = num_mp * p.num_n;
+    const int U0 = num_mp * p.num_n;
+    const int U = U0 + (DUAL ? p.num_n2 : 0);
     constexpr uint16_t kPair = 0x3;
 
     if (threadIdx.x == 0) {
@@ -146,6 +249,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (DUAL) {
+            tma_prefetch_desc(&tmA2);
+            tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -171,7 +278,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t it = 0;  // stages issued so far
             bool ok = true;
             for (int u = slot; u < U && ok; u += nslots) {
-                const int m = (u % num_mp) * CL + rank, n = u / num_mp;
+                const bool second = DUAL && u >= U0;
+                const int m = second ? 0 : (u % num_mp) * CL + rank;
+                const int n = second ? u - U0 : u / num_mp;
+                const CUtensorMap* mA = second ? &tmA2 : &tmA;
+                const CUtensorMap* mB = second ? &tmB2 : &tmB;
+                const uint32_t tx = (second ? p.a_bytes2 : p.a_bytes) + p.bn * BK * 2;
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -180,13 +292,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], p.a_bytes + p.bn * BK * 2);
-                    tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kc * BK, m * BM, pol_a);
+                    mbar_arrive_expect_tx(&full[s], tx);
+                    tma_load_2d(sA + s * A_BYTES, mA, &full[s], kc * BK, m * BM, pol_a);
                     if constexpr (CL == 2)
-                        tma_load_2d_multicast(sB + s * B_BYTES + rank * half * BK * 2, &tmB, &full[s], kc * BK,
+                        tma_load_2d_multicast(sB + s * B_BYTES + rank * half * BK * 2, mB, &full[s], kc * BK,
                                               n * p.bn + rank * half, kPair, pol_w);
                     else
-                        tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kc * BK, n * p.bn, pol_w);
+                        tma_load_2d(sB + s * B_BYTES, mB, &full[s], kc * BK, n * p.bn, pol_w);
                 }
             }
             if (!ok || *abort_flag) {
@@ -246,84 +358,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         float em = -INFINITY, es = 0.f, et = 0.f;   // ENT: this row's running softmax statistics
         uint32_t tile_i = 0;
         for (int u = slot; u < U; u += nslots, ++tile_i) {
-            const int m = (u % num_mp) * CL + rank, n = u / num_mp;
-            const uint32_t acc = tile_i & 1;
-            const uint32_t acc_ph = (tile_i >> 1) & 1;
-            const bool quad_live = m * BM + q * 32 < p.M_rows;
-            const int row = m * BM + rit;
-            if (!mbar_wait(&tfull[acc], acc_ph, p.timeout_ns, abort_flag)) {
-                gemm_fail(p.ctrl, abort_flag, 0x300);
-                break;
-            }
-            tc_fence_after();
-            float tv[KT];
-            int ti[KT];
-#pragma unroll
-            for (int j = 0; j < KT; ++j) {
-                tv[j] = -INFINITY;
-                ti[j] = 0;
-            }
-            if (quad_live) {
-                const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-                for (int c0 = 0; c0 < p.bn; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tbase + c0, r);
-                    tmem_ld_wait();
-                    const int col0 = n * p.bn + c0;
-                    // columns >= lim are past the weight matrix or past this tile; rows
-                    // past the activations (stale shared-memory rows) take no part
-                    const int lim = row < p.M_rows ? min(p.N_w - col0, p.bn - c0) : 0;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float v = __uint_as_float(r[j]);
-                        if (j < lim) {
-                            if constexpr (KT == 1) {
-                                if (v > tv[0]) {
-                                    tv[0] = v;
-                                    ti[0] = col0 + j;
-                                }
-                            } else {
-                                if (v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
-                            }
-                        }
-                    }
-                    if constexpr (ENT) {
-                        float cmax = -INFINITY;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < lim) cmax = fmaxf(cmax, __uint_as_float(r[j]));
-                        if (cmax > em) {   // new running maximum: rescale what was summed so far
-                            if (es > 0.f) {
-                                const float sc = __expf(em - cmax);
-                                et = (et + (em - cmax) * es) * sc;
-                                es *= sc;
-                            }
-                            em = cmax;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < lim) {
-                                const float z = __uint_as_float(r[j]) - em;
-                                const float e = __expf(z);
-                                es += e;
-                                et = fmaf(z, e, et);
-                            }
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-            if (quad_live && row < p.M_rows) {
-                if constexpr (KT == 1) {
-                    atomicMax(reinterpret_cast<unsigned long long*>(p.keys + row),
-                              (unsigned long long)pack_key(tv[0], (uint32_t)ti[0]));
-                } else {
-                    const size_t t = (size_t)n * p.num_m + m;   // the candidate list of tile (m, n)
-                    uint64_t* dst = p.cand + (t * BM + rit) * p.k;
-                    for (int j = 0; j < KT; ++j)
-                        if (j < p.k) dst[j] = tv[j] == -INFINITY ? 0ull : pack_key(tv[j], (uint32_t)ti[j]);
-                }
-            }
+            bool ok;
+            if (DUAL && u >= U0)
+                ok = epilogue_tile<KT_TOPK, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
+                                                   p.M_rows2, p.N_w2, 0, u - U0, 1, em, es, et);
+            else
+                ok = epilogue_tile<KT, ENT>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
+                                            p.N_w, (u % num_mp) * CL + rank, u / num_mp, p.num_m, em, es, et);
+            if (!ok) break;
         }
         if constexpr (ENT) {
             // this CTA's rows are fixed (rank's activation tile); publish their statistics
@@ -496,13 +538,15 @@ int num_sms();
 // Weight rows per tile.  Several activation tiles: 256 (largest operand reuse).
 // One activation tile (the weight-streaming case): the multiple of 16 in
 // [BN_MIN, 256] that minimises the busiest CTA's rows, waves x (bn + 16) - the
-// 16 standing for a tile's fixed cost - so the last wave is not left mostly idle.
-static int pick_bn(int num_m, int N_w, int sms) {
+// 16 standing for a tile's fixed cost - so the last wave is not left mostly
+// idle.  N_w2 > 0: a second weight matrix swept in the same launch.
+static int pick_bn(int num_m, int N_w, int sms, int N_w2 = 0) {
     if (num_m > 1) return BN;
     int best = BN;
     long best_cost = -1;
     for (int bn = BN; bn >= BN_MIN; bn -= 16) {
-        const long waves = cdiv(cdiv(N_w, bn), sms);
+        const long tiles = cdiv(N_w, bn) + (N_w2 > 0 ? cdiv(N_w2, bn) : 0);
+        const long waves = cdiv(tiles, sms);
         const long cost = waves * (bn + 16);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
@@ -512,7 +556,6 @@ static int pick_bn(int num_m, int N_w, int sms) {
     return best;
 }
 
-// Clusters of two that can be resident at once (queried once per device).
 // Clusters of two that can be resident at once (queried once per device).
 template <int KT, bool ENT>
 static int pair_slots(int dev) {
@@ -530,7 +573,7 @@ static int pair_slots(int dev) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, 2, ENT>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, 2, ENT, false>, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = num_sms() / 2;
     }
@@ -545,9 +588,9 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1, ENT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(gemm_select_kernel<KT, 2, ENT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(gemm_select_kernel<KT, 2, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
@@ -580,14 +623,15 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
         const int tiles = p.num_m * p.num_n;
         int grid = tiles < num_sms() ? tiles : num_sms();
         if (ENT && grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
-        return launch(gemm_select_kernel<KT, 1, ENT>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, p);
+        return launch(gemm_select_kernel<KT, 1, ENT, false>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, ta,
+                      tb, p);
     }
     const int pairs = cdiv(num_m, 2) * p.num_n;
     int slots = pair_slots<KT, ENT>(dev);
     if (ENT && slots > ENT_MAX_SLOTS) slots = ENT_MAX_SLOTS;
     const int grid = 2 * (pairs < slots ? pairs : slots);
-    return launch_cluster(gemm_select_kernel<KT, 2, ENT>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta, tb,
-                          p);
+    return launch_cluster(gemm_select_kernel<KT, 2, ENT, false>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta,
+                          tb, ta, tb, p);
 }
 
 static GemmParams params_for(void* ws) {
@@ -634,6 +678,66 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     const int bn = pick_bn(cdiv(B, BM), Vd, num_sms());
     return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, (const uint64_t*)p.cand, B, cdiv(B, BM),
                   cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids, vals, p.ctrl);
+}
+
+// Target LM head (argmax over P <= BM rows) and draft head (candidate lists of
+// the top k over B <= BM rows) in one persistent sweep of W then Wd.  The
+// candidate lists are merged by launch_topk_merge with the tile height this
+// returns in *bn_out.
+wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
+                              float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
+                              size_t cand_off, int* bn_out, cudaStream_t s) {
+    if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_select_kernel<1, 1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM) != cudaSuccess)
+            return WF_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    const int sms = num_sms();
+    const int bn = pick_bn(1, V, sms, Vd);
+    const int a_rows = (P + 7) / 8 * 8, a_rows2 = (B + 7) / 8 * 8;
+    CUtensorMap ta, tb, ta2, tb2;
+    if (!make_map(&ta, hidden, (uint64_t)P, (uint64_t)d, (uint32_t)a_rows) ||
+        !make_map(&tb, W, (uint64_t)V, (uint64_t)d, (uint32_t)bn) ||
+        !make_map(&ta2, x, (uint64_t)B, (uint64_t)d, (uint32_t)a_rows2) ||
+        !make_map(&tb2, Wd, (uint64_t)Vd, (uint64_t)d, (uint32_t)bn))
+        return WF_ERR_CUDA;
+    GemmParams p = params_for(ws);
+    p.M_rows = P;
+    p.N_w = V;
+    p.num_m = 1;
+    p.num_n = cdiv(V, bn);
+    p.bn = bn;
+    p.idesc = umma_idesc_bf16(BM, bn);
+    p.num_k = cdiv(d, BK);
+    p.weight_evict_first = 1;
+    p.a_bytes = a_rows * BK * 2;
+    p.ids = ids;
+    p.maxlogit = maxlogit;
+    p.k = k;
+    p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    p.M_rows2 = B;
+    p.N_w2 = Vd;
+    p.num_n2 = cdiv(Vd, bn);
+    p.a_bytes2 = a_rows2 * BK * 2;
+    p.timeout_ns = wait_timeout_ns();
+    const int tiles = p.num_n + p.num_n2;
+    *bn_out = bn;
+    return launch(gemm_select_kernel<1, 1, false, true>, dim3(tiles < sms ? tiles : sms), dim3(GEMM_THREADS),
+                  GEMM_SMEM, s, ta, tb, ta2, tb2, p);
+}
+
+// Merge the per-tile candidate lists of B rows (one activation tile) into the
+// top k, mapped through d2t.
+wf_status launch_topk_merge(int B, int Vd, int bn, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+                            float* vals, void* ws, size_t cand_off, cudaStream_t s) {
+    const uint64_t* cand = reinterpret_cast<const uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, cand, B, cdiv(B, BM), cdiv(Vd, bn), k, d2t,
+                  Vd, draft_ids, tids, vals, reinterpret_cast<Control*>(ws));
 }
 
 }  // namespace wf

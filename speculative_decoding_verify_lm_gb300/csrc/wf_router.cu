@@ -22,6 +22,11 @@ constexpr int ROUTER_THREADS = ROUTER_UNITS_PER_CTA * 32;
 constexpr int ROUTER_RB = 8;        // hidden rows per pass
 constexpr int ROUTER_ROWS_PER_CTA = 32;   // rows one CTA routes (more rows: more CTAs along y)
 constexpr int ROUTER_WREG = 20;     // float4 of a W1 row held per lane: d <= 32 * 4 * 20 = 2560
+constexpr int ROUTER_LB = 2;        // column groups whose loads are issued together (divides WREG)
+// At most 160 registers a thread: two router warps then fit in one SM
+// sub-partition's 16K registers beside two warps of the LM-head kernel (up to
+// 88 registers each), so the router really runs beside that kernel.
+constexpr int ROUTER_MAX_REGS = 160;
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 
@@ -32,7 +37,7 @@ __device__ __forceinline__ float dot4(const float4 w, const uint2 h, float acc) 
     return fmaf(w.w, __uint_as_float(h.y & 0xFFFF0000u), acc);
 }
 
-__global__ void __launch_bounds__(ROUTER_THREADS)
+__global__ void __maxnreg__(ROUTER_MAX_REGS)
     router_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
                   int P, const float* __restrict__ W1, const float* __restrict__ b1, const float* __restrict__ w2,
                   float b2, float tau, float* delta_al, int32_t* route, float* part, Control* ctrl) {
@@ -91,20 +96,20 @@ __global__ void __launch_bounds__(ROUTER_THREADS)
         for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = 0.f;
         if (unit_live) {
             if (in_regs) {
-                // loads of four column groups x RB rows are issued together before
-                // their FMAs, so a lane keeps 32 loads in flight
+                // loads of ROUTER_LB column groups x RB rows are issued together
+                // before their FMAs, so a lane keeps LB * RB loads in flight
 #pragma unroll
-                for (int u0 = 0; u0 < ROUTER_WREG; u0 += 4) {
-                    uint2 hx[4][ROUTER_RB];
+                for (int u0 = 0; u0 < ROUTER_WREG; u0 += ROUTER_LB) {
+                    uint2 hx[ROUTER_LB][ROUTER_RB];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < ROUTER_LB; ++u) {
                         const int c = lane + 32 * (u0 + u);
 #pragma unroll
                         for (int rb = 0; rb < ROUTER_RB; ++rb)
                             hx[u][rb] = (hv[rb] && c < d4) ? __ldg(hrow[rb] + c) : make_uint2(0u, 0u);
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
+                    for (int u = 0; u < ROUTER_LB; ++u)
 #pragma unroll
                         for (int rb = 0; rb < ROUTER_RB; ++rb) acc[rb] = dot4(wv[u0 + u], hx[u][rb], acc[rb]);
                 }

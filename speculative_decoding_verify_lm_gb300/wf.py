@@ -82,6 +82,9 @@ _SIGS = {
                              _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "wf_draft_topk": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p,
                              _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "wf_lmhead_draft_topk": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
+                                    _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
+                                    _c_void_p, _sz, _c_void_p]),
     "wf_round": (_i32, [ctypes.POINTER(RoundArgs), _c_void_p, _sz, _c_void_p]),
 }
 
@@ -325,6 +328,30 @@ def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, 
                              _check(vals, "vals", _F32), ws.ptr, ws.nbytes, _stream(stream))
     _raise(st, "wf_draft_topk")
     return draft_ids, tids, vals
+
+
+def wf_lmhead_draft_topk(hidden, W, x, Wd, d2t, k: int, ws: Workspace, ids=None, maxlogit=None, draft_ids=None,
+                         tids=None, vals=None, stream=None):
+    """Target argmax over the rows of hidden and draft top-k over the rows of x
+    in one weight sweep (at most 128 rows each)."""
+    P, d = hidden.shape
+    V = W.shape[0]
+    B = x.shape[0]
+    Vd = Wd.shape[0]
+    if x.shape[1] != d or W.shape[1] != d or Wd.shape[1] != d:
+        raise ValueError("hidden, W, x and Wd must share the hidden size d")
+    dev = hidden.device
+    ids = torch.empty(P, dtype=torch.int32, device=dev) if ids is None else ids
+    draft_ids = torch.empty((B, k), dtype=torch.int32, device=dev) if draft_ids is None else draft_ids
+    tids = torch.empty((B, k), dtype=torch.int32, device=dev) if tids is None else tids
+    vals = torch.empty((B, k), dtype=torch.float32, device=dev) if vals is None else vals
+    st = lib().wf_lmhead_draft_topk(_check(hidden, "hidden", _BF16), _check(W, "W", _BF16), P, d, V,
+                                    _check(ids, "ids", _I32), _check(maxlogit, "maxlogit", _F32, True),
+                                    _check(x, "x", _BF16), _check(Wd, "Wd", _BF16), _check(d2t, "d2t", _I32), B, Vd,
+                                    k, _check(draft_ids, "draft_ids", _I32), _check(tids, "tids", _I32),
+                                    _check(vals, "vals", _F32), ws.ptr, ws.nbytes, _stream(stream))
+    _raise(st, "wf_lmhead_draft_topk")
+    return ids, draft_ids, tids, vals
 
 
 def _packed(spec, device):

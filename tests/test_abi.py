@@ -61,6 +61,10 @@ NULL = None
     ("wf_router_mlp", (256, 256, 1, 64, 0, 256, 256, 256, 0.0, 1.0, 256, 256, 256, 1 << 20, NULL)),  # m = 0
     ("wf_draft_topk", (256, 256, 256, 1, 64, 100, 17, 256, 256, 256, 256, 1 << 20, NULL)),          # k > 16
     ("wf_draft_topk", (256, 256, 256, 1, 64, 5, 6, 256, 256, 256, 256, 1 << 20, NULL)),             # k > Vd
+    ("wf_lmhead_draft_topk", (256, 256, 4, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 0, NULL, 256, 256, 256,
+                              1 << 20, NULL)),                                                     # k = 0
+    ("wf_lmhead_draft_topk", (256, 256, 4, 64, 100, 256, NULL, 264, 256, 256, 1, 50, 4, NULL, 256, 256, 256,
+                              1 << 20, NULL)),                                                     # misaligned x
 ])
 def test_invalid_arguments_rejected_on_host(call, args):
     assert getattr(wf.lib(), call)(*args) == 1
@@ -70,6 +74,15 @@ def test_invalid_arguments_rejected_on_host(call, args):
 def test_workspace_checked_on_host(ws, nbytes):
     st = wf.lib().wf_lmhead_argmax(256, 256, 4, 64, 10, 256, NULL, ws, nbytes, NULL)
     assert st == 2
+
+
+def test_shared_sweep_limited_to_one_activation_tile():
+    # more than 128 rows in either head: unsupported, nothing enqueued (no device needed)
+    L = wf.lib()
+    assert L.wf_lmhead_draft_topk(256, 256, 129, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 4, NULL, 256, 256, 256,
+                                  1 << 20, NULL) == 4
+    assert L.wf_lmhead_draft_topk(256, 256, 128, 64, 100, 256, NULL, 256, 256, 256, 129, 50, 4, NULL, 256, 256,
+                                  256, 1 << 20, NULL) == 4
 
 
 def test_round_rejects_missing_tree_description():

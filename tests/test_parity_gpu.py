@@ -161,11 +161,10 @@ def test_router(B, d, m):
 
 
 # ------------------------------------------------------------------ draft head
-@pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
-                                      (1, 2560, 32000, 10)])
-def test_draft_topk(B, d, Vd, k):
-    # logit scale ~1 at d = 2560 (std 0.02), larger for the small shapes so that
-    # the top-(k+1) spacing clears the 1e-2 rule in a few draws
+def _draft_case(B, d, Vd, k):
+    """Draft weights, id map and inputs whose adjacent top-(k+1) logits are
+    >= 1e-2 apart, with the oracle's answer.  Logit scale ~1 at d = 2560 (std
+    0.02), larger for the small shapes so that the rule holds in a few draws."""
     Wd = synth.normal_bf16(Vd + d, 0, Vd, d, 0.02 if d >= 2560 else 4.0 / d ** 0.5)
     d2t = np.random.default_rng(Vd).permutation(151936)[:Vd].astype(np.int32)
     x = synth.normal_bf16(B + 1, 1, B, d, 1.0)
@@ -177,6 +176,13 @@ def test_draft_topk(B, d, Vd, k):
         for r in bad:
             x[r] = synth.hidden_row(B + 1, int(r), a, d)
     assert (mg >= synth.GAP_MIN).all(), "gap rule not met: expected ids would be stale"
+    return Wd, d2t, x, dids, tids, vals
+
+
+@pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
+                                      (1, 2560, 32000, 10)])
+def test_draft_topk(B, d, Vd, k):
+    Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
     ws = wf.Workspace(1, B, 1, Vd, k)
     for _ in range(2):
         gi, gt, gv = wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), k, ws)
@@ -186,6 +192,29 @@ def test_draft_topk(B, d, Vd, k):
         assert np.all(np.abs(host(gv) - vals) <= bound)
     assert ws.device_error() == (0, 0)
     assert not ws.buf.any().item()
+
+
+@pytest.mark.parametrize("P,B,d,V,Vd,k", [(17, 1, 256, 8192, 4000, 10), (128, 128, 64, 777, 300, 16),
+                                          (61, 2, 72, 1000, 129, 1), (1, 1, 2560, 151936, 32000, 10)])
+def test_lmhead_draft_topk_shared_sweep(P, B, d, V, Vd, k):
+    """Both heads in one sweep give the oracle's argmax and top-k (and leave the
+    workspace zeroed), here and on a reused workspace."""
+    W = synth.normal_bf16(7 + P, 0, V, d, 0.02 if d >= 256 else 0.1)
+    h = _gapped_hidden(11 + V, P, d, W)
+    ids_ref, mx_ref, _ = o().lmhead_argmax(h, W)
+    Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
+    ws = wf.Workspace(P, B, 1, Vd, k, d=d)
+    mx = torch.empty(P, dtype=torch.float32, device=DEV)
+    for _ in range(2):
+        ids, gi, gt, gv = wf.wf_lmhead_draft_topk(dev(h), dev(W), dev(x), dev(Wd), dev(d2t), k, ws, maxlogit=mx)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(ids), ids_ref)
+        assert np.all(np.abs(host(mx) - mx_ref) <= logit_error_bound(h, W, ids_ref))
+        assert np.array_equal(host(gi), dids) and np.array_equal(host(gt), tids)
+        bound = np.stack([logit_error_bound(x[b:b + 1].repeat(k, 0), Wd, dids[b]) for b in range(B)])
+        assert np.all(np.abs(host(gv) - vals) <= bound)
+    assert ws.device_error() == (0, 0)
+    assert not ws.buf.any().item(), "workspace must be left zeroed"
 
 
 def test_draft_topk_bad_map():
@@ -257,6 +286,26 @@ def test_round_batch256_sampled():
     xs = [0, 137, 255]
     dids, tids, _, _, _ = o().draft_topk(wl.x[xs], wl.Wd, wl.d2t, wl.topk)
     assert np.array_equal(out["draft_ids"][xs], dids) and np.array_equal(out["tids"][xs], tids)
+
+
+@pytest.mark.parametrize("kinds,K,d,V,Vd,k", [([1], 16, 128, 3000, 1000, 10), ([0, 1], 16, 64, 777, 301, 16),
+                                               ([0] * 8, 15, 72, 2049, 129, 1), ([0] * 7 + [1], 3, 256, 8192, 4000, 10)])
+def test_round_shared_sweep_with_draft(kinds, K, d, V, Vd, k):
+    """At most 128 verified rows and 128 sequences: the draft head shares the
+    LM head's weight sweep (W, then Wd) and its candidate lists are merged
+    after acceptance.  Ragged vocabularies; 128 rows exactly in one case."""
+    wl = synth.small_workload(500 + d + k, d=d, V=V, kinds=kinds, argmax_fn=oracle.argmax_fn, m=16, K=K,
+                              Vd=Vd, topk=k, router_fn=oracle.router_fn, topk_gap_fn=oracle.topk_gap_fn)
+    assert wl.P <= 128
+    r, out = round_on_gpu(wl)
+    assert r.ws.device_error() == (0, 0)
+    _compare_round(wl, out)
+    dids, tids, vals, _, _ = o().draft_topk(wl.x, wl.Wd, wl.d2t, wl.topk)
+    assert np.array_equal(out["draft_ids"], dids) and np.array_equal(out["tids"], tids)
+    assert np.max(np.abs(out["vals"] - vals)) <= 1e-3
+    out2 = {key: host(v) for key, v in r().items()}
+    for key in ("ids", "n_accept", "route", "draft_ids", "tids"):
+        assert np.array_equal(out2[key], out[key]), key
 
 
 def test_round_edge_shapes():
