@@ -205,6 +205,46 @@ class Oracle:
         assert rc == 0, rc
         return out
 
+    def rmsnorm(self, u, gamma, eps: float):
+        """u [din] bf16 bits, gamma [din] bf16 bits -> a f64 [din]."""
+        u = np.ascontiguousarray(u, np.uint16)
+        gamma = np.ascontiguousarray(gamma, np.uint16)
+        a = np.empty(u.shape[0], np.float64)
+        self.lib.oracle_rmsnorm(_p(u), ctypes.c_int64(u.shape[0]), _p(gamma), ctypes.c_double(eps), _p(a))
+        return a
+
+    def rope(self, x, pos: float, theta: float):
+        """x f64 [D] -> the rotated vector f64 [D]."""
+        x = np.ascontiguousarray(x, np.float64)
+        y = np.empty_like(x)
+        self.lib.oracle_rope(_p(x), ctypes.c_int(x.shape[0]), ctypes.c_double(pos), ctypes.c_double(theta), _p(y))
+        return y
+
+    def catchup(self, u, bl_off, cache_len, gamma, eps, theta, Wq, Wk, Wv, Wo, Kc, Vc, H: int, G: int):
+        """KV-only catch-up.  u [N, din], Wq [H*D, din], Wk / Wv [G*D, din], Wo [din, H*D], gamma [din],
+        caches Kc / Vc [B, cap, G*D] (all bf16 bits; the caches are copied, not modified) ->
+        dict(Kc, Vc, q [B, H*D], attn [B, H*D], out [B, din]) and rc (2: a sequence without backlog or
+        beyond its cache)."""
+        u = np.ascontiguousarray(u, np.uint16)
+        bl_off = np.ascontiguousarray(bl_off, np.int32)
+        cache_len = np.ascontiguousarray(cache_len, np.int32)
+        gamma = np.ascontiguousarray(gamma, np.uint16)
+        Wq, Wk, Wv, Wo = (np.ascontiguousarray(w, np.uint16) for w in (Wq, Wk, Wv, Wo))
+        Kc = np.array(Kc, np.uint16, copy=True, order="C")
+        Vc = np.array(Vc, np.uint16, copy=True, order="C")
+        B = len(bl_off) - 1
+        din = u.shape[1]
+        D = Wk.shape[0] // G
+        cap = Kc.shape[1]
+        assert Wq.shape == (H * D, din) and Wk.shape == (G * D, din) and Wv.shape == Wk.shape
+        assert Wo.shape == (din, H * D) and Kc.shape == (B, cap, G * D) and Vc.shape == Kc.shape
+        out = dict(Kc=Kc, Vc=Vc, q=np.empty((B, H * D)), attn=np.empty((B, H * D)), out=np.empty((B, din)))
+        rc = self.lib.oracle_catchup(_p(u), _p(bl_off), _p(cache_len), ctypes.c_int(B), ctypes.c_int64(din),
+                                     ctypes.c_int(H), ctypes.c_int(G), ctypes.c_int(D), _p(gamma),
+                                     ctypes.c_double(eps), ctypes.c_double(theta), _p(Wq), _p(Wk), _p(Wv), _p(Wo),
+                                     _p(Kc), _p(Vc), ctypes.c_int64(cap), _p(out["q"]), _p(out["attn"]),
+                                     _p(out["out"]))
+        return out, rc
 
 
 def default() -> Oracle:
@@ -249,6 +289,10 @@ def entropy(*a, **k):
 
 def round_(*a, **k):
     return default().round_(*a, **k)
+
+
+def catchup(*a, **k):
+    return default().catchup(*a, **k)
 
 
 # ---- adapters in the shape the input generator asks for --------------------------------

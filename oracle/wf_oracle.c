@@ -448,3 +448,157 @@ int oracle_round(const uint16_t* hidden, const uint16_t* W, int64_t d, int64_t V
     }
     return oracle_router(hidden, last_pos, B, d, m, W1, b1, w2, b2, tau, delta, route);
 }
+
+/* ------------------------------------------------------------------------
+ * KV-only catch-up of the autoregressive drafter (paper Sec. 3.4 "Lazy
+ * Catch-up" and "KV-only Prefill"): when the router switches to the EAGLE-3
+ * drafter, the tokens accepted while it was idle (the backlog) enter its KV
+ * cache in one batch; for them only the attention layer's keys and values
+ * are computed, and only the final backlog token runs through the layer in
+ * full.  The drafter is one Llama-style decoder layer (EAGLE3 card,
+ * "Technical Specifications": LlamaForCausalLMEagle3, 1 decoder layer,
+ * hidden 2560, 32 attention heads, 8 KV heads).  The steps of that layer's
+ * attention part, as used here:
+ *   a     = RMSNorm(u) * gamma                (pre-attention norm)
+ *   k     = rope(Wk a, pos),  v = Wv a         (per KV head, head size D)
+ *   q     = rope(Wq a, pos)                    (final token only)
+ *   o_h   = softmax_t(<q_h, K_g[t]> / sqrt D) V_g   over the whole cache,
+ *           query head h reading KV head g = h / (H / G)
+ *   out   = u + Wo o                           (residual; final token only)
+ * The cache holds bf16 values (the drafter runs in bf16, paper Sec. 4).
+ * ---------------------------------------------------------------------- */
+
+/* Round to the nearest bf16, ties to even (through the nearest binary32). */
+static uint16_t bf16_round(double x) {
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* RMSNorm: a[i] = u[i] / sqrt(mean_k u[k]^2 + eps) * gamma[i]. */
+void oracle_rmsnorm(const uint16_t* u, int64_t din, const uint16_t* gamma, double eps, double* a) {
+    double ss = 0.0;
+    for (int64_t i = 0; i < din; ++i) ss += bf16_value(u[i]) * bf16_value(u[i]);
+    const double r = 1.0 / sqrt(ss / (double)din + eps);
+    for (int64_t i = 0; i < din; ++i) a[i] = bf16_value(u[i]) * r * bf16_value(gamma[i]);
+}
+
+/*
+ * Rotary position embedding of one head vector x[D] at position pos: the
+ * pair (x[i], x[i + D/2]) turns by the angle pos * theta^(-2i/D), i < D/2
+ * (the "rotate half" pairing of Llama-style layers).
+ */
+void oracle_rope(const double* x, int D, double pos, double theta, double* y) {
+    const int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+        const double ang = pos * pow(theta, -2.0 * (double)i / (double)D);
+        const double c = cos(ang), s = sin(ang);
+        const double x1 = x[i], x2 = x[i + half];
+        y[i] = x1 * c - x2 * s;
+        y[i + half] = x2 * c + x1 * s;
+    }
+}
+
+/* <W[row], a> for a bf16 weight row and a double vector, summed in index order. */
+static double row_dot(const uint16_t* w, const double* a, int64_t n) {
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += bf16_value(w[i]) * a[i];
+    return s;
+}
+
+/*
+ * Catch-up of B sequences.  Sequence b has n_b = bl_off[b+1] - bl_off[b] >= 1
+ * backlog tokens with layer inputs u[bl_off[b] + j] ([N, din] bf16) and
+ * L_b = cache_len[b] entries already in its caches Kc, Vc ([B, cap, G*D] bf16,
+ * KV head g at columns g*D ..).  Backlog token j sits at position L_b + j;
+ * its key and value go to cache row L_b + j.  For the final token
+ * (j = n_b - 1): q[b] ([B, H*D], may be NULL) after the rotation, attn[b]
+ * ([B, H*D], may be NULL) the attention output over cache rows
+ * 0 .. L_b + n_b - 1, and out[b] ([B, din]) = u_final + Wo attn.
+ * Wq [H*D, din], Wk / Wv [G*D, din], Wo [din, H*D], gamma [din], all bf16.
+ * Returns 2 if a sequence has no backlog or does not fit its cache.
+ */
+int oracle_catchup(const uint16_t* u, const int32_t* bl_off, const int32_t* cache_len, int B, int64_t din, int H,
+                   int G, int D, const uint16_t* gamma, double eps, double theta, const uint16_t* Wq,
+                   const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo, uint16_t* Kc, uint16_t* Vc,
+                   int64_t cap, double* q, double* attn, double* out) {
+    if (!u || !bl_off || !cache_len || !gamma || !Wq || !Wk || !Wv || !Wo || !Kc || !Vc || !out) return 1;
+    if (B < 0 || din < 1 || H < 1 || G < 1 || H % G || D < 2 || D % 2) return 1;
+    for (int b = 0; b < B; ++b) {
+        const int64_t n = bl_off[b + 1] - bl_off[b];
+        if (n < 1 || cache_len[b] < 0 || cache_len[b] + n > cap) return 2;
+    }
+    const int64_t GD = (int64_t)G * D, HD = (int64_t)H * D;
+    const int64_t N = bl_off[B];
+    /* keys and values of every backlog token (independent rows) */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < N; ++r) {
+        int b = 0;
+        while (bl_off[b + 1] <= r) ++b;
+        const int64_t pos = cache_len[b] + (r - bl_off[b]);
+        double* a = (double*)malloc((size_t)din * sizeof(double));
+        double* kh = (double*)malloc((size_t)D * sizeof(double));
+        double* kr = (double*)malloc((size_t)D * sizeof(double));
+        oracle_rmsnorm(u + r * din, din, gamma, eps, a);
+        uint16_t* krow = Kc + ((int64_t)b * cap + pos) * GD;
+        uint16_t* vrow = Vc + ((int64_t)b * cap + pos) * GD;
+        for (int g = 0; g < G; ++g) {
+            for (int e = 0; e < D; ++e) kh[e] = row_dot(Wk + ((int64_t)g * D + e) * din, a, din);
+            oracle_rope(kh, D, (double)pos, theta, kr);
+            for (int e = 0; e < D; ++e) {
+                krow[(int64_t)g * D + e] = bf16_round(kr[e]);
+                vrow[(int64_t)g * D + e] = bf16_round(row_dot(Wv + ((int64_t)g * D + e) * din, a, din));
+            }
+        }
+        free(a); free(kh); free(kr);
+    }
+    /* the final backlog token of each sequence, through the attention sublayer */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        const int64_t f = bl_off[b + 1] - 1;
+        const int64_t T = cache_len[b] + (bl_off[b + 1] - bl_off[b]);
+        const double pos = (double)(T - 1);
+        double* a = (double*)malloc((size_t)din * sizeof(double));
+        double* qb = (double*)malloc((size_t)HD * sizeof(double));
+        double* ob = (double*)malloc((size_t)HD * sizeof(double));
+        double* tmp = (double*)malloc((size_t)D * sizeof(double));
+        double* sc = (double*)malloc((size_t)T * sizeof(double));
+        oracle_rmsnorm(u + f * din, din, gamma, eps, a);
+        for (int h = 0; h < H; ++h) {
+            for (int e = 0; e < D; ++e) tmp[e] = row_dot(Wq + ((int64_t)h * D + e) * din, a, din);
+            oracle_rope(tmp, D, pos, theta, qb + (int64_t)h * D);
+        }
+        for (int h = 0; h < H; ++h) {
+            const int g = h / (H / G);
+            const double* qh = qb + (int64_t)h * D;
+            double mx = -INFINITY;
+            for (int64_t t = 0; t < T; ++t) {
+                const uint16_t* kt = Kc + ((int64_t)b * cap + t) * GD + (int64_t)g * D;
+                double s = 0.0;
+                for (int e = 0; e < D; ++e) s += qh[e] * bf16_value(kt[e]);
+                sc[t] = s / sqrt((double)D);
+                if (sc[t] > mx) mx = sc[t];
+            }
+            double Z = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                sc[t] = exp(sc[t] - mx);
+                Z += sc[t];
+            }
+            for (int e = 0; e < D; ++e) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < T; ++t)
+                    acc += sc[t] * bf16_value(Vc[((int64_t)b * cap + t) * GD + (int64_t)g * D + e]);
+                ob[(int64_t)h * D + e] = acc / Z;
+            }
+        }
+        for (int64_t i = 0; i < din; ++i)
+            out[(int64_t)b * din + i] = bf16_value(u[f * din + i]) + row_dot(Wo + i * HD, ob, HD);
+        if (q) memcpy(q + (int64_t)b * HD, qb, (size_t)HD * sizeof(double));
+        if (attn) memcpy(attn + (int64_t)b * HD, ob, (size_t)HD * sizeof(double));
+        free(a); free(qb); free(ob); free(tmp); free(sc);
+    }
+    return 0;
+}

@@ -458,8 +458,178 @@ def check_build_tree(o):
     assert o.build_tree(np.zeros((1, 2, 2, 2), np.int32), bad, 3)[4] == 2
 
 
+# ---------------------------------------------------------------- KV-only catch-up
+def check_rmsnorm(o):
+    """Hand-worked: u = (3, 4, 0, 0), unit gain, eps = 0 -> rms 2.5 -> (1.2, 1.6, 0, 0).
+    Constant input c: every element is gamma_i * c / sqrt(c^2 + eps) (eps inside the root);
+    with eps = 0 the result does not change when u doubles."""
+    one = to_bf16_bits(np.ones(4, np.float32))
+    a = o.rmsnorm(to_bf16_bits(np.array([3, 4, 0, 0], np.float32)), one, 0.0)
+    assert np.allclose(a, [1.2, 1.6, 0.0, 0.0], rtol=1e-15, atol=0)
+    rng = np.random.default_rng(40)
+    gamma = _rand_bf16(rng, 16, 1.0)
+    for c, eps in ((1.5, 0.0), (-0.375, 1e-6), (0.0078125, 0.25)):
+        a = o.rmsnorm(to_bf16_bits(np.full(16, c, np.float32)), gamma, eps)
+        assert np.allclose(a, _f64(gamma) * c / math.sqrt(c * c + eps), rtol=1e-14, atol=0)
+    u = _rand_bf16(rng, 16, 1.0)
+    assert np.allclose(o.rmsnorm(u, gamma, 0.0), o.rmsnorm(to_bf16_bits(_f64(u) * 2), gamma, 0.0), rtol=1e-14)
+
+
+def check_rope(o):
+    """Basis vectors: with theta = 10^4 and D = 8 the pair frequencies are 1, 10^-1,
+    10^-2, 10^-3, so e_0 at position p turns to (cos p) e_0 + (sin p) e_4 and e_2 at
+    p = 100 to (cos 1) e_2 + (sin 1) e_6.  Position 0 is the identity; turning by a
+    then b is turning by a + b; scores depend only on the distance of the positions."""
+    th, D = 1e4, 8
+    for p in (0.0, 1.0, 2.5, 1000.0):
+        y = o.rope(np.eye(D)[0], p, th)
+        assert np.allclose(y, np.cos(p) * np.eye(D)[0] + np.sin(p) * np.eye(D)[4], atol=1e-13)
+    y = o.rope(np.eye(D)[2], 100.0, th)
+    assert np.allclose(y, np.cos(1.0) * np.eye(D)[2] + np.sin(1.0) * np.eye(D)[6], atol=1e-12)
+    y = o.rope(np.eye(D)[7], 5000.0, th)       # frequency 10^-3: angle 5, second member of the pair
+    assert np.allclose(y, np.cos(5.0) * np.eye(D)[7] - np.sin(5.0) * np.eye(D)[3], atol=1e-12)
+    rng = np.random.default_rng(41)
+    x, k = rng.standard_normal(D), rng.standard_normal(D)
+    assert np.allclose(o.rope(x, 0.0, th), x, atol=0)
+    assert np.allclose(o.rope(o.rope(x, 3.0, th), 11.0, th), o.rope(x, 14.0, th), atol=1e-12)
+    for m, n in ((5, 2), (40, 33), (7, 7)):
+        assert np.isclose(o.rope(x, m, th) @ o.rope(k, n, th), o.rope(x, m - n, th) @ k, atol=1e-12)
+
+
+def catchup_case(seed, din=16, H=4, G=2, D=4, n=(3, 1), L=(2, 0), cap=8, theta=1e4, eps=1e-6):
+    """A small random catch-up problem (weights ~N(0, 1/din), inputs ~N(0, 1))."""
+    rng = np.random.default_rng(seed)
+    B = len(n)
+    bl_off = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    c = dict(u=_rand_bf16(rng, (int(bl_off[-1]), din), 1.0), bl_off=bl_off, cache_len=np.array(L, np.int32),
+             gamma=to_bf16_bits((1.0 + 0.1 * rng.standard_normal(din)).astype(np.float32)), eps=eps, theta=theta,
+             Wq=_rand_bf16(rng, (H * D, din), din ** -0.5), Wk=_rand_bf16(rng, (G * D, din), din ** -0.5),
+             Wv=_rand_bf16(rng, (G * D, din), din ** -0.5), Wo=_rand_bf16(rng, (din, H * D), (H * D) ** -0.5),
+             Kc=_rand_bf16(rng, (B, cap, G * D), 1.0), Vc=_rand_bf16(rng, (B, cap, G * D), 1.0), H=H, G=G)
+    return c
+
+
+def check_catchup_single_entry(o):
+    """An empty cache and one backlog token: every head attends to that token alone,
+    so its output is the token's own cached value; with Wo = 0 the output is the input."""
+    c = catchup_case(42, n=(1,), L=(0,))
+    c["Wo"] = np.zeros_like(c["Wo"])
+    r, rc = o.catchup(**c)
+    assert rc == 0
+    D = c["Wk"].shape[0] // c["G"]
+    for h in range(c["H"]):
+        g = h // (c["H"] // c["G"])
+        assert np.allclose(r["attn"][0, h * D:(h + 1) * D], _f64(r["Vc"][0, 0, g * D:(g + 1) * D]), atol=1e-15)
+    assert np.array_equal(r["out"][0], _f64(c["u"][0]))
+
+
+def check_catchup_two_entries(o):
+    """Two cache rows (one cached, one new): each head's output is the logistic mix
+    s(x) v0 + s(-x) v1 with x = (<q, k0> - <q, k1>) / 2 (D = 4, so sqrt D = 2);
+    identical keys give the mean of the two values."""
+    c = catchup_case(43, n=(1,), L=(1,), H=2, G=1)
+    r, rc = o.catchup(**c)
+    assert rc == 0
+    D = 4
+    k = _f64(r["Kc"][0, :2]).reshape(2, 1, D)
+    v = _f64(r["Vc"][0, :2]).reshape(2, 1, D)
+    for h in range(2):
+        q = r["q"][0, h * D:(h + 1) * D]
+        x = (q @ k[0, 0] - q @ k[1, 0]) / 2.0
+        w0 = 1.0 / (1.0 + math.exp(-x))
+        assert np.allclose(r["attn"][0, h * D:(h + 1) * D], w0 * v[0, 0] + (1 - w0) * v[1, 0], atol=1e-12)
+    c2 = catchup_case(44, n=(1,), L=(1,), H=2, G=1)
+    # a zero key projection and a zero cached key: every score is 0, equal weights
+    c2["Wk"] = np.zeros_like(c2["Wk"])
+    c2["Kc"] = np.zeros_like(c2["Kc"])
+    r, rc = o.catchup(**c2)
+    mean = (_f64(r["Vc"][0, 0]) + _f64(r["Vc"][0, 1])) / 2
+    assert np.allclose(r["attn"][0, :D], mean, atol=1e-14) and np.allclose(r["attn"][0, D:], mean, atol=1e-14)
+
+
+def check_catchup_head_groups(o):
+    """8 query heads over 2 KV heads: heads 0-3 read KV head 0, heads 4-7 KV head 1.
+    A KV head whose values are all zero silences exactly its own group."""
+    c = catchup_case(45, H=8, G=2, D=4, n=(2,), L=(3,))
+    D = 4
+    c["Vc"][:, :, D:] = 0
+    c["Wv"][D:] = 0
+    r, rc = o.catchup(**c)
+    assert rc == 0
+    assert np.all(r["attn"][0, 4 * D:] == 0) and np.all(np.abs(r["attn"][0, :4 * D]).max() > 0)
+
+
+def check_catchup_lazy_equals_eager(o):
+    """Lazy catch-up leaves the result unchanged (paper Sec. 4, Table 3: the accepted
+    tokens are identical): entering the backlog in one batch gives the same caches and
+    final output as entering it one token at a time.  Rows outside the backlog are
+    untouched."""
+    c = catchup_case(46, n=(3, 1, 4), L=(2, 0, 1), cap=6)
+    batch, rc = o.catchup(**c)
+    assert rc == 0
+    Kc, Vc = c["Kc"].copy(), c["Vc"].copy()
+    L = c["cache_len"].copy()
+    out_last = {}
+    for b in range(3):
+        for j in range(int(c["bl_off"][b]), int(c["bl_off"][b + 1])):
+            one = dict(c, u=c["u"][j:j + 1], bl_off=np.array([0, 1], np.int32), cache_len=L[b:b + 1],
+                       Kc=Kc[b:b + 1], Vc=Vc[b:b + 1])
+            r, rc = o.catchup(**one)
+            assert rc == 0
+            Kc[b], Vc[b] = r["Kc"][0], r["Vc"][0]
+            L[b] += 1
+            out_last[b] = r["out"][0]
+    assert np.array_equal(Kc, batch["Kc"]) and np.array_equal(Vc, batch["Vc"])
+    for b in range(3):
+        assert np.allclose(out_last[b], batch["out"][b], rtol=0, atol=1e-13)
+        end = int(c["cache_len"][b] + c["bl_off"][b + 1] - c["bl_off"][b])
+        assert np.array_equal(batch["Kc"][b, :c["cache_len"][b]], c["Kc"][b, :c["cache_len"][b]])
+        assert np.array_equal(batch["Kc"][b, end:], c["Kc"][b, end:])
+
+
+def check_catchup_final_query(o):
+    """With Wq = Wk and one query head per KV head, the final token's rotated query,
+    rounded to bf16, is the key it wrote at its own position L + n - 1.  Identity
+    value weights (G D = din) cache the normalised input itself."""
+    c = catchup_case(47, din=8, H=2, G=2, D=4, n=(3, 2), L=(1, 4), cap=8)
+    c["Wq"] = c["Wk"].copy()
+    c["Wv"] = to_bf16_bits(np.eye(8, dtype=np.float32))
+    r, rc = o.catchup(**c)
+    assert rc == 0
+    for b, (L, n) in enumerate(((1, 3), (4, 2))):
+        assert np.array_equal(to_bf16_bits(r["q"][b].astype(np.float32)), r["Kc"][b, L + n - 1])
+        f = int(c["bl_off"][b + 1]) - 1
+        a = o.rmsnorm(c["u"][f], c["gamma"], c["eps"])
+        assert np.array_equal(r["Vc"][b, L + n - 1], to_bf16_bits(a.astype(np.float32)))
+
+
+def check_catchup_output_projection(o):
+    """Wo maps the attention output (H D wide) to the layer width din, out x in: with a
+    single unit weight at (row 0, column 5) the output is the input plus attn[5] in
+    element 0, and the input unchanged everywhere else."""
+    c = catchup_case(49, din=16, H=4, G=2, D=4, n=(2,), L=(1,))
+    Wo = np.zeros((16, 16), np.float32)
+    Wo[0, 5] = 1.0
+    c["Wo"] = to_bf16_bits(Wo)
+    r, rc = o.catchup(**c)
+    assert rc == 0
+    u = _f64(c["u"][1])
+    assert r["out"][0, 0] == u[0] + r["attn"][0, 5]
+    assert np.array_equal(r["out"][0, 1:], u[1:])
+
+
+def check_catchup_rejects_overflow(o):
+    """A backlog that does not fit the cache, or an empty one, is refused."""
+    c = catchup_case(48, n=(3,), L=(6,), cap=8)
+    assert o.catchup(**c)[1] == 2
+    c = catchup_case(48, n=(0, 2), L=(0, 0), cap=8)
+    assert o.catchup(**c)[1] == 2
+
+
 ALL_CHECKS = [check_argmax_bruteforce, check_argmax_ties, check_argmax_closed_form, check_chain_golden,
               check_tree_golden, check_tree_bruteforce, check_chain_is_linear_tree, check_tree_bad_parent,
               check_gelu_values, check_router_closed_forms, check_route_strict, check_topk_bruteforce,
               check_topk_ties, check_entropy, check_entropy_route_strict, check_accepted_rows,
-              check_build_tree]
+              check_build_tree, check_rmsnorm, check_rope, check_catchup_single_entry, check_catchup_two_entries,
+              check_catchup_head_groups, check_catchup_lazy_equals_eager, check_catchup_final_query,
+              check_catchup_output_projection, check_catchup_rejects_overflow]

@@ -61,6 +61,39 @@ MUTANTS = [
      "return (x->idx < y->idx) - (x->idx > y->idx);\n}\n\nint oracle_build_tree", [pins.check_build_tree]),
     ("top-k maps through the wrong id", "tids[(int64_t)b * k + j] = d2t[s[j].id];",
      "tids[(int64_t)b * k + j] = s[j].id;", [pins.check_topk_bruteforce]),
+    ("RMSNorm with eps outside the root", "const double r = 1.0 / sqrt(ss / (double)din + eps);",
+     "const double r = 1.0 / (sqrt(ss / (double)din) + eps);", [pins.check_rmsnorm]),
+    ("RMSNorm over the sum, not the mean", "const double r = 1.0 / sqrt(ss / (double)din + eps);",
+     "const double r = 1.0 / sqrt(ss + eps);", [pins.check_rmsnorm]),
+    ("rotation turns the wrong way", "y[i] = x1 * c - x2 * s;\n        y[i + half] = x2 * c + x1 * s;",
+     "y[i] = x1 * c + x2 * s;\n        y[i + half] = x2 * c - x1 * s;", [pins.check_rope]),
+    ("rotation frequencies theta^(-i/D)", "pow(theta, -2.0 * (double)i / (double)D)",
+     "pow(theta, -(double)i / (double)D)", [pins.check_rope]),
+    ("rotation pairs neighbours (2i, 2i+1)", "const double x1 = x[i], x2 = x[i + half];\n        y[i] = x1 * c - x2 * s;\n        y[i + half] = x2 * c + x1 * s;",
+     "const double x1 = x[2 * i], x2 = x[2 * i + 1];\n        y[2 * i] = x1 * c - x2 * s;\n        y[2 * i + 1] = x2 * c + x1 * s;",
+     [pins.check_rope]),
+    ("query head h reads KV head h mod G", "const int g = h / (H / G);", "const int g = h % G;",
+     [pins.check_catchup_head_groups, pins.check_catchup_single_entry]),
+    ("scores not scaled by 1/sqrt(D)", "sc[t] = s / sqrt((double)D);", "sc[t] = s;",
+     [pins.check_catchup_two_entries]),
+    ("backlog positions ignore the cached length", "const int64_t pos = cache_len[b] + (r - bl_off[b]);",
+     "const int64_t pos = r - bl_off[b];", [pins.check_catchup_lazy_equals_eager]),
+    ("final query rotated one position late", "const double pos = (double)(T - 1);", "const double pos = (double)T;",
+     [pins.check_catchup_final_query]),
+    ("final token taken from the start of the backlog", "const int64_t f = bl_off[b + 1] - 1;",
+     "const int64_t f = bl_off[b];", [pins.check_catchup_final_query, pins.check_catchup_lazy_equals_eager]),
+    ("final token does not attend to itself",
+     "const int64_t T = cache_len[b] + (bl_off[b + 1] - bl_off[b]);",
+     "const int64_t T = cache_len[b] + (bl_off[b + 1] - bl_off[b]) - 1;",
+     [pins.check_catchup_two_entries, pins.check_catchup_single_entry]),
+    ("residual dropped", "out[(int64_t)b * din + i] = bf16_value(u[f * din + i]) + row_dot(Wo + i * HD, ob, HD);",
+     "out[(int64_t)b * din + i] = row_dot(Wo + i * HD, ob, HD);", [pins.check_catchup_single_entry]),
+    ("output projection reads Wo transposed", "row_dot(Wo + i * HD, ob, HD)", "row_dot(Wo + i, ob, HD)",
+     [pins.check_catchup_output_projection]),
+    ("value projection applied without the norm",
+     "vrow[(int64_t)g * D + e] = bf16_round(row_dot(Wv + ((int64_t)g * D + e) * din, a, din));",
+     "vrow[(int64_t)g * D + e] = bf16_round(row_dot(Wv + ((int64_t)g * D + e) * din, a, din) / bf16_value(gamma[0]));",
+     [pins.check_catchup_final_query]),
 ]
 
 
