@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct wf_round calls instead of a CUDA graph")
+    ap.add_argument("--catchup", type=int, default=None,
+                    help="time the drafter's KV-only catch-up on this workload (index 0-3) instead of a round")
     return ap.parse_args()
 
 
@@ -81,41 +83,80 @@ def allreduce_sum(pg, value: float, device) -> float:
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """SM clock and clock-event (throttle) reasons of one GPU, read while the timed
+    region runs: NVML (read-only queries through ctypes) polled in a loop while the
+    host waits for the region's last event, else nvidia-smi every 200 ms."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.proc = None
+    def __init__(self, gpu_uuid):
+        import ctypes
+        self.ct = ctypes
+        self.sm, self.mx, self.reasons = [], [], set()
+        self.nvml = self.handle = self.proc = None
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=subprocess.PIPE,
-                                         stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if lib.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(h)) == 0:
+                    self.nvml, self.handle = lib, h
+                    fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                    self.reason_fn = fn or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is None:
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                              "-lms", "200", "-i", gpu_uuid], stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+
+    def sample(self):
+        if self.nvml is None:
+            return
+        ct = self.ct
+        c, m, r = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(c)) == 0:          # NVML_CLOCK_SM
+            self.sm.append(float(c.value))
+        if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ct.byref(m)) == 0:
+            self.mx.append(float(m.value))
+        if self.reason_fn(self.handle, ct.byref(r)) == 0:
+            for bit, name in self.REASONS.items():
+                if r.value & bit:
+                    self.reasons.add(name)
+
+    def wait(self, event):
+        """Sample until `event` (the timed region's last event) has completed."""
+        while not event.query():
+            self.sample()
+            time.sleep(0.0002)
+        self.sample()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        sm, mx, reasons = [], [], set()
-        for ln in out.splitlines():
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 7:
-                continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for name, v in zip(self.NAMES, f[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self.proc is not None:
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            for ln in out.splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                if len(f) < 7:
+                    continue
+                try:
+                    self.sm.append(float(f[0]))
+                    self.mx.append(float(f[1]))
+                except ValueError:
+                    continue
+                for name, v in zip(self.NAMES, f[3:7]):
+                    if v.lower().startswith("active"):
+                        self.reasons.add(name)
+        src = "nvml" if self.nvml is not None else ("nvidia-smi" if self.proc is not None else "unavailable")
+        return {"sm_mhz": statistics.median(self.sm) if self.sm else None,
+                "sm_max_mhz": max(self.mx) if self.mx else None, "reasons": sorted(self.reasons),
+                "samples": len(self.sm), "source": src}
 
 
 KERNEL_SOURCES = {"gemm_select_kernel<1>": ("wf_gemm_select.cu", "wf_internal.cuh"),
@@ -220,10 +261,157 @@ def run_reference(args, cfg_name, wl):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- KV-only catch-up
+def run_catchup_reference(args):
+    """The oracle's catch-up, timed on the host cores (the reference arm of --catchup)."""
+    import oracle
+    from speculative_decoding_verify_lm_gb300 import synth
+    cfg = synth.CATCHUP_CONFIGS[args.catchup]
+    c = synth.catchup_workload(args.catchup)
+    for _ in range(args.warmup):
+        oracle.catchup(**c)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.catchup(**c)
+    dt = time.perf_counter() - t0
+    N = int(c["bl_off"][-1])
+    val = N * args.steps / dt
+    print(json.dumps({"impl": "reference", "metric": "KV-only catch-up: backlog tokens entered per second",
+                      "value": val, "unit": "backlog tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                      "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": {"workload": cfg.name},
+                      "cpu_baseline": {"value": val, "unit": "backlog tokens/s", "cores": oracle.threads(),
+                                       "kind": "oracle", "sample": "whole oracle catch-up calls of this workload"},
+                      "e2e": {"value": val, "unit": "backlog tokens/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}), flush=True)
+
+
+
+def catchup_work(c):
+    """Algorithmic bytes and flops of one catch-up call."""
+    N, din = c["u"].shape
+    B = len(c["bl_off"]) - 1
+    GD, HD = c["Wk"].shape[0], c["Wq"].shape[0]
+    T = int(sum(int(L) + int(c["bl_off"][b + 1] - c["bl_off"][b]) for b, L in enumerate(c["cache_len"])))
+    weights = 2 * (2 * GD * din + 2 * HD * din + din)
+    nbytes = weights + 2 * N * din + 2 * 2 * N * GD + 2 * 2 * T * GD + 4 * B * din + 4 * B * HD + 4 * (2 * B + 1)
+    flops = 2.0 * N * din * 2 * GD + 2.0 * B * din * HD + 4.0 * T * HD + 2.0 * B * HD * din
+    return nbytes, flops, T
+
+
+def run_catchup(args, rank, local, pg):
+    import torch
+    from speculative_decoding_verify_lm_gb300 import synth, wf
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    cfg = synth.CATCHUP_CONFIGS[args.catchup]
+    c = synth.catchup_workload(args.catchup)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16  # noqa: E731
+                                   else np.ascontiguousarray(a)).to(device)
+    Kc, Vc = t(c["Kc"]), t(c["Vc"])
+    u = t(c["u"])
+    cu = wf.Catchup(u, t(c["bl_off"]), t(c["cache_len"]), t(c["gamma"]), t(c["Wk"]), t(c["Wv"]), Kc, Vc, c["G"],
+                    Wq=t(c["Wq"]), Wo=t(c["Wo"]), eps=c["eps"], theta=c["theta"])
+    stream = torch.cuda.current_stream(device)
+    l2buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    for _ in range(max(args.warmup, 3)):
+        cu()
+    torch.cuda.synchronize(device)
+    code, info = cu.ws.device_error()
+    if code:
+        raise RuntimeError(f"device error {code} (info {info}) during warm-up")
+    step = cu
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cu()
+        step = g.replay
+        step()
+    torch.cuda.synchronize(device)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        l2buf.zero_()   # weights and caches come from HBM every call
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    sampler.wait(ev[-1][1])
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    ms_mean = statistics.mean(ms)
+    N = int(c["bl_off"][-1])
+    B = len(cfg.n)
+    nbytes, flops, T = catchup_work(c)
+    hbm_peak, tc_peak, peak_src = measured_peaks()
+    achieved = nbytes / (ms_mean / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "traffic": None, "kernel": "catch-up call (norm, projections, attention, output projection)",
+            "algorithmic_per_launch": nbytes, "launch_ms": ms_mean,
+            "flops_per_call": flops, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
+    # end to end: the backlog's layer inputs in from pinned host memory, the output back
+    h_u = torch.empty(u.shape, dtype=u.dtype, pin_memory=True)
+    h_u.copy_(u)
+    h_out = torch.empty(cu.out.shape, dtype=cu.out.dtype, pin_memory=True)
+    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for _ in range(2):
+        u.copy_(h_u, non_blocking=True)
+        step()
+        h_out.copy_(cu.out, non_blocking=True)
+    torch.cuda.synchronize(device)
+    e2e_ev[0].record(stream)
+    for _ in range(args.steps):
+        u.copy_(h_u, non_blocking=True)
+        step()
+        h_out.copy_(cu.out, non_blocking=True)
+    e2e_ev[1].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_s = e2e_ev[0].elapsed_time(e2e_ev[1]) / 1e3
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        import oracle
+        oracle.catchup(**c)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 30.0) or reps == 0:
+            oracle.catchup(**c)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": N * reps / dt, "unit": "backlog tokens/s", "cores": oracle.threads(), "kind": "oracle",
+               "sample": f"{reps} whole oracle catch-up call(s) of this workload"}
+    line = {"metric": "KV-only catch-up: backlog tokens entered per second; % of HBM roofline",
+            "value": N * args.steps / (sum(ms) / 1e3), "unit": "backlog tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "B": B, "backlog": list(cfg.n), "cache_len": list(cfg.L),
+                       "din": cfg.din, "H": cfg.H, "G": cfg.G, "D": cfg.D,
+                       "l2": "L2 flushed (256 MB write) before every call",
+                       "launch": "wf_catchup captured in a CUDA graph" if not args.no_graph else "direct calls"},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": N * args.steps / e2e_s, "unit": "backlog tokens/s",
+                    "h2d_bytes_per_step": int(h_u.numel() * h_u.element_size()),
+                    "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size())},
+            "clocks": clocks, "gpu_launches": 4 * args.steps, "impl": "ours"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     args = parse()
     world, rank, local, pg = dist_setup(args)
+    if args.catchup is not None:
+        if args.impl == "reference":
+            if rank == 0:
+                run_catchup_reference(args)
+            return
+        run_catchup(args, rank, local, pg)
+        return
     from speculative_decoding_verify_lm_gb300 import synth
     cfg = synth.CONFIGS[args.config]
     cfg_name = cfg.name if args.router_width is None else f"{cfg.name}_m{args.router_width}"
@@ -305,6 +493,7 @@ def main():
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
+    sampler.wait(ev[-1][1])
     torch.cuda.synchronize(device)
     if pg is not None:
         pg.barrier()
@@ -348,6 +537,12 @@ def main():
         alg_flops = 2.0 * P * V * d
         kernel_name = "gemm_select_kernel<1>"
     for _ in range(3):
+        kernel_call()
+    if not args.no_graph:   # replayed from a CUDA graph: host argument checks stay out of the events
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg):
+            kernel_call()
+        kernel_call = kg.replay
         kernel_call()
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):

@@ -16,6 +16,7 @@
  *   wf_draft_topk     EAGLE-3 draft head, top-k, draft-to-target id map
  *   wf_lmhead_draft_topk  the target and draft heads in one weight sweep
  *   wf_round          all of the above as one stream-ordered round
+ *   wf_catchup        KV-only catch-up of the EAGLE-3 drafter after a switch
  *
  * Conventions shared by every call
  * - Pointers named as device buffers must be device (or managed) memory
@@ -372,6 +373,61 @@ typedef struct wf_round_args {
 #define WF_ROUTER_ENTROPY 1
 
 WF_API wf_status wf_round(const wf_round_args* args, void* ws, size_t ws_bytes, wf_stream_t stream);
+
+/*
+ * KV-only catch-up of the autoregressive drafter (paper Sec. 3.4, "Lazy
+ * Catch-up" and "KV-only Prefill"): after a switch to the EAGLE-3 drafter,
+ * the tokens accepted while it was idle (its backlog) enter its KV cache in
+ * one batch.  For every backlog token only the keys and values of the
+ * drafter's attention layer are computed; only the final backlog token runs
+ * through the attention sublayer in full, so that its state can feed the
+ * next draft round.  The drafter is one Llama-style decoder layer (EAGLE3
+ * card, "Technical Specifications": hidden 2560, 32 attention heads, 8 KV
+ * heads; head size D = 2560 / 32 = 80).  Per backlog token j of sequence b,
+ * at position pos = cache_len[b] + j:
+ *   a      = u / sqrt(mean(u^2) + eps) * gamma                 (RMSNorm)
+ *   Kc[b, pos] = rope(Wk a, pos),  Vc[b, pos] = Wv a            (bf16)
+ * rope turns each pair (x[i], x[i + D/2]) of a head by pos * theta^(-2i/D).
+ * For the final token f of each sequence (wf_catchup only):
+ *   q      = rope(Wq a_f, pos_f)
+ *   attn_h = softmax_t(<q_h, Kc[b, t, g]> / sqrt D) Vc[b, t, g],
+ *            t < cache_len[b] + n_b, KV head g = h / (H / G)
+ *   out[b] = u_f + Wo attn                                      (residual)
+ * The MLP of the final token is the drafter's ordinary decode step and is not
+ * part of this call.
+ */
+typedef struct wf_catchup_args {
+    const uint16_t* u;         /* [N, din] bf16: the backlog tokens' layer inputs, sequences packed */
+    const int32_t* bl_off;     /* [B+1] backlog offsets: bl_off[0] = 0, bl_off[B] = N, n_b >= 1 */
+    const int32_t* cache_len;  /* [B] entries already in each sequence's caches */
+    int B, N, din;             /* din % 8 == 0, 8 <= din <= 16384 */
+    int H, G, D;               /* query heads, KV heads (H % G == 0), head size (D % 16 == 0, <= 256) */
+    const uint16_t* gamma;     /* [din] bf16 RMSNorm gain */
+    float eps, theta;          /* RMSNorm epsilon (>= 0), rotary base (> 0) */
+    const uint16_t* Wq;        /* [H*D, din] bf16 (out x in) */
+    const uint16_t* Wk;        /* [G*D, din] bf16 */
+    const uint16_t* Wv;        /* [G*D, din] bf16 */
+    const uint16_t* Wo;        /* [din, H*D] bf16 */
+    uint16_t* Kc;              /* [B, cap, G*D] bf16 key cache (rotated keys), in/out */
+    uint16_t* Vc;              /* [B, cap, G*D] bf16 value cache, in/out */
+    int cap;                   /* cache rows per sequence */
+    float* out;                /* [B, din] fp32 out (wf_catchup) */
+    float* attn;               /* [B, H*D] fp32 out or NULL: the final token's attention output */
+} wf_catchup_args;
+
+/* Workspace (bytes) for wf_catchup / wf_catchup_kv with these shapes. */
+WF_API size_t wf_catchup_workspace_bytes(int B, int N, int din, int H, int G, int D);
+
+/*
+ * The KV-only part alone: writes cache rows cache_len[b] .. cache_len[b] + n_b - 1
+ * of every sequence and nothing else (Wq, Wo, out, attn unused).  A sequence
+ * with no backlog or a backlog past `cap` sets WF_ERR_BAD_DATA (info = b)
+ * and its rows past the cache are not written.
+ */
+WF_API wf_status wf_catchup_kv(const wf_catchup_args* args, void* ws, size_t ws_bytes, wf_stream_t stream);
+
+/* The whole catch-up: wf_catchup_kv, then the final token's attention sublayer. */
+WF_API wf_status wf_catchup(const wf_catchup_args* args, void* ws, size_t ws_bytes, wf_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -36,6 +36,9 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
                               size_t cand_off, int* bn_out, cudaStream_t s);
 wf_status launch_topk_merge(int B, int Vd, int bn, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                             float* vals, void* ws, size_t cand_off, cudaStream_t s);
+wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s);
+size_t catchup_workspace_bytes(int B, int N, int din, int H, int G, int D);
+size_t catchup_attend_smem(int H, int G, int D);
 wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, cudaStream_t s);
 
@@ -260,6 +263,43 @@ wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P,
     return launch_topk_merge(B, Vd, bn, k, d2t, draft_ids, tids, vals, ws, L.cand, stream);
 }
 
+static bool bad_catchup_shape(int B, int N, int din, int H, int G, int D) {
+    if (B < 1 || N < B || din < 8 || din % 8 || din > 16384) return true;
+    if (G < 1 || H < G || H % G || D < 16 || D % 16 || D > 192) return true;
+    if ((long)H * D > 16384) return true;
+    return catchup_attend_smem(H, G, D) > 200 * 1024;
+}
+
+size_t wf_catchup_workspace_bytes(int B, int N, int din, int H, int G, int D) {
+    if (bad_catchup_shape(B, N, din, H, G, D)) return 0;
+    return catchup_workspace_bytes(B, N, din, H, G, D);
+}
+
+static wf_status check_catchup(const wf_catchup_args* a, void* ws, size_t ws_bytes, bool with_final) {
+    if (!a) return WF_ERR_INVALID_ARG;
+    if (bad_catchup_shape(a->B, a->N, a->din, a->H, a->G, a->D) || a->cap < 1) return WF_ERR_INVALID_ARG;
+    if (!a->u || !a->bl_off || !a->cache_len || !a->gamma || !a->Wk || !a->Wv || !a->Kc || !a->Vc)
+        return WF_ERR_INVALID_ARG;
+    if (with_final && (!a->Wq || !a->Wo || !a->out)) return WF_ERR_INVALID_ARG;
+    if (!(a->eps >= 0.f) || !(a->theta > 0.f)) return WF_ERR_INVALID_ARG;
+    if (!aligned16(a->u) || !aligned16(a->gamma) || !aligned16(a->Wk) || !aligned16(a->Wv) || !aligned16(a->Kc) ||
+        !aligned16(a->Vc))
+        return WF_ERR_INVALID_ARG;
+    if (with_final && (!aligned16(a->Wq) || !aligned16(a->Wo))) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_ws(ws, ws_bytes, catchup_workspace_bytes(a->B, a->N, a->din, a->H, a->G, a->D)));
+    return check_device();
+}
+
+wf_status wf_catchup_kv(const wf_catchup_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    WF_TRY(check_catchup(a, ws, ws_bytes, false));
+    return launch_catchup(a, ws, false, stream);
+}
+
+wf_status wf_catchup(const wf_catchup_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {
+    WF_TRY(check_catchup(a, ws, ws_bytes, true));
+    return launch_catchup(a, ws, true, stream);
+}
+
 wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {
     if (!a) return WF_ERR_INVALID_ARG;
     if (!a->hidden || !a->W || bad_gemm_shape(a->P, a->d, a->V)) return WF_ERR_INVALID_ARG;
@@ -300,38 +340,42 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         WF_TRY(launch_gather_rows(a->hidden, a->P, a->d, a->last_pos, a->B, gath, ws, stream));
         WF_TRY(launch_lmhead_entropy(gath, a->W, a->B, a->d, a->V, nullptr, nullptr, a->delta_al, a->route, a->tau,
                                      a->last_pos, a->P, ws, L.ent, stream));
-    } else if (draft && a->P <= BM && a->B <= BM) {
-        // One activation tile each: the LM head and the draft head share one
-        // sweep (W, then Wd); the router runs on every row beside it, the
-        // acceptance step picks the accepted row's output, and the draft
-        // candidates are merged last.
-        int bn = 0;
-        WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B, a->Vd,
-                                   a->k, ws, L.cand, &bn, stream));
-        WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
-                             nullptr, ws, L.part, stream));
-        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
-                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{dall, a->tau, a->delta_al, a->route}));
-        return launch_topk_merge(a->B, a->Vd, bn, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws, L.cand, stream);
-    } else if (a->P <= ROUTE_ALL_ROWS_MAX) {
-        // Few rows: the router runs on every verified row beside the LM head
-        // (it needs only the hidden states and its weights, and waits for the
-        // LM head just before it exits); acceptance then picks the output of
-        // the row it accepted.
-        WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
-        WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
-                             nullptr, ws, L.part, stream));
-        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
-                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{dall, a->tau, a->delta_al, a->route}));
     } else {
-        WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
-        WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
-                             a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{}));
-        WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
-                             a->delta_al, a->route, ws, L.part, stream));
+        // Neural router.  With few rows it runs on every verified row beside
+        // the LM head (it needs only the hidden states and its weights, and
+        // waits for the LM head just before it exits) and acceptance picks the
+        // accepted row's output; otherwise it routes each sequence's accepted
+        // row after acceptance, its weights already loaded while acceptance
+        // runs.  With one activation tile per head the draft head shares the
+        // LM head's weight sweep (W, then Wd) and its candidates are merged last.
+        const bool beside = a->P <= ROUTER_BESIDE_MAX_ROWS;
+        const bool shared = draft && a->P <= BM && a->B <= BM;
+        int bn = 0;
+        if (shared)
+            WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
+                                       a->Vd, a->k, ws, L.cand, &bn, stream));
+        else
+            WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        if (beside) {
+            WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
+                                 nullptr, ws, L.part, stream));
+            WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                                 a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
+                                 stream, RoutePick{dall, a->tau, a->delta_al, a->route}));
+        } else {
+            WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
+                                 a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
+                                 stream, RoutePick{}));
+            WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
+                                 a->delta_al, a->route, ws, L.part, stream));
+        }
+        if (shared)
+            return launch_topk_merge(a->B, a->Vd, bn, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws, L.cand,
+                                     stream);
+        if (draft)
+            WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals,
+                                     ws, L.cand, stream));
+        return WF_OK;
     }
     if (draft)
         WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals, ws,

@@ -1,0 +1,780 @@
+// KV-only catch-up of the EAGLE-3 drafter after a switch (WhiFlash paper
+// Sec. 3.4, "Lazy Catch-up" and "KV-only Prefill"; drafter geometry from the
+// Qwen3-4B-EAGLE3 card, "Technical Specifications").
+//
+// Four launches, stream-ordered with programmatic dependent launch:
+//   norm_kernel    RMSNorm of every backlog row (and a compact copy of each
+//                  sequence's final row) into bf16 tensor-core operands, and
+//                  the rotary frequency table
+//   proj_kernel    tcgen05 GEMM  act[M, K] x W[N, K]^T  split along K over the
+//                  SMs; the splits of an output tile form a thread-block
+//                  cluster and sum their partial tiles over distributed shared
+//                  memory in a fixed order (the result does not depend on CTA
+//                  scheduling), each finishing a slice of the tile's rows:
+//                    KEY    rotary embedding, bf16 rows appended to the key cache
+//                    VALUE  bf16 rows appended to the value cache
+//                    QUERY  rotary embedding, fp32 query of the final token
+//                    OUT    residual: the final token's input plus the product
+//                  One launch covers the key, value and query projections
+//                  (segments of one tile space); a second one Wo.
+//   attend_kernel  the final token's grouped-query attention over the whole
+//                  cache, split along the cache rows across CTAs; the last
+//                  CTA of each (sequence, KV head) merges the splits in a
+//                  fixed order
+//
+// Every wait inside a kernel is bounded (WF_ERR_TIMEOUT, no trap).
+#include <math.h>
+
+#include "wf_internal.cuh"
+
+#define CU_TRY(x)                      \
+    do {                               \
+        const wf_status _st = (x);     \
+        if (_st != WF_OK) return _st;  \
+    } while (0)
+
+namespace wf {
+
+// ------------------------------------------------------------------ geometry
+constexpr int PJ_STAGES = 4;
+constexpr int PJ_THREADS = 192;
+constexpr int PJ_BN_MAX = 256;
+constexpr int PJ_A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int PJ_B_BYTES = PJ_BN_MAX * BK * 2;    // 32 KB
+// ring, alignment slack, barriers and the destination row of each tile row
+constexpr int PJ_SMEM = PJ_STAGES * (PJ_A_BYTES + PJ_B_BYTES) + 1024 + 256 + BM * 8;
+constexpr int PJ_MAX_SPLIT = 8;      // K splits of one tile: the portable cluster size
+constexpr int PJ_BN_CU = 192;        // widest output tile: partial, reduced and staged tiles fit the ring
+constexpr int AT_MAX_CHUNKS = 64;    // cache-row splits per (sequence, KV head)
+constexpr int NORM_ROWS_PER_CTA = 4;
+
+enum : int { PJ_KEY = 0, PJ_VALUE = 1, PJ_QUERY = 2, PJ_OUT = 3 };
+
+// Output tile width: whole heads, dividing both the KV width (G heads) and the
+// query width (H heads), at most PJ_BN_CU columns (one head if D is wider).
+inline int cu_bn(int G, int D) {
+    int hp = PJ_BN_CU / D;
+    if (hp < 1) hp = 1;
+    while (hp > 1 && G % hp) --hp;
+    return hp * D;
+}
+
+struct CuLayout {
+    size_t cnt, ahat, afin, obf, q, rope, apart, total;
+    int bn;
+};
+
+inline CuLayout cu_layout(int B, int N, int din, int H, int G, int D) {
+    CuLayout L;
+    L.bn = cu_bn(G, D);
+    const int hq = H / G;
+    size_t off = sizeof(Control);
+    L.cnt = off;                                          // (sequence, KV head) arrivals, zero at rest
+    off = align_up(off + sizeof(uint32_t) * (size_t)B * G, 256);
+    L.ahat = off;
+    off = align_up(off + 2 * (size_t)N * din, 256);
+    L.afin = off;
+    off = align_up(off + 2 * (size_t)B * din, 256);
+    L.obf = off;
+    off = align_up(off + 2 * (size_t)B * H * D, 256);
+    L.q = off;
+    off = align_up(off + 4 * (size_t)B * H * D, 256);
+    L.rope = off;
+    off = align_up(off + sizeof(float2) * (size_t)(D / 2), 256);
+    L.apart = off;
+    off = align_up(off + 4 * (size_t)B * G * AT_MAX_CHUNKS * hq * (D + 2), 256);
+    L.total = off;
+    return L;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// fp32 -> bf16, round to nearest even (finite inputs; NaN stays NaN)
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// Sequence of packed backlog row r: the b with bl_off[b] <= r < bl_off[b + 1].
+__device__ __forceinline__ int seq_of(const int32_t* bl_off, int B, int r) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(bl_off + mid) <= r) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Rotation of the pair (x1, x2) by pos * theta^(-2i/D).  tab = theta^(-2i/D) / pi
+// as a float pair hi + lo, so the angle is pi * (pos * hi + pos * lo): the
+// product is split exactly (pos * hi rounded, plus its rounding error from an
+// fma), the rounded part is reduced modulo 2 exactly, and sincospi takes the
+// small remainder - the angle keeps ~1e-7 absolute accuracy for any position.
+__device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, float2 tab) {
+    const float p = (float)pos;
+    const float prod = p * tab.x;
+    const float err = fmaf(p, tab.x, -prod) + p * tab.y;
+    const float red = prod - 2.0f * rintf(prod * 0.5f);   // exact: prod mod 2, in [-1, 1]
+    float s, c;
+    sincospif(red + err, &s, &c);
+    const float y1 = x1 * c - x2 * s;
+    const float y2 = x2 * c + x1 * s;
+    x1 = y1;
+    x2 = y2;
+}
+
+// ------------------------------------------------------------------ RMSNorm
+// One warp per row.  Rows 0..N-1: the backlog rows (-> ahat).  Rows N..N+B-1:
+// sequence b's final backlog row (-> afin), which also checks the sequence's
+// offsets against its cache.  CTA 0 writes the rotary table.
+__global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
+    norm_kernel(const uint16_t* __restrict__ u, const int32_t* __restrict__ bl_off,
+                const int32_t* __restrict__ cache_len, int B, int N, int din, int cap,
+                const uint16_t* __restrict__ gamma, float eps, int with_final, float theta, int D,
+                uint16_t* __restrict__ ahat, uint16_t* __restrict__ afin, float2* __restrict__ rope, Control* ctrl) {
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0 && threadIdx.x < D / 2) {
+        const double f = pow((double)theta, -2.0 * (double)threadIdx.x / (double)D) / 3.14159265358979323846;
+        const float hi = (float)f;
+        rope[threadIdx.x] = make_float2(hi, (float)(f - (double)hi));
+    }
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * NORM_ROWS_PER_CTA + (threadIdx.x >> 5);
+    const int rows = N + (with_final ? B : 0);
+    if (r >= rows) return;
+    int src;
+    uint16_t* dst;
+    if (r < N) {
+        src = r;
+        dst = ahat + (size_t)r * din;
+    } else {
+        const int b = r - N;
+        const int n = bl_off[b + 1] - bl_off[b];
+        const int L = cache_len[b];
+        if (n < 1 || L < 0 || L + n > cap || bl_off[b] < 0 || bl_off[b + 1] > N) {
+            if (lane == 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+            src = -1;
+        } else {
+            src = bl_off[b + 1] - 1;
+        }
+        dst = afin + (size_t)b * din;
+    }
+    const int chunks = din >> 3;
+    if (src < 0) {
+        for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4* x = reinterpret_cast<const uint4*>(u + (size_t)src * din);
+    float ss = 0.f;
+    for (int c = lane; c < chunks; c += 32) {
+        const uint4 v = __ldg(x + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rs = 1.0f / sqrtf(ss / (float)din + eps);
+    const uint4* gm = reinterpret_cast<const uint4*>(gamma);
+    for (int c = lane; c < chunks; c += 32) {
+        const uint4 v = __ldg(x + c), gv = __ldg(gm + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w}, g[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a0 = __uint_as_float(w[j] << 16) * rs * __uint_as_float(g[j] << 16);
+            const float a1 = __uint_as_float(w[j] & 0xFFFF0000u) * rs * __uint_as_float(g[j] & 0xFFFF0000u);
+            o[j] = (uint32_t)f32_to_bf16(a0) | ((uint32_t)f32_to_bf16(a1) << 16);
+        }
+        reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ------------------------------------------------------------------ projections
+struct PjSeg {
+    int mode;       // PJ_KEY / PJ_VALUE / PJ_QUERY / PJ_OUT
+    int a;          // activation map: 0 or 1
+    int w;          // weight map: 0, 1 or 2
+    int M, N;       // activation rows, output features
+    int a_rows;     // rows one activation box delivers
+    int tiles_n;    // output tiles along N
+    int tile0;      // first tile of the segment in the launch's tile space
+};
+
+struct PjParams {
+    PjSeg seg[3];
+    int nseg;
+    int bn, num_k, kb_per, S;   // tile width, K blocks, K blocks per split, splits (= cluster size)
+    uint32_t idesc;
+    const int32_t* bl_off;
+    const int32_t* cache_len;
+    int B, N, cap, GD, HD, din;
+    const float2* rope;         // [D/2]
+    int D;
+    uint16_t* Kc;
+    uint16_t* Vc;
+    float* q;                   // [B, HD]
+    float* out;                 // [B, din]
+    const uint16_t* u;          // backlog inputs (OUT residual)
+    Control* ctrl;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// One CTA per (output tile, K split); the S splits of a tile form one
+// cluster.  Each split leaves its fp32 partial tile in its own shared memory;
+// after a cluster barrier, split r sums rows [r BM/S, (r+1) BM/S) of all S
+// partials (in split order) over distributed shared memory and applies the
+// epilogue to them.
+__global__ void __launch_bounds__(PJ_THREADS, 1)
+    proj_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                const __grid_constant__ CUtensorMap tmW2, const PjParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + PJ_STAGES * PJ_A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + PJ_STAGES * PJ_B_BYTES);
+    uint64_t* empty = full + PJ_STAGES;
+    uint64_t* tfull = empty + PJ_STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int64_t* rowdst = reinterpret_cast<int64_t*>(tmem_slot + 4);   // [BM] destination cache row, or -1
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.S;
+    const int t = blockIdx.x / S, split = blockIdx.x % S;   // split = rank in the cluster
+    int si = 0;
+    while (si + 1 < p.nseg && t >= p.seg[si + 1].tile0) ++si;
+    const PjSeg g = p.seg[si];
+    const int lt = t - g.tile0, mt = lt / g.tiles_n, nt = lt % g.tiles_n;
+    const int kb0 = split * p.kb_per;
+    const int kb1 = min(p.num_k, kb0 + p.kb_per);
+    const CUtensorMap* mA = g.a ? &tmA1 : &tmA0;
+    const CUtensorMap* mW = g.w == 0 ? &tmW0 : (g.w == 1 ? &tmW1 : &tmW2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PJ_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(mA);
+        tma_prefetch_desc(mW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, PJ_BN_MAX);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            const uint32_t tx = (uint32_t)(g.a_rows * BK * 2 + p.bn * BK * 2);
+            int i = 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++i) {
+                const int s = i % PJ_STAGES;
+                if (!mbar_wait(&empty[s], ((i / PJ_STAGES) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                    *abort_flag = 1;
+                    record_error(p.ctrl, WF_ERR_TIMEOUT, 0x500 + s);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], tx);
+                tma_load_2d(sA + s * PJ_A_BYTES, mA, &full[s], kb * BK, mt * BM, pol_a);
+                tma_load_2d(sB + s * PJ_B_BYTES, mW, &full[s], kb * BK, nt * p.bn, pol_w);
+            }
+            if (*abort_flag)   // let every copy issued above land before the shared memory is reused
+                for (int j = (i > PJ_STAGES ? i - PJ_STAGES : 0); j < i; ++j)
+                    mbar_wait(&full[j % PJ_STAGES], (j / PJ_STAGES) & 1, p.timeout_ns, nullptr);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int i = 0;
+            for (int kb = kb0; kb < kb1; ++kb, ++i) {
+                const int s = i % PJ_STAGES;
+                if (!mbar_wait(&full[s], (i / PJ_STAGES) & 1, p.timeout_ns, abort_flag)) {
+                    *abort_flag = 1;
+                    record_error(p.ctrl, WF_ERR_TIMEOUT, 0x510 + s);
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t adesc = umma_desc_sw128(smem_u32(sA + s * PJ_A_BYTES));
+                const uint64_t bdesc = umma_desc_sw128(smem_u32(sB + s * PJ_B_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, p.idesc, (i | kk) != 0);
+                umma_commit(&empty[s]);
+            }
+            umma_commit(tfull);   // arrives once every MMA issued above has completed
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps: accumulator -> own partial tile
+        const int q4 = warp & 3;
+        const int rit = q4 * 32 + lane;
+        if (!mbar_wait(tfull, 0, p.timeout_ns, abort_flag)) {
+            *abort_flag = 1;
+            record_error(p.ctrl, WF_ERR_TIMEOUT, 0x520);
+        }
+        tc_fence_after();
+        if (!*abort_flag) {
+            // the ring is free: every MMA (hence every copy) of this CTA has completed
+            float* pf = reinterpret_cast<float*>(smem);   // [bn][BM]
+            const uint32_t tb = tmem_base + ((uint32_t)(q4 * 32) << 16);
+            for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tb + c0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < p.bn) pf[(c0 + j) * BM + rit] = __uint_as_float(r[j]);
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (S > 1) cluster_sync();   // every split's partial tile is in its shared memory
+
+    // ---------------------------------------------------- reduce this split's rows over the cluster
+    const int rpc = BM / S;                 // rows this CTA finishes
+    const int r0 = split * rpc;
+    const int col0 = nt * p.bn;
+    const int ncols = min(p.bn, g.N - col0);
+    const float* pf = reinterpret_cast<const float*>(smem);
+    float* sf = reinterpret_cast<float*>(smem + (size_t)p.bn * BM * 4);   // [rpc][bn + 1] (S > 1)
+    const int sfs = p.bn + 1;
+    if (S > 1) {
+        const uint32_t pf_local = smem_u32(pf);
+        for (int idx = threadIdx.x; idx < rpc * ncols; idx += PJ_THREADS) {
+            const int c = idx / rpc, rl = idx - c * rpc;
+            const uint32_t off = (uint32_t)((c * BM + r0 + rl) * 4);
+            float x = 0.f;
+            for (int s = 0; s < S; ++s) x += dsmem_ld(dsmem_map(pf_local + off, (uint32_t)s));
+            sf[rl * sfs + c] = x;
+        }
+        __syncthreads();
+        cluster_sync();   // no CTA leaves while a peer may still read its partial tile
+    }
+    auto val = [&](int rl, int c) { return S > 1 ? sf[rl * sfs + c] : pf[c * BM + rl]; };
+
+    // ---------------------------------------------------- epilogue of rows r0 .. r0 + rpc - 1
+    if (!*abort_flag) {
+        const int rl = threadIdx.x;
+        const int row = mt * BM + r0 + rl;
+        const bool live = rl < rpc && row < g.M;
+        if (g.mode == PJ_KEY || g.mode == PJ_VALUE) {
+            uint16_t* stile = reinterpret_cast<uint16_t*>(smem + (size_t)p.bn * BM * 4 +
+                                                          (S > 1 ? align_up((size_t)rpc * sfs * 4, 16) : 0));
+            int64_t dst = -1;
+            int pos = 0;
+            if (live) {
+                const int b = seq_of(p.bl_off, p.B, row);
+                pos = p.cache_len[b] + (row - p.bl_off[b]);
+                if (pos >= 0 && pos < p.cap) dst = (int64_t)b * p.cap + pos;
+                else record_error(p.ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+            }
+            if (rl < rpc) rowdst[rl] = dst;
+            if (dst >= 0) {
+                if (g.mode == PJ_KEY) {
+                    const int half = p.D / 2;
+                    for (int h0 = 0; h0 < ncols; h0 += p.D)
+                        for (int i = 0; i < half; ++i) {
+                            float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
+                            rope_pair(x1, x2, pos, p.rope[i]);
+                            stile[rl * p.bn + h0 + i] = f32_to_bf16(x1);
+                            stile[rl * p.bn + h0 + i + half] = f32_to_bf16(x2);
+                        }
+                } else {
+                    for (int c = 0; c < ncols; ++c) stile[rl * p.bn + c] = f32_to_bf16(val(rl, c));
+                }
+            }
+            __syncthreads();
+            uint16_t* cache = g.mode == PJ_KEY ? p.Kc : p.Vc;
+            const int cpr = ncols / 8;   // 16-byte pieces of a row segment
+            for (int idx = threadIdx.x; idx < rpc * cpr; idx += PJ_THREADS) {
+                const int rr = idx / cpr, j = idx - rr * cpr;
+                const int64_t d = rowdst[rr];
+                if (d >= 0)
+                    *reinterpret_cast<uint4*>(cache + d * p.GD + col0 + j * 8) =
+                        *reinterpret_cast<const uint4*>(stile + rr * p.bn + j * 8);
+            }
+        } else if (live && g.mode == PJ_QUERY) {
+            const int b = row;
+            const int pos = p.cache_len[b] + (p.bl_off[b + 1] - p.bl_off[b]) - 1;
+            const int half = p.D / 2;
+            for (int h0 = 0; h0 < ncols; h0 += p.D)
+                for (int i = 0; i < half; ++i) {
+                    float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
+                    rope_pair(x1, x2, pos, p.rope[i]);
+                    p.q[(size_t)b * p.HD + col0 + h0 + i] = x1;
+                    p.q[(size_t)b * p.HD + col0 + h0 + i + half] = x2;
+                }
+        } else if (live && g.mode == PJ_OUT) {
+            const int b = row;
+            const int f = p.bl_off[b + 1] - 1;
+            const bool fok = f >= 0 && f < p.N;
+            for (int c = 0; c < ncols; ++c) {
+                const float res = fok ? bf16_to_f32(p.u[(size_t)f * p.din + col0 + c]) : 0.f;
+                p.out[(size_t)b * p.din + col0 + c] = res + val(rl, c);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, PJ_BN_MAX);
+}
+
+// ------------------------------------------------------------------ attention
+struct AtParams {
+    const float* q;            // [B, HD] rotated queries
+    const uint16_t* Kc;        // [B, cap, GD]
+    const uint16_t* Vc;
+    const int32_t* bl_off;
+    const int32_t* cache_len;
+    int B, cap, G, D, hq, GD, HD, chunks;
+    float* part;               // [B][G][chunks][hq][D + 2]: unnormalised output, running max (log2), sum
+    uint32_t* cnt;             // [B * G] arrivals, zero at rest
+    uint16_t* obf;             // [B, HD] bf16 output (operand of the output projection)
+    float* attn;               // [B, HD] fp32 output or null
+};
+
+// One CTA per (cache-row split, KV head, sequence).  A pass takes `nthr` cache
+// rows into shared memory; thread t scores row t against the hq query heads of
+// the group, then thread (j, e) accumulates output pair e of head j.  Scores
+// are kept in the base-2 domain (q pre-scaled by log2(e) / sqrt(D)).
+__global__ void attend_kernel(const AtParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const int nthr = blockDim.x;
+    const int D = p.D, hq = p.hq, half = D / 2;
+    const int kstride = D + 8;   // padded row (bf16 elements) against bank conflicts
+    uint16_t* Ks = reinterpret_cast<uint16_t*>(smem_raw);
+    uint16_t* Vs = Ks + (size_t)nthr * kstride;
+    float* qs = reinterpret_cast<float*>(Vs + (size_t)nthr * D);     // [hq][D]
+    float* sc = qs + hq * D;                                         // [hq][nthr]
+    float* mrun = sc + (size_t)hq * nthr;                            // [hq]
+    float* lrun = mrun + hq;                                         // [hq]
+    float* alpha = lrun + hq;                                        // [hq]
+    int* last = reinterpret_cast<int*>(alpha + hq);
+
+    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = nthr >> 5;
+    pdl_wait();
+    pdl_trigger();
+    int T = p.cache_len[b] + (p.bl_off[b + 1] - p.bl_off[b]);
+    T = T < 0 ? 0 : (T > p.cap ? p.cap : T);
+    const int per = (T + p.chunks - 1) / p.chunks;
+    const int t0 = c * per, t1 = min(T, t0 + per);
+    const float qscale = 1.4426950408889634f / sqrtf((float)D);
+    for (int i = tid; i < hq * D; i += nthr) qs[i] = p.q[(size_t)b * p.HD + (size_t)g * hq * D + i] * qscale;
+    if (tid < hq) {
+        mrun[tid] = -INFINITY;
+        lrun[tid] = 0.f;
+    }
+    const int oj = tid / half, oe = tid - oj * half;   // output pair (2 oe, 2 oe + 1) of head oj
+    const bool owner = tid < hq * half;
+    float o0 = 0.f, o1 = 0.f;
+    const uint16_t* Kb = p.Kc + (size_t)b * p.cap * p.GD + (size_t)g * D;
+    const uint16_t* Vb = p.Vc + (size_t)b * p.cap * p.GD + (size_t)g * D;
+    const int cpr = D / 8;   // 16-byte pieces per row
+    __syncthreads();
+    for (int p0 = t0; p0 < t1; p0 += nthr) {
+        const int nr = min(nthr, t1 - p0);
+        for (int idx = tid; idx < nr * cpr; idx += nthr) {
+            const int r = idx / cpr, j = idx - r * cpr;
+            const uint4 kv = __ldcs(reinterpret_cast<const uint4*>(Kb + (size_t)(p0 + r) * p.GD) + j);
+            const uint4 vv = __ldcs(reinterpret_cast<const uint4*>(Vb + (size_t)(p0 + r) * p.GD) + j);
+            *reinterpret_cast<uint4*>(Ks + (size_t)r * kstride + j * 8) = kv;
+            *reinterpret_cast<uint4*>(Vs + (size_t)r * D + j * 8) = vv;
+        }
+        __syncthreads();
+        if (tid < nr) {
+            float s[8];
+            for (int j0 = 0; j0 < hq; j0 += 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s[j] = 0.f;
+                for (int e8 = 0; e8 < D; e8 += 8) {
+                    const uint4 kv = *reinterpret_cast<const uint4*>(Ks + (size_t)tid * kstride + e8);
+                    const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float k0 = __uint_as_float(w[h] << 16), k1 = __uint_as_float(w[h] & 0xFFFF0000u);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (j0 + j < hq) {
+                                s[j] = fmaf(qs[(j0 + j) * D + e8 + 2 * h], k0, s[j]);
+                                s[j] = fmaf(qs[(j0 + j) * D + e8 + 2 * h + 1], k1, s[j]);
+                            }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j0 + j < hq) sc[(j0 + j) * nthr + tid] = s[j];
+            }
+        } else {
+            for (int j = 0; j < hq; ++j) sc[j * nthr + tid] = -INFINITY;
+        }
+        __syncthreads();
+        // softmax statistics of this pass, one warp per head
+        for (int j = warp; j < hq; j += nwarp) {
+            float mx = -INFINITY;
+            for (int t = lane; t < nthr; t += 32) mx = fmaxf(mx, sc[j * nthr + t]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float mnew = fmaxf(mrun[j], mx);
+            float sum = 0.f;
+            for (int t = lane; t < nthr; t += 32) {
+                const float e = exp2f(sc[j * nthr + t] - mnew);
+                sc[j * nthr + t] = e;
+                sum += e;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) {
+                const float a = exp2f(mrun[j] - mnew);   // 0 on the first pass (mrun = -inf)
+                alpha[j] = a;
+                lrun[j] = lrun[j] * a + sum;
+                mrun[j] = mnew;
+            }
+        }
+        __syncthreads();
+        if (owner) {
+            const float a = alpha[oj];
+            o0 *= a;
+            o1 *= a;
+            const float* pj = sc + (size_t)oj * nthr;
+            for (int t = 0; t < nr; ++t) {
+                const uint32_t v = *reinterpret_cast<const uint32_t*>(Vs + (size_t)t * D + 2 * oe);
+                o0 = fmaf(pj[t], __uint_as_float(v << 16), o0);
+                o1 = fmaf(pj[t], __uint_as_float(v & 0xFFFF0000u), o1);
+            }
+        }
+        __syncthreads();
+    }
+    // this split's partial result
+    float* mypart = p.part + (((size_t)b * p.G + g) * p.chunks + c) * hq * (D + 2);
+    if (owner) {
+        mypart[(size_t)oj * (D + 2) + 2 * oe] = o0;
+        mypart[(size_t)oj * (D + 2) + 2 * oe + 1] = o1;
+    }
+    if (tid < hq) {
+        mypart[(size_t)tid * (D + 2) + D] = mrun[tid];
+        mypart[(size_t)tid * (D + 2) + D + 1] = lrun[tid];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) *last = atomicAdd(&p.cnt[(size_t)b * p.G + g], 1u) == (uint32_t)(p.chunks - 1);
+    __syncthreads();
+    if (!*last) return;
+    __threadfence();
+    // merge the splits in index order
+    const float* allp = p.part + ((size_t)b * p.G + g) * p.chunks * hq * (D + 2);
+    if (owner) {
+        float M = -INFINITY;
+        for (int s = 0; s < p.chunks; ++s) M = fmaxf(M, __ldcg(allp + ((size_t)s * hq + oj) * (D + 2) + D));
+        float L = 0.f, a0 = 0.f, a1 = 0.f;
+        for (int s = 0; s < p.chunks; ++s) {
+            const float* ps = allp + ((size_t)s * hq + oj) * (D + 2);
+            const float ms = __ldcg(ps + D);
+            if (ms == -INFINITY) continue;   // a split with no rows
+            const float w = exp2f(ms - M);
+            L = fmaf(w, __ldcg(ps + D + 1), L);
+            a0 = fmaf(w, __ldcg(ps + 2 * oe), a0);
+            a1 = fmaf(w, __ldcg(ps + 2 * oe + 1), a1);
+        }
+        const float r0 = L > 0.f ? a0 / L : 0.f, r1 = L > 0.f ? a1 / L : 0.f;
+        const size_t o = (size_t)b * p.HD + ((size_t)g * hq + oj) * D + 2 * oe;
+        *reinterpret_cast<uint32_t*>(p.obf + o) = (uint32_t)f32_to_bf16(r0) | ((uint32_t)f32_to_bf16(r1) << 16);
+        if (p.attn) {
+            p.attn[o] = r0;
+            p.attn[o + 1] = r1;
+        }
+    }
+    if (tid == 0) p.cnt[(size_t)b * p.G + g] = 0;
+}
+
+// ------------------------------------------------------------------ host side
+static wf_status launch_proj(const CUtensorMap* mA, const CUtensorMap* mW, PjParams p, int tiles, cudaStream_t s) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PJ_SMEM) != cudaSuccess)
+            return WF_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    // split K (a power of two up to the portable cluster size) so that about
+    // one wave of CTAs covers the SMs
+    int S = 1;
+    while (S < PJ_MAX_SPLIT && tiles * 2 * S <= num_sms() && 2 * S <= p.num_k) S *= 2;
+    p.kb_per = cdiv(p.num_k, S);
+    while (S > 1 && (S - 1) * p.kb_per >= p.num_k) S /= 2;   // every split gets at least one K block
+    p.kb_per = cdiv(p.num_k, S);
+    p.S = S;
+    return launch_cluster(proj_kernel, dim3(tiles * S), dim3(PJ_THREADS), PJ_SMEM, s, (unsigned)S, mA[0], mA[1],
+                          mW[0], mW[1], mW[2], p);
+}
+
+static PjParams proj_params(const wf_catchup_args* a, const CuLayout& L, void* ws) {
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    PjParams p = {};
+    p.bn = L.bn;
+    p.idesc = umma_idesc_bf16(BM, L.bn);
+    p.bl_off = a->bl_off;
+    p.cache_len = a->cache_len;
+    p.B = a->B;
+    p.N = a->N;
+    p.cap = a->cap;
+    p.GD = a->G * a->D;
+    p.HD = a->H * a->D;
+    p.din = a->din;
+    p.rope = reinterpret_cast<const float2*>(w + L.rope);
+    p.D = a->D;
+    p.Kc = a->Kc;
+    p.Vc = a->Vc;
+    p.q = reinterpret_cast<float*>(w + L.q);
+    p.out = a->out;
+    p.u = a->u;
+    p.ctrl = reinterpret_cast<Control*>(ws);
+    p.timeout_ns = wait_timeout_ns();
+    return p;
+}
+
+static int add_seg(PjParams& p, int tile0, int mode, int am, int wm, int M, int N, int bn) {
+    PjSeg& g = p.seg[p.nseg++];
+    g.mode = mode;
+    g.a = am;
+    g.w = wm;
+    g.M = M;
+    g.N = N;
+    g.a_rows = M <= BM ? (M + 7) / 8 * 8 : BM;
+    g.tiles_n = cdiv(N, bn);
+    g.tile0 = tile0;
+    return tile0 + cdiv(M, BM) * g.tiles_n;
+}
+
+// act [rows, cols] box: the rows present (one tile) or BM
+static bool act_map(CUtensorMap* m, const void* base, int rows, int cols) {
+    return make_map(m, base, (uint64_t)rows, (uint64_t)cols, (uint32_t)(rows <= BM ? (rows + 7) / 8 * 8 : BM));
+}
+
+wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s) {
+    const CuLayout L = cu_layout(a->B, a->N, a->din, a->H, a->G, a->D);
+    uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+    Control* ctrl = reinterpret_cast<Control*>(ws);
+    uint16_t* ahat = reinterpret_cast<uint16_t*>(w + L.ahat);
+    uint16_t* afin = reinterpret_cast<uint16_t*>(w + L.afin);
+    const int GD = a->G * a->D, HD = a->H * a->D;
+    const int rows = a->N + (with_final ? a->B : 0);
+    CU_TRY(launch(norm_kernel, dim3(cdiv(rows, NORM_ROWS_PER_CTA)), dim3(32 * NORM_ROWS_PER_CTA), 0, s, a->u,
+                         a->bl_off, a->cache_len, a->B, a->N, a->din, a->cap, a->gamma, a->eps, (int)with_final,
+                         a->theta, a->D, ahat, afin, reinterpret_cast<float2*>(w + L.rope), ctrl));
+    // keys, values (and the final token's query) in one launch
+    CUtensorMap mA[2], mW[3];
+    if (!act_map(&mA[0], ahat, a->N, a->din) || !make_map(&mW[0], a->Wk, GD, a->din, L.bn) ||
+        !make_map(&mW[1], a->Wv, GD, a->din, L.bn))
+        return WF_ERR_CUDA;
+    mA[1] = mA[0];
+    mW[2] = mW[0];
+    PjParams p = proj_params(a, L, ws);
+    p.num_k = cdiv(a->din, BK);
+    int tiles = add_seg(p, 0, PJ_KEY, 0, 0, a->N, GD, L.bn);
+    tiles = add_seg(p, tiles, PJ_VALUE, 0, 1, a->N, GD, L.bn);
+    if (with_final) {
+        if (!act_map(&mA[1], afin, a->B, a->din) || !make_map(&mW[2], a->Wq, HD, a->din, L.bn)) return WF_ERR_CUDA;
+        tiles = add_seg(p, tiles, PJ_QUERY, 1, 2, a->B, HD, L.bn);
+    }
+    CU_TRY(launch_proj(mA, mW, p, tiles, s));
+    if (!with_final) return WF_OK;
+
+    // the final token's attention over its whole cache
+    AtParams ap = {};
+    ap.q = reinterpret_cast<const float*>(w + L.q);
+    ap.Kc = a->Kc;
+    ap.Vc = a->Vc;
+    ap.bl_off = a->bl_off;
+    ap.cache_len = a->cache_len;
+    ap.B = a->B;
+    ap.cap = a->cap;
+    ap.G = a->G;
+    ap.D = a->D;
+    ap.hq = a->H / a->G;
+    ap.GD = GD;
+    ap.HD = HD;
+    const int want = 2 * num_sms() / (a->B * a->G);
+    ap.chunks = want < 1 ? 1 : (want > AT_MAX_CHUNKS ? AT_MAX_CHUNKS : want);
+    ap.part = reinterpret_cast<float*>(w + L.apart);
+    ap.cnt = reinterpret_cast<uint32_t*>(w + L.cnt);
+    ap.obf = reinterpret_cast<uint16_t*>(w + L.obf);
+    ap.attn = a->attn;
+    int nthr = ap.hq * (a->D / 2);
+    nthr = nthr < 64 ? 64 : nthr;
+    nthr = (nthr + 31) / 32 * 32;
+    const size_t at_smem = (size_t)nthr * (a->D + 8) * 2 + (size_t)nthr * a->D * 2 + 4 * (size_t)ap.hq * a->D +
+                           4 * (size_t)ap.hq * nthr + 4 * 3 * (size_t)ap.hq + 16;
+    static bool at_attr[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !at_attr[dev]) {
+        if (cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+            cudaSuccess)
+            return WF_ERR_CUDA;
+        at_attr[dev] = true;
+    }
+    CU_TRY(launch(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(nthr), at_smem, s, ap));
+
+    // output projection with the residual
+    CUtensorMap oA[2], oW[3];
+    if (!act_map(&oA[0], ap.obf, a->B, HD) || !make_map(&oW[0], a->Wo, a->din, HD, L.bn)) return WF_ERR_CUDA;
+    oA[1] = oA[0];
+    oW[1] = oW[2] = oW[0];
+    PjParams po = proj_params(a, L, ws);
+    po.num_k = cdiv(HD, BK);
+    const int otiles = add_seg(po, 0, PJ_OUT, 0, 0, a->B, a->din, L.bn);
+    return launch_proj(oA, oW, po, otiles, s);
+}
+
+size_t catchup_workspace_bytes(int B, int N, int din, int H, int G, int D) {
+    return cu_layout(B, N, din, H, G, D).total;
+}
+
+// Shared memory an attention CTA asks for (validated on the host).
+size_t catchup_attend_smem(int H, int G, int D) {
+    const int hq = H / G;
+    int nthr = hq * (D / 2);
+    nthr = nthr < 64 ? 64 : nthr;
+    nthr = (nthr + 31) / 32 * 32;
+    return (size_t)nthr * (D + 8) * 2 + (size_t)nthr * D * 2 + 4 * (size_t)hq * D + 4 * (size_t)hq * nthr +
+           4 * 3 * (size_t)hq + 16;
+}
+
+}  // namespace wf

@@ -430,30 +430,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // --------------------------------------------------------------------- top-k merge
-// One warp per activation row: every lane keeps the 16 best of its share of
-// the per-tile candidate lists, then k rounds of a warp-wide max pick the
-// winners in order.  Keys are unique per row (each weight row lives in one tile).
-__global__ void __launch_bounds__(128) topk_merge_kernel(const uint64_t* __restrict__ cand, int B, int num_m,
-                                                         int num_n, int k, const int32_t* __restrict__ d2t, int Vd,
-                                                         int32_t* draft_ids, int32_t* tids, float* vals,
-                                                         Control* ctrl) {
+// One CTA per activation row: every thread keeps the KT best of its share of
+// the per-tile candidate lists, then k rounds of a block-wide max pick the
+// winners in order.  Keys are unique per row (each weight row lives in one
+// tile), so exactly one thread owns each winner.
+constexpr int MERGE_THREADS = 128;
+
+__global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const uint64_t* __restrict__ cand, int B,
+                                                                   int num_m, int num_n, int k,
+                                                                   const int32_t* __restrict__ d2t, int Vd,
+                                                                   int32_t* draft_ids, int32_t* tids, float* vals,
+                                                                   Control* ctrl) {
+    __shared__ uint64_t wbest[MERGE_THREADS / 32];
     pdl_wait();
     pdl_trigger();
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= B) return;
+    const int row = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int m = row / BM, rit = row % BM;
     uint64_t loc[KT_TOPK];
 #pragma unroll
     for (int j = 0; j < KT_TOPK; ++j) loc[j] = 0;
     const int total = num_n * k;
-    constexpr int BATCH = 8;   // candidates in flight per lane
-    for (int base = 0; base < total; base += 32 * BATCH) {
+    constexpr int BATCH = 4;   // candidates in flight per thread
+    for (int base = 0; base < total; base += MERGE_THREADS * BATCH) {
         uint64_t kb[BATCH];
         uint64_t* src[BATCH];
 #pragma unroll
         for (int u = 0; u < BATCH; ++u) {
-            const int idx = base + u * 32 + lane;
+            const int idx = base + u * MERGE_THREADS + threadIdx.x;
             const int n = idx / k, j = idx - n * k;
             src[u] = idx < total ? const_cast<uint64_t*>(cand) + (((size_t)n * num_m + m) * BM + rit) * k + j
                                  : nullptr;
@@ -483,12 +487,17 @@ __global__ void __launch_bounds__(128) topk_merge_kernel(const uint64_t* __restr
             const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
             best = o > best ? o : best;
         }
+        if (lane == 0) wbest[warp] = best;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < MERGE_THREADS / 32; ++w) best = wbest[w] > best ? wbest[w] : best;
+        __syncthreads();   // every thread has read wbest before the next round writes it
         if (loc[0] == best && best != 0) {  // the (unique) owner pops its head
 #pragma unroll
             for (int s = 0; s < KT_TOPK - 1; ++s) loc[s] = loc[s + 1];
             loc[KT_TOPK - 1] = 0;
         }
-        if (lane == 0) {
+        if (threadIdx.x == 0) {
             const size_t o = (size_t)row * k + j;
             int32_t id = -1, tid = -1;
             float v = __int_as_float(0x7fc00000);
@@ -521,7 +530,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [rows, cols] bf16 row-major; boxes of 64 columns (128 B, swizzled) x box_rows rows.
-static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
@@ -676,7 +685,7 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s);
     if (st != WF_OK) return st;
     const int bn = pick_bn(cdiv(B, BM), Vd, num_sms());
-    return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, (const uint64_t*)p.cand, B, cdiv(B, BM),
+    return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, (const uint64_t*)p.cand, B, cdiv(B, BM),
                   cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids, vals, p.ctrl);
 }
 
@@ -736,7 +745,7 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
 wf_status launch_topk_merge(int B, int Vd, int bn, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                             float* vals, void* ws, size_t cand_off, cudaStream_t s) {
     const uint64_t* cand = reinterpret_cast<const uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
-    return launch(topk_merge_kernel, dim3(cdiv(B, 4)), dim3(128), 0, s, cand, B, cdiv(B, BM), cdiv(Vd, bn), k, d2t,
+    return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, cand, B, cdiv(B, BM), cdiv(Vd, bn), k, d2t,
                   Vd, draft_ids, tids, vals, reinterpret_cast<Control*>(ws));
 }
 

@@ -43,6 +43,11 @@ constexpr int ENT_MAX_ROWS = 256;
 // just picks the row it accepted.  Larger rounds route only the last accepted
 // row of each sequence, after the acceptance step.
 constexpr int ROUTE_ALL_ROWS_MAX = 128;
+// The neural router runs on every row beside the LM head only for rounds this
+// small: one row chunk per router CTA, all of them resident beside the LM-head
+// CTAs.  Beyond it the router's sweep over all rows outlasts its benefit and it
+// routes the accepted rows after acceptance instead.
+constexpr int ROUTER_BESIDE_MAX_ROWS = 32;
 
 // Optional tail of the acceptance step: copy the router output of the
 // accepted row (computed for every row beforehand) and take the decision.
@@ -101,6 +106,11 @@ inline Layout layout(int P, int B, int d, int m, int Vd, int k) {
 
 // process-wide bound on device waits (ns)
 uint64_t wait_timeout_ns();
+// SMs of the current device
+int num_sms();
+// TMA map of a [rows, cols] row-major bf16 matrix read in boxes of BK columns
+// (128 bytes, 128-byte swizzle) by box_rows rows
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 // ----------------------------------------------------------------- launches
 // Every kernel is launched with programmatic stream serialization: it may be

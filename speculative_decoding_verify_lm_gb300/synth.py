@@ -487,3 +487,62 @@ def small_workload(seed: int, d: int, V: int, kinds: list, argmax_fn: ArgmaxFn,
             else:
                 raise RuntimeError("draft top-k gap rule not met")
     return wl
+
+
+# --------------------------------------------------------------------------- KV-only catch-up
+# The EAGLE-3 drafter of the Qwen3-4B-EAGLE3 card ("Technical Specifications":
+# one decoder layer, hidden 2560, 32 attention heads, 8 KV heads; head size
+# 2560 / 32 = 80) catching up its backlog after a switch.  Cache lengths and
+# backlogs span the switching-cost tables of the paper (Sec. 4, Table 4 and
+# App. Table 12: base KV lengths 512 .. 16384, backlogs 1 .. 1024, typically
+# 80-90 tokens).  Layer inputs ~N(0, 1) like hidden states, weights ~N(0, 0.02^2)
+# like the other weights here, RMSNorm gains 1 + N(0, 0.1^2), cached keys and
+# values ~N(0, 1); all bf16.
+_T_CU = 100   # first stream tag of the catch-up tensors
+
+
+@dataclasses.dataclass(frozen=True)
+class CatchupConfig:
+    name: str
+    n: tuple             # backlog tokens per sequence
+    L: tuple             # entries already cached per sequence
+    din: int = 2560
+    H: int = 32
+    G: int = 8
+    D: int = 80
+    eps: float = 1e-6
+    theta: float = 10000.0
+    w_std: float = 0.02
+
+
+CATCHUP_CONFIGS = [
+    CatchupConfig("eagle3_catchup_b1_L2048_n85", n=(85,), L=(2048,)),
+    CatchupConfig("eagle3_catchup_b1_L16384_n1024", n=(1024,), L=(16384,)),
+    CatchupConfig("eagle3_catchup_b4_mixed", n=(1, 64, 128, 7), L=(0, 511, 1024, 4000)),
+    CatchupConfig("eagle3_catchup_b8_L8192_n128", n=(128,) * 8, L=(8192,) * 8),
+]
+
+
+def catchup_workload(index: int, cap_extra: int = 0) -> dict:
+    """Inputs of one catch-up call (bf16 bits / int32), keyed like the oracle's arguments.
+    Each cache holds cache_len + backlog (+ cap_extra) rows."""
+    cfg = CATCHUP_CONFIGS[index]
+    seed = BASE_SEED + 1000 + index
+    B = len(cfg.n)
+    GD, HD = cfg.G * cfg.D, cfg.H * cfg.D
+    cap = max(L + n for L, n in zip(cfg.L, cfg.n)) + cap_extra
+    bl_off = np.concatenate([[0], np.cumsum(cfg.n)]).astype(np.int32)
+    N = int(bl_off[-1])
+    g = _rng(seed, _T_CU + 1).standard_normal(cfg.din, dtype=np.float32)
+    return dict(
+        u=normal_bf16(seed, _T_CU + 0, N, cfg.din, 1.0),
+        bl_off=bl_off, cache_len=np.array(cfg.L, np.int32),
+        gamma=to_bf16_bits(np.float32(1.0) + np.float32(0.1) * g),
+        eps=cfg.eps, theta=cfg.theta,
+        Wq=normal_bf16(seed, _T_CU + 2, HD, cfg.din, cfg.w_std),
+        Wk=normal_bf16(seed, _T_CU + 3, GD, cfg.din, cfg.w_std),
+        Wv=normal_bf16(seed, _T_CU + 4, GD, cfg.din, cfg.w_std),
+        Wo=normal_bf16(seed, _T_CU + 5, cfg.din, HD, cfg.w_std),
+        Kc=normal_bf16(seed, _T_CU + 6, B * cap, GD, 1.0).reshape(B, cap, GD),
+        Vc=normal_bf16(seed, _T_CU + 7, B * cap, GD, 1.0).reshape(B, cap, GD),
+        H=cfg.H, G=cfg.G)

@@ -57,6 +57,16 @@ WF_ROUTER_NEURAL = 0
 WF_ROUTER_ENTROPY = 1
 
 
+class CatchupArgs(ctypes.Structure):
+    """Mirror of ``wf_catchup_args``."""
+    _fields_ = [
+        ("u", _c_void_p), ("bl_off", _c_void_p), ("cache_len", _c_void_p), ("B", _i32), ("N", _i32), ("din", _i32),
+        ("H", _i32), ("G", _i32), ("D", _i32), ("gamma", _c_void_p), ("eps", _f32), ("theta", _f32),
+        ("Wq", _c_void_p), ("Wk", _c_void_p), ("Wv", _c_void_p), ("Wo", _c_void_p), ("Kc", _c_void_p),
+        ("Vc", _c_void_p), ("cap", _i32), ("out", _c_void_p), ("attn", _c_void_p),
+    ]
+
+
 _SIGS = {
     "wf_status_string": (ctypes.c_char_p, [_i32]),
     "wf_version": (_i32, []),
@@ -86,6 +96,9 @@ _SIGS = {
                                     _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                     _c_void_p, _sz, _c_void_p]),
     "wf_round": (_i32, [ctypes.POINTER(RoundArgs), _c_void_p, _sz, _c_void_p]),
+    "wf_catchup_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
+    "wf_catchup_kv": (_i32, [ctypes.POINTER(CatchupArgs), _c_void_p, _sz, _c_void_p]),
+    "wf_catchup": (_i32, [ctypes.POINTER(CatchupArgs), _c_void_p, _sz, _c_void_p]),
 }
 
 
@@ -352,6 +365,67 @@ def wf_lmhead_draft_topk(hidden, W, x, Wd, d2t, k: int, ws: Workspace, ids=None,
                                     _check(vals, "vals", _F32), ws.ptr, ws.nbytes, _stream(stream))
     _raise(st, "wf_lmhead_draft_topk")
     return ids, draft_ids, tids, vals
+
+
+class CatchupWorkspace(Workspace):
+    """Workspace of wf_catchup / wf_catchup_kv for B sequences, N backlog rows and the drafter's shapes."""
+
+    def __init__(self, B: int, N: int, din: int, H: int, G: int, D: int, device=None, stream=None):
+        self.nbytes = int(lib().wf_catchup_workspace_bytes(B, N, din, H, G, D))
+        if self.nbytes == 0:
+            raise ValueError("catch-up shapes outside the library's range")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        _raise(lib().wf_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream)), "wf_workspace_init")
+
+
+class Catchup:
+    """One KV-only catch-up call (wf_catchup, or wf_catchup_kv with kv_only) over
+    device tensors, repeatable and capturable in a CUDA graph.  u [N, din],
+    bl_off [B+1], cache_len [B] int32; gamma [din], Wq [H*D, din], Wk / Wv
+    [G*D, din], Wo [din, H*D] bf16; caches Kc / Vc [B, cap, G*D] bf16 (updated
+    in place); outputs out [B, din] and attn [B, H*D] fp32."""
+
+    def __init__(self, u, bl_off, cache_len, gamma, Wk, Wv, Kc, Vc, G: int, Wq=None, Wo=None, eps: float = 1e-6,
+                 theta: float = 1e4, kv_only: bool = False, with_attn: bool = True):
+        N, din = u.shape
+        B = bl_off.numel() - 1
+        D = Wk.shape[0] // G
+        H = Wq.shape[0] // D if Wq is not None else G
+        if Kc.shape != Vc.shape or Kc.dim() != 3 or Kc.shape[0] != B or Kc.shape[2] != G * D:
+            raise ValueError("caches must be [B, cap, G*D]")
+        if Wk.shape != (G * D, din) or Wv.shape != Wk.shape or gamma.numel() != din:
+            raise ValueError("Wk / Wv must be [G*D, din] and gamma [din]")
+        if not kv_only and (Wq is None or Wo is None or Wq.shape != (H * D, din) or Wo.shape != (din, H * D)):
+            raise ValueError("wf_catchup needs Wq [H*D, din] and Wo [din, H*D]")
+        dev = u.device
+        self.kv_only = kv_only
+        self.out = None if kv_only else torch.empty((B, din), dtype=torch.float32, device=dev)
+        self.attn = None if kv_only or not with_attn else torch.empty((B, H * D), dtype=torch.float32, device=dev)
+        self.ws = CatchupWorkspace(B, N, din, H, G, D, device=dev)
+        self.tensors = (u, bl_off, cache_len, gamma, Wq, Wk, Wv, Wo, Kc, Vc)   # kept alive
+        a = CatchupArgs()
+        a.u = _check(u, "u", _BF16)
+        a.bl_off = _check(bl_off, "bl_off", _I32)
+        a.cache_len = _check(cache_len, "cache_len", _I32)
+        a.B, a.N, a.din, a.H, a.G, a.D = B, N, din, H, G, D
+        a.gamma = _check(gamma, "gamma", _BF16)
+        a.eps, a.theta = float(eps), float(theta)
+        a.Wq = _check(Wq, "Wq", _BF16, True)
+        a.Wk = _check(Wk, "Wk", _BF16)
+        a.Wv = _check(Wv, "Wv", _BF16)
+        a.Wo = _check(Wo, "Wo", _BF16, True)
+        a.Kc = _check(Kc, "Kc", _BF16)
+        a.Vc = _check(Vc, "Vc", _BF16)
+        a.cap = Kc.shape[1]
+        a.out = _check(self.out, "out", _F32, True)
+        a.attn = _check(self.attn, "attn", _F32, True)
+        self.args = a
+
+    def __call__(self, stream=None):
+        fn = lib().wf_catchup_kv if self.kv_only else lib().wf_catchup
+        st = fn(ctypes.byref(self.args), self.ws.ptr, self.ws.nbytes, _stream(stream))
+        _raise(st, "wf_catchup_kv" if self.kv_only else "wf_catchup")
+        return self.out, self.attn
 
 
 def _packed(spec, device):

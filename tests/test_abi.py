@@ -20,7 +20,7 @@ def declared():
 def test_header_declares_the_boundary():
     names = declared()
     for must in ("wf_lmhead_argmax", "wf_verify_chain", "wf_verify_tree", "wf_router_mlp", "wf_draft_topk",
-                 "wf_round", "wf_workspace_bytes", "wf_status_string"):
+                 "wf_round", "wf_workspace_bytes", "wf_status_string", "wf_catchup", "wf_catchup_kv"):
         assert must in names
 
 
@@ -83,6 +83,27 @@ def test_shared_sweep_limited_to_one_activation_tile():
                                   1 << 20, NULL) == 4
     assert L.wf_lmhead_draft_topk(256, 256, 128, 64, 100, 256, NULL, 256, 256, 256, 129, 50, 4, NULL, 256, 256,
                                   256, 1 << 20, NULL) == 4
+
+
+def test_catchup_shapes_checked_on_host():
+    L = wf.lib()
+    assert L.wf_catchup_workspace_bytes(1, 85, 2560, 32, 8, 80) > 0
+    assert L.wf_catchup_workspace_bytes(1, 85, 2560, 32, 8, 72) == 0     # head size not a multiple of 16
+    assert L.wf_catchup_workspace_bytes(1, 85, 2560, 30, 8, 80) == 0     # query heads not a multiple of KV heads
+    assert L.wf_catchup_workspace_bytes(2, 1, 2560, 32, 8, 80) == 0      # fewer backlog rows than sequences
+    a = wf.CatchupArgs()
+    a.u = a.bl_off = a.cache_len = a.gamma = a.Wq = a.Wk = a.Wv = a.Wo = a.Kc = a.Vc = a.out = 256
+    a.B, a.N, a.din, a.H, a.G, a.D, a.cap, a.eps, a.theta = 1, 4, 64, 4, 2, 16, 8, 1e-6, 1e4
+    ws = 256
+    nbytes = L.wf_catchup_workspace_bytes(1, 4, 64, 4, 2, 16)
+    a.Wq = None
+    assert L.wf_catchup(ctypes.byref(a), ws, nbytes, None) == 1          # the full call needs Wq
+    a.Wq, a.theta = 256, 0.0
+    assert L.wf_catchup_kv(ctypes.byref(a), ws, nbytes, None) == 1       # rotary base must be positive
+    a.theta, a.Kc = 1e4, 264
+    assert L.wf_catchup_kv(ctypes.byref(a), ws, nbytes, None) == 1       # misaligned cache
+    a.Kc = 256
+    assert L.wf_catchup_kv(ctypes.byref(a), ws, nbytes - 256, None) == 2  # workspace too small
 
 
 def test_round_rejects_missing_tree_description():
