@@ -401,7 +401,7 @@ typedef struct wf_catchup_args {
     const int32_t* bl_off;     /* [B+1] backlog offsets: bl_off[0] = 0, bl_off[B] = N, n_b >= 1 */
     const int32_t* cache_len;  /* [B] entries already in each sequence's caches */
     int B, N, din;             /* din % 8 == 0, 8 <= din <= 16384 */
-    int H, G, D;               /* query heads, KV heads (H % G == 0), head size (D % 16 == 0, <= 256) */
+    int H, G, D;               /* query heads, KV heads (H % G == 0, H / G <= 16), head size (D % 16 == 0, <= 128) */
     const uint16_t* gamma;     /* [din] bf16 RMSNorm gain */
     float eps, theta;          /* RMSNorm epsilon (>= 0), rotary base (> 0) */
     const uint16_t* Wq;        /* [H*D, din] bf16 (out x in) */

@@ -265,7 +265,7 @@ wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P,
 
 static bool bad_catchup_shape(int B, int N, int din, int H, int G, int D) {
     if (B < 1 || N < B || din < 8 || din % 8 || din > 16384) return true;
-    if (G < 1 || H < G || H % G || D < 16 || D % 16 || D > 192) return true;
+    if (G < 1 || H < G || H % G || H / G > 16 || D < 16 || D % 16 || D > 128) return true;
     if ((long)H * D > 16384) return true;
     return catchup_attend_smem(H, G, D) > 200 * 1024;
 }

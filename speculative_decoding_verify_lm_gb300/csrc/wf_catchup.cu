@@ -41,12 +41,14 @@ constexpr int PJ_THREADS = 192;
 constexpr int PJ_BN_MAX = 256;
 constexpr int PJ_A_BYTES = BM * BK * 2;           // 16 KB
 constexpr int PJ_B_BYTES = PJ_BN_MAX * BK * 2;    // 32 KB
-// ring, alignment slack, barriers and the destination row of each tile row
-constexpr int PJ_SMEM = PJ_STAGES * (PJ_A_BYTES + PJ_B_BYTES) + 1024 + 256 + BM * 8;
+// ring, alignment slack, barriers and the destination row and position of each tile row
+constexpr int PJ_SMEM = PJ_STAGES * (PJ_A_BYTES + PJ_B_BYTES) + 1024 + 256 + BM * 12;
 constexpr int PJ_MAX_SPLIT = 8;      // K splits of one tile: the portable cluster size
 constexpr int PJ_BN_CU = 192;        // widest output tile: partial, reduced and staged tiles fit the ring
 constexpr int AT_MAX_CHUNKS = 64;    // cache-row splits per (sequence, KV head)
+constexpr int AT_PASS_ROWS = 128;    // cache rows an attention CTA stages per pass (two passes in flight)
 constexpr int NORM_ROWS_PER_CTA = 4;
+constexpr int NORM_REG_CHUNKS = 16;  // 16-byte pieces of a row a lane keeps in registers
 
 enum : int { PJ_KEY = 0, PJ_VALUE = 1, PJ_QUERY = 2, PJ_OUT = 3 };
 
@@ -137,10 +139,22 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
                 uint16_t* __restrict__ ahat, uint16_t* __restrict__ afin, float2* __restrict__ rope, Control* ctrl) {
     pdl_wait();
     pdl_trigger();
-    if (blockIdx.x == 0 && threadIdx.x < D / 2) {
-        const double f = pow((double)theta, -2.0 * (double)threadIdx.x / (double)D) / 3.14159265358979323846;
-        const float hi = (float)f;
-        rope[threadIdx.x] = make_float2(hi, (float)(f - (double)hi));
+    if (blockIdx.x == 0) {
+        // the rotary table depends on (theta, D) only: it is rebuilt (in double
+        // precision, slow on this GPU) only when they differ from the tagged ones
+        const uint32_t tb = __float_as_uint(theta), td = (uint32_t)D + 1u;
+        const bool stale = ctrl->rope_tag[0] != tb || ctrl->rope_tag[1] != td;
+        if (stale && threadIdx.x < D / 2) {
+            const double f = pow((double)theta, -2.0 * (double)threadIdx.x / (double)D) / 3.14159265358979323846;
+            const float hi = (float)f;
+            rope[threadIdx.x] = make_float2(hi, (float)(f - (double)hi));
+        }
+        __syncthreads();
+        if (stale && threadIdx.x == 0) {
+            __threadfence();
+            ctrl->rope_tag[0] = tb;
+            ctrl->rope_tag[1] = td;
+        }
     }
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * NORM_ROWS_PER_CTA + (threadIdx.x >> 5);
@@ -169,9 +183,11 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
         return;
     }
     const uint4* x = reinterpret_cast<const uint4*>(u + (size_t)src * din);
+    // rows up to 32 * NORM_REG_CHUNKS * 8 wide stay in registers (one read of the row)
+    const bool in_regs = chunks <= 32 * NORM_REG_CHUNKS;
+    uint4 xr[NORM_REG_CHUNKS];
     float ss = 0.f;
-    for (int c = lane; c < chunks; c += 32) {
-        const uint4 v = __ldg(x + c);
+    auto sumsq = [&](const uint4 v) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -179,13 +195,24 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
             ss = fmaf(lo, lo, ss);
             ss = fmaf(hi, hi, ss);
         }
+    };
+    if (in_regs) {
+#pragma unroll
+        for (int k = 0; k < NORM_REG_CHUNKS; ++k) {
+            const int c = lane + 32 * k;
+            xr[k] = c < chunks ? __ldg(x + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < NORM_REG_CHUNKS; ++k) sumsq(xr[k]);
+    } else {
+        for (int c = lane; c < chunks; c += 32) sumsq(__ldg(x + c));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rs = 1.0f / sqrtf(ss / (float)din + eps);
     const uint4* gm = reinterpret_cast<const uint4*>(gamma);
-    for (int c = lane; c < chunks; c += 32) {
-        const uint4 v = __ldg(x + c), gv = __ldg(gm + c);
+    auto emit = [&](int c, const uint4 v) {
+        const uint4 gv = __ldg(gm + c);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w}, g[4] = {gv.x, gv.y, gv.z, gv.w};
         uint32_t o[4];
 #pragma unroll
@@ -195,6 +222,13 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
             o[j] = (uint32_t)f32_to_bf16(a0) | ((uint32_t)f32_to_bf16(a1) << 16);
         }
         reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    if (in_regs) {
+#pragma unroll
+        for (int k = 0; k < NORM_REG_CHUNKS; ++k)
+            if (lane + 32 * k < chunks) emit(lane + 32 * k, xr[k]);
+    } else {
+        for (int c = lane; c < chunks; c += 32) emit(c, __ldg(x + c));
     }
 }
 
@@ -258,6 +292,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int64_t* rowdst = reinterpret_cast<int64_t*>(tmem_slot + 4);   // [BM] destination cache row, or -1
+                                                                   // then [BM] int: position / final row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.S;
@@ -366,84 +401,112 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     // ---------------------------------------------------- reduce this split's rows over the cluster
     const int rpc = BM / S;                 // rows this CTA finishes
     const int r0 = split * rpc;
+    const int nrows = max(0, min(rpc, g.M - (mt * BM + r0)));   // of them, rows that exist
     const int col0 = nt * p.bn;
     const int ncols = min(p.bn, g.N - col0);
     const float* pf = reinterpret_cast<const float*>(smem);
     float* sf = reinterpret_cast<float*>(smem + (size_t)p.bn * BM * 4);   // [rpc][bn + 1] (S > 1)
     const int sfs = p.bn + 1;
     if (S > 1) {
+        // item (row, column), row fastest; four items per thread in flight
         const uint32_t pf_local = smem_u32(pf);
-        for (int idx = threadIdx.x; idx < rpc * ncols; idx += PJ_THREADS) {
-            const int c = idx / rpc, rl = idx - c * rpc;
-            const uint32_t off = (uint32_t)((c * BM + r0 + rl) * 4);
-            float x = 0.f;
-            for (int s = 0; s < S; ++s) x += dsmem_ld(dsmem_map(pf_local + off, (uint32_t)s));
-            sf[rl * sfs + c] = x;
+        const int items = nrows * ncols;
+        for (int base = threadIdx.x; base < items; base += 4 * PJ_THREADS) {
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t off[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = min(base + u * PJ_THREADS, items - 1);
+                const int c = idx / nrows, rl = idx - c * nrows;
+                off[u] = pf_local + (uint32_t)((c * BM + r0 + rl) * 4);
+            }
+            for (int s = 0; s < S; ++s) {
+                float y[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) y[u] = dsmem_ld(dsmem_map(off[u], (uint32_t)s));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) x[u] += y[u];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = base + u * PJ_THREADS;
+                if (idx < items) {
+                    const int c = idx / nrows, rl = idx - c * nrows;
+                    sf[rl * sfs + c] = x[u];
+                }
+            }
         }
         __syncthreads();
         cluster_sync();   // no CTA leaves while a peer may still read its partial tile
     }
-    auto val = [&](int rl, int c) { return S > 1 ? sf[rl * sfs + c] : pf[c * BM + rl]; };
+    auto val = [&](int rl, int c) { return S > 1 ? sf[rl * sfs + c] : pf[c * BM + r0 + rl]; };
 
-    // ---------------------------------------------------- epilogue of rows r0 .. r0 + rpc - 1
-    if (!*abort_flag) {
-        const int rl = threadIdx.x;
-        const int row = mt * BM + r0 + rl;
-        const bool live = rl < rpc && row < g.M;
-        if (g.mode == PJ_KEY || g.mode == PJ_VALUE) {
-            uint16_t* stile = reinterpret_cast<uint16_t*>(smem + (size_t)p.bn * BM * 4 +
-                                                          (S > 1 ? align_up((size_t)rpc * sfs * 4, 16) : 0));
-            int64_t dst = -1;
-            int pos = 0;
-            if (live) {
+    // ---------------------------------------------------- epilogue of rows r0 .. r0 + nrows - 1
+    int* rowpos = reinterpret_cast<int*>(rowdst + BM);
+    if (!*abort_flag && nrows > 0) {
+        const bool cached = g.mode == PJ_KEY || g.mode == PJ_VALUE;
+        if (threadIdx.x < nrows) {   // per-row position / destination
+            const int rl = threadIdx.x;
+            const int row = mt * BM + r0 + rl;
+            if (cached) {
                 const int b = seq_of(p.bl_off, p.B, row);
-                pos = p.cache_len[b] + (row - p.bl_off[b]);
+                const int pos = p.cache_len[b] + (row - p.bl_off[b]);
+                int64_t dst = -1;
                 if (pos >= 0 && pos < p.cap) dst = (int64_t)b * p.cap + pos;
                 else record_error(p.ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+                rowdst[rl] = dst;
+                rowpos[rl] = pos;
+            } else if (g.mode == PJ_QUERY) {
+                rowpos[rl] = p.cache_len[row] + (p.bl_off[row + 1] - p.bl_off[row]) - 1;
+            } else {
+                rowpos[rl] = p.bl_off[row + 1] - 1;   // the final backlog row (residual)
             }
-            if (rl < rpc) rowdst[rl] = dst;
-            if (dst >= 0) {
+        }
+        __syncthreads();
+        uint16_t* stile = reinterpret_cast<uint16_t*>(smem + (size_t)p.bn * BM * 4 +
+                                                      (S > 1 ? align_up((size_t)rpc * sfs * 4, 16) : 0));
+        if (g.mode == PJ_KEY || g.mode == PJ_QUERY) {
+            // item (row, rotation pair), row fastest
+            const int half = p.D / 2;
+            const int items = nrows * (ncols / 2);
+            for (int idx = threadIdx.x; idx < items; idx += PJ_THREADS) {
+                const int pi = idx / nrows, rl = idx - pi * nrows;
+                const int h0 = (pi / half) * p.D, i = pi - (pi / half) * half;
+                float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
+                rope_pair(x1, x2, rowpos[rl], p.rope[i]);
                 if (g.mode == PJ_KEY) {
-                    const int half = p.D / 2;
-                    for (int h0 = 0; h0 < ncols; h0 += p.D)
-                        for (int i = 0; i < half; ++i) {
-                            float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
-                            rope_pair(x1, x2, pos, p.rope[i]);
-                            stile[rl * p.bn + h0 + i] = f32_to_bf16(x1);
-                            stile[rl * p.bn + h0 + i + half] = f32_to_bf16(x2);
-                        }
+                    stile[rl * p.bn + h0 + i] = f32_to_bf16(x1);
+                    stile[rl * p.bn + h0 + i + half] = f32_to_bf16(x2);
                 } else {
-                    for (int c = 0; c < ncols; ++c) stile[rl * p.bn + c] = f32_to_bf16(val(rl, c));
+                    const size_t o = (size_t)(mt * BM + r0 + rl) * p.HD + col0 + h0 + i;
+                    p.q[o] = x1;
+                    p.q[o + half] = x2;
                 }
             }
+        } else {
+            const int items = nrows * ncols;
+            for (int idx = threadIdx.x; idx < items; idx += PJ_THREADS) {
+                const int c = idx / nrows, rl = idx - c * nrows;
+                const float x = val(rl, c);
+                if (g.mode == PJ_VALUE) {
+                    stile[rl * p.bn + c] = f32_to_bf16(x);
+                } else {
+                    const int f = rowpos[rl];
+                    const float res = (f >= 0 && f < p.N) ? bf16_to_f32(p.u[(size_t)f * p.din + col0 + c]) : 0.f;
+                    p.out[(size_t)(mt * BM + r0 + rl) * p.din + col0 + c] = res + x;
+                }
+            }
+        }
+        if (cached) {
             __syncthreads();
             uint16_t* cache = g.mode == PJ_KEY ? p.Kc : p.Vc;
             const int cpr = ncols / 8;   // 16-byte pieces of a row segment
-            for (int idx = threadIdx.x; idx < rpc * cpr; idx += PJ_THREADS) {
+            for (int idx = threadIdx.x; idx < nrows * cpr; idx += PJ_THREADS) {
                 const int rr = idx / cpr, j = idx - rr * cpr;
                 const int64_t d = rowdst[rr];
                 if (d >= 0)
                     *reinterpret_cast<uint4*>(cache + d * p.GD + col0 + j * 8) =
                         *reinterpret_cast<const uint4*>(stile + rr * p.bn + j * 8);
-            }
-        } else if (live && g.mode == PJ_QUERY) {
-            const int b = row;
-            const int pos = p.cache_len[b] + (p.bl_off[b + 1] - p.bl_off[b]) - 1;
-            const int half = p.D / 2;
-            for (int h0 = 0; h0 < ncols; h0 += p.D)
-                for (int i = 0; i < half; ++i) {
-                    float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
-                    rope_pair(x1, x2, pos, p.rope[i]);
-                    p.q[(size_t)b * p.HD + col0 + h0 + i] = x1;
-                    p.q[(size_t)b * p.HD + col0 + h0 + i + half] = x2;
-                }
-        } else if (live && g.mode == PJ_OUT) {
-            const int b = row;
-            const int f = p.bl_off[b + 1] - 1;
-            const bool fok = f >= 0 && f < p.N;
-            for (int c = 0; c < ncols; ++c) {
-                const float res = fok ? bf16_to_f32(p.u[(size_t)f * p.din + col0 + c]) : 0.f;
-                p.out[(size_t)b * p.din + col0 + c] = res + val(rl, c);
             }
         }
     }
@@ -455,6 +518,13 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ attention
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 struct AtParams {
     const float* q;            // [B, HD] rotated queries
     const uint16_t* Kc;        // [B, cap, GD]
@@ -468,26 +538,57 @@ struct AtParams {
     float* attn;               // [B, HD] fp32 output or null
 };
 
-// One CTA per (cache-row split, KV head, sequence).  A pass takes `nthr` cache
-// rows into shared memory; thread t scores row t against the hq query heads of
-// the group, then thread (j, e) accumulates output pair e of head j.  Scores
-// are kept in the base-2 domain (q pre-scaled by log2(e) / sqrt(D)).
-__global__ void attend_kernel(const AtParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const int nthr = blockDim.x;
-    const int D = p.D, hq = p.hq, half = D / 2;
-    const int kstride = D + 8;   // padded row (bf16 elements) against bank conflicts
-    uint16_t* Ks = reinterpret_cast<uint16_t*>(smem_raw);
-    uint16_t* Vs = Ks + (size_t)nthr * kstride;
-    float* qs = reinterpret_cast<float*>(Vs + (size_t)nthr * D);     // [hq][D]
-    float* sc = qs + hq * D;                                         // [hq][nthr]
-    float* mrun = sc + (size_t)hq * nthr;                            // [hq]
-    float* lrun = mrun + hq;                                         // [hq]
-    float* alpha = lrun + hq;                                        // [hq]
-    int* last = reinterpret_cast<int*>(alpha + hq);
+// mma.sync m16n8k16, bf16 inputs, fp32 accumulators (row-major A, column-major B)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+}
+
+// One CTA (4 warps) per (cache-row split, KV head, sequence).  The group's hq
+// <= 16 query heads form the 16 rows of an mma.sync A operand (bf16, pre-scaled
+// by log2(e) / sqrt(D), padding rows zero); a pass stages 128 cache rows of K
+// and V in shared memory with asynchronous copies (the next pass streams in
+// while this one is computed) and each warp takes 32 of them:
+//   S = Q K^T      (D/16 k-steps x 4 key tiles of 8)
+//   running max / sum per head in the base-2 domain, P = exp2(S - max) as bf16
+//   O += P V       (2 key steps of 16 x D/8 dim tiles; V fragments by ldmatrix.trans)
+// Each warp keeps its own (max, sum, O) over its keys; the four are merged at
+// the end, and the last CTA of each (sequence, KV head) merges the splits in
+// index order.
+constexpr int AT_THREADS = 128;
+constexpr int AT_WARP_ROWS = 32;   // cache rows a warp takes per pass
+constexpr int AT_MAX_DT = 16;      // D / 8 dim tiles: D <= 128
+
+__global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int D = p.D, hq = p.hq;
+    const int R = AT_PASS_ROWS;
+    const int stride = D + 8;                 // padded row (bf16 elements): conflict-free fragment loads
+    const size_t buf = (size_t)2 * R * stride;   // one pass: K rows then V rows
+    uint16_t* Kbuf = reinterpret_cast<uint16_t*>(smem_raw);
+    uint16_t* qs = Kbuf + 2 * buf;            // [16][stride] bf16 query rows (zero padding)
+    int* last = reinterpret_cast<int*>(qs + 16 * stride);
+    float* red = reinterpret_cast<float*>(Kbuf);   // warp merge area, after the last pass
 
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = nthr >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, cq = lane & 3;   // fragment row group, column pair
     pdl_wait();
     pdl_trigger();
     int T = p.cache_len[b] + (p.bl_off[b + 1] - p.bl_off[b]);
@@ -495,100 +596,178 @@ __global__ void attend_kernel(const AtParams p) {
     const int per = (T + p.chunks - 1) / p.chunks;
     const int t0 = c * per, t1 = min(T, t0 + per);
     const float qscale = 1.4426950408889634f / sqrtf((float)D);
-    for (int i = tid; i < hq * D; i += nthr) qs[i] = p.q[(size_t)b * p.HD + (size_t)g * hq * D + i] * qscale;
-    if (tid < hq) {
-        mrun[tid] = -INFINITY;
-        lrun[tid] = 0.f;
+    for (int i = tid; i < 16 * D; i += AT_THREADS) {
+        const int h = i / D, e = i - h * D;
+        const float v = h < hq ? p.q[(size_t)b * p.HD + ((size_t)g * hq + h) * D + e] * qscale : 0.f;
+        qs[h * stride + e] = f32_to_bf16(v);
     }
-    const int oj = tid / half, oe = tid - oj * half;   // output pair (2 oe, 2 oe + 1) of head oj
-    const bool owner = tid < hq * half;
-    float o0 = 0.f, o1 = 0.f;
     const uint16_t* Kb = p.Kc + (size_t)b * p.cap * p.GD + (size_t)g * D;
     const uint16_t* Vb = p.Vc + (size_t)b * p.cap * p.GD + (size_t)g * D;
     const int cpr = D / 8;   // 16-byte pieces per row
-    __syncthreads();
-    for (int p0 = t0; p0 < t1; p0 += nthr) {
-        const int nr = min(nthr, t1 - p0);
-        for (int idx = tid; idx < nr * cpr; idx += nthr) {
+    auto stage = [&](int p0, int which) {
+        const int nr = min(R, t1 - p0);
+        uint16_t* Kd = Kbuf + which * buf;
+        uint16_t* Vd = Kd + (size_t)R * stride;
+        for (int idx = tid; idx < nr * cpr; idx += AT_THREADS) {
             const int r = idx / cpr, j = idx - r * cpr;
-            const uint4 kv = __ldcs(reinterpret_cast<const uint4*>(Kb + (size_t)(p0 + r) * p.GD) + j);
-            const uint4 vv = __ldcs(reinterpret_cast<const uint4*>(Vb + (size_t)(p0 + r) * p.GD) + j);
-            *reinterpret_cast<uint4*>(Ks + (size_t)r * kstride + j * 8) = kv;
-            *reinterpret_cast<uint4*>(Vs + (size_t)r * D + j * 8) = vv;
+            cp_async16(Kd + (size_t)r * stride + j * 8, Kb + (size_t)(p0 + r) * p.GD + j * 8);
+            cp_async16(Vd + (size_t)r * stride + j * 8, Vb + (size_t)(p0 + r) * p.GD + j * 8);
         }
-        __syncthreads();
-        if (tid < nr) {
-            float s[8];
-            for (int j0 = 0; j0 < hq; j0 += 8) {
+        // value rows past the range are multiplied by probability 0: they must
+        // hold numbers, not whatever the buffer held before
+        for (int idx = tid; idx < (R - nr) * cpr; idx += AT_THREADS) {
+            const int r = nr + idx / cpr, j = idx - (idx / cpr) * cpr;
+            *reinterpret_cast<uint4*>(Vd + (size_t)r * stride + j * 8) = make_uint4(0, 0, 0, 0);
+        }
+        cp_async_commit();
+    };
+    if (t0 < t1) stage(t0, 0);
+    __syncthreads();   // qs written
+
+    const int nks = D / 16, ndt = D / 8;
+    // Q fragments (A operand), one set per 16-dim k-step
+    uint32_t qa[AT_MAX_DT / 2][4];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) s[j] = 0.f;
-                for (int e8 = 0; e8 < D; e8 += 8) {
-                    const uint4 kv = *reinterpret_cast<const uint4*>(Ks + (size_t)tid * kstride + e8);
-                    const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+    for (int ks = 0; ks < AT_MAX_DT / 2; ++ks)
+        if (ks < nks) {
+            const int mi = lane >> 3, r = lane & 7;
+            ldsm_x4(qa[ks], smem_u32(qs + ((mi & 1) * 8 + r) * stride + ks * 16 + (mi >> 1) * 8));
+        }
+    float o[AT_MAX_DT][4];
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float k0 = __uint_as_float(w[h] << 16), k1 = __uint_as_float(w[h] & 0xFFFF0000u);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (j0 + j < hq) {
-                                s[j] = fmaf(qs[(j0 + j) * D + e8 + 2 * h], k0, s[j]);
-                                s[j] = fmaf(qs[(j0 + j) * D + e8 + 2 * h + 1], k1, s[j]);
-                            }
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (j0 + j < hq) sc[(j0 + j) * nthr + tid] = s[j];
-            }
+    for (int i = 0; i < AT_MAX_DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY;   // running max of rows gq and gq + 8
+    float l_lo = 0.f, l_hi = 0.f;               // this thread's share of the running sums
+
+    int pass = 0;
+    for (int p0 = t0; p0 < t1; p0 += R, ++pass) {
+        if (p0 + R < t1) {
+            stage(p0 + R, (pass + 1) & 1);
+            cp_async_wait_1();
         } else {
-            for (int j = 0; j < hq; ++j) sc[j * nthr + tid] = -INFINITY;
+            cp_async_wait_0();
         }
         __syncthreads();
-        // softmax statistics of this pass, one warp per head
-        for (int j = warp; j < hq; j += nwarp) {
-            float mx = -INFINITY;
-            for (int t = lane; t < nthr; t += 32) mx = fmaxf(mx, sc[j * nthr + t]);
+        const uint16_t* Ks = Kbuf + (pass & 1) * buf;
+        const uint16_t* Vs = Ks + (size_t)R * stride;
+        const int k0 = warp * AT_WARP_ROWS;                     // this warp's rows of the pass
+        const int nvalid = min(AT_WARP_ROWS, t1 - p0 - k0);     // may be <= 0
+        if (nvalid > 0) {
+            // S = Q K^T over this warp's 32 rows: four 8-row key tiles
+            float sc[4][4];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float mnew = fmaxf(mrun[j], mx);
-            float sum = 0.f;
-            for (int t = lane; t < nthr; t += 32) {
-                const float e = exp2f(sc[j * nthr + t] - mnew);
-                sc[j * nthr + t] = e;
-                sum += e;
+            for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < AT_MAX_DT / 2; ++ks) {
+                if (ks >= nks) break;
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {   // two key tiles per ldmatrix.x4
+                    uint32_t kb[4];
+                    const int mi = lane >> 3, r = lane & 7;
+                    ldsm_x4(kb, smem_u32(Ks + (size_t)(k0 + np * 16 + (mi >> 1) * 8 + r) * stride + ks * 16 +
+                                         (mi & 1) * 8));
+                    mma_bf16_16816(sc[np * 2], qa[ks], kb[0], kb[1]);
+                    mma_bf16_16816(sc[np * 2 + 1], qa[ks], kb[2], kb[3]);
+                }
+            }
+            // mask rows past the range, then the running max / sum (rows gq, gq + 8)
+            float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int key = nt * 8 + 2 * cq;
+                if (key >= nvalid) sc[nt][0] = sc[nt][2] = -INFINITY;
+                if (key + 1 >= nvalid) sc[nt][1] = sc[nt][3] = -INFINITY;
+                mx_lo = fmaxf(mx_lo, fmaxf(sc[nt][0], sc[nt][1]));
+                mx_hi = fmaxf(mx_hi, fmaxf(sc[nt][2], sc[nt][3]));
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (lane == 0) {
-                const float a = exp2f(mrun[j] - mnew);   // 0 on the first pass (mrun = -inf)
-                alpha[j] = a;
-                lrun[j] = lrun[j] * a + sum;
-                mrun[j] = mnew;
+            for (int off = 1; off <= 2; off <<= 1) {
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, off));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, off));
+            }
+            const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+            const float a_lo = exp2f(m_lo - mn_lo), a_hi = exp2f(m_hi - mn_hi);   // 0 while the max was -inf
+            m_lo = mn_lo;
+            m_hi = mn_hi;
+            l_lo *= a_lo;
+            l_hi *= a_hi;
+#pragma unroll
+            for (int i = 0; i < AT_MAX_DT; ++i) {
+                o[i][0] *= a_lo;
+                o[i][1] *= a_lo;
+                o[i][2] *= a_hi;
+                o[i][3] *= a_hi;
+            }
+            uint32_t pa[2][4];   // P as the A operand of two 16-key steps
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const float p0v = exp2f(sc[nt][0] - mn_lo), p1v = exp2f(sc[nt][1] - mn_lo);
+                const float p2v = exp2f(sc[nt][2] - mn_hi), p3v = exp2f(sc[nt][3] - mn_hi);
+                l_lo += p0v + p1v;
+                l_hi += p2v + p3v;
+                pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0v, p1v);
+                pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2v, p3v);
+            }
+            // O += P V: V fragments (keys x dims) through ldmatrix.trans
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+                for (int dp = 0; dp < AT_MAX_DT / 2; ++dp) {   // two dim tiles per ldmatrix.x4
+                    if (2 * dp >= ndt) break;
+                    uint32_t vb[4];
+                    const int mi = lane >> 3, r = lane & 7;
+                    ldsm_x4_trans(vb, smem_u32(Vs + (size_t)(k0 + kk * 16 + (mi & 1) * 8 + r) * stride + dp * 16 +
+                                               (mi >> 1) * 8));
+                    mma_bf16_16816(o[2 * dp], pa[kk], vb[0], vb[1]);
+                    mma_bf16_16816(o[2 * dp + 1], pa[kk], vb[2], vb[3]);
+                }
             }
         }
-        __syncthreads();
-        if (owner) {
-            const float a = alpha[oj];
-            o0 *= a;
-            o1 *= a;
-            const float* pj = sc + (size_t)oj * nthr;
-            for (int t = 0; t < nr; ++t) {
-                const uint32_t v = *reinterpret_cast<const uint32_t*>(Vs + (size_t)t * D + 2 * oe);
-                o0 = fmaf(pj[t], __uint_as_float(v << 16), o0);
-                o1 = fmaf(pj[t], __uint_as_float(v & 0xFFFF0000u), o1);
-            }
-        }
-        __syncthreads();
+        __syncthreads();   // the buffer is rewritten by the next pass's copies
     }
-    // this split's partial result
+    // sums over the four threads of each row
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, off);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, off);
+    }
+    // merge the four warps: red[w][row][0..D) = O, [D] = max, [D+1] = sum
+    // (4 x 16 x (D + 2) floats: within the pass buffers, 2 x 2 x 128 x (D + 8) bf16)
+    const int rs = D + 2;
+    float* rw = red + (size_t)warp * 16 * rs;
+#pragma unroll
+    for (int i = 0; i < AT_MAX_DT; ++i)
+        if (i < ndt) {
+            rw[gq * rs + i * 8 + 2 * cq] = o[i][0];
+            rw[gq * rs + i * 8 + 2 * cq + 1] = o[i][1];
+            rw[(gq + 8) * rs + i * 8 + 2 * cq] = o[i][2];
+            rw[(gq + 8) * rs + i * 8 + 2 * cq + 1] = o[i][3];
+        }
+    if (cq == 0) {
+        rw[gq * rs + D] = m_lo;
+        rw[gq * rs + D + 1] = l_lo;
+        rw[(gq + 8) * rs + D] = m_hi;
+        rw[(gq + 8) * rs + D + 1] = l_hi;
+    }
+    __syncthreads();
     float* mypart = p.part + (((size_t)b * p.G + g) * p.chunks + c) * hq * (D + 2);
-    if (owner) {
-        mypart[(size_t)oj * (D + 2) + 2 * oe] = o0;
-        mypart[(size_t)oj * (D + 2) + 2 * oe + 1] = o1;
-    }
-    if (tid < hq) {
-        mypart[(size_t)tid * (D + 2) + D] = mrun[tid];
-        mypart[(size_t)tid * (D + 2) + D + 1] = lrun[tid];
+    for (int idx = tid; idx < hq * (D + 2); idx += AT_THREADS) {
+        const int h = idx / (D + 2), e = idx - h * (D + 2);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * 16 + h) * rs + D]);
+        float v = 0.f;
+        if (e == D) {
+            v = M;
+        } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float mw = red[(w * 16 + h) * rs + D];
+                const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                v = fmaf(wt, red[(w * 16 + h) * rs + (e == D + 1 ? D + 1 : e)], v);
+            }
+        }
+        mypart[idx] = v;
     }
     __threadfence();
     __syncthreads();
@@ -596,27 +775,48 @@ __global__ void attend_kernel(const AtParams p) {
     __syncthreads();
     if (!*last) return;
     __threadfence();
-    // merge the splits in index order
+    // merge the splits in index order: every split's (max, sum) per head into
+    // shared memory (the pass buffers are free now), one weight per split and
+    // head, then each output element sums the splits with independent loads
     const float* allp = p.part + ((size_t)b * p.G + g) * p.chunks * hq * (D + 2);
-    if (owner) {
+    float* wgt = reinterpret_cast<float*>(Kbuf);        // [chunks][hq] split weights
+    float* lsum = wgt + (size_t)p.chunks * hq;          // [chunks][hq] split sums
+    float* mtot = lsum + (size_t)p.chunks * hq;         // [hq] 1 / merged sum
+    for (int idx = tid; idx < p.chunks * hq; idx += AT_THREADS) {
+        const float* ps = allp + (size_t)idx * (D + 2);
+        wgt[idx] = __ldcg(ps + D);
+        lsum[idx] = __ldcg(ps + D + 1);
+    }
+    __syncthreads();
+    if (tid < hq) {
         float M = -INFINITY;
-        for (int s = 0; s < p.chunks; ++s) M = fmaxf(M, __ldcg(allp + ((size_t)s * hq + oj) * (D + 2) + D));
-        float L = 0.f, a0 = 0.f, a1 = 0.f;
-        for (int s = 0; s < p.chunks; ++s) {
-            const float* ps = allp + ((size_t)s * hq + oj) * (D + 2);
-            const float ms = __ldcg(ps + D);
-            if (ms == -INFINITY) continue;   // a split with no rows
-            const float w = exp2f(ms - M);
-            L = fmaf(w, __ldcg(ps + D + 1), L);
-            a0 = fmaf(w, __ldcg(ps + 2 * oe), a0);
-            a1 = fmaf(w, __ldcg(ps + 2 * oe + 1), a1);
+        for (int s2 = 0; s2 < p.chunks; ++s2) M = fmaxf(M, wgt[s2 * hq + tid]);
+        float L = 0.f;
+        for (int s2 = 0; s2 < p.chunks; ++s2) {
+            const float ms = wgt[s2 * hq + tid];
+            const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);   // a split with no rows weighs 0
+            wgt[s2 * hq + tid] = w;
+            L = fmaf(w, lsum[s2 * hq + tid], L);
         }
-        const float r0 = L > 0.f ? a0 / L : 0.f, r1 = L > 0.f ? a1 / L : 0.f;
-        const size_t o = (size_t)b * p.HD + ((size_t)g * hq + oj) * D + 2 * oe;
-        *reinterpret_cast<uint32_t*>(p.obf + o) = (uint32_t)f32_to_bf16(r0) | ((uint32_t)f32_to_bf16(r1) << 16);
+        mtot[tid] = L > 0.f ? 1.f / L : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < hq * D / 2; idx += AT_THREADS) {
+        const int h = idx / (D / 2), e2 = idx - h * (D / 2);
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+        for (int s2 = 0; s2 < p.chunks; ++s2) {
+            const float w = wgt[s2 * hq + h];
+            const float2 ov = __ldcg(reinterpret_cast<const float2*>(allp + ((size_t)s2 * hq + h) * (D + 2) + 2 * e2));
+            a0 = fmaf(w, ov.x, a0);
+            a1 = fmaf(w, ov.y, a1);
+        }
+        const float r0 = a0 * mtot[h], r1 = a1 * mtot[h];
+        const size_t o2 = (size_t)b * p.HD + ((size_t)g * hq + h) * D + 2 * e2;
+        *reinterpret_cast<uint32_t*>(p.obf + o2) = pack_bf16x2(r0, r1);
         if (p.attn) {
-            p.attn[o] = r0;
-            p.attn[o + 1] = r1;
+            p.attn[o2] = r0;
+            p.attn[o2 + 1] = r1;
         }
     }
     if (tid == 0) p.cnt[(size_t)b * p.G + g] = 0;
@@ -687,6 +887,8 @@ static bool act_map(CUtensorMap* m, const void* base, int rows, int cols) {
     return make_map(m, base, (uint64_t)rows, (uint64_t)cols, (uint32_t)(rows <= BM ? (rows + 7) / 8 * 8 : BM));
 }
 
+size_t catchup_attend_smem(int H, int G, int D);
+
 wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s) {
     const CuLayout L = cu_layout(a->B, a->N, a->din, a->H, a->G, a->D);
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
@@ -736,11 +938,7 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     ap.cnt = reinterpret_cast<uint32_t*>(w + L.cnt);
     ap.obf = reinterpret_cast<uint16_t*>(w + L.obf);
     ap.attn = a->attn;
-    int nthr = ap.hq * (a->D / 2);
-    nthr = nthr < 64 ? 64 : nthr;
-    nthr = (nthr + 31) / 32 * 32;
-    const size_t at_smem = (size_t)nthr * (a->D + 8) * 2 + (size_t)nthr * a->D * 2 + 4 * (size_t)ap.hq * a->D +
-                           4 * (size_t)ap.hq * nthr + 4 * 3 * (size_t)ap.hq + 16;
+    const size_t at_smem = catchup_attend_smem(a->H, a->G, a->D);
     static bool at_attr[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
@@ -750,7 +948,7 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
             return WF_ERR_CUDA;
         at_attr[dev] = true;
     }
-    CU_TRY(launch(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(nthr), at_smem, s, ap));
+    CU_TRY(launch(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s, ap));
 
     // output projection with the residual
     CUtensorMap oA[2], oW[3];
@@ -769,12 +967,10 @@ size_t catchup_workspace_bytes(int B, int N, int din, int H, int G, int D) {
 
 // Shared memory an attention CTA asks for (validated on the host).
 size_t catchup_attend_smem(int H, int G, int D) {
-    const int hq = H / G;
-    int nthr = hq * (D / 2);
-    nthr = nthr < 64 ? 64 : nthr;
-    nthr = (nthr + 31) / 32 * 32;
-    return (size_t)nthr * (D + 8) * 2 + (size_t)nthr * D * 2 + 4 * (size_t)hq * D + 4 * (size_t)hq * nthr +
-           4 * 3 * (size_t)hq + 16;
+    (void)H;
+    (void)G;
+    const size_t stride = (size_t)D + 8;
+    return 2 * (2 * (size_t)AT_PASS_ROWS * stride * 2) + 16 * stride * 2 + 16;
 }
 
 }  // namespace wf

@@ -23,7 +23,8 @@ struct Control {
     uint32_t err_info;
     uint32_t router_done;     // CTAs finished in the current router launch
     uint32_t gemm_done;       // CTAs finished in the current LM-head launch
-    uint32_t pad[60];
+    uint32_t rope_tag[2];     // catch-up: (theta bits, D + 1) of the rotary table held in the workspace
+    uint32_t pad[58];
 };
 static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 

@@ -1,15 +1,16 @@
 """KV-only catch-up on the GPU vs the CPU oracle, through the C ABI.
 
 The oracle computes the exact definition in fp64 and rounds only what the
-method stores in bf16 (the cache rows).  The GPU rounds at three more points:
-the normalised inputs a (bf16 tensor-core operands), the fp32 accumulations,
-and the attention output before Wo (bf16 operand).  Every comparison uses a
+method stores in bf16 (the cache rows).  The GPU rounds at more points: the
+normalised inputs a, the query and the attention probabilities (bf16
+tensor-core operands), the fp32 accumulations, and the attention output
+before Wo (bf16 operand).  Every comparison uses a
 first-order bound built from those rounding points (unit roundoff u = 2^-8
 for bf16, 2^-24 per fp32 addition) with a factor 2 of slack:
   k, v before storing   |dk| <= (u + din 2^-24) sum_i |W_i a_i|  (+ the rotation mixes a pair)
   cache entries         |dk| plus one bf16 rounding of either side
-  scores                |ds_t| <= (|dq| |k_t| + |q| |dk_t|) / sqrt(D)
-  attention output      |do| <= 2 max|ds| sum_t p_t |v_t| + sum_t p_t |dv_t|
+  scores                |ds_t| <= (|dq| |k_t| + |q| |dk_t|) / sqrt(D),  |dq| including u |q|
+  attention output      |do| <= 2 max|ds| sum_t p_t |v_t| + sum_t p_t |dv_t| + u sum_t p_t |v_t|
   output                |dout| <= sum_c |Wo_c| (|do_c| + u |o_c|)
 """
 import math
@@ -88,13 +89,13 @@ def bounds(c, ref):
         for h in range(H):
             g = h // hq
             q = ref["q"][b, h * D:(h + 1) * D]
-            dq = eq[h * D:(h + 1) * D]
+            dq = eq[h * D:(h + 1) * D] + U * np.abs(q)        # + the bf16 query operand
             s = K[:, g] @ q / math.sqrt(D)
             p = np.exp(s - s.max())
             p /= p.sum()
             ds = (np.abs(K[:, g]) @ dq + (dK[:, g] @ (np.abs(q) + dq))) / math.sqrt(D)
-            tolA[b, h * D:(h + 1) * D] = 2 * (2 * ds.max() * (p @ np.abs(V[:, g])) + p @ dV[:, g]) + \
-                1e-5 * (p @ np.abs(V[:, g]))
+            tolA[b, h * D:(h + 1) * D] = 2 * ((2 * ds.max() + U) * (p @ np.abs(V[:, g])) + p @ dV[:, g]) + \
+                1e-5 * (p @ np.abs(V[:, g]))                    # U: the bf16 probabilities
         oabs = np.abs(ref["attn"][b])
         tolO[b] = 2 * (np.abs(_f64(c["Wo"])) @ (tolA[b] + U * oabs)) + 2 * (H * D) * E32 * \
             (np.abs(_f64(c["Wo"])) @ oabs) + 1e-6
