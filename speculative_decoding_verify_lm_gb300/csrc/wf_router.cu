@@ -9,11 +9,15 @@
 // kernel before this one in a round (the acceptance step), so each warp loads
 // its W1 row into registers (d <= 2560) before waiting on that kernel: the
 // weight stream overlaps it, and only the rows to route and the hidden states
-// are read after the wait.  Each pass takes RB hidden rows (read through L1,
-// shared by the CTA's warps) and keeps RB dot products per warp; units are folded per
-// CTA into w2[j] * GELU(z_j) partials, and the last CTA to finish sums the
-// partials of every sequence in a fixed order (the result does not depend on
-// CTA scheduling) and writes delta_al and route.
+// are read after the wait.  Each pass takes RB hidden rows, shared by the
+// CTA's warps, and keeps RB dot products per warp.  STAGED (routing chosen
+// rows after acceptance): the rows of the next pass stream into shared memory
+// with asynchronous copies while this pass is computed.  Otherwise (every row
+// of a small round, beside the LM head, which leaves no shared memory) they are
+// read through L1.  Units are folded per CTA into w2[j] * GELU(z_j) partials,
+// and the last CTA to finish sums the partials of every sequence in a fixed
+// order (the result does not depend on CTA scheduling) and writes delta_al and
+// route.
 #include "wf_internal.cuh"
 
 namespace wf {
@@ -37,6 +41,11 @@ __device__ __forceinline__ float dot4(const float4 w, const uint2 h, float acc) 
     return fmaf(w.w, __uint_as_float(h.y & 0xFFFF0000u), acc);
 }
 
+__device__ __forceinline__ void router_cp16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+template <bool STAGED>
 __global__ void __maxnreg__(ROUTER_MAX_REGS)
     router_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
                   int P, const float* __restrict__ W1, const float* __restrict__ b1, const float* __restrict__ w2,
@@ -44,6 +53,7 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
     // part: [B][gridDim.x] partial sums, zero on entry and on exit
     __shared__ float red[ROUTER_UNITS_PER_CTA][ROUTER_RB];
     __shared__ int s_last;
+    extern __shared__ __align__(16) uint8_t rstage[];   // STAGED: two passes of RB rows (bf16)
 
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -77,19 +87,47 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
     // this CTA's rows: blockIdx.y picks a chunk of ROUTER_ROWS_PER_CTA
     const int y0 = blockIdx.y * ROUTER_ROWS_PER_CTA;
     const int y1 = min(B, y0 + ROUTER_ROWS_PER_CTA);
-    for (int b0 = y0; b0 < y1; b0 += ROUTER_RB) {
+    auto row_of = [&](int bb) {   // hidden row of routed entry bb, or -1
+        int r = rows ? rows[bb] : bb;   // no rows: route every row
+        if (r < 0 || (P >= 0 && r >= P)) r = -1;
+        return r;
+    };
+    const int chunks = d >> 3;   // 16-byte pieces of a row
+    // STAGED: copies of pass b0's rows into buffer `which`
+    auto stage = [&](int b0, int which) {
         const int nb = min(ROUTER_RB, y1 - b0);
+        uint16_t* dst = reinterpret_cast<uint16_t*>(rstage) + (size_t)which * ROUTER_RB * d;
+        for (int idx = threadIdx.x; idx < nb * chunks; idx += ROUTER_THREADS) {
+            const int rb = idx / chunks, c = idx - rb * chunks;
+            const int r = row_of(b0 + rb);
+            if (r >= 0) router_cp16(dst + (size_t)rb * d + c * 8, hidden + (size_t)r * d + c * 8);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (STAGED && y0 < y1) stage(y0, 0);
+    int pass = 0;
+    for (int b0 = y0; b0 < y1; b0 += ROUTER_RB, ++pass) {
+        const int nb = min(ROUTER_RB, y1 - b0);
+        if constexpr (STAGED) {
+            if (b0 + ROUTER_RB < y1) {
+                stage(b0 + ROUTER_RB, (pass + 1) & 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            __syncthreads();
+        }
         const uint2* hrow[ROUTER_RB];
         bool hv[ROUTER_RB];
 #pragma unroll
         for (int rb = 0; rb < ROUTER_RB; ++rb) {
-            int r = -1;
-            if (rb < nb) {
-                r = rows ? rows[b0 + rb] : b0 + rb;   // no rows: route every row
-                if (r < 0 || (P >= 0 && r >= P)) r = -1;
-            }
+            const int r = rb < nb ? row_of(b0 + rb) : -1;
             hv[rb] = r >= 0;
-            hrow[rb] = reinterpret_cast<const uint2*>(hidden + (size_t)(r >= 0 ? r : 0) * d);
+            if (STAGED)
+                hrow[rb] = reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(rstage) +
+                                                          ((size_t)(pass & 1) * ROUTER_RB + rb) * d);
+            else
+                hrow[rb] = reinterpret_cast<const uint2*>(hidden + (size_t)(r >= 0 ? r : 0) * d);
         }
         float acc[ROUTER_RB];
 #pragma unroll
@@ -106,7 +144,8 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
                         const int c = lane + 32 * (u0 + u);
 #pragma unroll
                         for (int rb = 0; rb < ROUTER_RB; ++rb)
-                            hx[u][rb] = (hv[rb] && c < d4) ? __ldg(hrow[rb] + c) : make_uint2(0u, 0u);
+                            hx[u][rb] = (hv[rb] && c < d4) ? (STAGED ? hrow[rb][c] : __ldg(hrow[rb] + c))
+                                                           : make_uint2(0u, 0u);
                     }
 #pragma unroll
                     for (int u = 0; u < ROUTER_LB; ++u)
@@ -125,7 +164,8 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
                         if (c < d4) {
 #pragma unroll
                             for (int rb = 0; rb < ROUTER_RB; ++rb)
-                                if (hv[rb]) acc[rb] = dot4(wl[u], __ldg(hrow[rb] + c), acc[rb]);
+                                if (hv[rb])
+                                    acc[rb] = dot4(wl[u], STAGED ? hrow[rb][c] : __ldg(hrow[rb] + c), acc[rb]);
                         }
                     }
                 }
@@ -190,9 +230,23 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
     if (B == 0) return WF_OK;
     Control* ctrl = reinterpret_cast<Control*>(ws);
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
-    return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA), cdiv(B, ROUTER_ROWS_PER_CTA)),
-                  dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d, m, P, W1, b1, w2, b2, tau, delta_al, route, part,
-                  ctrl);
+    const dim3 grid(cdiv(m, ROUTER_UNITS_PER_CTA), cdiv(B, ROUTER_ROWS_PER_CTA));
+    if (rows == nullptr || d > 32 * 4 * ROUTER_WREG)
+        return launch(router_kernel<false>, grid, dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d, m, P, W1, b1, w2,
+                      b2, tau, delta_al, route, part, ctrl);
+    // chosen rows after acceptance: rows staged in shared memory, two passes in flight
+    const size_t smem = (size_t)2 * ROUTER_RB * d * 2;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(router_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 2 * ROUTER_RB * 32 * 4 * ROUTER_WREG * 2) != cudaSuccess)
+            return WF_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    return launch(router_kernel<true>, grid, dim3(ROUTER_THREADS), smem, s, hidden, rows, B, d, m, P, W1, b1, w2,
+                  b2, tau, delta_al, route, part, ctrl);
 }
 
 }  // namespace wf
