@@ -41,8 +41,6 @@ constexpr int PJ_THREADS = 192;
 constexpr int PJ_BN_MAX = 256;
 constexpr int PJ_A_BYTES = BM * BK * 2;           // 16 KB
 constexpr int PJ_B_BYTES = PJ_BN_MAX * BK * 2;    // 32 KB
-// ring, alignment slack, barriers and the destination row and position of each tile row
-constexpr int PJ_SMEM = PJ_STAGES * (PJ_A_BYTES + PJ_B_BYTES) + 1024 + 256 + BM * 12;
 constexpr int PJ_MAX_SPLIT = 8;      // K splits of one tile: the portable cluster size
 constexpr int PJ_BN_CU = 192;        // widest output tile: partial, reduced and staged tiles fit the ring
 constexpr int AT_MAX_CHUNKS = 64;    // cache-row splits per (sequence, KV head)
@@ -247,6 +245,7 @@ struct PjParams {
     PjSeg seg[3];
     int nseg;
     int bn, num_k, kb_per, S;   // tile width, K blocks, K blocks per split, splits (= cluster size)
+    int stages, tmem_cols;      // ring stages; TMEM columns allocated (a power of two >= bn)
     uint32_t idesc;
     const int32_t* bl_off;
     const int32_t* cache_len;
@@ -274,25 +273,31 @@ __device__ __forceinline__ float dsmem_ld(uint32_t addr) {
 }
 
 // One CTA per (output tile, K split); the S splits of a tile form one
-// cluster.  Each split leaves its fp32 partial tile in its own shared memory;
-// after a cluster barrier, split r sums rows [r BM/S, (r+1) BM/S) of all S
-// partials (in split order) over distributed shared memory and applies the
-// epilogue to them.
-__global__ void __launch_bounds__(PJ_THREADS, 1)
+// cluster.  Each split leaves its fp32 partial tile in its own shared memory
+// (row-major, odd row pitch); after a cluster barrier, split r finishes rows
+// [r BM/S, (r+1) BM/S) of the tile, summing the S partials (in split order)
+// over distributed shared memory as it goes.  Epilogue items run column
+// (or rotation pair) fastest, so shared-memory reads are conflict-free and a
+// warp's global stores are contiguous.  The ring holds p.stages stages of a
+// 128-row activation box and a bn-row weight box; with a short ring two CTAs
+// share an SM.
+__global__ void __launch_bounds__(PJ_THREADS)
     proj_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                 const __grid_constant__ CUtensorMap tmW2, const PjParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stages = p.stages;
+    const int bstage = p.bn * BK * 2;
     uint8_t* sA = smem;
-    uint8_t* sB = smem + PJ_STAGES * PJ_A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + PJ_STAGES * PJ_B_BYTES);
-    uint64_t* empty = full + PJ_STAGES;
-    uint64_t* tfull = empty + PJ_STAGES;
+    uint8_t* sB = smem + stages * PJ_A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + stages * bstage);
+    uint64_t* empty = full + stages;
+    uint64_t* tfull = empty + stages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int64_t* rowdst = reinterpret_cast<int64_t*>(tmem_slot + 4);   // [BM] destination cache row, or -1
-                                                                   // then [BM] int: position / final row
+    int* rowpos = reinterpret_cast<int*>(rowdst + BM);              // [BM] position / final backlog row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.S;
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     const CUtensorMap* mW = g.w == 0 ? &tmW0 : (g.w == 1 ? &tmW1 : &tmW2);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < PJ_STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -318,52 +323,63 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
         tma_prefetch_desc(mW);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, PJ_BN_MAX);
+        tmem_alloc(tmem_slot, p.tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The weights are no earlier kernel's output: the first ring stages'
+    // weight boxes are requested before waiting for the kernel that writes the
+    // activations, and their activation boxes right after it.
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    const uint32_t tx = (uint32_t)(g.a_rows * BK * 2 + bstage);
+    const int early = min(stages, kb1 - kb0);   // stages whose weights are requested early
+    if (warp == 0 && lane == 0)
+        for (int i = 0; i < early; ++i) {   // fresh barriers: the ring is empty
+            mbar_arrive_expect_tx(&full[i], tx);
+            tma_load_2d(sB + i * bstage, mW, &full[i], (kb0 + i) * BK, nt * p.bn, pol_w);
+        }
     pdl_wait();
     pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_a = policy_evict_last();
-            const uint32_t tx = (uint32_t)(g.a_rows * BK * 2 + p.bn * BK * 2);
-            int i = 0;
-            for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                const int s = i % PJ_STAGES;
-                if (!mbar_wait(&empty[s], ((i / PJ_STAGES) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+            for (int i = 0; i < early; ++i)
+                tma_load_2d(sA + i * PJ_A_BYTES, mA, &full[i], (kb0 + i) * BK, mt * BM, pol_a);
+            int i = early;
+            for (int kb = kb0 + early; kb < kb1; ++kb, ++i) {
+                const int s = i % stages;
+                if (!mbar_wait(&empty[s], ((i / stages) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                     *abort_flag = 1;
                     record_error(p.ctrl, WF_ERR_TIMEOUT, 0x500 + s);
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], tx);
                 tma_load_2d(sA + s * PJ_A_BYTES, mA, &full[s], kb * BK, mt * BM, pol_a);
-                tma_load_2d(sB + s * PJ_B_BYTES, mW, &full[s], kb * BK, nt * p.bn, pol_w);
+                tma_load_2d(sB + s * bstage, mW, &full[s], kb * BK, nt * p.bn, pol_w);
             }
             if (*abort_flag)   // let every copy issued above land before the shared memory is reused
-                for (int j = (i > PJ_STAGES ? i - PJ_STAGES : 0); j < i; ++j)
-                    mbar_wait(&full[j % PJ_STAGES], (j / PJ_STAGES) & 1, p.timeout_ns, nullptr);
+                for (int j = (i > stages ? i - stages : 0); j < i; ++j)
+                    mbar_wait(&full[j % stages], (j / stages) & 1, p.timeout_ns, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int i = 0;
             for (int kb = kb0; kb < kb1; ++kb, ++i) {
-                const int s = i % PJ_STAGES;
-                if (!mbar_wait(&full[s], (i / PJ_STAGES) & 1, p.timeout_ns, abort_flag)) {
+                const int s = i % stages;
+                if (!mbar_wait(&full[s], (i / stages) & 1, p.timeout_ns, abort_flag)) {
                     *abort_flag = 1;
                     record_error(p.ctrl, WF_ERR_TIMEOUT, 0x510 + s);
                     break;
                 }
                 tc_fence_after();
                 const uint64_t adesc = umma_desc_sw128(smem_u32(sA + s * PJ_A_BYTES));
-                const uint64_t bdesc = umma_desc_sw128(smem_u32(sB + s * PJ_B_BYTES));
+                const uint64_t bdesc = umma_desc_sw128(smem_u32(sB + s * bstage));
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, p.idesc, (i | kk) != 0);
@@ -382,7 +398,8 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
         tc_fence_after();
         if (!*abort_flag) {
             // the ring is free: every MMA (hence every copy) of this CTA has completed
-            float* pf = reinterpret_cast<float*>(smem);   // [bn][BM]
+            float* pf = reinterpret_cast<float*>(smem);   // [BM][bn + 1]
+            const int pfs = p.bn + 1;
             const uint32_t tb = tmem_base + ((uint32_t)(q4 * 32) << 16);
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
                 uint32_t r[32];
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (c0 + j < p.bn) pf[(c0 + j) * BM + rit] = __uint_as_float(r[j]);
+                    if (c0 + j < p.bn) pf[rit * pfs + c0 + j] = __uint_as_float(r[j]);
             }
         }
         tc_fence_before();
@@ -398,51 +415,27 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
     __syncthreads();
     if (S > 1) cluster_sync();   // every split's partial tile is in its shared memory
 
-    // ---------------------------------------------------- reduce this split's rows over the cluster
+    // ---------------------------------------------------- epilogue of this split's rows
     const int rpc = BM / S;                 // rows this CTA finishes
     const int r0 = split * rpc;
     const int nrows = max(0, min(rpc, g.M - (mt * BM + r0)));   // of them, rows that exist
     const int col0 = nt * p.bn;
     const int ncols = min(p.bn, g.N - col0);
+    const int pfs = p.bn + 1;
     const float* pf = reinterpret_cast<const float*>(smem);
-    float* sf = reinterpret_cast<float*>(smem + (size_t)p.bn * BM * 4);   // [rpc][bn + 1] (S > 1)
-    const int sfs = p.bn + 1;
-    if (S > 1) {
-        // item (row, column), row fastest; four items per thread in flight
-        const uint32_t pf_local = smem_u32(pf);
-        const int items = nrows * ncols;
-        for (int base = threadIdx.x; base < items; base += 4 * PJ_THREADS) {
-            float x[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t off[4];
+    const uint32_t pf_local = smem_u32(pf);
+    // row rl's column c, summed over the splits in split order
+    auto val = [&](int rl, int c) {
+        if (S == 1) return pf[(r0 + rl) * pfs + c];
+        const uint32_t off = pf_local + (uint32_t)(((r0 + rl) * pfs + c) * 4);
+        float y[PJ_MAX_SPLIT];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int idx = min(base + u * PJ_THREADS, items - 1);
-                const int c = idx / nrows, rl = idx - c * nrows;
-                off[u] = pf_local + (uint32_t)((c * BM + r0 + rl) * 4);
-            }
-            for (int s = 0; s < S; ++s) {
-                float y[4];
+        for (int s2 = 0; s2 < PJ_MAX_SPLIT; ++s2) y[s2] = s2 < S ? dsmem_ld(dsmem_map(off, (uint32_t)s2)) : 0.f;
+        float x = 0.f;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) y[u] = dsmem_ld(dsmem_map(off[u], (uint32_t)s));
-#pragma unroll
-                for (int u = 0; u < 4; ++u) x[u] += y[u];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int idx = base + u * PJ_THREADS;
-                if (idx < items) {
-                    const int c = idx / nrows, rl = idx - c * nrows;
-                    sf[rl * sfs + c] = x[u];
-                }
-            }
-        }
-        __syncthreads();
-        cluster_sync();   // no CTA leaves while a peer may still read its partial tile
-    }
-    auto val = [&](int rl, int c) { return S > 1 ? sf[rl * sfs + c] : pf[c * BM + r0 + rl]; };
-
-    // ---------------------------------------------------- epilogue of rows r0 .. r0 + nrows - 1
-    int* rowpos = reinterpret_cast<int*>(rowdst + BM);
+        for (int s2 = 0; s2 < PJ_MAX_SPLIT; ++s2) x += y[s2];
+        return x;
+    };
     if (!*abort_flag && nrows > 0) {
         const bool cached = g.mode == PJ_KEY || g.mode == PJ_VALUE;
         if (threadIdx.x < nrows) {   // per-row position / destination
@@ -463,20 +456,21 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
             }
         }
         __syncthreads();
-        uint16_t* stile = reinterpret_cast<uint16_t*>(smem + (size_t)p.bn * BM * 4 +
-                                                      (S > 1 ? align_up((size_t)rpc * sfs * 4, 16) : 0));
         if (g.mode == PJ_KEY || g.mode == PJ_QUERY) {
-            // item (row, rotation pair), row fastest
+            // item (row, rotation pair), pair fastest
             const int half = p.D / 2;
-            const int items = nrows * (ncols / 2);
-            for (int idx = threadIdx.x; idx < items; idx += PJ_THREADS) {
-                const int pi = idx / nrows, rl = idx - pi * nrows;
+            const int npairs = ncols / 2;
+            for (int idx = threadIdx.x; idx < nrows * npairs; idx += PJ_THREADS) {
+                const int rl = idx / npairs, pi = idx - rl * npairs;
                 const int h0 = (pi / half) * p.D, i = pi - (pi / half) * half;
                 float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
                 rope_pair(x1, x2, rowpos[rl], p.rope[i]);
                 if (g.mode == PJ_KEY) {
-                    stile[rl * p.bn + h0 + i] = f32_to_bf16(x1);
-                    stile[rl * p.bn + h0 + i + half] = f32_to_bf16(x2);
+                    const int64_t d = rowdst[rl];
+                    if (d >= 0) {
+                        p.Kc[d * p.GD + col0 + h0 + i] = f32_to_bf16(x1);
+                        p.Kc[d * p.GD + col0 + h0 + i + half] = f32_to_bf16(x2);
+                    }
                 } else {
                     const size_t o = (size_t)(mt * BM + r0 + rl) * p.HD + col0 + h0 + i;
                     p.q[o] = x1;
@@ -484,12 +478,13 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
                 }
             }
         } else {
-            const int items = nrows * ncols;
-            for (int idx = threadIdx.x; idx < items; idx += PJ_THREADS) {
-                const int c = idx / nrows, rl = idx - c * nrows;
+            // item (row, column), column fastest
+            for (int idx = threadIdx.x; idx < nrows * ncols; idx += PJ_THREADS) {
+                const int rl = idx / ncols, c = idx - rl * ncols;
                 const float x = val(rl, c);
                 if (g.mode == PJ_VALUE) {
-                    stile[rl * p.bn + c] = f32_to_bf16(x);
+                    const int64_t d = rowdst[rl];
+                    if (d >= 0) p.Vc[d * p.GD + col0 + c] = f32_to_bf16(x);
                 } else {
                     const int f = rowpos[rl];
                     const float res = (f >= 0 && f < p.N) ? bf16_to_f32(p.u[(size_t)f * p.din + col0 + c]) : 0.f;
@@ -497,24 +492,16 @@ __global__ void __launch_bounds__(PJ_THREADS, 1)
                 }
             }
         }
-        if (cached) {
-            __syncthreads();
-            uint16_t* cache = g.mode == PJ_KEY ? p.Kc : p.Vc;
-            const int cpr = ncols / 8;   // 16-byte pieces of a row segment
-            for (int idx = threadIdx.x; idx < nrows * cpr; idx += PJ_THREADS) {
-                const int rr = idx / cpr, j = idx - rr * cpr;
-                const int64_t d = rowdst[rr];
-                if (d >= 0)
-                    *reinterpret_cast<uint4*>(cache + d * p.GD + col0 + j * 8) =
-                        *reinterpret_cast<const uint4*>(stile + rr * p.bn + j * 8);
-            }
-        }
+    }
+    if (S > 1) {
+        __syncthreads();
+        cluster_sync();   // no CTA leaves while a peer may still read its partial tile
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, PJ_BN_MAX);
+    if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
 // ------------------------------------------------------------------ attention
@@ -589,39 +576,62 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, cq = lane & 3;   // fragment row group, column pair
-    pdl_wait();
-    pdl_trigger();
+    // the split's rows follow from the call's inputs alone
     int T = p.cache_len[b] + (p.bl_off[b + 1] - p.bl_off[b]);
     T = T < 0 ? 0 : (T > p.cap ? p.cap : T);
+    int Lold = p.cache_len[b];   // rows cached before this call: no kernel of the call writes them
+    Lold = Lold < 0 ? 0 : (Lold > T ? T : Lold);
     const int per = (T + p.chunks - 1) / p.chunks;
     const int t0 = c * per, t1 = min(T, t0 + per);
+    const uint16_t* Kb = p.Kc + (size_t)b * p.cap * p.GD + (size_t)g * D;
+    const uint16_t* Vb = p.Vc + (size_t)b * p.cap * p.GD + (size_t)g * D;
+    const int cpr = D / 8;   // 16-byte pieces per row
+    // asynchronous copies of rows [rfrom, rto) of the pass at p0 into buffer `which`
+    auto stage_rows = [&](int p0, int which, int rfrom, int rto) {
+        uint16_t* Kd = Kbuf + which * buf;
+        uint16_t* Vd = Kd + (size_t)R * stride;
+        for (int idx = tid; idx < (rto - rfrom) * cpr; idx += AT_THREADS) {
+            const int r = rfrom + idx / cpr, j = idx - (idx / cpr) * cpr;
+            cp_async16(Kd + (size_t)r * stride + j * 8, Kb + (size_t)(p0 + r) * p.GD + j * 8);
+            cp_async16(Vd + (size_t)r * stride + j * 8, Vb + (size_t)(p0 + r) * p.GD + j * 8);
+        }
+    };
+    // value rows past the range are multiplied by probability 0: they must
+    // hold numbers, not whatever the buffer held before
+    auto zero_tail = [&](int which, int nr) {
+        uint16_t* Vd = Kbuf + which * buf + (size_t)R * stride;
+        for (int idx = tid; idx < (R - nr) * cpr; idx += AT_THREADS) {
+            const int r = nr + idx / cpr, j = idx - (idx / cpr) * cpr;
+            *reinterpret_cast<uint4*>(Vd + (size_t)r * stride + j * 8) = make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto stage = [&](int p0, int which) {
+        const int nr = min(R, t1 - p0);
+        stage_rows(p0, which, 0, nr);
+        zero_tail(which, nr);
+        cp_async_commit();
+    };
+    // the first pass's previously cached rows stream in while the kernel
+    // before this one (which writes the new rows and the query) finishes
+    const int nr0 = t0 < t1 ? min(R, t1 - t0) : 0;
+    const int split0 = max(0, min(nr0, Lold - t0));
+    if (nr0 > 0) {
+        stage_rows(t0, 0, 0, split0);
+        zero_tail(0, nr0);
+        cp_async_commit();
+    }
+    pdl_wait();
+    pdl_trigger();
     const float qscale = 1.4426950408889634f / sqrtf((float)D);
     for (int i = tid; i < 16 * D; i += AT_THREADS) {
         const int h = i / D, e = i - h * D;
         const float v = h < hq ? p.q[(size_t)b * p.HD + ((size_t)g * hq + h) * D + e] * qscale : 0.f;
         qs[h * stride + e] = f32_to_bf16(v);
     }
-    const uint16_t* Kb = p.Kc + (size_t)b * p.cap * p.GD + (size_t)g * D;
-    const uint16_t* Vb = p.Vc + (size_t)b * p.cap * p.GD + (size_t)g * D;
-    const int cpr = D / 8;   // 16-byte pieces per row
-    auto stage = [&](int p0, int which) {
-        const int nr = min(R, t1 - p0);
-        uint16_t* Kd = Kbuf + which * buf;
-        uint16_t* Vd = Kd + (size_t)R * stride;
-        for (int idx = tid; idx < nr * cpr; idx += AT_THREADS) {
-            const int r = idx / cpr, j = idx - r * cpr;
-            cp_async16(Kd + (size_t)r * stride + j * 8, Kb + (size_t)(p0 + r) * p.GD + j * 8);
-            cp_async16(Vd + (size_t)r * stride + j * 8, Vb + (size_t)(p0 + r) * p.GD + j * 8);
-        }
-        // value rows past the range are multiplied by probability 0: they must
-        // hold numbers, not whatever the buffer held before
-        for (int idx = tid; idx < (R - nr) * cpr; idx += AT_THREADS) {
-            const int r = nr + idx / cpr, j = idx - (idx / cpr) * cpr;
-            *reinterpret_cast<uint4*>(Vd + (size_t)r * stride + j * 8) = make_uint4(0, 0, 0, 0);
-        }
+    if (nr0 > 0) {
+        stage_rows(t0, 0, split0, nr0);
         cp_async_commit();
-    };
-    if (t0 < t1) stage(t0, 0);
+    }
     __syncthreads();   // qs written
 
     const int nks = D / 16, ndt = D / 8;
@@ -801,46 +811,90 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
         mtot[tid] = L > 0.f ? 1.f / L : 0.f;
     }
     __syncthreads();
-    for (int idx = tid; idx < hq * D / 2; idx += AT_THREADS) {
-        const int h = idx / (D / 2), e2 = idx - h * (D / 2);
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll 8
-        for (int s2 = 0; s2 < p.chunks; ++s2) {
-            const float w = wgt[s2 * hq + h];
-            const float2 ov = __ldcg(reinterpret_cast<const float2*>(allp + ((size_t)s2 * hq + h) * (D + 2) + 2 * e2));
-            a0 = fmaf(w, ov.x, a0);
-            a1 = fmaf(w, ov.y, a1);
+    // two output pairs per thread at a time, eight splits each per step: 16 loads in flight
+    const int nitems = hq * D / 2;
+    for (int base = tid; base < nitems; base += 2 * AT_THREADS) {
+        int hh[2], ee[2];
+        bool live[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int idx = base + u * AT_THREADS;
+            live[u] = idx < nitems;
+            const int id = live[u] ? idx : 0;
+            hh[u] = id / (D / 2);
+            ee[u] = id - hh[u] * (D / 2);
         }
-        const float r0 = a0 * mtot[h], r1 = a1 * mtot[h];
-        const size_t o2 = (size_t)b * p.HD + ((size_t)g * hq + h) * D + 2 * e2;
-        *reinterpret_cast<uint32_t*>(p.obf + o2) = pack_bf16x2(r0, r1);
-        if (p.attn) {
-            p.attn[o2] = r0;
-            p.attn[o2 + 1] = r1;
+        float a0[2] = {0.f, 0.f}, a1[2] = {0.f, 0.f};
+        for (int s0 = 0; s0 < p.chunks; s0 += 8) {
+            float2 ov[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    ov[u][j] = (s0 + j < p.chunks)
+                                   ? __ldcg(reinterpret_cast<const float2*>(
+                                         allp + ((size_t)(s0 + j) * hq + hh[u]) * (D + 2) + 2 * ee[u]))
+                                   : make_float2(0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (s0 + j < p.chunks) {
+                        const float w = wgt[(s0 + j) * hq + hh[u]];
+                        a0[u] = fmaf(w, ov[u][j].x, a0[u]);
+                        a1[u] = fmaf(w, ov[u][j].y, a1[u]);
+                    }
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (live[u]) {
+                const float r0 = a0[u] * mtot[hh[u]], r1 = a1[u] * mtot[hh[u]];
+                const size_t o2 = (size_t)b * p.HD + ((size_t)g * hq + hh[u]) * D + 2 * ee[u];
+                *reinterpret_cast<uint32_t*>(p.obf + o2) = pack_bf16x2(r0, r1);
+                if (p.attn) {
+                    p.attn[o2] = r0;
+                    p.attn[o2 + 1] = r1;
+                }
+            }
     }
     if (tid == 0) p.cnt[(size_t)b * p.G + g] = 0;
 }
 
 // ------------------------------------------------------------------ host side
+// Shared memory of a proj_kernel CTA with `stages` ring stages of tile width bn.
+static size_t proj_smem(int stages, int bn) {
+    return 1024 + (size_t)stages * (PJ_A_BYTES + (size_t)bn * BK * 2) + 256 + BM * 12;
+}
+
 static wf_status launch_proj(const CUtensorMap* mA, const CUtensorMap* mW, PjParams p, int tiles, cudaStream_t s) {
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PJ_SMEM) != cudaSuccess)
+        if (cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)proj_smem(PJ_STAGES, PJ_BN_CU)) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
     }
-    // split K (a power of two up to the portable cluster size) so that about
-    // one wave of CTAs covers the SMs
+    // A three-stage ring lets two CTAs share an SM when the tile is narrow;
+    // the partial tile ([BM][bn + 1] fp32) reuses the ring and must fit in it.
+    int stages = 3;
+    if (2 * (proj_smem(stages, p.bn) + 1024) > 228 * 1024) stages = PJ_STAGES;
+    while ((size_t)stages * (PJ_A_BYTES + (size_t)p.bn * BK * 2) < (size_t)BM * (p.bn + 1) * 4) ++stages;
+    const size_t smem = proj_smem(stages, p.bn);
+    const int per_sm = 2 * (smem + 1024) <= 228 * 1024 ? 2 : 1;
+    p.stages = stages;
+    p.tmem_cols = 32;
+    while (p.tmem_cols < p.bn) p.tmem_cols *= 2;
+    // split K (a power of two up to the portable cluster size) so that the
+    // CTAs fill the SMs about once
     int S = 1;
-    while (S < PJ_MAX_SPLIT && tiles * 2 * S <= num_sms() && 2 * S <= p.num_k) S *= 2;
+    while (S < PJ_MAX_SPLIT && tiles * 2 * S <= per_sm * num_sms() && 2 * S <= p.num_k) S *= 2;
     p.kb_per = cdiv(p.num_k, S);
     while (S > 1 && (S - 1) * p.kb_per >= p.num_k) S /= 2;   // every split gets at least one K block
     p.kb_per = cdiv(p.num_k, S);
     p.S = S;
-    return launch_cluster(proj_kernel, dim3(tiles * S), dim3(PJ_THREADS), PJ_SMEM, s, (unsigned)S, mA[0], mA[1],
+    return launch_cluster(proj_kernel, dim3(tiles * S), dim3(PJ_THREADS), smem, s, (unsigned)S, mA[0], mA[1],
                           mW[0], mW[1], mW[2], p);
 }
 
