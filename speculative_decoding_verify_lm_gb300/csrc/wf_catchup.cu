@@ -38,13 +38,13 @@ namespace wf {
 // ------------------------------------------------------------------ geometry
 constexpr int PJ_STAGES = 4;
 constexpr int PJ_THREADS = 192;
-constexpr int PJ_BN_MAX = 256;
 constexpr int PJ_A_BYTES = BM * BK * 2;           // 16 KB
-constexpr int PJ_B_BYTES = PJ_BN_MAX * BK * 2;    // 32 KB
+
 constexpr int PJ_MAX_SPLIT = 8;      // K splits of one tile: the portable cluster size
 constexpr int PJ_BN_CU = 192;        // widest output tile: partial, reduced and staged tiles fit the ring
 constexpr int AT_MAX_CHUNKS = 64;    // cache-row splits per (sequence, KV head)
 constexpr int AT_PASS_ROWS = 128;    // cache rows an attention CTA stages per pass (two passes in flight)
+constexpr int AT_SPLIT_ROWS = 256;   // smallest split of a cache worth its merge
 constexpr int NORM_ROWS_PER_CTA = 4;
 constexpr int NORM_REG_CHUNKS = 16;  // 16-byte pieces of a row a lane keeps in registers
 
@@ -209,8 +209,7 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float rs = 1.0f / sqrtf(ss / (float)din + eps);
     const uint4* gm = reinterpret_cast<const uint4*>(gamma);
-    auto emit = [&](int c, const uint4 v) {
-        const uint4 gv = __ldg(gm + c);
+    auto emit_g = [&](int c, const uint4 v, const uint4 gv) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w}, g[4] = {gv.x, gv.y, gv.z, gv.w};
         uint32_t o[4];
 #pragma unroll
@@ -222,11 +221,16 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
         reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
     };
     if (in_regs) {
+        // the gains first, all loads in flight together, then the outputs
+        uint4 gr[NORM_REG_CHUNKS];
 #pragma unroll
         for (int k = 0; k < NORM_REG_CHUNKS; ++k)
-            if (lane + 32 * k < chunks) emit(lane + 32 * k, xr[k]);
+            gr[k] = lane + 32 * k < chunks ? __ldg(gm + lane + 32 * k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < NORM_REG_CHUNKS; ++k)
+            if (lane + 32 * k < chunks) emit_g(lane + 32 * k, xr[k], gr[k]);
     } else {
-        for (int c = lane; c < chunks; c += 32) emit(c, __ldg(x + c));
+        for (int c = lane; c < chunks; c += 32) emit_g(c, __ldg(x + c), __ldg(gm + c));
     }
 }
 
@@ -266,10 +270,139 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float dsmem_ld(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    return (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
+}
+
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
     return v;
+}
+
+struct EpiCtx {
+    const PjParams& p;
+    const PjSeg& g;
+    int mt, r0, nrows, col0, ncols, pfs;
+    uint32_t pf_local;
+    const int64_t* rowdst;
+    const int* rowpos;
+    const float2* srope;
+};
+
+// Four columns of row rl (local row of this split's slice) starting at
+// column c, summed over the S splits' partial tiles in split order (and, with
+// pair_off, the same columns pair_off further on).  All of the loads are
+// issued before any is used.
+template <int S>
+__device__ __forceinline__ void pull4(const EpiCtx& e, int rl, int c, int pair_off, float4& x, float4& x2) {
+    const uint32_t off = e.pf_local + (uint32_t)(((e.r0 + rl) * e.pfs + c) * 4);
+    float4 y[S], y2[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const uint32_t a = S == 1 ? off : dsmem_map(off, (uint32_t)s);
+        if (S == 1) {
+            y[s] = *reinterpret_cast<const float4*>(__cvta_shared_to_generic(a));
+            if (pair_off) y2[s] = *reinterpret_cast<const float4*>(__cvta_shared_to_generic(a + pair_off * 4));
+        } else {
+            y[s] = dsmem_ld4(a);
+            if (pair_off) y2[s] = dsmem_ld4(a + (uint32_t)pair_off * 4);
+        }
+    }
+    x = y[0];
+    x2 = pair_off ? y2[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 1; s < S; ++s) {
+        x.x += y[s].x; x.y += y[s].y; x.z += y[s].z; x.w += y[s].w;
+        if (pair_off) { x2.x += y2[s].x; x2.y += y2[s].y; x2.z += y2[s].z; x2.w += y2[s].w; }
+    }
+}
+
+// The epilogue of one split's rows: items of 4 columns (or 4 rotation pairs),
+// columns fastest, NB items per thread in flight together (NB x S x 2 vector
+// loads at most 16).
+template <int S>
+__device__ void proj_epilogue(const EpiCtx& e) {
+    constexpr int NB = 8 / S > 0 ? 8 / S : 1;
+    const PjParams& p = e.p;
+    const PjSeg& g = e.g;
+    if (g.mode == PJ_KEY || g.mode == PJ_QUERY) {
+        const int half = p.D / 2;              // a multiple of 8
+        const int nq = e.ncols / 8;            // groups of 4 pairs per row
+        const int items = e.nrows * nq;
+        for (int base = threadIdx.x; base < items; base += NB * PJ_THREADS) {
+            int rl[NB], cc[NB], ii[NB];
+            float4 x1[NB], x2[NB];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int idx = min(base + u * PJ_THREADS, items - 1);
+                rl[u] = idx / nq;
+                const int pi = (idx - rl[u] * nq) * 4;   // first pair of the group
+                ii[u] = pi - (pi / half) * half;
+                cc[u] = (pi / half) * p.D + ii[u];
+                pull4<S>(e, rl[u], cc[u], half, x1[u], x2[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                if (base + u * PJ_THREADS >= items) continue;
+                float a1[4] = {x1[u].x, x1[u].y, x1[u].z, x1[u].w};
+                float a2[4] = {x2[u].x, x2[u].y, x2[u].z, x2[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) rope_pair(a1[j], a2[j], e.rowpos[rl[u]], e.srope[ii[u] + j]);
+                if (g.mode == PJ_KEY) {
+                    const int64_t d = e.rowdst[rl[u]];
+                    if (d >= 0) {
+                        uint16_t* k1 = p.Kc + d * p.GD + e.col0 + cc[u];
+                        *reinterpret_cast<uint2*>(k1) = make_uint2(pack2_bf16(a1[0], a1[1]), pack2_bf16(a1[2], a1[3]));
+                        *reinterpret_cast<uint2*>(k1 + half) =
+                            make_uint2(pack2_bf16(a2[0], a2[1]), pack2_bf16(a2[2], a2[3]));
+                    }
+                } else {
+                    float* q1 = p.q + (size_t)(e.mt * BM + e.r0 + rl[u]) * p.HD + e.col0 + cc[u];
+                    *reinterpret_cast<float4*>(q1) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+                    *reinterpret_cast<float4*>(q1 + half) = make_float4(a2[0], a2[1], a2[2], a2[3]);
+                }
+            }
+        }
+    } else {
+        constexpr int NB2 = 2 * NB;
+        const int nq = (e.ncols + 3) / 4;
+        const int items = e.nrows * nq;
+        for (int base = threadIdx.x; base < items; base += NB2 * PJ_THREADS) {
+            int rl[NB2], cc[NB2];
+            float4 x[NB2], unused;
+#pragma unroll
+            for (int u = 0; u < NB2; ++u) {
+                const int idx = min(base + u * PJ_THREADS, items - 1);
+                rl[u] = idx / nq;
+                cc[u] = (idx - rl[u] * nq) * 4;
+                pull4<S>(e, rl[u], cc[u], 0, x[u], unused);
+            }
+#pragma unroll
+            for (int u = 0; u < NB2; ++u) {
+                if (base + u * PJ_THREADS >= items) continue;
+                const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                if (g.mode == PJ_VALUE) {
+                    const int64_t d = e.rowdst[rl[u]];
+                    if (d >= 0)   // whole heads: ncols is a multiple of 16
+                        *reinterpret_cast<uint2*>(p.Vc + d * p.GD + e.col0 + cc[u]) =
+                            make_uint2(pack2_bf16(xv[0], xv[1]), pack2_bf16(xv[2], xv[3]));
+                } else {
+                    const int f = e.rowpos[rl[u]];
+                    const bool fok = f >= 0 && f < p.N;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (cc[u] + j < e.ncols) {
+                            const float res = fok ? bf16_to_f32(p.u[(size_t)f * p.din + e.col0 + cc[u] + j]) : 0.f;
+                            p.out[(size_t)(e.mt * BM + e.r0 + rl[u]) * p.din + e.col0 + cc[u] + j] = res + xv[j];
+                        }
+                }
+            }
+        }
+    }
 }
 
 // One CTA per (output tile, K split); the S splits of a tile form one
@@ -298,6 +431,7 @@ __global__ void __launch_bounds__(PJ_THREADS)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int64_t* rowdst = reinterpret_cast<int64_t*>(tmem_slot + 4);   // [BM] destination cache row, or -1
     int* rowpos = reinterpret_cast<int*>(rowdst + BM);              // [BM] position / final backlog row
+    float2* srope = reinterpret_cast<float2*>(rowpos + BM);         // [D / 2] rotary table
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.S;
@@ -398,16 +532,17 @@ __global__ void __launch_bounds__(PJ_THREADS)
         tc_fence_after();
         if (!*abort_flag) {
             // the ring is free: every MMA (hence every copy) of this CTA has completed
-            float* pf = reinterpret_cast<float*>(smem);   // [BM][bn + 1]
-            const int pfs = p.bn + 1;
+            float* pf = reinterpret_cast<float*>(smem);   // [BM][bn + 4]
+            const int pfs = p.bn + 4;
             const uint32_t tb = tmem_base + ((uint32_t)(q4 * 32) << 16);
             for (int c0 = 0; c0 < p.bn; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tb + c0, r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < p.bn) pf[rit * pfs + c0 + j] = __uint_as_float(r[j]);
+                for (int j = 0; j < 32; j += 4)
+                    if (c0 + j < p.bn)
+                        *reinterpret_cast<uint4*>(pf + rit * pfs + c0 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
             }
         }
         tc_fence_before();
@@ -416,28 +551,19 @@ __global__ void __launch_bounds__(PJ_THREADS)
     if (S > 1) cluster_sync();   // every split's partial tile is in its shared memory
 
     // ---------------------------------------------------- epilogue of this split's rows
-    const int rpc = BM / S;                 // rows this CTA finishes
+    // Split r finishes rows [r0, r0 + rpc) of the tile, rpc = BM / S, pulling
+    // the other splits' partial rows over distributed shared memory (every
+    // split's loads of an item in flight together) and summing in split order.
+    const int rpc = BM / S;
     const int r0 = split * rpc;
     const int nrows = max(0, min(rpc, g.M - (mt * BM + r0)));   // of them, rows that exist
     const int col0 = nt * p.bn;
     const int ncols = min(p.bn, g.N - col0);
-    const int pfs = p.bn + 1;
-    const float* pf = reinterpret_cast<const float*>(smem);
-    const uint32_t pf_local = smem_u32(pf);
-    // row rl's column c, summed over the splits in split order
-    auto val = [&](int rl, int c) {
-        if (S == 1) return pf[(r0 + rl) * pfs + c];
-        const uint32_t off = pf_local + (uint32_t)(((r0 + rl) * pfs + c) * 4);
-        float y[PJ_MAX_SPLIT];
-#pragma unroll
-        for (int s2 = 0; s2 < PJ_MAX_SPLIT; ++s2) y[s2] = s2 < S ? dsmem_ld(dsmem_map(off, (uint32_t)s2)) : 0.f;
-        float x = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < PJ_MAX_SPLIT; ++s2) x += y[s2];
-        return x;
-    };
+    const int pfs = p.bn + 4;   // row pitch: 16-byte aligned rows for vector reads
+    const uint32_t pf_local = smem_u32(smem);
     if (!*abort_flag && nrows > 0) {
         const bool cached = g.mode == PJ_KEY || g.mode == PJ_VALUE;
+        if ((g.mode == PJ_KEY || g.mode == PJ_QUERY) && threadIdx.x < p.D / 2) srope[threadIdx.x] = p.rope[threadIdx.x];
         if (threadIdx.x < nrows) {   // per-row position / destination
             const int rl = threadIdx.x;
             const int row = mt * BM + r0 + rl;
@@ -456,41 +582,12 @@ __global__ void __launch_bounds__(PJ_THREADS)
             }
         }
         __syncthreads();
-        if (g.mode == PJ_KEY || g.mode == PJ_QUERY) {
-            // item (row, rotation pair), pair fastest
-            const int half = p.D / 2;
-            const int npairs = ncols / 2;
-            for (int idx = threadIdx.x; idx < nrows * npairs; idx += PJ_THREADS) {
-                const int rl = idx / npairs, pi = idx - rl * npairs;
-                const int h0 = (pi / half) * p.D, i = pi - (pi / half) * half;
-                float x1 = val(rl, h0 + i), x2 = val(rl, h0 + i + half);
-                rope_pair(x1, x2, rowpos[rl], p.rope[i]);
-                if (g.mode == PJ_KEY) {
-                    const int64_t d = rowdst[rl];
-                    if (d >= 0) {
-                        p.Kc[d * p.GD + col0 + h0 + i] = f32_to_bf16(x1);
-                        p.Kc[d * p.GD + col0 + h0 + i + half] = f32_to_bf16(x2);
-                    }
-                } else {
-                    const size_t o = (size_t)(mt * BM + r0 + rl) * p.HD + col0 + h0 + i;
-                    p.q[o] = x1;
-                    p.q[o + half] = x2;
-                }
-            }
-        } else {
-            // item (row, column), column fastest
-            for (int idx = threadIdx.x; idx < nrows * ncols; idx += PJ_THREADS) {
-                const int rl = idx / ncols, c = idx - rl * ncols;
-                const float x = val(rl, c);
-                if (g.mode == PJ_VALUE) {
-                    const int64_t d = rowdst[rl];
-                    if (d >= 0) p.Vc[d * p.GD + col0 + c] = f32_to_bf16(x);
-                } else {
-                    const int f = rowpos[rl];
-                    const float res = (f >= 0 && f < p.N) ? bf16_to_f32(p.u[(size_t)f * p.din + col0 + c]) : 0.f;
-                    p.out[(size_t)(mt * BM + r0 + rl) * p.din + col0 + c] = res + x;
-                }
-            }
+        const EpiCtx e{p, g, mt, r0, nrows, col0, ncols, pfs, pf_local, rowdst, rowpos, srope};
+        switch (S) {
+            case 1: proj_epilogue<1>(e); break;
+            case 2: proj_epilogue<2>(e); break;
+            case 4: proj_epilogue<4>(e); break;
+            default: proj_epilogue<8>(e); break;
         }
     }
     if (S > 1) {
@@ -789,13 +886,26 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     // shared memory (the pass buffers are free now), one weight per split and
     // head, then each output element sums the splits with independent loads
     const float* allp = p.part + ((size_t)b * p.G + g) * p.chunks * hq * (D + 2);
-    float* wgt = reinterpret_cast<float*>(Kbuf);        // [chunks][hq] split weights
-    float* lsum = wgt + (size_t)p.chunks * hq;          // [chunks][hq] split sums
-    float* mtot = lsum + (size_t)p.chunks * hq;         // [hq] 1 / merged sum
+    // every split's partial (outputs, max, sum) of this (sequence, KV head) into
+    // shared memory at once, when it fits beside the weights; else read from L2
+    const size_t nf = (size_t)p.chunks * hq * (D + 2);
+    const bool staged = (nf + 2 * (size_t)p.chunks * hq + hq) * 4 <= 2 * buf * 2;
+    float* pm = reinterpret_cast<float*>(Kbuf);                 // [chunks][hq][D + 2] (staged)
+    float* wgt = staged ? pm + nf : reinterpret_cast<float*>(Kbuf);   // [chunks][hq] split weights
+    float* lsum = wgt + (size_t)p.chunks * hq;                  // [chunks][hq] split sums
+    float* mtot = lsum + (size_t)p.chunks * hq;                 // [hq] 1 / merged sum
+    if (staged) {
+        for (size_t i = tid; i < nf / 2; i += AT_THREADS)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(pm + 2 * i)), "l"(allp + 2 * i)
+                         : "memory");
+        cp_async_commit();
+        cp_async_wait_0();
+        __syncthreads();
+    }
+    const float* src = staged ? pm : allp;
     for (int idx = tid; idx < p.chunks * hq; idx += AT_THREADS) {
-        const float* ps = allp + (size_t)idx * (D + 2);
-        wgt[idx] = __ldcg(ps + D);
-        lsum[idx] = __ldcg(ps + D + 1);
+        wgt[idx] = staged ? src[(size_t)idx * (D + 2) + D] : __ldcg(src + (size_t)idx * (D + 2) + D);
+        lsum[idx] = staged ? src[(size_t)idx * (D + 2) + D + 1] : __ldcg(src + (size_t)idx * (D + 2) + D + 1);
     }
     __syncthreads();
     if (tid < hq) {
@@ -811,7 +921,7 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
         mtot[tid] = L > 0.f ? 1.f / L : 0.f;
     }
     __syncthreads();
-    // two output pairs per thread at a time, eight splits each per step: 16 loads in flight
+    // two output pairs per thread at a time, eight splits each per step
     const int nitems = hq * D / 2;
     for (int base = tid; base < nitems; base += 2 * AT_THREADS) {
         int hh[2], ee[2];
@@ -830,11 +940,13 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 8; ++j) {
+                    const float* q2 = src + ((size_t)(s0 + j) * hq + hh[u]) * (D + 2) + 2 * ee[u];
                     ov[u][j] = (s0 + j < p.chunks)
-                                   ? __ldcg(reinterpret_cast<const float2*>(
-                                         allp + ((size_t)(s0 + j) * hq + hh[u]) * (D + 2) + 2 * ee[u]))
+                                   ? (staged ? *reinterpret_cast<const float2*>(q2)
+                                             : __ldcg(reinterpret_cast<const float2*>(q2)))
                                    : make_float2(0.f, 0.f);
+                }
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -863,7 +975,7 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
 // ------------------------------------------------------------------ host side
 // Shared memory of a proj_kernel CTA with `stages` ring stages of tile width bn.
 static size_t proj_smem(int stages, int bn) {
-    return 1024 + (size_t)stages * (PJ_A_BYTES + (size_t)bn * BK * 2) + 256 + BM * 12;
+    return 1024 + (size_t)stages * (PJ_A_BYTES + (size_t)bn * BK * 2) + 256 + BM * 12 + 512;
 }
 
 static wf_status launch_proj(const CUtensorMap* mA, const CUtensorMap* mW, PjParams p, int tiles, cudaStream_t s) {
@@ -871,16 +983,20 @@ static wf_status launch_proj(const CUtensorMap* mA, const CUtensorMap* mW, PjPar
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
+        // Every catch-up kernel asks for the largest shared-memory carveout, so
+        // that an SM need not drain to switch it when the next kernel's CTAs
+        // arrive (they then start beside the previous kernel's last CTAs).
         if (cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)proj_smem(PJ_STAGES, PJ_BN_CU)) != cudaSuccess)
+                                 (int)proj_smem(PJ_STAGES, PJ_BN_CU)) != cudaSuccess ||
+            cudaFuncSetAttribute(proj_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
     }
     // A three-stage ring lets two CTAs share an SM when the tile is narrow;
-    // the partial tile ([BM][bn + 1] fp32) reuses the ring and must fit in it.
+    // the partial tile ([BM][bn + 4] fp32) reuses the ring and must fit in it.
     int stages = 3;
     if (2 * (proj_smem(stages, p.bn) + 1024) > 228 * 1024) stages = PJ_STAGES;
-    while ((size_t)stages * (PJ_A_BYTES + (size_t)p.bn * BK * 2) < (size_t)BM * (p.bn + 1) * 4) ++stages;
+    while ((size_t)stages * (PJ_A_BYTES + (size_t)p.bn * BK * 2) < (size_t)BM * (p.bn + 4) * 4) ++stages;
     const size_t smem = proj_smem(stages, p.bn);
     const int per_sm = 2 * (smem + 1024) <= 228 * 1024 ? 2 : 1;
     p.stages = stages;
@@ -951,6 +1067,14 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     uint16_t* afin = reinterpret_cast<uint16_t*>(w + L.afin);
     const int GD = a->G * a->D, HD = a->H * a->D;
     const int rows = a->N + (with_final ? a->B : 0);
+    static bool norm_attr[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    if (dev < 64 && !norm_attr[dev]) {   // see launch_proj: the largest shared-memory carveout
+        if (cudaFuncSetAttribute(norm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            return WF_ERR_CUDA;
+        norm_attr[dev] = true;
+    }
     CU_TRY(launch(norm_kernel, dim3(cdiv(rows, NORM_ROWS_PER_CTA)), dim3(32 * NORM_ROWS_PER_CTA), 0, s, a->u,
                          a->bl_off, a->cache_len, a->B, a->N, a->din, a->cap, a->gamma, a->eps, (int)with_final,
                          a->theta, a->D, ahat, afin, reinterpret_cast<float2*>(w + L.rope), ctrl));
@@ -986,19 +1110,23 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     ap.hq = a->H / a->G;
     ap.GD = GD;
     ap.HD = HD;
+    // splits of each sequence's cache rows: about two CTAs per SM over all
+    // (sequence, KV head) pairs, but no split shorter than AT_SPLIT_ROWS of the
+    // cache capacity - short splits cost more to merge than to read
     const int want = 2 * num_sms() / (a->B * a->G);
-    ap.chunks = want < 1 ? 1 : (want > AT_MAX_CHUNKS ? AT_MAX_CHUNKS : want);
+    const int by_rows = cdiv(a->cap, AT_SPLIT_ROWS);
+    int chunks = want < by_rows ? want : by_rows;
+    ap.chunks = chunks < 1 ? 1 : (chunks > AT_MAX_CHUNKS ? AT_MAX_CHUNKS : chunks);
     ap.part = reinterpret_cast<float*>(w + L.apart);
     ap.cnt = reinterpret_cast<uint32_t*>(w + L.cnt);
     ap.obf = reinterpret_cast<uint16_t*>(w + L.obf);
     ap.attn = a->attn;
     const size_t at_smem = catchup_attend_smem(a->H, a->G, a->D);
     static bool at_attr[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !at_attr[dev]) {
         if (cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
             return WF_ERR_CUDA;
         at_attr[dev] = true;
     }
