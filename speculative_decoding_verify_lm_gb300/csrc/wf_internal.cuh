@@ -71,6 +71,9 @@ constexpr int BN = 256;    // weight rows per tile      (UMMA N, largest)
 constexpr int BN_MIN = 128;  // smallest weight-row tile the scheduler picks
 constexpr int BK = 64;     // K elements per pipeline stage (128 bytes of bf16)
 constexpr int ROUTER_UNITS_PER_CTA = 8;
+// The tiled router keeps at most this many (32-row x 128-unit tile, K split)
+// partial tiles of fp32 in the workspace at once (about two CTAs per SM).
+constexpr int ROUTER_GEMM_SLOTS = 320;
 constexpr int ROUTER_MAX_WIDTH = 65536;
 
 inline int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
@@ -93,7 +96,14 @@ inline Layout layout(int P, int B, int d, int m, int Vd, int k) {
     }
     L.part = off;
     const int routed = small_P > B ? small_P : B;
-    off = align_up(off + sizeof(float) * (size_t)routed * (size_t)cdiv(m > 0 ? m : 1, ROUTER_UNITS_PER_CTA), 256);
+    const int mm = m > 0 ? m : 1;
+    // router partials: [rows][m / 8] (beside the LM head) or [K splits][B][m]
+    // of the tiled router, at most ROUTER_GEMM_SLOTS tiles of 32 x 128 (or B x m
+    // with one split)
+    const size_t beside_part = (size_t)routed * (size_t)cdiv(mm, ROUTER_UNITS_PER_CTA);
+    const size_t tiles = (size_t)cdiv(B > 0 ? B : 1, 32) * (size_t)cdiv(mm, 128);
+    const size_t gemm_part = (tiles > ROUTER_GEMM_SLOTS ? tiles : (size_t)ROUTER_GEMM_SLOTS) * 32 * 128;
+    off = align_up(off + sizeof(float) * (beside_part > gemm_part ? beside_part : gemm_part), 256);
     L.dall = off;
     off = align_up(off + sizeof(float) * (size_t)(small_P > ent_rows ? small_P : ent_rows), 256);
     L.ent = off;

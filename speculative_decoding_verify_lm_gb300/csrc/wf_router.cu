@@ -5,19 +5,21 @@
 // with h_b the bf16 hidden row rows[b] widened to fp32, exact-erf GELU, and
 // dropout as the identity.
 //
-// One warp per hidden unit j (8 units per CTA).  W1 is not written by the
-// kernel before this one in a round (the acceptance step), so each warp loads
-// its W1 row into registers (d <= 2560) before waiting on that kernel: the
-// weight stream overlaps it, and only the rows to route and the hidden states
-// are read after the wait.  Each pass takes RB hidden rows, shared by the
-// CTA's warps, and keeps RB dot products per warp.  STAGED (routing chosen
-// rows after acceptance): the rows of the next pass stream into shared memory
-// with asynchronous copies while this pass is computed.  Otherwise (every row
-// of a small round, beside the LM head, which leaves no shared memory) they are
-// read through L1.  Units are folded per CTA into w2[j] * GELU(z_j) partials,
-// and the last CTA to finish sums the partials of every sequence in a fixed
-// order (the result does not depend on CTA scheduling) and writes delta_al and
-// route.
+// Two kernels compute it.
+//
+// router_kernel routes every row of a small round beside the LM head: one
+// warp per hidden unit j (8 units per CTA), the W1 row held in registers
+// (d <= 2560) and loaded before the dependency wait, RB hidden rows per pass
+// read through L1 (no shared memory, so its CTAs fit beside the LM-head CTAs).
+// Units are folded per CTA into w2[j] * GELU(z_j) partials, and the last CTA
+// to finish sums them per row in a fixed order and writes delta_al and route.
+//
+// router_gemm_kernel + router_finish_kernel route chosen rows after
+// acceptance: Z = H W1^T as a tiled fp32 GEMM on the CUDA cores (tiles of 32
+// rows x 128 units, a 4 x 4 register micro-tile per thread, bf16 rows widened
+// once into shared memory, K split across CTAs so the tiles fill the SMs),
+// then one CTA per row adds the K splits in order, applies b1, GELU and w2,
+// sums over units in a fixed order and takes the decision.
 #include "wf_internal.cuh"
 
 namespace wf {
@@ -41,11 +43,6 @@ __device__ __forceinline__ float dot4(const float4 w, const uint2 h, float acc) 
     return fmaf(w.w, __uint_as_float(h.y & 0xFFFF0000u), acc);
 }
 
-__device__ __forceinline__ void router_cp16(void* smem_dst, const void* gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-
-template <bool STAGED>
 __global__ void __maxnreg__(ROUTER_MAX_REGS)
     router_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
                   int P, const float* __restrict__ W1, const float* __restrict__ b1, const float* __restrict__ w2,
@@ -53,7 +50,6 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
     // part: [B][gridDim.x] partial sums, zero on entry and on exit
     __shared__ float red[ROUTER_UNITS_PER_CTA][ROUTER_RB];
     __shared__ int s_last;
-    extern __shared__ __align__(16) uint8_t rstage[];   // STAGED: two passes of RB rows (bf16)
 
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -92,42 +88,15 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
         if (r < 0 || (P >= 0 && r >= P)) r = -1;
         return r;
     };
-    const int chunks = d >> 3;   // 16-byte pieces of a row
-    // STAGED: copies of pass b0's rows into buffer `which`
-    auto stage = [&](int b0, int which) {
+    for (int b0 = y0; b0 < y1; b0 += ROUTER_RB) {
         const int nb = min(ROUTER_RB, y1 - b0);
-        uint16_t* dst = reinterpret_cast<uint16_t*>(rstage) + (size_t)which * ROUTER_RB * d;
-        for (int idx = threadIdx.x; idx < nb * chunks; idx += ROUTER_THREADS) {
-            const int rb = idx / chunks, c = idx - rb * chunks;
-            const int r = row_of(b0 + rb);
-            if (r >= 0) router_cp16(dst + (size_t)rb * d + c * 8, hidden + (size_t)r * d + c * 8);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    if (STAGED && y0 < y1) stage(y0, 0);
-    int pass = 0;
-    for (int b0 = y0; b0 < y1; b0 += ROUTER_RB, ++pass) {
-        const int nb = min(ROUTER_RB, y1 - b0);
-        if constexpr (STAGED) {
-            if (b0 + ROUTER_RB < y1) {
-                stage(b0 + ROUTER_RB, (pass + 1) & 1);
-                asm volatile("cp.async.wait_group 1;" ::: "memory");
-            } else {
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
-            }
-            __syncthreads();
-        }
         const uint2* hrow[ROUTER_RB];
         bool hv[ROUTER_RB];
 #pragma unroll
         for (int rb = 0; rb < ROUTER_RB; ++rb) {
             const int r = rb < nb ? row_of(b0 + rb) : -1;
             hv[rb] = r >= 0;
-            if (STAGED)
-                hrow[rb] = reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(rstage) +
-                                                          ((size_t)(pass & 1) * ROUTER_RB + rb) * d);
-            else
-                hrow[rb] = reinterpret_cast<const uint2*>(hidden + (size_t)(r >= 0 ? r : 0) * d);
+            hrow[rb] = reinterpret_cast<const uint2*>(hidden + (size_t)(r >= 0 ? r : 0) * d);
         }
         float acc[ROUTER_RB];
 #pragma unroll
@@ -144,8 +113,7 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
                         const int c = lane + 32 * (u0 + u);
 #pragma unroll
                         for (int rb = 0; rb < ROUTER_RB; ++rb)
-                            hx[u][rb] = (hv[rb] && c < d4) ? (STAGED ? hrow[rb][c] : __ldg(hrow[rb] + c))
-                                                           : make_uint2(0u, 0u);
+                            hx[u][rb] = (hv[rb] && c < d4) ? __ldg(hrow[rb] + c) : make_uint2(0u, 0u);
                     }
 #pragma unroll
                     for (int u = 0; u < ROUTER_LB; ++u)
@@ -164,8 +132,7 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
                         if (c < d4) {
 #pragma unroll
                             for (int rb = 0; rb < ROUTER_RB; ++rb)
-                                if (hv[rb])
-                                    acc[rb] = dot4(wl[u], STAGED ? hrow[rb][c] : __ldg(hrow[rb] + c), acc[rb]);
+                                if (hv[rb]) acc[rb] = dot4(wl[u], __ldg(hrow[rb] + c), acc[rb]);
                         }
                     }
                 }
@@ -224,29 +191,193 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
     if (beside) pdl_wait();
 }
 
+// ------------------------------------------------------------------ tiled router (chosen rows)
+constexpr int RG_TB = 32;       // rows per tile
+constexpr int RG_TU = 128;      // units per tile
+constexpr int RG_KC = 32;       // K per stage
+constexpr int RG_THREADS = 256;
+constexpr int RG_HP = RG_KC + 4;   // shared row pitch of the widened rows (floats)
+constexpr int RG_WP = RG_TU + 4;   // shared row pitch of the transposed weights (floats)
+
+// Zp[ks][b][j] = sum over this split's K range of h_b[k] * W1[j, k]; warp w
+// computes rows 4w..4w+3, lane l units 4l..4l+3 of the tile.
+__global__ void __launch_bounds__(RG_THREADS)
+    router_gemm_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
+                       int P, const float* __restrict__ W1, int kc_per, float* __restrict__ Zp) {
+    __shared__ __align__(16) float Hs[2][RG_TB][RG_HP];
+    __shared__ __align__(16) float Ws[2][RG_KC][RG_WP];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int u0 = blockIdx.x * RG_TU, b0 = blockIdx.y * RG_TB, ks = blockIdx.z;
+    const int nkc = (d + RG_KC - 1) / RG_KC;
+    const int kc0 = ks * kc_per, kc1 = min(nkc, kc0 + kc_per);
+    // staging roles: weights - unit tid / 2, 16 of the 32 K of a stage; rows - row tid / 8, 4 K
+    const int wu = tid >> 1, wk = (tid & 1) * 16;
+    const int hr = tid >> 3, hk = (tid & 7) * 4;
+    float4 wreg[4];
+    uint2 hreg;
+    auto load_w = [&](int kc) {   // W1 is no earlier kernel's output
+        const int j = u0 + wu, k = kc * RG_KC + wk;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            wreg[q] = (j < m && k + 4 * q < d) ? __ldg(reinterpret_cast<const float4*>(W1 + (size_t)j * d + k) + q)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    int hsrc = -1;   // hidden row of this thread's staging row
+    auto load_h = [&](int kc) {
+        const int k = kc * RG_KC + hk;
+        hreg = (hsrc >= 0 && k < d) ? __ldg(reinterpret_cast<const uint2*>(hidden + (size_t)hsrc * d + k))
+                                    : make_uint2(0u, 0u);
+    };
+    auto store = [&](int buf) {
+        const float wv[16] = {wreg[0].x, wreg[0].y, wreg[0].z, wreg[0].w, wreg[1].x, wreg[1].y, wreg[1].z, wreg[1].w,
+                              wreg[2].x, wreg[2].y, wreg[2].z, wreg[2].w, wreg[3].x, wreg[3].y, wreg[3].z, wreg[3].w};
+#pragma unroll
+        for (int q = 0; q < 16; ++q) Ws[buf][wk + q][wu] = wv[q];
+        *reinterpret_cast<float4*>(&Hs[buf][hr][hk]) =
+            make_float4(__uint_as_float(hreg.x << 16), __uint_as_float(hreg.x & 0xFFFF0000u),
+                        __uint_as_float(hreg.y << 16), __uint_as_float(hreg.y & 0xFFFF0000u));
+    };
+    if (kc0 < kc1) load_w(kc0);
+    pdl_wait();   // rows[] is the acceptance step's output
+    pdl_trigger();
+    if (b0 + hr < B) {
+        const int r = rows[b0 + hr];
+        hsrc = (r >= 0 && (P < 0 || r < P)) ? r : -1;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    if (kc0 < kc1) {
+        load_h(kc0);
+        store(0);
+    }
+    __syncthreads();
+    for (int kc = kc0; kc < kc1; ++kc) {
+        const int buf = (kc - kc0) & 1;
+        if (kc + 1 < kc1) {   // the next stage's loads are in flight during this stage's FMAs
+            load_w(kc + 1);
+            load_h(kc + 1);
+        }
+#pragma unroll
+        for (int k = 0; k < RG_KC; k += 4) {
+            float4 h[4], wt[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = *reinterpret_cast<const float4*>(&Hs[buf][4 * w + i][k]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) wt[q] = *reinterpret_cast<const float4*>(&Ws[buf][k + q][4 * lane]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float hv[4] = {h[i].x, h[i].y, h[i].z, h[i].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[i][0] = fmaf(hv[q], wt[q].x, acc[i][0]);
+                    acc[i][1] = fmaf(hv[q], wt[q].y, acc[i][1]);
+                    acc[i][2] = fmaf(hv[q], wt[q].z, acc[i][2]);
+                    acc[i][3] = fmaf(hv[q], wt[q].w, acc[i][3]);
+                }
+            }
+        }
+        if (kc + 1 < kc1) {
+            __syncthreads();   // the other buffer was last read a stage ago; this one is read no more
+            store(buf ^ 1);
+            __syncthreads();
+        }
+    }
+    const int j = u0 + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int b = b0 + 4 * w + i;
+        if (b >= B) continue;
+        float* z = Zp + ((size_t)ks * B + b) * m + j;
+        if (j + 3 < m && (m & 3) == 0) {
+            *reinterpret_cast<float4*>(z) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (j + q < m) z[q] = acc[i][q];
+        }
+    }
+}
+
+// One CTA per routed row: z_j = b1[j] + sum over the K splits (in order),
+// delta = b2 + sum_j w2[j] GELU(z_j) summed in a fixed order, route = delta > tau.
+// A thread owns unit j; its split partials are fetched eight at a time (all
+// loads in flight together) and zeroed only after every one has been read.
+constexpr int RF_THREADS = 1024;
+
+__global__ void __launch_bounds__(RF_THREADS)
+    router_finish_kernel(float* Zp, int KS, const int32_t* __restrict__ rows, int B, int m, int P,
+                         const float* __restrict__ b1, const float* __restrict__ w2, float b2, float tau,
+                         float* delta_al, int32_t* route, Control* ctrl) {
+    __shared__ float wsum[RF_THREADS / 32];
+    pdl_wait();
+    pdl_trigger();
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const size_t stride = (size_t)B * m;
+    float t = 0.f;
+    for (int j = tid; j < m; j += RF_THREADS) {
+        float* zp = Zp + (size_t)b * m + j;
+        float z = b1[j];
+        int k = 0;
+        for (; k + 8 <= KS; k += 8) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(zp + (size_t)(k + i) * stride);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) z += v[i];
+        }
+        for (; k < KS; ++k) z += __ldcg(zp + (size_t)k * stride);
+        for (k = 0; k < KS; ++k) zp[(size_t)k * stride] = 0.f;   // leave the workspace zeroed
+        t = fmaf(w2[j], gelu_erf(z), t);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if ((tid & 31) == 0) wsum[tid >> 5] = t;
+    __syncthreads();
+    if (tid == 0) {
+        float s = b2;
+        for (int i = 0; i < RF_THREADS / 32; ++i) s += wsum[i];
+        const int r = rows[b];
+        if (r < 0 || (P >= 0 && r >= P)) {
+            if (delta_al) delta_al[b] = __int_as_float(0x7fc00000);
+            if (route) route[b] = -1;
+            record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+        } else {
+            if (delta_al) delta_al[b] = s;
+            if (route) route[b] = s > tau ? 1 : 0;
+        }
+    }
+}
+
+// K splits of the tiled router for B rows: the tiles times the splits fill
+// the SMs about once (at most ROUTER_GEMM_SLOTS tiles' partials in flight).
+int router_gemm_splits(int B, int d, int m) {
+    const int tiles = cdiv(B, RG_TB) * cdiv(m, RG_TU);
+    const int nkc = cdiv(d, RG_KC);
+    int ks = ROUTER_GEMM_SLOTS / tiles;
+    ks = ks < 1 ? 1 : (ks > nkc ? nkc : ks);
+    const int per = cdiv(nkc, ks);
+    return cdiv(nkc, per);
+}
+
 wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s) {
     if (B == 0) return WF_OK;
     Control* ctrl = reinterpret_cast<Control*>(ws);
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
-    const dim3 grid(cdiv(m, ROUTER_UNITS_PER_CTA), cdiv(B, ROUTER_ROWS_PER_CTA));
-    if (rows == nullptr || d > 32 * 4 * ROUTER_WREG)
-        return launch(router_kernel<false>, grid, dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d, m, P, W1, b1, w2,
-                      b2, tau, delta_al, route, part, ctrl);
-    // chosen rows after acceptance: rows staged in shared memory, two passes in flight
-    const size_t smem = (size_t)2 * ROUTER_RB * d * 2;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(router_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 2 * ROUTER_RB * 32 * 4 * ROUTER_WREG * 2) != cudaSuccess)
-            return WF_ERR_CUDA;
-        attr_set[dev] = true;
-    }
-    return launch(router_kernel<true>, grid, dim3(ROUTER_THREADS), smem, s, hidden, rows, B, d, m, P, W1, b1, w2,
-                  b2, tau, delta_al, route, part, ctrl);
+    if (rows == nullptr)   // every row of a small round, beside the LM head
+        return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA), cdiv(B, ROUTER_ROWS_PER_CTA)),
+                      dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d, m, P, W1, b1, w2, b2, tau, delta_al, route,
+                      part, ctrl);
+    // chosen rows: tiled GEMM with K split, then the finishing pass per row
+    const int ks = router_gemm_splits(B, d, m);
+    const int per = cdiv(cdiv(d, RG_KC), ks);
+    const dim3 grid(cdiv(m, RG_TU), cdiv(B, RG_TB), ks);
+    wf_status st = launch(router_gemm_kernel, grid, dim3(RG_THREADS), 0, s, hidden, rows, B, d, m, P, W1, per, part);
+    if (st != WF_OK) return st;
+    return launch(router_finish_kernel, dim3(B), dim3(RF_THREADS), 0, s, part, ks, rows, B, m, P, b1,
+                  w2, b2, tau, delta_al, route, ctrl);
 }
 
 }  // namespace wf
