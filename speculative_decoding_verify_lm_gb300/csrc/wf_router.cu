@@ -5,7 +5,7 @@
 // with h_b the bf16 hidden row rows[b] widened to fp32, exact-erf GELU, and
 // dropout as the identity.
 //
-// Two kernels compute it.
+// Three kernels compute it.
 //
 // router_kernel routes every row of a small round beside the LM head: one
 // warp per hidden unit j (8 units per CTA), the W1 row held in registers
@@ -14,7 +14,9 @@
 // Units are folded per CTA into w2[j] * GELU(z_j) partials, and the last CTA
 // to finish sums them per row in a fixed order and writes delta_al and route.
 //
-// router_gemm_kernel + router_finish_kernel route chosen rows after
+// It also routes up to 8 chosen rows after acceptance (one pass of rows).
+//
+// router_gemm_kernel + router_finish_kernel route more chosen rows after
 // acceptance: Z = H W1^T as a tiled fp32 GEMM on the CUDA cores (tiles of 32
 // rows x 128 units, a 4 x 4 register micro-tile per thread, bf16 rows widened
 // once into shared memory, K split across CTAs so the tiles fill the SMs),
@@ -366,7 +368,10 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
     if (B == 0) return WF_OK;
     Control* ctrl = reinterpret_cast<Control*>(ws);
     float* part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + part_off);
-    if (rows == nullptr)   // every row of a small round, beside the LM head
+    // every row of a small round beside the LM head, or a few chosen rows
+    // (one pass of router_kernel): the warp-per-unit kernel, whose W1 rows
+    // are in registers before the wait; more chosen rows: the tiled GEMM
+    if (rows == nullptr || B <= ROUTER_RB)
         return launch(router_kernel, dim3(cdiv(m, ROUTER_UNITS_PER_CTA), cdiv(B, ROUTER_ROWS_PER_CTA)),
                       dim3(ROUTER_THREADS), 0, s, hidden, rows, B, d, m, P, W1, b1, w2, b2, tau, delta_al, route,
                       part, ctrl);

@@ -139,7 +139,8 @@ def test_verify_bad_parent_sets_error():
 
 
 # ------------------------------------------------------------------ router
-@pytest.mark.parametrize("B,d,m", [(1, 2560, 1024), (1, 2560, 320), (7, 256, 128), (33, 64, 5), (256, 512, 64)])
+@pytest.mark.parametrize("B,d,m", [(1, 2560, 1024), (1, 2560, 320), (7, 256, 128), (8, 72, 40), (9, 72, 40),
+                                   (12, 2560, 1024), (33, 64, 5), (256, 512, 64)])
 def test_router(B, d, m):
     rng = np.random.default_rng(B * 7 + m)
     P = B + 3
