@@ -45,6 +45,7 @@ constexpr int PJ_BN_CU = 192;        // widest output tile: partial, reduced and
 constexpr int AT_MAX_CHUNKS = 64;    // cache-row splits per (sequence, KV head)
 constexpr int AT_PASS_ROWS = 128;    // cache rows an attention CTA stages per pass (two passes in flight)
 constexpr int AT_SPLIT_ROWS = 256;   // smallest split of a cache worth its merge
+constexpr int AT_CLUSTER_MAX = 16;   // splits merged inside one thread-block cluster (non-portable above 8)
 constexpr int NORM_ROWS_PER_CTA = 4;
 constexpr int NORM_REG_CHUNKS = 16;  // 16-byte pieces of a row a lane keeps in registers
 
@@ -265,6 +266,14 @@ struct PjParams {
     uint64_t timeout_ns;
 };
 
+// A weight box brought into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
@@ -471,11 +480,14 @@ __global__ void __launch_bounds__(PJ_THREADS)
     const uint64_t pol_a = policy_evict_last();
     const uint32_t tx = (uint32_t)(g.a_rows * BK * 2 + bstage);
     const int early = min(stages, kb1 - kb0);   // stages whose weights are requested early
-    if (warp == 0 && lane == 0)
+    if (warp == 0 && lane == 0) {
         for (int i = 0; i < early; ++i) {   // fresh barriers: the ring is empty
             mbar_arrive_expect_tx(&full[i], tx);
             tma_load_2d(sB + i * bstage, mW, &full[i], (kb0 + i) * BK, nt * p.bn, pol_w);
         }
+        // the split's other weight boxes wait in L2 until a stage frees up
+        for (int kb = kb0 + early; kb < kb1; ++kb) tma_prefetch_l2_2d(mW, kb * BK, nt * p.bn);
+    }
     pdl_wait();
     pdl_trigger();
 
@@ -616,6 +628,8 @@ struct AtParams {
     const int32_t* bl_off;
     const int32_t* cache_len;
     int B, cap, G, D, hq, GD, HD, chunks;
+    int cluster;               // 1: the chunks of a (sequence, KV head) form one cluster and merge over
+                               // distributed shared memory; 0: through part / cnt and the last CTA
     float* part;               // [B][G][chunks][hq][D + 2]: unnormalised output, running max (log2), sum
     uint32_t* cnt;             // [B * G] arrivals, zero at rest
     uint16_t* obf;             // [B, HD] bf16 output (operand of the output projection)
@@ -643,6 +657,16 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return (uint32_t)f32_to_bf16(lo) | ((uint32_t)f32_to_bf16(hi) << 16);
 }
+__device__ __forceinline__ float dsmem_ld1(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 dsmem_ld2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
 
 // One CTA (4 warps) per (cache-row split, KV head, sequence).  The group's hq
 // <= 16 query heads form the 16 rows of an mma.sync A operand (bf16, pre-scaled
@@ -653,8 +677,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   running max / sum per head in the base-2 domain, P = exp2(S - max) as bf16
 //   O += P V       (2 key steps of 16 x D/8 dim tiles; V fragments by ldmatrix.trans)
 // Each warp keeps its own (max, sum, O) over its keys; the four are merged at
-// the end, and the last CTA of each (sequence, KV head) merges the splits in
-// index order.
+// the end.  The splits of a (sequence, KV head) are then merged in index
+// order: with at most AT_CLUSTER_MAX splits they form one thread-block
+// cluster, each leaves its partial in its own shared memory and finishes a
+// slice of the outputs over distributed shared memory; with more, partials go
+// through global memory and the last CTA to arrive merges them.  The old cache
+// rows of the first two passes are copied before the dependency wait.
 constexpr int AT_THREADS = 128;
 constexpr int AT_WARP_ROWS = 32;   // cache rows a warp takes per pass
 constexpr int AT_MAX_DT = 16;      // D / 8 dim tiles: D <= 128
@@ -708,15 +736,21 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
         zero_tail(which, nr);
         cp_async_commit();
     };
-    // the first pass's previously cached rows stream in while the kernel
-    // before this one (which writes the new rows and the query) finishes
+    // the previously cached rows of the first two passes stream in while the
+    // kernel before this one (which writes the new rows and the query) finishes
     const int nr0 = t0 < t1 ? min(R, t1 - t0) : 0;
     const int split0 = max(0, min(nr0, Lold - t0));
+    const int nr1 = t0 + R < t1 ? min(R, t1 - t0 - R) : 0;
+    const int split1 = max(0, min(nr1, Lold - t0 - R));
     if (nr0 > 0) {
         stage_rows(t0, 0, 0, split0);
         zero_tail(0, nr0);
-        cp_async_commit();
     }
+    if (nr1 > 0) {
+        stage_rows(t0 + R, 1, 0, split1);
+        zero_tail(1, nr1);
+    }
+    cp_async_commit();
     pdl_wait();
     pdl_trigger();
     const float qscale = 1.4426950408889634f / sqrtf((float)D);
@@ -725,10 +759,9 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
         const float v = h < hq ? p.q[(size_t)b * p.HD + ((size_t)g * hq + h) * D + e] * qscale : 0.f;
         qs[h * stride + e] = f32_to_bf16(v);
     }
-    if (nr0 > 0) {
-        stage_rows(t0, 0, split0, nr0);
-        cp_async_commit();
-    }
+    if (nr0 > 0) stage_rows(t0, 0, split0, nr0);   // rows this call appends
+    if (nr1 > 0) stage_rows(t0 + R, 1, split1, nr1);
+    cp_async_commit();
     __syncthreads();   // qs written
 
     const int nks = D / 16, ndt = D / 8;
@@ -748,7 +781,7 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
 
     int pass = 0;
     for (int p0 = t0; p0 < t1; p0 += R, ++pass) {
-        if (p0 + R < t1) {
+        if (pass >= 1 && p0 + R < t1) {   // passes 0 and 1 were staged before the loop
             stage(p0 + R, (pass + 1) & 1);
             cp_async_wait_1();
         } else {
@@ -857,6 +890,82 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
         rw[(gq + 8) * rs + D + 1] = l_hi;
     }
     __syncthreads();
+    if (p.cluster) {
+        // this split's partial stays in its own shared memory, after the warp merge area
+        float* mine = red + (size_t)4 * 16 * rs;            // [hq][D + 2]
+        float* stat = mine + (size_t)hq * (D + 2);           // [chunks][hq] max -> weight, [chunks][hq] sum
+        float* mtot = stat + (size_t)2 * p.chunks * hq;      // [hq] 1 / merged sum
+        for (int idx = tid; idx < hq * (D + 2); idx += AT_THREADS) {
+            const int h = idx / (D + 2), e = idx - h * (D + 2);
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * 16 + h) * rs + D]);
+            float v = 0.f;
+            if (e == D) {
+                v = M;
+            } else {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float mw = red[(w * 16 + h) * rs + D];
+                    const float wt = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                    v = fmaf(wt, red[(w * 16 + h) * rs + (e == D + 1 ? D + 1 : e)], v);
+                }
+            }
+            mine[idx] = v;
+        }
+        cluster_sync();   // every split's partial is in its shared memory
+        const int CS = p.chunks;
+        const uint32_t mine_s = smem_u32(mine);
+        for (int i = tid; i < CS * hq; i += AT_THREADS) {
+            const int s2 = i / hq, h = i - s2 * hq;
+            const uint32_t a = dsmem_map(mine_s + (uint32_t)((h * (D + 2) + D) * 4), (uint32_t)s2);
+            stat[i] = dsmem_ld1(a);
+            stat[CS * hq + i] = dsmem_ld1(a + 4);
+        }
+        __syncthreads();
+        if (tid < hq) {
+            float M = -INFINITY;
+            for (int s2 = 0; s2 < CS; ++s2) M = fmaxf(M, stat[s2 * hq + tid]);
+            float L = 0.f;
+            for (int s2 = 0; s2 < CS; ++s2) {
+                const float ms = stat[s2 * hq + tid];
+                const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);   // a split with no rows weighs 0
+                stat[s2 * hq + tid] = w;
+                L = fmaf(w, stat[CS * hq + s2 * hq + tid], L);
+            }
+            mtot[tid] = L > 0.f ? 1.f / L : 0.f;
+        }
+        __syncthreads();
+        // this split finishes output pairs [c * per_c, (c + 1) * per_c), every split's values in index order
+        const int items = hq * (D / 2);
+        const int per_c = (items + CS - 1) / CS;
+        const int i1 = min(items, (c + 1) * per_c);
+        for (int it = c * per_c + tid; it < i1; it += AT_THREADS) {
+            const int h = it / (D / 2), e = it - h * (D / 2);
+            const uint32_t a = mine_s + (uint32_t)((h * (D + 2) + 2 * e) * 4);
+            float2 ov[AT_CLUSTER_MAX];
+#pragma unroll
+            for (int s2 = 0; s2 < AT_CLUSTER_MAX; ++s2)
+                if (s2 < CS) ov[s2] = dsmem_ld2(dsmem_map(a, (uint32_t)s2));
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < AT_CLUSTER_MAX; ++s2)
+                if (s2 < CS) {
+                    const float w = stat[s2 * hq + h];
+                    a0 = fmaf(w, ov[s2].x, a0);
+                    a1 = fmaf(w, ov[s2].y, a1);
+                }
+            const float r0 = a0 * mtot[h], r1 = a1 * mtot[h];
+            const size_t o2 = (size_t)b * p.HD + ((size_t)g * hq + h) * D + 2 * e;
+            *reinterpret_cast<uint32_t*>(p.obf + o2) = pack_bf16x2(r0, r1);
+            if (p.attn) {
+                p.attn[o2] = r0;
+                p.attn[o2 + 1] = r1;
+            }
+        }
+        cluster_sync();   // no split leaves while a peer may still read its partial
+        return;
+    }
     float* mypart = p.part + (((size_t)b * p.G + g) * p.chunks + c) * hq * (D + 2);
     for (int idx = tid; idx < hq * (D + 2); idx += AT_THREADS) {
         const int h = idx / (D + 2), e = idx - h * (D + 2);
@@ -1059,6 +1168,38 @@ static bool act_map(CUtensorMap* m, const void* base, int rows, int cols) {
 
 size_t catchup_attend_smem(int H, int G, int D);
 
+// How many clusters of `size` attention CTAs with `smem` bytes each can be
+// resident at once (one query per device, size and shared-memory size).
+static int attend_resident_clusters(int dev, int size, size_t smem) {
+    struct Entry {
+        int dev, size;
+        size_t smem;
+        int n;
+    };
+    static Entry seen[64];
+    static int nseen = 0;
+    for (int i = 0; i < nseen; ++i)
+        if (seen[i].dev == dev && seen[i].size == size && seen[i].smem == smem) return seen[i].n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(size, 1, 1);
+    cfg.blockDim = dim3(AT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = size;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    if (nseen < 64) seen[nseen++] = {dev, size, smem, n};
+    return n;
+}
+
 wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s) {
     const CuLayout L = cu_layout(a->B, a->N, a->din, a->H, a->G, a->D);
     uint8_t* w = reinterpret_cast<uint8_t*>(ws);
@@ -1126,11 +1267,20 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     if (dev < 64 && !at_attr[dev]) {
         if (cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
+            cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return WF_ERR_CUDA;
         at_attr[dev] = true;
     }
-    CU_TRY(launch(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s, ap));
+    // few splits: each (sequence, KV head) is one cluster and merges on chip,
+    // provided all of the clusters are resident at once (a CTA that finishes
+    // early holds its slot until its cluster has merged)
+    ap.cluster = ap.chunks > 1 && ap.chunks <= AT_CLUSTER_MAX &&
+                         a->B * a->G <= attend_resident_clusters(dev, ap.chunks, at_smem)
+                     ? 1
+                     : 0;
+    CU_TRY(launch_cluster(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s,
+                          ap.cluster ? (unsigned)ap.chunks : 1u, ap));
 
     // output projection with the residual
     CUtensorMap oA[2], oW[3];

@@ -129,6 +129,8 @@ def check_against_oracle(c, res, kv_only=False):
     (3, 512, 8, 8, 64, (1,), (300,), 301),                                # one token, cache filled exactly
     (4, 128, 4, 1, 128, (40, 200), (7, 0), 256),                          # one KV head, > 128 rows
     (5, 192, 6, 3, 48, tuple([1] * 130), tuple(range(130)), 131),         # 130 sequences: two row tiles
+    (6, 64, 2, 1, 16, (50,), (4000,), 4096),                              # 16 splits: the largest cluster merge
+    (7, 128, 4, 2, 32, (40,), (5000,), 5100),                             # 20 splits: merged through global memory
 ])
 def test_catchup_small_shapes(seed, din, H, G, D, n, L, cap):
     c = pins.catchup_case(seed, din=din, H=H, G=G, D=D, n=n, L=L, cap=cap)
