@@ -451,6 +451,9 @@ __global__ void __launch_bounds__(PJ_THREADS)
     const int lt = t - g.tile0, mt = lt / g.tiles_n, nt = lt % g.tiles_n;
     const int kb0 = split * p.kb_per;
     const int kb1 = min(p.num_k, kb0 + p.kb_per);
+    const int rpc = BM / S;                                        // rows of the tile each split finishes
+    const int r0 = split * rpc;
+    const int nrows = max(0, min(rpc, g.M - (mt * BM + r0)));     // of them, rows that exist
     const CUtensorMap* mA = g.a ? &tmA1 : &tmA0;
     const CUtensorMap* mW = g.w == 0 ? &tmW0 : (g.w == 1 ? &tmW1 : &tmW2);
 
@@ -535,6 +538,26 @@ __global__ void __launch_bounds__(PJ_THREADS)
         }
     } else {
         // ------------------------------------------------ epilogue warps: accumulator -> own partial tile
+        // While the MMAs run: the rotary table and, for each row this split
+        // finishes, its position and cache destination (inputs of the call).
+        const int et = (int)threadIdx.x - 64;
+        if ((g.mode == PJ_KEY || g.mode == PJ_QUERY) && et < p.D / 2) srope[et] = p.rope[et];
+        if (et < nrows) {
+            const int row = mt * BM + r0 + et;
+            if (g.mode == PJ_KEY || g.mode == PJ_VALUE) {
+                const int b = seq_of(p.bl_off, p.B, row);
+                const int pos = p.cache_len[b] + (row - p.bl_off[b]);
+                int64_t dst = -1;
+                if (pos >= 0 && pos < p.cap) dst = (int64_t)b * p.cap + pos;
+                else record_error(p.ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
+                rowdst[et] = dst;
+                rowpos[et] = pos;
+            } else if (g.mode == PJ_QUERY) {
+                rowpos[et] = p.cache_len[row] + (p.bl_off[row + 1] - p.bl_off[row]) - 1;
+            } else {
+                rowpos[et] = p.bl_off[row + 1] - 1;   // the final backlog row (residual)
+            }
+        }
         const int q4 = warp & 3;
         const int rit = q4 * 32 + lane;
         if (!mbar_wait(tfull, 0, p.timeout_ns, abort_flag)) {
@@ -559,41 +582,18 @@ __global__ void __launch_bounds__(PJ_THREADS)
         }
         tc_fence_before();
     }
-    __syncthreads();
+    __syncthreads();   // partial tile, row lookups and rotary table written
     if (S > 1) cluster_sync();   // every split's partial tile is in its shared memory
 
     // ---------------------------------------------------- epilogue of this split's rows
-    // Split r finishes rows [r0, r0 + rpc) of the tile, rpc = BM / S, pulling
-    // the other splits' partial rows over distributed shared memory (every
-    // split's loads of an item in flight together) and summing in split order.
-    const int rpc = BM / S;
-    const int r0 = split * rpc;
-    const int nrows = max(0, min(rpc, g.M - (mt * BM + r0)));   // of them, rows that exist
+    // Split r finishes rows [r0, r0 + rpc) of the tile, pulling the other
+    // splits' partial rows over distributed shared memory (every split's loads
+    // of an item in flight together) and summing in split order.
     const int col0 = nt * p.bn;
     const int ncols = min(p.bn, g.N - col0);
     const int pfs = p.bn + 4;   // row pitch: 16-byte aligned rows for vector reads
     const uint32_t pf_local = smem_u32(smem);
     if (!*abort_flag && nrows > 0) {
-        const bool cached = g.mode == PJ_KEY || g.mode == PJ_VALUE;
-        if ((g.mode == PJ_KEY || g.mode == PJ_QUERY) && threadIdx.x < p.D / 2) srope[threadIdx.x] = p.rope[threadIdx.x];
-        if (threadIdx.x < nrows) {   // per-row position / destination
-            const int rl = threadIdx.x;
-            const int row = mt * BM + r0 + rl;
-            if (cached) {
-                const int b = seq_of(p.bl_off, p.B, row);
-                const int pos = p.cache_len[b] + (row - p.bl_off[b]);
-                int64_t dst = -1;
-                if (pos >= 0 && pos < p.cap) dst = (int64_t)b * p.cap + pos;
-                else record_error(p.ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
-                rowdst[rl] = dst;
-                rowpos[rl] = pos;
-            } else if (g.mode == PJ_QUERY) {
-                rowpos[rl] = p.cache_len[row] + (p.bl_off[row + 1] - p.bl_off[row]) - 1;
-            } else {
-                rowpos[rl] = p.bl_off[row + 1] - 1;   // the final backlog row (residual)
-            }
-        }
-        __syncthreads();
         const EpiCtx e{p, g, mt, r0, nrows, col0, ncols, pfs, pf_local, rowdst, rowpos, srope};
         switch (S) {
             case 1: proj_epilogue<1>(e); break;
