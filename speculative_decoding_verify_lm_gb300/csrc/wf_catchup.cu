@@ -1081,6 +1081,113 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     if (tid == 0) p.cnt[(size_t)b * p.G + g] = 0;
 }
 
+// ------------------------------------------------------------------ output projection, few rows
+// out[b, n] = u[final row of b, n] + sum_k obf[b, k] Wo[n, k] for B <= OG_MAX_B
+// rows.  CTA c owns output rows [16 c, 16 c + 16) with the whole K: its slice
+// of Wo (16 consecutive rows) and the residual entries are copied into shared
+// memory before the dependency wait (neither is an earlier kernel's output),
+// so after it only the B attention rows are fetched, and no K split means no
+// reduction between CTAs.  The product runs on mma.sync m16n8k16 (bf16
+// operands, fp32 accumulators): output rows are M (one tile of 16), the B
+// rows N (8, zero-padded), each of the 8 warps takes a contiguous eighth of
+// the K steps and loads its B fragments straight from global memory (all in
+// flight together), and the warps' partial tiles are summed in warp order.
+// Weight rows are padded by 16 bytes so that ldmatrix reads are free of bank
+// conflicts.  At about 87 KB of shared memory (HD = 2560) a CTA fits beside
+// an attention CTA, so the whole grid is resident, and its weights in flight,
+// while the attention runs.
+constexpr int OG_THREADS = 256;
+constexpr int OG_WARPS = OG_THREADS / 32;
+constexpr int OG_MAX_B = 8;
+constexpr int OG_R = 16;         // output rows a CTA owns: one 16-row tile
+constexpr int OG_MAX_KPW = 24;   // K steps of 16 a warp takes: HD <= 8 x 24 x 16
+
+struct OgParams {
+    const uint16_t* Wo;   // [din, HD]
+    const uint16_t* obf;  // [B, HD] attention output (bf16)
+    const uint16_t* u;    // [N, din] backlog inputs (residual)
+    const int32_t* bl_off;
+    float* out;           // [B, din]
+    int B, N, din, HD;
+};
+
+__global__ void __launch_bounds__(OG_THREADS) oproj_gemv_kernel(const OgParams p) {
+    extern __shared__ __align__(16) uint8_t og_smem[];
+    constexpr int R = OG_R;
+    const int HD = p.HD, B = p.B;
+    const int pitch = HD + 8;                                          // bf16 elements per shared row
+    uint16_t* Ws = reinterpret_cast<uint16_t*>(og_smem);               // [16][pitch] weight rows
+    float* res = reinterpret_cast<float*>(Ws + (size_t)R * pitch);     // [B][16] residual entries
+    float* red = res + OG_MAX_B * R;                                   // [warps][16][8] partial tiles
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n0 = blockIdx.x * R;
+    const int nr = min(R, p.din - n0);
+    const int cpr = HD / 8;   // 16-byte pieces of a row
+    const uint16_t* wsrc = p.Wo + (size_t)n0 * HD;
+    for (int i = tid; i < nr * cpr; i += OG_THREADS) {
+        const int r = i / cpr, j = i - r * cpr;
+        cp_async16(Ws + (size_t)r * pitch + j * 8, wsrc + (size_t)r * HD + j * 8);
+    }
+    cp_async_commit();
+    // rows the MMAs read but no output keeps: zero, so they hold numbers
+    for (int i = tid; i < (R - nr) * cpr; i += OG_THREADS) {
+        const int r = nr + i / cpr, j = i - (i / cpr) * cpr;
+        *reinterpret_cast<uint4*>(Ws + (size_t)r * pitch + j * 8) = make_uint4(0, 0, 0, 0);
+    }
+    for (int i = tid; i < B * R; i += OG_THREADS) {
+        const int b = i / R, r = i - b * R;
+        const int f = p.bl_off[b + 1] - 1;   // the final backlog row of sequence b
+        res[i] = (r < nr && f >= 0 && f < p.N) ? bf16_to_f32(p.u[(size_t)f * p.din + n0 + r]) : 0.f;
+    }
+    const int nks = HD / 16;
+    const int kper = (nks + OG_WARPS - 1) / OG_WARPS;
+    const int k0 = warp * kper, k1 = min(nks, k0 + kper);
+    const int gq = lane >> 2, cq = lane & 3;
+    pdl_wait();   // obf is the attention kernel's output
+    pdl_trigger();
+    // B fragments of this warp's K steps: row gq of the attention output,
+    // columns 16 ks + 2 cq (+1) and 16 ks + 8 + 2 cq (+1)
+    uint32_t bf[OG_MAX_KPW][2];
+#pragma unroll
+    for (int j = 0; j < OG_MAX_KPW; ++j) {
+        const int ks = k0 + j;
+        const bool ok = ks < k1 && gq < B;
+        const unsigned int* src = reinterpret_cast<const unsigned int*>(p.obf + (size_t)gq * HD + ks * 16 + 2 * cq);
+        bf[j][0] = ok ? __ldcg(src) : 0u;
+        bf[j][1] = ok ? __ldcg(src + 4) : 0u;
+    }
+    cp_async_wait_0();
+    __syncthreads();   // the weight slice has landed
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+    for (int j = 0; j < OG_MAX_KPW; ++j) {
+        const int ks = k0 + j;
+        if (ks >= k1) break;
+        uint32_t a[4];
+        ldsm_x4(a, smem_u32(Ws + (size_t)((mi & 1) * 8 + r8) * pitch + ks * 16 + (mi >> 1) * 8));
+        mma_bf16_16816(c, a, bf[j][0], bf[j][1]);
+    }
+    // partial tiles -> shared memory: thread holds rows gq, gq + 8 and columns 2 cq, 2 cq + 1
+    float* rw = red + (size_t)warp * R * 8;
+    rw[gq * 8 + 2 * cq] = c[0];
+    rw[gq * 8 + 2 * cq + 1] = c[1];
+    rw[(gq + 8) * 8 + 2 * cq] = c[2];
+    rw[(gq + 8) * 8 + 2 * cq + 1] = c[3];
+    __syncthreads();
+    if (tid < R * 8) {
+        const int row = tid >> 3, col = tid & 7;   // 16 rows x 8 columns, one a thread
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < OG_WARPS; ++w) v += red[(size_t)w * R * 8 + row * 8 + col];
+        if (row < nr && col < B) p.out[(size_t)col * p.din + n0 + row] = res[col * R + row] + v;
+    }
+}
+
+size_t catchup_oproj_gemv_smem(int HD) {
+    return (size_t)OG_R * (HD + 8) * 2 + (size_t)OG_MAX_B * OG_R * 4 + (size_t)OG_WARPS * OG_R * 8 * 4;
+}
+
 // ------------------------------------------------------------------ host side
 // Shared memory of a proj_kernel CTA with `stages` ring stages of tile width bn.
 static size_t proj_smem(int stages, int bn) {
@@ -1282,7 +1389,33 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     CU_TRY(launch_cluster(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s,
                           ap.cluster ? (unsigned)ap.chunks : 1u, ap));
 
-    // output projection with the residual
+    // output projection with the residual: a GEMV for a few rows whose weight
+    // slices fit in shared memory in one wave, else the tensor-core kernel
+    const int og_ctas = cdiv(a->din, OG_R);
+    const size_t og_smem = catchup_oproj_gemv_smem(HD);
+    if (a->B <= OG_MAX_B && og_ctas <= 2 * num_sms() && HD <= OG_WARPS * OG_MAX_KPW * 16 &&
+        og_smem <= 110 * 1024) {
+        static bool og_attr[64] = {false};
+        if (dev < 64 && !og_attr[dev]) {
+            if (cudaFuncSetAttribute(oproj_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(oproj_gemv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+                    cudaSuccess)
+                return WF_ERR_CUDA;
+            og_attr[dev] = true;
+        }
+        OgParams og = {};
+        og.Wo = a->Wo;
+        og.obf = ap.obf;
+        og.u = a->u;
+        og.bl_off = a->bl_off;
+        og.out = a->out;
+        og.B = a->B;
+        og.N = a->N;
+        og.din = a->din;
+        og.HD = HD;
+        return launch(oproj_gemv_kernel, dim3(og_ctas), dim3(OG_THREADS), og_smem, s, og);
+    }
     CUtensorMap oA[2], oW[3];
     if (!act_map(&oA[0], ap.obf, a->B, HD) || !make_map(&oW[0], a->Wo, a->din, HD, L.bn)) return WF_ERR_CUDA;
     oA[1] = oA[0];
