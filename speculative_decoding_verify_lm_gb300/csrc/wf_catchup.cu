@@ -893,8 +893,6 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     if (p.cluster) {
         // this split's partial stays in its own shared memory, after the warp merge area
         float* mine = red + (size_t)4 * 16 * rs;            // [hq][D + 2]
-        float* stat = mine + (size_t)hq * (D + 2);           // [chunks][hq] max -> weight, [chunks][hq] sum
-        float* mtot = stat + (size_t)2 * p.chunks * hq;      // [hq] 1 / merged sum
         for (int idx = tid; idx < hq * (D + 2); idx += AT_THREADS) {
             const int h = idx / (D + 2), e = idx - h * (D + 2);
             float M = -INFINITY;
@@ -914,48 +912,40 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
             mine[idx] = v;
         }
         cluster_sync();   // every split's partial is in its shared memory
+        // this split finishes output pairs [c * per_c, (c + 1) * per_c): a
+        // thread fetches every split's (max, sum) of its head and its two
+        // values in one batch, then weighs the splits in index order
         const int CS = p.chunks;
         const uint32_t mine_s = smem_u32(mine);
-        for (int i = tid; i < CS * hq; i += AT_THREADS) {
-            const int s2 = i / hq, h = i - s2 * hq;
-            const uint32_t a = dsmem_map(mine_s + (uint32_t)((h * (D + 2) + D) * 4), (uint32_t)s2);
-            stat[i] = dsmem_ld1(a);
-            stat[CS * hq + i] = dsmem_ld1(a + 4);
-        }
-        __syncthreads();
-        if (tid < hq) {
-            float M = -INFINITY;
-            for (int s2 = 0; s2 < CS; ++s2) M = fmaxf(M, stat[s2 * hq + tid]);
-            float L = 0.f;
-            for (int s2 = 0; s2 < CS; ++s2) {
-                const float ms = stat[s2 * hq + tid];
-                const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);   // a split with no rows weighs 0
-                stat[s2 * hq + tid] = w;
-                L = fmaf(w, stat[CS * hq + s2 * hq + tid], L);
-            }
-            mtot[tid] = L > 0.f ? 1.f / L : 0.f;
-        }
-        __syncthreads();
-        // this split finishes output pairs [c * per_c, (c + 1) * per_c), every split's values in index order
         const int items = hq * (D / 2);
         const int per_c = (items + CS - 1) / CS;
         const int i1 = min(items, (c + 1) * per_c);
         for (int it = c * per_c + tid; it < i1; it += AT_THREADS) {
             const int h = it / (D / 2), e = it - h * (D / 2);
-            const uint32_t a = mine_s + (uint32_t)((h * (D + 2) + 2 * e) * 4);
-            float2 ov[AT_CLUSTER_MAX];
-#pragma unroll
-            for (int s2 = 0; s2 < AT_CLUSTER_MAX; ++s2)
-                if (s2 < CS) ov[s2] = dsmem_ld2(dsmem_map(a, (uint32_t)s2));
-            float a0 = 0.f, a1 = 0.f;
+            const uint32_t av = mine_s + (uint32_t)((h * (D + 2) + 2 * e) * 4);
+            const uint32_t as = mine_s + (uint32_t)((h * (D + 2) + D) * 4);   // (max, sum), adjacent
+            float2 ov[AT_CLUSTER_MAX], st[AT_CLUSTER_MAX];
 #pragma unroll
             for (int s2 = 0; s2 < AT_CLUSTER_MAX; ++s2)
                 if (s2 < CS) {
-                    const float w = stat[s2 * hq + h];
+                    ov[s2] = dsmem_ld2(dsmem_map(av, (uint32_t)s2));
+                    st[s2] = dsmem_ld2(dsmem_map(as, (uint32_t)s2));
+                }
+            float M = -INFINITY;
+#pragma unroll
+            for (int s2 = 0; s2 < AT_CLUSTER_MAX; ++s2)
+                if (s2 < CS) M = fmaxf(M, st[s2].x);
+            float L = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < AT_CLUSTER_MAX; ++s2)
+                if (s2 < CS) {
+                    const float w = st[s2].x == -INFINITY ? 0.f : exp2f(st[s2].x - M);   // a split with no rows weighs 0
+                    L = fmaf(w, st[s2].y, L);
                     a0 = fmaf(w, ov[s2].x, a0);
                     a1 = fmaf(w, ov[s2].y, a1);
                 }
-            const float r0 = a0 * mtot[h], r1 = a1 * mtot[h];
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float r0 = a0 * inv, r1 = a1 * inv;
             const size_t o2 = (size_t)b * p.HD + ((size_t)g * hq + h) * D + 2 * e;
             *reinterpret_cast<uint32_t*>(p.obf + o2) = pack_bf16x2(r0, r1);
             if (p.attn) {
