@@ -451,9 +451,11 @@ __global__ void __launch_bounds__(PJ_THREADS)
     const int lt = t - g.tile0, mt = lt / g.tiles_n, nt = lt % g.tiles_n;
     const int kb0 = split * p.kb_per;
     const int kb1 = min(p.num_k, kb0 + p.kb_per);
-    const int rpc = BM / S;                                        // rows of the tile each split finishes
-    const int r0 = split * rpc;
-    const int nrows = max(0, min(rpc, g.M - (mt * BM + r0)));     // of them, rows that exist
+    // the tile's rows that exist, shared out evenly: split r finishes rows [r0, r0 + nrows)
+    const int tile_rows = max(0, min(BM, g.M - mt * BM));
+    const int rpc = (tile_rows + S - 1) / S;
+    const int r0 = min(tile_rows, split * rpc);
+    const int nrows = max(0, min(rpc, tile_rows - r0));
     const CUtensorMap* mA = g.a ? &tmA1 : &tmA0;
     const CUtensorMap* mW = g.w == 0 ? &tmW0 : (g.w == 1 ? &tmW1 : &tmW2);
 
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(PJ_THREADS)
     if (S > 1) cluster_sync();   // every split's partial tile is in its shared memory
 
     // ---------------------------------------------------- epilogue of this split's rows
-    // Split r finishes rows [r0, r0 + rpc) of the tile, pulling the other
+    // Split r finishes rows [r0, r0 + nrows) of the tile, pulling the other
     // splits' partial rows over distributed shared memory (every split's loads
     // of an item in flight together) and summing in split order.
     const int col0 = nt * p.bn;
@@ -759,7 +761,10 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
         const float v = h < hq ? p.q[(size_t)b * p.HD + ((size_t)g * hq + h) * D + e] * qscale : 0.f;
         qs[h * stride + e] = f32_to_bf16(v);
     }
-    if (nr0 > 0) stage_rows(t0, 0, split0, nr0);   // rows this call appends
+    // rows this call appends, one copy group per pass, so that the first pass
+    // need not wait for the second pass's rows
+    if (nr0 > 0) stage_rows(t0, 0, split0, nr0);
+    cp_async_commit();
     if (nr1 > 0) stage_rows(t0 + R, 1, split1, nr1);
     cp_async_commit();
     __syncthreads();   // qs written
@@ -781,7 +786,9 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
 
     int pass = 0;
     for (int p0 = t0; p0 < t1; p0 += R, ++pass) {
-        if (pass >= 1 && p0 + R < t1) {   // passes 0 and 1 were staged before the loop
+        if (pass == 0) {
+            cp_async_wait_1();   // all but the second pass's appended rows
+        } else if (p0 + R < t1) {   // passes 0 and 1 were staged before the loop
             stage(p0 + R, (pass + 1) & 1);
             cp_async_wait_1();
         } else {
