@@ -131,6 +131,8 @@ def check_against_oracle(c, res, kv_only=False):
     (5, 192, 6, 3, 48, tuple([1] * 130), tuple(range(130)), 131),         # 130 sequences: two row tiles
     (6, 64, 2, 1, 16, (50,), (4000,), 4096),                              # 16 splits: the largest cluster merge
     (7, 128, 4, 2, 32, (40,), (5000,), 5100),                             # 20 splits: merged through global memory
+    (8, 160, 4, 2, 32, (2, 3, 1, 5, 2, 1, 4, 2), (5,) * 8, 16),           # 8 sequences: the few-row output projection
+    (9, 160, 4, 2, 32, (2, 3, 1, 5, 2, 1, 4, 2, 3), (5,) * 9, 16),        # 9: the tensor-core output projection
 ])
 def test_catchup_small_shapes(seed, din, H, G, D, n, L, cap):
     c = pins.catchup_case(seed, din=din, H=H, G=G, D=D, n=n, L=L, cap=cap)
