@@ -33,8 +33,8 @@ wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t
                              void* ws, cudaStream_t s);
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
-                              size_t cand_off, int* bn_out, cudaStream_t s);
-wf_status launch_topk_merge(int B, int Vd, int bn, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+                              size_t cand_off, int* num_n2_out, cudaStream_t s);
+wf_status launch_topk_merge(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                             float* vals, void* ws, size_t cand_off, cudaStream_t s);
 wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s);
 size_t catchup_workspace_bytes(int B, int N, int din, int H, int G, int D);
@@ -258,9 +258,9 @@ wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P,
     const Layout L = layout(P, B, d, 0, Vd, k);
     WF_TRY(check_ws(ws, ws_bytes, L.part));   // control block, keys and top-k candidates
     WF_TRY(check_device());
-    int bn = 0;
-    WF_TRY(launch_lmhead_draft(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, L.cand, &bn, stream));
-    return launch_topk_merge(B, Vd, bn, k, d2t, draft_ids, tids, vals, ws, L.cand, stream);
+    int num_n2 = 0;
+    WF_TRY(launch_lmhead_draft(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, L.cand, &num_n2, stream));
+    return launch_topk_merge(B, Vd, num_n2, k, d2t, draft_ids, tids, vals, ws, L.cand, stream);
 }
 
 static bool bad_catchup_shape(int B, int N, int din, int H, int G, int D) {
@@ -350,10 +350,10 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         // LM head's weight sweep (W, then Wd) and its candidates are merged last.
         const bool beside = a->P <= ROUTER_BESIDE_MAX_ROWS;
         const bool shared = draft && a->P <= BM && a->B <= BM;
-        int bn = 0;
+        int num_n2 = 0;
         if (shared)
             WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
-                                       a->Vd, a->k, ws, L.cand, &bn, stream));
+                                       a->Vd, a->k, ws, L.cand, &num_n2, stream));
         else
             WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
         if (beside) {
@@ -370,7 +370,7 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
                                  a->delta_al, a->route, ws, L.part, stream));
         }
         if (shared)
-            return launch_topk_merge(a->B, a->Vd, bn, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws, L.cand,
+            return launch_topk_merge(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws, L.cand,
                                      stream);
         if (draft)
             WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals,

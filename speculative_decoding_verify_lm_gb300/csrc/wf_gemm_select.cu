@@ -45,7 +45,9 @@ struct GemmParams {
     int num_m, num_n, num_k;
     int k;             // top-k count (top-k mode)
     int bn;            // weight rows per tile (UMMA N): a multiple of 16, 128..256
+    int nbig;          // tiles of bn rows; the other num_n - nbig tiles have bn - 16 (big ones first)
     uint32_t idesc;    // instruction descriptor for M = BM, N = bn
+    uint32_t idesc_s;  // ... N = bn - 16
     int weight_evict_first;
     int a_bytes;       // bytes one activation box delivers (box rows x 128 B)
     uint64_t* keys;    // argmax: [M_rows] packed keys, zero on entry, zero on exit
@@ -61,6 +63,8 @@ struct GemmParams {
     // DUAL: the second problem (top-k, one activation tile) whose num_n2 tiles
     // follow the first problem's; its candidate lists go to cand
     int M_rows2, N_w2, num_n2, a_bytes2;
+    int bn2, nbig2;             // its tile heights: nbig2 of bn2 rows, the rest bn2 - 16 (big ones last)
+    uint32_t idesc2, idesc2_s;
     Control* ctrl;
     uint64_t timeout_ns;
 };
@@ -102,6 +106,24 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], floa
     }
 }
 
+// Weight rows of tile n of a problem with num_n tiles: nbig of them are bn
+// rows high, the others bn - 16 (all bn when nbig = num_n), the big ones first
+// or last.  Two heights let the tile count be a multiple of the CTA count, so
+// that every CTA sweeps the same number of weight rows within 16 a tile.
+struct TileSpan {
+    int row0, rows;
+    bool big;
+};
+__device__ __forceinline__ TileSpan tile_span(int n, int num_n, int bn, int nbig, bool big_first) {
+    const int ns = num_n - nbig;
+    if (big_first) {
+        if (n < nbig) return {n * bn, bn, true};
+        return {nbig * bn + (n - nbig) * (bn - 16), bn - 16, false};
+    }
+    if (n < ns) return {n * (bn - 16), bn - 16, false};
+    return {ns * (bn - 16) + (n - ns) * bn, bn, true};
+}
+
 // One finished accumulator as epilogue thread rit sees it (activation row
 // m * BM + rit of a problem with M_rows rows and N_w weight rows): wait for
 // it, keep the row's best (KT = 1) or top KT over the tile's columns and, with
@@ -111,8 +133,8 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KT], int (&ti)[KT], floa
 template <int KT, bool ENT>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfull, uint64_t* tempty,
                                               volatile int* abort_flag, uint32_t tmem_base, uint32_t tile_i, int q,
-                                              int rit, int M_rows, int N_w, int m, int n, int cand_num_m, float& em,
-                                              float& es, float& et) {
+                                              int rit, int M_rows, int N_w, int m, int n, const TileSpan sp,
+                                              int cand_num_m, float& em, float& es, float& et) {
     const uint32_t acc = tile_i & 1;
     const uint32_t acc_ph = (tile_i >> 1) & 1;
     const bool quad_live = m * BM + q * 32 < M_rows;
@@ -131,14 +153,14 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
     }
     if (quad_live) {
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-        for (int c0 = 0; c0 < p.bn; c0 += 32) {
+        for (int c0 = 0; c0 < sp.rows; c0 += 32) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tbase + c0, r);
             tmem_ld_wait();
-            const int col0 = n * p.bn + c0;
+            const int col0 = sp.row0 + c0;
             // columns >= lim are past the weight matrix or past this tile; rows
             // past the activations (stale shared-memory rows) take no part
-            const int lim = row < M_rows ? min(N_w - col0, p.bn - c0) : 0;
+            const int lim = row < M_rows ? min(N_w - col0, sp.rows - c0) : 0;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float v = __uint_as_float(r[j]);
@@ -209,6 +231,7 @@ template <int KT, int CL, bool ENT, bool DUAL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                       const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB2s,
                        const GemmParams p) {
     static_assert(!DUAL || (KT == 1 && CL == 1 && !ENT), "the dual sweep pairs an argmax head with a top-k head");
     extern __shared__ uint8_t smem_raw[];
@@ -249,9 +272,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (p.nbig < p.num_n) tma_prefetch_desc(&tmBs);
         if constexpr (DUAL) {
             tma_prefetch_desc(&tmA2);
             tma_prefetch_desc(&tmB2);
+            if (p.nbig2 < p.num_n2) tma_prefetch_desc(&tmB2s);
         }
     }
     if (warp == 1) {
@@ -274,16 +299,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_w = p.weight_evict_first ? policy_evict_first() : policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
-            const int half = p.bn / CL;                // weight rows this CTA fetches per stage
+            const int half = p.bn / CL;                // weight rows this CTA fetches per stage (pairs: uniform tiles)
             uint32_t it = 0;  // stages issued so far
             bool ok = true;
             for (int u = slot; u < U && ok; u += nslots) {
                 const bool second = DUAL && u >= U0;
                 const int m = second ? 0 : (u % num_mp) * CL + rank;
                 const int n = second ? u - U0 : u / num_mp;
+                const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
+                                           : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const CUtensorMap* mA = second ? &tmA2 : &tmA;
-                const CUtensorMap* mB = second ? &tmB2 : &tmB;
-                const uint32_t tx = (second ? p.a_bytes2 : p.a_bytes) + p.bn * BK * 2;
+                const CUtensorMap* mB = second ? (sp.big ? &tmB2 : &tmB2s) : (sp.big ? &tmB : &tmBs);
+                const uint32_t tx = (second ? p.a_bytes2 : p.a_bytes) + sp.rows * BK * 2;
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -296,9 +323,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tma_load_2d(sA + s * A_BYTES, mA, &full[s], kc * BK, m * BM, pol_a);
                     if constexpr (CL == 2)
                         tma_load_2d_multicast(sB + s * B_BYTES + rank * half * BK * 2, mB, &full[s], kc * BK,
-                                              n * p.bn + rank * half, kPair, pol_w);
+                                              sp.row0 + rank * half, kPair, pol_w);
                     else
-                        tma_load_2d(sB + s * B_BYTES, mB, &full[s], kc * BK, n * p.bn, pol_w);
+                        tma_load_2d(sB + s * B_BYTES, mB, &full[s], kc * BK, sp.row0, pol_w);
                 }
             }
             if (!ok || *abort_flag) {
@@ -310,10 +337,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = p.idesc;
             uint32_t it = 0, tile_i = 0;
             bool ok = true, issued = false;
             for (int u = slot; u < U && ok; u += nslots, ++tile_i) {
+                const bool second = DUAL && u >= U0;
+                const int n = second ? u - U0 : u / num_mp;
+                const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
+                                           : tile_span(n, p.num_n, p.bn, p.nbig, true);
+                const uint32_t idesc = second ? (sp.big ? p.idesc2 : p.idesc2_s) : (sp.big ? p.idesc : p.idesc_s);
                 const uint32_t acc = tile_i & 1;
                 const uint32_t acc_ph = (tile_i >> 1) & 1;
                 if (!mbar_wait(&tempty[acc], acc_ph ^ 1, p.timeout_ns, abort_flag)) {
@@ -361,10 +392,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             bool ok;
             if (DUAL && u >= U0)
                 ok = epilogue_tile<KT_TOPK, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
-                                                   p.M_rows2, p.N_w2, 0, u - U0, 1, em, es, et);
+                                                   p.M_rows2, p.N_w2, 0, u - U0,
+                                                   tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false), 1, em, es, et);
             else
                 ok = epilogue_tile<KT, ENT>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
-                                            p.N_w, (u % num_mp) * CL + rank, u / num_mp, p.num_m, em, es, et);
+                                            p.N_w, (u % num_mp) * CL + rank, u / num_mp,
+                                            tile_span(u / num_mp, p.num_n, p.bn, p.nbig, true), p.num_m, em, es, et);
             if (!ok) break;
         }
         if constexpr (ENT) {
@@ -565,6 +598,30 @@ static int pick_bn(int num_m, int N_w, int sms, int N_w2 = 0) {
     return best;
 }
 
+// Balanced tiles for one weight matrix swept by `sms` CTAs with one
+// activation tile: the fewest tiles of at most BN rows whose count is a
+// multiple of sms, nbig of them bn rows high and the rest bn - 16, so that the
+// round-robin tile schedule gives every CTA the same number of tiles and the
+// same weight rows within 16 a tile.  False when a CTA would get fewer than
+// BN_MIN rows (pick_bn's uniform tiles are used then).
+struct TileGeom {
+    int num_n, bn, nbig;
+};
+static bool balanced_tiles(int N_w, int sms, TileGeom* g) {
+    if (sms < 1 || N_w < sms * BN_MIN) return false;
+    const int T = sms * cdiv(N_w, sms * BN);
+    const int hs = N_w / T / 16 * 16;   // the average height, rounded down to 16
+    g->num_n = T;
+    if (T * hs == N_w) {
+        g->bn = hs;
+        g->nbig = T;
+    } else {
+        g->bn = hs + 16;
+        g->nbig = cdiv(N_w - T * hs, 16);   // the last tile may reach up to 15 rows past the matrix
+    }
+    return true;
+}
+
 // Clusters of two that can be resident at once (queried once per device).
 template <int KT, bool ENT>
 static int pair_slots(int dev) {
@@ -592,7 +649,7 @@ static int pair_slots(int dev) {
 
 template <int KT, bool ENT>
 static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, GemmParams p,
-                               cudaStream_t s) {
+                               cudaStream_t s, int* num_n_out = nullptr) {
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
@@ -604,7 +661,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
             return WF_ERR_CUDA;
         attr_set[dev] = true;
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tbs;
     const int num_m = cdiv(M_rows, BM);
     if (ENT && num_m > 2) return WF_ERR_UNSUPPORTED;
     // several activation tiles: pairs of CTAs share each weight tile (multicast)
@@ -615,15 +672,27 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     // box hold stale data and produce accumulator rows the epilogue never keeps.
     const int a_rows = num_m == 1 ? (M_rows + 7) / 8 * 8 : BM;
     if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, (uint32_t)a_rows)) return WF_ERR_CUDA;
-    const int bn = pick_bn(num_m, N_w, num_sms());
+    TileGeom tg;
+    if (CL == 1 && balanced_tiles(N_w, num_sms(), &tg)) {
+        p.num_n = tg.num_n;
+        p.bn = tg.bn;
+        p.nbig = tg.nbig;
+    } else {
+        p.bn = pick_bn(num_m, N_w, num_sms());
+        p.num_n = cdiv(N_w, p.bn);
+        p.nbig = p.num_n;
+    }
+    const int bn = p.bn;
     // each CTA of a pair fetches half of the weight tile
     if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn / CL))) return WF_ERR_CUDA;
+    tbs = tb;
+    if (p.nbig < p.num_n && !make_map(&tbs, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn - 16))) return WF_ERR_CUDA;
+    if (num_n_out) *num_n_out = p.num_n;
     p.M_rows = M_rows;
     p.N_w = N_w;
     p.num_m = num_m;
-    p.num_n = cdiv(N_w, bn);
-    p.bn = bn;
     p.idesc = umma_idesc_bf16(BM, bn);
+    p.idesc_s = p.nbig < p.num_n ? umma_idesc_bf16(BM, bn - 16) : p.idesc;
     p.num_k = cdiv(d, BK);
     p.weight_evict_first = p.num_m == 1;
     p.a_bytes = a_rows * BK * 2;
@@ -633,14 +702,14 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
         int grid = tiles < num_sms() ? tiles : num_sms();
         if (ENT && grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
         return launch(gemm_select_kernel<KT, 1, ENT, false>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, ta,
-                      tb, p);
+                      tb, tbs, tbs, p);
     }
     const int pairs = cdiv(num_m, 2) * p.num_n;
     int slots = pair_slots<KT, ENT>(dev);
     if (ENT && slots > ENT_MAX_SLOTS) slots = ENT_MAX_SLOTS;
     const int grid = 2 * (pairs < slots ? pairs : slots);
     return launch_cluster(gemm_select_kernel<KT, 2, ENT, false>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta,
-                          tb, ta, tb, p);
+                          tb, ta, tb, tb, tb, p);
 }
 
 static GemmParams params_for(void* ws) {
@@ -682,20 +751,20 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     GemmParams p = params_for(ws);
     p.k = k;
     p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
-    wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s);
+    int num_n = 0;
+    wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s, &num_n);
     if (st != WF_OK) return st;
-    const int bn = pick_bn(cdiv(B, BM), Vd, num_sms());
     return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, (const uint64_t*)p.cand, B, cdiv(B, BM),
-                  cdiv(Vd, bn), k, d2t, Vd, draft_ids, tids, vals, p.ctrl);
+                  num_n, k, d2t, Vd, draft_ids, tids, vals, p.ctrl);
 }
 
 // Target LM head (argmax over P <= BM rows) and draft head (candidate lists of
 // the top k over B <= BM rows) in one persistent sweep of W then Wd.  The
-// candidate lists are merged by launch_topk_merge with the tile height this
-// returns in *bn_out.
+// candidate lists are merged by launch_topk_merge over the draft-head tile
+// count this returns in *num_n2_out.
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
-                              size_t cand_off, int* bn_out, cudaStream_t s) {
+                              size_t cand_off, int* num_n2_out, cudaStream_t s) {
     if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -707,21 +776,41 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
         attr_set[dev] = true;
     }
     const int sms = num_sms();
-    const int bn = pick_bn(1, V, sms, Vd);
-    const int a_rows = (P + 7) / 8 * 8, a_rows2 = (B + 7) / 8 * 8;
-    CUtensorMap ta, tb, ta2, tb2;
-    if (!make_map(&ta, hidden, (uint64_t)P, (uint64_t)d, (uint32_t)a_rows) ||
-        !make_map(&tb, W, (uint64_t)V, (uint64_t)d, (uint32_t)bn) ||
-        !make_map(&ta2, x, (uint64_t)B, (uint64_t)d, (uint32_t)a_rows2) ||
-        !make_map(&tb2, Wd, (uint64_t)Vd, (uint64_t)d, (uint32_t)bn))
-        return WF_ERR_CUDA;
     GemmParams p = params_for(ws);
+    // both matrices in balanced tiles (every CTA sweeps the same rows of each),
+    // else one uniform tile height over both
+    TileGeom g1, g2;
+    if (balanced_tiles(V, sms, &g1) && balanced_tiles(Vd, sms, &g2)) {
+        p.num_n = g1.num_n;
+        p.bn = g1.bn;
+        p.nbig = g1.nbig;
+        p.num_n2 = g2.num_n;
+        p.bn2 = g2.bn;
+        p.nbig2 = g2.nbig;
+    } else {
+        p.bn = p.bn2 = pick_bn(1, V, sms, Vd);
+        p.num_n = p.nbig = cdiv(V, p.bn);
+        p.num_n2 = p.nbig2 = cdiv(Vd, p.bn);
+    }
+    const int a_rows = (P + 7) / 8 * 8, a_rows2 = (B + 7) / 8 * 8;
+    CUtensorMap ta, tb, ta2, tb2, tbs, tb2s;
+    if (!make_map(&ta, hidden, (uint64_t)P, (uint64_t)d, (uint32_t)a_rows) ||
+        !make_map(&tb, W, (uint64_t)V, (uint64_t)d, (uint32_t)p.bn) ||
+        !make_map(&ta2, x, (uint64_t)B, (uint64_t)d, (uint32_t)a_rows2) ||
+        !make_map(&tb2, Wd, (uint64_t)Vd, (uint64_t)d, (uint32_t)p.bn2))
+        return WF_ERR_CUDA;
+    tbs = tb;
+    tb2s = tb2;
+    if (p.nbig < p.num_n && !make_map(&tbs, W, (uint64_t)V, (uint64_t)d, (uint32_t)(p.bn - 16))) return WF_ERR_CUDA;
+    if (p.nbig2 < p.num_n2 && !make_map(&tb2s, Wd, (uint64_t)Vd, (uint64_t)d, (uint32_t)(p.bn2 - 16)))
+        return WF_ERR_CUDA;
     p.M_rows = P;
     p.N_w = V;
     p.num_m = 1;
-    p.num_n = cdiv(V, bn);
-    p.bn = bn;
-    p.idesc = umma_idesc_bf16(BM, bn);
+    p.idesc = umma_idesc_bf16(BM, p.bn);
+    p.idesc_s = p.nbig < p.num_n ? umma_idesc_bf16(BM, p.bn - 16) : p.idesc;
+    p.idesc2 = umma_idesc_bf16(BM, p.bn2);
+    p.idesc2_s = p.nbig2 < p.num_n2 ? umma_idesc_bf16(BM, p.bn2 - 16) : p.idesc2;
     p.num_k = cdiv(d, BK);
     p.weight_evict_first = 1;
     p.a_bytes = a_rows * BK * 2;
@@ -731,21 +820,20 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
     p.M_rows2 = B;
     p.N_w2 = Vd;
-    p.num_n2 = cdiv(Vd, bn);
     p.a_bytes2 = a_rows2 * BK * 2;
     p.timeout_ns = wait_timeout_ns();
     const int tiles = p.num_n + p.num_n2;
-    *bn_out = bn;
+    *num_n2_out = p.num_n2;
     return launch(gemm_select_kernel<1, 1, false, true>, dim3(tiles < sms ? tiles : sms), dim3(GEMM_THREADS),
-                  GEMM_SMEM, s, ta, tb, ta2, tb2, p);
+                  GEMM_SMEM, s, ta, tb, ta2, tb2, tbs, tb2s, p);
 }
 
 // Merge the per-tile candidate lists of B rows (one activation tile) into the
 // top k, mapped through d2t.
-wf_status launch_topk_merge(int B, int Vd, int bn, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+wf_status launch_topk_merge(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                             float* vals, void* ws, size_t cand_off, cudaStream_t s) {
     const uint64_t* cand = reinterpret_cast<const uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
-    return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, cand, B, cdiv(B, BM), cdiv(Vd, bn), k, d2t,
+    return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, cand, B, cdiv(B, BM), num_n, k, d2t,
                   Vd, draft_ids, tids, vals, reinterpret_cast<Control*>(ws));
 }
 
