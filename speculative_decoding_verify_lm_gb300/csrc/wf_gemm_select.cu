@@ -6,7 +6,10 @@
 // Per CTA (one per SM, persistent over tiles of BM activation rows x BN
 // weight rows):
 //   warp 0     TMA producer: stages [BK x BM] activation and [BK x BN] weight
-//              boxes (128-byte swizzle) into a STAGES-deep shared-memory ring
+//              boxes (128-byte swizzle) into a shared-memory ring of p.stages
+//              stages (4 with several activation tiles; with one, the
+//              activation slot is only as large as the box and the ring 5-6
+//              stages deep, so more weight bytes are in flight per SM)
 //   warp 1     allocates TMEM (2 x BN fp32 columns = two accumulators) and one
 //              elected lane issues tcgen05.mma (M=128, N=256, K=16) per stage
 //   warps 2-5  epilogue: tcgen05.ld the finished accumulator (thread = one
@@ -31,18 +34,26 @@
 
 namespace wf {
 
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;             // ring depth with several activation tiles
+constexpr int STAGES_MAX = 8;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int GEMM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
 constexpr int GEMM_SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
+// Ring bytes with one activation tile: leaves room on the SM for the small
+// CTAs that run beside the sweep (the router over every row of a short round).
+constexpr int RING_BUDGET = 210 * 1024;
+constexpr int GEMM_SMEM_MAX = RING_BUDGET + 1024 + 256;
 constexpr int KT_TOPK = WF_MAX_TOPK;
 
 struct GemmParams {
     int M_rows;        // activation rows (P or B)
     int N_w;           // weight rows (V or Vd)
     int num_m, num_n, num_k;
+    int stages;        // ring stages (<= STAGES_MAX)
+    int stage_bytes;   // activation slot + weight slot (a multiple of 1024)
+    int a_alloc;       // activation slot bytes (a multiple of 1024)
     int k;             // top-k count (top-k mode)
     int bn;            // weight rows per tile (UMMA N): a multiple of 16, 128..256
     int nbig;          // tiles of bn rows; the other num_n - nbig tiles have bn - 16 (big ones first)
@@ -236,11 +247,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     static_assert(!DUAL || (KT == 1 && CL == 1 && !ENT), "the dual sweep pairs an argmax head with a top-k head");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;
+    const int stages = p.stages;
+    // stage s: activation slot at s * stage_bytes, weight slot a_alloc bytes on
+    // (the MMA reads BM activation rows; past a short box those are the same
+    // stage's weight rows, which only feed accumulator rows nobody keeps)
+    auto stA = [&](int st) { return smem + (size_t)st * p.stage_bytes; };
+    auto stB = [&](int st) { return smem + (size_t)st * p.stage_bytes + p.a_alloc; };
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * p.stage_bytes);
+    uint64_t* empty = full + STAGES_MAX;
+    uint64_t* tfull = empty + STAGES_MAX;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -258,7 +273,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     constexpr uint16_t kPair = 0x3;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], CL);
         }
@@ -301,6 +316,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const uint64_t pol_a = policy_evict_last();
             const int half = p.bn / CL;                // weight rows this CTA fetches per stage (pairs: uniform tiles)
             uint32_t it = 0;  // stages issued so far
+            int s = 0;        // = it % stages
+            uint32_t ph = 0;  // = (it / stages) & 1
             bool ok = true;
             for (int u = slot; u < U && ok; u += nslots) {
                 const bool second = DUAL && u >= U0;
@@ -312,32 +329,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const CUtensorMap* mB = second ? (sp.big ? &tmB2 : &tmB2s) : (sp.big ? &tmB : &tmBs);
                 const uint32_t tx = (second ? p.a_bytes2 : p.a_bytes) + sp.rows * BK * 2;
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
+                    if (it > 0) {
+                        if (++s == stages) {
+                            s = 0;
+                            ph ^= 1;
+                        }
+                    }
                     if (!mbar_wait(&empty[s], ph ^ 1, p.timeout_ns, abort_flag)) {
                         gemm_fail(p.ctrl, abort_flag, 0x100 + s);
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], tx);
-                    tma_load_2d(sA + s * A_BYTES, mA, &full[s], kc * BK, m * BM, pol_a);
+                    tma_load_2d(stA(s), mA, &full[s], kc * BK, m * BM, pol_a);
                     if constexpr (CL == 2)
-                        tma_load_2d_multicast(sB + s * B_BYTES + rank * half * BK * 2, mB, &full[s], kc * BK,
+                        tma_load_2d_multicast(stB(s) + rank * half * BK * 2, mB, &full[s], kc * BK,
                                               sp.row0 + rank * half, kPair, pol_w);
                     else
-                        tma_load_2d(sB + s * B_BYTES, mB, &full[s], kc * BK, sp.row0, pol_w);
+                        tma_load_2d(stB(s), mB, &full[s], kc * BK, sp.row0, pol_w);
                 }
             }
             if (!ok || *abort_flag) {
                 // let every copy this thread issued land before the CTA exits
-                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                    mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.timeout_ns, nullptr);
+                for (uint32_t j = (it > (uint32_t)stages ? it - stages : 0); j < it; ++j)
+                    mbar_wait(&full[j % stages], (j / stages) & 1, p.timeout_ns, nullptr);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t it = 0, tile_i = 0;
+            int s = 0;        // = it % stages
+            uint32_t ph = 0;  // = (it / stages) & 1
             bool ok = true, issued = false;
             for (int u = slot; u < U && ok; u += nslots, ++tile_i) {
                 const bool second = DUAL && u >= U0;
@@ -355,16 +378,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
+                    if (it > 0) {
+                        if (++s == stages) {
+                            s = 0;
+                            ph ^= 1;
+                        }
+                    }
                     if (!mbar_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
                         gemm_fail(p.ctrl, abort_flag, 0x210 + s);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = umma_desc_sw128(smem_u32(sA + s * A_BYTES));
-                    const uint64_t bdesc = umma_desc_sw128(smem_u32(sB + s * B_BYTES));
+                    const uint64_t adesc = umma_desc_sw128(smem_u32(stA(s)));
+                    const uint64_t bdesc = umma_desc_sw128(smem_u32(stB(s)));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per step (encoded >> 4)
                         umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
@@ -622,6 +649,23 @@ static bool balanced_tiles(int N_w, int sms, TileGeom* g) {
     return true;
 }
 
+// The shared-memory ring: with several activation tiles, STAGES stages of a
+// full activation box and a full weight box; with one, an activation slot as
+// large as its box (a_rows x 128 bytes) and as many stages as RING_BUDGET
+// holds.  Returns the dynamic shared memory of the launch.
+static int set_ring(GemmParams& p, int one_tile_a_rows) {
+    if (one_tile_a_rows <= 0) {
+        p.a_alloc = A_BYTES;
+        p.stages = STAGES;
+    } else {
+        p.a_alloc = one_tile_a_rows * BK * 2;   // a multiple of 1024 (rows come in 8s)
+        int st = RING_BUDGET / (p.a_alloc + B_BYTES);
+        p.stages = st < STAGES ? STAGES : (st > STAGES_MAX ? STAGES_MAX : st);
+    }
+    p.stage_bytes = p.a_alloc + B_BYTES;
+    return p.stages * p.stage_bytes + 1024 + 256;
+}
+
 // Clusters of two that can be resident at once (queried once per device).
 template <int KT, bool ENT>
 static int pair_slots(int dev) {
@@ -655,7 +699,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
         if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM) != cudaSuccess ||
+                                 GEMM_SMEM_MAX) != cudaSuccess ||
             cudaFuncSetAttribute(gemm_select_kernel<KT, 2, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM) != cudaSuccess)
             return WF_ERR_CUDA;
@@ -697,18 +741,19 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.weight_evict_first = p.num_m == 1;
     p.a_bytes = a_rows * BK * 2;
     p.timeout_ns = wait_timeout_ns();
+    const int smem = set_ring(p, num_m == 1 ? a_rows : 0);
     if (CL == 1) {
         const int tiles = p.num_m * p.num_n;
         int grid = tiles < num_sms() ? tiles : num_sms();
         if (ENT && grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
-        return launch(gemm_select_kernel<KT, 1, ENT, false>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, ta, tb, ta,
+        return launch(gemm_select_kernel<KT, 1, ENT, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta,
                       tb, tbs, tbs, p);
     }
     const int pairs = cdiv(num_m, 2) * p.num_n;
     int slots = pair_slots<KT, ENT>(dev);
     if (ENT && slots > ENT_MAX_SLOTS) slots = ENT_MAX_SLOTS;
     const int grid = 2 * (pairs < slots ? pairs : slots);
-    return launch_cluster(gemm_select_kernel<KT, 2, ENT, false>, dim3(grid), dim3(GEMM_THREADS), GEMM_SMEM, s, 2u, ta,
+    return launch_cluster(gemm_select_kernel<KT, 2, ENT, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, 2u, ta,
                           tb, ta, tb, tb, tb, p);
 }
 
@@ -771,7 +816,7 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
         if (cudaFuncSetAttribute(gemm_select_kernel<1, 1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM) != cudaSuccess)
+                                 GEMM_SMEM_MAX) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
     }
@@ -824,8 +869,9 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     p.timeout_ns = wait_timeout_ns();
     const int tiles = p.num_n + p.num_n2;
     *num_n2_out = p.num_n2;
-    return launch(gemm_select_kernel<1, 1, false, true>, dim3(tiles < sms ? tiles : sms), dim3(GEMM_THREADS),
-                  GEMM_SMEM, s, ta, tb, ta2, tb2, tbs, tb2s, p);
+    const int smem = set_ring(p, a_rows > a_rows2 ? a_rows : a_rows2);
+    return launch(gemm_select_kernel<1, 1, false, true>, dim3(tiles < sms ? tiles : sms), dim3(GEMM_THREADS), smem,
+                  s, ta, tb, ta2, tb2, tbs, tb2s, p);
 }
 
 // Merge the per-tile candidate lists of B rows (one activation tile) into the
