@@ -43,7 +43,9 @@ def _gapped_hidden(seed, P, d, W, reject=True):
 
 # ------------------------------------------------------------------ LM head
 @pytest.mark.parametrize("P,d,V", [(1, 64, 300), (17, 256, 8192), (61, 128, 1000), (200, 64, 513), (130, 72, 777),
-                                   (5, 8, 40), (256, 192, 2048), (129, 256, 257)])
+                                   (5, 8, 40), (256, 192, 2048), (129, 256, 257),
+                                   # evened-out tiles of two heights; the last one past the matrix
+                                   (40, 256, 76000), (97, 128, 76003)])
 def test_lmhead_argmax(P, d, V):
     W = synth.normal_bf16(7 + P, 0, V, d, 0.02 if d >= 256 else 0.1)
     h = _gapped_hidden(11 + V, P, d, W)
@@ -196,7 +198,8 @@ def test_draft_topk(B, d, Vd, k):
 
 
 @pytest.mark.parametrize("P,B,d,V,Vd,k", [(17, 1, 256, 8192, 4000, 10), (128, 128, 64, 777, 300, 16),
-                                          (61, 2, 72, 1000, 129, 1), (1, 1, 2560, 151936, 32000, 10)])
+                                          (61, 2, 72, 1000, 129, 1), (1, 1, 2560, 151936, 32000, 10),
+                                          (40, 2, 256, 76000, 19456, 10)])
 def test_lmhead_draft_topk_shared_sweep(P, B, d, V, Vd, k):
     """Both heads in one sweep give the oracle's argmax and top-k (and leave the
     workspace zeroed), here and on a reused workspace."""
