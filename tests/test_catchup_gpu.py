@@ -133,6 +133,8 @@ def check_against_oracle(c, res, kv_only=False):
     (7, 128, 4, 2, 32, (40,), (5000,), 5100),                             # 20 splits: merged through global memory
     (8, 160, 4, 2, 32, (2, 3, 1, 5, 2, 1, 4, 2), (5,) * 8, 16),           # 8 sequences: the few-row output projection
     (9, 160, 4, 2, 32, (2, 3, 1, 5, 2, 1, 4, 2, 3), (5,) * 9, 16),        # 9: the tensor-core output projection
+    (10, 4096, 8, 2, 64, (6, 2), (20, 3), 32),                            # a wide input (64 K blocks)
+    (11, 1024, 128, 8, 128, (3,), (10,), 16),                             # H x D = 16384, the largest
 ])
 def test_catchup_small_shapes(seed, din, H, G, D, n, L, cap):
     c = pins.catchup_case(seed, din=din, H=H, G=G, D=D, n=n, L=L, cap=cap)

@@ -45,7 +45,8 @@ def _gapped_hidden(seed, P, d, W, reject=True):
 @pytest.mark.parametrize("P,d,V", [(1, 64, 300), (17, 256, 8192), (61, 128, 1000), (200, 64, 513), (130, 72, 777),
                                    (5, 8, 40), (256, 192, 2048), (129, 256, 257),
                                    # evened-out tiles of two heights; the last one past the matrix
-                                   (40, 256, 76000), (97, 128, 76003)])
+                                   (40, 256, 76000), (97, 128, 76003),
+                                   (9, 16384, 1000)])   # the largest hidden size
 def test_lmhead_argmax(P, d, V):
     W = synth.normal_bf16(7 + P, 0, V, d, 0.02 if d >= 256 else 0.1)
     h = _gapped_hidden(11 + V, P, d, W)
@@ -142,7 +143,8 @@ def test_verify_bad_parent_sets_error():
 
 # ------------------------------------------------------------------ router
 @pytest.mark.parametrize("B,d,m", [(1, 2560, 1024), (1, 2560, 320), (7, 256, 128), (8, 72, 40), (9, 72, 40),
-                                   (12, 2560, 1024), (33, 64, 5), (256, 512, 64)])
+                                   (12, 2560, 1024), (33, 64, 5), (256, 512, 64),
+                                   (3, 4096, 256), (20, 4096, 256)])   # rows too wide for W1 in registers
 def test_router(B, d, m):
     rng = np.random.default_rng(B * 7 + m)
     P = B + 3
@@ -183,7 +185,7 @@ def _draft_case(B, d, Vd, k):
 
 
 @pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
-                                      (1, 2560, 32000, 10)])
+                                      (1, 2560, 32000, 10), (2, 16384, 500, 16)])
 def test_draft_topk(B, d, Vd, k):
     Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
     ws = wf.Workspace(1, B, 1, Vd, k)
