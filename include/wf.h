@@ -34,6 +34,13 @@
  *   affected outputs into -1.  The device never traps; read the word with
  *   wf_read_device_error.  Every wait inside a kernel is bounded
  *   (wf_set_wait_timeout_ns); a wait that gives up records WF_ERR_TIMEOUT.
+ * - Stream order: a call reads its per-call inputs (hidden states, drafts,
+ *   parents, offsets, rows, backlog) only after everything enqueued before it
+ *   on `stream` has finished.  Model state — weight matrices, biases, gains,
+ *   the draft-to-target map — may be fetched as soon as a kernel of the call
+ *   starts, which can be while the previous kernel on the stream is still
+ *   running (programmatic dependent launch): do not have work that is still
+ *   in flight on the stream write it.
  * - Workspace: caller-owned device memory of at least wf_workspace_bytes()
  *   bytes, zeroed once with wf_workspace_init() before first use.  Calls
  *   leave it zeroed where that matters, so it can be reused without

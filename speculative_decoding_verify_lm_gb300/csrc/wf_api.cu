@@ -15,7 +15,7 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
-                        void* ws, cudaStream_t s, RoutePick pick);
+                        void* ws, cudaStream_t s, RoutePick pick, bool early_inputs);
 wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s);
@@ -207,7 +207,7 @@ wf_status wf_verify_chain(const int32_t* g, const int32_t* draft, const int32_t*
     WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
     WF_TRY(check_device());
     return launch_verify(g, draft, nullptr, nullptr, 0, pos_off, node_off, B, -1, path ? path_stride : 0,
-                         n_accept, bonus, last_pos, path, ws, stream, RoutePick{});
+                         n_accept, bonus, last_pos, path, ws, stream, RoutePick{}, false);
 }
 
 wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* node_off,
@@ -219,7 +219,7 @@ wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int32_t* pa
     WF_TRY(check_ws(ws, ws_bytes, sizeof(Control)));
     WF_TRY(check_device());
     return launch_verify(g, tok, parent, nullptr, 1, pos_off, node_off, B, -1, path ? path_stride : 0, n_accept,
-                         bonus, last_pos, path, ws, stream, RoutePick{});
+                         bonus, last_pos, path, ws, stream, RoutePick{}, false);
 }
 
 wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, const float* W1,
@@ -329,13 +329,13 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
                                      nullptr, 0, ws, L.ent, stream));
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{dall, a->tau, a->delta_al, a->route}));
+                             RoutePick{dall, a->tau, a->delta_al, a->route}, true));
     } else if (entropy) {
         // many rows: a second sweep over the weights for the B accepted rows only
         WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{}));
+                             RoutePick{}, true));
         uint16_t* gath = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.gath);
         WF_TRY(launch_gather_rows(a->hidden, a->P, a->d, a->last_pos, a->B, gath, ws, stream));
         WF_TRY(launch_lmhead_entropy(gath, a->W, a->B, a->d, a->V, nullptr, nullptr, a->delta_al, a->route, a->tau,
@@ -361,11 +361,11 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
                                  nullptr, ws, L.part, stream));
             WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                                  a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
-                                 stream, RoutePick{dall, a->tau, a->delta_al, a->route}));
+                                 stream, RoutePick{dall, a->tau, a->delta_al, a->route}, true));
         } else {
             WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                                  a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
-                                 stream, RoutePick{}));
+                                 stream, RoutePick{}, true));
             WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
                                  a->delta_al, a->route, ws, L.part, stream));
         }

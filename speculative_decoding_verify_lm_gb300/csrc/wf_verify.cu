@@ -22,7 +22,8 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     verify_kernel(const int32_t* __restrict__ g, const int32_t* __restrict__ tok, const int32_t* __restrict__ parent,
                   const int32_t* __restrict__ kind, int default_kind, const int32_t* __restrict__ pos_off,
                   const int32_t* __restrict__ node_off, int B, int P, int path_stride, int32_t* n_accept,
-                  int32_t* bonus, int32_t* last_pos, int32_t* path, RoutePick pick, Control* ctrl) {
+                  int32_t* bonus, int32_t* last_pos, int32_t* path, RoutePick pick, int early_inputs,
+                  Control* ctrl) {
     __shared__ int16_t s_par[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_anc[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_dist[VERIFY_WARPS][WF_MAX_SEQ_NODES];
@@ -35,8 +36,11 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     const int b = blockIdx.x * VERIFY_WARPS + w;
     const bool live = b < B;
 
-    // ---- inputs the predecessor (the LM head, in a round) does not write:
-    // read while it is still running
+    // ---- inside a round the predecessor is the round's LM head (or the router
+    // beside it), which started only after everything before the round had
+    // finished: the round's own inputs (offsets, drafts, parents) are read
+    // while it is still running.  A call of its own reads them after the wait.
+    if (!early_inputs) pdl_wait();
     int r0 = 0, N = 0, kd = default_kind;
     bool shape_ok = false;
     int tk[NODES_PER_LANE], pa[NODES_PER_LANE];
@@ -56,7 +60,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
             pa[s] = (in && kd != 0 && parent) ? parent[n0 + i] : -1;
         }
     }
-    pdl_wait();   // the target choices g come from the kernel before this one
+    if (early_inputs) pdl_wait();   // the target choices g come from the kernel before this one
     pdl_trigger();
     if (!live) return;
 
@@ -196,11 +200,11 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
-                        void* ws, cudaStream_t s, RoutePick pick) {
+                        void* ws, cudaStream_t s, RoutePick pick, bool early_inputs) {
     if (B == 0) return WF_OK;
     return launch(verify_kernel, dim3(cdiv(B, VERIFY_WARPS)), dim3(VERIFY_WARPS * 32), 0, s, g, tok, parent, kind,
                   default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path, pick,
-                  reinterpret_cast<Control*>(ws));
+                  (int)early_inputs, reinterpret_cast<Control*>(ws));
 }
 
 }  // namespace wf

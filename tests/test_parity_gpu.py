@@ -413,6 +413,33 @@ def test_build_tree(B, D, k, N):
     assert ws.device_error() == (0, 0)
 
 
+def test_verify_right_after_tree_construction():
+    """A verify call enqueued straight after the call that builds its tree (same
+    stream, no synchronisation in between) sees the built parents and tokens:
+    a call on its own reads its inputs only after the work before it."""
+    B, D, k, N = 6, 6, 4, 40
+    rng = np.random.default_rng(5)
+    tid = rng.integers(0, 4, (B, D, k, k)).astype(np.int32)    # a tiny alphabet: many matches
+    lp = np.log(rng.dirichlet(np.ones(k) * 0.7, (B, D, k))).astype(np.float32)
+    lp[lp < -60] = -60.0
+    rpar, rtok, _, _, rc = o().build_tree(tid, lp, N)
+    assert rc == 0
+    node_off = (np.arange(B + 1) * N).astype(np.int32)
+    pos_off = (np.arange(B + 1) * (N + 1)).astype(np.int32)
+    g = rng.integers(0, 4, B * (N + 1)).astype(np.int32)
+    ref = o().verify_tree(g, rtok.ravel(), rpar.ravel(), node_off, pos_off, 8)
+    assert ref[4] == 0 and ref[0].max() >= 2
+    ws = wf.Workspace(B * (N + 1), B)
+    g_d, no_d, po_d = dev(g), dev(node_off), dev(pos_off)
+    for _ in range(3):
+        parent, token, _, _ = wf.wf_build_tree(dev(tid), dev(lp), N, ws)
+        n, bo, la, pa = wf.wf_verify_tree(g_d, token.view(-1), parent.view(-1), no_d, po_d, ws, path_stride=8)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(n), ref[0]) and np.array_equal(host(bo), ref[1])
+        assert np.array_equal(host(la), ref[2]) and np.array_equal(host(pa), ref[3])
+    assert ws.device_error() == (0, 0)
+
+
 def test_build_tree_bad_logprob():
     tid = np.zeros((2, 2, 2, 2), np.int32)
     lp = np.full((2, 2, 2, 2), -0.5, np.float32)
