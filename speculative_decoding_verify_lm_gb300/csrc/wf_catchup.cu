@@ -16,11 +16,16 @@
 //                    QUERY  rotary embedding, fp32 query of the final token
 //                    OUT    residual: the final token's input plus the product
 //                  One launch covers the key, value and query projections
-//                  (segments of one tile space); a second one Wo.
+//                  (segments of one tile space); with more than 8 sequences
+//                  a second one does Wo.
 //   attend_kernel  the final token's grouped-query attention over the whole
-//                  cache, split along the cache rows across CTAs; the last
-//                  CTA of each (sequence, KV head) merges the splits in a
-//                  fixed order
+//                  cache, split along the cache rows across CTAs; the splits
+//                  of each (sequence, KV head) are merged in a fixed order,
+//                  inside a thread-block cluster when they fit one, else by
+//                  the last CTA to arrive
+//   oproj_gemv_kernel  Wo and the residual for up to 8 sequences: each CTA
+//                  owns 16 output rows with the whole K, its slice of Wo in
+//                  shared memory before the dependency wait (mma.sync)
 //
 // Every wait inside a kernel is bounded (WF_ERR_TIMEOUT, no trap).
 #include <math.h>

@@ -11,11 +11,15 @@
 //              activation slot is only as large as the box and the ring 5-6
 //              stages deep, so more weight bytes are in flight per SM)
 //   warp 1     allocates TMEM (2 x BN fp32 columns = two accumulators) and one
-//              elected lane issues tcgen05.mma (M=128, N=256, K=16) per stage
+//              elected lane issues tcgen05.mma (M=128, N = the tile's weight
+//              rows <= 256, K=16) per stage
 //   warps 2-5  epilogue: tcgen05.ld the finished accumulator (thread = one
 //              activation row, 32 columns per load), keep the running best
 //              (argmax) or a sorted top-k per row, and release the
 //              accumulator so the next tile's MMAs overlap this scan.
+// With one activation tile, each weight matrix is cut into a multiple of the
+// CTA count of tiles of two heights (h and h - 16), so that every CTA sweeps
+// the same weight rows.
 // Argmax rows are combined across CTAs with a 64-bit atomicMax on a packed
 // (order-preserving logit, ~id) key; the last CTA to finish converts the keys
 // to ids and resets them to zero.  Top-k rows write one sorted candidate list
