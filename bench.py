@@ -509,8 +509,8 @@ def main():
     # the round's composition (wf_round): with at most 128 verified rows the
     # router runs beside the LM head and the draft head shares its sweep
     shared = draft and P <= 128 and B <= 128
-    # (shared: both heads, router, acceptance, top-k merge)
-    launches_per_round = 4 if shared else 3 + (2 if draft else 0)
+    # (shared: both heads; router; acceptance with the top-k merge in the same launch)
+    launches_per_round = 3 if shared else 3 + (2 if draft else 0)
 
     # ---- the dominant kernel on its own, CUDA events per launch: the shared
     # sweep of both heads (timed with its top-k merge) or the LM head alone

@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "wf_internal.cuh"
+#include "wf_merge.cuh"
 
 namespace wf {
 
@@ -15,7 +16,7 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
-                        void* ws, cudaStream_t s, RoutePick pick, bool early_inputs);
+                        void* ws, cudaStream_t s, RoutePick pick, bool early_inputs, const MergeArgs* merge = nullptr);
 wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int d, int m, int P, const float* W1,
                         const float* b1, const float* w2, float b2, float tau, float* delta_al, int32_t* route,
                         void* ws, size_t part_off, cudaStream_t s);
@@ -34,8 +35,9 @@ wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
                               size_t cand_off, int* num_n2_out, cudaStream_t s);
-wf_status launch_topk_merge(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
-                            float* vals, void* ws, size_t cand_off, cudaStream_t s);
+MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+                     float* vals, void* ws, size_t cand_off);
+wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
 wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s);
 size_t catchup_workspace_bytes(int B, int N, int din, int H, int G, int D);
 size_t catchup_attend_smem(int H, int G, int D);
@@ -260,7 +262,7 @@ wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P,
     WF_TRY(check_device());
     int num_n2 = 0;
     WF_TRY(launch_lmhead_draft(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, L.cand, &num_n2, stream));
-    return launch_topk_merge(B, Vd, num_n2, k, d2t, draft_ids, tids, vals, ws, L.cand, stream);
+    return launch_topk_merge(merge_args(B, Vd, num_n2, k, d2t, draft_ids, tids, vals, ws, L.cand), ws, stream);
 }
 
 static bool bad_catchup_shape(int B, int N, int din, int H, int G, int D) {
@@ -356,22 +358,25 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
                                        a->Vd, a->k, ws, L.cand, &num_n2, stream));
         else
             WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        // the shared sweep's candidate lists are merged by extra CTAs of the
+        // verification launch, beside the verification
+        const MergeArgs mg = merge_args(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws,
+                                        L.cand);
+        const MergeArgs* mgp = shared ? &mg : nullptr;
         if (beside) {
             WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
                                  nullptr, ws, L.part, stream));
             WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                                  a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
-                                 stream, RoutePick{dall, a->tau, a->delta_al, a->route}, true));
+                                 stream, RoutePick{dall, a->tau, a->delta_al, a->route}, true, mgp));
         } else {
             WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                                  a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
-                                 stream, RoutePick{}, true));
+                                 stream, RoutePick{}, true, mgp));
             WF_TRY(launch_router(a->hidden, a->last_pos, a->B, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau,
                                  a->delta_al, a->route, ws, L.part, stream));
         }
-        if (shared)
-            return launch_topk_merge(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws, L.cand,
-                                     stream);
+        if (shared) return WF_OK;
         if (draft)
             WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals,
                                      ws, L.cand, stream));

@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include "wf_internal.cuh"
+#include "wf_merge.cuh"
 
 namespace wf {
 
@@ -50,6 +51,9 @@ constexpr int GEMM_SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
 constexpr int RING_BUDGET = 210 * 1024;
 constexpr int GEMM_SMEM_MAX = RING_BUDGET + 1024 + 256;
 constexpr int KT_TOPK = WF_MAX_TOPK;
+MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+                     float* vals, void* ws, size_t cand_off);
+wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
 
 struct GemmParams {
     int M_rows;        // activation rows (P or B)
@@ -494,88 +498,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // --------------------------------------------------------------------- top-k merge
-// One CTA per activation row: every thread keeps the KT best of its share of
-// the per-tile candidate lists, then k rounds of a block-wide max pick the
-// winners in order.  Keys are unique per row (each weight row lives in one
-// tile), so exactly one thread owns each winner.
-constexpr int MERGE_THREADS = 128;
-
-__global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const uint64_t* __restrict__ cand, int B,
-                                                                   int num_m, int num_n, int k,
-                                                                   const int32_t* __restrict__ d2t, int Vd,
-                                                                   int32_t* draft_ids, int32_t* tids, float* vals,
-                                                                   Control* ctrl) {
+// One CTA per activation row (wf_merge.cuh).
+__global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const MergeArgs a, Control* ctrl) {
     __shared__ uint64_t wbest[MERGE_THREADS / 32];
     pdl_wait();
     pdl_trigger();
-    const int row = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int m = row / BM, rit = row % BM;
-    uint64_t loc[KT_TOPK];
-#pragma unroll
-    for (int j = 0; j < KT_TOPK; ++j) loc[j] = 0;
-    const int total = num_n * k;
-    constexpr int BATCH = 4;   // candidates in flight per thread
-    for (int base = 0; base < total; base += MERGE_THREADS * BATCH) {
-        uint64_t kb[BATCH];
-        uint64_t* src[BATCH];
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int idx = base + u * MERGE_THREADS + threadIdx.x;
-            const int n = idx / k, j = idx - n * k;
-            src[u] = idx < total ? const_cast<uint64_t*>(cand) + (((size_t)n * num_m + m) * BM + rit) * k + j
-                                 : nullptr;
-            kb[u] = src[u] ? *src[u] : 0ull;
-        }
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u)
-            if (src[u]) *src[u] = 0;  // leave the workspace zeroed
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const uint64_t key = kb[u];
-            if (key > loc[KT_TOPK - 1]) {
-#pragma unroll
-                for (int s = KT_TOPK - 1; s > 0; --s) {
-                    const bool shift = loc[s - 1] < key;
-                    const bool land = !shift && loc[s] < key;
-                    loc[s] = shift ? loc[s - 1] : (land ? key : loc[s]);
-                }
-                if (loc[0] < key) loc[0] = key;
-            }
-        }
-    }
-    for (int j = 0; j < k; ++j) {
-        uint64_t best = loc[0];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
-        }
-        if (lane == 0) wbest[warp] = best;
-        __syncthreads();
-#pragma unroll
-        for (int w = 0; w < MERGE_THREADS / 32; ++w) best = wbest[w] > best ? wbest[w] : best;
-        __syncthreads();   // every thread has read wbest before the next round writes it
-        if (loc[0] == best && best != 0) {  // the (unique) owner pops its head
-#pragma unroll
-            for (int s = 0; s < KT_TOPK - 1; ++s) loc[s] = loc[s + 1];
-            loc[KT_TOPK - 1] = 0;
-        }
-        if (threadIdx.x == 0) {
-            const size_t o = (size_t)row * k + j;
-            int32_t id = -1, tid = -1;
-            float v = __int_as_float(0x7fc00000);
-            if (best != 0) {
-                id = (int32_t)key_id(best);
-                v = key_val(best);
-                tid = (id >= 0 && id < Vd) ? d2t[id] : -1;
-                if (tid < 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)row);
-            }
-            if (draft_ids) draft_ids[o] = id;
-            if (tids) tids[o] = tid;
-            if (vals) vals[o] = v;
-        }
-    }
+    topk_merge_row(a, blockIdx.x, wbest, ctrl);
 }
 
 // --------------------------------------------------------------------- host side
@@ -803,8 +731,7 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     int num_n = 0;
     wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s, &num_n);
     if (st != WF_OK) return st;
-    return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, (const uint64_t*)p.cand, B, cdiv(B, BM),
-                  num_n, k, d2t, Vd, draft_ids, tids, vals, p.ctrl);
+    return launch_topk_merge(merge_args(B, Vd, num_n, k, d2t, draft_ids, tids, vals, ws, cand_off), ws, s);
 }
 
 // Target LM head (argmax over P <= BM rows) and draft head (candidate lists of
@@ -878,13 +805,27 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
                   s, ta, tb, ta2, tb2, tbs, tb2s, p);
 }
 
-// Merge the per-tile candidate lists of B rows (one activation tile) into the
-// top k, mapped through d2t.
-wf_status launch_topk_merge(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
-                            float* vals, void* ws, size_t cand_off, cudaStream_t s) {
-    const uint64_t* cand = reinterpret_cast<const uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
-    return launch(topk_merge_kernel, dim3(B), dim3(MERGE_THREADS), 0, s, cand, B, cdiv(B, BM), num_n, k, d2t,
-                  Vd, draft_ids, tids, vals, reinterpret_cast<Control*>(ws));
+// The merge of the per-tile candidate lists of B rows (num_n weight tiles)
+// into the top k, mapped through d2t.
+MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
+                     float* vals, void* ws, size_t cand_off) {
+    MergeArgs a = {};
+    a.cand = reinterpret_cast<const uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    a.B = B;
+    a.num_m = cdiv(B, BM);
+    a.num_n = num_n;
+    a.k = k;
+    a.d2t = d2t;
+    a.Vd = Vd;
+    a.draft_ids = draft_ids;
+    a.tids = tids;
+    a.vals = vals;
+    return a;
+}
+
+wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s) {
+    if (a.B == 0) return WF_OK;
+    return launch(topk_merge_kernel, dim3(a.B), dim3(MERGE_THREADS), 0, s, a, reinterpret_cast<Control*>(ws));
 }
 
 }  // namespace wf

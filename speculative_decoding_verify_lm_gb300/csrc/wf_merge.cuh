@@ -1,0 +1,102 @@
+// The draft head's top-k merge (EAGLE-3 draft head, "top-k" candidates of
+// the next-token distribution over the draft vocabulary, mapped to target ids
+// through d2t): the per-tile sorted candidate lists of one activation row,
+// merged into its k best.  Used by topk_merge_kernel and, inside a round, by
+// extra CTAs of the verification launch (the merge depends only on the weight
+// sweep, so it runs beside the verification instead of after it).
+#pragma once
+
+#include "wf_internal.cuh"
+
+namespace wf {
+
+constexpr int MERGE_THREADS = 128;
+
+struct MergeArgs {
+    const uint64_t* cand;   // [num_n][num_m * BM][k] packed keys (0 = none), zeroed as read
+    int B, num_m, num_n, k;
+    const int32_t* d2t;     // [Vd] draft id -> target id
+    int Vd;
+    int32_t* draft_ids;     // [B, k] or null
+    int32_t* tids;          // [B, k] or null
+    float* vals;            // [B, k] or null
+};
+
+// One CTA (MERGE_THREADS threads) merges row `row`: every thread keeps the
+// WF_MAX_TOPK best of its share of the candidate lists, then k rounds of a
+// block-wide max pick the winners in order.  Keys are unique per row (each
+// weight row lives in one tile), so exactly one thread owns each winner.
+// wbest: MERGE_THREADS / 32 words of shared memory.
+__device__ __forceinline__ void topk_merge_row(const MergeArgs& a, int row, uint64_t* wbest, Control* ctrl) {
+    constexpr int KT = WF_MAX_TOPK;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int m = row / BM, rit = row % BM;
+    const int k = a.k;
+    uint64_t loc[KT];
+#pragma unroll
+    for (int j = 0; j < KT; ++j) loc[j] = 0;
+    const int total = a.num_n * k;
+    constexpr int BATCH = 4;   // candidates in flight per thread
+    for (int base = 0; base < total; base += MERGE_THREADS * BATCH) {
+        uint64_t kb[BATCH];
+        uint64_t* src[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int idx = base + u * MERGE_THREADS + threadIdx.x;
+            const int n = idx / k, j = idx - n * k;
+            src[u] = idx < total ? const_cast<uint64_t*>(a.cand) + (((size_t)n * a.num_m + m) * BM + rit) * k + j
+                                 : nullptr;
+            kb[u] = src[u] ? *src[u] : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u)
+            if (src[u]) *src[u] = 0;  // leave the workspace zeroed
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const uint64_t key = kb[u];
+            if (key > loc[KT - 1]) {
+#pragma unroll
+                for (int s = KT - 1; s > 0; --s) {
+                    const bool shift = loc[s - 1] < key;
+                    const bool land = !shift && loc[s] < key;
+                    loc[s] = shift ? loc[s - 1] : (land ? key : loc[s]);
+                }
+                if (loc[0] < key) loc[0] = key;
+            }
+        }
+    }
+    for (int j = 0; j < k; ++j) {
+        uint64_t best = loc[0];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
+        }
+        if (lane == 0) wbest[warp] = best;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < MERGE_THREADS / 32; ++w) best = wbest[w] > best ? wbest[w] : best;
+        __syncthreads();   // every thread has read wbest before the next round writes it
+        if (loc[0] == best && best != 0) {  // the (unique) owner pops its head
+#pragma unroll
+            for (int s = 0; s < KT - 1; ++s) loc[s] = loc[s + 1];
+            loc[KT - 1] = 0;
+        }
+        if (threadIdx.x == 0) {
+            const size_t o = (size_t)row * k + j;
+            int32_t id = -1, tid = -1;
+            float v = __int_as_float(0x7fc00000);
+            if (best != 0) {
+                id = (int32_t)key_id(best);
+                v = key_val(best);
+                tid = (id >= 0 && id < a.Vd) ? a.d2t[id] : -1;
+                if (tid < 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)row);
+            }
+            if (a.draft_ids) a.draft_ids[o] = id;
+            if (a.tids) a.tids[o] = tid;
+            if (a.vals) a.vals[o] = v;
+        }
+    }
+}
+
+}  // namespace wf

@@ -12,6 +12,7 @@
 // path and its depth; the deepest accepted node (lowest index on a tie) wins
 // a warp max over packed (depth, ~index) keys.
 #include "wf_internal.cuh"
+#include "wf_merge.cuh"
 
 namespace wf {
 
@@ -23,13 +24,22 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
                   const int32_t* __restrict__ kind, int default_kind, const int32_t* __restrict__ pos_off,
                   const int32_t* __restrict__ node_off, int B, int P, int path_stride, int32_t* n_accept,
                   int32_t* bonus, int32_t* last_pos, int32_t* path, RoutePick pick, int early_inputs,
-                  Control* ctrl) {
+                  MergeArgs mg, int nverify, Control* ctrl) {
     __shared__ int16_t s_par[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_anc[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int16_t s_dist[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ uint8_t s_ok[VERIFY_WARPS][WF_MAX_SEQ_NODES];
     __shared__ int32_t s_g[VERIFY_WARPS][WF_MAX_SEQ_NODES + 1];
 
+    // CTAs past the verification ones merge the draft head's candidate lists
+    // (one row each): they depend on the weight sweep only, like verification
+    if ((int)blockIdx.x >= nverify) {
+        __shared__ uint64_t s_wbest[MERGE_THREADS / 32];
+        pdl_wait();
+        pdl_trigger();
+        topk_merge_row(mg, (int)blockIdx.x - nverify, s_wbest, ctrl);
+        return;
+    }
     const unsigned FULL = 0xffffffffu;
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -200,11 +210,14 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
-                        void* ws, cudaStream_t s, RoutePick pick, bool early_inputs) {
-    if (B == 0) return WF_OK;
-    return launch(verify_kernel, dim3(cdiv(B, VERIFY_WARPS)), dim3(VERIFY_WARPS * 32), 0, s, g, tok, parent, kind,
+                        void* ws, cudaStream_t s, RoutePick pick, bool early_inputs, const MergeArgs* merge) {
+    static_assert(MERGE_THREADS == VERIFY_WARPS * 32, "merge CTAs share the verification launch's block size");
+    const int nverify = cdiv(B, VERIFY_WARPS);
+    const int nmerge = merge ? merge->B : 0;
+    if (nverify + nmerge == 0) return WF_OK;
+    return launch(verify_kernel, dim3(nverify + nmerge), dim3(VERIFY_WARPS * 32), 0, s, g, tok, parent, kind,
                   default_kind, pos_off, node_off, B, P, path_stride, n_accept, bonus, last_pos, path, pick,
-                  (int)early_inputs, reinterpret_cast<Control*>(ws));
+                  (int)early_inputs, merge ? *merge : MergeArgs{}, nverify, reinterpret_cast<Control*>(ws));
 }
 
 }  // namespace wf
