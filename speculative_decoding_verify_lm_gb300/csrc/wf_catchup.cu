@@ -30,6 +30,8 @@
 // Every wait inside a kernel is bounded (WF_ERR_TIMEOUT, no trap).
 #include <math.h>
 
+#include <mutex>
+
 #include "wf_internal.cuh"
 
 #define CU_TRY(x)                      \
@@ -1278,7 +1280,8 @@ static bool act_map(CUtensorMap* m, const void* base, int rows, int cols) {
 size_t catchup_attend_smem(int H, int G, int D);
 
 // How many clusters of `size` attention CTAs with `smem` bytes each can be
-// resident at once (one query per device, size and shared-memory size).
+// resident at once (one query per device, size and shared-memory size; the
+// cache is shared by host threads).
 static int attend_resident_clusters(int dev, int size, size_t smem) {
     struct Entry {
         int dev, size;
@@ -1287,6 +1290,8 @@ static int attend_resident_clusters(int dev, int size, size_t smem) {
     };
     static Entry seen[64];
     static int nseen = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < nseen; ++i)
         if (seen[i].dev == dev && seen[i].size == size && seen[i].smem == smem) return seen[i].n;
     cudaLaunchConfig_t cfg = {};
