@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, help="workload index 0-4 (default 1: DFlash chain, batch 1)")
     ap.add_argument("--router-width", type=int, default=None, help="override m (the paper's m = d/8 = 320)")
+    ap.add_argument("--router", choices=["neural", "entropy"], default="neural",
+                    help="the round's routing policy: the neural router (default) or WhiFlash-Entropy")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct wf_round calls instead of a CUDA graph")
@@ -196,7 +198,17 @@ def traffic_for(kernel: str, workload: str):
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
-def cpu_sample(wl, budget_s: float):
+def oracle_round(o, sub, entropy: bool):
+    """One oracle round: LM-head argmax, acceptance and the neural router, or
+    with entropy routing also the entropy of the target distribution at each
+    sequence's accepted row."""
+    out = o.round_(*sub)
+    if entropy:
+        o.entropy(sub[0], out["last_pos"], sub[1], sub[11])
+    return out
+
+
+def cpu_sample(wl, budget_s: float, entropy: bool = False):
     """Time the oracle round on a bounded sample of the workload; returns (positions/s, sample text, cores)."""
     import oracle
     o = oracle.default()
@@ -211,12 +223,12 @@ def cpu_sample(wl, budget_s: float):
             break
     sub = _subset(wl, seqs)
     t0 = time.perf_counter()
-    o.round_(*sub)
+    oracle_round(o, sub, entropy)
     t_probe = time.perf_counter() - t0
     reps = max(1, int(budget_s / max(t_probe, 1e-6)))
     t0 = time.perf_counter()
     for _ in range(reps):
-        o.round_(*sub)
+        oracle_round(o, sub, entropy)
     dt = time.perf_counter() - t0
     P_sub = int(sub[2][-1])
     return P_sub * reps / dt, f"{reps} oracle rounds over {len(seqs)} of {B} sequences ({P_sub} verified rows each)", \
@@ -237,15 +249,16 @@ def run_reference(args, cfg_name, wl):
     """--impl reference: the CPU oracle, as it stands, on the host cores."""
     import oracle
     o = oracle.default()
+    entropy = args.router == "entropy"
     per_step_budget = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
-    value, sample, cores, t_round, P_sub = cpu_sample(wl, per_step_budget)
+    value, sample, cores, t_round, P_sub = cpu_sample(wl, per_step_budget, entropy)
     sub = _subset(wl, list(range(min(wl.B, 1))))
     for _ in range(args.warmup):
-        o.round_(*sub)
+        oracle_round(o, sub, entropy)
     t0 = time.perf_counter()
     acc = 0
     for _ in range(args.steps):
-        out = o.round_(*sub)
+        out = oracle_round(o, sub, entropy)
         acc += int((out["n_accept"] + 1).sum())
     dt = time.perf_counter() - t0
     P1 = int(sub[2][-1])
@@ -415,6 +428,9 @@ def main():
     from speculative_decoding_verify_lm_gb300 import synth
     cfg = synth.CONFIGS[args.config]
     cfg_name = cfg.name if args.router_width is None else f"{cfg.name}_m{args.router_width}"
+    entropy = args.router == "entropy"
+    if entropy:
+        cfg_name += "_entropy"
 
     if args.impl == "reference":
         if rank == 0:
@@ -450,7 +466,7 @@ def main():
     r = wf.Round(t(wl.hidden), Wdev, t(wl.pos_off), t(wl.node_off), t(wl.tok), t(wl.W1), t(wl.b1), t(wl.w2),
                  wl.b2, wl.tau, kind=t(wl.kind), parent=t(wl.parent), path_stride=wl.max_depth,
                  x=t(wl.x) if draft else None, Wd=t(wl.Wd) if draft else None, d2t=t(wl.d2t) if draft else None,
-                 k=wl.topk if draft else 0)
+                 k=wl.topk if draft else 0, router_kind=wf.WF_ROUTER_ENTROPY if entropy else wf.WF_ROUTER_NEURAL)
     P, B, d, V = wl.P, wl.B, cfg.d, cfg.V
     weight_bytes = V * d * 2 + (wl.Wd.nbytes if draft else 0) + wl.W1.nbytes
     flush = weight_bytes < 2 * L2_BYTES
@@ -508,9 +524,15 @@ def main():
     value = tot_rows / max_s
     # the round's composition (wf_round): with at most 128 verified rows the
     # router runs beside the LM head and the draft head shares its sweep
-    shared = draft and P <= 128 and B <= 128
+    shared = draft and P <= 128 and B <= 128 and not entropy
     # (shared: both heads; router; acceptance with the top-k merge in the same launch)
     launches_per_round = 3 if shared else 3 + (2 if draft else 0)
+    # entropy routing: the LM-head sweep with the entropy statistics, then
+    # acceptance; with more rows, the LM head, acceptance, the gather of the
+    # accepted rows and a second sweep for their entropy (draft head after)
+    ent_fused = entropy and P <= 128
+    if entropy:
+        launches_per_round = (2 if ent_fused else 4) + (2 if draft else 0)
 
     # ---- the dominant kernel on its own, CUDA events per launch: the shared
     # sweep of both heads (timed with its top-k merge) or the LM head alone
@@ -530,6 +552,14 @@ def main():
         alg_bytes = (V + Vd) * d * 2 + (P + B) * d * 2 + Vd * 4 + P * 4 + B * k * 12
         alg_flops = 2.0 * d * (P * V + B * Vd)
         kernel_name = "gemm_select_kernel<1,1,0,1>"
+    elif ent_fused:
+        ws1 = wf.Workspace(P, P, d=d, device=device)
+        Hbuf = torch.empty(P, dtype=torch.float32, device=device)
+        rbuf = torch.empty(P, dtype=torch.int32, device=device)
+        kernel_call = lambda: wf.wf_lmhead_entropy(hdev, Wdev, wl.tau, ws1, H=Hbuf, route=rbuf)  # noqa: E731
+        alg_bytes = V * d * 2 + P * d * 2 + P * 8
+        alg_flops = 2.0 * P * V * d
+        kernel_name = "gemm_select_kernel<1,1,1>"
     else:
         ws1 = wf.Workspace(P, device=device)
         kernel_call = lambda: wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)  # noqa: E731
@@ -607,13 +637,14 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        v, sample, cores, _, _ = cpu_sample(wl, args.cpu_seconds)
+        v, sample, cores, _, _ = cpu_sample(wl, args.cpu_seconds, entropy)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": sum(step_ms) / len(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg_name, "P": P, "B": B, "d": d, "V": V, "router_m": int(wl.W1.shape[0]),
+        "config": {"workload": cfg_name, "P": P, "B": B, "d": d, "V": V,
+                   "router": "entropy" if entropy else f"neural, m = {int(wl.W1.shape[0])}",
                    "draft_head": f"{cfg.Vd}x{d} top-{wl.topk}" if draft else None,
                    "l2": "flushed between steps (working set < 2x L2)" if flush
                    else f"inputs larger than L2 (weights {weight_bytes / 1e6:.0f} MB streamed per step)",
