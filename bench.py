@@ -531,8 +531,9 @@ def main():
     # acceptance; with more rows, the LM head, acceptance, the gather of the
     # accepted rows and a second sweep for their entropy (draft head after)
     ent_fused = entropy and P <= 128
-    if entropy:
-        launches_per_round = (2 if ent_fused else 4) + (2 if draft else 0)
+    if entropy:   # with one activation tile per head the draft head shares the entropy sweep
+        ent_shared = ent_fused and draft and B <= 128
+        launches_per_round = 2 if ent_shared else (2 if ent_fused else 4) + (2 if draft else 0)
 
     # ---- the dominant kernel on its own, CUDA events per launch: the shared
     # sweep of both heads (timed with its top-k merge) or the LM head alone

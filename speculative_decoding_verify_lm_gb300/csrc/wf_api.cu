@@ -34,7 +34,8 @@ wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t
                              void* ws, cudaStream_t s);
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
-                              size_t cand_off, int* num_n2_out, cudaStream_t s);
+                              size_t cand_off, int* num_n2_out, cudaStream_t s, float* H = nullptr,
+                              float tau = 0.f, size_t ent_off = 0);
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                      float* vals, void* ws, size_t cand_off);
 wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
@@ -326,12 +327,23 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
     float* dall = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.dall);
     if (entropy && a->P <= ROUTE_ALL_ROWS_MAX) {
         // WhiFlash-Entropy, few rows: the LM-head sweep also yields the entropy
-        // of every row; acceptance picks the accepted row's
-        WF_TRY(launch_lmhead_entropy(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, dall, nullptr, a->tau,
-                                     nullptr, 0, ws, L.ent, stream));
+        // of every row; acceptance picks the accepted row's.  With one
+        // activation tile per head the draft head shares that sweep and its
+        // top-k merge runs in the verification launch.
+        const bool shared = draft && a->P <= BM && a->B <= BM;
+        int num_n2 = 0;
+        if (shared)
+            WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
+                                       a->Vd, a->k, ws, L.cand, &num_n2, stream, dall, a->tau, L.ent));
+        else
+            WF_TRY(launch_lmhead_entropy(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, dall, nullptr,
+                                         a->tau, nullptr, 0, ws, L.ent, stream));
+        const MergeArgs mg = merge_args(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws,
+                                        L.cand);
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{dall, a->tau, a->delta_al, a->route}, true));
+                             RoutePick{dall, a->tau, a->delta_al, a->route}, true, shared ? &mg : nullptr));
+        if (shared) return WF_OK;
     } else if (entropy) {
         // many rows: a second sweep over the weights for the B accepted rows only
         WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));

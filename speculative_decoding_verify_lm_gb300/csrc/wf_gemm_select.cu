@@ -244,15 +244,16 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
 // logits so that the entropy of the next-token distribution comes out of the
 // same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
 // activation tiles).
-// DUAL (with KT = 1, CL = 1, no ENT): tiles U0.. are the second problem's
-// (activation map tmA2, weight map tmB2, top-k into p.cand).
+// DUAL (with KT = 1, CL = 1): tiles U0.. are the second problem's
+// (activation map tmA2, weight map tmB2, top-k into p.cand); with ENT the
+// first problem's tiles also feed the entropy statistics.
 template <int KT, int CL, bool ENT, bool DUAL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB2s,
                        const GemmParams p) {
-    static_assert(!DUAL || (KT == 1 && CL == 1 && !ENT), "the dual sweep pairs an argmax head with a top-k head");
+    static_assert(!DUAL || (KT == 1 && CL == 1), "the dual sweep pairs an argmax head with a top-k head");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
@@ -762,13 +763,16 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
 // count this returns in *num_n2_out.
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
-                              size_t cand_off, int* num_n2_out, cudaStream_t s) {
+                              size_t cand_off, int* num_n2_out, cudaStream_t s, float* H, float tau,
+                              size_t ent_off) {
     if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
     static bool attr_set[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
     if (dev < 64 && !attr_set[dev]) {
         if (cudaFuncSetAttribute(gemm_select_kernel<1, 1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GEMM_SMEM_MAX) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_select_kernel<1, 1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GEMM_SMEM_MAX) != cudaSuccess)
             return WF_ERR_CUDA;
         attr_set[dev] = true;
@@ -823,8 +827,20 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     const int tiles = p.num_n + p.num_n2;
     *num_n2_out = p.num_n2;
     const int smem = set_ring(p, a_rows > a_rows2 ? a_rows : a_rows2);
-    return launch(gemm_select_kernel<1, 1, false, true>, dim3(tiles < sms ? tiles : sms), dim3(GEMM_THREADS), smem,
-                  s, ta, tb, ta2, tb2, tbs, tb2s, p);
+    int grid = tiles < sms ? tiles : sms;
+    if (H) {   // the target head's entropy statistics as well (WhiFlash-Entropy)
+        p.ent = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(ws) + ent_off);
+        p.H = H;
+        p.route = nullptr;
+        p.tau = tau;
+        p.src_rows = nullptr;
+        p.src_P = 0;
+        if (grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
+        return launch(gemm_select_kernel<1, 1, true, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2,
+                      tb2, tbs, tb2s, p);
+    }
+    return launch(gemm_select_kernel<1, 1, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2, tb2,
+                  tbs, tb2s, p);
 }
 
 // The merge of the per-tile candidate lists of B rows (num_n weight tiles)

@@ -360,15 +360,34 @@ def test_round_entropy_router(kinds):
     <= 128 rows, a second sweep over the accepted rows otherwise."""
     wl = synth.small_workload(77 + len(kinds), d=128, V=3000, kinds=kinds, argmax_fn=oracle.argmax_fn, m=8,
                               n_nodes=60, depth=8, branch=10)
+    assert (wl.P <= 128) == (len(kinds) == 2)   # both paths: the fused sweep and the second sweep
+    _check_entropy_round(wl)
+
+
+def test_round_entropy_router_with_draft_head():
+    """The same with a draft head: its top-k shares the LM head's sweep (which
+    also gathers the entropy statistics) and is merged in the verification
+    launch."""
+    wl = synth.small_workload(91, d=128, V=3000, kinds=[1, 0], argmax_fn=oracle.argmax_fn, m=8, n_nodes=60,
+                              depth=8, branch=10, Vd=700, topk=10, topk_gap_fn=oracle.topk_gap_fn)
+    out = _check_entropy_round(wl)
+    dids, tids, _, _, _ = o().draft_topk(wl.x, wl.Wd, wl.d2t, wl.topk)
+    assert np.array_equal(out["draft_ids"], dids) and np.array_equal(out["tids"], tids)
+
+
+def _check_entropy_round(wl):
     rr = wl.pos_off[1:]
     ref = o().round_(wl.hidden, wl.W, wl.pos_off, wl.node_off, wl.kind, wl.tok, wl.parent, wl.W1, wl.b1, wl.w2,
                      wl.b2, wl.tau, wl.max_depth)
     H_ref, _ = o().entropy(wl.hidden, ref["last_pos"], wl.W)
     tau = float(np.median(H_ref)) + 0.0041
+    draft = wl.Wd is not None
     r = wf.Round(dev(wl.hidden), dev(wl.W), dev(wl.pos_off), dev(wl.node_off), dev(wl.tok), dev(wl.W1),
                  dev(wl.b1), dev(wl.w2), wl.b2, tau, kind=dev(wl.kind), parent=dev(wl.parent),
-                 path_stride=wl.max_depth, router_kind=wf.WF_ROUTER_ENTROPY)
-    assert (wl.P <= 128) == (len(kinds) == 2) and rr[-1] == wl.P
+                 path_stride=wl.max_depth, router_kind=wf.WF_ROUTER_ENTROPY, x=dev(wl.x) if draft else None,
+                 Wd=dev(wl.Wd) if draft else None, d2t=dev(wl.d2t) if draft else None,
+                 k=wl.topk if draft else 0)
+    assert rr[-1] == wl.P
     for _ in range(2):
         out = {k: host(v) for k, v in r().items()}
         torch.cuda.synchronize()
@@ -378,6 +397,7 @@ def test_round_entropy_router(kinds):
         clear = np.abs(H_ref - tau) >= synth.GAP_MIN
         assert np.array_equal(out["route"][clear], (H_ref > tau).astype(np.int32)[clear])
     assert r.ws.device_error() == (0, 0)
+    return out
 
 
 # ------------------------------------------------------------------ kept rows
