@@ -46,6 +46,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct wf_round calls instead of a CUDA graph")
+    ap.add_argument("--op", choices=["build_tree", "kept_rows"], default=None,
+                    help="time one of the round's side steps instead of a round: the EAGLE-3 draft-tree "
+                         "construction or the kept rows of the accepted paths")
+    ap.add_argument("--op-batch", type=int, default=1, help="sequences per --op call")
     ap.add_argument("--catchup", type=int, default=None,
                     help="time the drafter's KV-only catch-up on this workload (index 0-3) instead of a round")
     return ap.parse_args()
@@ -414,10 +418,228 @@ def run_catchup(args, rank, local, pg):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- side steps of a round
+def op_inputs(op: str, B: int):
+    """Seeded inputs of one --op call at the pages' tree shape (depth 8, top-10,
+    60 draft nodes): per-step top-k children for tree construction; accepted
+    paths of random 60-node trees and the rows' hidden states (d = 2560) for
+    the kept rows.  Host-side structure only (no arithmetic of the method)."""
+    from speculative_decoding_verify_lm_gb300 import synth
+    rng = np.random.default_rng(20261202 + 3000 + (0 if op == "build_tree" else 1))
+    if op == "build_tree":
+        D, k, N = 8, 10, 60
+        tid = rng.integers(0, 32000, (B, D, k, k)).astype(np.int32)
+        lp = np.log(rng.dirichlet(np.ones(k) * 0.7, (B, D, k))).astype(np.float32)
+        lp[lp < -60] = -60.0
+        return dict(tid=tid, lp=lp, N=N)
+    n_nodes, depth, d = 60, 8, 2560
+    n = np.zeros(B, np.int32)
+    path = np.full((B, depth), -1, np.int32)
+    for b in range(B):
+        parent, node_depth = synth.random_tree(rng, n_nodes, depth, 10)
+        acc = int(rng.integers(0, depth + 1))
+        n[b] = acc
+        if acc:
+            node = int(rng.choice(np.nonzero(node_depth == acc)[0]))
+            chain = []
+            while node >= 0:
+                chain.append(node)
+                node = int(parent[node])
+            path[b, :acc] = chain[::-1]
+    pos_off = (np.arange(B + 1) * (n_nodes + 1)).astype(np.int32)
+    hidden = synth.normal_bf16(20261202 + 3001, 1, B * (n_nodes + 1), d, 1.0)
+    return dict(n=n, path=path, pos_off=pos_off, hidden=hidden)
+
+
+def op_oracle(op: str, x: dict):
+    import oracle
+    o = oracle.default()
+    if op == "build_tree":
+        return o.build_tree(x["tid"], x["lp"], x["N"])
+    rows, off = o.accepted_rows(x["n"], x["path"], x["pos_off"])
+    kept = np.concatenate([rows[b][:x["n"][b] + 1] for b in range(len(x["n"]))])
+    return rows, off, x["hidden"][kept]
+
+
+def op_names(op: str, B: int):
+    if op == "build_tree":
+        return (f"eagle3_tree_build_b{B}_d8_k10_n60", "EAGLE-3 draft-tree construction: trees built per second",
+                "trees/s")
+    return (f"kept_rows_b{B}_n60_d2560", "kept rows of the accepted paths: committed rows gathered per second",
+            "rows/s")
+
+
+def run_op_reference(args):
+    """The oracle's side step on the host cores (the reference arm of --op)."""
+    import oracle
+    x = op_inputs(args.op, args.op_batch)
+    name, metric, unit = op_names(args.op, args.op_batch)
+    units = args.op_batch if args.op == "build_tree" else int(np.sum(x["n"] + 1))
+    for _ in range(args.warmup):
+        op_oracle(args.op, x)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        op_oracle(args.op, x)
+    dt = time.perf_counter() - t0
+    val = units * args.steps / dt
+    print(json.dumps({"impl": "reference", "metric": metric, "value": val, "unit": unit, "n_gpus": args.gpus,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic", "config": {"workload": name},
+                      "cpu_baseline": {"value": val, "unit": unit, "cores": oracle.threads(), "kind": "oracle",
+                                       "sample": "whole oracle calls of this workload"},
+                      "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+          flush=True)
+
+
+def run_op(args, rank, local, pg):
+    import torch
+    from speculative_decoding_verify_lm_gb300 import wf
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    B = args.op_batch
+    x = op_inputs(args.op, B)
+    name, metric, unit = op_names(args.op, B)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16  # noqa: E731
+                                   else np.ascontiguousarray(a)).to(device)
+    stream = torch.cuda.current_stream(device)
+    ws = wf.Workspace(1, device=device)
+    if args.op == "build_tree":
+        N = x["N"]
+        ins = [t(x["tid"]), t(x["lp"])]
+        outs = [torch.empty((B, N), dtype=torch.int32, device=device), torch.empty((B, N), dtype=torch.int32,
+                device=device), torch.empty((B, N), dtype=torch.float32, device=device),
+                torch.empty((B, N), dtype=torch.int32, device=device)]
+        D, k = x["tid"].shape[1], x["tid"].shape[2]
+
+        def call():
+            st = wf.lib().wf_build_tree(ins[0].data_ptr(), ins[1].data_ptr(), B, D, k, N,
+                                        *(o_.data_ptr() for o_ in outs), ws.ptr, ws.nbytes, stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"wf_build_tree: status {st}")
+        units = B
+        nbytes = sum(a.numel() * a.element_size() for a in ins + outs)
+        launches = 1
+    else:
+        d = x["hidden"].shape[1]
+        total = int(np.sum(x["n"] + 1))
+        ins = [t(x["n"]), t(x["path"]), t(x["pos_off"]), t(x["hidden"])]
+        ps = x["path"].shape[1]
+        outs = [torch.empty((B, ps + 1), dtype=torch.int32, device=device),
+                torch.empty(B + 1, dtype=torch.int32, device=device),
+                torch.empty((total, d), dtype=torch.int16, device=device)]
+
+        def call():
+            st = wf.lib().wf_accepted_rows(ins[0].data_ptr(), ins[1].data_ptr(), ps, ins[2].data_ptr(), B,
+                                           outs[0].data_ptr(), outs[1].data_ptr(), ins[3].data_ptr(), d,
+                                           outs[2].data_ptr(), stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"wf_accepted_rows: status {st}")
+        units = total
+        # the kept rows' hidden states are read and written once; the rest is small
+        nbytes = 2 * total * d * 2 + sum(a.numel() * a.element_size() for a in ins[:3] + outs[:2])
+        launches = 2
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(device)
+    ref = op_oracle(args.op, x)   # the timed outputs are the oracle's
+    got = [o_.cpu().numpy() for o_ in outs]
+    if args.op == "build_tree":
+        ok = all(np.array_equal(a, e) for a, e in zip(got, ref[:4]))
+    else:
+        ok = np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1]) and \
+            np.array_equal(got[2].view(np.uint16), ref[2])
+    if not ok:
+        raise RuntimeError(f"--op {args.op}: outputs disagree with the oracle")
+    step = call
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        step = g.replay
+        step()
+    torch.cuda.synchronize(device)
+    l2buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        l2buf.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    sampler.wait(ev[-1][1])
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    ms_mean = statistics.mean(ms)
+    hbm_peak, _, peak_src = measured_peaks()
+    achieved = nbytes / (ms_mean / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "traffic": None, "kernel": "build_tree_kernel" if args.op == "build_tree"
+            else "accepted_rows_kernel + gather_kept_kernel",
+            "algorithmic_per_launch": nbytes, "launch_ms": ms_mean, "peak_source": f"{peak_src} (hbm_gbs, burst)"}
+    # end to end: the inputs in from pinned host memory, every output back
+    h_in = [torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for a in ins]
+    for h_, a in zip(h_in, ins):
+        h_.copy_(a)
+    h_out = [torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for a in outs]
+    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def host_step():
+        for a, h_ in zip(ins, h_in):
+            a.copy_(h_, non_blocking=True)
+        step()
+        for h_, a in zip(h_out, outs):
+            h_.copy_(a, non_blocking=True)
+    host_step()
+    torch.cuda.synchronize(device)
+    e2e_ev[0].record(stream)
+    for _ in range(args.steps):
+        host_step()
+    e2e_ev[1].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_s = e2e_ev[0].elapsed_time(e2e_ev[1]) / 1e3
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        import oracle
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 10.0) or reps == 0:
+            op_oracle(args.op, x)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": units * reps / dt, "unit": unit, "cores": oracle.threads(), "kind": "oracle",
+               "sample": f"{reps} whole oracle call(s) of this workload"}
+    line = {"metric": metric, "value": units * args.steps / (sum(ms) / 1e3), "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_mean, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32" if args.op == "build_tree" else "bf16",
+            "data": "synthetic",
+            "config": {"workload": name, "B": B, "l2": "L2 flushed (256 MB write) before every call",
+                       "launch": "captured in a CUDA graph" if not args.no_graph else "direct calls"},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": units * args.steps / e2e_s, "unit": unit,
+                    "h2d_bytes_per_step": int(sum(a.numel() * a.element_size() for a in ins)),
+                    "d2h_bytes_per_step": int(sum(a.numel() * a.element_size() for a in outs))},
+            "clocks": clocks, "gpu_launches": launches * args.steps, "impl": "ours"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     args = parse()
     world, rank, local, pg = dist_setup(args)
+    if args.op is not None:
+        if args.impl == "reference":
+            if rank == 0:
+                run_op_reference(args)
+            return
+        run_op(args, rank, local, pg)
+        return
     if args.catchup is not None:
         if args.impl == "reference":
             if rank == 0:
