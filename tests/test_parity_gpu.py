@@ -260,6 +260,30 @@ def test_round_batch1_configs(index):
         assert np.array_equal(out2[key], out[key])
 
 
+def test_round_entropy_tree_b1_full_size():
+    """The EAGLE-3 tree round at full size (V = 151,936, draft head over 32,000)
+    under WhiFlash-Entropy routing: the entropy statistics ride the shared
+    sweep of both heads on its evened-out tiles."""
+    wl = synth.make_workload(2, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn)
+    ref = o().round_(wl.hidden, wl.W, wl.pos_off, wl.node_off, wl.kind, wl.tok, wl.parent, wl.W1, wl.b1, wl.w2,
+                     wl.b2, wl.tau, wl.max_depth)
+    H_ref, _ = o().entropy(wl.hidden, ref["last_pos"], wl.W)
+    tau = float(H_ref[0]) - 0.05
+    r = wf.Round(dev(wl.hidden), dev(wl.W), dev(wl.pos_off), dev(wl.node_off), dev(wl.tok), dev(wl.W1),
+                 dev(wl.b1), dev(wl.w2), wl.b2, tau, kind=dev(wl.kind), parent=dev(wl.parent),
+                 path_stride=wl.max_depth, x=dev(wl.x), Wd=dev(wl.Wd), d2t=dev(wl.d2t), k=wl.topk,
+                 router_kind=wf.WF_ROUTER_ENTROPY)
+    for _ in range(2):
+        out = {k: host(v) for k, v in r().items()}
+        torch.cuda.synchronize()
+        for key in ("ids", "n_accept", "bonus", "last_pos", "path"):
+            assert np.array_equal(out[key], ref[key]), key
+        assert np.max(np.abs(out["delta_al"] - H_ref)) <= 1e-3 and out["route"][0] == 1
+        dids, tids, _, _, _ = o().draft_topk(wl.x, wl.Wd, wl.d2t, wl.topk)
+        assert np.array_equal(out["draft_ids"], dids) and np.array_equal(out["tids"], tids)
+    assert r.ws.device_error() == (0, 0)
+
+
 def _sampled_round(index, plant):
     wl = synth.make_workload(index, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn, plant_seqs=plant)
     r, out = round_on_gpu(wl)
