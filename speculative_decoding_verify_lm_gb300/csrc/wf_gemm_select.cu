@@ -458,56 +458,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (p.maxlogit) p.maxlogit[r] = key ? key_val(key) : __int_as_float(0x7fc00000);
                     p.keys[r] = 0;
                 }
-                if constexpr (ENT) {
-                    // entropy per row: merge the slots' statistics in a fixed order
-                    // (each lane its slots in increasing order, then a fixed shuffle
-                    // tree), H = log S - T / S.  A warp takes ENT_RB rows at a time
-                    // with every slot load of them in flight before any is used.
-                    static_assert(ENT_MAX_SLOTS % 32 == 0, "slots are shared out evenly over the lanes");
-                    constexpr int SPL = ENT_MAX_SLOTS / 32;   // slots per lane
-                    constexpr int ENT_RB = 4;
-                    const int wid = (threadIdx.x - 64) >> 5;
-                    for (int r0 = wid * ENT_RB; r0 < p.M_rows; r0 += 4 * ENT_RB) {
-                        float4 st[ENT_RB][SPL];
-#pragma unroll
-                        for (int q = 0; q < ENT_RB; ++q)
-#pragma unroll
-                            for (int i = 0; i < SPL; ++i) {
-                                const int r = r0 + q, sl = lane + 32 * i;
-                                st[q][i] = (r < p.M_rows && sl < nslots) ? __ldcg(p.ent + (size_t)sl * p.M_rows + r)
-                                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-#pragma unroll
-                        for (int q = 0; q < ENT_RB; ++q)
-#pragma unroll
-                            for (int i = 0; i < SPL; ++i) {
-                                const int r = r0 + q, sl = lane + 32 * i;
-                                if (r < p.M_rows && sl < nslots)   // leave the workspace zeroed
-                                    p.ent[(size_t)sl * p.M_rows + r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-#pragma unroll
-                        for (int q = 0; q < ENT_RB; ++q) {
-                            const int r = r0 + q;
-                            float M = -INFINITY, S = 0.f, T = 0.f;
-#pragma unroll
-                            for (int i = 0; i < SPL; ++i) ent_merge(M, S, T, st[q][i].x, st[q][i].y, st[q][i].z);
-#pragma unroll
-                            for (int off = 16; off > 0; off >>= 1) {
-                                const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
-                                const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
-                                const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
-                                ent_merge(M, S, T, m2, s2, t2);
-                            }
-                            if (lane == 0 && r < p.M_rows) {
-                                // gathered rows: a source row outside [0, src_P) has no entropy
-                                const bool bad = p.src_rows && (p.src_rows[r] < 0 || p.src_rows[r] >= p.src_P);
-                                const float h = bad ? __int_as_float(0x7fc00000) : logf(S) - T / S;
-                                p.H[r] = h;
-                                if (p.route) p.route[r] = bad ? -1 : (h > p.tau ? 1 : 0);
-                            }
-                        }
-                    }
-                }
                 if (threadIdx.x == 64) p.ctrl->gemm_done = 0;
             }
         }
@@ -515,6 +465,60 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (ENT && KT == 1) {
+        // The last CTA: entropy per row from every CTA's softmax statistics,
+        // merged in a fixed order (each lane its slots in increasing order, then
+        // a fixed shuffle tree), H = log S - T / S.  All of its warps take part,
+        // ENT_RB rows each at a time with every slot load in flight before any
+        // is used.
+        if (*last_flag) {
+            static_assert(ENT_MAX_SLOTS % 32 == 0, "slots are shared out evenly over the lanes");
+            constexpr int SPL = ENT_MAX_SLOTS / 32;   // slots per lane
+            constexpr int ENT_RB = 4;
+            constexpr int NW = GEMM_THREADS / 32;
+            __threadfence();   // after the epilogue warps' arrival count: read every CTA's slots
+            for (int r0 = warp * ENT_RB; r0 < p.M_rows; r0 += NW * ENT_RB) {
+                float4 st[ENT_RB][SPL];
+#pragma unroll
+                for (int q = 0; q < ENT_RB; ++q)
+#pragma unroll
+                    for (int i = 0; i < SPL; ++i) {
+                        const int r = r0 + q, sl = lane + 32 * i;
+                        st[q][i] = (r < p.M_rows && sl < nslots) ? __ldcg(p.ent + (size_t)sl * p.M_rows + r)
+                                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                for (int q = 0; q < ENT_RB; ++q)
+#pragma unroll
+                    for (int i = 0; i < SPL; ++i) {
+                        const int r = r0 + q, sl = lane + 32 * i;
+                        if (r < p.M_rows && sl < nslots)   // leave the workspace zeroed
+                            p.ent[(size_t)sl * p.M_rows + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                for (int q = 0; q < ENT_RB; ++q) {
+                    const int r = r0 + q;
+                    float M = -INFINITY, S = 0.f, T = 0.f;
+#pragma unroll
+                    for (int i = 0; i < SPL; ++i) ent_merge(M, S, T, st[q][i].x, st[q][i].y, st[q][i].z);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+                        const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
+                        const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
+                        ent_merge(M, S, T, m2, s2, t2);
+                    }
+                    if (lane == 0 && r < p.M_rows) {
+                        // gathered rows: a source row outside [0, src_P) has no entropy
+                        const bool bad = p.src_rows && (p.src_rows[r] < 0 || p.src_rows[r] >= p.src_P);
+                        const float h = bad ? __int_as_float(0x7fc00000) : logf(S) - T / S;
+                        p.H[r] = h;
+                        if (p.route) p.route[r] = bad ? -1 : (h > p.tau ? 1 : 0);
+                    }
+                }
+            }
+        }
+    }
     if constexpr (CL == 2) cluster_sync();   // the peer may still arrive on, or copy into, this CTA
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
