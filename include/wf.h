@@ -232,7 +232,8 @@ WF_API wf_status wf_verify_tree(const int32_t* g, const int32_t* tok, const int3
  * and, if hidden_out != NULL, hidden_out[acc_off[b] + j] = hidden[acc_rows[b][j]]
  * (the hidden states the next drafting step conditions on, packed).
  * n_accept, path as returned by wf_verify_* / wf_round with the same
- * path_stride (n_accept[b] <= path_stride); pos_off [B+1]; all device int32.
+ * path_stride (n_accept[b] <= path_stride; a larger value is taken as
+ * path_stride, -1 keeps no row); pos_off [B+1]; all device int32.
  * acc_rows [B, path_stride+1], acc_off [B+1] device int32 out; hidden [*, d],
  * hidden_out [sum(n_accept+1), d] device bf16 bits (both NULL to skip).
  */

@@ -265,7 +265,9 @@ __global__ void __launch_bounds__(1024)
         const int b = b0 + threadIdx.x;
         int cnt = 0;
         if (b < B) {
-            const int n = n_accept[b];
+            // n_accept beyond the path's columns is taken as the columns; -1 (a
+            // sequence with bad data) keeps no row
+            const int n = max(-1, min(n_accept[b], path_stride));
             cnt = n + 1;
             int32_t* out = acc_rows + (size_t)b * (path_stride + 1);
             out[0] = pos_off[b];

@@ -243,33 +243,48 @@ def wf_lmhead_argmax_noalloc(hidden, W, ids=None, maxlogit=None, stream=None):
     return ids
 
 
-def wf_build_tree(tid, lp, N: int, ws: Workspace, stream=None):
-    """EAGLE-3 draft tree from per-step, per-slot top-k children -> (parent, token, score, depth) [B, N]."""
+def wf_build_tree(tid, lp, N: int, ws: Workspace, parent=None, token=None, score=None, depth=None, stream=None):
+    """EAGLE-3 draft tree from per-step, per-slot top-k children -> (parent, token, score, depth) [B, N].
+    Outputs not given are allocated."""
     B, D, k, _ = tid.shape
     dev = tid.device
-    parent = torch.empty((B, N), dtype=torch.int32, device=dev)
-    token = torch.empty((B, N), dtype=torch.int32, device=dev)
-    score = torch.empty((B, N), dtype=torch.float32, device=dev)
-    depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    parent = torch.empty((B, N), dtype=torch.int32, device=dev) if parent is None else parent
+    token = torch.empty((B, N), dtype=torch.int32, device=dev) if token is None else token
+    score = torch.empty((B, N), dtype=torch.float32, device=dev) if score is None else score
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev) if depth is None else depth
+    for name, t_, dt in (("parent", parent, _I32), ("token", token, _I32), ("score", score, _F32),
+                         ("depth", depth, _I32)):
+        if t_.numel() < B * N:
+            raise ValueError(f"{name}: needs {B * N} elements")
+        _check(t_, name, dt)
     st = lib().wf_build_tree(_check(tid, "tid", _I32), _check(lp, "lp", _F32), B, D, k, N, parent.data_ptr(),
                              token.data_ptr(), score.data_ptr(), depth.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
     _raise(st, "wf_build_tree")
     return parent, token, score, depth
 
 
-def wf_accepted_rows(n_accept, path, pos_off, hidden=None, stream=None):
+def wf_accepted_rows(n_accept, path, pos_off, hidden=None, acc_rows=None, acc_off=None, hidden_out=None,
+                     stream=None):
     """Kept rows of each sequence (root + accepted path), their packed offsets and,
-    if ``hidden`` is given, the packed hidden states of those rows."""
+    if ``hidden`` is given, the packed hidden states of those rows.  Outputs not
+    given are allocated; a ``hidden_out`` not given is sized by a host read of
+    n_accept (pass one with room for B * (path stride + 1) rows to stay on the
+    stream, e.g. inside a CUDA graph)."""
     B, ps = path.shape
     dev = n_accept.device
-    acc_rows = torch.empty((B, ps + 1), dtype=torch.int32, device=dev)
-    acc_off = torch.empty(B + 1, dtype=torch.int32, device=dev)
-    out = None
+    acc_rows = torch.empty((B, ps + 1), dtype=torch.int32, device=dev) if acc_rows is None else acc_rows
+    acc_off = torch.empty(B + 1, dtype=torch.int32, device=dev) if acc_off is None else acc_off
+    if acc_rows.numel() < B * (ps + 1) or acc_off.numel() < B + 1:
+        raise ValueError("acc_rows needs B * (path stride + 1) elements and acc_off B + 1")
+    out = hidden_out
     d = 0
     if hidden is not None:
         d = hidden.shape[1]
-        total = int(n_accept.clamp(min=-1).add(1).sum().item())   # host read of the packed size
-        out = torch.empty((max(total, 1), d), dtype=hidden.dtype, device=dev)
+        if out is not None and (out.dim() != 2 or out.shape[1] != d or out.shape[0] < B * (ps + 1)):
+            raise ValueError("hidden_out needs room for B * (path stride + 1) rows of d columns")
+        if out is None:
+            total = int(n_accept.clamp(min=-1).add(1).sum().item())   # host read of the packed size
+            out = torch.empty((max(total, 1), d), dtype=hidden.dtype, device=dev)
     st = lib().wf_accepted_rows(_check(n_accept, "n_accept", _I32), _check(path, "path", _I32), ps,
                                 _check(pos_off, "pos_off", _I32), B, _check(acc_rows, "acc_rows", _I32),
                                 _check(acc_off, "acc_off", _I32), _check(hidden, "hidden", _BF16, True), d,

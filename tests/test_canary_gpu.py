@@ -139,9 +139,7 @@ def test_build_tree_outputs():
             Guarded((B, N), torch.int32)]
     ws = wf.Workspace(1)
     t_tid, t_lp = dev(tid), dev(lp)
-    st = wf.lib().wf_build_tree(t_tid.data_ptr(), t_lp.data_ptr(), B, D, k, N, *(g.t.data_ptr() for g in outs),
-                                ws.ptr, ws.nbytes, wf._stream(None))
-    assert st == 0
+    wf.wf_build_tree(t_tid, t_lp, N, ws, parent=outs[0].t, token=outs[1].t, score=outs[2].t, depth=outs[3].t)
     for g, e in zip(outs, ref[:4]):
         assert np.array_equal(host(g.t), e)
     assert all_intact(*outs)
@@ -155,16 +153,14 @@ def test_accepted_rows_outputs():
     d = 72
     h = synth.normal_bf16(12, 1, int(pos_off[-1]), d, 1.0)
     total = int(np.sum(n + 1))
-    rows_g, off_g, hid_g = Guarded((7, ps + 1), torch.int32), Guarded((8,), torch.int32), Guarded((total, d),
-                                                                                                  torch.int16)
-    t_n, t_path, t_pos, t_h = dev(n), dev(path), dev(pos_off), dev(h)
-    st = wf.lib().wf_accepted_rows(t_n.data_ptr(), t_path.data_ptr(), ps, t_pos.data_ptr(), 7, rows_g.t.data_ptr(),
-                                   off_g.t.data_ptr(), t_h.data_ptr(), d, hid_g.t.data_ptr(),
-                                   wf._stream(None))
-    assert st == 0
+    rows_g, off_g = Guarded((7, ps + 1), torch.int32), Guarded((8,), torch.int32)
+    hid_g = Guarded((7 * (ps + 1), d), torch.int16)   # the bound the binding asks for
+    wf.wf_accepted_rows(dev(n), dev(path), dev(pos_off), hidden=dev(h), acc_rows=rows_g.t, acc_off=off_g.t,
+                        hidden_out=hid_g.t)
     assert np.array_equal(host(rows_g.t), acc_rows) and np.array_equal(host(off_g.t), acc_off)
     kept = np.concatenate([acc_rows[b][:n[b] + 1] for b in range(7)])
-    assert np.array_equal(host(hid_g.t).view(np.uint16), h[kept]) and all_intact(rows_g, off_g, hid_g)
+    assert len(kept) == total
+    assert np.array_equal(host(hid_g.t)[:total].view(np.uint16), h[kept]) and all_intact(rows_g, off_g, hid_g)
 
 
 @pytest.mark.parametrize("n,L,cap", [((3, 1, 5), (2, 0, 9), 16), ((50,), (4000,), 4096)])
@@ -184,3 +180,28 @@ def test_catchup_outputs(n, L, cap):
     assert np.allclose(host(out.t), ref["out"], rtol=0, atol=5e-2) and np.allclose(host(attn.t), ref["attn"], rtol=0,
                                                                                      atol=5e-2)
     assert all_intact(out, attn)
+
+
+def test_accepted_rows_counts_past_the_stride():
+    """Accepted counts beyond the path's columns (outside the documented input
+    range) are taken as the columns and -1 keeps no row: the result equals the
+    oracle's on the clamped counts, and nothing is written past the buffers
+    sized for path_stride + 1 rows a sequence."""
+    g, tok, par, pos_off, node_off, _ = _random_trees(14, 4, 30)
+    ps = 5
+    n_ref, _, _, path_ref, _ = o().verify_tree(g, tok, par, node_off, pos_off, ps)
+    n = np.array([3, 12, -1, 9], np.int32)   # 12 and 9 exceed the 5 path columns
+    path = path_ref.copy()
+    clamped = np.clip(n, -1, ps)
+    acc_rows, acc_off = o().accepted_rows(clamped, path, pos_off)
+    d = 16
+    h = synth.normal_bf16(14, 1, int(pos_off[-1]), d, 1.0)
+    rows_g, off_g = Guarded((4, ps + 1), torch.int32), Guarded((5,), torch.int32)
+    hid_g = Guarded((4 * (ps + 1), d), torch.int16)
+    wf.wf_accepted_rows(dev(n), dev(path), dev(pos_off), hidden=dev(h), acc_rows=rows_g.t, acc_off=off_g.t,
+                        hidden_out=hid_g.t)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(rows_g.t), acc_rows) and np.array_equal(host(off_g.t), acc_off)
+    kept = np.concatenate([acc_rows[b][:clamped[b] + 1] for b in range(4)])
+    assert np.array_equal(host(hid_g.t)[:len(kept)].view(np.uint16), h[kept])
+    assert all_intact(rows_g, off_g, hid_g)
