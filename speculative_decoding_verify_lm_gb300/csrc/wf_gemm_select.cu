@@ -73,7 +73,7 @@ struct GemmParams {
     int32_t* ids;      // argmax: [M_rows] out
     float* maxlogit;   // argmax: [M_rows] out or null
     uint64_t* cand;    // top-k: [tiles][BM][k]
-    float4* ent;       // entropy: [CTA slot][M_rows] running (max, sum e^z, sum z e^z), z = logit - max
+    float4* ent;       // entropy: [M_rows][CTA slots] running (max, sum e^z, sum z e^z), z = logit - max
     float* H;          // entropy: [M_rows] out
     int32_t* route;    // entropy: [M_rows] out (H > tau) or null
     float tau;
@@ -93,20 +93,29 @@ __device__ __forceinline__ void gemm_fail(Control* ctrl, volatile int* abort_fla
     record_error(ctrl, WF_ERR_TIMEOUT, where);
 }
 
-// Merge two partial softmax states (M, S = sum e^(L-M), T = sum (L-M) e^(L-M)).
+// Merge two partial softmax states (M, S = sum e^(L-M), T = sum (L-M) e^(L-M));
+// a state with S = 0 is empty and leaves the other as it is.  Written with
+// selects only, so that the chains of several rows can run interleaved.
 __device__ __forceinline__ void ent_merge(float& M, float& S, float& T, float m2, float s2, float t2) {
-    if (!(s2 > 0.f)) return;
-    if (!(S > 0.f)) {
-        M = m2;
-        S = s2;
-        T = t2;
-        return;
-    }
-    const float mx = fmaxf(M, m2);
-    const float a1 = __expf(M - mx), a2 = __expf(m2 - mx);
-    T = (T + (M - mx) * S) * a1 + (t2 + (m2 - mx) * s2) * a2;
-    S = S * a1 + s2 * a2;
+    const bool h1 = S > 0.f, h2 = s2 > 0.f;
+    const float mx = h1 ? (h2 ? fmaxf(M, m2) : M) : m2;
+    const float d1 = h1 ? M - mx : 0.f, d2 = h2 ? m2 - mx : 0.f;
+    const float a1 = h1 ? __expf(d1) : 0.f, a2 = h2 ? __expf(d2) : 0.f;
+    T = (h1 ? (T + d1 * S) * a1 : 0.f) + (h2 ? (t2 + d2 * s2) * a2 : 0.f);
+    S = (h1 ? S * a1 : 0.f) + (h2 ? s2 * a2 : 0.f);
     M = mx;
+}
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// 2^x by the PTX approximate base-2 exponential (a few ulp of fp32; results
+// below the normal range flush to zero, which only drops terms under 2^-126
+// of the row maximum's).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Insert (v, id) into a descending list of KT entries (earlier entry wins ties).
@@ -154,6 +163,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
                                               volatile int* abort_flag, uint32_t tmem_base, uint32_t tile_i, int q,
                                               int rit, int M_rows, int N_w, int m, int n, const TileSpan sp,
                                               int cand_num_m, float& em, float& es, float& et) {
+    static_assert(!ENT || KT == 1, "the softmax statistics ride on the argmax epilogue");
     const uint32_t acc = tile_i & 1;
     const uint32_t acc_ph = (tile_i >> 1) & 1;
     const bool quad_live = m * BM + q * 32 < M_rows;
@@ -195,23 +205,26 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
                 }
             }
             if constexpr (ENT) {
-                float cmax = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j < lim) cmax = fmaxf(cmax, __uint_as_float(r[j]));
-                if (cmax > em) {   // new running maximum: rescale what was summed so far
+                // tv[0] is the largest column of this tile so far and em the
+                // largest before it, so a new running maximum shows in tv[0].
+                // Sums run in base 2: z = (v - em) log2 e, es = sum 2^z (the
+                // same terms as sum e^(v - em)), et = sum z 2^z (ln 2 times the
+                // natural-log sum; scaled back when published).
+                if (tv[0] > em) {   // new running maximum: rescale what was summed so far
                     if (es > 0.f) {
-                        const float sc = __expf(em - cmax);
-                        et = (et + (em - cmax) * es) * sc;
+                        const float dz = (em - tv[0]) * LOG2E;
+                        const float sc = ex2_approx(dz);
+                        et = (et + dz * es) * sc;
                         es *= sc;
                     }
-                    em = cmax;
+                    em = tv[0];
                 }
+                const float off = em * LOG2E;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (j < lim) {
-                        const float z = __uint_as_float(r[j]) - em;
-                        const float e = __expf(z);
+                        const float z = fmaf(__uint_as_float(r[j]), LOG2E, -off);
+                        const float e = ex2_approx(z);
                         es += e;
                         et = fmaf(z, e, et);
                     }
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if constexpr (ENT) {
             // this CTA's rows are fixed (rank's activation tile); publish their statistics
             const int row = rank * BM + rit;
-            if (row < p.M_rows) p.ent[(size_t)slot * p.M_rows + row] = make_float4(em, es, et, 0.f);
+            if (row < p.M_rows) p.ent[(size_t)row * nslots + slot] = make_float4(em, es, et * LN2, 0.f);
         }
         if (KT == 1 && !*abort_flag) {
             // last CTA to finish turns the keys into ids and zeroes them again
@@ -469,8 +482,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // The last CTA: entropy per row from every CTA's softmax statistics,
         // merged in a fixed order (each lane its slots in increasing order, then
         // a fixed shuffle tree), H = log S - T / S.  All of its warps take part,
-        // ENT_RB rows each at a time with every slot load in flight before any
-        // is used.
+        // ENT_RB rows each at a time: every slot load in flight before any is
+        // used (a row's slots are contiguous, so each load is coalesced), the
+        // rows' merge chains interleaved, and lane q finishing row q.
         if (*last_flag) {
             static_assert(ENT_MAX_SLOTS % 32 == 0, "slots are shared out evenly over the lanes");
             constexpr int SPL = ENT_MAX_SLOTS / 32;   // slots per lane
@@ -478,44 +492,60 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             constexpr int NW = GEMM_THREADS / 32;
             __threadfence();   // after the epilogue warps' arrival count: read every CTA's slots
             for (int r0 = warp * ENT_RB; r0 < p.M_rows; r0 += NW * ENT_RB) {
+                const int rl = r0 + lane;   // the row lane q < ENT_RB finishes
+                // gathered rows: a source row outside [0, src_P) has no entropy
+                const int src = (p.src_rows && lane < ENT_RB && rl < p.M_rows) ? p.src_rows[rl] : 0;
                 float4 st[ENT_RB][SPL];
 #pragma unroll
                 for (int q = 0; q < ENT_RB; ++q)
 #pragma unroll
                     for (int i = 0; i < SPL; ++i) {
                         const int r = r0 + q, sl = lane + 32 * i;
-                        st[q][i] = (r < p.M_rows && sl < nslots) ? __ldcg(p.ent + (size_t)sl * p.M_rows + r)
+                        st[q][i] = (r < p.M_rows && sl < nslots) ? __ldcg(p.ent + (size_t)r * nslots + sl)
                                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
+                float M[ENT_RB], S[ENT_RB], T[ENT_RB];
+#pragma unroll
+                for (int q = 0; q < ENT_RB; ++q) {
+                    M[q] = -INFINITY;
+                    S[q] = 0.f;
+                    T[q] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < SPL; ++i) ent_merge(M[q], S[q], T[q], st[q][i].x, st[q][i].y, st[q][i].z);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int q = 0; q < ENT_RB; ++q) {
+                        const float m2 = __shfl_xor_sync(0xffffffffu, M[q], off);
+                        const float s2 = __shfl_xor_sync(0xffffffffu, S[q], off);
+                        const float t2 = __shfl_xor_sync(0xffffffffu, T[q], off);
+                        ent_merge(M[q], S[q], T[q], m2, s2, t2);
+                    }
+                // every lane holds every row's totals; lane q takes row r0 + q
+                float Sq = S[0], Tq = T[0];
+#pragma unroll
+                for (int q = 1; q < ENT_RB; ++q)
+                    if (lane == q) {
+                        Sq = S[q];
+                        Tq = T[q];
+                    }
+                if (lane < ENT_RB && rl < p.M_rows) {
+                    const bool bad = p.src_rows && (src < 0 || src >= p.src_P);
+                    const float h = bad ? __int_as_float(0x7fc00000) : logf(Sq) - Tq / Sq;
+                    p.H[rl] = h;
+                    if (p.route) p.route[rl] = bad ? -1 : (h > p.tau ? 1 : 0);
+                }
+                // leave the workspace zeroed (after the loads are used: a store
+                // to an address with a load still in flight waits for it)
 #pragma unroll
                 for (int q = 0; q < ENT_RB; ++q)
 #pragma unroll
                     for (int i = 0; i < SPL; ++i) {
                         const int r = r0 + q, sl = lane + 32 * i;
-                        if (r < p.M_rows && sl < nslots)   // leave the workspace zeroed
-                            p.ent[(size_t)sl * p.M_rows + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (r < p.M_rows && sl < nslots)
+                            p.ent[(size_t)r * nslots + sl] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-#pragma unroll
-                for (int q = 0; q < ENT_RB; ++q) {
-                    const int r = r0 + q;
-                    float M = -INFINITY, S = 0.f, T = 0.f;
-#pragma unroll
-                    for (int i = 0; i < SPL; ++i) ent_merge(M, S, T, st[q][i].x, st[q][i].y, st[q][i].z);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
-                        const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
-                        const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
-                        ent_merge(M, S, T, m2, s2, t2);
-                    }
-                    if (lane == 0 && r < p.M_rows) {
-                        // gathered rows: a source row outside [0, src_P) has no entropy
-                        const bool bad = p.src_rows && (p.src_rows[r] < 0 || p.src_rows[r] >= p.src_P);
-                        const float h = bad ? __int_as_float(0x7fc00000) : logf(S) - T / S;
-                        p.H[r] = h;
-                        if (p.route) p.route[r] = bad ? -1 : (h > p.tau ? 1 : 0);
-                    }
-                }
             }
         }
     }
