@@ -182,52 +182,86 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
     }
     if (quad_live) {
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-        for (int c0 = 0; c0 < sp.rows; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tbase + c0, r);
-            tmem_ld_wait();
-            const int col0 = sp.row0 + c0;
-            // columns >= lim are past the weight matrix or past this tile; rows
-            // past the activations (stale shared-memory rows) take no part
-            const int lim = row < M_rows ? min(N_w - col0, sp.rows - c0) : 0;
+        if constexpr (KT == 1) {
+            // two 32-column loads in flight per wait; each chunk's best by a
+            // pairwise tree over adjacent columns (a strict > keeps the lower
+            // column on ties, as a left-to-right scan would)
+            for (int c00 = 0; c00 < sp.rows; c00 += 64) {
+                uint32_t r2[2][32];
+                const bool two = c00 + 32 < sp.rows;   // the same for the whole warp
+                tmem_ld_32x32b_x32(tbase + c00, r2[0]);
+                if (two) tmem_ld_32x32b_x32(tbase + c00 + 32, r2[1]);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float v = __uint_as_float(r[j]);
-                if (j < lim) {
-                    if constexpr (KT == 1) {
-                        if (v > tv[0]) {
-                            tv[0] = v;
-                            ti[0] = col0 + j;
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (hh == 1 && !two) break;
+                    const uint32_t (&r)[32] = r2[hh];
+                    const int c0 = c00 + 32 * hh;
+                    const int col0 = sp.row0 + c0;
+                    // columns >= lim are past the weight matrix or past this tile; rows
+                    // past the activations (stale shared-memory rows) take no part
+                    const int lim = row < M_rows ? min(N_w - col0, sp.rows - c0) : 0;
+                    float bv[16];
+                    int bj[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float a = 2 * j < lim ? __uint_as_float(r[2 * j]) : -INFINITY;
+                        const float b = 2 * j + 1 < lim ? __uint_as_float(r[2 * j + 1]) : -INFINITY;
+                        const bool t = b > a;
+                        bv[j] = t ? b : a;
+                        bj[j] = t ? 2 * j + 1 : 2 * j;
+                    }
+#pragma unroll
+                    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int j = 0; j < w; ++j) {
+                            const bool t = bv[2 * j + 1] > bv[2 * j];
+                            bv[j] = t ? bv[2 * j + 1] : bv[2 * j];
+                            bj[j] = t ? bj[2 * j + 1] : bj[2 * j];
                         }
-                    } else {
-                        if (v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
+                    if (bv[0] > tv[0]) {
+                        tv[0] = bv[0];
+                        ti[0] = col0 + bj[0];
+                    }
+                    if constexpr (ENT) {
+                        // tv[0] is the largest column of this tile so far and em the
+                        // largest before it, so a new running maximum shows in tv[0].
+                        // Sums run in base 2: z = (v - em) log2 e, es = sum 2^z (the
+                        // same terms as sum e^(v - em)), et = sum z 2^z (ln 2 times the
+                        // natural-log sum; scaled back when published).
+                        if (tv[0] > em) {   // new running maximum: rescale what was summed so far
+                            if (es > 0.f) {
+                                const float dz = (em - tv[0]) * LOG2E;
+                                const float sc = ex2_approx(dz);
+                                et = (et + dz * es) * sc;
+                                es *= sc;
+                            }
+                            em = tv[0];
+                        }
+                        const float off = em * LOG2E;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < lim) {
+                                const float z = fmaf(__uint_as_float(r[j]), LOG2E, -off);
+                                const float e = ex2_approx(z);
+                                es += e;
+                                et = fmaf(z, e, et);
+                            }
                     }
                 }
             }
-            if constexpr (ENT) {
-                // tv[0] is the largest column of this tile so far and em the
-                // largest before it, so a new running maximum shows in tv[0].
-                // Sums run in base 2: z = (v - em) log2 e, es = sum 2^z (the
-                // same terms as sum e^(v - em)), et = sum z 2^z (ln 2 times the
-                // natural-log sum; scaled back when published).
-                if (tv[0] > em) {   // new running maximum: rescale what was summed so far
-                    if (es > 0.f) {
-                        const float dz = (em - tv[0]) * LOG2E;
-                        const float sc = ex2_approx(dz);
-                        et = (et + dz * es) * sc;
-                        es *= sc;
-                    }
-                    em = tv[0];
-                }
-                const float off = em * LOG2E;
+        } else {
+            for (int c0 = 0; c0 < sp.rows; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + c0, r);
+                tmem_ld_wait();
+                const int col0 = sp.row0 + c0;
+                const int lim = row < M_rows ? min(N_w - col0, sp.rows - c0) : 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j < lim) {
-                        const float z = fmaf(__uint_as_float(r[j]), LOG2E, -off);
-                        const float e = ex2_approx(z);
-                        es += e;
-                        et = fmaf(z, e, et);
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    const float v = __uint_as_float(r[j]);
+                    if (j < lim && v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
+                }
             }
         }
     }
@@ -247,6 +281,19 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
     return true;
 }
 
+// Tile u of the v-th position in the schedule.  DUAL: the second problem's
+// tiles (u >= U0, top-k, the costlier epilogue) come first, so that a CTA's
+// last tile, whose epilogue nothing overlaps, is an argmax tile.  Each tile
+// stays with the same CTA as in plain order when both problems' tile counts
+// are multiples of the CTA count (balanced tiles); otherwise the CTAs still
+// split the tiles exactly once between them.
+template <bool DUAL>
+__device__ __forceinline__ int tile_order(int v, int U0, int U) {
+    if constexpr (!DUAL) return v;
+    const int n2 = U - U0;
+    return v < n2 ? U0 + v : v - n2;
+}
+
 // CL = 1: each CTA loads its own activation and weight boxes.
 // CL = 2: CTAs run in clusters of two on tile pairs (m, n) and (m + 1, n) that
 // share the weight tile: each CTA loads half of it and multicasts that half to
@@ -258,8 +305,9 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
 // same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
 // activation tiles).
 // DUAL (with KT = 1, CL = 1): tiles U0.. are the second problem's
-// (activation map tmA2, weight map tmB2, top-k into p.cand); with ENT the
-// first problem's tiles also feed the entropy statistics.
+// (activation map tmA2, weight map tmB2, top-k into p.cand), swept first
+// (tile_order); with ENT the first problem's tiles also feed the entropy
+// statistics.
 template <int KT, int CL, bool ENT, bool DUAL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -341,7 +389,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             int s = 0;        // = it % stages
             uint32_t ph = 0;  // = (it / stages) & 1
             bool ok = true;
-            for (int u = slot; u < U && ok; u += nslots) {
+            for (int v = slot; v < U && ok; v += nslots) {
+                const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
                 const int m = second ? 0 : (u % num_mp) * CL + rank;
                 const int n = second ? u - U0 : u / num_mp;
@@ -384,7 +433,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             int s = 0;        // = it % stages
             uint32_t ph = 0;  // = (it / stages) & 1
             bool ok = true, issued = false;
-            for (int u = slot; u < U && ok; u += nslots, ++tile_i) {
+            for (int v = slot; v < U && ok; v += nslots, ++tile_i) {
+                const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
                 const int n = second ? u - U0 : u / num_mp;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
@@ -437,7 +487,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int rit = q * 32 + lane;
         float em = -INFINITY, es = 0.f, et = 0.f;   // ENT: this row's running softmax statistics
         uint32_t tile_i = 0;
-        for (int u = slot; u < U; u += nslots, ++tile_i) {
+        for (int v = slot; v < U; v += nslots, ++tile_i) {
+            const int u = tile_order<DUAL>(v, U0, U);
             bool ok;
             if (DUAL && u >= U0)
                 ok = epilogue_tile<KT_TOPK, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
