@@ -143,6 +143,63 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
                 const int32_t* __restrict__ cache_len, int B, int N, int din, int cap,
                 const uint16_t* __restrict__ gamma, float eps, int with_final, float theta, int D,
                 uint16_t* __restrict__ ahat, uint16_t* __restrict__ afin, float2* __restrict__ rope, Control* ctrl) {
+    // Everything read before the dependency wait is an input of the call (the
+    // backlog rows, the gains, the offsets): both row loads go out together.
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * NORM_ROWS_PER_CTA + (threadIdx.x >> 5);
+    const int rows = N + (with_final ? B : 0);
+    const bool active = r < rows;
+    const int chunks = din >> 3;
+    int src = -1, bad_b = -1;
+    uint16_t* dst = nullptr;
+    if (active) {
+        if (r < N) {
+            src = r;
+            dst = ahat + (size_t)r * din;
+        } else {
+            const int b = r - N;
+            const int n = bl_off[b + 1] - bl_off[b];
+            const int L = cache_len[b];
+            if (n < 1 || L < 0 || L + n > cap || bl_off[b] < 0 || bl_off[b + 1] > N)
+                bad_b = b;
+            else
+                src = bl_off[b + 1] - 1;
+            dst = afin + (size_t)b * din;
+        }
+    }
+    const uint4* x = reinterpret_cast<const uint4*>(u + (size_t)(src < 0 ? 0 : src) * din);
+    const uint4* gm = reinterpret_cast<const uint4*>(gamma);
+    // rows up to 32 * NORM_REG_CHUNKS * 8 wide stay in registers (one read of the row)
+    const bool in_regs = chunks <= 32 * NORM_REG_CHUNKS;
+    uint4 xr[NORM_REG_CHUNKS], gr[NORM_REG_CHUNKS];
+    float ss = 0.f;
+    auto sumsq = [&](const uint4 v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+        }
+    };
+    if (src >= 0 && in_regs) {
+#pragma unroll
+        for (int k = 0; k < NORM_REG_CHUNKS; ++k) {
+            const int c = lane + 32 * k;
+            xr[k] = c < chunks ? __ldg(x + c) : make_uint4(0, 0, 0, 0);
+            gr[k] = c < chunks ? __ldg(gm + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < NORM_REG_CHUNKS; ++k) sumsq(xr[k]);
+    } else if (src >= 0) {
+        for (int c = lane; c < chunks; c += 32) sumsq(__ldg(x + c));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rs = 1.0f / sqrtf(ss / (float)din + eps);
+
+    // the workspace (rotary table, control block, the normalised rows) only
+    // after the previous kernel on the stream is done with it
     pdl_wait();
     pdl_trigger();
     if (blockIdx.x == 0) {
@@ -162,61 +219,12 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
             ctrl->rope_tag[1] = td;
         }
     }
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * NORM_ROWS_PER_CTA + (threadIdx.x >> 5);
-    const int rows = N + (with_final ? B : 0);
-    if (r >= rows) return;
-    int src;
-    uint16_t* dst;
-    if (r < N) {
-        src = r;
-        dst = ahat + (size_t)r * din;
-    } else {
-        const int b = r - N;
-        const int n = bl_off[b + 1] - bl_off[b];
-        const int L = cache_len[b];
-        if (n < 1 || L < 0 || L + n > cap || bl_off[b] < 0 || bl_off[b + 1] > N) {
-            if (lane == 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
-            src = -1;
-        } else {
-            src = bl_off[b + 1] - 1;
-        }
-        dst = afin + (size_t)b * din;
-    }
-    const int chunks = din >> 3;
+    if (!active) return;
     if (src < 0) {
+        if (lane == 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)bad_b);
         for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
         return;
     }
-    const uint4* x = reinterpret_cast<const uint4*>(u + (size_t)src * din);
-    // rows up to 32 * NORM_REG_CHUNKS * 8 wide stay in registers (one read of the row)
-    const bool in_regs = chunks <= 32 * NORM_REG_CHUNKS;
-    uint4 xr[NORM_REG_CHUNKS];
-    float ss = 0.f;
-    auto sumsq = [&](const uint4 v) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-            ss = fmaf(lo, lo, ss);
-            ss = fmaf(hi, hi, ss);
-        }
-    };
-    if (in_regs) {
-#pragma unroll
-        for (int k = 0; k < NORM_REG_CHUNKS; ++k) {
-            const int c = lane + 32 * k;
-            xr[k] = c < chunks ? __ldg(x + c) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < NORM_REG_CHUNKS; ++k) sumsq(xr[k]);
-    } else {
-        for (int c = lane; c < chunks; c += 32) sumsq(__ldg(x + c));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float rs = 1.0f / sqrtf(ss / (float)din + eps);
-    const uint4* gm = reinterpret_cast<const uint4*>(gamma);
     auto emit_g = [&](int c, const uint4 v, const uint4 gv) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w}, g[4] = {gv.x, gv.y, gv.z, gv.w};
         uint32_t o[4];
@@ -229,11 +237,6 @@ __global__ void __launch_bounds__(32 * NORM_ROWS_PER_CTA)
         reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
     };
     if (in_regs) {
-        // the gains first, all loads in flight together, then the outputs
-        uint4 gr[NORM_REG_CHUNKS];
-#pragma unroll
-        for (int k = 0; k < NORM_REG_CHUNKS; ++k)
-            gr[k] = lane + 32 * k < chunks ? __ldg(gm + lane + 32 * k) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int k = 0; k < NORM_REG_CHUNKS; ++k)
             if (lane + 32 * k < chunks) emit_g(lane + 32 * k, xr[k], gr[k]);
