@@ -152,13 +152,41 @@ __device__ __forceinline__ TileSpan tile_span(int n, int num_n, int bn, int nbig
     return {ns * (bn - 16) + (n - ns) * bn, bn, true};
 }
 
+// Fold the columns j < lim of one 32-column chunk into a row's running
+// softmax statistics; tv0 is the row's largest column so far in this tile,
+// this chunk included, and em the largest before the tile, so a new running
+// maximum shows in tv0.  Sums run in base 2: z = (v - em) log2 e, es = sum
+// 2^z (the same terms as sum e^(v - em)), et = sum z 2^z (ln 2 times the
+// natural-log sum; scaled back when published).
+__device__ __forceinline__ void ent_fold(const uint32_t (&r)[32], int lim, float tv0, float& em, float& es,
+                                         float& et) {
+    if (tv0 > em) {   // new running maximum: rescale what was summed so far
+        if (es > 0.f) {
+            const float dz = (em - tv0) * LOG2E;
+            const float sc = ex2_approx(dz);
+            et = (et + dz * es) * sc;
+            es *= sc;
+        }
+        em = tv0;
+    }
+    const float off = em * LOG2E;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j < lim) {
+            const float z = fmaf(__uint_as_float(r[j]), LOG2E, -off);
+            const float e = ex2_approx(z);
+            es += e;
+            et = fmaf(z, e, et);
+        }
+}
+
 // One finished accumulator as epilogue thread rit sees it (activation row
 // m * BM + rit of a problem with M_rows rows and N_w weight rows): wait for
 // it, keep the row's best (KT = 1) or top KT over the tile's columns and, with
 // ENT, fold the columns into the row's softmax statistics; hand the
 // accumulator back to the MMA warp, then publish the row's result (a packed
 // key for argmax, the tile's sorted candidate list for top-k).
-template <int KT, bool ENT>
+template <int KT, bool ENT, bool TAIL>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfull, uint64_t* tempty,
                                               volatile int* abort_flag, uint32_t tmem_base, uint32_t tile_i, int q,
                                               int rit, int M_rows, int N_w, int m, int n, const TileSpan sp,
@@ -182,7 +210,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
     }
     if (quad_live) {
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-        if constexpr (KT == 1) {
+        if constexpr (KT == 1 && TAIL) {
             // two 32-column loads in flight per wait; each chunk's best by a
             // pairwise tree over adjacent columns (a strict > keeps the lower
             // column on ties, as a left-to-right scan would)
@@ -223,34 +251,13 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
                         tv[0] = bv[0];
                         ti[0] = col0 + bj[0];
                     }
-                    if constexpr (ENT) {
-                        // tv[0] is the largest column of this tile so far and em the
-                        // largest before it, so a new running maximum shows in tv[0].
-                        // Sums run in base 2: z = (v - em) log2 e, es = sum 2^z (the
-                        // same terms as sum e^(v - em)), et = sum z 2^z (ln 2 times the
-                        // natural-log sum; scaled back when published).
-                        if (tv[0] > em) {   // new running maximum: rescale what was summed so far
-                            if (es > 0.f) {
-                                const float dz = (em - tv[0]) * LOG2E;
-                                const float sc = ex2_approx(dz);
-                                et = (et + dz * es) * sc;
-                                es *= sc;
-                            }
-                            em = tv[0];
-                        }
-                        const float off = em * LOG2E;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < lim) {
-                                const float z = fmaf(__uint_as_float(r[j]), LOG2E, -off);
-                                const float e = ex2_approx(z);
-                                es += e;
-                                et = fmaf(z, e, et);
-                            }
-                    }
+                    if constexpr (ENT) ent_fold(r, lim, tv[0], em, es, et);
                 }
             }
         } else {
+            // one load per wait and a left-to-right scan: fewer registers and
+            // TMEM reads beside the MMAs of a tensor-bound sweep, whose tiles
+            // are long enough to hide the epilogue
             for (int c0 = 0; c0 < sp.rows; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + c0, r);
@@ -260,8 +267,18 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float v = __uint_as_float(r[j]);
-                    if (j < lim && v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
+                    if (j < lim) {
+                        if constexpr (KT == 1) {
+                            if (v > tv[0]) {
+                                tv[0] = v;
+                                ti[0] = col0 + j;
+                            }
+                        } else {
+                            if (v > tv[KT - 1]) topk_insert<KT>(tv, ti, v, col0 + j);
+                        }
+                    }
                 }
+                if constexpr (ENT) ent_fold(r, lim, tv[0], em, es, et);
             }
         }
     }
@@ -491,11 +508,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             const int u = tile_order<DUAL>(v, U0, U);
             bool ok;
             if (DUAL && u >= U0)
-                ok = epilogue_tile<KT_TOPK, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
+                ok = epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
                                                    p.M_rows2, p.N_w2, 0, u - U0,
                                                    tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false), 1, em, es, et);
             else
-                ok = epilogue_tile<KT, ENT>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
+                ok = epilogue_tile<KT, ENT, CL == 1>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
                                             p.N_w, (u % num_mp) * CL + rank, u / num_mp,
                                             tile_span(u / num_mp, p.num_n, p.bn, p.nbig, true), p.num_m, em, es, et);
             if (!ok) break;
