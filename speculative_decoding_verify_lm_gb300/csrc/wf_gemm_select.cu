@@ -15,7 +15,8 @@
 //              rows <= 256, K=16) per stage
 //   warps 2-5  epilogue: tcgen05.ld the finished accumulator (thread = one
 //              activation row, 32 columns per load), keep the running best
-//              (argmax) or a sorted top-k per row, and release the
+//              (argmax; a pairwise tree per 32 columns where the last tile's
+//              scan is exposed) or a sorted top-k per row, and release the
 //              accumulator so the next tile's MMAs overlap this scan.
 // With one activation tile, each weight matrix is cut into a multiple of the
 // CTA count of tiles of two heights (h and h - 16), so that every CTA sweeps
@@ -25,9 +26,10 @@
 // to ids and resets them to zero.  Top-k rows write one sorted candidate list
 // per tile; wf_topk_merge combines them.
 // DUAL: one launch sweeps two problems with one activation tile each - the
-// target LM head (argmax) and then the EAGLE-3 draft head (top-k) - through
-// the same pipeline, so the smaller draft matrix streams at full bandwidth
-// behind the larger one instead of as a second, under-filled sweep.
+// target LM head (argmax) and the EAGLE-3 draft head (top-k) - through the
+// same pipeline, so the smaller draft matrix streams at full bandwidth with
+// the larger one instead of as a second, under-filled sweep; each CTA takes
+// its draft-head tile first, so that its last tile has the cheap epilogue.
 //
 // Every wait is bounded: a wait that runs out records WF_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, drains its own in-flight copies / MMAs (again bounded)
