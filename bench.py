@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "verified positions/s and accepted tokens/s per round; % of HBM/TC roofline"
+CATCHUP_METRIC = "KV-only catch-up: backlog tokens entered per second; % of HBM roofline"
 UNIT = "verified positions/s"
 L2_BYTES = 129 * 2 ** 20
 
@@ -249,6 +250,14 @@ def _subset(wl, seqs):
             wl.b1, wl.w2, wl.b2, wl.tau, wl.max_depth)
 
 
+def round_config(cfg_name, cfg, wl, entropy):
+    """The workload keys of a round's JSON line, the same for both arms."""
+    draft = wl.Wd is not None
+    return {"workload": cfg_name, "P": int(wl.P), "B": int(wl.B), "d": cfg.d, "V": cfg.V,
+            "router": "entropy" if entropy else f"neural, m = {int(wl.W1.shape[0])}",
+            "draft_head": f"{cfg.Vd}x{cfg.d} top-{wl.topk}" if draft else None}
+
+
 def run_reference(args, cfg_name, wl):
     """--impl reference: the CPU oracle, as it stands, on the host cores."""
     import oracle
@@ -270,7 +279,7 @@ def run_reference(args, cfg_name, wl):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg_name, "rows_per_step": P1},
+            "config": dict(round_config(cfg_name, args.cfg, wl, entropy), rows_per_step=P1),
             "accepted_tokens_per_s": acc / dt,
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step: one oracle round over the first sequence ({P1} verified rows)"},
@@ -279,6 +288,12 @@ def run_reference(args, cfg_name, wl):
 
 
 # ----------------------------------------------------------------------------- KV-only catch-up
+def catchup_config(cfg):
+    """The workload keys of a catch-up JSON line, the same for both arms."""
+    return {"workload": cfg.name, "B": len(cfg.n), "backlog": list(cfg.n), "cache_len": list(cfg.L),
+            "din": cfg.din, "H": cfg.H, "G": cfg.G, "D": cfg.D}
+
+
 def run_catchup_reference(args):
     """The oracle's catch-up, timed on the host cores (the reference arm of --catchup)."""
     import oracle
@@ -293,11 +308,11 @@ def run_catchup_reference(args):
     dt = time.perf_counter() - t0
     N = int(c["bl_off"][-1])
     val = N * args.steps / dt
-    print(json.dumps({"impl": "reference", "metric": "KV-only catch-up: backlog tokens entered per second",
+    print(json.dumps({"impl": "reference", "metric": CATCHUP_METRIC,
                       "value": val, "unit": "backlog tokens/s", "n_gpus": args.gpus, "steps": args.steps,
                       "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
                       "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                      "config": {"workload": cfg.name},
+                      "config": catchup_config(cfg),
                       "cpu_baseline": {"value": val, "unit": "backlog tokens/s", "cores": oracle.threads(),
                                        "kind": "oracle", "sample": "whole oracle catch-up calls of this workload"},
                       "e2e": {"value": val, "unit": "backlog tokens/s", "h2d_bytes_per_step": 0,
@@ -401,12 +416,11 @@ def run_catchup(args, rank, local, pg):
         dt = time.perf_counter() - t0
         cpu = {"value": N * reps / dt, "unit": "backlog tokens/s", "cores": oracle.threads(), "kind": "oracle",
                "sample": f"{reps} whole oracle catch-up call(s) of this workload"}
-    line = {"metric": "KV-only catch-up: backlog tokens entered per second; % of HBM roofline",
+    line = {"metric": CATCHUP_METRIC,
             "value": N * args.steps / (sum(ms) / 1e3), "unit": "backlog tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": cfg.name, "B": B, "backlog": list(cfg.n), "cache_len": list(cfg.L),
-                       "din": cfg.din, "H": cfg.H, "G": cfg.G, "D": cfg.D,
+            "config": {**catchup_config(cfg),
                        "l2": "L2 flushed (256 MB write) before every call",
                        "launch": "wf_catchup captured in a CUDA graph" if not args.no_graph else "direct calls"},
             "roofline": roof, "cpu_baseline": cpu,
@@ -485,7 +499,7 @@ def run_op_reference(args):
     print(json.dumps({"impl": "reference", "metric": metric, "value": val, "unit": unit, "n_gpus": args.gpus,
                       "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
                       "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                      "data": "synthetic", "config": {"workload": name},
+                      "data": "synthetic", "config": {"workload": name, "B": args.op_batch},
                       "cpu_baseline": {"value": val, "unit": unit, "cores": oracle.threads(), "kind": "oracle",
                                        "sample": "whole oracle calls of this workload"},
                       "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
@@ -659,6 +673,7 @@ def main():
             import oracle
             wl = synth.make_workload(args.config, oracle.argmax_fn, reject=False, m=args.router_width,
                                      plant_seqs=[0])
+            args.cfg = cfg
             run_reference(args, cfg_name, wl)
         return
 
@@ -866,9 +881,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": sum(step_ms) / len(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg_name, "P": P, "B": B, "d": d, "V": V,
-                   "router": "entropy" if entropy else f"neural, m = {int(wl.W1.shape[0])}",
-                   "draft_head": f"{cfg.Vd}x{d} top-{wl.topk}" if draft else None,
+        "config": {**round_config(cfg_name, cfg, wl, entropy),
                    "l2": "flushed between steps (working set < 2x L2)" if flush
                    else f"inputs larger than L2 (weights {weight_bytes / 1e6:.0f} MB streamed per step)",
                    "parallelism": f"replicas x{world}",

@@ -50,3 +50,31 @@ def test_reference_arm_line(op):
         assert key in j, key
     assert j["impl"] == "reference" and j["value"] > 0 and j["cpu_baseline"]["kind"] == "oracle"
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["e2e"]["value"] == j["value"]
+
+
+@pytest.mark.parametrize("mode,metric", [(["--config", "0"], "METRIC"), (["--config", "0", "--router", "entropy"], "METRIC"),
+                                         (["--catchup", "0"], "CATCHUP_METRIC")])
+def test_reference_arm_matches_own_arm(mode, metric):
+    """The reference arm of a round or a catch-up prints the metric, unit and
+    workload keys the GPU arm prints for the same mode (the driver compares
+    the two lines)."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *mode,
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["metric"] == getattr(bench, metric) and j["higher_is_better"] is True
+    assert j["value"] > 0 and j["e2e"]["value"] == j["value"] and j["cpu_baseline"]["kind"] == "oracle"
+    from speculative_decoding_verify_lm_gb300 import synth
+    if metric == "METRIC":
+        cfg = synth.CONFIGS[0]
+        wl = synth.make_workload(0, oracle.argmax_fn, reject=False, plant_seqs=[0])
+        entropy = "entropy" in mode
+        want = bench.round_config(cfg.name + ("_entropy" if entropy else ""), cfg, wl, entropy)
+        assert j["unit"] == bench.UNIT
+    else:
+        want = bench.catchup_config(synth.CATCHUP_CONFIGS[0])
+        assert j["unit"] == "backlog tokens/s"
+    for k, v in want.items():
+        assert j["config"][k] == v, k
