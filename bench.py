@@ -258,7 +258,7 @@ def round_config(cfg_name, cfg, wl, entropy):
             "draft_head": f"{cfg.Vd}x{cfg.d} top-{wl.topk}" if draft else None}
 
 
-def run_reference(args, cfg_name, wl):
+def run_reference(args, cfg_name, cfg, wl):
     """--impl reference: the CPU oracle, as it stands, on the host cores."""
     import oracle
     o = oracle.default()
@@ -279,7 +279,7 @@ def run_reference(args, cfg_name, wl):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(round_config(cfg_name, args.cfg, wl, entropy), rows_per_step=P1),
+            "config": dict(round_config(cfg_name, cfg, wl, entropy), rows_per_step=P1),
             "accepted_tokens_per_s": acc / dt,
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step: one oracle round over the first sequence ({P1} verified rows)"},
@@ -673,8 +673,7 @@ def main():
             import oracle
             wl = synth.make_workload(args.config, oracle.argmax_fn, reject=False, m=args.router_width,
                                      plant_seqs=[0])
-            args.cfg = cfg
-            run_reference(args, cfg_name, wl)
+            run_reference(args, cfg_name, cfg, wl)
         return
 
     import torch
