@@ -6,7 +6,11 @@ LM-head argmax at every verified row, chain / tree acceptance with the bonus
 token, the neural router on each sequence's last accepted row, and (for the
 EAGLE-3 workloads) the draft head's top-10.  Inputs are the seeded synthetic
 workloads of ``speculative_decoding_verify_lm_gb300.synth`` (default: the
-Qwen3-4B-shaped DFlash chain, batch 1, hidden 2560, vocabulary 151,936).
+largest one, 256 EAGLE-3 trees of 60 nodes plus a root each = 15,616 verified
+rows over the Qwen3-4B-shaped LM head, hidden 2560, vocabulary 151,936, with
+the draft head's top-10 over 32,000 ids), rebuilt from the record that the
+oracle's full-size answers are stored with, so that every drafted token is
+planted from the oracle's target argmax and both arms time the same inputs.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (a deliberately slow baseline, not a GPU program).
@@ -40,7 +44,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, help="workload index 0-4 (default 1: DFlash chain, batch 1)")
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload index 0-4 (default 4: 256 EAGLE-3 trees, 15,616 verified rows)")
     ap.add_argument("--router-width", type=int, default=None, help="override m (the paper's m = d/8 = 320)")
     ap.add_argument("--router", choices=["neural", "entropy"], default="neural",
                     help="the round's routing policy: the neural router (default) or WhiFlash-Entropy")
@@ -166,8 +171,9 @@ class ClockSampler:
                 "samples": len(self.sm), "source": src}
 
 
-KERNEL_SOURCES = {"gemm_select_kernel<1>": ("wf_gemm_select.cu", "wf_internal.cuh"),
-                  "gemm_select_kernel<1,1,0,1>": ("wf_gemm_select.cu", "wf_internal.cuh")}
+# kernel label -> the source files it is built from (template arguments: top-k width, entropy, both heads)
+KERNEL_SOURCES = {name: ("wf_gemm_select.cu", "wf_internal.cuh")
+                  for name in ("gemm_select_kernel<1,0,0>", "gemm_select_kernel<1,1,0>", "gemm_select_kernel<1,0,1>")}
 
 
 def source_sha(kernel: str) -> str:
@@ -181,12 +187,13 @@ def source_sha(kernel: str) -> str:
 
 
 def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             j = json.load(f)
-        return j["hbm_gbs"], j["bf16_tflops"], "measured"
-    return 6800.0, 1900.0, "fallback"
+        return j["hbm_gbs"], j["bf16_tflops"], j.get("bf16_tflops_sustained", j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 def traffic_for(kernel: str, workload: str):
@@ -250,22 +257,60 @@ def _subset(wl, seqs):
             wl.b1, wl.w2, wl.b2, wl.tau, wl.max_depth)
 
 
-def round_config(cfg_name, cfg, wl, entropy):
+def round_config(cfg_name, cfg, wl, entropy, world=1):
     """The workload keys of a round's JSON line, the same for both arms."""
     draft = wl.Wd is not None
+    weight_bytes = cfg.V * cfg.d * 2 + (wl.Wd.nbytes if draft else 0) + wl.W1.nbytes
     return {"workload": cfg_name, "P": int(wl.P), "B": int(wl.B), "d": cfg.d, "V": cfg.V,
             "router": "entropy" if entropy else f"neural, m = {int(wl.W1.shape[0])}",
-            "draft_head": f"{cfg.Vd}x{cfg.d} top-{wl.topk}" if draft else None}
+            "draft_head": f"{cfg.Vd}x{cfg.d} top-{wl.topk}" if draft else None,
+            "inputs": "rebuilt from the stored oracle record: every sequence planted from the oracle's target argmax",
+            "l2": "flushed between steps (working set < 2x L2)" if flush_l2(weight_bytes)
+            else f"inputs larger than L2 (weights {weight_bytes / 1e6:.0f} MB streamed per step)",
+            "parallelism": f"replicas x{world}"}
 
 
-def run_reference(args, cfg_name, cfg, wl):
-    """--impl reference: the CPU oracle, as it stands, on the host cores."""
+def flush_l2(weight_bytes: int) -> bool:
+    return weight_bytes < 2 * L2_BYTES
+
+
+def golden_record(index: int) -> dict:
+    """The oracle's stored full-size answers for workload ``index`` (written by
+    tests/golden/make_full_goldens.py, which calls only the oracle); read here
+    only for the generation record that rebuilds the inputs."""
+    from speculative_decoding_verify_lm_gb300 import synth
+    path = os.path.join(ROOT, "tests", "golden", f"round_{synth.CONFIGS[index].name}.json")
+    with open(path) as f:
+        return json.load(f)
+
+
+def load_workload(index: int, m=None):
+    from speculative_decoding_verify_lm_gb300 import synth
+    return synth.workload_from_record(golden_record(index), m=m)
+
+
+def round_launches(P: int, B: int, draft: bool, entropy: bool) -> int:
+    """Kernel launches of one wf_round (the composition in wf_round: the LM
+    head or both heads in one sweep, acceptance, the router, the draft head)."""
+    shared = draft and P <= 128 and B <= 128
+    if entropy:
+        if P <= 128:
+            return 2 + (0 if shared else (2 if draft else 0))
+        return 4 + (2 if draft else 0)
+    if P <= 32:   # router beside the LM head over every row
+        return 3 + (0 if shared else (2 if draft else 0))
+    router = 1 if B <= 8 else 2
+    return 2 + router + (0 if shared else (2 if draft else 0))
+
+
+def run_reference(args, cfg_name, cfg, wl, world):
+    """--impl reference: the CPU oracle, as it stands, on the host cores.  Each
+    step is one oracle round over a bounded sample of the workload (its first
+    sequence; the whole workload would take minutes to hours per step)."""
     import oracle
     o = oracle.default()
     entropy = args.router == "entropy"
-    per_step_budget = max(0.5, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
-    value, sample, cores, t_round, P_sub = cpu_sample(wl, per_step_budget, entropy)
-    sub = _subset(wl, list(range(min(wl.B, 1))))
+    sub = _subset(wl, [0])
     for _ in range(args.warmup):
         oracle_round(o, sub, entropy)
     t0 = time.perf_counter()
@@ -279,10 +324,11 @@ def run_reference(args, cfg_name, cfg, wl):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(round_config(cfg_name, cfg, wl, entropy), rows_per_step=P1),
+            "config": round_config(cfg_name, cfg, wl, entropy, world),
             "accepted_tokens_per_s": acc / dt,
-            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"each step: one oracle round over the first sequence ({P1} verified rows)"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": o.threads(), "kind": "oracle",
+                             "sample": f"each step: one oracle round over the workload's first sequence "
+                                       f"({P1} of {wl.P} verified rows)"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -291,7 +337,7 @@ def run_reference(args, cfg_name, cfg, wl):
 def catchup_config(cfg):
     """The workload keys of a catch-up JSON line, the same for both arms."""
     return {"workload": cfg.name, "B": len(cfg.n), "backlog": list(cfg.n), "cache_len": list(cfg.L),
-            "din": cfg.din, "H": cfg.H, "G": cfg.G, "D": cfg.D}
+            "din": cfg.din, "H": cfg.H, "G": cfg.G, "D": cfg.D, "l2": "L2 flushed (256 MB write) before every call"}
 
 
 def run_catchup_reference(args):
@@ -380,7 +426,7 @@ def run_catchup(args, rank, local, pg):
     N = int(c["bl_off"][-1])
     B = len(cfg.n)
     nbytes, flops, T = catchup_work(c)
-    hbm_peak, tc_peak, peak_src = measured_peaks()
+    hbm_peak, tc_peak, _, peak_src = measured_peaks()
     achieved = nbytes / (ms_mean / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
             "traffic": None, "kernel": "catch-up call (norm, projections, attention, output projection)",
@@ -420,9 +466,8 @@ def run_catchup(args, rank, local, pg):
             "value": N * args.steps / (sum(ms) / 1e3), "unit": "backlog tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {**catchup_config(cfg),
-                       "l2": "L2 flushed (256 MB write) before every call",
-                       "launch": "wf_catchup captured in a CUDA graph" if not args.no_graph else "direct calls"},
+            "config": catchup_config(cfg),
+            "launch": "wf_catchup captured in a CUDA graph" if not args.no_graph else "direct calls",
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": N * args.steps / e2e_s, "unit": "backlog tokens/s",
                     "h2d_bytes_per_step": int(h_u.numel() * h_u.element_size()),
@@ -475,6 +520,11 @@ def op_oracle(op: str, x: dict):
     return rows, off, x["hidden"][kept]
 
 
+def op_config(op: str, B: int) -> dict:
+    """The workload keys of a side step's JSON line, the same for both arms."""
+    return {"workload": op_names(op, B)[0], "B": B, "l2": "L2 flushed (256 MB write) before every call"}
+
+
 def op_names(op: str, B: int):
     if op == "build_tree":
         return (f"eagle3_tree_build_b{B}_d8_k10_n60", "EAGLE-3 draft-tree construction: trees built per second",
@@ -499,7 +549,7 @@ def run_op_reference(args):
     print(json.dumps({"impl": "reference", "metric": metric, "value": val, "unit": unit, "n_gpus": args.gpus,
                       "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
                       "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                      "data": "synthetic", "config": {"workload": name, "B": args.op_batch},
+                      "data": "synthetic", "config": op_config(args.op, args.op_batch),
                       "cpu_baseline": {"value": val, "unit": unit, "cores": oracle.threads(), "kind": "oracle",
                                        "sample": "whole oracle calls of this workload"},
                       "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
@@ -590,7 +640,7 @@ def run_op(args, rank, local, pg):
     clocks = sampler.stop()
     ms = [a.elapsed_time(b) for a, b in ev]
     ms_mean = statistics.mean(ms)
-    hbm_peak, _, peak_src = measured_peaks()
+    hbm_peak, _, _, peak_src = measured_peaks()
     achieved = nbytes / (ms_mean / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
             "traffic": None, "kernel": "build_tree_kernel" if args.op == "build_tree"
@@ -632,8 +682,8 @@ def run_op(args, rank, local, pg):
             "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_mean, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int32" if args.op == "build_tree" else "bf16",
             "data": "synthetic",
-            "config": {"workload": name, "B": B, "l2": "L2 flushed (256 MB write) before every call",
-                       "launch": "captured in a CUDA graph" if not args.no_graph else "direct calls"},
+            "config": op_config(args.op, B),
+            "launch": "captured in a CUDA graph" if not args.no_graph else "direct calls",
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": units * args.steps / e2e_s, "unit": unit,
                     "h2d_bytes_per_step": int(sum(a.numel() * a.element_size() for a in ins)),
@@ -667,13 +717,12 @@ def main():
     entropy = args.router == "entropy"
     if entropy:
         cfg_name += "_entropy"
+    # both arms: the inputs the oracle's stored answers were computed on
+    wl = load_workload(args.config, m=args.router_width)
 
     if args.impl == "reference":
         if rank == 0:
-            import oracle
-            wl = synth.make_workload(args.config, oracle.argmax_fn, reject=False, m=args.router_width,
-                                     plant_seqs=[0])
-            run_reference(args, cfg_name, cfg, wl)
+            run_reference(args, cfg_name, cfg, wl, world)
         return
 
     import torch
@@ -682,22 +731,9 @@ def main():
     device = torch.device("cuda", local)
     wf.lib()
 
-    # ---- workload: weights on the device once; the library's own argmax plants the drafts
-    cache = {}
-
-    def gpu_argmax(W, rows):
-        key = id(W)
-        if key not in cache:
-            cache[key] = torch.from_numpy(W.view(np.int16)).to(device)
-        h = torch.from_numpy(np.ascontiguousarray(rows).view(np.int16)).to(device)
-        ws = wf.Workspace(h.shape[0], device=device)
-        ids = wf.wf_lmhead_argmax(h, cache[key], ws)
-        return ids.cpu().numpy(), None
-
-    wl = synth.make_workload(args.config, gpu_argmax, reject=False, m=args.router_width)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16  # noqa: E731
                                    else np.ascontiguousarray(a)).to(device)
-    Wdev = cache[id(wl.W)]
+    Wdev = t(wl.W)
     draft = wl.Wd is not None
     r = wf.Round(t(wl.hidden), Wdev, t(wl.pos_off), t(wl.node_off), t(wl.tok), t(wl.W1), t(wl.b1), t(wl.w2),
                  wl.b2, wl.tau, kind=t(wl.kind), parent=t(wl.parent), path_stride=wl.max_depth,
@@ -705,7 +741,7 @@ def main():
                  k=wl.topk if draft else 0, router_kind=wf.WF_ROUTER_ENTROPY if entropy else wf.WF_ROUTER_NEURAL)
     P, B, d, V = wl.P, wl.B, cfg.d, cfg.V
     weight_bytes = V * d * 2 + (wl.Wd.nbytes if draft else 0) + wl.W1.nbytes
-    flush = weight_bytes < 2 * L2_BYTES
+    flush = flush_l2(weight_bytes)
     l2buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device) if flush else None
     stream = torch.cuda.current_stream(device)
 
@@ -729,51 +765,12 @@ def main():
         if not torch.equal(ref_ids, r.out["ids"]):
             raise RuntimeError("graph replay disagrees with a direct wf_round call")
 
-    # ---- timed region: K whole rounds, CUDA events on the launching stream
-    if pg is not None:
-        pg.barrier()
-    torch.cuda.synchronize(device)
-    try:   # the physical GPU behind this rank's device (CUDA_VISIBLE_DEVICES may renumber)
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        gpu_id = str(local)
-    sampler = ClockSampler(gpu_id)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        if flush:
-            l2buf.zero_()
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    sampler.wait(ev[-1][1])
-    torch.cuda.synchronize(device)
-    if pg is not None:
-        pg.barrier()
-    clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    dev_s = sum(step_ms) / 1e3
-    out = {k: (v.cpu().numpy() if v is not None else None) for k, v in r.out.items()}
-    accepted = int((out["n_accept"] + 1).sum())
-    max_s = allreduce_max(pg, dev_s, device)
-    tot_rows = allreduce_sum(pg, P * args.steps, device)
-    tot_acc = allreduce_sum(pg, accepted * args.steps, device)
-    value = tot_rows / max_s
-    # the round's composition (wf_round): with at most 128 verified rows the
-    # router runs beside the LM head and the draft head shares its sweep
+    # ---- the dominant kernel on its own: the shared sweep of both heads
+    # (timed with its top-k merge) or the LM head alone (with the entropy
+    # statistics under entropy routing, when one sweep yields them)
     shared = draft and P <= 128 and B <= 128 and not entropy
-    # (shared: both heads; router; acceptance with the top-k merge in the same launch)
-    launches_per_round = 3 if shared else 3 + (2 if draft else 0)
-    # entropy routing: the LM-head sweep with the entropy statistics, then
-    # acceptance; with more rows, the LM head, acceptance, the gather of the
-    # accepted rows and a second sweep for their entropy (draft head after)
     ent_fused = entropy and P <= 128
-    if entropy:   # with one activation tile per head the draft head shares the entropy sweep
-        ent_shared = ent_fused and draft and B <= 128
-        launches_per_round = 2 if ent_shared else (2 if ent_fused else 4) + (2 if draft else 0)
-
-    # ---- the dominant kernel on its own, CUDA events per launch: the shared
-    # sweep of both heads (timed with its top-k merge) or the LM head alone
-    hbm_peak, tc_peak, peak_src = measured_peaks()
+    hbm_peak, tc_peak, tc_sus, peak_src = measured_peaks()
     ids_buf = torch.empty(P, dtype=torch.int32, device=device)
     hdev = r.inputs["hidden"]
     if shared:
@@ -788,7 +785,7 @@ def main():
         Vd = wl.Wd.shape[0]
         alg_bytes = (V + Vd) * d * 2 + (P + B) * d * 2 + Vd * 4 + P * 4 + B * k * 12
         alg_flops = 2.0 * d * (P * V + B * Vd)
-        kernel_name = "gemm_select_kernel<1,1,0,1>"
+        kernel_name, kernel_launches = "gemm_select_kernel<1,0,1>", 2
     elif ent_fused:
         ws1 = wf.Workspace(P, P, d=d, device=device)
         Hbuf = torch.empty(P, dtype=torch.float32, device=device)
@@ -796,13 +793,13 @@ def main():
         kernel_call = lambda: wf.wf_lmhead_entropy(hdev, Wdev, wl.tau, ws1, H=Hbuf, route=rbuf)  # noqa: E731
         alg_bytes = V * d * 2 + P * d * 2 + P * 8
         alg_flops = 2.0 * P * V * d
-        kernel_name = "gemm_select_kernel<1,1,1>"
+        kernel_name, kernel_launches = "gemm_select_kernel<1,1,0>", 1
     else:
         ws1 = wf.Workspace(P, device=device)
         kernel_call = lambda: wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)  # noqa: E731
         alg_bytes = V * d * 2 + P * d * 2 + P * 4
         alg_flops = 2.0 * P * V * d
-        kernel_name = "gemm_select_kernel<1>"
+        kernel_name, kernel_launches = "gemm_select_kernel<1,0,0>", 1
     for _ in range(3):
         kernel_call()
     if not args.no_graph:   # replayed from a CUDA graph: host argument checks stay out of the events
@@ -811,25 +808,75 @@ def main():
             kernel_call()
         kernel_call = kg.replay
         kernel_call()
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(device)
+
+    # ---- timed region: K steps.  Each step is one whole round, then the
+    # dominant kernel alone, both on this stream between CUDA events (after an
+    # L2 flush when the weights would fit in L2), so both see the same clocks
+    # and power state.  The host keeps one step queued ahead of the GPU (an
+    # idle GPU would put the host's launch latency between the events) and
+    # reads the SM clock while it waits for each step to end.
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize(device)
+    try:   # the physical GPU behind this rank's device (CUDA_VISIBLE_DEVICES may renumber)
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(mk(), mk(), mk(), mk()) for _ in range(args.steps)]
+    step_mhz = []
+
+    def wait_step(j):
+        n0 = len(sampler.sm)
+        sampler.wait(ev[j][3])
+        step_mhz.append(statistics.median(sampler.sm[n0:]) if len(sampler.sm) > n0 else None)
+
     for i in range(args.steps):
         if flush:
             l2buf.zero_()
-        kev[i][0].record(stream)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        if flush:
+            l2buf.zero_()
+        ev[i][2].record(stream)
         kernel_call()
-        kev[i][1].record(stream)
+        ev[i][3].record(stream)
+        if i > 0:
+            wait_step(i - 1)
+    wait_step(args.steps - 1)
     torch.cuda.synchronize(device)
-    k_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    k_ms_all = [e[2].elapsed_time(e[3]) for e in ev]
+    dev_s = sum(step_ms) / 1e3
+    out = {k_: (v.cpu().numpy() if v is not None else None) for k_, v in r.out.items()}
+    accepted = int((out["n_accept"] + 1).sum())
+    max_s = allreduce_max(pg, dev_s, device)
+    tot_rows = allreduce_sum(pg, P * args.steps, device)
+    tot_acc = allreduce_sum(pg, accepted * args.steps, device)
+    value = tot_rows / max_s
+    launches_per_round = round_launches(P, B, draft, entropy)
+
+    k_ms = statistics.mean(k_ms_all)
+    k_med = statistics.median(k_ms_all)
     hbm_bound = alg_flops / alg_bytes < (tc_peak * 1e12) / (hbm_peak * 1e9)
     if hbm_bound:
         achieved = alg_bytes / (k_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak}
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "frac_of_median_launch": alg_bytes / (k_med / 1e3) / 1e9 / hbm_peak}
     else:
         achieved = alg_flops / (k_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": achieved / tc_peak}
+                "frac": achieved / tc_peak, "frac_of_median_launch": alg_flops / (k_med / 1e3) / 1e12 / tc_peak,
+                "peak_sustained": tc_sus, "frac_sustained": achieved / tc_sus}
     roof.update({"traffic": traffic_for(kernel_name, cfg_name), "kernel": kernel_name,
                  "algorithmic_per_launch": alg_bytes if hbm_bound else alg_flops, "launch_ms": k_ms,
+                 "launch_ms_median": k_med,
                  "peak_source": f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'}, burst)"})
 
     # ---- end to end through the public API: every step copies the round's inputs
@@ -880,18 +927,19 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": sum(step_ms) / len(step_ms), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {**round_config(cfg_name, cfg, wl, entropy),
-                   "l2": "flushed between steps (working set < 2x L2)" if flush
-                   else f"inputs larger than L2 (weights {weight_bytes / 1e6:.0f} MB streamed per step)",
-                   "parallelism": f"replicas x{world}",
-                   "launch": "direct wf_round calls" if args.no_graph else "wf_round captured in a CUDA graph"},
+        "config": round_config(cfg_name, cfg, wl, entropy, world),
+        "launch": "direct wf_round calls" if args.no_graph else "wf_round captured in a CUDA graph",
+        "ms_per_step_median": statistics.median(step_ms),
         "accepted_tokens_per_s": tot_acc / max_s,
         "mean_acceptance_length": accepted / B,
         "roofline": roof,
+        "samples": [{"round_ms": round(a, 5), "kernel_ms": round(b, 5), "sm_mhz": c}
+                    for a, b, c in zip(step_ms, k_ms_all, step_mhz)],
         "cpu_baseline": cpu,
         "e2e": {"value": tot_rows / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks,
-        "gpu_launches": launches_per_round * args.steps,
+        # the round's launches and the dominant kernel's own, every step of the timed region
+        "gpu_launches": (launches_per_round + kernel_launches) * args.steps,
         "impl": "ours",
     }
     print(json.dumps(line), flush=True)

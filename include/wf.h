@@ -156,13 +156,22 @@ WF_API wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int
  * process exits.  All calls on a device share it: calls that overlap on the
  * GPU race, so serialise them (one stream).  The first call on a device looks
  * up the array's address and should come before any stream capture.  It
- * allocates nothing; each call clears the part of the array it uses.
- * Device-side timeouts of this variant are not reported (its error word is
- * cleared by the next call).
+ * allocates nothing; each call clears the part of the array it uses,
+ * including the array's error word: read a call's device-side status with
+ * wf_noalloc_read_device_error before the next call on that device.
  */
 #define WF_NOALLOC_MAX_ROWS 16384
 WF_API wf_status wf_lmhead_argmax_noalloc(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
                                           int32_t* ids, float* maxlogit, wf_stream_t stream);
+
+/*
+ * The device-side status left by the last wf_lmhead_argmax_noalloc call on the
+ * current device (0, or WF_ERR_TIMEOUT if one of its bounded waits gave up;
+ * *info as in wf_read_device_error).  Synchronises `stream` first; clear != 0
+ * resets the word.  Like the entry point above, this has no counterpart on the
+ * pages.
+ */
+WF_API wf_status wf_noalloc_read_device_error(int* code, int* info, int clear, wf_stream_t stream);
 
 /*
  * Runtime-informed router, WhiFlash-Entropy (paper Sec. 3.3.1): at each
@@ -293,14 +302,23 @@ WF_API wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int 
  *   logits L[b,v] = sum_k x[b,k] * Wd[v,k], v < Vd
  *   for each b the k largest (logit desc, draft id asc):
  *   draft_ids[b,j] (optional), tids[b,j] = d2t[draft id], vals[b,j] = logit (fp32)
+ *   lse[b] = log sum_v exp(L[b,v]) over all Vd draft ids (optional)
+ *
+ * lse turns the top-k logits into the draft distribution's log-probabilities,
+ * vals[b,j] - lse[b], which EAGLE-3 tree construction accumulates along a
+ * branch (WhiFlash paper App. A "Drafter Hyperparameters", Table 7: depth 8,
+ * top-k 10, 60 draft tokens; see wf_build_tree).
  *
  * x device [B, d] bf16 bits (drafter hidden state); Wd device [Vd, d] bf16 bits;
  * d2t device [Vd] int32 absolute target ids; 1 <= k <= WF_MAX_TOPK, k <= Vd.
+ * Outputs device: draft_ids / tids [B, k] int32, vals [B, k] fp32, lse [B]
+ * fp32; each may be NULL, not all.  lse is fp32 (per-tile sums of e^(L - max)
+ * merged in a fixed order).
  * A d2t entry < 0 sets WF_ERR_BAD_DATA (info = b) and writes -1 for that id.
  */
 WF_API wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d,
-                        int Vd, int k, int32_t* draft_ids, int32_t* tids, float* vals, void* ws,
-                        size_t ws_bytes, wf_stream_t stream);
+                        int Vd, int k, int32_t* draft_ids, int32_t* tids, float* vals, float* lse,
+                        void* ws, size_t ws_bytes, wf_stream_t stream);
 
 /*
  * Both heads of a round in one weight sweep: the results of wf_lmhead_argmax
@@ -314,14 +332,14 @@ WF_API wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int3
  * fills the GPU poorly.  No passage corresponds to the fused call itself.
  *
  * Arguments as in wf_lmhead_argmax (hidden, W, P, d, V, ids, maxlogit) and
- * wf_draft_topk (x, Wd, d2t, B, Vd, k, draft_ids, tids, vals), one shared d.
+ * wf_draft_topk (x, Wd, d2t, B, Vd, k, draft_ids, tids, vals, lse), one shared d.
  * P <= 128 and B <= 128 (one activation tile each), else WF_ERR_UNSUPPORTED:
  * call the two entry points.  Workspace: wf_workspace_bytes(P, B, d, 0, Vd, k).
  */
 WF_API wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
                                int32_t* ids, float* maxlogit, const uint16_t* x, const uint16_t* Wd,
                                const int32_t* d2t, int B, int Vd, int k, int32_t* draft_ids,
-                               int32_t* tids, float* vals, void* ws, size_t ws_bytes,
+                               int32_t* tids, float* vals, float* lse, void* ws, size_t ws_bytes,
                                wf_stream_t stream);
 
 /*
@@ -375,6 +393,7 @@ typedef struct wf_round_args {
      * W1 / b1 / w2 / m are not read).  The entropy policy needs P <= 128 or
      * B <= 256. */
     int router_kind;
+    float* lse;                /* [B] draft head's log-sum-exp (as in wf_draft_topk) or NULL */
 } wf_round_args;
 
 #define WF_ROUTER_NEURAL 0

@@ -1,6 +1,7 @@
 // C ABI entry points: host-side validation, workspace layout and the
 // stream-ordered composition of one verify-and-route round.
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "wf_internal.cuh"
@@ -11,8 +12,8 @@ namespace wf {
 wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                float* maxlogit, void* ws, cudaStream_t s);
 wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
-                            int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t cand_off,
-                            cudaStream_t s);
+                            int32_t* draft_ids, int32_t* tids, float* vals, float* lse, void* ws, size_t cand_off,
+                            size_t lsep_off, cudaStream_t s);
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,
                         int default_kind, const int32_t* pos_off, const int32_t* node_off, int B, int P,
                         int path_stride, int32_t* n_accept, int32_t* bonus, int32_t* last_pos, int32_t* path,
@@ -34,16 +35,17 @@ wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t
                              void* ws, cudaStream_t s);
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
-                              size_t cand_off, int* num_n2_out, cudaStream_t s, float* H = nullptr,
+                              size_t cand_off, size_t lsep_off, int* num_n2_out, cudaStream_t s, float* H = nullptr,
                               float tau = 0.f, size_t ent_off = 0);
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
-                     float* vals, void* ws, size_t cand_off);
+                     float* vals, void* ws, size_t cand_off, float* lse = nullptr, size_t lsep_off = 0);
 wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
 wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cudaStream_t s);
 size_t catchup_workspace_bytes(int B, int N, int din, int H, int G, int D);
 size_t catchup_attend_smem(int H, int G, int D);
 wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, cudaStream_t s);
+wf_status noalloc_read_device_error(int* code, int* info, int clear, cudaStream_t s);
 
 static std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
@@ -78,6 +80,29 @@ static wf_status check_device() {
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A buffer the kernels read with the tensor-memory accelerator must be memory
+// of the current device itself (device or managed memory): a host pointer, or
+// another GPU's memory reached through a peer mapping, is refused before any
+// tensor map is built or anything enqueued.
+static bool local_device_memory(const void* p) {
+    if (!p) return true;   // optional operand not given
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();   // clear the error the failed query recorded
+        return false;
+    }
+    if (at.type == cudaMemoryTypeManaged) return true;
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+static wf_status check_local(std::initializer_list<const void*> ptrs) {
+    for (const void* p : ptrs)
+        if (!local_device_memory(p)) return WF_ERR_INVALID_ARG;
+    return WF_OK;
+}
 
 static wf_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return WF_ERR_WORKSPACE;
@@ -151,6 +176,7 @@ wf_status wf_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P, int
     if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
     WF_TRY(check_ws(ws, ws_bytes, layout(P, 0, d, 0, 0, 0).cand));   // control block and keys
     WF_TRY(check_device());
+    WF_TRY(check_local({hidden, W}));
     return launch_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, ws, stream);
 }
 
@@ -159,7 +185,14 @@ wf_status wf_lmhead_argmax_noalloc(const uint16_t* hidden, const uint16_t* W, in
     if (!hidden || !W || !ids || bad_gemm_shape(P, d, V) || P > WF_NOALLOC_MAX_ROWS) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W)) return WF_ERR_INVALID_ARG;
     WF_TRY(check_device());
+    WF_TRY(check_local({hidden, W}));
     return noalloc_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, stream);
+}
+
+wf_status wf_noalloc_read_device_error(int* code, int* info, int clear, wf_stream_t stream) {
+    if (!code) return WF_ERR_INVALID_ARG;
+    WF_TRY(check_device());
+    return noalloc_read_device_error(code, info, clear, stream);
 }
 
 wf_status wf_lmhead_entropy(const uint16_t* hidden, int P, int d, const int32_t* rows, int B, const uint16_t* W,
@@ -171,6 +204,7 @@ wf_status wf_lmhead_entropy(const uint16_t* hidden, int P, int d, const int32_t*
     const Layout L = layout(0, B, d, 0, 0, 0);
     WF_TRY(check_ws(ws, ws_bytes, rows ? L.total : L.gath));   // the gather area only when rows are given
     WF_TRY(check_device());
+    WF_TRY(check_local({hidden, W, rows ? ws : nullptr}));
     const uint16_t* act = hidden;
     if (rows) {
         uint16_t* gath = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.gath);
@@ -238,32 +272,36 @@ wf_status wf_router_mlp(const uint16_t* hidden, const int32_t* rows, int B, int 
 }
 
 wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
-                        int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t ws_bytes,
+                        int32_t* draft_ids, int32_t* tids, float* vals, float* lse, void* ws, size_t ws_bytes,
                         wf_stream_t stream) {
     if (!x || !Wd || !d2t || bad_gemm_shape(B, d, Vd)) return WF_ERR_INVALID_ARG;
-    if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals)) return WF_ERR_INVALID_ARG;
+    if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals && !lse)) return WF_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
     const Layout L = layout(0, B, d, 0, Vd, k);
-    WF_TRY(check_ws(ws, ws_bytes, L.part));   // up to the end of the top-k candidates
+    WF_TRY(check_ws(ws, ws_bytes, L.part));   // up to the end of the top-k candidates and their sums
     WF_TRY(check_device());
-    return launch_draft_topk(x, Wd, d2t, B, d, Vd, k, draft_ids, tids, vals, ws, L.cand, stream);
+    WF_TRY(check_local({x, Wd}));
+    return launch_draft_topk(x, Wd, d2t, B, d, Vd, k, draft_ids, tids, vals, lse, ws, L.cand, L.lsep, stream);
 }
 
 wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                float* maxlogit, const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B,
-                               int Vd, int k, int32_t* draft_ids, int32_t* tids, float* vals, void* ws,
+                               int Vd, int k, int32_t* draft_ids, int32_t* tids, float* vals, float* lse, void* ws,
                                size_t ws_bytes, wf_stream_t stream) {
     if (!hidden || !W || !ids || bad_gemm_shape(P, d, V)) return WF_ERR_INVALID_ARG;
     if (!x || !Wd || !d2t || bad_gemm_shape(B, d, Vd)) return WF_ERR_INVALID_ARG;
-    if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals)) return WF_ERR_INVALID_ARG;
+    if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals && !lse)) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W) || !aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
     if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
     const Layout L = layout(P, B, d, 0, Vd, k);
     WF_TRY(check_ws(ws, ws_bytes, L.part));   // control block, keys and top-k candidates
     WF_TRY(check_device());
+    WF_TRY(check_local({hidden, W, x, Wd}));
     int num_n2 = 0;
-    WF_TRY(launch_lmhead_draft(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, L.cand, &num_n2, stream));
-    return launch_topk_merge(merge_args(B, Vd, num_n2, k, d2t, draft_ids, tids, vals, ws, L.cand), ws, stream);
+    WF_TRY(launch_lmhead_draft(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, L.cand, lse ? L.lsep : 0,
+                               &num_n2, stream));
+    return launch_topk_merge(merge_args(B, Vd, num_n2, k, d2t, draft_ids, tids, vals, ws, L.cand, lse, L.lsep), ws,
+                             stream);
 }
 
 static bool bad_catchup_shape(int B, int N, int din, int H, int G, int D) {
@@ -290,7 +328,9 @@ static wf_status check_catchup(const wf_catchup_args* a, void* ws, size_t ws_byt
         return WF_ERR_INVALID_ARG;
     if (with_final && (!aligned16(a->Wq) || !aligned16(a->Wo))) return WF_ERR_INVALID_ARG;
     WF_TRY(check_ws(ws, ws_bytes, catchup_workspace_bytes(a->B, a->N, a->din, a->H, a->G, a->D)));
-    return check_device();
+    WF_TRY(check_device());
+    // the projections read the weights and the normalised rows (in the workspace) by TMA
+    return check_local({a->u, a->Wk, a->Wv, a->Wq, a->Wo, ws});
 }
 
 wf_status wf_catchup_kv(const wf_catchup_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {
@@ -324,6 +364,7 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
     const Layout L = layout(a->P, a->B, a->d, entropy ? 1 : a->m, draft ? a->Vd : 0, draft ? a->k : 0);
     WF_TRY(check_ws(ws, ws_bytes, L.total));
     WF_TRY(check_device());
+    WF_TRY(check_local({a->hidden, a->W, draft ? a->x : nullptr, draft ? a->Wd : nullptr, entropy ? ws : nullptr}));
     float* dall = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + L.dall);
     if (entropy && a->P <= ROUTE_ALL_ROWS_MAX) {
         // WhiFlash-Entropy, few rows: the LM-head sweep also yields the entropy
@@ -334,12 +375,13 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         int num_n2 = 0;
         if (shared)
             WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
-                                       a->Vd, a->k, ws, L.cand, &num_n2, stream, dall, a->tau, L.ent));
+                                       a->Vd, a->k, ws, L.cand, a->lse ? L.lsep : 0, &num_n2, stream, dall, a->tau,
+                                       L.ent));
         else
             WF_TRY(launch_lmhead_entropy(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, dall, nullptr,
                                          a->tau, nullptr, 0, ws, L.ent, stream));
         const MergeArgs mg = merge_args(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws,
-                                        L.cand);
+                                        L.cand, a->lse, L.lsep);
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
                              RoutePick{dall, a->tau, a->delta_al, a->route}, true, shared ? &mg : nullptr));
@@ -367,13 +409,13 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         int num_n2 = 0;
         if (shared)
             WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
-                                       a->Vd, a->k, ws, L.cand, &num_n2, stream));
+                                       a->Vd, a->k, ws, L.cand, a->lse ? L.lsep : 0, &num_n2, stream));
         else
             WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
         // the shared sweep's candidate lists are merged by extra CTAs of the
         // verification launch, beside the verification
         const MergeArgs mg = merge_args(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws,
-                                        L.cand);
+                                        L.cand, a->lse, L.lsep);
         const MergeArgs* mgp = shared ? &mg : nullptr;
         if (beside) {
             WF_TRY(launch_router(a->hidden, nullptr, a->P, a->d, a->m, a->P, a->W1, a->b1, a->w2, a->b2, a->tau, dall,
@@ -391,12 +433,12 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         if (shared) return WF_OK;
         if (draft)
             WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals,
-                                     ws, L.cand, stream));
+                                     a->lse, ws, L.cand, L.lsep, stream));
         return WF_OK;
     }
     if (draft)
-        WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals, ws,
-                                 L.cand, stream));
+        WF_TRY(launch_draft_topk(a->x, a->Wd, a->d2t, a->B, a->d, a->Vd, a->k, a->draft_ids, a->tids, a->vals,
+                                 a->lse, ws, L.cand, L.lsep, stream));
     return WF_OK;
 }
 

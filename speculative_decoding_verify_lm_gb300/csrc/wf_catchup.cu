@@ -1202,19 +1202,16 @@ static size_t proj_smem(int stages, int bn) {
 }
 
 static wf_status launch_proj(const CUtensorMap* mA, const CUtensorMap* mW, PjParams p, int tiles, cudaStream_t s) {
+    static std::mutex mu;
     static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        // Every catch-up kernel asks for the largest shared-memory carveout, so
-        // that an SM need not drain to switch it when the next kernel's CTAs
-        // arrive (they then start beside the previous kernel's last CTAs).
-        if (cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)proj_smem(PJ_STAGES, PJ_BN_CU)) != cudaSuccess ||
-            cudaFuncSetAttribute(proj_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-            return WF_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    // Every catch-up kernel asks for the largest shared-memory carveout, so
+    // that an SM need not drain to switch it when the next kernel's CTAs
+    // arrive (they then start beside the previous kernel's last CTAs).
+    CU_TRY(configure_once(mu, attr_set, [] {
+        return cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)proj_smem(PJ_STAGES, PJ_BN_CU)) == cudaSuccess &&
+               cudaFuncSetAttribute(proj_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+    }));
     // A three-stage ring lets two CTAs share an SM when the tile is narrow;
     // the partial tile ([BM][bn + 4] fp32) reuses the ring and must fit in it.
     int stages = 3;

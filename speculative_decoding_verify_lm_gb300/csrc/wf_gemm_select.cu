@@ -47,14 +47,13 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int GEMM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
-constexpr int GEMM_SMEM = STAGES * (A_BYTES + B_BYTES) + 1024 + 256;
 // Ring bytes with one activation tile: leaves room on the SM for the small
 // CTAs that run beside the sweep (the router over every row of a short round).
 constexpr int RING_BUDGET = 210 * 1024;
 constexpr int GEMM_SMEM_MAX = RING_BUDGET + 1024 + 256;
 constexpr int KT_TOPK = WF_MAX_TOPK;
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
-                     float* vals, void* ws, size_t cand_off);
+                     float* vals, void* ws, size_t cand_off, float* lse = nullptr, size_t lsep_off = 0);
 wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
 
 struct GemmParams {
@@ -75,6 +74,7 @@ struct GemmParams {
     int32_t* ids;      // argmax: [M_rows] out
     float* maxlogit;   // argmax: [M_rows] out or null
     uint64_t* cand;    // top-k: [tiles][BM][k]
+    float2* lsep;      // top-k: [tiles][BM] (max, sum e^(logit - max)) over the tile's columns, or null
     float4* ent;       // entropy: [M_rows][CTA slots] running (max, sum e^z, sum z e^z), z = logit - max
     float* H;          // entropy: [M_rows] out
     int32_t* route;    // entropy: [M_rows] out (H > tau) or null
@@ -108,17 +108,6 @@ __device__ __forceinline__ void ent_merge(float& M, float& S, float& T, float m2
     M = mx;
 }
 
-constexpr float LOG2E = 1.4426950408889634f;
-constexpr float LN2 = 0.6931471805599453f;
-
-// 2^x by the PTX approximate base-2 exponential (a few ulp of fp32; results
-// below the normal range flush to zero, which only drops terms under 2^-126
-// of the row maximum's).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // Insert (v, id) into a descending list of KT entries (earlier entry wins ties).
 template <int KT>
@@ -182,6 +171,20 @@ __device__ __forceinline__ void ent_fold(const uint32_t (&r)[32], int lim, float
         }
 }
 
+// Fold the columns j < lim of one chunk into a row's running (max lm, sum
+// ls = sum e^(v - lm)) over one tile; tv0 is the tile's largest column so far,
+// this chunk included.  Sums run in base 2 (the same terms: 2^((v - lm) log2 e)).
+__device__ __forceinline__ void lse_fold(const uint32_t (&r)[32], int lim, float tv0, float& lm, float& ls) {
+    if (tv0 > lm) {
+        if (ls > 0.f) ls *= ex2_approx((lm - tv0) * LOG2E);
+        lm = tv0;
+    }
+    const float off = lm * LOG2E;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j < lim) ls += ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, -off));
+}
+
 // One finished accumulator as epilogue thread rit sees it (activation row
 // m * BM + rit of a problem with M_rows rows and N_w weight rows): wait for
 // it, keep the row's best (KT = 1) or top KT over the tile's columns and, with
@@ -210,6 +213,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
         tv[j] = -INFINITY;
         ti[j] = 0;
     }
+    float lm = -INFINITY, ls = 0.f;   // top-k with log-sum-exp: this tile's (max, sum e^(v - max)) of the row
     if (quad_live) {
         const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
         if constexpr (KT == 1 && TAIL) {
@@ -260,6 +264,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
             // one load per wait and a left-to-right scan: fewer registers and
             // TMEM reads beside the MMAs of a tensor-bound sweep, whose tiles
             // are long enough to hide the epilogue
+            const bool want_lse = KT > 1 && p.lsep != nullptr;
             for (int c0 = 0; c0 < sp.rows; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tbase + c0, r);
@@ -281,6 +286,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
                     }
                 }
                 if constexpr (ENT) ent_fold(r, lim, tv[0], em, es, et);
+                if (want_lse) lse_fold(r, lim, tv[0], lm, ls);
             }
         }
     }
@@ -295,6 +301,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
             uint64_t* dst = p.cand + (t * BM + rit) * p.k;
             for (int j = 0; j < KT; ++j)
                 if (j < p.k) dst[j] = tv[j] == -INFINITY ? 0ull : pack_key(tv[j], (uint32_t)ti[j]);
+            if (p.lsep) p.lsep[t * BM + rit] = make_float2(lm, ls);
         }
     }
     return true;
@@ -313,27 +320,24 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
     return v < n2 ? U0 + v : v - n2;
 }
 
-// CL = 1: each CTA loads its own activation and weight boxes.
-// CL = 2: CTAs run in clusters of two on tile pairs (m, n) and (m + 1, n) that
-// share the weight tile: each CTA loads half of it and multicasts that half to
-// both, so every weight byte crosses the L2 -> SM crossbar once per pair.  A
-// stage is then written by both producers, so each CTA's "empty" barrier
-// counts the MMA completions of both CTAs.
+// Each CTA loads its own activation and weight boxes; tiles (m, n) are visited
+// in the order t = n * num_m + m, so the CTAs working at the same time share
+// the weight tile through L2.
 // ENT (with KT = 1): also accumulate, per row, the softmax statistics of the
 // logits so that the entropy of the next-token distribution comes out of the
 // same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
-// activation tiles).
-// DUAL (with KT = 1, CL = 1): tiles U0.. are the second problem's
+// activation tiles and a grid that is a multiple of their count).
+// DUAL (with KT = 1): tiles U0.. are the second problem's
 // (activation map tmA2, weight map tmB2, top-k into p.cand), swept first
 // (tile_order); with ENT the first problem's tiles also feed the entropy
 // statistics.
-template <int KT, int CL, bool ENT, bool DUAL>
+template <int KT, bool ENT, bool DUAL>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB2s,
                        const GemmParams p) {
-    static_assert(!DUAL || (KT == 1 && CL == 1), "the dual sweep pairs an argmax head with a top-k head");
+    static_assert(!DUAL || KT == 1, "the dual sweep pairs an argmax head with a top-k head");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
@@ -353,18 +357,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // tile pairs (CL = 2) or tiles (CL = 1): u -> (activation tile m, weight tile n)
-    const int rank = CL == 2 ? (int)cluster_ctarank() : 0;
-    const int slot = blockIdx.x / CL, nslots = gridDim.x / CL;
-    const int num_mp = (p.num_m + CL - 1) / CL;
-    const int U0 = num_mp * p.num_n;
+    // tiles: u -> (activation tile m = u % num_m, weight tile n = u / num_m)
+    const int slot = blockIdx.x, nslots = gridDim.x;
+    const int num_m = p.num_m;
+    const int U0 = num_m * p.num_n;
     const int U = U0 + (DUAL ? p.num_n2 : 0);
-    constexpr uint16_t kPair = 0x3;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CL);
+            mbar_init(&empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -389,7 +391,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CL == 2) cluster_sync();   // the peer's barriers exist before anything is multicast to them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // the prologue above overlaps the previous kernel on the stream; inputs and
@@ -403,7 +404,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_w = p.weight_evict_first ? policy_evict_first() : policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
-            const int half = p.bn / CL;                // weight rows this CTA fetches per stage (pairs: uniform tiles)
             uint32_t it = 0;  // stages issued so far
             int s = 0;        // = it % stages
             uint32_t ph = 0;  // = (it / stages) & 1
@@ -411,8 +411,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = slot; v < U && ok; v += nslots) {
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
-                const int m = second ? 0 : (u % num_mp) * CL + rank;
-                const int n = second ? u - U0 : u / num_mp;
+                const int m = second ? 0 : u % num_m;
+                const int n = second ? u - U0 : u / num_m;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const CUtensorMap* mA = second ? &tmA2 : &tmA;
@@ -432,11 +432,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                     mbar_arrive_expect_tx(&full[s], tx);
                     tma_load_2d(stA(s), mA, &full[s], kc * BK, m * BM, pol_a);
-                    if constexpr (CL == 2)
-                        tma_load_2d_multicast(stB(s) + rank * half * BK * 2, mB, &full[s], kc * BK,
-                                              sp.row0 + rank * half, kPair, pol_w);
-                    else
-                        tma_load_2d(stB(s), mB, &full[s], kc * BK, sp.row0, pol_w);
+                    tma_load_2d(stB(s), mB, &full[s], kc * BK, sp.row0, pol_w);
                 }
             }
             if (!ok || *abort_flag) {
@@ -455,7 +451,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = slot; v < U && ok; v += nslots, ++tile_i) {
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
-                const int n = second ? u - U0 : u / num_mp;
+                const int n = second ? u - U0 : u / num_m;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const uint32_t idesc = second ? (sp.big ? p.idesc2 : p.idesc2_s) : (sp.big ? p.idesc : p.idesc_s);
@@ -486,16 +482,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per step (encoded >> 4)
                         umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
-                    if constexpr (CL == 2)
-                        umma_commit_multicast(&empty[s], kPair);   // both CTAs wrote this stage
-                    else
-                        umma_commit(&empty[s]);
+                    umma_commit(&empty[s]);
                     issued = true;
                 }
                 if (ok) umma_commit(&tfull[acc]);
             }
-            if (issued && (!ok || CL == 2)) {
-                // every MMA issued above (and its arrivals, possibly on the peer) has completed
+            if (issued && !ok) {
+                // every MMA issued above has completed before the CTA frees its TMEM
                 umma_commit(drain);
                 mbar_wait(drain, 0, p.timeout_ns, nullptr);
             }
@@ -513,15 +506,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ok = epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
                                                    p.M_rows2, p.N_w2, 0, u - U0,
                                                    tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false), 1, em, es, et);
+            else if (num_m == 1)   // the weight-streaming sweep: the last tile's scan is exposed
+                ok = epilogue_tile<KT, ENT, true>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
+                                                  p.N_w, 0, u, tile_span(u, p.num_n, p.bn, p.nbig, true), 1, em, es,
+                                                  et);
             else
-                ok = epilogue_tile<KT, ENT, CL == 1>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
-                                            p.N_w, (u % num_mp) * CL + rank, u / num_mp,
-                                            tile_span(u / num_mp, p.num_n, p.bn, p.nbig, true), p.num_m, em, es, et);
+                ok = epilogue_tile<KT, ENT, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
+                                                   p.N_w, u % num_m, u / num_m,
+                                                   tile_span(u / num_m, p.num_n, p.bn, p.nbig, true), num_m, em, es,
+                                                   et);
             if (!ok) break;
         }
         if constexpr (ENT) {
-            // this CTA's rows are fixed (rank's activation tile); publish their statistics
-            const int row = rank * BM + rit;
+            // this CTA's rows are fixed (the grid is a multiple of num_m); publish their statistics
+            const int row = (slot % num_m) * BM + rit;
             if (row < p.M_rows) p.ent[(size_t)row * nslots + slot] = make_float4(em, es, et * LN2, 0.f);
         }
         if (KT == 1 && !*abort_flag) {
@@ -619,7 +617,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
     }
-    if constexpr (CL == 2) cluster_sync();   // the peer may still arrive on, or copy into, this CTA
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -725,50 +722,19 @@ static int set_ring(GemmParams& p, int one_tile_a_rows) {
     return p.stages * p.stage_bytes + 1024 + 256;
 }
 
-// Clusters of two that can be resident at once (queried once per device).
-template <int KT, bool ENT>
-static int pair_slots(int dev) {
-    static int cached[64];
-    if (dev < 64 && cached[dev]) return cached[dev];
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 64);
-    cfg.blockDim = dim3(GEMM_THREADS);
-    cfg.dynamicSmemBytes = GEMM_SMEM;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, 2, ENT, false>, &cfg) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = num_sms() / 2;
-    }
-    if (dev < 64) cached[dev] = n;
-    return n;
-}
-
 template <int KT, bool ENT>
 static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, GemmParams p,
                                cudaStream_t s, int* num_n_out = nullptr) {
+    static std::mutex mu;
     static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_select_kernel<KT, 1, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_MAX) != cudaSuccess ||
-            cudaFuncSetAttribute(gemm_select_kernel<KT, 2, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM) != cudaSuccess)
-            return WF_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    const wf_status cst = configure_once(mu, attr_set, [] {
+        return cudaFuncSetAttribute(gemm_select_kernel<KT, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    GEMM_SMEM_MAX) == cudaSuccess;
+    });
+    if (cst != WF_OK) return cst;
     CUtensorMap ta, tb, tbs;
     const int num_m = cdiv(M_rows, BM);
     if (ENT && num_m > 2) return WF_ERR_UNSUPPORTED;
-    // several activation tiles: pairs of CTAs share each weight tile (multicast)
-    const int CL = num_m > 1 ? 2 : 1;
     // With a single activation tile the box covers only the rows that exist
     // (rounded up to a whole 8-row swizzle atom): no zero rows cross the
     // crossbar.  The UMMA still reads all BM rows of the stage; rows past the
@@ -776,7 +742,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     const int a_rows = num_m == 1 ? (M_rows + 7) / 8 * 8 : BM;
     if (!make_map(&ta, act, (uint64_t)M_rows, (uint64_t)d, (uint32_t)a_rows)) return WF_ERR_CUDA;
     TileGeom tg;
-    if (CL == 1 && balanced_tiles(N_w, num_sms(), &tg)) {
+    if (balanced_tiles(N_w, num_sms(), &tg)) {
         p.num_n = tg.num_n;
         p.bn = tg.bn;
         p.nbig = tg.nbig;
@@ -786,8 +752,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
         p.nbig = p.num_n;
     }
     const int bn = p.bn;
-    // each CTA of a pair fetches half of the weight tile
-    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn / CL))) return WF_ERR_CUDA;
+    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)bn)) return WF_ERR_CUDA;
     tbs = tb;
     if (p.nbig < p.num_n && !make_map(&tbs, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn - 16))) return WF_ERR_CUDA;
     if (num_n_out) *num_n_out = p.num_n;
@@ -801,19 +766,14 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.a_bytes = a_rows * BK * 2;
     p.timeout_ns = wait_timeout_ns();
     const int smem = set_ring(p, num_m == 1 ? a_rows : 0);
-    if (CL == 1) {
-        const int tiles = p.num_m * p.num_n;
-        int grid = tiles < num_sms() ? tiles : num_sms();
-        if (ENT && grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
-        return launch(gemm_select_kernel<KT, 1, ENT, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta,
-                      tb, tbs, tbs, p);
+    const int tiles = p.num_m * p.num_n;
+    int grid = tiles < num_sms() ? tiles : num_sms();
+    if (ENT) {   // every CTA keeps the rows of one activation tile: a grid that is a multiple of num_m
+        if (grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
+        grid -= grid % num_m;
     }
-    const int pairs = cdiv(num_m, 2) * p.num_n;
-    int slots = pair_slots<KT, ENT>(dev);
-    if (ENT && slots > ENT_MAX_SLOTS) slots = ENT_MAX_SLOTS;
-    const int grid = 2 * (pairs < slots ? pairs : slots);
-    return launch_cluster(gemm_select_kernel<KT, 2, ENT, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, 2u, ta,
-                          tb, ta, tb, tb, tb, p);
+    return launch(gemm_select_kernel<KT, ENT, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta, tb, tbs,
+                  tbs, p);
 }
 
 static GemmParams params_for(void* ws) {
@@ -850,15 +810,17 @@ wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P
 }
 
 wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
-                            int32_t* draft_ids, int32_t* tids, float* vals, void* ws, size_t cand_off,
-                            cudaStream_t s) {
+                            int32_t* draft_ids, int32_t* tids, float* vals, float* lse, void* ws, size_t cand_off,
+                            size_t lsep_off, cudaStream_t s) {
     GemmParams p = params_for(ws);
     p.k = k;
     p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    p.lsep = lse ? reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws) + lsep_off) : nullptr;
     int num_n = 0;
     wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s, &num_n);
     if (st != WF_OK) return st;
-    return launch_topk_merge(merge_args(B, Vd, num_n, k, d2t, draft_ids, tids, vals, ws, cand_off), ws, s);
+    return launch_topk_merge(merge_args(B, Vd, num_n, k, d2t, draft_ids, tids, vals, ws, cand_off, lse, lsep_off),
+                             ws, s);
 }
 
 // Target LM head (argmax over P <= BM rows) and draft head (candidate lists of
@@ -867,20 +829,18 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
 // count this returns in *num_n2_out.
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
-                              size_t cand_off, int* num_n2_out, cudaStream_t s, float* H, float tau,
+                              size_t cand_off, size_t lsep_off, int* num_n2_out, cudaStream_t s, float* H, float tau,
                               size_t ent_off) {
     if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
+    static std::mutex mu;
     static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_select_kernel<1, 1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_MAX) != cudaSuccess ||
-            cudaFuncSetAttribute(gemm_select_kernel<1, 1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GEMM_SMEM_MAX) != cudaSuccess)
-            return WF_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    const wf_status cst = configure_once(mu, attr_set, [] {
+        return cudaFuncSetAttribute(gemm_select_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    GEMM_SMEM_MAX) == cudaSuccess &&
+               cudaFuncSetAttribute(gemm_select_kernel<1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    GEMM_SMEM_MAX) == cudaSuccess;
+    });
+    if (cst != WF_OK) return cst;
     const int sms = num_sms();
     GemmParams p = params_for(ws);
     // both matrices in balanced tiles (every CTA sweeps the same rows of each),
@@ -924,6 +884,7 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     p.maxlogit = maxlogit;
     p.k = k;
     p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    p.lsep = lsep_off ? reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws) + lsep_off) : nullptr;
     p.M_rows2 = B;
     p.N_w2 = Vd;
     p.a_bytes2 = a_rows2 * BK * 2;
@@ -940,19 +901,21 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
         p.src_rows = nullptr;
         p.src_P = 0;
         if (grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
-        return launch(gemm_select_kernel<1, 1, true, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2,
+        return launch(gemm_select_kernel<1, true, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2,
                       tb2, tbs, tb2s, p);
     }
-    return launch(gemm_select_kernel<1, 1, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2, tb2,
+    return launch(gemm_select_kernel<1, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2, tb2,
                   tbs, tb2s, p);
 }
 
 // The merge of the per-tile candidate lists of B rows (num_n weight tiles)
 // into the top k, mapped through d2t.
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
-                     float* vals, void* ws, size_t cand_off) {
+                     float* vals, void* ws, size_t cand_off, float* lse, size_t lsep_off) {
     MergeArgs a = {};
     a.cand = reinterpret_cast<const uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    a.lse = lse;
+    a.lsep = lse ? reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws) + lsep_off) : nullptr;
     a.B = B;
     a.num_m = cdiv(B, BM);
     a.num_n = num_n;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "wf.h"
@@ -31,7 +32,7 @@ static_assert(sizeof(Control) == 256, "control block is 256 bytes");
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t keys, cand, part, dall, ent, gath, total;
+    size_t keys, cand, lsep, part, dall, ent, gath, total;
 };
 
 // Entropy statistics are kept per CTA slot; the LM-head grid never exceeds this.
@@ -90,9 +91,13 @@ inline Layout layout(int P, int B, int d, int m, int Vd, int k) {
     L.keys = off;
     off = align_up(off + sizeof(uint64_t) * (size_t)(P > ent_rows ? P : ent_rows), 256);
     L.cand = off;
+    L.lsep = off;
     if (Vd > 0 && k > 0) {
         size_t tiles = (size_t)cdiv(B, BM) * (size_t)cdiv(Vd, BN_MIN);
         off = align_up(off + tiles * BM * (size_t)k * sizeof(uint64_t), 256);
+        // per tile and row: (max, sum of e^(logit - max)) over the tile's columns, for the log-sum-exp
+        L.lsep = off;
+        off = align_up(off + tiles * BM * sizeof(float2), 256);
     }
     L.part = off;
     const int routed = small_P > B ? small_P : B;
@@ -122,6 +127,21 @@ int num_sms();
 // TMA map of a [rows, cols] row-major bf16 matrix read in boxes of BK columns
 // (128 bytes, 128-byte swizzle) by box_rows rows
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+// One-time configuration of a call site's kernels on the current device
+// (cudaFuncSetAttribute and the like), done under the site's own lock so that
+// host threads making their first calls at the same time do not race on it.
+// `done` holds one flag per device (devices past 64 are configured every call).
+template <typename F>
+inline wf_status configure_once(std::mutex& mu, bool (&done)[64], F&& configure) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && done[dev]) return WF_OK;
+    if (!configure()) return WF_ERR_CUDA;
+    if (dev < 64) done[dev] = true;
+    return WF_OK;
+}
 
 // ----------------------------------------------------------------- launches
 // Every kernel is launched with programmatic stream serialization: it may be
@@ -194,6 +214,31 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+// 2^x by the PTX approximate base-2 exponential (a few ulp of fp32; results
+// below the normal range flush to zero, which only drops terms under 2^-126
+// of the row maximum's).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Merge two partial log-sum-exp states (M, S = sum e^(v - M)); S = 0 is empty.
+__device__ __forceinline__ void lse_merge(float& M, float& S, float m2, float s2) {
+    if (!(s2 > 0.f)) return;
+    if (!(S > 0.f)) {
+        M = m2;
+        S = s2;
+        return;
+    }
+    const float mx = fmaxf(M, m2);
+    S = S * ex2_approx((M - mx) * LOG2E) + s2 * ex2_approx((m2 - mx) * LOG2E);
+    M = mx;
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -245,16 +290,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-// Same, delivered to the same shared-memory offset (and mbarrier) of every
-// CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                                      int y, uint16_t cta_mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -313,15 +348,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-// Same, arriving on the mbarrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // 32 lanes x 32 columns of 32-bit words from TMEM: thread t gets its lane's 32 columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

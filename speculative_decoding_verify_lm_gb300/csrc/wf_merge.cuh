@@ -20,6 +20,8 @@ struct MergeArgs {
     int32_t* draft_ids;     // [B, k] or null
     int32_t* tids;          // [B, k] or null
     float* vals;            // [B, k] or null
+    float2* lsep;           // [num_n][num_m * BM] per-tile (max, sum e^(logit - max)), zeroed as read; or null
+    float* lse;             // [B] log-sum-exp of the row's logits over the draft vocabulary, or null
 };
 
 // One CTA (MERGE_THREADS threads) merges row `row`: every thread keeps the
@@ -32,6 +34,34 @@ __device__ __forceinline__ void topk_merge_row(const MergeArgs& a, int row, uint
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int m = row / BM, rit = row % BM;
     const int k = a.k;
+    if (a.lsep) {
+        // log-sum-exp over the draft vocabulary: every thread folds its tiles'
+        // (max, sum) pairs in increasing tile order, then a fixed shuffle tree
+        // and the warps in order (the same result on every run)
+        float M = -INFINITY, S = 0.f;
+        for (int n = threadIdx.x; n < a.num_n; n += MERGE_THREADS) {
+            float2* src = a.lsep + ((size_t)n * a.num_m + m) * BM + rit;
+            const float2 v = *src;
+            *src = make_float2(0.f, 0.f);   // leave the workspace zeroed
+            lse_merge(M, S, v.x, v.y);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+            const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
+            lse_merge(M, S, m2, s2);
+        }
+        float2* wl = reinterpret_cast<float2*>(wbest);   // MERGE_THREADS / 32 words of 8 bytes
+        if (lane == 0) wl[warp] = make_float2(M, S);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float Mt = -INFINITY, St = 0.f;
+#pragma unroll
+            for (int w = 0; w < MERGE_THREADS / 32; ++w) lse_merge(Mt, St, wl[w].x, wl[w].y);
+            a.lse[row] = St > 0.f ? Mt + logf(St) : __int_as_float(0x7fc00000);
+        }
+        __syncthreads();   // wbest is reused below
+    }
     uint64_t loc[KT];
 #pragma unroll
     for (int j = 0; j < KT; ++j) loc[j] = 0;

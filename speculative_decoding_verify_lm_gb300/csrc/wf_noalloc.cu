@@ -63,4 +63,23 @@ wf_status noalloc_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P
     return launch_lmhead_argmax(hidden, W, P, d, V, ids, maxlogit, scratch, s);
 }
 
+// The error word of the array's control block (a bounded wait that gave up
+// records WF_ERR_TIMEOUT there): copied out after the work before it on the
+// stream, optionally cleared.
+wf_status noalloc_read_device_error(int* code, int* info, int clear, cudaStream_t s) {
+    void* scratch = nullptr;
+    const wf_status st = noalloc_scratch(&scratch);
+    if (st != WF_OK) return st;
+    uint32_t h[2] = {0, 0};
+    if (cudaMemcpyAsync(h, scratch, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return WF_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return WF_ERR_CUDA;
+    *code = (int)h[0];
+    if (info) *info = (int)h[1];
+    if (clear) {
+        if (cudaMemsetAsync(scratch, 0, sizeof h, s) != cudaSuccess) return WF_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return WF_ERR_CUDA;
+    }
+    return WF_OK;
+}
+
 }  // namespace wf

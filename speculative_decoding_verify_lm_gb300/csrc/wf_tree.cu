@@ -157,15 +157,13 @@ wf_status launch_build_tree(const int32_t* tid, const float* lp, int B, int D, i
                             int32_t* token, float* score, int32_t* depth, void* ws, cudaStream_t s) {
     if (B == 0) return WF_OK;
     const size_t smem = build_tree_smem(D, k);
+    static std::mutex mu;
     static bool attr_set[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-            cudaSuccess)
-            return WF_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    const wf_status cst = configure_once(mu, attr_set, [] {
+        return cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+               cudaSuccess;
+    });
+    if (cst != WF_OK) return cst;
     return launch(build_tree_kernel, dim3(cdiv(B, TREE_WARPS)), dim3(TREE_WARPS * 32), smem, s, tid, lp, B, D, k, N,
                   parent, token, score, depth, reinterpret_cast<Control*>(ws));
 }

@@ -180,6 +180,9 @@ class Workload:
     d2t: Optional[np.ndarray] = None  # [Vd] int32
     topk: int = 0
     path_nodes: list = dataclasses.field(default_factory=list)  # per sequence: planted root path (tree)
+    # rejection record: final resample attempt of each resampled hidden row / drafter row
+    hidden_attempts: dict = dataclasses.field(default_factory=dict)
+    x_attempts: dict = dataclasses.field(default_factory=dict)
 
     @property
     def P(self) -> int:
@@ -385,7 +388,59 @@ def make_workload(index: int, argmax_fn: ArgmaxFn, router_fn: Optional[RouterFn]
                 todo = bad
             else:
                 raise RuntimeError("draft top-k gap rule not met")
+            wl.x_attempts = dict(xa)
+    wl.hidden_attempts = dict(attempts)
     return wl
+
+
+def replay_workload(index: int, hidden_attempts: dict, x_attempts: dict, tok: np.ndarray,
+                    m: Optional[int] = None) -> Workload:
+    """Rebuild workload ``index`` as ``make_workload`` left it, from its record:
+    the final resample attempt of each rejected hidden row and drafter row and
+    the drafted tokens (which ``make_workload`` planted from the target argmax).
+    Everything else is redrawn from the seed, so no argmax is needed here."""
+    cfg = CONFIGS[index]
+    seed = seed_of(index)
+    B = cfg.B
+    m = cfg.m if m is None else m
+    d, V = cfg.d, cfg.V
+    kinds, parents, paths, cuts, pos_off, node_off = _structure(cfg, seed, B)
+    P = int(pos_off[-1])
+    W = normal_bf16(seed, _T_W, V, d, cfg.w_std)
+    hidden = normal_bf16(seed, _T_HID, P, d, 1.0)
+    for row, a in hidden_attempts.items():
+        hidden[int(row)] = hidden_row(seed, int(row), int(a), d)
+    rr = _rng(seed, _T_ROUTER)
+    W1 = (rr.standard_normal((m, d), dtype=np.float32) * np.float32(cfg.r_std))
+    b1 = (rr.standard_normal(m, dtype=np.float32) * np.float32(cfg.r_std))
+    w2 = (rr.standard_normal(m, dtype=np.float32) * np.float32(cfg.r_std))
+    b2 = float(np.float32(rr.standard_normal() * cfg.r_std))
+    tok = np.asarray(tok, np.int32)
+    if len(tok) != int(node_off[-1]):
+        raise ValueError(f"record holds {len(tok)} drafted tokens, the workload has {int(node_off[-1])}")
+    wl = Workload(cfg=cfg, seed=seed, hidden=hidden, W=W, pos_off=pos_off, node_off=node_off,
+                  kind=kinds, tok=tok.copy(), parent=np.concatenate(parents).astype(np.int32), W1=W1, b1=b1,
+                  w2=w2, b2=b2, tau=cfg.tau, cut=cuts, planted=np.ones(B, bool),
+                  max_depth=cfg.K if cfg.kind == "chain" else (cfg.depth if cfg.kind == "tree" else max(cfg.K, cfg.depth)),
+                  path_nodes=paths, hidden_attempts={int(k): int(v) for k, v in hidden_attempts.items()},
+                  x_attempts={int(k): int(v) for k, v in x_attempts.items()})
+    if cfg.draft_head:
+        wl.Wd = normal_bf16(seed, _T_WD, cfg.Vd, d, cfg.w_std)
+        wl.x = normal_bf16(seed, _T_X, B, d, 1.0)
+        for b, a in x_attempts.items():
+            wl.x[int(b)] = hidden_row(seed, int(b), int(a), d, tag=_T_X_RS)
+        wl.d2t = _rng(seed, _T_D2T).choice(V, size=cfg.Vd, replace=False).astype(np.int32)
+        wl.topk = cfg.topk
+    return wl
+
+
+def workload_from_record(rec: dict, m: Optional[int] = None) -> Workload:
+    """``replay_workload`` from a stored record: a dict with the workload index
+    and an ``inputs`` entry holding ``hidden_attempts`` and ``x_attempts`` as
+    [row, attempt] pairs and the drafted tokens ``tok``."""
+    inp = rec["inputs"]
+    return replay_workload(int(rec["index"]), {r: a for r, a in inp["hidden_attempts"]},
+                           {b: a for b, a in inp["x_attempts"]}, np.array(inp["tok"], np.int32), m=m)
 
 
 def small_workload(seed: int, d: int, V: int, kinds: list, argmax_fn: ArgmaxFn,

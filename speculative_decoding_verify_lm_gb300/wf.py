@@ -50,6 +50,7 @@ class RoundArgs(ctypes.Structure):
         ("ids", _c_void_p), ("maxlogit", _c_void_p), ("n_accept", _c_void_p), ("bonus", _c_void_p),
         ("last_pos", _c_void_p), ("path", _c_void_p), ("delta_al", _c_void_p), ("route", _c_void_p),
         ("draft_ids", _c_void_p), ("tids", _c_void_p), ("vals", _c_void_p), ("router_kind", _i32),
+        ("lse", _c_void_p),
     ]
 
 
@@ -80,6 +81,7 @@ _SIGS = {
     "wf_lmhead_argmax": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _sz,
                                 _c_void_p]),
     "wf_lmhead_argmax_noalloc": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p]),
+    "wf_noalloc_read_device_error": (_i32, [ctypes.POINTER(_i32), ctypes.POINTER(_i32), _i32, _c_void_p]),
     "wf_build_tree": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                              _c_void_p, _sz, _c_void_p]),
     "wf_accepted_rows": (_i32, [_c_void_p, _c_void_p, _i32, _c_void_p, _i32, _c_void_p, _c_void_p, _c_void_p, _i32,
@@ -91,10 +93,10 @@ _SIGS = {
     "wf_router_mlp": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p, _f32, _f32,
                              _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "wf_draft_topk": (_i32, [_c_void_p, _c_void_p, _c_void_p, _i32, _i32, _i32, _i32, _c_void_p, _c_void_p,
-                             _c_void_p, _c_void_p, _sz, _c_void_p]),
+                             _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
     "wf_lmhead_draft_topk": (_i32, [_c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
                                     _c_void_p, _c_void_p, _i32, _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
-                                    _c_void_p, _sz, _c_void_p]),
+                                    _c_void_p, _c_void_p, _sz, _c_void_p]),
     "wf_round": (_i32, [ctypes.POINTER(RoundArgs), _c_void_p, _sz, _c_void_p]),
     "wf_catchup_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32]),
     "wf_catchup_kv": (_i32, [ctypes.POINTER(CatchupArgs), _c_void_p, _sz, _c_void_p]),
@@ -243,6 +245,14 @@ def wf_lmhead_argmax_noalloc(hidden, W, ids=None, maxlogit=None, stream=None):
     return ids
 
 
+def wf_noalloc_read_device_error(clear: bool = True, stream=None):
+    """(code, info) left on the device by the last wf_lmhead_argmax_noalloc call."""
+    code, info = _i32(0), _i32(0)
+    _raise(lib().wf_noalloc_read_device_error(ctypes.byref(code), ctypes.byref(info), int(clear), _stream(stream)),
+           "wf_noalloc_read_device_error")
+    return code.value, info.value
+
+
 def wf_build_tree(tid, lp, N: int, ws: Workspace, parent=None, token=None, score=None, depth=None, stream=None):
     """EAGLE-3 draft tree from per-step, per-slot top-k children -> (parent, token, score, depth) [B, N].
     Outputs not given are allocated."""
@@ -344,7 +354,10 @@ def wf_router_mlp(hidden, rows, W1, b1, w2, b2: float, tau: float, ws: Workspace
     return delta_al, route
 
 
-def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, vals=None, stream=None):
+def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, vals=None, lse=None,
+                  stream=None):
+    """-> (draft_ids, tids, vals); pass ``lse`` (a [B] fp32 tensor) to also receive
+    each row's log-sum-exp over the draft vocabulary."""
     B, d = x.shape
     Vd = Wd.shape[0]
     dev = x.device
@@ -353,13 +366,14 @@ def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, 
     vals = torch.empty((B, k), dtype=torch.float32, device=dev) if vals is None else vals
     st = lib().wf_draft_topk(_check(x, "x", _BF16), _check(Wd, "Wd", _BF16), _check(d2t, "d2t", _I32), B, d, Vd, k,
                              _check(draft_ids, "draft_ids", _I32), _check(tids, "tids", _I32),
-                             _check(vals, "vals", _F32), ws.ptr, ws.nbytes, _stream(stream))
+                             _check(vals, "vals", _F32), _check(lse, "lse", _F32, True), ws.ptr, ws.nbytes,
+                             _stream(stream))
     _raise(st, "wf_draft_topk")
     return draft_ids, tids, vals
 
 
 def wf_lmhead_draft_topk(hidden, W, x, Wd, d2t, k: int, ws: Workspace, ids=None, maxlogit=None, draft_ids=None,
-                         tids=None, vals=None, stream=None):
+                         tids=None, vals=None, lse=None, stream=None):
     """Target argmax over the rows of hidden and draft top-k over the rows of x
     in one weight sweep (at most 128 rows each)."""
     P, d = hidden.shape
@@ -377,7 +391,8 @@ def wf_lmhead_draft_topk(hidden, W, x, Wd, d2t, k: int, ws: Workspace, ids=None,
                                     _check(ids, "ids", _I32), _check(maxlogit, "maxlogit", _F32, True),
                                     _check(x, "x", _BF16), _check(Wd, "Wd", _BF16), _check(d2t, "d2t", _I32), B, Vd,
                                     k, _check(draft_ids, "draft_ids", _I32), _check(tids, "tids", _I32),
-                                    _check(vals, "vals", _F32), ws.ptr, ws.nbytes, _stream(stream))
+                                    _check(vals, "vals", _F32), _check(lse, "lse", _F32, True), ws.ptr, ws.nbytes,
+                                    _stream(stream))
     _raise(st, "wf_lmhead_draft_topk")
     return ids, draft_ids, tids, vals
 
@@ -508,10 +523,10 @@ class Round:
             out_spec.append(("maxlogit", torch.float32, (P,)))
         if draft:
             out_spec += [("draft_ids", torch.int32, (B, k)), ("tids", torch.int32, (B, k)),
-                         ("vals", torch.float32, (B, k))]
+                         ("vals", torch.float32, (B, k)), ("lse", torch.float32, (B,))]
         self.out_buf, outs = _packed(out_spec, dev)
         self.out = {name: outs.get(name) for name in ("ids", "n_accept", "bonus", "last_pos", "path", "delta_al",
-                                                      "route", "maxlogit", "draft_ids", "tids", "vals")}
+                                                      "route", "maxlogit", "draft_ids", "tids", "vals", "lse")}
         self._in_spec, self._out_spec = in_spec, out_spec
         a = RoundArgs()
         a.hidden = _check(hidden, "hidden", _BF16)
@@ -536,7 +551,7 @@ class Round:
         a.k = k if Wd is not None else 0
         a.router_kind = int(router_kind)
         for name in ("ids", "maxlogit", "n_accept", "bonus", "last_pos", "path", "delta_al", "route", "draft_ids",
-                     "tids", "vals"):
+                     "tids", "vals", "lse"):
             t = self.out[name]
             setattr(a, name, t.data_ptr() if t is not None else None)
         self.args = a

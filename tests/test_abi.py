@@ -59,12 +59,13 @@ NULL = None
     ("wf_verify_tree", (256, 256, NULL, 256, 256, 1, 0, 256, 256, 256, NULL, 256, 1 << 20, NULL)),
     ("wf_verify_chain", (256, 256, 256, 256, -1, 0, 256, 256, 256, NULL, 256, 1 << 20, NULL)),
     ("wf_router_mlp", (256, 256, 1, 64, 0, 256, 256, 256, 0.0, 1.0, 256, 256, 256, 1 << 20, NULL)),  # m = 0
-    ("wf_draft_topk", (256, 256, 256, 1, 64, 100, 17, 256, 256, 256, 256, 1 << 20, NULL)),          # k > 16
-    ("wf_draft_topk", (256, 256, 256, 1, 64, 5, 6, 256, 256, 256, 256, 1 << 20, NULL)),             # k > Vd
-    ("wf_lmhead_draft_topk", (256, 256, 4, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 0, NULL, 256, 256, 256,
-                              1 << 20, NULL)),                                                     # k = 0
-    ("wf_lmhead_draft_topk", (256, 256, 4, 64, 100, 256, NULL, 264, 256, 256, 1, 50, 4, NULL, 256, 256, 256,
-                              1 << 20, NULL)),                                                     # misaligned x
+    ("wf_draft_topk", (256, 256, 256, 1, 64, 100, 17, 256, 256, 256, NULL, 256, 1 << 20, NULL)),    # k > 16
+    ("wf_draft_topk", (256, 256, 256, 1, 64, 5, 6, 256, 256, 256, NULL, 256, 1 << 20, NULL)),       # k > Vd
+    ("wf_draft_topk", (256, 256, 256, 1, 64, 100, 4, NULL, NULL, NULL, NULL, 256, 1 << 20, NULL)),  # no output
+    ("wf_lmhead_draft_topk", (256, 256, 4, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 0, NULL, 256, 256, NULL,
+                              256, 1 << 20, NULL)),                                                # k = 0
+    ("wf_lmhead_draft_topk", (256, 256, 4, 64, 100, 256, NULL, 264, 256, 256, 1, 50, 4, NULL, 256, 256, NULL,
+                              256, 1 << 20, NULL)),                                                # misaligned x
 ])
 def test_invalid_arguments_rejected_on_host(call, args):
     assert getattr(wf.lib(), call)(*args) == 1
@@ -79,10 +80,10 @@ def test_workspace_checked_on_host(ws, nbytes):
 def test_shared_sweep_limited_to_one_activation_tile():
     # more than 128 rows in either head: unsupported, nothing enqueued (no device needed)
     L = wf.lib()
-    assert L.wf_lmhead_draft_topk(256, 256, 129, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 4, NULL, 256, 256, 256,
-                                  1 << 20, NULL) == 4
-    assert L.wf_lmhead_draft_topk(256, 256, 128, 64, 100, 256, NULL, 256, 256, 256, 129, 50, 4, NULL, 256, 256,
+    assert L.wf_lmhead_draft_topk(256, 256, 129, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 4, NULL, 256, 256, NULL,
                                   256, 1 << 20, NULL) == 4
+    assert L.wf_lmhead_draft_topk(256, 256, 128, 64, 100, 256, NULL, 256, 256, 256, 129, 50, 4, NULL, 256, 256,
+                                  NULL, 256, 1 << 20, NULL) == 4
 
 
 def test_catchup_shapes_checked_on_host():

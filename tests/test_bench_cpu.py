@@ -69,12 +69,33 @@ def test_reference_arm_matches_own_arm(mode, metric):
     from speculative_decoding_verify_lm_gb300 import synth
     if metric == "METRIC":
         cfg = synth.CONFIGS[0]
-        wl = synth.make_workload(0, oracle.argmax_fn, reject=False, plant_seqs=[0])
+        wl = bench.load_workload(0)
         entropy = "entropy" in mode
-        want = bench.round_config(cfg.name + ("_entropy" if entropy else ""), cfg, wl, entropy)
+        want = bench.round_config(cfg.name + ("_entropy" if entropy else ""), cfg, wl, entropy, 1)
         assert j["unit"] == bench.UNIT
+        assert j["config"] == want   # exactly the keys the GPU arm prints
     else:
         want = bench.catchup_config(synth.CATCHUP_CONFIGS[0])
         assert j["unit"] == "backlog tokens/s"
     for k, v in want.items():
         assert j["config"][k] == v, k
+
+
+def test_round_launch_count_follows_the_composition():
+    """The launch count a round line claims, per wf_round's composition."""
+    assert bench.round_launches(17, 1, False, False) == 3       # LM head, router beside it, acceptance
+    assert bench.round_launches(61, 1, True, False) == 3        # both heads in one sweep, acceptance + merge, router
+    assert bench.round_launches(1248, 32, False, False) == 4    # LM head, acceptance, router GEMM + finish
+    assert bench.round_launches(15616, 256, True, False) == 6   # ... plus the draft head's sweep and merge
+    assert bench.round_launches(17, 1, False, True) == 2        # entropy sweep, acceptance
+    assert bench.round_launches(15616, 256, True, True) == 6    # LM head, acceptance, gather, entropy sweep, draft head
+
+
+def test_bench_workload_is_the_stored_record():
+    """Both arms rebuild the inputs the oracle's stored answers were computed on."""
+    import sys as _s
+    _s.path.insert(0, os.path.join(ROOT, "tests", "golden"))
+    import make_full_goldens as fg
+    rec = fg.load(1)
+    wl = bench.load_workload(1)
+    assert fg.input_hashes(wl) == rec["inputs"]["sha256"]

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import DEV, check_round_properties, dev, host, logit_error_bound, round_on_gpu
+from gpu_util import DEV, dev, host, logit_error_bound, round_on_gpu
 from speculative_decoding_verify_lm_gb300 import synth, wf
 
 pytestmark = pytest.mark.gpu
@@ -173,15 +173,28 @@ def _draft_case(B, d, Vd, k):
     Wd = synth.normal_bf16(Vd + d, 0, Vd, d, 0.02 if d >= 2560 else 4.0 / d ** 0.5)
     d2t = np.random.default_rng(Vd).permutation(151936)[:Vd].astype(np.int32)
     x = synth.normal_bf16(B + 1, 1, B, d, 1.0)
-    for a in range(1, 400):
-        dids, tids, vals, _, mg = o().draft_topk(x, Wd, d2t, k)
+    dids, tids, vals, lse, mg = o().draft_topk(x, Wd, d2t, k)
+    for a in range(1, 400):   # resample the offending rows only
         bad = np.nonzero(mg < synth.GAP_MIN)[0]
         if not len(bad):
             break
         for r in bad:
             x[r] = synth.hidden_row(B + 1, int(r), a, d)
+        got = o().draft_topk(x[bad], Wd, d2t, k)
+        for full, part in zip((dids, tids, vals, lse, mg), got):
+            full[bad] = part
     assert (mg >= synth.GAP_MIN).all(), "gap rule not met: expected ids would be stale"
+    _lse_ref[id(x)] = lse
     return Wd, d2t, x, dids, tids, vals
+
+
+_lse_ref = {}   # the oracle's log-sum-exp of each _draft_case's rows, by the x array
+
+
+def _check_lse(got, x):
+    """Log-sum-exp over the draft vocabulary: fp32 partial sums of e^(L - max)
+    per tile, merged in fp32; well within 1e-3 of the fp64 value at these sizes."""
+    assert np.max(np.abs(got - _lse_ref[id(x)])) <= 1e-3
 
 
 @pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
@@ -189,12 +202,15 @@ def _draft_case(B, d, Vd, k):
 def test_draft_topk(B, d, Vd, k):
     Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
     ws = wf.Workspace(1, B, 1, Vd, k)
-    for _ in range(2):
-        gi, gt, gv = wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), k, ws)
+    lse = torch.empty(B, dtype=torch.float32, device=DEV)
+    for it in range(3):   # with the log-sum-exp, without it, with it again (the workspace stays clean)
+        gi, gt, gv = wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), k, ws, lse=lse if it != 1 else None)
         torch.cuda.synchronize()
         assert np.array_equal(host(gi), dids) and np.array_equal(host(gt), tids)
         bound = np.stack([logit_error_bound(x[b:b + 1].repeat(k, 0), Wd, dids[b]) for b in range(B)])
         assert np.all(np.abs(host(gv) - vals) <= bound)
+        if it != 1:
+            _check_lse(host(lse), x)
     assert ws.device_error() == (0, 0)
     assert not ws.buf.any().item()
 
@@ -211,9 +227,13 @@ def test_lmhead_draft_topk_shared_sweep(P, B, d, V, Vd, k):
     Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
     ws = wf.Workspace(P, B, 1, Vd, k, d=d)
     mx = torch.empty(P, dtype=torch.float32, device=DEV)
-    for _ in range(2):
-        ids, gi, gt, gv = wf.wf_lmhead_draft_topk(dev(h), dev(W), dev(x), dev(Wd), dev(d2t), k, ws, maxlogit=mx)
+    lse = torch.empty(B, dtype=torch.float32, device=DEV)
+    for it in range(2):
+        ids, gi, gt, gv = wf.wf_lmhead_draft_topk(dev(h), dev(W), dev(x), dev(Wd), dev(d2t), k, ws, maxlogit=mx,
+                                                  lse=lse if it == 0 else None)
         torch.cuda.synchronize()
+        if it == 0:
+            _check_lse(host(lse), x)
         assert np.array_equal(host(ids), ids_ref)
         assert np.all(np.abs(host(mx) - mx_ref) <= logit_error_bound(h, W, ids_ref))
         assert np.array_equal(host(gi), dids) and np.array_equal(host(gt), tids)
@@ -244,78 +264,8 @@ def _compare_round(wl, out, seqs=None):
     assert np.array_equal(out["n_accept"][wl.planted], wl.cut[wl.planted])
 
 
-@pytest.mark.parametrize("index", [0, 1, 2])
-def test_round_batch1_configs(index):
-    wl = synth.make_workload(index, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn)
-    r, out = round_on_gpu(wl)
-    assert r.ws.device_error() == (0, 0)
-    _compare_round(wl, out)
-    check_round_properties(wl, out)
-    if wl.Wd is not None:
-        dids, tids, vals, _, _ = o().draft_topk(wl.x, wl.Wd, wl.d2t, wl.topk)
-        assert np.array_equal(out["draft_ids"], dids) and np.array_equal(out["tids"], tids)
-    # a second round on the same workspace gives the same answer
-    out2 = {k: host(v) for k, v in r().items()}
-    for key in ("ids", "n_accept", "bonus", "route"):
-        assert np.array_equal(out2[key], out[key])
-
-
-def test_round_entropy_tree_b1_full_size():
-    """The EAGLE-3 tree round at full size (V = 151,936, draft head over 32,000)
-    under WhiFlash-Entropy routing: the entropy statistics ride the shared
-    sweep of both heads on its evened-out tiles."""
-    wl = synth.make_workload(2, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn)
-    ref = o().round_(wl.hidden, wl.W, wl.pos_off, wl.node_off, wl.kind, wl.tok, wl.parent, wl.W1, wl.b1, wl.w2,
-                     wl.b2, wl.tau, wl.max_depth)
-    H_ref, _ = o().entropy(wl.hidden, ref["last_pos"], wl.W)
-    tau = float(H_ref[0]) - 0.05
-    r = wf.Round(dev(wl.hidden), dev(wl.W), dev(wl.pos_off), dev(wl.node_off), dev(wl.tok), dev(wl.W1),
-                 dev(wl.b1), dev(wl.w2), wl.b2, tau, kind=dev(wl.kind), parent=dev(wl.parent),
-                 path_stride=wl.max_depth, x=dev(wl.x), Wd=dev(wl.Wd), d2t=dev(wl.d2t), k=wl.topk,
-                 router_kind=wf.WF_ROUTER_ENTROPY)
-    for _ in range(2):
-        out = {k: host(v) for k, v in r().items()}
-        torch.cuda.synchronize()
-        for key in ("ids", "n_accept", "bonus", "last_pos", "path"):
-            assert np.array_equal(out[key], ref[key]), key
-        assert np.max(np.abs(out["delta_al"] - H_ref)) <= 1e-3 and out["route"][0] == 1
-        dids, tids, _, _, _ = o().draft_topk(wl.x, wl.Wd, wl.d2t, wl.topk)
-        assert np.array_equal(out["draft_ids"], dids) and np.array_equal(out["tids"], tids)
-    assert r.ws.device_error() == (0, 0)
-
-
-def _sampled_round(index, plant):
-    wl = synth.make_workload(index, oracle.argmax_fn, oracle.router_fn, oracle.topk_gap_fn, plant_seqs=plant)
-    r, out = round_on_gpu(wl)
-    assert r.ws.device_error() == (0, 0)
-    check_round_properties(wl, out)
-    rows = np.concatenate([np.arange(wl.pos_off[b], wl.pos_off[b + 1]) for b in plant])
-    ids, _, _ = o().lmhead_argmax(wl.hidden[rows], wl.W)
-    assert np.array_equal(out["ids"][rows], ids)
-    assert np.array_equal(out["n_accept"][plant], wl.cut[plant])
-    last = np.array([wl.expected_last_pos(b) for b in plant], np.int32)
-    assert np.array_equal(out["last_pos"][plant], last)
-    delta, route = o().router(wl.hidden, last, wl.W1, wl.b1, wl.w2, wl.b2, wl.tau)
-    assert np.max(np.abs(out["delta_al"][plant] - delta)) <= 1e-3
-    assert np.array_equal(out["route"][plant], route)
-    # router at every sequence's own last row (GPU rows, oracle arithmetic)
-    delta_all, _ = o().router(wl.hidden, out["last_pos"], wl.W1, wl.b1, wl.w2, wl.b2, wl.tau)
-    assert np.max(np.abs(out["delta_al"] - delta_all)) <= 1e-3
-    return wl, out
-
-
-def test_round_mixed_batch32_sampled():
-    wl0 = synth._structure(synth.CONFIGS[3], synth.seed_of(3), 32)[0]
-    chains = [b for b in range(32) if wl0[b] == 0][:2]
-    trees = [b for b in range(32) if wl0[b] == 1][:2]
-    _sampled_round(3, chains + trees)
-
-
-def test_round_batch256_sampled():
-    wl, out = _sampled_round(4, [0, 137, 255])
-    xs = [0, 137, 255]
-    dids, tids, _, _, _ = o().draft_topk(wl.x[xs], wl.Wd, wl.d2t, wl.topk)
-    assert np.array_equal(out["draft_ids"][xs], dids) and np.array_equal(out["tids"][xs], tids)
+# The five round workloads at full size are compared with the oracle's stored
+# answers in test_full_size_gpu.py.
 
 
 @pytest.mark.parametrize("kinds,K,d,V,Vd,k", [([1], 16, 128, 3000, 1000, 10), ([0, 1], 16, 64, 777, 301, 16),
@@ -481,6 +431,42 @@ def test_verify_right_after_tree_construction():
         torch.cuda.synchronize()
         assert np.array_equal(host(n), ref[0]) and np.array_equal(host(bo), ref[1])
         assert np.array_equal(host(la), ref[2]) and np.array_equal(host(pa), ref[3])
+    assert ws.device_error() == (0, 0)
+
+
+def test_draft_head_to_tree_construction_chain():
+    """The draft head feeds tree construction on one stream: top-10 target ids
+    and logits over the 32,000-id draft vocabulary with the log-sum-exp
+    (wf_draft_topk), log-probabilities = logits - lse, then the depth-8,
+    60-node tree (wf_build_tree) - the EAGLE-3 settings (WhiFlash paper App. A
+    Table 7; Qwen3-4B-EAGLE3 card, "Factors").  Each (sequence, step, slot)
+    has its own drafter state.  The oracle runs the same chain in fp64; its
+    tree is first checked to stay the same under perturbations of the
+    log-probabilities well above the fp32 error, so that the comparison does
+    not hinge on rounding."""
+    B, D, k, N, d, Vd = 1, 8, 10, 60, 2560, 32000
+    Wd, d2t, x, dids, tids, vals = _draft_case(B * D * k, d, Vd, k)
+    lse_ref = _lse_ref[id(x)]
+    lp_ref = (vals - lse_ref[:, None]).astype(np.float32).reshape(B, D, k, k)
+    tid_ref = tids.reshape(B, D, k, k)
+    tree_ref = o().build_tree(tid_ref, lp_ref, N)
+    assert tree_ref[4] == 0
+    rng = np.random.default_rng(7)
+    for _ in range(8):   # the oracle's tree does not hinge on the last few bits of a log-probability
+        jitter = rng.uniform(-5e-4, 5e-4, lp_ref.shape).astype(np.float32)
+        alt = o().build_tree(tid_ref, np.minimum(lp_ref + jitter, 0).astype(np.float32), N)
+        assert all(np.array_equal(a, e) for a, e in zip(alt[:2], tree_ref[:2]))
+    ws = wf.Workspace(1, B * D * k, 1, Vd, k, d=d)
+    lse = torch.empty(B * D * k, dtype=torch.float32, device=DEV)
+    _, gt, gv = wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), k, ws, lse=lse)
+    lp = (gv - lse[:, None]).view(B, D, k, k)   # same stream, no synchronisation
+    parent, token, score, depth = wf.wf_build_tree(gt.view(B, D, k, k), lp, N, ws)
+    torch.cuda.synchronize()
+    _check_lse(host(lse), x)
+    assert np.max(np.abs(host(lp) - lp_ref)) <= 2e-3
+    assert np.array_equal(host(parent), tree_ref[0]) and np.array_equal(host(token), tree_ref[1])
+    assert np.array_equal(host(depth), tree_ref[3])
+    assert np.max(np.abs(host(score) - tree_ref[2])) <= 2e-2
     assert ws.device_error() == (0, 0)
 
 

@@ -1,6 +1,7 @@
 """wf_lmhead_argmax_noalloc, the variant for callers that cannot allocate
 device memory (its scratch is a fixed array inside the library), must give
-exactly what the workspace-based wf_lmhead_argmax gives, call after call.
+exactly what the workspace-based wf_lmhead_argmax gives, call after call, and
+the CPU oracle's argmax on inputs whose top-2 logit gap is at least 1e-2.
 
 Kept in a file of its own that pytest collects last."""
 import ctypes
@@ -42,6 +43,36 @@ def test_noalloc_matches_workspace_call(P, d, V):
         wf_ = synth.bf16_bits_to_f32(W_np[ids_ref.cpu().numpy()]).astype(np.float64)
         bound = 2.0 * d * 2.0 ** -24 * np.abs(hf * wf_).sum(axis=1)
         assert np.all(np.abs(mx.cpu().numpy() - mx_ref.cpu().numpy()) <= bound)
+
+
+@pytest.mark.parametrize("P,d,V", [(17, 2560, 151936), (300, 256, 5000)])
+def test_noalloc_matches_oracle(P, d, V):
+    """Against the oracle, on inputs resampled until every row's top-2 logit gap
+    is >= 1e-2 (fp32 accumulation and fp64 then pick the same id)."""
+    import oracle
+    W = synth.normal_bf16(300 + P, 0, V, d, d ** -0.5)
+    h = synth.normal_bf16(300 + P, 1, P, d, 1.0)
+    ids_ref, mx_ref, gap = oracle.lmhead_argmax(h, W)
+    for a in range(1, 100):
+        bad = np.nonzero(gap < synth.GAP_MIN)[0]
+        if not len(bad):
+            break
+        for r in bad:
+            h[r] = synth.hidden_row(300 + P, int(r), a, d)
+        i2, m2, g2 = oracle.lmhead_argmax(h[bad], W)
+        ids_ref[bad], mx_ref[bad], gap[bad] = i2, m2, g2
+    assert (gap >= synth.GAP_MIN).all()
+    t = lambda a: torch.from_numpy(a.view(np.int16)).to("cuda:0")  # noqa: E731
+    hd, Wdv = t(h), t(W)
+    for _ in range(2):
+        ids = torch.full((P,), -7, dtype=torch.int32, device="cuda:0")
+        mx = torch.empty(P, dtype=torch.float32, device="cuda:0")
+        wf.wf_lmhead_argmax_noalloc(hd, Wdv, ids=ids, maxlogit=mx)
+        assert wf.wf_noalloc_read_device_error() == (0, 0)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        hf = synth.bf16_bits_to_f32(h).astype(np.float64)
+        wr = synth.bf16_bits_to_f32(W[ids_ref]).astype(np.float64)
+        assert np.all(np.abs(mx.cpu().numpy() - mx_ref) <= 2.0 * d * 2.0 ** -24 * np.abs(hf * wr).sum(axis=1))
 
 
 def test_noalloc_rejects_rows_beyond_its_array():
