@@ -813,9 +813,9 @@ def main():
     # ---- timed region: K steps.  Each step is one whole round, then the
     # dominant kernel alone, both on this stream between CUDA events (after an
     # L2 flush when the weights would fit in L2), so both see the same clocks
-    # and power state.  The host keeps one step queued ahead of the GPU (an
-    # idle GPU would put the host's launch latency between the events) and
-    # reads the SM clock while it waits for each step to end.
+    # and power state.  Every step is queued before the first one ends (an
+    # idle GPU would put the host's launch latency between the events); the
+    # host then reads the SM clock while it waits for each step to end.
     if pg is not None:
         pg.barrier()
     torch.cuda.synchronize(device)
@@ -844,9 +844,8 @@ def main():
         ev[i][2].record(stream)
         kernel_call()
         ev[i][3].record(stream)
-        if i > 0:
-            wait_step(i - 1)
-    wait_step(args.steps - 1)
+    for i in range(args.steps):
+        wait_step(i)
     torch.cuda.synchronize(device)
     if pg is not None:
         pg.barrier()

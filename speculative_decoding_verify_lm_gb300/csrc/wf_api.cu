@@ -25,7 +25,7 @@ wf_status launch_router(const uint16_t* hidden, const int32_t* rows, int B, int 
 wf_status launch_wait_probe(uint64_t timeout_ns, void* ws, cudaStream_t s);
 wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, float* H, int32_t* route, float tau, const int32_t* src_rows,
-                                int src_P, void* ws, size_t ent_off, cudaStream_t s);
+                                int src_P, void* ws, size_t ent_off, cudaStream_t s, int* defer_slots = nullptr);
 wf_status launch_build_tree(const int32_t* tid, const float* lp, int B, int D, int k, int N, int32_t* parent,
                             int32_t* token, float* score, int32_t* depth, void* ws, cudaStream_t s);
 wf_status launch_accepted_rows(const int32_t* n_accept, const int32_t* path, int path_stride, const int32_t* pos_off,
@@ -36,7 +36,7 @@ wf_status launch_gather_rows(const uint16_t* hidden, int P, int d, const int32_t
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
                               size_t cand_off, size_t lsep_off, int* num_n2_out, cudaStream_t s, float* H = nullptr,
-                              float tau = 0.f, size_t ent_off = 0);
+                              float tau = 0.f, size_t ent_off = 0, int* defer_slots = nullptr);
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                      float* vals, void* ws, size_t cand_off, float* lse = nullptr, size_t lsep_off = 0);
 wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
@@ -371,20 +371,24 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         // of every row; acceptance picks the accepted row's.  With one
         // activation tile per head the draft head shares that sweep and its
         // top-k merge runs in the verification launch.
+        // The sweep leaves its per-CTA softmax statistics in the workspace and
+        // acceptance merges them at each sequence's accepted row only.
         const bool shared = draft && a->P <= BM && a->B <= BM;
-        int num_n2 = 0;
+        int num_n2 = 0, nslots = 0;
         if (shared)
             WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
-                                       a->Vd, a->k, ws, L.cand, a->lse ? L.lsep : 0, &num_n2, stream, dall, a->tau,
-                                       L.ent));
+                                       a->Vd, a->k, ws, L.cand, a->lse ? L.lsep : 0, &num_n2, stream, nullptr, a->tau,
+                                       L.ent, &nslots));
         else
-            WF_TRY(launch_lmhead_entropy(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, dall, nullptr,
-                                         a->tau, nullptr, 0, ws, L.ent, stream));
+            WF_TRY(launch_lmhead_entropy(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, nullptr, nullptr,
+                                         a->tau, nullptr, 0, ws, L.ent, stream, &nslots));
         const MergeArgs mg = merge_args(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws,
                                         L.cand, a->lse, L.lsep);
+        const float4* ent = reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(ws) + L.ent);
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{dall, a->tau, a->delta_al, a->route}, true, shared ? &mg : nullptr));
+                             RoutePick{nullptr, ent, nslots, a->tau, a->delta_al, a->route}, true,
+                             shared ? &mg : nullptr));
         if (shared) return WF_OK;
     } else if (entropy) {
         // many rows: a second sweep over the weights for the B accepted rows only
@@ -422,7 +426,7 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
                                  nullptr, ws, L.part, stream));
             WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                                  a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,
-                                 stream, RoutePick{dall, a->tau, a->delta_al, a->route}, true, mgp));
+                                 stream, RoutePick{dall, nullptr, 0, a->tau, a->delta_al, a->route}, true, mgp));
         } else {
             WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                                  a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws,

@@ -1322,14 +1322,13 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     uint16_t* afin = reinterpret_cast<uint16_t*>(w + L.afin);
     const int GD = a->G * a->D, HD = a->H * a->D;
     const int rows = a->N + (with_final ? a->B : 0);
+    static std::mutex norm_mu;
     static bool norm_attr[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return WF_ERR_CUDA;
-    if (dev < 64 && !norm_attr[dev]) {   // see launch_proj: the largest shared-memory carveout
-        if (cudaFuncSetAttribute(norm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-            return WF_ERR_CUDA;
-        norm_attr[dev] = true;
-    }
+    CU_TRY(configure_once(norm_mu, norm_attr, [] {   // see launch_proj: the largest shared-memory carveout
+        return cudaFuncSetAttribute(norm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+    }));
     CU_TRY(launch(norm_kernel, dim3(cdiv(rows, NORM_ROWS_PER_CTA)), dim3(32 * NORM_ROWS_PER_CTA), 0, s, a->u,
                          a->bl_off, a->cache_len, a->B, a->N, a->din, a->cap, a->gamma, a->eps, (int)with_final,
                          a->theta, a->D, ahat, afin, reinterpret_cast<float2*>(w + L.rope), ctrl));
@@ -1377,15 +1376,15 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     ap.obf = reinterpret_cast<uint16_t*>(w + L.obf);
     ap.attn = a->attn;
     const size_t at_smem = catchup_attend_smem(a->H, a->G, a->D);
+    static std::mutex at_mu;
     static bool at_attr[64] = {false};
-    if (dev < 64 && !at_attr[dev]) {
-        if (cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
-            cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-            return WF_ERR_CUDA;
-        at_attr[dev] = true;
-    }
+    CU_TRY(configure_once(at_mu, at_attr, [] {
+        return cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    }));
     // few splits: each (sequence, KV head) is one cluster and merges on chip,
     // provided all of the clusters are resident at once (a CTA that finishes
     // early holds its slot until its cluster has merged)
@@ -1402,15 +1401,14 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     const size_t og_smem = catchup_oproj_gemv_smem(HD);
     if (a->B <= OG_MAX_B && og_ctas <= 2 * num_sms() && HD <= OG_WARPS * OG_MAX_KPW * 16 &&
         og_smem <= 110 * 1024) {
+        static std::mutex og_mu;
         static bool og_attr[64] = {false};
-        if (dev < 64 && !og_attr[dev]) {
-            if (cudaFuncSetAttribute(oproj_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-                    cudaSuccess ||
-                cudaFuncSetAttribute(oproj_gemv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
-                    cudaSuccess)
-                return WF_ERR_CUDA;
-            og_attr[dev] = true;
-        }
+        CU_TRY(configure_once(og_mu, og_attr, [] {
+            return cudaFuncSetAttribute(oproj_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+                       cudaSuccess &&
+                   cudaFuncSetAttribute(oproj_gemv_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
+                       cudaSuccess;
+        }));
         OgParams og = {};
         og.Wo = a->Wo;
         og.obf = ap.obf;

@@ -77,6 +77,7 @@ struct GemmParams {
     float2* lsep;      // top-k: [tiles][BM] (max, sum e^(logit - max)) over the tile's columns, or null
     float4* ent;       // entropy: [M_rows][CTA slots] running (max, sum e^z, sum z e^z), z = logit - max
     float* H;          // entropy: [M_rows] out
+    int ent_defer;     // entropy: leave the statistics for the acceptance step to merge at the accepted rows
     int32_t* route;    // entropy: [M_rows] out (H > tau) or null
     float tau;
     const int32_t* src_rows;   // entropy over gathered rows: the source row of each, or null
@@ -93,19 +94,6 @@ struct GemmParams {
 __device__ __forceinline__ void gemm_fail(Control* ctrl, volatile int* abort_flag, uint32_t where) {
     *abort_flag = 1;
     record_error(ctrl, WF_ERR_TIMEOUT, where);
-}
-
-// Merge two partial softmax states (M, S = sum e^(L-M), T = sum (L-M) e^(L-M));
-// a state with S = 0 is empty and leaves the other as it is.  Written with
-// selects only, so that the chains of several rows can run interleaved.
-__device__ __forceinline__ void ent_merge(float& M, float& S, float& T, float m2, float s2, float t2) {
-    const bool h1 = S > 0.f, h2 = s2 > 0.f;
-    const float mx = h1 ? (h2 ? fmaxf(M, m2) : M) : m2;
-    const float d1 = h1 ? M - mx : 0.f, d2 = h2 ? m2 - mx : 0.f;
-    const float a1 = h1 ? __expf(d1) : 0.f, a2 = h2 ? __expf(d2) : 0.f;
-    T = (h1 ? (T + d1 * S) * a1 : 0.f) + (h2 ? (t2 + d2 * s2) * a2 : 0.f);
-    S = (h1 ? S * a1 : 0.f) + (h2 ? s2 * a2 : 0.f);
-    M = mx;
 }
 
 
@@ -191,11 +179,14 @@ __device__ __forceinline__ void lse_fold(const uint32_t (&r)[32], int lim, float
 // ENT, fold the columns into the row's softmax statistics; hand the
 // accumulator back to the MMA warp, then publish the row's result (a packed
 // key for argmax, the tile's sorted candidate list for top-k).
+// tempty_first: in the second CTA of a pair, the shared::cluster address of
+// the first CTA's accumulator-empty barriers (the first CTA issues the MMAs
+// into both CTAs' TMEM); 0 otherwise.
 template <int KT, bool ENT, bool TAIL>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfull, uint64_t* tempty,
-                                              volatile int* abort_flag, uint32_t tmem_base, uint32_t tile_i, int q,
-                                              int rit, int M_rows, int N_w, int m, int n, const TileSpan sp,
-                                              int cand_num_m, float& em, float& es, float& et) {
+                                              uint32_t tempty_first, volatile int* abort_flag, uint32_t tmem_base,
+                                              uint32_t tile_i, int q, int rit, int M_rows, int N_w, int m, int n,
+                                              const TileSpan sp, int cand_num_m, float& em, float& es, float& et) {
     static_assert(!ENT || KT == 1, "the softmax statistics ride on the argmax epilogue");
     const uint32_t acc = tile_i & 1;
     const uint32_t acc_ph = (tile_i >> 1) & 1;
@@ -291,7 +282,10 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
         }
     }
     tc_fence_before();
-    mbar_arrive(&tempty[acc]);
+    if (tempty_first)
+        mbar_arrive_remote(tempty_first + acc * (uint32_t)sizeof(uint64_t), 1u);
+    else
+        mbar_arrive(&tempty[acc]);
     if (quad_live && row < M_rows) {
         if constexpr (KT == 1) {
             atomicMax(reinterpret_cast<unsigned long long*>(p.keys + row),
@@ -323,6 +317,13 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
 // Each CTA loads its own activation and weight boxes; tiles (m, n) are visited
 // in the order t = n * num_m + m, so the CTAs working at the same time share
 // the weight tile through L2.
+// PAIR (several activation tiles, no ENT / DUAL): clusters of two CTAs take
+// tile pairs (m, n), (m + 1, n) with one paired MMA of M = 256 rows: each CTA
+// loads its own activation tile and half of the weight tile (its bytes are
+// counted on the first CTA's stage barrier), the first CTA issues every MMA
+// and commits to both CTAs' barriers, and each CTA's epilogue reads its own
+// TMEM rows.  A weight byte crosses the L2 -> SM crossbar and is read from
+// shared memory once per pair.
 // ENT (with KT = 1): also accumulate, per row, the softmax statistics of the
 // logits so that the entropy of the next-token distribution comes out of the
 // same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
@@ -331,13 +332,14 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
 // (activation map tmA2, weight map tmB2, top-k into p.cand), swept first
 // (tile_order); with ENT the first problem's tiles also feed the entropy
 // statistics.
-template <int KT, bool ENT, bool DUAL>
+template <int KT, bool ENT, bool DUAL, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB2s,
                        const GemmParams p) {
     static_assert(!DUAL || KT == 1, "the dual sweep pairs an argmax head with a top-k head");
+    static_assert(!PAIR || (!ENT && !DUAL), "paired MMAs only for the plain sweeps of several activation tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
@@ -357,10 +359,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // tiles: u -> (activation tile m = u % num_m, weight tile n = u / num_m)
-    const int slot = blockIdx.x, nslots = gridDim.x;
+    // tiles: u -> (activation tile m = u % num_m, weight tile n = u / num_m);
+    // PAIR: u -> activation tiles 2 (u % num_mt) + rank of the pair, weight tile u / num_mt
+    const int rank = PAIR ? (int)(cluster_ctarank() & 1u) : 0;
+    const bool first = rank == 0;   // PAIR: the CTA that issues the MMAs
+    const int slot = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nslots = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
     const int num_m = p.num_m;
-    const int U0 = num_m * p.num_n;
+    const int num_mt = PAIR ? (num_m + 1) >> 1 : num_m;
+    const int U0 = num_mt * p.num_n;
     const int U = U0 + (DUAL ? p.num_n2 : 0);
 
     if (threadIdx.x == 0) {
@@ -370,7 +377,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 128);
+            mbar_init(&tempty[a], PAIR ? 256 : 128);   // PAIR: both CTAs' epilogue threads release
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -386,11 +393,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers and TMEM exist before either uses the other's
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     // the prologue above overlaps the previous kernel on the stream; inputs and
@@ -404,6 +417,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_w = p.weight_evict_first ? policy_evict_first() : policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
+            // PAIR: both CTAs' copies of a stage are counted on the first CTA's barrier
+            const uint32_t full_first = PAIR ? cluster_addr(&full[0], 0) : 0;
             uint32_t it = 0;  // stages issued so far
             int s = 0;        // = it % stages
             uint32_t ph = 0;  // = (it / stages) & 1
@@ -411,13 +426,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = slot; v < U && ok; v += nslots) {
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
-                const int m = second ? 0 : u % num_m;
-                const int n = second ? u - U0 : u / num_m;
+                const int m = second ? 0 : (PAIR ? 2 * (u % num_mt) + rank : u % num_m);
+                const int n = second ? u - U0 : u / num_mt;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const CUtensorMap* mA = second ? &tmA2 : &tmA;
                 const CUtensorMap* mB = second ? (sp.big ? &tmB2 : &tmB2s) : (sp.big ? &tmB : &tmBs);
-                const uint32_t tx = (second ? p.a_bytes2 : p.a_bytes) + sp.rows * BK * 2;
+                const int wrows = PAIR ? sp.rows / 2 : sp.rows;   // weight rows this CTA loads
+                const uint32_t tx = PAIR ? 2u * (uint32_t)(p.a_bytes + wrows * BK * 2)
+                                         : (uint32_t)((second ? p.a_bytes2 : p.a_bytes) + sp.rows * BK * 2);
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
                     if (it > 0) {
                         if (++s == stages) {
@@ -430,20 +447,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], tx);
-                    tma_load_2d(stA(s), mA, &full[s], kc * BK, m * BM, pol_a);
-                    tma_load_2d(stB(s), mB, &full[s], kc * BK, sp.row0, pol_w);
+                    if constexpr (PAIR) {
+                        if (first) mbar_arrive_expect_tx(&full[s], tx);
+                        const uint32_t bar = full_first + (uint32_t)(s * sizeof(uint64_t));
+                        tma_load_2d_pair(stA(s), mA, bar, kc * BK, m * BM, pol_a);
+                        tma_load_2d_pair(stB(s), mB, bar, kc * BK, sp.row0 + rank * wrows, pol_w);
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], tx);
+                        tma_load_2d(stA(s), mA, &full[s], kc * BK, m * BM, pol_a);
+                        tma_load_2d(stB(s), mB, &full[s], kc * BK, sp.row0, pol_w);
+                    }
                 }
             }
             if (!ok || *abort_flag) {
                 // let every copy this thread issued land before the CTA exits
-                for (uint32_t j = (it > (uint32_t)stages ? it - stages : 0); j < it; ++j)
-                    mbar_wait(&full[j % stages], (j / stages) & 1, p.timeout_ns, nullptr);
+                if (!PAIR || first) {
+                    for (uint32_t j = (it > (uint32_t)stages ? it - stages : 0); j < it; ++j)
+                        mbar_wait(&full[j % stages], (j / stages) & 1, p.timeout_ns, nullptr);
+                } else {
+                    // the second CTA's copies are counted on the first CTA's
+                    // barriers, which it cannot wait on: give them a fixed
+                    // 200 us (a copy from L2 or HBM takes a few)
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 200000ull) {
+                    }
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && first) {
+            // PAIR: the first CTA's commits arrive on both CTAs' barriers
+            const uint32_t empty_peer = PAIR ? cluster_addr(&empty[0], 1) : 0;
+            const uint32_t tfull_peer = PAIR ? cluster_addr(&tfull[0], 1) : 0;
             uint32_t it = 0, tile_i = 0;
             int s = 0;        // = it % stages
             uint32_t ph = 0;  // = (it / stages) & 1
@@ -451,13 +487,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = slot; v < U && ok; v += nslots, ++tile_i) {
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
-                const int n = second ? u - U0 : u / num_m;
+                const int n = second ? u - U0 : u / num_mt;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const uint32_t idesc = second ? (sp.big ? p.idesc2 : p.idesc2_s) : (sp.big ? p.idesc : p.idesc_s);
                 const uint32_t acc = tile_i & 1;
                 const uint32_t acc_ph = (tile_i >> 1) & 1;
-                if (!mbar_wait(&tempty[acc], acc_ph ^ 1, p.timeout_ns, abort_flag)) {
+                // PAIR: released by both CTAs' epilogues (the second's arrivals are remote)
+                if (!(PAIR ? mbar_wait_cluster(&tempty[acc], acc_ph ^ 1, p.timeout_ns, abort_flag)
+                           : mbar_wait(&tempty[acc], acc_ph ^ 1, p.timeout_ns, abort_flag))) {
                     gemm_fail(p.ctrl, abort_flag, 0x200);
                     ok = false;
                     break;
@@ -479,17 +517,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tc_fence_after();
                     const uint64_t adesc = umma_desc_sw128(smem_u32(stA(s)));
                     const uint64_t bdesc = umma_desc_sw128(smem_u32(stB(s)));
+                    if constexpr (PAIR) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per step (encoded >> 4)
-                        umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
-                    umma_commit(&empty[s]);
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
+                        umma_commit_pair(smem_u32(&empty[s]));
+                        umma_commit_pair(empty_peer + (uint32_t)(s * sizeof(uint64_t)));
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes of K per step (encoded >> 4)
+                            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kc | kk) != 0);
+                        umma_commit(&empty[s]);
+                    }
                     issued = true;
                 }
-                if (ok) umma_commit(&tfull[acc]);
+                if (ok) {
+                    if constexpr (PAIR) {
+                        umma_commit_pair(smem_u32(&tfull[acc]));
+                        umma_commit_pair(tfull_peer + acc * (uint32_t)sizeof(uint64_t));
+                    } else {
+                        umma_commit(&tfull[acc]);
+                    }
+                }
             }
-            if (issued && !ok) {
-                // every MMA issued above has completed before the CTA frees its TMEM
-                umma_commit(drain);
+            if (issued && (!ok || PAIR)) {
+                // every MMA issued above (PAIR: into both CTAs' TMEM) has
+                // completed before TMEM is freed
+                if constexpr (PAIR)
+                    umma_commit_pair(smem_u32(drain));
+                else
+                    umma_commit(drain);
                 mbar_wait(drain, 0, p.timeout_ns, nullptr);
             }
         }
@@ -498,29 +555,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int rit = q * 32 + lane;
         float em = -INFINITY, es = 0.f, et = 0.f;   // ENT: this row's running softmax statistics
+        const uint32_t tempty_first = (PAIR && !first) ? cluster_addr(&tempty[0], 0) : 0;
         uint32_t tile_i = 0;
         for (int v = slot; v < U; v += nslots, ++tile_i) {
             const int u = tile_order<DUAL>(v, U0, U);
             bool ok;
             if (DUAL && u >= U0)
-                ok = epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit,
-                                                   p.M_rows2, p.N_w2, 0, u - U0,
-                                                   tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false), 1, em, es, et);
-            else if (num_m == 1)   // the weight-streaming sweep: the last tile's scan is exposed
-                ok = epilogue_tile<KT, ENT, true>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
-                                                  p.N_w, 0, u, tile_span(u, p.num_n, p.bn, p.nbig, true), 1, em, es,
-                                                  et);
+                ok = epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, 0, abort_flag, tmem_base, tile_i, q, rit,
+                                                          p.M_rows2, p.N_w2, 0, u - U0,
+                                                          tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false), 1, em,
+                                                          es, et);
+            else if (!PAIR && num_m == 1)   // the weight-streaming sweep: the last tile's scan is exposed
+                ok = epilogue_tile<KT, ENT, true>(p, tfull, tempty, 0, abort_flag, tmem_base, tile_i, q, rit,
+                                                  p.M_rows, p.N_w, 0, u, tile_span(u, p.num_n, p.bn, p.nbig, true), 1,
+                                                  em, es, et);
             else
-                ok = epilogue_tile<KT, ENT, false>(p, tfull, tempty, abort_flag, tmem_base, tile_i, q, rit, p.M_rows,
-                                                   p.N_w, u % num_m, u / num_m,
-                                                   tile_span(u / num_m, p.num_n, p.bn, p.nbig, true), num_m, em, es,
+                ok = epilogue_tile<KT, ENT, false>(p, tfull, tempty, tempty_first, abort_flag, tmem_base, tile_i, q,
+                                                   rit, p.M_rows, p.N_w,
+                                                   PAIR ? 2 * (u % num_mt) + rank : u % num_m, u / num_mt,
+                                                   tile_span(u / num_mt, p.num_n, p.bn, p.nbig, true), num_m, em, es,
                                                    et);
             if (!ok) break;
         }
         if constexpr (ENT) {
-            // this CTA's rows are fixed (the grid is a multiple of num_m); publish their statistics
-            const int row = (slot % num_m) * BM + rit;
-            if (row < p.M_rows) p.ent[(size_t)row * nslots + slot] = make_float4(em, es, et * LN2, 0.f);
+            // this CTA's rows are fixed (the grid is a multiple of num_m); publish
+            // their statistics, and an empty state (S = 0) for the other
+            // activation tile's rows, so that every slot a merge reads was
+            // written by this launch
+            for (int mm = 0; mm < num_m; ++mm) {
+                const int row = mm * BM + rit;
+                if (row < p.M_rows)
+                    p.ent[(size_t)row * nslots + slot] =
+                        mm == slot % num_m ? make_float4(em, es, et * LN2, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         if (KT == 1 && !*abort_flag) {
             // last CTA to finish turns the keys into ids and zeroes them again
@@ -553,7 +620,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // ENT_RB rows each at a time: every slot load in flight before any is
         // used (a row's slots are contiguous, so each load is coalesced), the
         // rows' merge chains interleaved, and lane q finishing row q.
-        if (*last_flag) {
+        if (*last_flag && !p.ent_defer) {
             static_assert(ENT_MAX_SLOTS % 32 == 0, "slots are shared out evenly over the lanes");
             constexpr int SPL = ENT_MAX_SLOTS / 32;   // slots per lane
             constexpr int ENT_RB = 4;
@@ -617,8 +684,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
     }
+    if constexpr (PAIR) cluster_sync();   // the first CTA's MMAs and the second's remote arrivals are done
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
+    }
 }
 
 // --------------------------------------------------------------------- top-k merge
@@ -709,32 +782,71 @@ static bool balanced_tiles(int N_w, int sms, TileGeom* g) {
 // full activation box and a full weight box; with one, an activation slot as
 // large as its box (a_rows x 128 bytes) and as many stages as RING_BUDGET
 // holds.  Returns the dynamic shared memory of the launch.
-static int set_ring(GemmParams& p, int one_tile_a_rows) {
-    if (one_tile_a_rows <= 0) {
+// Paired-CTA sweeps: the weight slot holds half a tile (BN / 2 rows), so the
+// same budget holds six stages.
+static int set_ring(GemmParams& p, int one_tile_a_rows, bool pair = false) {
+    const int b_bytes = pair ? B_BYTES / 2 : B_BYTES;
+    if (one_tile_a_rows <= 0 && !pair) {
         p.a_alloc = A_BYTES;
         p.stages = STAGES;
     } else {
-        p.a_alloc = one_tile_a_rows * BK * 2;   // a multiple of 1024 (rows come in 8s)
-        int st = RING_BUDGET / (p.a_alloc + B_BYTES);
+        p.a_alloc = one_tile_a_rows > 0 ? one_tile_a_rows * BK * 2 : A_BYTES;   // a multiple of 1024
+        int st = RING_BUDGET / (p.a_alloc + b_bytes);
         p.stages = st < STAGES ? STAGES : (st > STAGES_MAX ? STAGES_MAX : st);
     }
-    p.stage_bytes = p.a_alloc + B_BYTES;
+    p.stage_bytes = p.a_alloc + b_bytes;
     return p.stages * p.stage_bytes + 1024 + 256;
+}
+
+// Clusters of two paired-CTA sweep CTAs that can be resident at once (queried
+// once per device).
+template <int KT>
+static int pair_slots(int smem) {
+    static std::mutex mu;
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return num_sms() / 2;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cached[dev]) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 64);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, false, false, true>, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = num_sms() / 2;
+    }
+    if (dev < 64) cached[dev] = n;
+    return n;
 }
 
 template <int KT, bool ENT>
 static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* W, int N_w, int d, GemmParams p,
-                               cudaStream_t s, int* num_n_out = nullptr) {
+                               cudaStream_t s, int* num_n_out = nullptr, int* grid_out = nullptr) {
     static std::mutex mu;
     static bool attr_set[64] = {false};
     const wf_status cst = configure_once(mu, attr_set, [] {
-        return cudaFuncSetAttribute(gemm_select_kernel<KT, ENT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    GEMM_SMEM_MAX) == cudaSuccess;
+        return cudaFuncSetAttribute(gemm_select_kernel<KT, ENT, false, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_MAX) == cudaSuccess &&
+               (ENT || cudaFuncSetAttribute(gemm_select_kernel<KT, false, false, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            GEMM_SMEM_MAX) == cudaSuccess);
     });
     if (cst != WF_OK) return cst;
     CUtensorMap ta, tb, tbs;
     const int num_m = cdiv(M_rows, BM);
     if (ENT && num_m > 2) return WF_ERR_UNSUPPORTED;
+    // several activation tiles: CTA pairs with the paired MMA (M = 256), each
+    // loading half of every weight tile
+    const bool pair = !ENT && num_m > 1;
     // With a single activation tile the box covers only the rows that exist
     // (rounded up to a whole 8-row swizzle atom): no zero rows cross the
     // crossbar.  The UMMA still reads all BM rows of the stage; rows past the
@@ -752,28 +864,38 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
         p.nbig = p.num_n;
     }
     const int bn = p.bn;
-    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)bn)) return WF_ERR_CUDA;
+    const int split = pair ? 2 : 1;   // a pair's CTAs each load half of a weight tile (bn is a multiple of 16)
+    if (!make_map(&tb, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn / split))) return WF_ERR_CUDA;
     tbs = tb;
-    if (p.nbig < p.num_n && !make_map(&tbs, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)(bn - 16))) return WF_ERR_CUDA;
+    if (p.nbig < p.num_n && !make_map(&tbs, W, (uint64_t)N_w, (uint64_t)d, (uint32_t)((bn - 16) / split)))
+        return WF_ERR_CUDA;
     if (num_n_out) *num_n_out = p.num_n;
     p.M_rows = M_rows;
     p.N_w = N_w;
     p.num_m = num_m;
-    p.idesc = umma_idesc_bf16(BM, bn);
-    p.idesc_s = p.nbig < p.num_n ? umma_idesc_bf16(BM, bn - 16) : p.idesc;
+    p.idesc = umma_idesc_bf16(split * BM, bn);
+    p.idesc_s = p.nbig < p.num_n ? umma_idesc_bf16(split * BM, bn - 16) : p.idesc;
     p.num_k = cdiv(d, BK);
     p.weight_evict_first = p.num_m == 1;
     p.a_bytes = a_rows * BK * 2;
     p.timeout_ns = wait_timeout_ns();
-    const int smem = set_ring(p, num_m == 1 ? a_rows : 0);
+    const int smem = set_ring(p, num_m == 1 ? a_rows : 0, pair);
+    if (pair) {
+        const int pairs = cdiv(num_m, 2) * p.num_n;
+        const int slots = pair_slots<KT>(smem);
+        const int grid = 2 * (pairs < slots ? pairs : slots);
+        return launch_cluster(gemm_select_kernel<KT, false, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s,
+                              2u, ta, tb, ta, tb, tbs, tbs, p);
+    }
     const int tiles = p.num_m * p.num_n;
     int grid = tiles < num_sms() ? tiles : num_sms();
     if (ENT) {   // every CTA keeps the rows of one activation tile: a grid that is a multiple of num_m
         if (grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
         grid -= grid % num_m;
     }
-    return launch(gemm_select_kernel<KT, ENT, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta, tb, tbs,
-                  tbs, p);
+    if (grid_out) *grid_out = grid;
+    return launch(gemm_select_kernel<KT, ENT, false, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta, tb,
+                  tbs, tbs, p);
 }
 
 static GemmParams params_for(void* ws) {
@@ -795,8 +917,9 @@ wf_status launch_lmhead_argmax(const uint16_t* hidden, const uint16_t* W, int P,
 // The same sweep plus the entropy of softmax(logits) per row (rows <= 2 tiles).
 wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                                 float* maxlogit, float* H, int32_t* route, float tau, const int32_t* src_rows,
-                                int src_P, void* ws, size_t ent_off, cudaStream_t s) {
+                                int src_P, void* ws, size_t ent_off, cudaStream_t s, int* defer_slots) {
     GemmParams p = params_for(ws);
+    p.ent_defer = defer_slots != nullptr;
     p.k = 1;
     p.ids = ids;
     p.maxlogit = maxlogit;
@@ -806,7 +929,7 @@ wf_status launch_lmhead_entropy(const uint16_t* hidden, const uint16_t* W, int P
     p.tau = tau;
     p.src_rows = src_rows;
     p.src_P = src_P;
-    return launch_select<1, true>(hidden, P, W, V, d, p, s);
+    return launch_select<1, true>(hidden, P, W, V, d, p, s, nullptr, defer_slots);
 }
 
 wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t* d2t, int B, int d, int Vd, int k,
@@ -830,14 +953,14 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
                               size_t cand_off, size_t lsep_off, int* num_n2_out, cudaStream_t s, float* H, float tau,
-                              size_t ent_off) {
+                              size_t ent_off, int* defer_slots) {
     if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     const wf_status cst = configure_once(mu, attr_set, [] {
-        return cudaFuncSetAttribute(gemm_select_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(gemm_select_kernel<1, false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     GEMM_SMEM_MAX) == cudaSuccess &&
-               cudaFuncSetAttribute(gemm_select_kernel<1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+               cudaFuncSetAttribute(gemm_select_kernel<1, true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     GEMM_SMEM_MAX) == cudaSuccess;
     });
     if (cst != WF_OK) return cst;
@@ -893,18 +1016,20 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     *num_n2_out = p.num_n2;
     const int smem = set_ring(p, a_rows > a_rows2 ? a_rows : a_rows2);
     int grid = tiles < sms ? tiles : sms;
-    if (H) {   // the target head's entropy statistics as well (WhiFlash-Entropy)
+    if (H || defer_slots) {   // the target head's entropy statistics as well (WhiFlash-Entropy)
         p.ent = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(ws) + ent_off);
         p.H = H;
+        p.ent_defer = defer_slots != nullptr;
         p.route = nullptr;
         p.tau = tau;
         p.src_rows = nullptr;
         p.src_P = 0;
         if (grid > ENT_MAX_SLOTS) grid = ENT_MAX_SLOTS;
-        return launch(gemm_select_kernel<1, true, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2,
+        if (defer_slots) *defer_slots = grid;
+        return launch(gemm_select_kernel<1, true, true, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2,
                       tb2, tbs, tb2s, p);
     }
-    return launch(gemm_select_kernel<1, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2, tb2,
+    return launch(gemm_select_kernel<1, false, true, false>, dim3(grid), dim3(GEMM_THREADS), smem, s, ta, tb, ta2, tb2,
                   tbs, tb2s, p);
 }
 

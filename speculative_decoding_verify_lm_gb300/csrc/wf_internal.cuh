@@ -51,18 +51,61 @@ constexpr int ROUTE_ALL_ROWS_MAX = 128;
 // routes the accepted rows after acceptance instead.
 constexpr int ROUTER_BESIDE_MAX_ROWS = 32;
 
-// Optional tail of the acceptance step: copy the router output of the
-// accepted row (computed for every row beforehand) and take the decision.
+// Merge two partial softmax states (M, S = sum e^(L-M), T = sum (L-M) e^(L-M));
+// a state with S = 0 is empty and leaves the other as it is.  Written with
+// selects only, so that the chains of several rows can run interleaved.
+__device__ __forceinline__ void ent_merge(float& M, float& S, float& T, float m2, float s2, float t2) {
+    const bool h1 = S > 0.f, h2 = s2 > 0.f;
+    const float mx = h1 ? (h2 ? fmaxf(M, m2) : M) : m2;
+    const float d1 = h1 ? M - mx : 0.f, d2 = h2 ? m2 - mx : 0.f;
+    const float a1 = h1 ? __expf(d1) : 0.f, a2 = h2 ? __expf(d2) : 0.f;
+    T = (h1 ? (T + d1 * S) * a1 : 0.f) + (h2 ? (t2 + d2 * s2) * a2 : 0.f);
+    S = (h1 ? S * a1 : 0.f) + (h2 ? s2 * a2 : 0.f);
+    M = mx;
+}
+
+// Optional tail of the acceptance step: the routing decision at the accepted
+// row.  Either the router output of that row (computed for every row
+// beforehand) is copied, or - WhiFlash-Entropy - the softmax statistics the
+// LM-head sweep left per (row, CTA slot) are merged for that row alone.
 struct RoutePick {
-    const float* delta_all;   // [P] router output per verified row, or null (no pick)
+    const float* delta_all;   // [P] router output per verified row, or null
+    const float4* ent;        // [P][nslots] softmax statistics (max, sum e^z, sum z e^z), or null
+    int nslots;
     float tau;
     float* delta_al;          // [B]
     int32_t* route;           // [B]
-    __device__ __forceinline__ void write(int b, int row) const {
-        if (!delta_all) return;
-        const float v = row >= 0 ? delta_all[row] : __int_as_float(0x7fc00000);
-        delta_al[b] = v;
-        route[b] = row >= 0 ? (v > tau ? 1 : 0) : -1;
+    // Warp-collective (all 32 lanes, the same b and row); row < 0 marks a failed sequence.
+    __device__ __forceinline__ void publish(int b, int row, int lane) const {
+        if (ent) {
+            constexpr int SPL = ENT_MAX_SLOTS / 32;   // slots per lane
+            float4 st[SPL];
+#pragma unroll
+            for (int i = 0; i < SPL; ++i) {   // every load in flight before any is used
+                const int sl = lane + 32 * i;
+                st[i] = (row >= 0 && sl < nslots) ? __ldcg(ent + (size_t)row * nslots + sl)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float M = -INFINITY, S = 0.f, T = 0.f;
+#pragma unroll
+            for (int i = 0; i < SPL; ++i) ent_merge(M, S, T, st[i].x, st[i].y, st[i].z);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+                const float s2 = __shfl_xor_sync(0xffffffffu, S, off);
+                const float t2 = __shfl_xor_sync(0xffffffffu, T, off);
+                ent_merge(M, S, T, m2, s2, t2);
+            }
+            if (lane == 0) {
+                const float h = row >= 0 ? logf(S) - T / S : __int_as_float(0x7fc00000);
+                delta_al[b] = h;
+                route[b] = row >= 0 ? (h > tau ? 1 : 0) : -1;
+            }
+        } else if (delta_all && lane == 0) {
+            const float v = row >= 0 ? delta_all[row] : __int_as_float(0x7fc00000);
+            delta_al[b] = v;
+            route[b] = row >= 0 ? (v > tau ? 1 : 0) : -1;
+        }
     }
 };
 
@@ -292,6 +335,49 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// The same load issued by one CTA of a pair that computes with the paired-CTA
+// MMA: the copy lands in this CTA's shared memory and its byte count is
+// signalled on the mbarrier at `bar` (a shared::cluster address, here the
+// first CTA's barrier, which the pair's MMA issuer waits on).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+// shared::cluster address of the same shared-memory offset in cluster CTA `rank`
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+// Arrive `count` times on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// mbar_try_wait with acquire at cluster scope (a phase completed by arrivals from another CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                                  volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t start = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer_ns() - start > timeout_ns) return false;
+    }
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -348,6 +434,39 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
+// The paired-CTA forms (cta_group::2): the two CTAs of a cluster pair share
+// one MMA of M = 256 rows - A's rows 0-127 from the first CTA's shared memory,
+// 128-255 from the second's at the same offset, B's N columns split in halves
+// the same way, D's rows in each CTA's own TMEM at the same address.  Both
+// CTAs allocate and free their TMEM together (one warp of each); the first
+// CTA issues the MMAs and commits.  Every tcgen05 instruction of such a
+// kernel uses the paired form.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at shared::cluster address `bar` (this CTA's or
+// the peer's) when all paired MMAs this thread issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit words from TMEM: thread t gets its lane's 32 columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

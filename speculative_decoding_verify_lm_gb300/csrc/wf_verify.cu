@@ -74,14 +74,14 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     pdl_trigger();
     if (!live) return;
 
-    auto fail = [&]() {
+    auto fail = [&]() {   // warp-uniform
         if (lane == 0) {
             record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)b);
             n_accept[b] = -1;
             bonus[b] = -1;
             last_pos[b] = -1;
-            pick.write(b, -1);
         }
+        pick.publish(b, -1, lane);
         if (path)
             for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = -1;
     };
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
             n_accept[b] = n;
             last_pos[b] = r0 + n;
             bonus[b] = gs[n];
-            pick.write(b, r0 + n);
         }
+        pick.publish(b, r0 + n, lane);
         if (path)
             for (int j = lane; j < path_stride; j += 32) path[(size_t)b * path_stride + j] = j < n ? j : -1;
         return;
@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
         n_accept[b] = n;
         last_pos[b] = r0 + 1 + node;   // the root row when node = -1
         bonus[b] = gs[1 + node];
-        pick.write(b, r0 + 1 + node);
     }
+    pick.publish(b, r0 + 1 + node, lane);
 }
 
 wf_status launch_verify(const int32_t* g, const int32_t* tok, const int32_t* parent, const int32_t* kind,

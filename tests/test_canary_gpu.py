@@ -97,10 +97,12 @@ def test_router_outputs(B, d, m):
 def test_draft_topk_outputs():
     B, d, Vd, k = 3, 128, 3001, 7
     Wd, d2t, x, dids, tids, _ = _draft_case(B, d, Vd, k)
-    outs = [Guarded((B, k), torch.int32), Guarded((B, k), torch.int32), Guarded((B, k), torch.float32)]
+    outs = [Guarded((B, k), torch.int32), Guarded((B, k), torch.int32), Guarded((B, k), torch.float32),
+            Guarded((B,), torch.float32)]
     wf.wf_draft_topk(dev(x), dev(Wd), dev(d2t), k, wf.Workspace(1, B, 1, Vd, k), draft_ids=outs[0].t,
-                     tids=outs[1].t, vals=outs[2].t)
+                     tids=outs[1].t, vals=outs[2].t, lse=outs[3].t)
     assert np.array_equal(host(outs[0].t), dids) and np.array_equal(host(outs[1].t), tids) and all_intact(*outs)
+    assert np.isfinite(host(outs[3].t)).all()
 
 
 @pytest.mark.parametrize("P,B,d,V,Vd,k", [(17, 1, 256, 8192, 4000, 10), (61, 3, 2560, 151936, 32000, 10)])
@@ -110,9 +112,10 @@ def test_shared_sweep_outputs(P, B, d, V, Vd, k):
     ids_ref, _, _ = o().lmhead_argmax(h, W)
     Wd, d2t, x, dids, tids, _ = _draft_case(B, d, Vd, k)
     outs = [Guarded((P,), torch.int32), Guarded((P,), torch.float32), Guarded((B, k), torch.int32),
-            Guarded((B, k), torch.int32), Guarded((B, k), torch.float32)]
+            Guarded((B, k), torch.int32), Guarded((B, k), torch.float32), Guarded((B,), torch.float32)]
     wf.wf_lmhead_draft_topk(dev(h), dev(W), dev(x), dev(Wd), dev(d2t), k, wf.Workspace(P, B, 1, Vd, k),
-                            ids=outs[0].t, maxlogit=outs[1].t, draft_ids=outs[2].t, tids=outs[3].t, vals=outs[4].t)
+                            ids=outs[0].t, maxlogit=outs[1].t, draft_ids=outs[2].t, tids=outs[3].t, vals=outs[4].t,
+                            lse=outs[5].t)
     assert np.array_equal(host(outs[0].t), ids_ref)
     assert np.array_equal(host(outs[2].t), dids) and np.array_equal(host(outs[3].t), tids) and all_intact(*outs)
 
