@@ -171,9 +171,11 @@ class ClockSampler:
                 "samples": len(self.sm), "source": src}
 
 
-# kernel label -> the source files it is built from (template arguments: top-k width, entropy, both heads)
+# kernel label -> the source files it is built from (template arguments: top-k
+# width, entropy, both heads, paired CTAs)
 KERNEL_SOURCES = {name: ("wf_gemm_select.cu", "wf_internal.cuh")
-                  for name in ("gemm_select_kernel<1,0,0>", "gemm_select_kernel<1,1,0>", "gemm_select_kernel<1,0,1>")}
+                  for name in ("gemm_select_kernel<1,0,0,0>", "gemm_select_kernel<1,0,0,1>",
+                               "gemm_select_kernel<1,1,0,0>", "gemm_select_kernel<1,0,1,0>")}
 
 
 def source_sha(kernel: str) -> str:
@@ -785,7 +787,7 @@ def main():
         Vd = wl.Wd.shape[0]
         alg_bytes = (V + Vd) * d * 2 + (P + B) * d * 2 + Vd * 4 + P * 4 + B * k * 12
         alg_flops = 2.0 * d * (P * V + B * Vd)
-        kernel_name, kernel_launches = "gemm_select_kernel<1,0,1>", 2
+        kernel_name, kernel_launches = "gemm_select_kernel<1,0,1,0>", 2
     elif ent_fused:
         ws1 = wf.Workspace(P, P, d=d, device=device)
         Hbuf = torch.empty(P, dtype=torch.float32, device=device)
@@ -793,13 +795,14 @@ def main():
         kernel_call = lambda: wf.wf_lmhead_entropy(hdev, Wdev, wl.tau, ws1, H=Hbuf, route=rbuf)  # noqa: E731
         alg_bytes = V * d * 2 + P * d * 2 + P * 8
         alg_flops = 2.0 * P * V * d
-        kernel_name, kernel_launches = "gemm_select_kernel<1,1,0>", 1
+        kernel_name, kernel_launches = "gemm_select_kernel<1,1,0,0>", 1
     else:
         ws1 = wf.Workspace(P, device=device)
         kernel_call = lambda: wf.wf_lmhead_argmax(hdev, Wdev, ws1, ids=ids_buf)  # noqa: E731
         alg_bytes = V * d * 2 + P * d * 2 + P * 4
         alg_flops = 2.0 * P * V * d
-        kernel_name, kernel_launches = "gemm_select_kernel<1,0,0>", 1
+        # several activation tiles: the paired-CTA sweep
+        kernel_name, kernel_launches = f"gemm_select_kernel<1,0,0,{int(P > 128)}>", 1
     for _ in range(3):
         kernel_call()
     if not args.no_graph:   # replayed from a CUDA graph: host argument checks stay out of the events

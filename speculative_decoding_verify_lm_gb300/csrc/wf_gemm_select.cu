@@ -50,7 +50,11 @@ constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
 // Ring bytes with one activation tile: leaves room on the SM for the small
 // CTAs that run beside the sweep (the router over every row of a short round).
 constexpr int RING_BUDGET = 210 * 1024;
-constexpr int GEMM_SMEM_MAX = RING_BUDGET + 1024 + 256;
+// Activation bytes a paired sweep keeps in L2 while the weights stream past.
+constexpr long PAIR_GROUP_BYTES = 48L << 20;
+// Paired-CTA sweeps run alone on their SMs: seven stages of 32 KB.
+constexpr int RING_BUDGET_PAIR = 224 * 1024;
+constexpr int GEMM_SMEM_MAX = RING_BUDGET_PAIR + 1024 + 256;
 constexpr int KT_TOPK = WF_MAX_TOPK;
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                      float* vals, void* ws, size_t cand_off, float* lse = nullptr, size_t lsep_off = 0);
@@ -69,6 +73,7 @@ struct GemmParams {
     uint32_t idesc;    // instruction descriptor for M = BM, N = bn
     uint32_t idesc_s;  // ... N = bn - 16
     int weight_evict_first;
+    int group;         // activation tiles (pairs of them with PAIR) swept against every weight tile before the next group
     int a_bytes;       // bytes one activation box delivers (box rows x 128 B)
     uint64_t* keys;    // argmax: [M_rows] packed keys, zero on entry, zero on exit
     int32_t* ids;      // argmax: [M_rows] out
@@ -301,6 +306,23 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint64_t* tfu
     return true;
 }
 
+// Tile u of the first problem -> (activation tile, or pair of them, mt; weight
+// tile n).  The activation tiles are taken in groups of `group`: every weight
+// tile meets one group's tiles before the next group starts, so a group's
+// activations stay in L2 while the weights stream past (the weights are read
+// once per group).  group >= num_mt gives the plain order u = n * num_mt + mt.
+struct TileMN {
+    int mt, n;
+};
+__device__ __forceinline__ TileMN tile_mn(int u, int num_mt, int num_n, int group) {
+    const int per = group * num_n;
+    const int g = u / per;
+    const int first = g * group;
+    const int size = min(group, num_mt - first);
+    const int r = u - g * per;
+    return {first + r % size, r / size};
+}
+
 // Tile u of the v-th position in the schedule.  DUAL: the second problem's
 // tiles (u >= U0, top-k, the costlier epilogue) come first, so that a CTA's
 // last tile, whose epilogue nothing overlaps, is an argmax tile.  Each tile
@@ -426,8 +448,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = slot; v < U && ok; v += nslots) {
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
-                const int m = second ? 0 : (PAIR ? 2 * (u % num_mt) + rank : u % num_m);
-                const int n = second ? u - U0 : u / num_mt;
+                const TileMN tm = tile_mn(second ? 0 : u, num_mt, p.num_n, p.group);
+                const int m = second ? 0 : (PAIR ? 2 * tm.mt + rank : tm.mt);
+                const int n = second ? u - U0 : tm.n;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const CUtensorMap* mA = second ? &tmA2 : &tmA;
@@ -487,7 +510,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int v = slot; v < U && ok; v += nslots, ++tile_i) {
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
-                const int n = second ? u - U0 : u / num_mt;
+                const int n = second ? u - U0 : tile_mn(u, num_mt, p.num_n, p.group).n;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const uint32_t idesc = second ? (sp.big ? p.idesc2 : p.idesc2_s) : (sp.big ? p.idesc : p.idesc_s);
@@ -569,12 +592,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 ok = epilogue_tile<KT, ENT, true>(p, tfull, tempty, 0, abort_flag, tmem_base, tile_i, q, rit,
                                                   p.M_rows, p.N_w, 0, u, tile_span(u, p.num_n, p.bn, p.nbig, true), 1,
                                                   em, es, et);
-            else
+            else {
+                const TileMN tm = tile_mn(u, num_mt, p.num_n, p.group);
                 ok = epilogue_tile<KT, ENT, false>(p, tfull, tempty, tempty_first, abort_flag, tmem_base, tile_i, q,
-                                                   rit, p.M_rows, p.N_w,
-                                                   PAIR ? 2 * (u % num_mt) + rank : u % num_m, u / num_mt,
-                                                   tile_span(u / num_mt, p.num_n, p.bn, p.nbig, true), num_m, em, es,
-                                                   et);
+                                                   rit, p.M_rows, p.N_w, PAIR ? 2 * tm.mt + rank : tm.mt, tm.n,
+                                                   tile_span(tm.n, p.num_n, p.bn, p.nbig, true), num_m, em, es, et);
+            }
             if (!ok) break;
         }
         if constexpr (ENT) {
@@ -791,7 +814,7 @@ static int set_ring(GemmParams& p, int one_tile_a_rows, bool pair = false) {
         p.stages = STAGES;
     } else {
         p.a_alloc = one_tile_a_rows > 0 ? one_tile_a_rows * BK * 2 : A_BYTES;   // a multiple of 1024
-        int st = RING_BUDGET / (p.a_alloc + b_bytes);
+        int st = (pair ? RING_BUDGET_PAIR : RING_BUDGET) / (p.a_alloc + b_bytes);
         p.stages = st < STAGES ? STAGES : (st > STAGES_MAX ? STAGES_MAX : st);
     }
     p.stage_bytes = p.a_alloc + b_bytes;
@@ -876,7 +899,19 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     p.idesc = umma_idesc_bf16(split * BM, bn);
     p.idesc_s = p.nbig < p.num_n ? umma_idesc_bf16(split * BM, bn - 16) : p.idesc;
     p.num_k = cdiv(d, BK);
-    p.weight_evict_first = p.num_m == 1;
+    // Weight tiles are read by every activation tile at about the same time and
+    // never again: first out of L2, so that the activations (read once per
+    // weight tile; 80 MB for 15,616 rows) stay resident.
+    p.weight_evict_first = 1;
+    // paired sweeps: activation groups of at most PAIR_GROUP_BYTES, evened out
+    const int num_mt = pair ? cdiv(num_m, 2) : num_m;
+    p.group = num_mt;
+    if (pair) {
+        const long per_mt = 2L * BM * d * 2;   // activation bytes of one tile pair
+        const int most = (int)(PAIR_GROUP_BYTES / per_mt) > 0 ? (int)(PAIR_GROUP_BYTES / per_mt) : 1;
+        const int groups = cdiv(num_mt, most);
+        p.group = cdiv(num_mt, groups);
+    }
     p.a_bytes = a_rows * BK * 2;
     p.timeout_ns = wait_timeout_ns();
     const int smem = set_ring(p, num_m == 1 ? a_rows : 0, pair);
@@ -1002,6 +1037,7 @@ wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, 
     p.idesc2_s = p.nbig2 < p.num_n2 ? umma_idesc_bf16(BM, p.bn2 - 16) : p.idesc2;
     p.num_k = cdiv(d, BK);
     p.weight_evict_first = 1;
+    p.group = 1;
     p.a_bytes = a_rows * BK * 2;
     p.ids = ids;
     p.maxlogit = maxlogit;
