@@ -46,7 +46,10 @@ def _gapped_hidden(seed, P, d, W, reject=True):
                                    (5, 8, 40), (256, 192, 2048), (129, 256, 257),
                                    # evened-out tiles of two heights; the last one past the matrix
                                    (40, 256, 76000), (97, 128, 76003),
-                                   (9, 16384, 1000)])   # the largest hidden size
+                                   (9, 16384, 1000),    # the largest hidden size
+                                   # paired CTAs with an odd count of activation tiles: the last
+                                   # pair's second CTA loads rows past the matrix (zero fill)
+                                   (300, 128, 3001), (1100, 64, 2049), (383, 2560, 5000)])
 def test_lmhead_argmax(P, d, V):
     W = synth.normal_bf16(7 + P, 0, V, d, 0.02 if d >= 256 else 0.1)
     h = _gapped_hidden(11 + V, P, d, W)
@@ -198,7 +201,8 @@ def _check_lse(got, x):
 
 
 @pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
-                                      (1, 2560, 32000, 10), (2, 16384, 500, 16)])
+                                      (1, 2560, 32000, 10), (2, 16384, 500, 16),
+                                      (300, 128, 4000, 10)])   # paired CTAs, odd count of activation tiles
 def test_draft_topk(B, d, Vd, k):
     Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
     ws = wf.Workspace(1, B, 1, Vd, k)
