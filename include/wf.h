@@ -21,7 +21,11 @@
  * Conventions shared by every call
  * - Pointers named as device buffers must be device (or managed) memory
  *   allocated by the caller; the library allocates nothing and keeps no
- *   per-call state outside the caller's workspace.
+ *   per-call state outside the caller's workspace.  Operands the kernels copy
+ *   with the tensor-memory accelerator or bulk copies (weight matrices,
+ *   hidden states, backlog rows, the key / value caches) must be memory of
+ *   the current device: a host pointer or another GPU's memory there returns
+ *   WF_ERR_INVALID_ARG.
  * - bf16 tensors are passed as raw uint16 bit patterns, row-major, densely
  *   packed (row stride = number of columns), 16-byte aligned.
  * - Every call is asynchronous on `stream`: it validates its arguments on the
@@ -437,7 +441,7 @@ typedef struct wf_catchup_args {
     const uint16_t* Wo;        /* [din, H*D] bf16 */
     uint16_t* Kc;              /* [B, cap, G*D] bf16 key cache (rotated keys), in/out */
     uint16_t* Vc;              /* [B, cap, G*D] bf16 value cache, in/out */
-    int cap;                   /* cache rows per sequence */
+    int cap;                   /* cache rows per sequence; B * cap < 2^31 - 4096 */
     float* out;                /* [B, din] fp32 out (wf_catchup) */
     float* attn;               /* [B, H*D] fp32 out or NULL: the final token's attention output */
 } wf_catchup_args;

@@ -319,6 +319,7 @@ size_t wf_catchup_workspace_bytes(int B, int N, int din, int H, int G, int D) {
 static wf_status check_catchup(const wf_catchup_args* a, void* ws, size_t ws_bytes, bool with_final) {
     if (!a) return WF_ERR_INVALID_ARG;
     if (bad_catchup_shape(a->B, a->N, a->din, a->H, a->G, a->D) || a->cap < 1) return WF_ERR_INVALID_ARG;
+    if ((long long)a->B * a->cap > 0x7FFFFFFFll - 4096) return WF_ERR_INVALID_ARG;   // cache rows as int coordinates
     if (!a->u || !a->bl_off || !a->cache_len || !a->gamma || !a->Wk || !a->Wv || !a->Kc || !a->Vc)
         return WF_ERR_INVALID_ARG;
     if (with_final && (!a->Wq || !a->Wo || !a->out)) return WF_ERR_INVALID_ARG;
@@ -330,7 +331,7 @@ static wf_status check_catchup(const wf_catchup_args* a, void* ws, size_t ws_byt
     WF_TRY(check_ws(ws, ws_bytes, catchup_workspace_bytes(a->B, a->N, a->din, a->H, a->G, a->D)));
     WF_TRY(check_device());
     // the projections read the weights and the normalised rows (in the workspace) by TMA
-    return check_local({a->u, a->Wk, a->Wv, a->Wq, a->Wo, ws});
+    return check_local({a->u, a->Wk, a->Wv, a->Wq, a->Wo, a->Kc, a->Vc, ws});
 }
 
 wf_status wf_catchup_kv(const wf_catchup_args* a, void* ws, size_t ws_bytes, wf_stream_t stream) {

@@ -28,6 +28,7 @@
 //                  shared memory before the dependency wait (mma.sync)
 //
 // Every wait inside a kernel is bounded (WF_ERR_TIMEOUT, no trap).
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include <mutex>
@@ -50,7 +51,8 @@ constexpr int PJ_A_BYTES = BM * BK * 2;           // 16 KB
 constexpr int PJ_MAX_SPLIT = 8;      // K splits of one tile: the portable cluster size
 constexpr int PJ_BN_CU = 192;        // widest output tile: partial, reduced and staged tiles fit the ring
 constexpr int AT_MAX_CHUNKS = 64;    // cache-row splits per (sequence, KV head)
-constexpr int AT_PASS_ROWS = 128;    // cache rows an attention CTA stages per pass (two passes in flight)
+constexpr int AT_PASS_ROWS = 64;     // cache rows of one ring stage of an attention CTA
+constexpr int AT_STAGES = 4;         // ring stages: three passes in flight while one is computed
 constexpr int AT_SPLIT_ROWS = 256;   // smallest split of a cache worth its merge
 constexpr int AT_CLUSTER_MAX = 16;   // splits merged inside one thread-block cluster (non-portable above 8)
 constexpr int NORM_ROWS_PER_CTA = 4;
@@ -646,6 +648,8 @@ struct AtParams {
     uint32_t* cnt;             // [B * G] arrivals, zero at rest
     uint16_t* obf;             // [B, HD] bf16 output (operand of the output projection)
     float* attn;               // [B, HD] fp32 output or null
+    Control* ctrl;
+    uint64_t timeout_ns;       // bound of every wait on a ring stage
 };
 
 // mma.sync m16n8k16, bf16 inputs, fp32 accumulators (row-major A, column-major B)
@@ -682,32 +686,39 @@ __device__ __forceinline__ float2 dsmem_ld2(uint32_t addr) {
 
 // One CTA (4 warps) per (cache-row split, KV head, sequence).  The group's hq
 // <= 16 query heads form the 16 rows of an mma.sync A operand (bf16, pre-scaled
-// by log2(e) / sqrt(D), padding rows zero); a pass stages 128 cache rows of K
-// and V in shared memory with asynchronous copies (the next pass streams in
-// while this one is computed) and each warp takes 32 of them:
-//   S = Q K^T      (D/16 k-steps x 4 key tiles of 8)
+// by log2(e) / sqrt(D), padding rows zero).  The split's cache rows stream
+// through a ring of AT_STAGES stages of 64 rows of K and V (asynchronous
+// copies; the next three passes are in flight while one is computed, so a
+// CTA keeps about 60 KB of loads outstanding) and each warp takes 16 rows of
+// a pass:
+//   S = Q K^T      (D/16 k-steps x 2 key tiles of 8)
 //   running max / sum per head in the base-2 domain, P = exp2(S - max) as bf16
-//   O += P V       (2 key steps of 16 x D/8 dim tiles; V fragments by ldmatrix.trans)
+//   O += P V       (one key step of 16 x D/8 dim tiles; V fragments by ldmatrix.trans)
 // Each warp keeps its own (max, sum, O) over its keys; the four are merged at
 // the end.  The splits of a (sequence, KV head) are then merged in index
 // order: with at most AT_CLUSTER_MAX splits they form one thread-block
 // cluster, each leaves its partial in its own shared memory and finishes a
 // slice of the outputs over distributed shared memory; with more, partials go
 // through global memory and the last CTA to arrive merges them.  The old cache
-// rows of the first two passes are copied before the dependency wait.
+// rows of the first three passes are copied before the dependency wait.
 constexpr int AT_THREADS = 128;
-constexpr int AT_WARP_ROWS = 32;   // cache rows a warp takes per pass
+constexpr int AT_WARP_ROWS = 16;   // cache rows a warp takes per pass
 constexpr int AT_MAX_DT = 16;      // D / 8 dim tiles: D <= 128
 
-__global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+__global__ void __launch_bounds__(AT_THREADS)
+    attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const AtParams p) {
+    extern __shared__ __align__(16) uint8_t smem_dyn[];
+    // tensor copies land on 128-byte boundaries
+    uint8_t* smem_raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
     const int D = p.D, hq = p.hq;
     const int R = AT_PASS_ROWS;
-    const int stride = D + 8;                 // padded row (bf16 elements): conflict-free fragment loads
-    const size_t buf = (size_t)2 * R * stride;   // one pass: K rows then V rows
+    const int stride = D;                     // a stage's rows as the tensor copy lays them out
+    const int qstride = D + 8;                // padded query rows: conflict-free fragment loads
+    const size_t buf = (size_t)2 * R * stride;   // one stage: K rows then V rows
     uint16_t* Kbuf = reinterpret_cast<uint16_t*>(smem_raw);
-    uint16_t* qs = Kbuf + 2 * buf;            // [16][stride] bf16 query rows (zero padding)
-    int* last = reinterpret_cast<int*>(qs + 16 * stride);
+    uint16_t* qs = Kbuf + AT_STAGES * buf;    // [16][qstride] bf16 query rows (zero padding)
+    uint64_t* full = reinterpret_cast<uint64_t*>(qs + 16 * qstride);   // [AT_STAGES] stage barriers
+    int* last = reinterpret_cast<int*>(full + AT_STAGES);
     float* red = reinterpret_cast<float*>(Kbuf);   // warp merge area, after the last pass
 
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -720,64 +731,62 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     Lold = Lold < 0 ? 0 : (Lold > T ? T : Lold);
     const int per = (T + p.chunks - 1) / p.chunks;
     const int t0 = c * per, t1 = min(T, t0 + per);
-    const uint16_t* Kb = p.Kc + (size_t)b * p.cap * p.GD + (size_t)g * D;
-    const uint16_t* Vb = p.Vc + (size_t)b * p.cap * p.GD + (size_t)g * D;
-    const int cpr = D / 8;   // 16-byte pieces per row
-    // asynchronous copies of rows [rfrom, rto) of the pass at p0 into buffer `which`
-    auto stage_rows = [&](int p0, int which, int rfrom, int rto) {
+    const int npass = t0 < t1 ? (t1 - t0 + R - 1) / R : 0;
+    // A stage is one box of R cache rows x D columns of keys and one of values,
+    // two tensor copies issued by one thread.  The box may run past the split
+    // (those rows are masked below; past the last sequence they read as zero).
+    const int gy0 = b * p.cap;   // this sequence's first row of the [B * cap, G * D] cache view
+    const uint64_t pol = policy_evict_first();   // the cache is read once
+    auto issue = [&](int pass) {   // thread 0
+        const int which = pass % AT_STAGES;
         uint16_t* Kd = Kbuf + which * buf;
-        uint16_t* Vd = Kd + (size_t)R * stride;
-        for (int idx = tid; idx < (rto - rfrom) * cpr; idx += AT_THREADS) {
-            const int r = rfrom + idx / cpr, j = idx - (idx / cpr) * cpr;
-            cp_async16(Kd + (size_t)r * stride + j * 8, Kb + (size_t)(p0 + r) * p.GD + j * 8);
-            cp_async16(Vd + (size_t)r * stride + j * 8, Vb + (size_t)(p0 + r) * p.GD + j * 8);
+        mbar_arrive_expect_tx(&full[which], 2u * (uint32_t)R * (uint32_t)D * 2u);
+        tma_load_2d(Kd, &tmK, &full[which], g * D, gy0 + t0 + pass * R, pol);
+        tma_load_2d(Kd + (size_t)R * stride, &tmV, &full[which], g * D, gy0 + t0 + pass * R, pol);
+    };
+    bool waits_ok = true;
+    auto wait_stage = [&](int pass) {
+        if (!mbar_wait(&full[pass % AT_STAGES], (uint32_t)(pass / AT_STAGES) & 1u, p.timeout_ns, nullptr) &&
+            waits_ok) {
+            waits_ok = false;
+            if (tid == 0) record_error(p.ctrl, WF_ERR_TIMEOUT, 0x600u + (uint32_t)c);
         }
     };
-    // value rows past the range are multiplied by probability 0: they must
-    // hold numbers, not whatever the buffer held before
-    auto zero_tail = [&](int which, int nr) {
-        uint16_t* Vd = Kbuf + which * buf + (size_t)R * stride;
-        for (int idx = tid; idx < (R - nr) * cpr; idx += AT_THREADS) {
-            const int r = nr + idx / cpr, j = idx - (idx / cpr) * cpr;
-            *reinterpret_cast<uint4*>(Vd + (size_t)r * stride + j * 8) = make_uint4(0, 0, 0, 0);
-        }
-    };
-    auto stage = [&](int p0, int which) {
-        const int nr = min(R, t1 - p0);
-        stage_rows(p0, which, 0, nr);
-        zero_tail(which, nr);
-        cp_async_commit();
-    };
-    // the previously cached rows of the first two passes stream in while the
-    // kernel before this one (which writes the new rows and the query) finishes
-    const int nr0 = t0 < t1 ? min(R, t1 - t0) : 0;
-    const int split0 = max(0, min(nr0, Lold - t0));
-    const int nr1 = t0 + R < t1 ? min(R, t1 - t0 - R) : 0;
-    const int split1 = max(0, min(nr1, Lold - t0 - R));
-    if (nr0 > 0) {
-        stage_rows(t0, 0, 0, split0);
-        zero_tail(0, nr0);
+    constexpr int PRE = AT_STAGES - 1;
+    // stages whose whole box lies in the previously cached rows (no kernel of
+    // this call writes them) stream in while the kernel before this one
+    // (which writes the new rows and the query) finishes; the rest after it
+    int npre = 0;
+    while (npre < PRE && npre < npass && t0 + (npre + 1) * R <= Lold) ++npre;
+    if (tid == 0) {
+        for (int i = 0; i < AT_STAGES; ++i) mbar_init(&full[i], 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        for (int i = 0; i < npre; ++i) issue(i);
     }
-    if (nr1 > 0) {
-        stage_rows(t0 + R, 1, 0, split1);
-        zero_tail(1, nr1);
+    // query padding rows (heads hq..15) are zero whatever the query
+    for (int i = tid; i < (16 - hq) * D; i += AT_THREADS) {
+        const int h = hq + i / D, e = i - (i / D) * D;
+        qs[h * qstride + e] = 0;
     }
-    cp_async_commit();
     pdl_wait();
     pdl_trigger();
+    if (tid == 0)
+        for (int i = npre; i < PRE && i < npass; ++i) issue(i);
     const float qscale = 1.4426950408889634f / sqrtf((float)D);
-    for (int i = tid; i < 16 * D; i += AT_THREADS) {
-        const int h = i / D, e = i - h * D;
-        const float v = h < hq ? p.q[(size_t)b * p.HD + ((size_t)g * hq + h) * D + e] * qscale : 0.f;
-        qs[h * stride + e] = f32_to_bf16(v);
+    {
+        const int nq4 = hq * D / 4;   // D is a multiple of 8
+        const float4* q4 = reinterpret_cast<const float4*>(p.q + (size_t)b * p.HD + (size_t)g * hq * D);
+        for (int i = tid; i < nq4; i += AT_THREADS) {
+            const float4 v = q4[i];
+            const int h = (4 * i) / D, e = 4 * i - h * D;
+            uint16_t* d = qs + h * qstride + e;
+            *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16x2(v.x * qscale, v.y * qscale),
+                                                      pack_bf16x2(v.z * qscale, v.w * qscale));
+        }
     }
-    // rows this call appends, one copy group per pass, so that the first pass
-    // need not wait for the second pass's rows
-    if (nr0 > 0) stage_rows(t0, 0, split0, nr0);
-    cp_async_commit();
-    if (nr1 > 0) stage_rows(t0 + R, 1, split1, nr1);
-    cp_async_commit();
-    __syncthreads();   // qs written
+    __syncthreads();   // qs written, the stage barriers initialised
 
     const int nks = D / 16, ndt = D / 8;
     // Q fragments (A operand), one set per 16-dim k-step
@@ -786,7 +795,7 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     for (int ks = 0; ks < AT_MAX_DT / 2; ++ks)
         if (ks < nks) {
             const int mi = lane >> 3, r = lane & 7;
-            ldsm_x4(qa[ks], smem_u32(qs + ((mi & 1) * 8 + r) * stride + ks * 16 + (mi >> 1) * 8));
+            ldsm_x4(qa[ks], smem_u32(qs + ((mi & 1) * 8 + r) * qstride + ks * 16 + (mi >> 1) * 8));
         }
     float o[AT_MAX_DT][4];
 #pragma unroll
@@ -794,43 +803,33 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     float m_lo = -INFINITY, m_hi = -INFINITY;   // running max of rows gq and gq + 8
     float l_lo = 0.f, l_hi = 0.f;               // this thread's share of the running sums
 
-    int pass = 0;
-    for (int p0 = t0; p0 < t1; p0 += R, ++pass) {
-        if (pass == 0) {
-            cp_async_wait_1();   // all but the second pass's appended rows
-        } else if (p0 + R < t1) {   // passes 0 and 1 were staged before the loop
-            stage(p0 + R, (pass + 1) & 1);
-            cp_async_wait_1();
-        } else {
-            cp_async_wait_0();
-        }
-        __syncthreads();
-        const uint16_t* Ks = Kbuf + (pass & 1) * buf;
+    for (int pass = 0; pass < npass; ++pass) {
+        // refill the stage the previous pass freed: PRE passes stay in flight
+        if (tid == 0 && pass + PRE < npass) issue(pass + PRE);   // the stage the previous pass freed
+        wait_stage(pass);   // this pass's rows have landed
+        const int p0 = t0 + pass * R;
+        const uint16_t* Ks = Kbuf + (pass % AT_STAGES) * buf;
         const uint16_t* Vs = Ks + (size_t)R * stride;
         const int k0 = warp * AT_WARP_ROWS;                     // this warp's rows of the pass
         const int nvalid = min(AT_WARP_ROWS, t1 - p0 - k0);     // may be <= 0
         if (nvalid > 0) {
-            // S = Q K^T over this warp's 32 rows: four 8-row key tiles
-            float sc[4][4];
+            // S = Q K^T over this warp's 16 rows: two 8-row key tiles
+            float sc[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < AT_MAX_DT / 2; ++ks) {
                 if (ks >= nks) break;
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {   // two key tiles per ldmatrix.x4
-                    uint32_t kb[4];
-                    const int mi = lane >> 3, r = lane & 7;
-                    ldsm_x4(kb, smem_u32(Ks + (size_t)(k0 + np * 16 + (mi >> 1) * 8 + r) * stride + ks * 16 +
-                                         (mi & 1) * 8));
-                    mma_bf16_16816(sc[np * 2], qa[ks], kb[0], kb[1]);
-                    mma_bf16_16816(sc[np * 2 + 1], qa[ks], kb[2], kb[3]);
-                }
+                uint32_t kb[4];   // both key tiles by one ldmatrix.x4
+                const int mi = lane >> 3, r = lane & 7;
+                ldsm_x4(kb, smem_u32(Ks + (size_t)(k0 + (mi >> 1) * 8 + r) * stride + ks * 16 + (mi & 1) * 8));
+                mma_bf16_16816(sc[0], qa[ks], kb[0], kb[1]);
+                mma_bf16_16816(sc[1], qa[ks], kb[2], kb[3]);
             }
             // mask rows past the range, then the running max / sum (rows gq, gq + 8)
             float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
+            for (int nt = 0; nt < 2; ++nt) {
                 const int key = nt * 8 + 2 * cq;
                 if (key >= nvalid) sc[nt][0] = sc[nt][2] = -INFINITY;
                 if (key + 1 >= nvalid) sc[nt][1] = sc[nt][3] = -INFINITY;
@@ -855,32 +854,38 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
                 o[i][2] *= a_hi;
                 o[i][3] *= a_hi;
             }
-            uint32_t pa[2][4];   // P as the A operand of two 16-key steps
+            uint32_t pa[4];   // P as the A operand of one 16-key step
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
+            for (int nt = 0; nt < 2; ++nt) {
                 const float p0v = exp2f(sc[nt][0] - mn_lo), p1v = exp2f(sc[nt][1] - mn_lo);
                 const float p2v = exp2f(sc[nt][2] - mn_hi), p3v = exp2f(sc[nt][3] - mn_hi);
                 l_lo += p0v + p1v;
                 l_hi += p2v + p3v;
-                pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0v, p1v);
-                pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2v, p3v);
+                pa[nt * 2 + 0] = pack_bf16x2(p0v, p1v);
+                pa[nt * 2 + 1] = pack_bf16x2(p2v, p3v);
             }
-            // O += P V: V fragments (keys x dims) through ldmatrix.trans
+            // O += P V: V fragments (keys x dims) through ldmatrix.trans; a lane
+            // holds keys 2 (lane & 3) + {0, 1} (and + 8) of the step
+            const int kl = 2 * cq;
+            const uint32_t vmask0 = (kl < nvalid ? 0x0000FFFFu : 0u) | (kl + 1 < nvalid ? 0xFFFF0000u : 0u);
+            const uint32_t vmask1 = (kl + 8 < nvalid ? 0x0000FFFFu : 0u) | (kl + 9 < nvalid ? 0xFFFF0000u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-                for (int dp = 0; dp < AT_MAX_DT / 2; ++dp) {   // two dim tiles per ldmatrix.x4
-                    if (2 * dp >= ndt) break;
-                    uint32_t vb[4];
-                    const int mi = lane >> 3, r = lane & 7;
-                    ldsm_x4_trans(vb, smem_u32(Vs + (size_t)(k0 + kk * 16 + (mi & 1) * 8 + r) * stride + dp * 16 +
-                                               (mi >> 1) * 8));
-                    mma_bf16_16816(o[2 * dp], pa[kk], vb[0], vb[1]);
-                    mma_bf16_16816(o[2 * dp + 1], pa[kk], vb[2], vb[3]);
+            for (int dp = 0; dp < AT_MAX_DT / 2; ++dp) {   // two dim tiles per ldmatrix.x4
+                if (2 * dp >= ndt) break;
+                uint32_t vb[4];
+                const int mi = lane >> 3, r = lane & 7;
+                ldsm_x4_trans(vb, smem_u32(Vs + (size_t)(k0 + (mi & 1) * 8 + r) * stride + dp * 16 + (mi >> 1) * 8));
+                if (nvalid < AT_WARP_ROWS) {   // rows past the split hold any bits: P is 0 there, V must be too
+                    vb[0] &= vmask0;
+                    vb[2] &= vmask0;
+                    vb[1] &= vmask1;
+                    vb[3] &= vmask1;
                 }
+                mma_bf16_16816(o[2 * dp], pa, vb[0], vb[1]);
+                mma_bf16_16816(o[2 * dp + 1], pa, vb[2], vb[3]);
             }
         }
-        __syncthreads();   // the buffer is rewritten by the next pass's copies
+        __syncthreads();   // the stage is rewritten by a later pass's copies
     }
     // sums over the four threads of each row
 #pragma unroll
@@ -1005,7 +1010,7 @@ __global__ void __launch_bounds__(AT_THREADS) attend_kernel(const AtParams p) {
     // every split's partial (outputs, max, sum) of this (sequence, KV head) into
     // shared memory at once, when it fits beside the weights; else read from L2
     const size_t nf = (size_t)p.chunks * hq * (D + 2);
-    const bool staged = (nf + 2 * (size_t)p.chunks * hq + hq) * 4 <= 2 * buf * 2;
+    const bool staged = (nf + 2 * (size_t)p.chunks * hq + hq) * 4 <= AT_STAGES * buf * 2;
     float* pm = reinterpret_cast<float*>(Kbuf);                 // [chunks][hq][D + 2] (staged)
     float* wgt = staged ? pm + nf : reinterpret_cast<float*>(Kbuf);   // [chunks][hq] split weights
     float* lsum = wgt + (size_t)p.chunks * hq;                  // [chunks][hq] split sums
@@ -1279,6 +1284,29 @@ static bool act_map(CUtensorMap* m, const void* base, int rows, int cols) {
 
 size_t catchup_attend_smem(int H, int G, int D);
 
+// [rows, cols] bf16 cache view, boxes of D columns x AT_PASS_ROWS rows laid
+// out densely (no swizzle); rows past the view read as zero
+static bool cache_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, int D) {
+    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)AT_PASS_ROWS};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // How many clusters of `size` attention CTAs with `smem` bytes each can be
 // resident at once (one query per device, size and shared-memory size; the
 // cache is shared by host threads).
@@ -1375,6 +1403,8 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     ap.cnt = reinterpret_cast<uint32_t*>(w + L.cnt);
     ap.obf = reinterpret_cast<uint16_t*>(w + L.obf);
     ap.attn = a->attn;
+    ap.ctrl = ctrl;
+    ap.timeout_ns = wait_timeout_ns();
     const size_t at_smem = catchup_attend_smem(a->H, a->G, a->D);
     static std::mutex at_mu;
     static bool at_attr[64] = {false};
@@ -1392,8 +1422,12 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
                          a->B * a->G <= attend_resident_clusters(dev, ap.chunks, at_smem)
                      ? 1
                      : 0;
+    CUtensorMap tmK, tmV;
+    if (!cache_map(&tmK, a->Kc, (uint64_t)a->B * a->cap, GD, a->D) ||
+        !cache_map(&tmV, a->Vc, (uint64_t)a->B * a->cap, GD, a->D))
+        return WF_ERR_CUDA;
     CU_TRY(launch_cluster(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s,
-                          ap.cluster ? (unsigned)ap.chunks : 1u, ap));
+                          ap.cluster ? (unsigned)ap.chunks : 1u, tmK, tmV, ap));
 
     // output projection with the residual: a GEMV for a few rows whose weight
     // slices fit in shared memory in one wave, else the tensor-core kernel
@@ -1440,7 +1474,7 @@ size_t catchup_attend_smem(int H, int G, int D) {
     (void)H;
     (void)G;
     const size_t stride = (size_t)D + 8;
-    return 2 * (2 * (size_t)AT_PASS_ROWS * stride * 2) + 16 * stride * 2 + 16;
+    return 128 + AT_STAGES * (2 * (size_t)AT_PASS_ROWS * (size_t)D * 2) + 16 * stride * 2 + AT_STAGES * 8 + 16;
 }
 
 }  // namespace wf

@@ -88,7 +88,7 @@ def test_catchup_refuses_host_weights():
     cache_len = torch.tensor([3], dtype=torch.int32, device=DEV)
     cu = wf.Catchup(u, bl_off, cache_len, gamma, Wk, Wv, Kc, Vc, G, Wq=Wq, Wo=Wo)
     for name, hp, keep in _host_buffers(H * D * din * 2):
-        for field in ("Wk", "Wv", "Wq", "Wo", "u"):
+        for field in ("Wk", "Wv", "Wq", "Wo", "u", "Kc", "Vc"):
             a = wf.CatchupArgs.from_buffer_copy(cu.args)
             setattr(a, field, hp)
             st = wf.lib().wf_catchup(ctypes.byref(a), cu.ws.ptr, cu.ws.nbytes, torch.cuda.current_stream().cuda_stream)
