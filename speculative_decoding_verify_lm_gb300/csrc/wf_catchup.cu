@@ -705,12 +705,17 @@ constexpr int AT_THREADS = 128;
 constexpr int AT_WARP_ROWS = 16;   // cache rows a warp takes per pass
 constexpr int AT_MAX_DT = 16;      // D / 8 dim tiles: D <= 128
 
+// DT = D / 8 dim tiles (a compile-time count: registers and unrolled loops
+// for exactly the head width).
+template <int DT>
 __global__ void __launch_bounds__(AT_THREADS)
     attend_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const AtParams p) {
+    static_assert(DT % 2 == 0 && DT >= 2 && DT <= AT_MAX_DT, "D is a multiple of 16, at most 128");
     extern __shared__ __align__(16) uint8_t smem_dyn[];
     // tensor copies land on 128-byte boundaries
     uint8_t* smem_raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
-    const int D = p.D, hq = p.hq;
+    constexpr int D = DT * 8;
+    const int hq = p.hq;
     const int R = AT_PASS_ROWS;
     const int stride = D;                     // a stage's rows as the tensor copy lays them out
     const int qstride = D + 8;                // padded query rows: conflict-free fragment loads
@@ -788,18 +793,17 @@ __global__ void __launch_bounds__(AT_THREADS)
     }
     __syncthreads();   // qs written, the stage barriers initialised
 
-    const int nks = D / 16, ndt = D / 8;
+    constexpr int nks = DT / 2, ndt = DT;
     // Q fragments (A operand), one set per 16-dim k-step
-    uint32_t qa[AT_MAX_DT / 2][4];
+    uint32_t qa[nks][4];
 #pragma unroll
-    for (int ks = 0; ks < AT_MAX_DT / 2; ++ks)
-        if (ks < nks) {
-            const int mi = lane >> 3, r = lane & 7;
-            ldsm_x4(qa[ks], smem_u32(qs + ((mi & 1) * 8 + r) * qstride + ks * 16 + (mi >> 1) * 8));
-        }
-    float o[AT_MAX_DT][4];
+    for (int ks = 0; ks < nks; ++ks) {
+        const int mi = lane >> 3, r = lane & 7;
+        ldsm_x4(qa[ks], smem_u32(qs + ((mi & 1) * 8 + r) * qstride + ks * 16 + (mi >> 1) * 8));
+    }
+    float o[ndt][4];
 #pragma unroll
-    for (int i = 0; i < AT_MAX_DT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < ndt; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m_lo = -INFINITY, m_hi = -INFINITY;   // running max of rows gq and gq + 8
     float l_lo = 0.f, l_hi = 0.f;               // this thread's share of the running sums
 
@@ -818,8 +822,7 @@ __global__ void __launch_bounds__(AT_THREADS)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-            for (int ks = 0; ks < AT_MAX_DT / 2; ++ks) {
-                if (ks >= nks) break;
+            for (int ks = 0; ks < nks; ++ks) {
                 uint32_t kb[4];   // both key tiles by one ldmatrix.x4
                 const int mi = lane >> 3, r = lane & 7;
                 ldsm_x4(kb, smem_u32(Ks + (size_t)(k0 + (mi >> 1) * 8 + r) * stride + ks * 16 + (mi & 1) * 8));
@@ -847,12 +850,14 @@ __global__ void __launch_bounds__(AT_THREADS)
             m_hi = mn_hi;
             l_lo *= a_lo;
             l_hi *= a_hi;
+            if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {   // a running maximum moved
 #pragma unroll
-            for (int i = 0; i < AT_MAX_DT; ++i) {
-                o[i][0] *= a_lo;
-                o[i][1] *= a_lo;
-                o[i][2] *= a_hi;
-                o[i][3] *= a_hi;
+                for (int i = 0; i < ndt; ++i) {
+                    o[i][0] *= a_lo;
+                    o[i][1] *= a_lo;
+                    o[i][2] *= a_hi;
+                    o[i][3] *= a_hi;
+                }
             }
             uint32_t pa[4];   // P as the A operand of one 16-key step
 #pragma unroll
@@ -870,8 +875,7 @@ __global__ void __launch_bounds__(AT_THREADS)
             const uint32_t vmask0 = (kl < nvalid ? 0x0000FFFFu : 0u) | (kl + 1 < nvalid ? 0xFFFF0000u : 0u);
             const uint32_t vmask1 = (kl + 8 < nvalid ? 0x0000FFFFu : 0u) | (kl + 9 < nvalid ? 0xFFFF0000u : 0u);
 #pragma unroll
-            for (int dp = 0; dp < AT_MAX_DT / 2; ++dp) {   // two dim tiles per ldmatrix.x4
-                if (2 * dp >= ndt) break;
+            for (int dp = 0; dp < ndt / 2; ++dp) {   // two dim tiles per ldmatrix.x4
                 uint32_t vb[4];
                 const int mi = lane >> 3, r = lane & 7;
                 ldsm_x4_trans(vb, smem_u32(Vs + (size_t)(k0 + (mi & 1) * 8 + r) * stride + dp * 16 + (mi >> 1) * 8));
@@ -898,13 +902,12 @@ __global__ void __launch_bounds__(AT_THREADS)
     const int rs = D + 2;
     float* rw = red + (size_t)warp * 16 * rs;
 #pragma unroll
-    for (int i = 0; i < AT_MAX_DT; ++i)
-        if (i < ndt) {
-            rw[gq * rs + i * 8 + 2 * cq] = o[i][0];
-            rw[gq * rs + i * 8 + 2 * cq + 1] = o[i][1];
-            rw[(gq + 8) * rs + i * 8 + 2 * cq] = o[i][2];
-            rw[(gq + 8) * rs + i * 8 + 2 * cq + 1] = o[i][3];
-        }
+    for (int i = 0; i < ndt; ++i) {
+        rw[gq * rs + i * 8 + 2 * cq] = o[i][0];
+        rw[gq * rs + i * 8 + 2 * cq + 1] = o[i][1];
+        rw[(gq + 8) * rs + i * 8 + 2 * cq] = o[i][2];
+        rw[(gq + 8) * rs + i * 8 + 2 * cq + 1] = o[i][3];
+    }
     if (cq == 0) {
         rw[gq * rs + D] = m_lo;
         rw[gq * rs + D + 1] = l_lo;
@@ -1284,6 +1287,22 @@ static bool act_map(CUtensorMap* m, const void* base, int rows, int cols) {
 
 size_t catchup_attend_smem(int H, int G, int D);
 
+using AttendFn = void (*)(CUtensorMap, CUtensorMap, AtParams);
+// the attention kernel for head width D (a multiple of 16 up to 128)
+static AttendFn attend_fn(int D) {
+    switch (D / 8) {
+        case 2: return attend_kernel<2>;
+        case 4: return attend_kernel<4>;
+        case 6: return attend_kernel<6>;
+        case 8: return attend_kernel<8>;
+        case 10: return attend_kernel<10>;
+        case 12: return attend_kernel<12>;
+        case 14: return attend_kernel<14>;
+        case 16: return attend_kernel<16>;
+        default: return nullptr;
+    }
+}
+
 // [rows, cols] bf16 cache view, boxes of D columns x AT_PASS_ROWS rows laid
 // out densely (no swizzle); rows past the view read as zero
 static bool cache_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, int D) {
@@ -1310,10 +1329,11 @@ static bool cache_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_
 // How many clusters of `size` attention CTAs with `smem` bytes each can be
 // resident at once (one query per device, size and shared-memory size; the
 // cache is shared by host threads).
-static int attend_resident_clusters(int dev, int size, size_t smem) {
+static int attend_resident_clusters(int dev, int size, size_t smem, AttendFn fn) {
     struct Entry {
         int dev, size;
         size_t smem;
+        AttendFn fn;
         int n;
     };
     static Entry seen[64];
@@ -1321,7 +1341,8 @@ static int attend_resident_clusters(int dev, int size, size_t smem) {
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < nseen; ++i)
-        if (seen[i].dev == dev && seen[i].size == size && seen[i].smem == smem) return seen[i].n;
+        if (seen[i].dev == dev && seen[i].size == size && seen[i].smem == smem && seen[i].fn == fn)
+            return seen[i].n;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size, 1, 1);
     cfg.blockDim = dim3(AT_THREADS, 1, 1);
@@ -1334,11 +1355,11 @@ static int attend_resident_clusters(int dev, int size, size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
     }
-    if (nseen < 64) seen[nseen++] = {dev, size, smem, n};
+    if (nseen < 64) seen[nseen++] = {dev, size, smem, fn, n};
     return n;
 }
 
@@ -1408,25 +1429,30 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     const size_t at_smem = catchup_attend_smem(a->H, a->G, a->D);
     static std::mutex at_mu;
     static bool at_attr[64] = {false};
+    const AttendFn at_fn = attend_fn(a->D);
+    if (!at_fn) return WF_ERR_INVALID_ARG;
     CU_TRY(configure_once(at_mu, at_attr, [] {
-        return cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
-                   cudaSuccess &&
-               cudaFuncSetAttribute(attend_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
-                   cudaSuccess &&
-               cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        for (int dt = 2; dt <= AT_MAX_DT; dt += 2) {
+            const AttendFn f = attend_fn(dt * 8);
+            if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess ||
+                cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
+                cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                return false;
+        }
+        return true;
     }));
     // few splits: each (sequence, KV head) is one cluster and merges on chip,
     // provided all of the clusters are resident at once (a CTA that finishes
     // early holds its slot until its cluster has merged)
     ap.cluster = ap.chunks > 1 && ap.chunks <= AT_CLUSTER_MAX &&
-                         a->B * a->G <= attend_resident_clusters(dev, ap.chunks, at_smem)
+                         a->B * a->G <= attend_resident_clusters(dev, ap.chunks, at_smem, at_fn)
                      ? 1
                      : 0;
     CUtensorMap tmK, tmV;
     if (!cache_map(&tmK, a->Kc, (uint64_t)a->B * a->cap, GD, a->D) ||
         !cache_map(&tmV, a->Vc, (uint64_t)a->B * a->cap, GD, a->D))
         return WF_ERR_CUDA;
-    CU_TRY(launch_cluster(attend_kernel, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s,
+    CU_TRY(launch_cluster(at_fn, dim3(ap.chunks, a->G, a->B), dim3(AT_THREADS), at_smem, s,
                           ap.cluster ? (unsigned)ap.chunks : 1u, tmK, tmV, ap));
 
     // output projection with the residual: a GEMV for a few rows whose weight
