@@ -56,6 +56,10 @@ constexpr long PAIR_GROUP_BYTES = 48L << 20;
 constexpr int RING_BUDGET_PAIR = 224 * 1024;
 constexpr int GEMM_SMEM_MAX = RING_BUDGET_PAIR + 1024 + 256;
 constexpr int KT_TOPK = WF_MAX_TOPK;
+// A narrower candidate list for k <= 10 (EAGLE-3's top-10): a tile's list is
+// its 10 best, so an insertion shifts 9 entries instead of 15 and fewer
+// logits clear the list's smallest entry.
+constexpr int KT_TOPK10 = 10;
 MergeArgs merge_args(int B, int Vd, int num_n, int k, const int32_t* d2t, int32_t* draft_ids, int32_t* tids,
                      float* vals, void* ws, size_t cand_off, float* lse = nullptr, size_t lsep_off = 0);
 wf_status launch_topk_merge(const MergeArgs& a, void* ws, cudaStream_t s);
@@ -720,7 +724,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // --------------------------------------------------------------------- top-k merge
 // One CTA per activation row (wf_merge.cuh).
 __global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const MergeArgs a, Control* ctrl) {
-    __shared__ uint64_t wbest[MERGE_THREADS / 32];
+    __shared__ uint64_t wbest[MERGE_SCRATCH];
     pdl_wait();
     pdl_trigger();
     topk_merge_row(a, blockIdx.x, wbest, ctrl);
@@ -975,7 +979,8 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
     p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
     p.lsep = lse ? reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws) + lsep_off) : nullptr;
     int num_n = 0;
-    wf_status st = launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s, &num_n);
+    wf_status st = k <= KT_TOPK10 ? launch_select<KT_TOPK10, false>(x, B, Wd, Vd, d, p, s, &num_n)
+                                  : launch_select<KT_TOPK, false>(x, B, Wd, Vd, d, p, s, &num_n);
     if (st != WF_OK) return st;
     return launch_topk_merge(merge_args(B, Vd, num_n, k, d2t, draft_ids, tids, vals, ws, cand_off, lse, lsep_off),
                              ws, s);

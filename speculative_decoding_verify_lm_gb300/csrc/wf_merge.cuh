@@ -11,6 +11,9 @@
 namespace wf {
 
 constexpr int MERGE_THREADS = 128;
+// Shared scratch of one merge (8-byte words): a word per warp for the
+// block-wide max, then the k winners in order.
+constexpr int MERGE_SCRATCH = MERGE_THREADS / 32 + WF_MAX_TOPK;
 
 struct MergeArgs {
     const uint64_t* cand;   // [num_n][num_m * BM][k] packed keys (0 = none), zeroed as read
@@ -26,9 +29,11 @@ struct MergeArgs {
 
 // One CTA (MERGE_THREADS threads) merges row `row`: every thread keeps the
 // WF_MAX_TOPK best of its share of the candidate lists, then k rounds of a
-// block-wide max pick the winners in order.  Keys are unique per row (each
-// weight row lives in one tile), so exactly one thread owns each winner.
-// wbest: MERGE_THREADS / 32 words of shared memory.
+// block-wide max pick the winners in order (on chip only); k threads then
+// map the winners to target ids and write them, all lookups in flight
+// together.  Keys are unique per row (each weight row lives in one tile), so
+// exactly one thread owns each winner.  wbest: MERGE_SCRATCH words of shared
+// memory.
 __device__ __forceinline__ void topk_merge_row(const MergeArgs& a, int row, uint64_t* wbest, Control* ctrl) {
     constexpr int KT = WF_MAX_TOPK;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -112,20 +117,24 @@ __device__ __forceinline__ void topk_merge_row(const MergeArgs& a, int row, uint
             for (int s = 0; s < KT - 1; ++s) loc[s] = loc[s + 1];
             loc[KT - 1] = 0;
         }
-        if (threadIdx.x == 0) {
-            const size_t o = (size_t)row * k + j;
-            int32_t id = -1, tid = -1;
-            float v = __int_as_float(0x7fc00000);
-            if (best != 0) {
-                id = (int32_t)key_id(best);
-                v = key_val(best);
-                tid = (id >= 0 && id < a.Vd) ? a.d2t[id] : -1;
-                if (tid < 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)row);
-            }
-            if (a.draft_ids) a.draft_ids[o] = id;
-            if (a.tids) a.tids[o] = tid;
-            if (a.vals) a.vals[o] = v;
+        if (threadIdx.x == 0) wbest[MERGE_THREADS / 32 + j] = best;
+    }
+    __syncthreads();
+    if ((int)threadIdx.x < k) {
+        const int j = threadIdx.x;
+        const uint64_t best = wbest[MERGE_THREADS / 32 + j];
+        const size_t o = (size_t)row * k + j;
+        int32_t id = -1, tid = -1;
+        float v = __int_as_float(0x7fc00000);
+        if (best != 0) {
+            id = (int32_t)key_id(best);
+            v = key_val(best);
+            tid = (id >= 0 && id < a.Vd) ? a.d2t[id] : -1;
+            if (tid < 0) record_error(ctrl, WF_ERR_BAD_DATA, (uint32_t)row);
         }
+        if (a.draft_ids) a.draft_ids[o] = id;
+        if (a.tids) a.tids[o] = tid;
+        if (a.vals) a.vals[o] = v;
     }
 }
 

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
     // CTAs past the verification ones merge the draft head's candidate lists
     // (one row each): they depend on the weight sweep only, like verification
     if ((int)blockIdx.x >= nverify) {
-        __shared__ uint64_t s_wbest[MERGE_THREADS / 32];
+        __shared__ uint64_t s_wbest[MERGE_SCRATCH];
         pdl_wait();
         pdl_trigger();
         topk_merge_row(mg, (int)blockIdx.x - nverify, s_wbest, ctrl);

@@ -202,7 +202,8 @@ def _check_lse(got, x):
 
 @pytest.mark.parametrize("B,d,Vd,k", [(1, 256, 1000, 10), (3, 128, 32000, 10), (130, 64, 700, 16), (2, 72, 300, 1),
                                       (1, 2560, 32000, 10), (2, 16384, 500, 16),
-                                      (300, 128, 4000, 10)])   # paired CTAs, odd count of activation tiles
+                                      (300, 128, 4000, 10),    # paired CTAs, odd count of activation tiles
+                                      (5, 96, 3000, 12)])      # the 16-wide candidate lists, 12 kept
 def test_draft_topk(B, d, Vd, k):
     Wd, d2t, x, dids, tids, vals = _draft_case(B, d, Vd, k)
     ws = wf.Workspace(1, B, 1, Vd, k)
