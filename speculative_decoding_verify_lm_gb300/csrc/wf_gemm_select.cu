@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) topk_merge_kernel(const MergeAr
     __shared__ uint64_t wbest[MERGE_SCRATCH];
     pdl_wait();
     pdl_trigger();
-    topk_merge_row(a, blockIdx.x, wbest, ctrl);
+    topk_merge_row<12>(a, blockIdx.x, wbest, ctrl);
 }
 
 // --------------------------------------------------------------------- host side

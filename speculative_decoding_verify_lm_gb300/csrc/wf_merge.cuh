@@ -33,7 +33,10 @@ struct MergeArgs {
 // map the winners to target ids and write them, all lookups in flight
 // together.  Keys are unique per row (each weight row lives in one tile), so
 // exactly one thread owns each winner.  wbest: MERGE_SCRATCH words of shared
-// memory.
+// memory.  BATCH candidates of a thread are loaded together: the standalone
+// merge (many rows, a CTA each) loads all of them at once, the merge CTAs
+// beside the verification keep to a few.
+template <int BATCH>
 __device__ __forceinline__ void topk_merge_row(const MergeArgs& a, int row, uint64_t* wbest, Control* ctrl) {
     constexpr int KT = WF_MAX_TOPK;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -71,7 +74,6 @@ __device__ __forceinline__ void topk_merge_row(const MergeArgs& a, int row, uint
 #pragma unroll
     for (int j = 0; j < KT; ++j) loc[j] = 0;
     const int total = a.num_n * k;
-    constexpr int BATCH = 4;   // candidates in flight per thread
     for (int base = 0; base < total; base += MERGE_THREADS * BATCH) {
         uint64_t kb[BATCH];
         uint64_t* src[BATCH];

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(VERIFY_WARPS * 32)
         __shared__ uint64_t s_wbest[MERGE_SCRATCH];
         pdl_wait();
         pdl_trigger();
-        topk_merge_row(mg, (int)blockIdx.x - nverify, s_wbest, ctrl);
+        topk_merge_row<4>(mg, (int)blockIdx.x - nverify, s_wbest, ctrl);
         return;
     }
     const unsigned FULL = 0xffffffffu;
