@@ -117,10 +117,18 @@ constexpr int BK = 64;     // K elements per pipeline stage (128 bytes of bf16)
 constexpr int ROUTER_UNITS_PER_CTA = 8;
 // The tiled router keeps at most this many (32-row x 128-unit tile, K split)
 // partial tiles of fp32 in the workspace at once (about two CTAs per SM).
-constexpr int ROUTER_GEMM_SLOTS = 320;
+constexpr int ROUTER_GEMM_SLOTS = 640;
 constexpr int ROUTER_MAX_WIDTH = 65536;
 
 inline int cdiv(long a, long b) { return (int)((a + b - 1) / b); }
+
+// Floats of the tiled router's K-split partials ([splits][B][m]) a workspace
+// holds: ROUTER_GEMM_SLOTS x 4096, and never less than one split.
+inline size_t router_part_floats(int B, int m) {
+    const size_t one = (size_t)(B > 0 ? B : 1) * (size_t)(m > 0 ? m : 1);
+    const size_t slots = (size_t)ROUTER_GEMM_SLOTS * 4096;
+    return slots > one ? slots : one;
+}
 
 // Workspace regions for a call with at most P verified rows, B sequences,
 // hidden size d, router width m, draft vocabulary Vd and top-k k.
@@ -146,11 +154,9 @@ inline Layout layout(int P, int B, int d, int m, int Vd, int k) {
     const int routed = small_P > B ? small_P : B;
     const int mm = m > 0 ? m : 1;
     // router partials: [rows][m / 8] (beside the LM head) or [K splits][B][m]
-    // of the tiled router, at most ROUTER_GEMM_SLOTS tiles of 32 x 128 (or B x m
-    // with one split)
+    // of the tiled router (router_part_floats)
     const size_t beside_part = (size_t)routed * (size_t)cdiv(mm, ROUTER_UNITS_PER_CTA);
-    const size_t tiles = (size_t)cdiv(B > 0 ? B : 1, 32) * (size_t)cdiv(mm, 128);
-    const size_t gemm_part = (tiles > ROUTER_GEMM_SLOTS ? tiles : (size_t)ROUTER_GEMM_SLOTS) * 32 * 128;
+    const size_t gemm_part = router_part_floats(B, mm);
     off = align_up(off + sizeof(float) * (beside_part > gemm_part ? beside_part : gemm_part), 256);
     L.dall = off;
     off = align_up(off + sizeof(float) * (size_t)(small_P > ent_rows ? small_P : ent_rows), 256);

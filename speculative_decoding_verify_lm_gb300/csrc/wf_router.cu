@@ -17,9 +17,9 @@
 // It also routes up to 8 chosen rows after acceptance (one pass of rows).
 //
 // router_gemm_kernel + router_finish_kernel route more chosen rows after
-// acceptance: Z = H W1^T as a tiled fp32 GEMM on the CUDA cores (tiles of 32
-// rows x 128 units, a 4 x 4 register micro-tile per thread, bf16 rows widened
-// once into shared memory, K split across CTAs so the tiles fill the SMs),
+// acceptance: Z = H W1^T as a tiled fp32 GEMM on the CUDA cores (tiles of 128
+// rows x 128 units, an 8 x 8 register micro-tile per thread, bf16 rows widened
+// as they are staged in shared memory, K split so the CTAs fill the SMs once),
 // then one CTA per row adds the K splits in order, applies b1, GELU and w2,
 // sums over units in a fixed order and takes the decision.
 #include "wf_internal.cuh"
@@ -194,109 +194,121 @@ __global__ void __maxnreg__(ROUTER_MAX_REGS)
 }
 
 // ------------------------------------------------------------------ tiled router (chosen rows)
-constexpr int RG_TB = 32;       // rows per tile
+constexpr int RG_TB = 128;      // rows per tile
 constexpr int RG_TU = 128;      // units per tile
-constexpr int RG_KC = 32;       // K per stage
-constexpr int RG_THREADS = 256;
-constexpr int RG_HP = RG_KC + 4;   // shared row pitch of the widened rows (floats)
-constexpr int RG_WP = RG_TU + 4;   // shared row pitch of the transposed weights (floats)
+constexpr int RG_KC = 8;        // K per shared-memory stage
+constexpr int RG_THREADS = 256; // 16 x 16 threads, 8 x 8 outputs each
+constexpr int RG_PD = 4;        // stages whose global loads are in flight (registers)
 
-// Zp[ks][b][j] = sum over this split's K range of h_b[k] * W1[j, k]; warp w
-// computes rows 4w..4w+3, lane l units 4l..4l+3 of the tile.
+// Zp[ks][b][j] = sum over this split's K range of h_b[k] * W1[j, k].  Thread
+// (ty, tx) = (tid / 16, tid % 16) owns rows {4ty + i, 64 + 4ty + i} and units
+// {4tx + j, 64 + 4tx + j} (i, j < 4) of the tile: per K step two float4 of
+// the widened rows and two of the weights feed 64 FMAs (the 4-wide halves at
+// a 16-byte stride keep the weight reads free of bank conflicts; a warp reads
+// two row addresses, which are broadcast).  Rows and weights are staged
+// K-major in shared memory, double-buffered; RG_PD stages of each thread's
+// global loads are in flight in registers.
 __global__ void __launch_bounds__(RG_THREADS)
     router_gemm_kernel(const uint16_t* __restrict__ hidden, const int32_t* __restrict__ rows, int B, int d, int m,
                        int P, const float* __restrict__ W1, int kc_per, float* __restrict__ Zp) {
-    __shared__ __align__(16) float Hs[2][RG_TB][RG_HP];
-    __shared__ __align__(16) float Ws[2][RG_KC][RG_WP];
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    __shared__ __align__(16) float Hs[2][RG_KC][RG_TB];
+    __shared__ __align__(16) float Ws[2][RG_KC][RG_TU];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int u0 = blockIdx.x * RG_TU, b0 = blockIdx.y * RG_TB, ks = blockIdx.z;
     const int nkc = (d + RG_KC - 1) / RG_KC;
     const int kc0 = ks * kc_per, kc1 = min(nkc, kc0 + kc_per);
-    // staging roles: weights - unit tid / 2, 16 of the 32 K of a stage; rows - row tid / 8, 4 K
-    const int wu = tid >> 1, wk = (tid & 1) * 16;
-    const int hr = tid >> 3, hk = (tid & 7) * 4;
-    float4 wreg[4];
-    uint2 hreg;
-    auto load_w = [&](int kc) {   // W1 is no earlier kernel's output
-        const int j = u0 + wu, k = kc * RG_KC + wk;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            wreg[q] = (j < m && k + 4 * q < d) ? __ldg(reinterpret_cast<const float4*>(W1 + (size_t)j * d + k) + q)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    // staging roles: row / unit tid / 2, K half (tid & 1) * 4 of a stage
+    const int sr = tid >> 1, sk = (tid & 1) * 4;
+    float4 wreg[RG_PD];
+    uint2 hreg[RG_PD];
+    const int wj = u0 + sr;
+    auto load_w = [&](int kc, int slot) {   // W1 is no earlier kernel's output
+        const int k = kc * RG_KC + sk;
+        wreg[slot] = (kc < kc1 && wj < m && k < d) ? __ldg(reinterpret_cast<const float4*>(W1 + (size_t)wj * d + k))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     int hsrc = -1;   // hidden row of this thread's staging row
-    auto load_h = [&](int kc) {
-        const int k = kc * RG_KC + hk;
-        hreg = (hsrc >= 0 && k < d) ? __ldg(reinterpret_cast<const uint2*>(hidden + (size_t)hsrc * d + k))
-                                    : make_uint2(0u, 0u);
+    auto load_h = [&](int kc, int slot) {
+        const int k = kc * RG_KC + sk;
+        hreg[slot] = (kc < kc1 && hsrc >= 0 && k < d)
+                         ? __ldg(reinterpret_cast<const uint2*>(hidden + (size_t)hsrc * d + k))
+                         : make_uint2(0u, 0u);
     };
-    auto store = [&](int buf) {
-        const float wv[16] = {wreg[0].x, wreg[0].y, wreg[0].z, wreg[0].w, wreg[1].x, wreg[1].y, wreg[1].z, wreg[1].w,
-                              wreg[2].x, wreg[2].y, wreg[2].z, wreg[2].w, wreg[3].x, wreg[3].y, wreg[3].z, wreg[3].w};
+    auto store = [&](int buf, int slot) {
+        const float4 wv = wreg[slot];
+        Ws[buf][sk + 0][sr] = wv.x;
+        Ws[buf][sk + 1][sr] = wv.y;
+        Ws[buf][sk + 2][sr] = wv.z;
+        Ws[buf][sk + 3][sr] = wv.w;
+        const uint2 hv = hreg[slot];
+        Hs[buf][sk + 0][sr] = __uint_as_float(hv.x << 16);
+        Hs[buf][sk + 1][sr] = __uint_as_float(hv.x & 0xFFFF0000u);
+        Hs[buf][sk + 2][sr] = __uint_as_float(hv.y << 16);
+        Hs[buf][sk + 3][sr] = __uint_as_float(hv.y & 0xFFFF0000u);
+    };
 #pragma unroll
-        for (int q = 0; q < 16; ++q) Ws[buf][wk + q][wu] = wv[q];
-        *reinterpret_cast<float4*>(&Hs[buf][hr][hk]) =
-            make_float4(__uint_as_float(hreg.x << 16), __uint_as_float(hreg.x & 0xFFFF0000u),
-                        __uint_as_float(hreg.y << 16), __uint_as_float(hreg.y & 0xFFFF0000u));
-    };
-    if (kc0 < kc1) load_w(kc0);
+    for (int i = 0; i < RG_PD; ++i) load_w(kc0 + i, i);
     pdl_wait();   // rows[] is the acceptance step's output
     pdl_trigger();
-    if (b0 + hr < B) {
-        const int r = rows[b0 + hr];
+    if (b0 + sr < B) {
+        const int r = rows[b0 + sr];
         hsrc = (r >= 0 && (P < 0 || r < P)) ? r : -1;
     }
-    float acc[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    if (kc0 < kc1) {
-        load_h(kc0);
-        store(0);
-    }
+    for (int i = 0; i < RG_PD; ++i) load_h(kc0 + i, i);
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    if (kc0 < kc1) store(0, 0);
     __syncthreads();
-    for (int kc = kc0; kc < kc1; ++kc) {
-        const int buf = (kc - kc0) & 1;
-        if (kc + 1 < kc1) {   // the next stage's loads are in flight during this stage's FMAs
-            load_w(kc + 1);
-            load_h(kc + 1);
-        }
+    // stages in groups of RG_PD so that every register slot index is a constant
+    for (int g0 = kc0; g0 < kc1; g0 += RG_PD) {
 #pragma unroll
-        for (int k = 0; k < RG_KC; k += 4) {
-            float4 h[4], wt[4];
+        for (int p = 0; p < RG_PD; ++p) {
+            const int kc = g0 + p;
+            if (kc >= kc1) break;
+            const int buf = (kc - kc0) & 1;
+            // slot p was stored for this stage: it now takes stage kc + RG_PD
+            load_w(kc + RG_PD, p);
+            load_h(kc + RG_PD, p);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) h[i] = *reinterpret_cast<const float4*>(&Hs[buf][4 * w + i][k]);
+            for (int k = 0; k < RG_KC; ++k) {
+                const float4 h0 = *reinterpret_cast<const float4*>(&Hs[buf][k][4 * ty]);
+                const float4 h1 = *reinterpret_cast<const float4*>(&Hs[buf][k][64 + 4 * ty]);
+                const float4 w0 = *reinterpret_cast<const float4*>(&Ws[buf][k][4 * tx]);
+                const float4 w1 = *reinterpret_cast<const float4*>(&Ws[buf][k][64 + 4 * tx]);
+                const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) wt[q] = *reinterpret_cast<const float4*>(&Ws[buf][k + q][4 * lane]);
+                for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float hv[4] = {h[i].x, h[i].y, h[i].z, h[i].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[i][0] = fmaf(hv[q], wt[q].x, acc[i][0]);
-                    acc[i][1] = fmaf(hv[q], wt[q].y, acc[i][1]);
-                    acc[i][2] = fmaf(hv[q], wt[q].z, acc[i][2]);
-                    acc[i][3] = fmaf(hv[q], wt[q].w, acc[i][3]);
-                }
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(hv[i], wv[j], acc[i][j]);
+            }
+            if (kc + 1 < kc1) {
+                __syncthreads();   // the other buffer was last read a stage ago; this one is read no more
+                store(buf ^ 1, (p + 1) % RG_PD);
+                __syncthreads();
             }
         }
-        if (kc + 1 < kc1) {
-            __syncthreads();   // the other buffer was last read a stage ago; this one is read no more
-            store(buf ^ 1);
-            __syncthreads();
-        }
     }
-    const int j = u0 + 4 * lane;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int b = b0 + 4 * w + i;
+    for (int i = 0; i < 8; ++i) {
+        const int b = b0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
         if (b >= B) continue;
-        float* z = Zp + ((size_t)ks * B + b) * m + j;
-        if (j + 3 < m && (m & 3) == 0) {
-            *reinterpret_cast<float4*>(z) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (j + q < m) z[q] = acc[i][q];
+        for (int h = 0; h < 2; ++h) {
+            const int j = u0 + 64 * h + 4 * tx;
+            float* z = Zp + ((size_t)ks * B + b) * m + j;
+            const float* a = &acc[i][4 * h];
+            if (j + 3 < m && (m & 3) == 0) {
+                *reinterpret_cast<float4*>(z) = make_float4(a[0], a[1], a[2], a[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j + q < m) z[q] = a[q];
+            }
         }
     }
 }
@@ -352,11 +364,14 @@ __global__ void __launch_bounds__(RF_THREADS)
 }
 
 // K splits of the tiled router for B rows: the tiles times the splits fill
-// the SMs about once (at most ROUTER_GEMM_SLOTS tiles' partials in flight).
+// the SMs once, a CTA an SM (the GEMM is bound by the FMA rate), within the
+// workspace's partials (router_part_floats).
 int router_gemm_splits(int B, int d, int m) {
     const int tiles = cdiv(B, RG_TB) * cdiv(m, RG_TU);
     const int nkc = cdiv(d, RG_KC);
-    int ks = ROUTER_GEMM_SLOTS / tiles;
+    int ks = num_sms() / tiles;
+    const long cap = (long)router_part_floats(B, m) / ((long)B * m);
+    if (ks > cap) ks = (int)cap;
     ks = ks < 1 ? 1 : (ks > nkc ? nkc : ks);
     const int per = cdiv(nkc, ks);
     return cdiv(nkc, per);
