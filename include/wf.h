@@ -326,9 +326,11 @@ WF_API wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int3
 
 /*
  * Both heads of a round in one weight sweep: the results of wf_lmhead_argmax
- * over the P rows of hidden and of wf_draft_topk over the B rows of x,
- * bit for bit, from one persistent launch that streams W and then Wd through
- * the same pipeline (plus a small merge of the draft candidates).  The pages
+ * over the P rows of hidden and of wf_draft_topk over the B rows of x (ids and
+ * logits bit for bit; the log-sum-exp to fp32 rounding, its per-tile partials
+ * being summed over this sweep's tiles), from one persistent launch that
+ * streams Wd and W through the same pipeline (plus a small merge of the draft
+ * candidates).  The pages
  * describe the two heads as separate steps (target verification, WhiFlash
  * paper Sec. 3.2; EAGLE-3 drafting, Qwen3-4B-EAGLE3 card); reading both
  * matrices in one pass is this library's scheduling, so that the smaller
@@ -337,8 +339,10 @@ WF_API wf_status wf_draft_topk(const uint16_t* x, const uint16_t* Wd, const int3
  *
  * Arguments as in wf_lmhead_argmax (hidden, W, P, d, V, ids, maxlogit) and
  * wf_draft_topk (x, Wd, d2t, B, Vd, k, draft_ids, tids, vals, lse), one shared d.
- * P <= 128 and B <= 128 (one activation tile each), else WF_ERR_UNSUPPORTED:
- * call the two entry points.  Workspace: wf_workspace_bytes(P, B, d, 0, Vd, k).
+ * P <= 128 and B <= 128 (one activation tile each), or P > 128 and B <= 256
+ * (the paired-CTA sweep of several activation tiles, the draft rows in one
+ * tile pair), else WF_ERR_UNSUPPORTED: call the two entry points.
+ * Workspace: wf_workspace_bytes(P, B, d, 0, Vd, k).
  */
 WF_API wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
                                int32_t* ids, float* maxlogit, const uint16_t* x, const uint16_t* Wd,
@@ -351,9 +355,9 @@ WF_API wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W,
  * every verified row -> per-sequence acceptance (chain or tree by kind[b])
  * -> router on each sequence's last accepted row -> route for the next round;
  * plus, if Wd != NULL, the draft head's top-k for every sequence.  All stages
- * are stream-ordered on `stream` with no host synchronisation.  With at most
- * 128 verified rows the draft head shares the LM head's weight sweep (as in
- * wf_lmhead_draft_topk).
+ * are stream-ordered on `stream` with no host synchronisation.  The draft
+ * head shares the LM head's weight sweep (as in wf_lmhead_draft_topk) when
+ * P <= 128 and B <= 128, or P > 128 and B <= 256.
  */
 typedef struct wf_round_args {
     /* verified rows */

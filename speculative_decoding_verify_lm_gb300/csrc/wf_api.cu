@@ -292,7 +292,7 @@ wf_status wf_lmhead_draft_topk(const uint16_t* hidden, const uint16_t* W, int P,
     if (!x || !Wd || !d2t || bad_gemm_shape(B, d, Vd)) return WF_ERR_INVALID_ARG;
     if (k < 1 || k > WF_MAX_TOPK || k > Vd || (!draft_ids && !tids && !vals && !lse)) return WF_ERR_INVALID_ARG;
     if (!aligned16(hidden) || !aligned16(W) || !aligned16(x) || !aligned16(Wd)) return WF_ERR_INVALID_ARG;
-    if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
+    if (P <= BM ? B > BM : B > 2 * BM) return WF_ERR_UNSUPPORTED;
     const Layout L = layout(P, B, d, 0, Vd, k);
     WF_TRY(check_ws(ws, ws_bytes, L.part));   // control block, keys and top-k candidates
     WF_TRY(check_device());
@@ -410,7 +410,7 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         // runs.  With one activation tile per head the draft head shares the
         // LM head's weight sweep (W, then Wd) and its candidates are merged last.
         const bool beside = a->P <= ROUTER_BESIDE_MAX_ROWS;
-        const bool shared = draft && a->P <= BM && a->B <= BM;
+        const bool shared = draft && (a->P <= BM ? a->B <= BM : a->B <= 2 * BM);
         int num_n2 = 0;
         if (shared)
             WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,

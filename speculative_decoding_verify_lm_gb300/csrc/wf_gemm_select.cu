@@ -343,7 +343,7 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
 // Each CTA loads its own activation and weight boxes; tiles (m, n) are visited
 // in the order t = n * num_m + m, so the CTAs working at the same time share
 // the weight tile through L2.
-// PAIR (several activation tiles, no ENT / DUAL): clusters of two CTAs take
+// PAIR (several activation tiles, no ENT): clusters of two CTAs take
 // tile pairs (m, n), (m + 1, n) with one paired MMA of M = 256 rows: each CTA
 // loads its own activation tile and half of the weight tile (its bytes are
 // counted on the first CTA's stage barrier), the first CTA issues every MMA
@@ -357,7 +357,8 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
 // DUAL (with KT = 1): tiles U0.. are the second problem's
 // (activation map tmA2, weight map tmB2, top-k into p.cand), swept first
 // (tile_order); with ENT the first problem's tiles also feed the entropy
-// statistics.
+// statistics; with PAIR they are pair tiles over the second problem's rows
+// (at most 2 BM: each CTA its own half).
 template <int KT, bool ENT, bool DUAL, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB2s,
                        const GemmParams p) {
     static_assert(!DUAL || KT == 1, "the dual sweep pairs an argmax head with a top-k head");
-    static_assert(!PAIR || (!ENT && !DUAL), "paired MMAs only for the plain sweeps of several activation tiles");
+    static_assert(!PAIR || !ENT, "paired MMAs: no softmax statistics (rows of one CTA change from tile to tile)");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
@@ -453,14 +454,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 const int u = tile_order<DUAL>(v, U0, U);
                 const bool second = DUAL && u >= U0;
                 const TileMN tm = tile_mn(second ? 0 : u, num_mt, p.num_n, p.group);
-                const int m = second ? 0 : (PAIR ? 2 * tm.mt + rank : tm.mt);
+                const int m = second ? (PAIR ? rank : 0) : (PAIR ? 2 * tm.mt + rank : tm.mt);
                 const int n = second ? u - U0 : tm.n;
                 const TileSpan sp = second ? tile_span(n, p.num_n2, p.bn2, p.nbig2, false)
                                            : tile_span(n, p.num_n, p.bn, p.nbig, true);
                 const CUtensorMap* mA = second ? &tmA2 : &tmA;
                 const CUtensorMap* mB = second ? (sp.big ? &tmB2 : &tmB2s) : (sp.big ? &tmB : &tmBs);
                 const int wrows = PAIR ? sp.rows / 2 : sp.rows;   // weight rows this CTA loads
-                const uint32_t tx = PAIR ? 2u * (uint32_t)(p.a_bytes + wrows * BK * 2)
+                const uint32_t tx = PAIR ? 2u * (uint32_t)((second ? p.a_bytes2 : p.a_bytes) + wrows * BK * 2)
                                          : (uint32_t)((second ? p.a_bytes2 : p.a_bytes) + sp.rows * BK * 2);
                 for (int kc = 0; kc < p.num_k; ++kc, ++it) {
                     if (it > 0) {
@@ -587,11 +588,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int v = slot; v < U; v += nslots, ++tile_i) {
             const int u = tile_order<DUAL>(v, U0, U);
             bool ok;
-            if (DUAL && u >= U0)
-                ok = epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, 0, abort_flag, tmem_base, tile_i, q, rit,
-                                                          p.M_rows2, p.N_w2, 0, u - U0,
-                                                          tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false), 1, em,
-                                                          es, et);
+            if (DUAL && u >= U0) {
+                // the second problem's tile: top-k candidates (a 10-wide list when k <= 10);
+                // PAIR: this CTA's half of the rows, lists per activation tile of the second problem
+                const TileSpan sp2 = tile_span(u - U0, p.num_n2, p.bn2, p.nbig2, false);
+                const int m2 = PAIR ? rank : 0, nm2 = PAIR ? (p.M_rows2 + BM - 1) / BM : 1;
+                ok = p.k <= KT_TOPK10
+                         ? epilogue_tile<KT_TOPK10, false, false>(p, tfull, tempty, tempty_first, abort_flag,
+                                                                  tmem_base, tile_i, q, rit, p.M_rows2, p.N_w2, m2,
+                                                                  u - U0, sp2, nm2, em, es, et)
+                         : epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, tempty_first, abort_flag, tmem_base,
+                                                                tile_i, q, rit, p.M_rows2, p.N_w2, m2, u - U0, sp2,
+                                                                nm2, em, es, et);
+            }
             else if (!PAIR && num_m == 1)   // the weight-streaming sweep: the last tile's scan is exposed
                 ok = epilogue_tile<KT, ENT, true>(p, tfull, tempty, 0, abort_flag, tmem_base, tile_i, q, rit,
                                                   p.M_rows, p.N_w, 0, u, tile_span(u, p.num_n, p.bn, p.nbig, true), 1,
@@ -826,8 +835,8 @@ static int set_ring(GemmParams& p, int one_tile_a_rows, bool pair = false) {
 }
 
 // Clusters of two paired-CTA sweep CTAs that can be resident at once (queried
-// once per device).
-template <int KT>
+// once per device).  DUAL: the sweep that also carries the draft head.
+template <int KT, bool DUAL = false>
 static int pair_slots(int smem) {
     static std::mutex mu;
     static int cached[64];
@@ -847,7 +856,7 @@ static int pair_slots(int smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, false, false, true>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, false, DUAL, true>, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = num_sms() / 2;
     }
@@ -986,15 +995,105 @@ wf_status launch_draft_topk(const uint16_t* x, const uint16_t* Wd, const int32_t
                              ws, s);
 }
 
+// The shared sweep for rounds of several activation tiles (P > BM, B <= 2 BM):
+// the paired-CTA LM head (argmax over every verified row) with the draft
+// head's tiles as extra work units of the same persistent loop, swept first
+// (each CTA's draft tiles: top-k candidate lists of its half of the draft
+// rows; their epilogue overlaps the LM head's first main loops), instead of
+// the draft head's own sweep after the round, which fills the SMs in under
+// two waves.
+static wf_status launch_lmhead_draft_pair(const uint16_t* hidden, const uint16_t* W, int P, int d, int V,
+                                          int32_t* ids, float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B,
+                                          int Vd, int k, void* ws, size_t cand_off, size_t lsep_off,
+                                          int* num_n2_out, cudaStream_t s) {
+    static std::mutex mu;
+    static bool attr_set[64] = {false};
+    const wf_status cst = configure_once(mu, attr_set, [] {
+        return cudaFuncSetAttribute(gemm_select_kernel<1, false, true, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_MAX) == cudaSuccess;
+    });
+    if (cst != WF_OK) return cst;
+    GemmParams p = params_for(ws);
+    const int num_m = cdiv(P, BM);
+    TileGeom tg;
+    if (balanced_tiles(V, num_sms(), &tg)) {
+        p.num_n = tg.num_n;
+        p.bn = tg.bn;
+        p.nbig = tg.nbig;
+    } else {
+        p.bn = pick_bn(num_m, V, num_sms());
+        p.num_n = p.nbig = cdiv(V, p.bn);
+    }
+    // draft head: balanced tiles too (the same number for every CTA pair),
+    // half of each loaded by either CTA of a pair
+    TileGeom tg2;
+    if (balanced_tiles(Vd, num_sms(), &tg2)) {
+        p.num_n2 = tg2.num_n;
+        p.bn2 = tg2.bn;
+        p.nbig2 = tg2.nbig;
+    } else {
+        p.bn2 = BN;
+        p.num_n2 = p.nbig2 = cdiv(Vd, BN);
+    }
+    CUtensorMap ta, tb, tbs, ta2, tb2, tb2s;
+    if (!make_map(&ta, hidden, (uint64_t)P, (uint64_t)d, (uint32_t)BM) ||
+        !make_map(&tb, W, (uint64_t)V, (uint64_t)d, (uint32_t)(p.bn / 2)) ||
+        !make_map(&ta2, x, (uint64_t)B, (uint64_t)d, (uint32_t)BM) ||
+        !make_map(&tb2, Wd, (uint64_t)Vd, (uint64_t)d, (uint32_t)(p.bn2 / 2)))
+        return WF_ERR_CUDA;
+    tbs = tb;
+    tb2s = tb2;
+    if (p.nbig < p.num_n && !make_map(&tbs, W, (uint64_t)V, (uint64_t)d, (uint32_t)((p.bn - 16) / 2)))
+        return WF_ERR_CUDA;
+    if (p.nbig2 < p.num_n2 && !make_map(&tb2s, Wd, (uint64_t)Vd, (uint64_t)d, (uint32_t)((p.bn2 - 16) / 2)))
+        return WF_ERR_CUDA;
+    p.M_rows = P;
+    p.N_w = V;
+    p.num_m = num_m;
+    p.idesc = umma_idesc_bf16(2 * BM, p.bn);
+    p.idesc_s = p.nbig < p.num_n ? umma_idesc_bf16(2 * BM, p.bn - 16) : p.idesc;
+    p.idesc2 = umma_idesc_bf16(2 * BM, p.bn2);
+    p.idesc2_s = p.nbig2 < p.num_n2 ? umma_idesc_bf16(2 * BM, p.bn2 - 16) : p.idesc2;
+    p.num_k = cdiv(d, BK);
+    p.weight_evict_first = 1;
+    // activation groups as in the plain paired sweep (launch_select)
+    const int num_mt = cdiv(num_m, 2);
+    const long per_mt = 2L * BM * d * 2;
+    const int most = (int)(PAIR_GROUP_BYTES / per_mt) > 0 ? (int)(PAIR_GROUP_BYTES / per_mt) : 1;
+    p.group = cdiv(num_mt, cdiv(num_mt, most));
+    p.a_bytes = p.a_bytes2 = BM * BK * 2;
+    p.ids = ids;
+    p.maxlogit = maxlogit;
+    p.k = k;
+    p.cand = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ws) + cand_off);
+    p.lsep = lsep_off ? reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws) + lsep_off) : nullptr;
+    p.M_rows2 = B;
+    p.N_w2 = Vd;
+    p.timeout_ns = wait_timeout_ns();
+    *num_n2_out = p.num_n2;
+    const int smem = set_ring(p, 0, true);
+    const int pairs = num_mt * p.num_n + p.num_n2;
+    const int slots = pair_slots<1, true>(smem);
+    const int grid = 2 * (pairs < slots ? pairs : slots);
+    return launch_cluster(gemm_select_kernel<1, false, true, true>, dim3(grid), dim3(GEMM_THREADS), smem, s, 2u, ta,
+                          tb, ta2, tb2, tbs, tb2s, p);
+}
+
 // Target LM head (argmax over P <= BM rows) and draft head (candidate lists of
-// the top k over B <= BM rows) in one persistent sweep of W then Wd.  The
+// the top k over B <= BM rows) in one persistent sweep of W then Wd (more rows:
+// launch_lmhead_draft_pair).  The
 // candidate lists are merged by launch_topk_merge over the draft-head tile
 // count this returns in *num_n2_out.
 wf_status launch_lmhead_draft(const uint16_t* hidden, const uint16_t* W, int P, int d, int V, int32_t* ids,
                               float* maxlogit, const uint16_t* x, const uint16_t* Wd, int B, int Vd, int k, void* ws,
                               size_t cand_off, size_t lsep_off, int* num_n2_out, cudaStream_t s, float* H, float tau,
                               size_t ent_off, int* defer_slots) {
-    if (P > BM || B > BM) return WF_ERR_UNSUPPORTED;
+    if (P > BM) {
+        if (B > 2 * BM || H || defer_slots) return WF_ERR_UNSUPPORTED;
+        return launch_lmhead_draft_pair(hidden, W, P, d, V, ids, maxlogit, x, Wd, B, Vd, k, ws, cand_off, lsep_off,
+                                        num_n2_out, s);
+    }
+    if (B > BM) return WF_ERR_UNSUPPORTED;
     static std::mutex mu;
     static bool attr_set[64] = {false};
     const wf_status cst = configure_once(mu, attr_set, [] {

@@ -375,7 +375,7 @@ def wf_draft_topk(x, Wd, d2t, k: int, ws: Workspace, draft_ids=None, tids=None, 
 def wf_lmhead_draft_topk(hidden, W, x, Wd, d2t, k: int, ws: Workspace, ids=None, maxlogit=None, draft_ids=None,
                          tids=None, vals=None, lse=None, stream=None):
     """Target argmax over the rows of hidden and draft top-k over the rows of x
-    in one weight sweep (at most 128 rows each)."""
+    in one weight sweep (P, B <= 128, or P > 128 and B <= 256)."""
     P, d = hidden.shape
     V = W.shape[0]
     B = x.shape[0]

@@ -222,7 +222,10 @@ def test_draft_topk(B, d, Vd, k):
 
 @pytest.mark.parametrize("P,B,d,V,Vd,k", [(17, 1, 256, 8192, 4000, 10), (128, 128, 64, 777, 300, 16),
                                           (61, 2, 72, 1000, 129, 1), (1, 1, 2560, 151936, 32000, 10),
-                                          (40, 2, 256, 76000, 19456, 10)])
+                                          (40, 2, 256, 76000, 19456, 10),
+                                          # several activation tiles: the paired sweep carries the draft head
+                                          (300, 200, 128, 5000, 3000, 10), (257, 64, 96, 2000, 1000, 16),
+                                          (600, 256, 64, 4096, 2050, 4), (129, 129, 2560, 33000, 7000, 10)])
 def test_lmhead_draft_topk_shared_sweep(P, B, d, V, Vd, k):
     """Both heads in one sweep give the oracle's argmax and top-k (and leave the
     workspace zeroed), here and on a reused workspace."""
