@@ -175,7 +175,8 @@ class ClockSampler:
 # width, entropy, both heads, paired CTAs)
 KERNEL_SOURCES = {name: ("wf_gemm_select.cu", "wf_internal.cuh")
                   for name in ("gemm_select_kernel<1,0,0,0>", "gemm_select_kernel<1,0,0,1>",
-                               "gemm_select_kernel<1,1,0,0>", "gemm_select_kernel<1,0,1,0>")}
+                               "gemm_select_kernel<1,1,0,0>", "gemm_select_kernel<1,0,1,0>",
+                               "gemm_select_kernel<1,0,1,1>")}
 
 
 def source_sha(kernel: str) -> str:
@@ -294,11 +295,11 @@ def load_workload(index: int, m=None):
 def round_launches(P: int, B: int, draft: bool, entropy: bool) -> int:
     """Kernel launches of one wf_round (the composition in wf_round: the LM
     head or both heads in one sweep, acceptance, the router, the draft head)."""
-    shared = draft and P <= 128 and B <= 128
+    shared = draft and (B <= 128 if P <= 128 else B <= 256)
     if entropy:
         if P <= 128:
             return 2 + (0 if shared else (2 if draft else 0))
-        return 4 + (2 if draft else 0)
+        return 4 + (2 if draft else 0)   # the draft head's own sweep and merge after the round
     if P <= 32:   # router beside the LM head over every row
         return 3 + (0 if shared else (2 if draft else 0))
     router = 1 if B <= 8 else 2
@@ -770,7 +771,7 @@ def main():
     # ---- the dominant kernel on its own: the shared sweep of both heads
     # (timed with its top-k merge) or the LM head alone (with the entropy
     # statistics under entropy routing, when one sweep yields them)
-    shared = draft and P <= 128 and B <= 128 and not entropy
+    shared = draft and (B <= 128 if P <= 128 else B <= 256) and not entropy
     ent_fused = entropy and P <= 128
     hbm_peak, tc_peak, tc_sus, peak_src = measured_peaks()
     ids_buf = torch.empty(P, dtype=torch.int32, device=device)
@@ -787,7 +788,8 @@ def main():
         Vd = wl.Wd.shape[0]
         alg_bytes = (V + Vd) * d * 2 + (P + B) * d * 2 + Vd * 4 + P * 4 + B * k * 12
         alg_flops = 2.0 * d * (P * V + B * Vd)
-        kernel_name, kernel_launches = "gemm_select_kernel<1,0,1,0>", 2
+        # several activation tiles: the paired-CTA sweep
+        kernel_name, kernel_launches = f"gemm_select_kernel<1,0,1,{int(P > 128)}>", 2
     elif ent_fused:
         ws1 = wf.Workspace(P, P, d=d, device=device)
         Hbuf = torch.empty(P, dtype=torch.float32, device=device)

@@ -86,7 +86,9 @@ def test_round_launch_count_follows_the_composition():
     assert bench.round_launches(17, 1, False, False) == 3       # LM head, router beside it, acceptance
     assert bench.round_launches(61, 1, True, False) == 3        # both heads in one sweep, acceptance + merge, router
     assert bench.round_launches(1248, 32, False, False) == 4    # LM head, acceptance, router GEMM + finish
-    assert bench.round_launches(15616, 256, True, False) == 6   # ... plus the draft head's sweep and merge
+    assert bench.round_launches(15616, 256, True, False) == 4   # both heads in one paired sweep, acceptance + merge,
+    #                                                              router GEMM + finish
+    assert bench.round_launches(15616, 300, True, False) == 6   # draft rows past one tile pair: its own sweep + merge
     assert bench.round_launches(17, 1, False, True) == 2        # entropy sweep, acceptance
     assert bench.round_launches(15616, 256, True, True) == 6    # LM head, acceptance, gather, entropy sweep, draft head
 
