@@ -299,7 +299,8 @@ def round_launches(P: int, B: int, draft: bool, entropy: bool) -> int:
     if entropy:
         if P <= 128:
             return 2 + (0 if shared else (2 if draft else 0))
-        return 4 + (2 if draft else 0)   # the draft head's own sweep and merge after the round
+        # the draft head in the first sweep (rows in one tile pair), else its own sweep and merge after the round
+        return 4 + (0 if draft and B <= 256 else (2 if draft else 0))
     if P <= 32:   # router beside the LM head over every row
         return 3 + (0 if shared else (2 if draft else 0))
     router = 1 if B <= 8 else 2
@@ -771,7 +772,7 @@ def main():
     # ---- the dominant kernel on its own: the shared sweep of both heads
     # (timed with its top-k merge) or the LM head alone (with the entropy
     # statistics under entropy routing, when one sweep yields them)
-    shared = draft and (B <= 128 if P <= 128 else B <= 256) and not entropy
+    shared = draft and (B <= 128 if P <= 128 else B <= 256) and not (entropy and P <= 128)
     ent_fused = entropy and P <= 128
     hbm_peak, tc_peak, tc_sus, peak_src = measured_peaks()
     ids_buf = torch.empty(P, dtype=torch.int32, device=device)

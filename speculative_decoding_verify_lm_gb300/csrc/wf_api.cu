@@ -392,15 +392,26 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
                              shared ? &mg : nullptr));
         if (shared) return WF_OK;
     } else if (entropy) {
-        // many rows: a second sweep over the weights for the B accepted rows only
-        WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        // many rows: a second sweep over the weights for the B accepted rows
+        // only.  The draft head rides in the first sweep (paired CTAs) when its
+        // rows fit one tile pair; its merge then runs beside the verification.
+        const bool shared = draft && a->B <= 2 * BM;
+        int num_n2 = 0;
+        if (shared)
+            WF_TRY(launch_lmhead_draft(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, a->x, a->Wd, a->B,
+                                       a->Vd, a->k, ws, L.cand, a->lse ? L.lsep : 0, &num_n2, stream));
+        else
+            WF_TRY(launch_lmhead_argmax(a->hidden, a->W, a->P, a->d, a->V, a->ids, a->maxlogit, ws, stream));
+        const MergeArgs mg = merge_args(a->B, a->Vd, num_n2, a->k, a->d2t, a->draft_ids, a->tids, a->vals, ws,
+                                        L.cand, a->lse, L.lsep);
         WF_TRY(launch_verify(a->ids, a->tok, a->parent, a->kind, 1, a->pos_off, a->node_off, a->B, a->P,
                              a->path ? a->path_stride : 0, a->n_accept, a->bonus, a->last_pos, a->path, ws, stream,
-                             RoutePick{}, true));
+                             RoutePick{}, true, shared ? &mg : nullptr));
         uint16_t* gath = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(ws) + L.gath);
         WF_TRY(launch_gather_rows(a->hidden, a->P, a->d, a->last_pos, a->B, gath, ws, stream));
         WF_TRY(launch_lmhead_entropy(gath, a->W, a->B, a->d, a->V, nullptr, nullptr, a->delta_al, a->route, a->tau,
                                      a->last_pos, a->P, ws, L.ent, stream));
+        if (shared) return WF_OK;
     } else {
         // Neural router.  With few rows it runs on every verified row beside
         // the LM head (it needs only the hidden states and its weights, and

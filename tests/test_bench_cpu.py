@@ -90,7 +90,7 @@ def test_round_launch_count_follows_the_composition():
     #                                                              router GEMM + finish
     assert bench.round_launches(15616, 300, True, False) == 6   # draft rows past one tile pair: its own sweep + merge
     assert bench.round_launches(17, 1, False, True) == 2        # entropy sweep, acceptance
-    assert bench.round_launches(15616, 256, True, True) == 6    # LM head, acceptance, gather, entropy sweep, draft head
+    assert bench.round_launches(15616, 256, True, True) == 4    # both heads, acceptance + merge, gather, entropy sweep
 
 
 def test_bench_workload_is_the_stored_record():
