@@ -25,11 +25,13 @@
 // (order-preserving logit, ~id) key; the last CTA to finish converts the keys
 // to ids and resets them to zero.  Top-k rows write one sorted candidate list
 // per tile; wf_topk_merge combines them.
-// DUAL: one launch sweeps two problems with one activation tile each - the
-// target LM head (argmax) and the EAGLE-3 draft head (top-k) - through the
-// same pipeline, so the smaller draft matrix streams at full bandwidth with
-// the larger one instead of as a second, under-filled sweep; each CTA takes
-// its draft-head tile first, so that its last tile has the cheap epilogue.
+// DUAL: one launch sweeps two problems - the target LM head (argmax) and the
+// EAGLE-3 draft head (top-k) - through the same pipeline, so the smaller draft
+// matrix streams with the larger one instead of as a second, under-filled
+// sweep; each CTA takes its draft-head tiles first, so that its last tile has
+// the cheap epilogue.  One activation tile each, or (with paired CTAs) the
+// LM head's tile pairs plus the draft head's rows in one tile pair.  A
+// draft-head tile keeps a 10-wide candidate list when k <= 10, else 16.
 //
 // Every wait is bounded: a wait that runs out records WF_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, drains its own in-flight copies / MMAs (again bounded)
@@ -600,8 +602,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                          : epilogue_tile<KT_TOPK, false, false>(p, tfull, tempty, tempty_first, abort_flag, tmem_base,
                                                                 tile_i, q, rit, p.M_rows2, p.N_w2, m2, u - U0, sp2,
                                                                 nm2, em, es, et);
-            }
-            else if (!PAIR && num_m == 1)   // the weight-streaming sweep: the last tile's scan is exposed
+            } else if (!PAIR && num_m == 1)   // the weight-streaming sweep: the last tile's scan is exposed
                 ok = epilogue_tile<KT, ENT, true>(p, tfull, tempty, 0, abort_flag, tmem_base, tile_i, q, rit,
                                                   p.M_rows, p.N_w, 0, u, tile_span(u, p.num_n, p.bn, p.nbig, true), 1,
                                                   em, es, et);
