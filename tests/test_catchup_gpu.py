@@ -160,6 +160,17 @@ def test_catchup_eagle3_geometry_batch():
     check_against_oracle(c, res)
 
 
+@pytest.mark.parametrize("index", [1, 3])
+def test_catchup_eagle3_geometry_long_backlogs(index):
+    """The two long-backlog workloads the bench times: 1,024 tokens onto a
+    16,384-entry cache (eight activation tiles, two K splits, the attention
+    merged through global memory) and 8 sequences of 128 onto 8,192."""
+    c = catchup_workload(index)
+    res, cu = run_gpu(c)
+    assert cu.ws.device_error() == (0, 0)
+    check_against_oracle(c, res)
+
+
 def test_catchup_kv_only_and_repeat():
     """The KV-only call writes exactly the backlog rows (same values as the full
     call), and a repeated call on the same workspace gives identical bits."""
