@@ -77,12 +77,14 @@ def test_workspace_checked_on_host(ws, nbytes):
     assert st == 2
 
 
-def test_shared_sweep_limited_to_one_activation_tile():
-    # more than 128 rows in either head: unsupported, nothing enqueued (no device needed)
+def test_shared_sweep_limits():
+    # draft rows past one activation tile (target rows in one tile) or past one
+    # tile pair (target rows in several): unsupported, nothing enqueued (no
+    # device needed)
     L = wf.lib()
-    assert L.wf_lmhead_draft_topk(256, 256, 129, 64, 100, 256, NULL, 256, 256, 256, 1, 50, 4, NULL, 256, 256, NULL,
-                                  256, 1 << 20, NULL) == 4
     assert L.wf_lmhead_draft_topk(256, 256, 128, 64, 100, 256, NULL, 256, 256, 256, 129, 50, 4, NULL, 256, 256,
+                                  NULL, 256, 1 << 20, NULL) == 4
+    assert L.wf_lmhead_draft_topk(256, 256, 129, 64, 100, 256, NULL, 256, 256, 256, 257, 50, 4, NULL, 256, 256,
                                   NULL, 256, 1 << 20, NULL) == 4
 
 
