@@ -418,8 +418,10 @@ wf_status wf_round(const wf_round_args* a, void* ws, size_t ws_bytes, wf_stream_
         // waits for the LM head just before it exits) and acceptance picks the
         // accepted row's output; otherwise it routes each sequence's accepted
         // row after acceptance, its weights already loaded while acceptance
-        // runs.  With one activation tile per head the draft head shares the
-        // LM head's weight sweep (W, then Wd) and its candidates are merged last.
+        // runs.  The draft head shares the LM head's weight sweep (its tiles
+        // first) when each head fits one activation tile, or, with several
+        // activation tiles, when the draft rows fit one tile pair of the paired
+        // sweep; its candidates are merged beside the verification.
         const bool beside = a->P <= ROUTER_BESIDE_MAX_ROWS;
         const bool shared = draft && (a->P <= BM ? a->B <= BM : a->B <= 2 * BM);
         int num_n2 = 0;
