@@ -2,7 +2,9 @@
 
 Each .cu file compiles in its own nvcc process (in parallel); the objects are
 linked with the static CUDA runtime, so the library loads without a GPU or a
-driver and resolves the driver's tensor-map encoder at run time."""
+driver and resolves the driver's tensor-map encoder at run time.  ptxas's
+resource report of each file (registers, spills, shared memory per kernel)
+is kept beside its object as ``_build/<file>.ptxas.txt``."""
 from __future__ import annotations
 
 import glob
@@ -38,6 +40,12 @@ def stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
+def ptxas_report(name: str) -> str:
+    """ptxas's resource report of csrc/<name> from the last build ("" if absent)."""
+    path = os.path.join(BUILD, name[:-3] + ".ptxas.txt")
+    return open(path).read() if os.path.exists(path) else ""
+
+
 def build(force: bool = False, verbose: bool = False, extra: list | None = None) -> str:
     if not force and not stale():
         return LIB
@@ -46,10 +54,12 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [NVCC, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
+        cmd = [NVCC, *ARCH, *CFLAGS, "-Xptxas", "-v", *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        with open(obj[:-2] + ".ptxas.txt", "w") as f:
+            f.write(r.stdout + r.stderr)
         if verbose and (r.stdout or r.stderr):
             print(r.stdout + r.stderr, file=sys.stderr)
         return obj
@@ -66,5 +76,4 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True,
-                extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None))
+    print(build(force="--force" in sys.argv, verbose="--ptxas-v" in sys.argv))

@@ -160,14 +160,19 @@ __device__ __forceinline__ void ent_fold(const uint32_t (&r)[32], int lim, float
         em = tv0;
     }
     const float off = em * LOG2E;
+    // four interleaved partial sums: the adds of one chunk form four short
+    // chains instead of one 32 long
+    float s4[4] = {0.f, 0.f, 0.f, 0.f}, t4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 32; ++j)
         if (j < lim) {
             const float z = fmaf(__uint_as_float(r[j]), LOG2E, -off);
             const float e = ex2_approx(z);
-            es += e;
-            et = fmaf(z, e, et);
+            s4[j & 3] += e;
+            t4[j & 3] = fmaf(z, e, t4[j & 3]);
         }
+    es += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    et += (t4[0] + t4[1]) + (t4[2] + t4[3]);
 }
 
 // Fold the columns j < lim of one chunk into a row's running (max lm, sum
@@ -361,6 +366,10 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
 // (tile_order); with ENT the first problem's tiles also feed the entropy
 // statistics; with PAIR they are pair tiles over the second problem's rows
 // (at most 2 BM: each CTA its own half).
+// The plain argmax sweep (<1, false, false, false>) runs beside the router
+// kernel at batch 1 and must stay within 96 registers a thread: two of its
+// warps and two 160-register router warps then fill one SM sub-partition's
+// 16K registers exactly (at 104 the router waits for the sweep to finish).
 template <int KT, bool ENT, bool DUAL, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_select_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

@@ -32,8 +32,8 @@ constexpr int ROUTER_ROWS_PER_CTA = 32;   // rows one CTA routes (more rows: mor
 constexpr int ROUTER_WREG = 20;     // float4 of a W1 row held per lane: d <= 32 * 4 * 20 = 2560
 constexpr int ROUTER_LB = 2;        // column groups whose loads are issued together (divides WREG)
 // At most 160 registers a thread: two router warps then fit in one SM
-// sub-partition's 16K registers beside two warps of the LM-head kernel (up to
-// 88 registers each), so the router really runs beside that kernel.
+// sub-partition's 16K registers beside two warps of the LM-head kernel (at
+// most 96 registers each), so the router really runs beside that kernel.
 constexpr int ROUTER_MAX_REGS = 160;
 
 __device__ __forceinline__ float gelu_erf(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
