@@ -609,10 +609,14 @@ __global__ void __launch_bounds__(PJ_THREADS)
     const uint32_t pf_local = smem_u32(smem);
     if (!*abort_flag && nrows > 0) {
         const EpiCtx e{p, g, mt, r0, nrows, col0, ncols, pfs, pf_local, rowdst, rowpos, srope};
-        switch (S) {
+        switch (S) {   // S <= PJ_MAX_SPLIT (host-checked)
             case 1: proj_epilogue<1>(e); break;
             case 2: proj_epilogue<2>(e); break;
+            case 3: proj_epilogue<3>(e); break;
             case 4: proj_epilogue<4>(e); break;
+            case 5: proj_epilogue<5>(e); break;
+            case 6: proj_epilogue<6>(e); break;
+            case 7: proj_epilogue<7>(e); break;
             default: proj_epilogue<8>(e); break;
         }
     }
@@ -1224,10 +1228,14 @@ static wf_status launch_proj(const CUtensorMap* mA, const CUtensorMap* mW, PjPar
     p.stages = stages;
     p.tmem_cols = 32;
     while (p.tmem_cols < p.bn) p.tmem_cols *= 2;
-    // split K (a power of two up to the portable cluster size) so that the
-    // CTAs fill the SMs about once
+    // split K (up to the portable cluster size): the most splits that keep
+    // the CTAs at about 1.6 an SM (8/5) when two fit, one otherwise, and at
+    // least two K blocks a split.  (Measured on a GB300 over S = 2..8: 1,024
+    // backlog rows - 80 tiles - take S = 3, 55 us a call against 59 at S = 2
+    // and 69 at S = 8; 24 tiles take S = 8; 32 tiles S = 7.)
+    const int budget = per_sm == 2 ? 8 * num_sms() / 5 : num_sms();
     int S = 1;
-    while (S < PJ_MAX_SPLIT && tiles * 2 * S <= per_sm * num_sms() && 2 * S <= p.num_k) S *= 2;
+    while (S < PJ_MAX_SPLIT && tiles * (S + 1) <= budget && 2 * (S + 1) <= p.num_k) ++S;
     p.kb_per = cdiv(p.num_k, S);
     while (S > 1 && (S - 1) * p.kb_per >= p.num_k) S /= 2;   // every split gets at least one K block
     p.kb_per = cdiv(p.num_k, S);
