@@ -1415,12 +1415,17 @@ wf_status launch_catchup(const wf_catchup_args* a, void* ws, bool with_final, cu
     ap.hq = a->H / a->G;
     ap.GD = GD;
     ap.HD = HD;
-    // splits of each sequence's cache rows: about two CTAs per SM over all
-    // (sequence, KV head) pairs, but no split shorter than AT_SPLIT_ROWS of the
-    // cache capacity - short splits cost more to merge than to read
-    const int want = 2 * num_sms() / (a->B * a->G);
+    // splits of each sequence's cache rows: about 1.25 CTAs an SM over all
+    // (sequence, KV head) pairs, at most AT_CLUSTER_MAX (so that a split's
+    // partials can merge on chip), and no split shorter than AT_SPLIT_ROWS of
+    // the cache capacity - short splits cost more to merge than to read.
+    // (Measured on a GB300, S = 2..38 a sequence: 8 x 128 onto 8,192 takes 3
+    // splits, 69 us a call against 72 at 4 and 73 at 8; 1,024 onto 16,384
+    // takes 16, 46 us against 48 at 38 with the global merge.)
+    const int want = cdiv(5 * num_sms(), 4 * a->B * a->G);
     const int by_rows = cdiv(a->cap, AT_SPLIT_ROWS);
     int chunks = want < by_rows ? want : by_rows;
+    if (chunks > AT_CLUSTER_MAX) chunks = AT_CLUSTER_MAX;
     ap.chunks = chunks < 1 ? 1 : (chunks > AT_MAX_CHUNKS ? AT_MAX_CHUNKS : chunks);
     ap.part = reinterpret_cast<float*>(w + L.apart);
     ap.cnt = reinterpret_cast<uint32_t*>(w + L.cnt);
