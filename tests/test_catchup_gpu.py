@@ -130,11 +130,16 @@ def check_against_oracle(c, res, kv_only=False):
     (4, 128, 4, 1, 128, (40, 200), (7, 0), 256),                          # one KV head, > 128 rows
     (5, 192, 6, 3, 48, tuple([1] * 130), tuple(range(130)), 131),         # 130 sequences: two row tiles
     (6, 64, 2, 1, 16, (50,), (4000,), 4096),                              # 16 splits: the largest cluster merge
-    (7, 128, 4, 2, 32, (40,), (5000,), 5100),                             # 20 splits: merged through global memory
+    (7, 128, 4, 2, 32, (40,), (5000,), 5100),                             # 20 splits by rows, capped at 16 (on chip)
     (8, 160, 4, 2, 32, (2, 3, 1, 5, 2, 1, 4, 2), (5,) * 8, 16),           # 8 sequences: the few-row output projection
     (9, 160, 4, 2, 32, (2, 3, 1, 5, 2, 1, 4, 2, 3), (5,) * 9, 16),        # 9: the tensor-core output projection
     (10, 4096, 8, 2, 64, (6, 2), (20, 3), 32),                            # a wide input (64 K blocks)
     (11, 1024, 128, 8, 128, (3,), (10,), 16),                             # H x D = 16384, the largest
+    (12, 2560, 32, 8, 80, (300,), (700,), 1000),                          # EAGLE-3 shape, 40 tiles: 6 K splits
+    (13, 2560, 32, 8, 80, (450,), (50,), 500),                            # 48 tiles: 5 K splits
+    # D = 128: one attention CTA an SM, 12 clusters of 16 splits cannot all be
+    # resident, so the splits merge through global memory
+    (14, 256, 16, 4, 128, (5, 3, 7), (4000, 4090, 3000), 4096),
 ])
 def test_catchup_small_shapes(seed, din, H, G, D, n, L, cap):
     c = pins.catchup_case(seed, din=din, H=H, G=G, D=D, n=n, L=L, cap=cap)
@@ -163,8 +168,9 @@ def test_catchup_eagle3_geometry_batch():
 @pytest.mark.parametrize("index", [1, 3])
 def test_catchup_eagle3_geometry_long_backlogs(index):
     """The two long-backlog workloads the bench times: 1,024 tokens onto a
-    16,384-entry cache (eight activation tiles, two K splits, the attention
-    merged through global memory) and 8 sequences of 128 onto 8,192."""
+    16,384-entry cache (eight activation tiles, three K splits, 16 attention
+    splits merged on chip) and 8 sequences of 128 onto 8,192 (three cache
+    splits a sequence)."""
     c = catchup_workload(index)
     res, cu = run_gpu(c)
     assert cu.ws.device_error() == (0, 0)
