@@ -359,8 +359,9 @@ __device__ __forceinline__ int tile_order(int v, int U0, int U) {
 // shared memory once per pair.
 // ENT (with KT = 1): also accumulate, per row, the softmax statistics of the
 // logits so that the entropy of the next-token distribution comes out of the
-// same weight sweep.  Needs every CTA's rows fixed over its tiles (at most two
-// activation tiles and a grid that is a multiple of their count).
+// same weight sweep.  Needs every CTA's rows fixed over its tiles: at most two
+// activation tiles, and a grid that is a multiple of their count or, with
+// PAIR, exactly two of them (each CTA of a pair keeps its own).
 // DUAL (with KT = 1): tiles U0.. are the second problem's
 // (activation map tmA2, weight map tmB2, top-k into p.cand), swept first
 // (tile_order); with ENT the first problem's tiles also feed the entropy
@@ -377,8 +378,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tmBs, const __grid_constant__ CUtensorMap tmB2s,
                        const GemmParams p) {
     static_assert(!DUAL || KT == 1, "the dual sweep pairs an argmax head with a top-k head");
-    static_assert(!PAIR || !ENT, "paired MMAs: no softmax statistics (rows of one CTA change from tile to tile)");
     extern __shared__ uint8_t smem_raw[];
+    // ENT needs every CTA's rows fixed over its tiles: with PAIR that holds
+    // for two activation tiles (each CTA of a pair keeps tile `rank`) only
+    if (ENT && PAIR && p.num_m > 2) {   // the host never launches this; both CTAs of a pair leave
+        if (threadIdx.x == 0) record_error(p.ctrl, WF_ERR_UNSUPPORTED, 0x330);
+        return;
+    }
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = p.stages;
     // stage s: activation slot at s * stage_bytes, weight slot a_alloc bytes on
@@ -630,9 +636,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // written by this launch
             for (int mm = 0; mm < num_m; ++mm) {
                 const int row = mm * BM + rit;
+                if (PAIR && mm != rank) continue;   // the pair's other CTA writes those rows' slot
                 if (row < p.M_rows)
                     p.ent[(size_t)row * nslots + slot] =
-                        mm == slot % num_m ? make_float4(em, es, et * LN2, 0.f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        PAIR || mm == slot % num_m ? make_float4(em, es, et * LN2, 0.f)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         if (KT == 1 && !*abort_flag) {
@@ -846,7 +854,7 @@ static int set_ring(GemmParams& p, int one_tile_a_rows, bool pair = false) {
 
 // Clusters of two paired-CTA sweep CTAs that can be resident at once (queried
 // once per device).  DUAL: the sweep that also carries the draft head.
-template <int KT, bool DUAL = false>
+template <int KT, bool DUAL = false, bool ENT = false>
 static int pair_slots(int smem) {
     static std::mutex mu;
     static int cached[64];
@@ -866,7 +874,7 @@ static int pair_slots(int smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, false, DUAL, true>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_select_kernel<KT, ENT, DUAL, true>, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = num_sms() / 2;
     }
@@ -882,9 +890,8 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     const wf_status cst = configure_once(mu, attr_set, [] {
         return cudaFuncSetAttribute(gemm_select_kernel<KT, ENT, false, false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_MAX) == cudaSuccess &&
-               (ENT || cudaFuncSetAttribute(gemm_select_kernel<KT, false, false, true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            GEMM_SMEM_MAX) == cudaSuccess);
+               cudaFuncSetAttribute(gemm_select_kernel<KT, ENT, false, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_MAX) == cudaSuccess;
     });
     if (cst != WF_OK) return cst;
     CUtensorMap ta, tb, tbs;
@@ -892,7 +899,7 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     if (ENT && num_m > 2) return WF_ERR_UNSUPPORTED;
     // several activation tiles: CTA pairs with the paired MMA (M = 256), each
     // loading half of every weight tile
-    const bool pair = !ENT && num_m > 1;
+    const bool pair = num_m > 1 && (!ENT || num_m == 2);
     // With a single activation tile the box covers only the rows that exist
     // (rounded up to a whole 8-row swizzle atom): no zero rows cross the
     // crossbar.  The UMMA still reads all BM rows of the stage; rows past the
@@ -940,9 +947,10 @@ static wf_status launch_select(const uint16_t* act, int M_rows, const uint16_t* 
     const int smem = set_ring(p, num_m == 1 ? a_rows : 0, pair);
     if (pair) {
         const int pairs = cdiv(num_m, 2) * p.num_n;
-        const int slots = pair_slots<KT>(smem);
+        const int slots = pair_slots<KT, false, ENT>(smem);
         const int grid = 2 * (pairs < slots ? pairs : slots);
-        return launch_cluster(gemm_select_kernel<KT, false, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s,
+        if (ENT && grid_out) *grid_out = grid / 2;   // ENT: the statistics' slots are the pairs
+        return launch_cluster(gemm_select_kernel<KT, ENT, false, true>, dim3(grid), dim3(GEMM_THREADS), smem, s,
                               2u, ta, tb, ta, tb, tbs, tbs, p);
     }
     const int tiles = p.num_m * p.num_n;

@@ -308,7 +308,8 @@ def test_round_edge_shapes():
 
 # ------------------------------------------------------------------ entropy router
 @pytest.mark.parametrize("P,d,V,rows", [(17, 256, 8192, None), (5, 64, 300, None), (61, 128, 5000, [60, 0, 7]),
-                                        (300, 64, 1000, list(range(299, 43, -1))), (40, 2560, 151936, [3, 39])])
+                                        (300, 64, 1000, list(range(299, 43, -1))), (40, 2560, 151936, [3, 39]),
+                                        (200, 256, 20000, None)])   # two row tiles (paired CTAs), ragged second
 def test_entropy(P, d, V, rows):
     W = synth.normal_bf16(V + d, 0, V, d, d ** -0.5 * 2.0)
     h = synth.normal_bf16(P + d, 1, P, d, 1.0)
