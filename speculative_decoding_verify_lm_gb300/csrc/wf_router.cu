@@ -263,6 +263,13 @@ __global__ void __launch_bounds__(RG_THREADS)
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
     if (kc0 < kc1) store(0, 0);
     __syncthreads();
+    // a warp's lanes share two values of ty, so its lower rows (4 ty + i) and
+    // upper rows (64 + 4 ty + i) are live or dead for the whole warp at once
+    // (any live lane makes the group live): with few rows (B = 32: half the
+    // warps and half of each live warp's block hold rows past B) the dead
+    // groups' multiply-adds are skipped, the staging and barriers are not
+    const bool lo_live = __any_sync(0xffffffffu, b0 + 4 * ty < B);
+    const bool hi_live = __any_sync(0xffffffffu, b0 + 64 + 4 * ty < B);
     // stages in groups of RG_PD so that every register slot index is a constant
     for (int g0 = kc0; g0 < kc1; g0 += RG_PD) {
 #pragma unroll
@@ -273,18 +280,33 @@ __global__ void __launch_bounds__(RG_THREADS)
             // slot p was stored for this stage: it now takes stage kc + RG_PD
             load_w(kc + RG_PD, p);
             load_h(kc + RG_PD, p);
+            if (hi_live) {
 #pragma unroll
-            for (int k = 0; k < RG_KC; ++k) {
-                const float4 h0 = *reinterpret_cast<const float4*>(&Hs[buf][k][4 * ty]);
-                const float4 h1 = *reinterpret_cast<const float4*>(&Hs[buf][k][64 + 4 * ty]);
-                const float4 w0 = *reinterpret_cast<const float4*>(&Ws[buf][k][4 * tx]);
-                const float4 w1 = *reinterpret_cast<const float4*>(&Ws[buf][k][64 + 4 * tx]);
-                const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-                const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                for (int k = 0; k < RG_KC; ++k) {
+                    const float4 h0 = *reinterpret_cast<const float4*>(&Hs[buf][k][4 * ty]);
+                    const float4 h1 = *reinterpret_cast<const float4*>(&Hs[buf][k][64 + 4 * ty]);
+                    const float4 w0 = *reinterpret_cast<const float4*>(&Ws[buf][k][4 * tx]);
+                    const float4 w1 = *reinterpret_cast<const float4*>(&Ws[buf][k][64 + 4 * tx]);
+                    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                    for (int i = 0; i < 8; ++i)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(hv[i], wv[j], acc[i][j]);
+                        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(hv[i], wv[j], acc[i][j]);
+                }
+            } else if (lo_live) {   // the upper rows are past B
+#pragma unroll
+                for (int k = 0; k < RG_KC; ++k) {
+                    const float4 h0 = *reinterpret_cast<const float4*>(&Hs[buf][k][4 * ty]);
+                    const float4 w0 = *reinterpret_cast<const float4*>(&Ws[buf][k][4 * tx]);
+                    const float4 w1 = *reinterpret_cast<const float4*>(&Ws[buf][k][64 + 4 * tx]);
+                    const float hv[4] = {h0.x, h0.y, h0.z, h0.w};
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(hv[i], wv[j], acc[i][j]);
+                }
             }
             if (kc + 1 < kc1) {
                 __syncthreads();   // the other buffer was last read a stage ago; this one is read no more
