@@ -428,9 +428,9 @@ __device__ void proj_epilogue(const EpiCtx& e) {
 
 // One CTA per (output tile, K split); the S splits of a tile form one
 // cluster.  Each split leaves its fp32 partial tile in its own shared memory
-// (row-major, odd row pitch); after a cluster barrier, split r finishes rows
-// [r BM/S, (r+1) BM/S) of the tile, summing the S partials (in split order)
-// over distributed shared memory as it goes.  Epilogue items run column
+// (row-major, odd row pitch); after a cluster barrier, split r finishes its
+// share (ceil(rows / S)) of the tile's rows, summing the S partials (in split
+// order) over distributed shared memory as it goes.  Epilogue items run column
 // (or rotation pair) fastest, so shared-memory reads are conflict-free and a
 // warp's global stores are contiguous.  The ring holds p.stages stages of a
 // 128-row activation box and a bn-row weight box; with a short ring two CTAs
@@ -694,10 +694,11 @@ __device__ __forceinline__ float2 dsmem_ld2(uint32_t addr) {
 //   O += P V       (one key step of 16 x D/8 dim tiles; V fragments by ldmatrix.trans)
 // Each warp keeps its own (max, sum, O) over its keys; the four are merged at
 // the end.  The splits of a (sequence, KV head) are then merged in index
-// order: with at most AT_CLUSTER_MAX splits they form one thread-block
-// cluster, each leaves its partial in its own shared memory and finishes a
-// slice of the outputs over distributed shared memory; with more, partials go
-// through global memory and the last CTA to arrive merges them.  The old cache
+// order: when every such group's cluster of splits (at most AT_CLUSTER_MAX)
+// can be resident at once they form one thread-block cluster, each leaves its
+// partial in its own shared memory and finishes a slice of the outputs over
+// distributed shared memory; otherwise partials go through global memory and
+// the last CTA to arrive merges them.  The old cache
 // rows of the first three passes are copied before the dependency wait.
 constexpr int AT_THREADS = 128;
 constexpr int AT_WARP_ROWS = 16;   // cache rows a warp takes per pass
