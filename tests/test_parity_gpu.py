@@ -147,6 +147,9 @@ def test_verify_bad_parent_sets_error():
 # ------------------------------------------------------------------ router
 @pytest.mark.parametrize("B,d,m", [(1, 2560, 1024), (1, 2560, 320), (7, 256, 128), (8, 72, 40), (9, 72, 40),
                                    (12, 2560, 1024), (33, 64, 5), (256, 512, 64),
+                                   # the GEMM's row groups at their edges: lower groups only, the
+                                   # first upper group, a second row tile of one row
+                                   (64, 256, 200), (65, 256, 200), (129, 128, 300),
                                    (3, 4096, 256), (20, 4096, 256)])   # rows too wide for W1 in registers
 def test_router(B, d, m):
     rng = np.random.default_rng(B * 7 + m)
@@ -309,7 +312,8 @@ def test_round_edge_shapes():
 # ------------------------------------------------------------------ entropy router
 @pytest.mark.parametrize("P,d,V,rows", [(17, 256, 8192, None), (5, 64, 300, None), (61, 128, 5000, [60, 0, 7]),
                                         (300, 64, 1000, list(range(299, 43, -1))), (40, 2560, 151936, [3, 39]),
-                                        (200, 256, 20000, None)])   # two row tiles (paired CTAs), ragged second
+                                        (200, 256, 20000, None),    # two row tiles (paired CTAs), ragged second
+                                        (129, 128, 3000, None)])    # the second tile holds one row
 def test_entropy(P, d, V, rows):
     W = synth.normal_bf16(V + d, 0, V, d, d ** -0.5 * 2.0)
     h = synth.normal_bf16(P + d, 1, P, d, 1.0)
