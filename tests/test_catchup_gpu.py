@@ -140,6 +140,8 @@ def check_against_oracle(c, res, kv_only=False):
     # D = 128: one attention CTA an SM, 12 clusters of 16 splits cannot all be
     # resident, so the splits merge through global memory
     (14, 256, 16, 4, 128, (5, 3, 7), (4000, 4090, 3000), 4096),
+    (15, 384, 8, 4, 96, (5, 2), (300, 7), 320),                           # D = 96 (12 dim tiles)
+    (16, 448, 8, 4, 112, (3,), (700,), 720),                              # D = 112 (14 dim tiles, 112-wide tiles)
 ])
 def test_catchup_small_shapes(seed, din, H, G, D, n, L, cap):
     c = pins.catchup_case(seed, din=din, H=H, G=G, D=D, n=n, L=L, cap=cap)
